@@ -1,0 +1,173 @@
+"""Reference restatement of the decode planner -- TEST INFRASTRUCTURE ONLY.
+
+A slow, plain-Python statement of the host scheduler's steps, written
+independently of the C++ planner inside the CUDA library.  Tests compare the
+library's schedule with this one integer for integer.  Only tests, the
+package smoke check and the benchmark's CPU-baseline leg import it.
+
+Steps and where they come from:
+
+P0  table check and lengths: indptr starts at 0 and is strictly increasing
+    (every request owns at least one page), 1 <= last_page_len <= P, page ids
+    inside the pool; l_i = P (n_i - 1) + r_i
+    ("FlashInfer 完全拆解", section 页表就是一张块稀疏矩阵;
+     "FlashInfer, in depth", section "Failure modes in production").
+P1  chunk size: with one query token per request and the GQA group folded
+    into the work unit, the work bound is L_kv = ceil(sum_i l_kv(i) / N_CTA)
+    ("FlashInfer 完全拆解", section 先切长 KV，再做最长任务优先分配).  The
+    chunk is L_kv rounded up to whole pages (a page is the block column),
+    and never below a floor, so short requests are not split ("FlashInfer,
+    in depth", section "Load balancing with split-KV"; "FlashInfer 完全拆解",
+    section Split-KV 解决的是并行度).  Reading taken where the pages leave it
+    open: the candidates L_kv, L_kv/2 and L_kv/4 are each scheduled and the
+    one with the smallest predicted makespan wins (ties: the larger chunk).
+P2  split and cost: a request longer than the chunk becomes chunks
+    [k c, min((k+1) c, l)); cost C = alpha * l_q + beta * l_kv with l_q = 1
+    and beta = 1, so C = alpha + len (same section, the cost model).
+P3  LPT: items in descending cost (ties: request, then chunk, ascending), each
+    given to the CTA with the least accumulated cost (ties: lowest CTA id)
+    (same section).
+P4  reduction map: split requests get contiguous partial slots in chunk
+    order; unsplit items write through to the output (slot -1)
+    ("FlashInfer 完全拆解", sections 先切长 KV (fixed reduction map, no
+    atomics) and Split-KV 解决的是并行度 (writethrough)).
+"""
+from __future__ import annotations
+
+import heapq
+from dataclasses import dataclass
+
+import numpy as np
+
+
+class TableError(ValueError):
+    pass
+
+
+def _ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def _round_up(a: int, b: int) -> int:
+    return _ceil_div(a, b) * b
+
+
+def lengths(indptr, last, indices, page_size: int, num_pages: int):
+    """P0: validate the CSR table and return per-request token counts."""
+    indptr = [int(x) for x in indptr]
+    last = [int(x) for x in last]
+    batch = len(last)
+    if len(indptr) != batch + 1:
+        raise TableError("indptr must have batch + 1 entries")
+    if batch and indptr[0] != 0:
+        raise TableError("indptr[0] must be 0")
+    lens = []
+    for i in range(batch):
+        n = indptr[i + 1] - indptr[i]
+        if n < 1:
+            raise TableError(f"request {i} owns no page")
+        r = last[i]
+        if not 1 <= r <= page_size:
+            raise TableError(f"last_page_len[{i}] = {r} outside 1..{page_size}")
+        lens.append(page_size * (n - 1) + r)
+    if batch:
+        idx = np.asarray(indices[: indptr[-1]], dtype=np.int64)
+        if idx.shape[0] != indptr[-1]:
+            raise TableError("indices shorter than indptr[-1]")
+        if idx.size and (idx.min() < 0 or idx.max() >= num_pages):
+            raise TableError("page id outside the pool")
+    return lens
+
+
+@dataclass
+class Plan:
+    chunk: int
+    makespan: int
+    cta_indptr: list          # [n_cta + 1]
+    items: list               # per item, queue order: (req, tok_begin, tok_end, dst_slot, page_off)
+    units: list               # per split request: (req, n_chunks)
+    merge_indptr: list        # [n_units + 1]
+    page_list: list           # page ids in queue order
+    lens: list
+
+    @property
+    def n_items(self):
+        return len(self.items)
+
+    @property
+    def n_slots(self):
+        return self.merge_indptr[-1] if self.merge_indptr else 0
+
+
+def _split(lens, chunk, alpha):
+    """P2: (cost, req, chunk_index, tok_begin, tok_end) per item."""
+    items = []
+    for i, l in enumerate(lens):
+        k = 0
+        t = 0
+        while t < l:
+            e = min(t + chunk, l)
+            items.append((alpha + (e - t), i, k, t, e))
+            t = e
+            k += 1
+    return items
+
+
+def _lpt(items, n_cta):
+    """P3: longest-processing-time-first onto n_cta queues."""
+    order = sorted(items, key=lambda it: (-it[0], it[1], it[2]))
+    heap = [(0, c) for c in range(n_cta)]
+    queues = [[] for _ in range(n_cta)]
+    for it in order:
+        load, c = heapq.heappop(heap)
+        queues[c].append(it)
+        heapq.heappush(heap, (load + it[0], c))
+    loads = [0] * n_cta
+    for load, c in heap:
+        loads[c] = load
+    return queues, max(loads) if loads else 0
+
+
+def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
+         alpha: int, min_chunk_tokens: int, chunk_divisors=(1, 2, 4)) -> Plan:
+    lens = lengths(indptr, last, indices, page_size, num_pages)
+    P = page_size
+    W = sum(lens)
+    L = _ceil_div(W, n_cta)
+    floor = _round_up(max(min_chunk_tokens, 1), P)
+    cands = []
+    for k in chunk_divisors:
+        c = max(_round_up(_ceil_div(L, k), P), floor)
+        if c not in cands:
+            cands.append(c)
+    best = None
+    for c in cands:
+        queues, makespan = _lpt(_split(lens, c, alpha), n_cta)
+        if best is None or makespan < best[1]:
+            best = (c, makespan, queues)
+    chunk, makespan, queues = best
+
+    # P4: reduction map over split requests, ascending request id
+    n_chunks = [_ceil_div(l, chunk) for l in lens]
+    units = [(i, n_chunks[i]) for i in range(len(lens)) if n_chunks[i] > 1]
+    merge_indptr = [0]
+    first_slot = {}
+    for req, nc in units:
+        first_slot[req] = merge_indptr[-1]
+        merge_indptr.append(merge_indptr[-1] + nc)
+
+    cta_indptr = [0]
+    items = []
+    page_list = []
+    indptr = [int(x) for x in indptr]
+    for q in queues:
+        for cost, req, k, tb, te in q:
+            dst = first_slot[req] + k if req in first_slot else -1
+            items.append((req, tb, te, dst, len(page_list)))
+            p0 = tb // P
+            p1 = _ceil_div(te, P)
+            base = indptr[req]
+            page_list.extend(int(indices[base + p]) for p in range(p0, p1))
+        cta_indptr.append(len(items))
+    return Plan(chunk, makespan, cta_indptr, items, units, merge_indptr,
+                page_list, lens)

@@ -1,0 +1,313 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* the worked page-table example printed on the pages (golden fixture);
+* the length identity l = P (n - 1) + r on the edge lengths the pages call
+  out (1, P, P + 1, exact multiples) and the off-by-one failure they warn of;
+* brute force: dense attention over K/V gathered page by page into
+  contiguous tensors, computed with torch's softmax / logsumexp in fp64;
+* closed forms: one token (out = v_0, lse = s_0), identical keys
+  (out = mean v, lse = s + ln l);
+* the state algebra: merging per-chunk states equals unsplit attention,
+  in any order and association; an empty state is the merge identity;
+* hand-worked schedules for the plan restatement, plus an exactly-once
+  coverage check on random tables.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from oracle import plan as oplan
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- page table
+
+def test_worked_example_page_table():
+    g = _golden("worked_example.json")
+    indptr, indices, last = workloads.page_table(g["kv_lens"], g["page_size"])
+    assert indptr.tolist() == g["indptr"]
+    assert indices.tolist() == g["indices"]
+    assert last.tolist() == g["last_page_len"]
+    lens = oracle.lengths(g["indptr"], g["indices"], g["last_page_len"],
+                          g["page_size"], num_pages=64)
+    assert lens.tolist() == g["kv_lens"]
+    assert oplan.lengths(g["indptr"], g["last_page_len"], g["indices"],
+                         g["page_size"], 64) == g["kv_lens"]
+
+
+@pytest.mark.parametrize("P", [1, 4, 16])
+def test_length_identity_edges(P):
+    lens = [1, max(P - 1, 1), P, P + 1, 2 * P, 3 * P, 100_000]
+    indptr, indices, last = workloads.page_table(lens, P)
+    assert all(1 <= r <= P for r in last.tolist())
+    for i, l in enumerate(lens):
+        n = indptr[i + 1] - indptr[i]
+        assert n == math.ceil(l / P)
+    got = oracle.lengths(indptr, indices, last, P, num_pages=int(indptr[-1]))
+    assert got.tolist() == lens
+    assert oplan.lengths(indptr, last, indices, P, int(indptr[-1])) == lens
+
+
+def test_table_errors_rejected():
+    P = 16
+    # exact multiple of P written with last_page_len = 0 (the off-by-one bug)
+    bad_last = ([0, 2], [0, 1], [0])
+    good = ([0, 2], [0, 1], [16])
+    assert oracle.lengths(*good, P, 4).tolist() == [32]
+    with pytest.raises(oracle.OracleError):
+        oracle.lengths(*bad_last, P, 4)
+    with pytest.raises(oplan.TableError):
+        oplan.lengths(bad_last[0], bad_last[2], bad_last[1], P, 4)
+    for indptr, indices, last in [
+        ([0, 0], [], [1]),            # request owning no page
+        ([0, 1], [0], [17]),          # last page longer than the page
+        ([0, 1], [4], [1]),           # page id outside the pool
+        ([0, 1], [-1], [1]),          # negative page id
+        ([1, 2], [0, 1], [1]),        # indptr not starting at 0
+    ]:
+        with pytest.raises(oracle.OracleError):
+            oracle.lengths(indptr, indices, last, P, 4)
+        with pytest.raises(oplan.TableError):
+            oplan.lengths(indptr, last, indices, P, 4)
+
+
+# ----------------------------------------------------------- attention pins
+
+def _tiny(seed, lens, P, hq, hkv, D=16, scale_q=1.0):
+    w = workloads.Workload(f"t{seed}", seed, hq, hkv, D, P, 1, tuple(lens),
+                           sum(math.ceil(l / P) for l in lens) + 2)
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w)[0]
+    if scale_q != 1.0:
+        q = (q.float() * scale_q).to(torch.bfloat16)
+    kv = workloads.make_kv(w)[0]
+    return w, t, q, kv
+
+
+def _dense_reference(w, t, q, kv):
+    """Gather K/V page by page into contiguous fp64 tensors, then torch."""
+    P, g = w.page_size, w.hq // w.hkv
+    out = torch.zeros(w.batch, w.hq, w.head_dim, dtype=torch.float64)
+    lse = torch.zeros(w.batch, w.hq, dtype=torch.float64)
+    for i in range(w.batch):
+        pages = t["indices"][t["indptr"][i]:t["indptr"][i + 1]]
+        ks, vs = [], []
+        for n, pg in enumerate(pages):
+            valid = P if n < len(pages) - 1 else int(t["last"][i])
+            ks.append(kv[int(pg), 0, :valid])      # [valid, Hkv, D]
+            vs.append(kv[int(pg), 1, :valid])
+        K = torch.cat(ks).double()
+        V = torch.cat(vs).double()
+        for h in range(w.hq):
+            qq = q[i, h].double()
+            s = (K[:, h // g, :] @ qq) / math.sqrt(w.head_dim)
+            out[i, h] = torch.softmax(s, dim=0) @ V[:, h // g, :]
+            lse[i, h] = torch.logsumexp(s, dim=0)
+    return out.numpy(), lse.numpy()
+
+
+@pytest.mark.parametrize("P,lens,hq,hkv", [
+    (16, [37, 16, 5], 8, 2),
+    (4, [1, 9, 12, 3], 4, 4),
+    (1, [7, 1, 13], 8, 1),
+    (3, [10, 3, 4], 6, 3),
+])
+def test_brute_force_dense(P, lens, hq, hkv):
+    w, t, q, kv = _tiny(7 + P, lens, P, hq, hkv)
+    ref_o, ref_l = _dense_reference(w, t, q, kv)
+    o, l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=hq, hkv=hkv)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_peaky_scores_brute_force():
+    w, t, q, kv = _tiny(3, [40, 17], 16, 4, 2, scale_q=8.0)
+    ref_o, ref_l = _dense_reference(w, t, q, kv)
+    o, l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=4, hkv=2)
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(l, ref_l, rtol=1e-13, atol=1e-11)
+
+
+def test_single_token_closed_form():
+    w, t, q, kv = _tiny(11, [1, 1], 16, 4, 2)
+    o, l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=4, hkv=2)
+    for i in range(2):
+        pg = int(t["indices"][t["indptr"][i]])
+        for h in range(4):
+            k = kv[pg, 0, 0, h // 2].double()
+            v = kv[pg, 1, 0, h // 2].double()
+            np.testing.assert_array_equal(o[i, h], v.numpy())
+            s = float(q[i, h].double() @ k) / math.sqrt(w.head_dim)
+            assert abs(l[i, h] - s) < 1e-12
+
+
+def test_identical_keys_closed_form():
+    w, t, q, kv = _tiny(12, [21], 4, 2, 1)
+    kv = kv.clone()
+    kv[:, 0] = kv[int(t["indices"][0]), 0, 0]      # every key equals one key
+    o, l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=2, hkv=1)
+    pages = t["indices"][t["indptr"][0]:t["indptr"][1]]
+    vs = [kv[int(pg), 1, :(4 if n < len(pages) - 1 else int(t["last"][0]))]
+          for n, pg in enumerate(pages)]
+    V = torch.cat(vs).double()[:, 0, :]
+    k = kv[int(t["indices"][0]), 0, 0, 0].double()
+    for h in range(2):
+        np.testing.assert_allclose(o[0, h], V.mean(0).numpy(), atol=1e-12)
+        s = float(q[0, h].double() @ k) / math.sqrt(w.head_dim)
+        assert abs(l[0, h] - (s + math.log(21))) < 1e-12
+
+
+def test_gqa_grouping_is_consecutive():
+    """Query head h reads KV head h // g: with distinct KV heads a wrong
+    grouping (e.g. h % Hkv) gives different numbers."""
+    w, t, q, kv = _tiny(13, [9], 16, 4, 2)
+    q = q.clone()
+    q[0, 1] = q[0, 0]
+    q[0, 2] = q[0, 0]
+    o, _ = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=4, hkv=2)
+    np.testing.assert_array_equal(o[0, 0], o[0, 1])      # same group
+    assert np.abs(o[0, 0] - o[0, 2]).max() > 1e-3         # other group
+
+
+# ------------------------------------------------------------- merge algebra
+
+def _chunk_states(q, kv, t, req, head, cuts, hq, hkv):
+    rows = [(req, head, a, b) for a, b in zip(cuts[:-1], cuts[1:])]
+    return oracle.attend(q, kv, t["indptr"], t["indices"], t["last"], rows,
+                         hq=hq, hkv=hkv)
+
+
+def test_merge_of_chunks_equals_unsplit():
+    w, t, q, kv = _tiny(21, [40, 33], 4, 4, 2)
+    for req, head in [(0, 0), (0, 3), (1, 2)]:
+        L = w.lens[req]
+        full_o, full_l = oracle.attend(q, kv, t["indptr"], t["indices"], t["last"],
+                                       [(req, head)], hq=4, hkv=2)
+        cuts = [0, 13, 29, L] if L > 29 else [0, 7, 19, L]
+        co, cl = _chunk_states(q, kv, t, req, head, cuts, 4, 2)
+        # left fold in chunk order
+        o, l = co[0:1], cl[0:1]
+        for k in range(1, len(co)):
+            o, l = oracle.merge(o, l, co[k:k + 1], cl[k:k + 1])
+        np.testing.assert_allclose(o, full_o, atol=1e-12)
+        np.testing.assert_allclose(l, full_l, atol=1e-12)
+        # every order and both associations give the same state
+        for perm in itertools.permutations(range(3)):
+            a, b, c = (co[p:p + 1] for p in perm)
+            la, lb, lc = (cl[p:p + 1] for p in perm)
+            o1, l1 = oracle.merge(*oracle.merge(a, la, b, lb), c, lc)
+            o2, l2 = oracle.merge(a, la, *oracle.merge(b, lb, c, lc))
+            np.testing.assert_allclose(o1, full_o, atol=1e-12)
+            np.testing.assert_allclose(o2, full_o, atol=1e-12)
+            np.testing.assert_allclose(l1, full_l, atol=1e-12)
+            np.testing.assert_allclose(l2, full_l, atol=1e-12)
+
+
+def test_merge_empty_state_and_closed_forms():
+    rng = np.random.default_rng(0)
+    o = rng.standard_normal((5, 8))
+    l = rng.standard_normal(5)
+    empty_o = rng.standard_normal((5, 8))
+    empty_l = np.full(5, -np.inf)
+    mo, ml = oracle.merge(o, l, empty_o, empty_l)
+    np.testing.assert_array_equal(mo, o)
+    np.testing.assert_array_equal(ml, l)
+    mo, ml = oracle.merge(empty_o, empty_l, o, l)
+    np.testing.assert_array_equal(mo, o)
+    # both empty: zero output, empty state
+    mo, ml = oracle.merge(empty_o, empty_l, empty_o, empty_l)
+    assert np.all(mo == 0) and np.all(np.isneginf(ml))
+    # equal lse: plain average, lse + ln 2
+    o2 = rng.standard_normal((5, 8))
+    mo, ml = oracle.merge(o, l, o2, l)
+    np.testing.assert_allclose(mo, (o + o2) / 2, atol=1e-15)
+    np.testing.assert_allclose(ml, l + math.log(2), atol=1e-15)
+    # weights follow exp(lse): lse_b = lse_a + ln 3 -> weights 1/4, 3/4
+    mo, ml = oracle.merge(o, l, o2, l + math.log(3))
+    np.testing.assert_allclose(mo, 0.25 * o + 0.75 * o2, atol=1e-14)
+    np.testing.assert_allclose(ml, l + math.log(4), atol=1e-14)
+
+
+# ------------------------------------------------------------ plan restatement
+
+def _check_plan_case(case):
+    P = case["page_size"]
+    indptr, indices, last = workloads.page_table(case["kv_lens"], P)
+    p = oplan.plan(indptr, indices, last, page_size=P, num_pages=int(indptr[-1]),
+                   n_cta=case["n_cta"], alpha=case["alpha"],
+                   min_chunk_tokens=case["min_chunk_tokens"])
+    assert p.chunk == case["chunk"]
+    assert p.makespan == case["makespan"]
+    assert p.cta_indptr == case["cta_indptr"]
+    assert [list(x) for x in p.items] == case["items"]
+    assert [list(x) for x in p.units] == case["units"]
+    assert p.merge_indptr == case["merge_indptr"]
+    if case.get("page_list_is_identity"):
+        assert p.page_list == list(range(int(indptr[-1])))
+    else:
+        assert p.page_list == case["page_list"]
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_plan_hand_worked(idx):
+    _check_plan_case(_golden("plan_hand.json")["cases"][idx])
+
+
+def coverage_check(p, indptr, indices, last, page_size):
+    """Independent check of a schedule: every valid token exactly once,
+    page_list consistent with the table, merge map in chunk order."""
+    P = page_size
+    lens = [P * (indptr[i + 1] - indptr[i] - 1) + last[i] for i in range(len(last))]
+    seen = [np.zeros(l, dtype=np.int32) for l in lens]
+    slots_of = {}
+    for n, (req, tb, te, dst, poff) in enumerate(p.items):
+        assert 0 <= tb < te <= lens[req]
+        assert tb % P == 0
+        seen[req][tb:te] += 1
+        for t in range(tb, te):
+            assert p.page_list[poff + (t - tb) // P] == indices[indptr[req] + t // P]
+        if dst >= 0:
+            slots_of.setdefault(req, []).append((tb, dst))
+    for s in seen:
+        assert np.all(s == 1)
+    assert p.cta_indptr[0] == 0 and p.cta_indptr[-1] == len(p.items)
+    assert all(a <= b for a, b in zip(p.cta_indptr, p.cta_indptr[1:]))
+    for u, (req, nc) in enumerate(p.units):
+        got = sorted(slots_of[req])
+        assert [d for _, d in got] == list(range(p.merge_indptr[u], p.merge_indptr[u + 1]))
+        assert nc == len(got) >= 2
+    assert set(slots_of) == {r for r, _ in p.units}
+    assert [r for r, _ in p.units] == sorted(r for r, _ in p.units)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_coverage_random(seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.choice([1, 2, 16]))
+    B = int(rng.integers(1, 40))
+    lens = rng.integers(1, 3000, B).tolist()
+    if seed % 2:
+        lens[0] = 20000
+    pool = sum(-(-l // P) for l in lens) + 5
+    ids = rng.permutation(pool).astype(np.int32)
+    indptr, indices, last = workloads.page_table(lens, P, ids)
+    n_cta = int(rng.choice([3, 16, 152]))
+    p = oplan.plan(indptr, indices, last, page_size=P, num_pages=pool, n_cta=n_cta,
+                   alpha=int(rng.integers(0, 64)), min_chunk_tokens=int(rng.choice([1, 64, 256])))
+    coverage_check(p, indptr.tolist(), indices.tolist(), last.tolist(), P)
+    W = sum(lens)
+    assert len(p.items) <= B + 4 * n_cta + 4
+    assert p.makespan * n_cta >= W                   # a makespan is at least the mean

@@ -1,0 +1,494 @@
+"""Decode-step benchmark: achieved HBM GB/s (and % of peak) and steps/s.
+
+Default workload: the Llama-3-8B-shaped decode step -- 32 layers, Hq 32,
+Hkv 8, D 128, bf16, page size 16, 64 requests with KV lengths uniform in
+[1, 8192] (seeded), pages scattered over the pool.  One step = plan on the
+host (schedule copied into the fixed workspace) + one CUDA-graph replay of
+the 32 per-layer runs (decode kernel + split merge each).
+
+Throughput counts ALGORITHMIC bytes: the valid K and V rows of every request
+(sum_i l_i x 2 x Hkv x D x 2 per layer), q, out, lse and the page table --
+not partials, unused slots of last pages or the schedule.  Per-layer caches
+(1.17 GB each) are larger than L2, and consecutive layers read different
+caches, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama8b_step|skewed|token_sparse|shared_prefix]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode-step KV throughput: achieved HBM GB/s (% of GB300 peak) and steps/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_llama8b_step.md")
+KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_decode_host_gb300", "csrc", "decode_kernel.cu")
+
+
+# --------------------------------------------------------------------- bytes
+
+def alg_bytes_per_layer(w, lens, nnz):
+    kv = sum(lens) * 2 * w.hkv * w.head_dim * 2
+    q = w.batch * w.hq * w.head_dim * 2
+    out = w.batch * w.hq * w.head_dim * 2
+    lse = w.batch * w.hq * 4
+    table = 4 * (nnz + 2 * w.batch + 1)
+    return kv + q + out + lse + table
+
+
+def _lens(t, P):
+    ip, last = t["indptr"], t["last"]
+    return [int(P * (ip[i + 1] - ip[i] - 1) + last[i]) for i in range(len(last))]
+
+
+# -------------------------------------------------------------------- peaks
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profile():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+        with open(KERNEL_SOURCE, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def _views(w, t):
+    if w.prefix_tokens:
+        return [("prefix", t["prefix"]), ("suffix", t["suffix"])]
+    return [("full", (t["indptr"], t["indices"], t["last"]))]
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import paged_kv_decode_host_gb300 as pkd
+
+    pkd.build()
+    pkd.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = workloads.workload(args.workload)
+    t = workloads.make_tables(w)
+    P = w.page_size
+    lens = _lens(t, P)
+    nnz = int(t["indptr"][-1])
+    layers = w.layers
+    # distinct caches per replay for single-layer workloads so no step reads
+    # another step's bytes out of L2
+    copies = 1 if layers > 1 else max(1, int(np.ceil(1.2e9 / (w.pool_pages * 2 * P * w.hkv * 256))))
+    n_kv = layers * copies
+    kvs = workloads.make_kv(w, device=dev, layers=n_kv)
+    qs = workloads.make_q(w, device=dev, layers=layers)
+    outs = [torch.empty_like(x) for x in qs]
+    lses = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in qs]
+    views = _views(w, t)
+    decs = []
+    for name, (ip, ix, la) in views:
+        d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
+                                            max_num_pages=int(ip[-1]), num_pages=w.pool_pages,
+                                            device=dev)
+        d.plan(ip, ix, la)
+        decs.append(d)
+    # graphs: one per cache copy; each captures the layers of a step
+    graphs = []
+    if w.prefix_tokens:
+        # prefix run + suffix run + merge_states, per cache copy
+        po = [torch.empty_like(qs[0]) for _ in range(copies)]
+        pl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
+        so = [torch.empty_like(qs[0]) for _ in range(copies)]
+        sl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
+        for c in range(copies):
+            gp = decs[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=True)
+            gs = decs[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=True)
+            graphs.append((gp, gs, c))
+    else:
+        for c in range(copies):
+            kv_c = kvs[c * layers:(c + 1) * layers]
+            graphs.append((decs[0].capture(qs, kv_c, outs, lses, timing=True), None, c))
+
+    stream = torch.cuda.current_stream()
+    host = {}
+
+    def step(k):
+        """One decode step.  With host buffers (e2e): q comes from pinned host
+        memory and out / lse go back to it, inside the step."""
+        if host:
+            for x, h in zip(qs, host["q"]):
+                x.copy_(h, non_blocking=True)
+        gp, gs, c = graphs[k % len(graphs)]
+        for (name, (ip, ix, la)), d in zip(views, decs):
+            d.plan(ip, ix, la)
+        gp.launch()
+        if gs is not None:
+            gs.launch()
+            pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
+        if host:
+            for x, h in zip(outs, host["out"]):
+                h.copy_(x, non_blocking=True)
+            for x, h in zip(lses, host["lse"]):
+                h.copy_(x, non_blocking=True)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    gpu_uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    sampler = ClockSampler(f"GPU-{gpu_uuid}" if gpu_uuid else dev.index)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with sampler:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for k in range(args.steps):
+            step(args.warmup + k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms_total = e0.elapsed_time(e1)
+    last = graphs[(args.warmup + args.steps - 1) % len(graphs)]
+    k1_ms = last[0].layer_times() + (last[1].layer_times() if last[1] is not None else [])
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+
+    # algorithmic bytes of one step
+    if w.prefix_tokens:
+        pre_lens = [w.prefix_tokens] * w.batch
+        suf_lens = list(w.suffix_lens)
+        kv_bytes = (w.prefix_tokens + sum(suf_lens)) * 2 * w.hkv * w.head_dim * 2  # prefix once
+        io = w.batch * w.hq * (w.head_dim * 2 * 2 + 4)
+        table = 4 * (int(t["prefix"][0][-1]) + int(t["suffix"][0][-1]) + 4 * w.batch + 2)
+        step_bytes = kv_bytes + io + table
+        layer_bytes = [alg_bytes_per_layer(w, pre_lens, int(t["prefix"][0][-1])),
+                       alg_bytes_per_layer(w, suf_lens, int(t["suffix"][0][-1]))]
+    else:
+        lb = alg_bytes_per_layer(w, lens, nnz)
+        step_bytes = lb * layers
+        layer_bytes = [lb] * layers
+    gbs = world * step_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    # roofline of the dominant kernel (decode), per launch
+    k1_gbs = [b / (ms * 1e-3) / 1e9 for b, ms in zip(layer_bytes, k1_ms) if ms > 0]
+    k1_mean_ms = float(np.mean(k1_ms))
+    achieved = float(np.sum(layer_bytes) / (np.sum(k1_ms) * 1e-3) / 1e9)
+    info = decs[0].plan_info()
+
+    # end to end: host q in, host out back, plan from host tables, per step
+    e2e = run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, dev)
+
+    clocks = sampler.summary()
+    launches_per_step = sum(g.layers for gg in graphs[:1] for g in gg[:2] if g is not None) * 2 + \
+        (1 if w.prefix_tokens else 0)
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "steps_per_s": round(1e3 / ms_step, 3),
+        "pct_of_peak": round(100.0 * gbs / world / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "accum_dtype": "fp32",
+        "data": "synthetic (seeded N(0,1) bf16 q/KV, seeded lengths and page permutation)",
+        "config": {
+            "workload": args.workload, "layers": layers, "batch": w.batch, "hq": w.hq,
+            "hkv": w.hkv, "head_dim": w.head_dim, "page_size": P,
+            "total_tokens_per_layer": int(sum(lens)), "pages_per_layer": nnz,
+            "alg_bytes_per_step": int(step_bytes),
+            "l2": "inputs larger than L2 (each layer's cache >= 0.49 GB, distinct per replay)",
+            "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
+                                          "makespan")},
+            "parallelism": f"replicas x{world} (no collective)",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback",
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": traffic_from_profile(),
+            "kernel": "decode_kernel", "launch_ms_mean": round(k1_mean_ms, 5),
+            "launch_gbs_min": round(min(k1_gbs), 1) if k1_gbs else None,
+            "launch_gbs_max": round(max(k1_gbs), 1) if k1_gbs else None,
+            "timing": "CUDA event nodes around each decode launch inside the replayed graph "
+                      "(last timed step)",
+        },
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, t, qs, kvs, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, dev):
+    """Same step through the public API with host buffers: pinned host q in,
+    out + lse back to pinned host, inside the timed region."""
+    import torch
+    host["q"] = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in qs]
+    for h, x in zip(host["q"], qs):
+        h.copy_(x)
+    host["out"] = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    host["lse"] = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
+    h2d = sum(x.numel() * x.element_size() for x in qs)
+    d2h = sum(x.numel() * x.element_size() for x in outs) + sum(x.numel() * 4 for x in lses)
+    sched = sum(4 * d.plan_info()["schedule_words"] for d in decs)
+    steps = max(3, args.steps // 2)
+    try:
+        for k in range(3):
+            step(k)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for k in range(steps):
+            step(k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) * 1e3 / steps
+        ms = max(e0.elapsed_time(e1) / steps, wall)
+    finally:
+        host.clear()
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d + sched),
+            "d2h_bytes_per_step": int(d2h),
+            "what": "pinned host q -> device, plan from host tables (schedule H2D), graph "
+                    "replay, out + lse -> pinned host; KV cache resident"}
+
+
+# ------------------------------------------------------------ cpu baseline
+
+def _oracle_sample(w, t, q_bits, kv_bits, rows_req):
+    import oracle
+    rows = np.array([(i, h) for i in rows_req for h in range(w.hq)], dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.attend(q_bits, kv_bits, t["indptr"], t["indices"], t["last"], rows,
+                  hq=w.hq, hkv=w.hkv)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
+    """The fp64 oracle on the host cores, on a bounded sample of the same
+    workload (requests of layer 0, all query heads), in the metric's unit."""
+    import oracle
+    from oracle import _bits
+    oracle.build()
+    if q_bits is None:
+        q_bits = _bits(qs[0])
+        kv_bits = _bits(kvs[0])
+    lens = _lens(t, w.page_size)
+    order = list(range(w.batch))
+    # calibrate on one request, then size the sample to the budget
+    t_one = _oracle_sample(w, t, q_bits, kv_bits, [order[0]])
+    per_tok = t_one / max(lens[order[0]], 1)
+    n_tok_target = budget_s / max(per_tok, 1e-9)
+    sample, acc = [], 0
+    for i in order:
+        if acc >= n_tok_target:
+            break
+        sample.append(i)
+        acc += lens[i]
+    secs = _oracle_sample(w, t, q_bits, kv_bits, sample)
+    s_lens = [lens[i] for i in sample]
+    bytes_ = alg_bytes_per_layer(
+        workloads.Workload("s", 0, w.hq, w.hkv, w.head_dim, w.page_size, 1, tuple(s_lens), 1),
+        s_lens, sum(-(-l // w.page_size) for l in s_lens))
+    return {"value": round(bytes_ / secs / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(secs, 3),
+            "sample": f"layer 0, requests 0..{len(sample) - 1} ({sum(s_lens)} tokens) x "
+                      f"{w.hq} query heads, fp64, all host cores"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    import torch
+    w = workloads.workload(args.workload)
+    t = workloads.make_tables(w)
+    from oracle import _bits
+    q = workloads.make_q(w, device="cpu", layers=1)[0]
+    # only the pages the sample touches need values; build the whole layer
+    kv = workloads.make_kv(w, device="cpu", layers=1)[0]
+    q_bits, kv_bits = _bits(q), _bits(kv)
+    del kv
+    per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    lens = _lens(t, w.page_size)
+    for _ in range(args.warmup):
+        cpu_baseline(w, t, None, None, budget_s=per_step_budget, q_bits=q_bits, kv_bits=kv_bits)
+    vals, secs = [], 0.0
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline(w, t, None, None, budget_s=per_step_budget, q_bits=q_bits,
+                            kv_bits=kv_bits)
+        vals.append(last["value"])
+        secs += last["seconds"]
+    v = float(np.mean(vals))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / max(args.steps, 1), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "layers": w.layers, "batch": w.batch, "hq": w.hq,
+                   "hkv": w.hkv, "head_dim": w.head_dim, "page_size": w.page_size,
+                   "sample_per_step": last["sample"] if last else None},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": last["sample"] if last else None},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# --------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_step",
+                    choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,211 @@
+/*
+ * pkd -- batched GQA decode attention over a CSR-paged KV cache, for GB300
+ * (sm_103a).  C ABI: plain pointers and sizes only.
+ *
+ * The problem (FlashInfer, in depth -- "The block-sparse page table",
+ * "Plan and run: the inspector-executor split", "Load balancing with
+ * split-KV"; FlashInfer 完全拆解 -- 页表就是一张块稀疏矩阵, 先切长 KV，再做
+ * 最长任务优先分配, 固定指针比固定内容更重要, 在线 Softmax 为什么允许任意切块):
+ *
+ *   A batch of B requests, each with one query token.  Request i owns the
+ *   pages indices[indptr[i] .. indptr[i+1]) of a page pool, in order; its
+ *   last page holds last_page_len[i] tokens (1..P), so its KV length is
+ *   l_i = P (n_i - 1) + last_page_len[i].  Each layer's cache is one tensor
+ *   [num_pages][2][P][Hkv][D] (NHD; K at index 0, V at index 1).  For every
+ *   request i and query head h (KV head h / g, g = Hq / Hkv):
+ *       out[i][h] = softmax(q[i][h] . K^T / sqrt(D)) V
+ *       lse[i][h] = log sum_t exp(q[i][h] . k_t / sqrt(D))   (natural log)
+ *
+ * Calls:
+ *   pkd_plan  -- once per decode step, on the host: checks the table, splits
+ *                long KV ranges into page-aligned chunks, assigns the work
+ *                items to a fixed set of CTAs (longest first onto the least
+ *                loaded), builds the reduction map, and copies the schedule
+ *                into the fixed-address device workspace.
+ *   pkd_run   -- once per layer: persistent decode kernel plus the merge of
+ *                split chunks.  Stream-ordered, no host sync, no allocation,
+ *                capturable in a CUDA graph.
+ *   pkd_merge_states -- exact combination of two attention states.
+ *
+ * Conventions.  Every device pointer is a plain CUDA device address; every
+ * stream argument is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  The caller owns every buffer, the workspace included; the
+ * library never allocates device memory.  Return values: PKD_OK (0) or a
+ * negative PKD_E_* code; pkd_status_str() names it.  Nothing aborts.
+ */
+#ifndef PKD_H_
+#define PKD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PKD_OK 0
+#define PKD_E_INVALID_ARG -1        /* null pointer, bad size, misaligned  */
+#define PKD_E_BAD_TABLE -2          /* indptr / last_page_len / page id    */
+#define PKD_E_UNSUPPORTED_SHAPE -3  /* D, Hq % Hkv, group size, Hkv        */
+#define PKD_E_WORKSPACE_TOO_SMALL -4
+#define PKD_E_NO_PLAN -5            /* run before any plan                  */
+#define PKD_E_STALE_PLAN -6         /* run against another plan's epoch    */
+#define PKD_E_CAPACITY -7           /* batch or page count above capacity  */
+#define PKD_E_CUDA -8               /* a CUDA runtime call failed          */
+#define PKD_E_DEVICE -9             /* the device reported an error word   */
+
+/* Device error word bits (pkd_last_device_error). */
+#define PKD_DEV_ERR_TIMEOUT 1       /* a bounded wait gave up               */
+#define PKD_DEV_ERR_BOUNDS 2        /* a schedule entry pointed out of range */
+
+/* ---- configuration ----------------------------------------------------- */
+typedef struct pkd_config {
+    int32_t num_qo_heads;      /* Hq                                        */
+    int32_t num_kv_heads;      /* Hkv, 1..8; Hq % Hkv == 0, g in {1,2,4,8}  */
+    int32_t head_dim;          /* D; 128                                    */
+    int32_t page_size;         /* P >= 1                                    */
+    int32_t max_batch;         /* capacity: requests per plan               */
+    int32_t max_num_pages;     /* capacity: page ids per plan (nnz)         */
+    int32_t num_pages;         /* pool size; page ids must be < num_pages   */
+    int32_t alpha;             /* per-item cost in tokens (cost = alpha +
+                                  tokens); < 0 selects the default (32)     */
+    int32_t min_chunk_tokens;  /* split floor in tokens; < 0 -> 256          */
+    int32_t num_ctas;          /* persistent grid; 0 -> SMs x CTAs per SM    */
+    uint32_t flags;            /* reserved, must be 0                        */
+} pkd_config;
+
+typedef struct pkd_ctx pkd_ctx;
+typedef struct pkd_graph pkd_graph;
+
+/* Summary of the last plan (host-side copy). */
+typedef struct pkd_plan_info {
+    int32_t batch;
+    int32_t num_ctas;
+    int32_t chunk_tokens;      /* chosen chunk (page multiple)             */
+    int32_t num_items;
+    int32_t num_units;         /* split requests                            */
+    int32_t num_slots;         /* partial states in the workspace           */
+    int64_t total_tokens;      /* sum of l_i                                */
+    int64_t makespan;          /* predicted max per-CTA cost                */
+    int32_t nnz;               /* pages referenced                          */
+    int32_t schedule_words;    /* int32 words pkd_plan_host writes          */
+} pkd_plan_info;
+
+/* Bytes of device workspace needed for this configuration.  With
+ * num_ctas == 0 the grid size is read from the current CUDA device.  Returns
+ * 0 when the configuration is invalid or the device query fails. */
+size_t pkd_workspace_bytes(const pkd_config *cfg);
+
+/* Create a context over a caller-owned device workspace (at least
+ * pkd_workspace_bytes(cfg) bytes, 256-byte aligned, kept alive and at the
+ * same address for the context's life: the schedule lives at fixed offsets
+ * inside it so that captured launches stay valid).  Allocates pinned host
+ * staging and two events.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * WORKSPACE_TOO_SMALL, CUDA. */
+int pkd_create(const pkd_config *cfg, void *d_workspace, size_t workspace_bytes,
+               pkd_ctx **out);
+
+/* Destroy a context (synchronizes with its pending staging copies). */
+void pkd_destroy(pkd_ctx *ctx);
+
+/* Plan one decode step.  Host arrays (int32): indptr[batch + 1],
+ * indices[indptr[batch]], last_page_len[batch].  They are copied into
+ * pinned staging before the call returns, so the caller may reuse them at
+ * once; the schedule reaches the workspace by cudaMemcpyAsync on `stream`
+ * (staging is double-buffered and fenced by events).  batch may be 0.
+ * On success *epoch (if not NULL) receives the new plan epoch (>= 1).
+ * Errors: INVALID_ARG, BAD_TABLE, CAPACITY, CUDA. */
+int pkd_plan(pkd_ctx *ctx, const int32_t *indptr, const int32_t *indices,
+             const int32_t *last_page_len, int32_t batch, void *stream,
+             uint64_t *epoch);
+
+/* Summary of the current plan.  Errors: INVALID_ARG, NO_PLAN. */
+int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
+
+/* Attention for one layer with the current plan.
+ *   q    : device bf16 [batch][Hq][D], contiguous, 16-byte aligned
+ *   kv   : device bf16 [num_pages][2][P][Hkv][D] (NHD), 16-byte aligned
+ *   out  : device bf16 [batch][Hq][D]
+ *   lse  : device fp32 [batch][Hq] or NULL (natural-log LSE of the scaled
+ *          scores)
+ * expect_epoch: 0 accepts any plan; otherwise must equal the current plan's
+ * epoch (STALE_PLAN otherwise).  Launches the decode kernel and the merge
+ * kernel on `stream`.  Errors: INVALID_ARG, NO_PLAN, STALE_PLAN, CUDA. */
+int pkd_run(pkd_ctx *ctx, const void *q, const void *kv, void *out, float *lse,
+            uint64_t expect_epoch, void *stream);
+
+/* merge_states: for each of n x heads rows,
+ *   m = max(s_a, s_b), w_a = exp(s_a - m), w_b = exp(s_b - m),
+ *   v = (w_a v_a + w_b v_b) / (w_a + w_b), s = m + log(w_a + w_b)
+ * (FlashInfer 完全拆解, 在线 Softmax 为什么允许任意切块; FlashInfer, in
+ * depth, "Load balancing with split-KV").  s = -inf marks an empty state;
+ * two empty states give v = 0, s = -inf.
+ *   v_a, v_b, v_out : device bf16 [n][heads][head_dim], 16-byte aligned
+ *   s_a, s_b, s_out : device fp32 [n][heads]
+ * head_dim must be a multiple of 8.  v_out may alias v_a or v_b, s_out may
+ * alias s_a or s_b.  Errors: INVALID_ARG, CUDA. */
+int pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
+                     const float *s_b, void *v_out, float *s_out, int32_t n,
+                     int32_t heads, int32_t head_dim, void *stream);
+
+/* Read and clear the device error word (synchronizes `stream`).
+ * *dev_err receives PKD_DEV_ERR_* bits (0 = none). */
+int pkd_last_device_error(pkd_ctx *ctx, void *stream, int32_t *dev_err);
+
+/* Copy the schedule in the device workspace back to the host (test aid;
+ * synchronizes `stream`).  Writes the same words pkd_plan_host produces. */
+int pkd_read_schedule(pkd_ctx *ctx, int32_t *host_words, size_t max_words,
+                      void *stream);
+
+/* The planner alone, on the host, without CUDA: validates the table and
+ * writes the schedule words for `num_ctas` CTAs into host_words (layout:
+ * see pkd_schedule_layout).  cfg->num_ctas must be > 0.  Errors:
+ * INVALID_ARG, BAD_TABLE, CAPACITY. */
+int pkd_plan_host(const pkd_config *cfg, const int32_t *indptr,
+                  const int32_t *indices, const int32_t *last_page_len,
+                  int32_t batch, int32_t *host_words, size_t max_words,
+                  pkd_plan_info *info);
+
+/* Word offsets of the schedule arrays (see pkd_plan_host):
+ *   off[0] cta_indptr[num_ctas + 1]
+ *   off[1] items[num_items][8] = {req, tok_begin, tok_end, dst_slot,
+ *                                 page_off, 0, 0, 0}
+ *   off[2] units[num_units][2] = {req, num_chunks}
+ *   off[3] merge_indptr[num_units + 1]
+ *   off[4] page_list[nnz]
+ *   off[5] total words
+ * Header words 0..15 hold: magic, batch, Hq, Hkv, D, P, num_ctas,
+ * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (low 31
+ * bits), 0, 0.  Errors: INVALID_ARG. */
+int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
+
+/* ---- CUDA-graph capture of a whole decode step ------------------------- */
+/* Capture `layers` pkd_run calls (the current plan's workspace is read at
+ * replay time, so re-planning between replays is allowed as long as batch
+ * and capacities fit) into a graph.  Arrays of device pointers, one per
+ * layer.  flags: PKD_GRAPH_TIMING records an event before and after each
+ * layer's decode kernel, readable with pkd_graph_layer_times.
+ * Errors: INVALID_ARG, NO_PLAN, CUDA. */
+#define PKD_GRAPH_TIMING 1u
+int pkd_graph_capture(pkd_ctx *ctx, int32_t layers, const void *const *q,
+                      const void *const *kv, void *const *out,
+                      float *const *lse, uint32_t flags, pkd_graph **graph);
+/* Launch the captured step on `stream`.  Errors: INVALID_ARG, CUDA. */
+int pkd_graph_launch(pkd_graph *graph, void *stream);
+/* After the launch has completed: decode-kernel milliseconds per layer
+ * (ms[layers]) of the most recent launch.  Errors: INVALID_ARG, CUDA. */
+int pkd_graph_layer_times(pkd_graph *graph, float *ms);
+void pkd_graph_destroy(pkd_graph *graph);
+
+/* Human-readable name of a status code. */
+const char *pkd_status_str(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pkd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKD_H_ */

@@ -1,0 +1,395 @@
+"""Paged-KV GQA decode attention for GB300 -- thin Python binding of libpkd.
+
+Every step of the computation runs in the CUDA library (``libpkd.so``, built
+in-tree by :func:`build`); this module only marshals arguments: it checks
+dtypes, shapes and devices, passes ``tensor.data_ptr()`` and the current
+CUDA stream through ctypes, and raises on a non-zero status.  There is no
+fallback: if the library is missing or was built for another machine, the
+import of the binding fails loudly.
+
+API (names follow the pages' plan / run / merge_states):
+
+* :class:`BatchDecodeWithPagedKVCache` -- ``plan(indptr, indices,
+  last_page_len)`` once per step, ``run(q, kv_cache)`` once per layer,
+  ``capture(...)`` for a CUDA graph of a whole step.
+* :func:`merge_states` -- exact LSE merge of two attention states.
+* :func:`plan_host` -- the scheduler alone on the host (no GPU), for tests.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states",
+    "plan_host", "schedule_layout", "Graph", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkd.so")
+
+STATUS = {
+    0: "PKD_OK", -1: "PKD_E_INVALID_ARG", -2: "PKD_E_BAD_TABLE",
+    -3: "PKD_E_UNSUPPORTED_SHAPE", -4: "PKD_E_WORKSPACE_TOO_SMALL",
+    -5: "PKD_E_NO_PLAN", -6: "PKD_E_STALE_PLAN", -7: "PKD_E_CAPACITY",
+    -8: "PKD_E_CUDA", -9: "PKD_E_DEVICE",
+}
+DEV_ERR_TIMEOUT = 1
+DEV_ERR_BOUNDS = 2
+GRAPH_TIMING = 1
+
+# Every entry point the C header declares (tests check the exports).
+EXPORTS = (
+    "pkd_workspace_bytes", "pkd_create", "pkd_destroy", "pkd_plan",
+    "pkd_get_plan_info", "pkd_run", "pkd_merge_states", "pkd_last_device_error",
+    "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
+    "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
+    "pkd_graph_destroy", "pkd_status_str", "pkd_version",
+)
+
+
+class PkdError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{what}: {self.name}" if what else self.name)
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_qo_heads", "num_kv_heads", "head_dim", "page_size", "max_batch",
+        "max_num_pages", "num_pages", "alpha", "min_chunk_tokens", "num_ctas")] + [
+        ("flags", ctypes.c_uint32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("chunk_tokens", ctypes.c_int32), ("num_items", ctypes.c_int32),
+                ("num_units", ctypes.c_int32), ("num_slots", ctypes.c_int32),
+                ("total_tokens", ctypes.c_int64), ("makespan", ctypes.c_int64),
+                ("nnz", ctypes.c_int32), ("schedule_words", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def build(force: bool = False) -> str:
+    """Compile libpkd.so for sm_103a (in-tree)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+_lib = None
+
+
+def load():
+    """Load libpkd.so (must have been built with :func:`build`)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "paged_kv_decode_host_gb300.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, u32, u64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32,
+                             ctypes.c_uint64, ctypes.c_size_t)
+    cfgp = ctypes.POINTER(Config)
+    sig = {
+        "pkd_workspace_bytes": (sz, [cfgp]),
+        "pkd_create": (ctypes.c_int, [cfgp, vp, sz, ctypes.POINTER(vp)]),
+        "pkd_destroy": (None, [vp]),
+        "pkd_plan": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, ctypes.POINTER(u64)]),
+        "pkd_get_plan_info": (ctypes.c_int, [vp, ctypes.POINTER(PlanInfo)]),
+        "pkd_run": (ctypes.c_int, [vp, vp, vp, vp, vp, u64, vp]),
+        "pkd_merge_states": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
+        "pkd_last_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
+        "pkd_read_schedule": (ctypes.c_int, [vp, vp, sz, vp]),
+        "pkd_plan_host": (ctypes.c_int, [cfgp, vp, vp, vp, i32, vp, sz,
+                                         ctypes.POINTER(PlanInfo)]),
+        "pkd_schedule_layout": (ctypes.c_int, [cfgp, vp]),
+        "pkd_graph_capture": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, u32, ctypes.POINTER(vp)]),
+        "pkd_graph_launch": (ctypes.c_int, [vp, vp]),
+        "pkd_graph_layer_times": (ctypes.c_int, [vp, vp]),
+        "pkd_graph_destroy": (None, [vp]),
+        "pkd_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "pkd_version": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status, what):
+    if status != 0:
+        raise PkdError(status, what)
+
+
+def _host_i32(a) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            if a.is_cuda:
+                raise ValueError("page-table arrays are host arrays (the planner runs on the CPU)")
+            if a.dtype != torch.int32:
+                raise TypeError("page-table arrays must be int32")
+            return np.ascontiguousarray(a.numpy())
+    except ImportError:
+        pass
+    arr = np.asarray(a)
+    if arr.dtype != np.int32:
+        raise TypeError("page-table arrays must be int32 (int64 indices are rejected)")
+    return np.ascontiguousarray(arr)
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a.size else ctypes.c_void_p(0)
+
+
+def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
+                num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0) -> Config:
+    return Config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
+                  num_pages, alpha, min_chunk_tokens, num_ctas, 0)
+
+
+def schedule_layout(cfg: Config):
+    lib = load()
+    off = (ctypes.c_int64 * 6)()
+    _check(lib.pkd_schedule_layout(ctypes.byref(cfg), off), "pkd_schedule_layout")
+    return list(off)
+
+
+def plan_host(cfg: Config, indptr, indices, last_page_len):
+    """Run the C++ scheduler on the host.  Returns (words, info dict, layout)."""
+    lib = load()
+    indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
+    off = schedule_layout(cfg)
+    words = np.zeros(off[5], dtype=np.int32)
+    info = PlanInfo()
+    st = lib.pkd_plan_host(ctypes.byref(cfg), _ptr(indptr), _ptr(indices), _ptr(last),
+                           int(last.shape[0]), _ptr(words), words.size, ctypes.byref(info))
+    _check(st, "pkd_plan_host")
+    return words, info.as_dict(), off
+
+
+def decode_schedule(words, off, info):
+    """Unpack schedule words into python lists (same shape as the plan
+    restatement's fields)."""
+    n_cta, n_items, n_units, nnz = (info["num_ctas"], info["num_items"], info["num_units"],
+                                    info["nnz"])
+    cta_indptr = words[off[0]:off[0] + n_cta + 1].tolist()
+    it = words[off[1]:off[1] + 8 * n_items].reshape(n_items, 8)
+    items = [tuple(int(x) for x in r[:5]) for r in it]
+    un = words[off[2]:off[2] + 2 * n_units].reshape(n_units, 2)
+    units = [tuple(int(x) for x in r) for r in un]
+    merge_indptr = words[off[3]:off[3] + n_units + 1].tolist()
+    page_list = words[off[4]:off[4] + nnz].tolist()
+    return dict(cta_indptr=cta_indptr, items=items, units=units, merge_indptr=merge_indptr,
+                page_list=page_list, header=words[:16].tolist())
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Graph:
+    """A captured decode step (``layers`` runs with fixed pointers)."""
+
+    def __init__(self, owner, handle, layers, keep):
+        self._owner = owner
+        self._h = handle
+        self.layers = layers
+        self._keep = keep  # tensors whose addresses the graph holds
+
+    def launch(self, stream=None):
+        _check(load().pkd_graph_launch(self._h, _stream_ptr(stream)), "pkd_graph_launch")
+
+    def layer_times(self):
+        """Decode-kernel milliseconds of each layer in the last launch."""
+        ms = (ctypes.c_float * self.layers)()
+        _check(load().pkd_graph_layer_times(self._h, ms), "pkd_graph_layer_times")
+        return list(ms)
+
+    def close(self):
+        if self._h:
+            load().pkd_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class BatchDecodeWithPagedKVCache:
+    """Plan once per decode step, run once per layer.
+
+    The workspace is one device tensor allocated here with torch (its size
+    and layout come from the library) and kept at a fixed address for the
+    object's life.  bf16 only; KV layout NHD ``[pages, 2, P, Hkv, D]``.
+    """
+
+    def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
+                 max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
+                 kv_layout="NHD", device=None):
+        import torch
+        if kv_layout != "NHD":
+            raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
+        lib = load()
+        self.device = torch.device("cuda" if device is None else device)
+        self.hq, self.hkv, self.d, self.p = num_qo_heads, num_kv_heads, head_dim, page_size
+        self.num_pages = num_pages
+        self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch,
+                               max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas)
+        with torch.cuda.device(self.device):
+            nbytes = lib.pkd_workspace_bytes(ctypes.byref(self.cfg))
+            if nbytes == 0:
+                raise PkdError(-3, "pkd_workspace_bytes (invalid or unsupported configuration)")
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            h = ctypes.c_void_p()
+            _check(lib.pkd_create(ctypes.byref(self.cfg), ctypes.c_void_p(self.workspace.data_ptr()),
+                                  nbytes, ctypes.byref(h)), "pkd_create")
+        self._h = h
+        self.epoch = 0
+        self.batch = None
+
+    # -- plan ---------------------------------------------------------------
+    def plan(self, indptr, indices, last_page_len, stream=None):
+        """Schedule one decode step from host int32 arrays.  Returns the epoch."""
+        lib = load()
+        indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
+        batch = int(last.shape[0])
+        if indptr.shape[0] != batch + 1:
+            raise PkdError(-2, "indptr must have batch + 1 entries")
+        if batch and indices.shape[0] < int(indptr[-1]):
+            raise PkdError(-2, "indices shorter than indptr[-1]")
+        ep = ctypes.c_uint64()
+        _check(lib.pkd_plan(self._h, _ptr(indptr), _ptr(indices), _ptr(last), batch,
+                            _stream_ptr(stream), ctypes.byref(ep)), "pkd_plan")
+        self.epoch = ep.value
+        self.batch = batch
+        return self.epoch
+
+    def plan_info(self):
+        info = PlanInfo()
+        _check(load().pkd_get_plan_info(self._h, ctypes.byref(info)), "pkd_get_plan_info")
+        return info.as_dict()
+
+    def schedule(self, stream=None):
+        """The schedule words currently in the device workspace."""
+        info = self.plan_info()
+        off = schedule_layout(self._layout_cfg(info))
+        words = np.zeros(off[4] + info["nnz"], dtype=np.int32)
+        _check(load().pkd_read_schedule(self._h, _ptr(words), words.size, _stream_ptr(stream)),
+               "pkd_read_schedule")
+        return words, info, off
+
+    def _layout_cfg(self, info):
+        c = Config.from_buffer_copy(self.cfg)
+        c.num_ctas = info["num_ctas"]
+        return c
+
+    # -- run ----------------------------------------------------------------
+    def _check_run_args(self, q, kv_cache, out, lse):
+        import torch
+        if self.batch is None:
+            raise PkdError(-5, "run before plan")
+        B = self.batch
+        for name, t, dt in (("q", q, torch.bfloat16), ("kv_cache", kv_cache, torch.bfloat16),
+                            ("out", out, torch.bfloat16)):
+            if t.dtype != dt:
+                raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+            if t.device != self.device and not (t.is_cuda and self.device.index is None):
+                raise ValueError(f"{name} is on {t.device}, the plan on {self.device}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        if tuple(q.shape) != (B, self.hq, self.d):
+            raise ValueError(f"q shape {tuple(q.shape)} != planned {(B, self.hq, self.d)}")
+        if tuple(out.shape) != (B, self.hq, self.d):
+            raise ValueError(f"out shape {tuple(out.shape)} != {(B, self.hq, self.d)}")
+        if tuple(kv_cache.shape) != (self.num_pages, 2, self.p, self.hkv, self.d):
+            raise ValueError(f"kv_cache shape {tuple(kv_cache.shape)} is not NHD "
+                             f"{(self.num_pages, 2, self.p, self.hkv, self.d)}")
+        if lse is not None:
+            if lse.dtype != torch.float32 or tuple(lse.shape) != (B, self.hq) or not lse.is_contiguous():
+                raise ValueError("lse must be contiguous float32 [batch, Hq]")
+
+    def run(self, q, kv_cache, out=None, lse=None, return_lse=True, expect_epoch=0,
+            stream=None):
+        """Attention for one layer.  Returns (out, lse) or out."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+        self._check_run_args(q, kv_cache, out, lse)
+        st = load().pkd_run(self._h, ctypes.c_void_p(q.data_ptr()),
+                            ctypes.c_void_p(kv_cache.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                            ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                            int(expect_epoch), _stream_ptr(stream))
+        _check(st, "pkd_run")
+        return (out, lse) if return_lse else out
+
+    def capture(self, qs, kvs, outs, lses=None, timing=False) -> Graph:
+        """Capture len(qs) runs (one decode step over all layers) in a graph."""
+        n = len(qs)
+        for l in range(n):
+            self._check_run_args(qs[l], kvs[l], outs[l], lses[l] if lses else None)
+        P = ctypes.c_void_p * n
+        q_arr = P(*[t.data_ptr() for t in qs])
+        kv_arr = P(*[t.data_ptr() for t in kvs])
+        o_arr = P(*[t.data_ptr() for t in outs])
+        l_arr = P(*[t.data_ptr() for t in lses]) if lses else None
+        h = ctypes.c_void_p()
+        as_vp = lambda a: ctypes.cast(a, ctypes.c_void_p) if a is not None else None
+        st = load().pkd_graph_capture(self._h, n, as_vp(q_arr), as_vp(kv_arr), as_vp(o_arr),
+                                      as_vp(l_arr),
+                                      GRAPH_TIMING if timing else 0, ctypes.byref(h))
+        _check(st, "pkd_graph_capture")
+        return Graph(self, h, n, (list(qs), list(kvs), list(outs), list(lses or [])))
+
+    def device_error(self, stream=None) -> int:
+        v = ctypes.c_int32()
+        _check(load().pkd_last_device_error(self._h, _stream_ptr(stream), ctypes.byref(v)),
+               "pkd_last_device_error")
+        return v.value
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().pkd_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def merge_states(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):
+    """Exact merge of two attention states: v [n, H, D] bf16, s [n, H] fp32."""
+    import torch
+    for name, t, dt in (("v_a", v_a, torch.bfloat16), ("v_b", v_b, torch.bfloat16),
+                        ("s_a", s_a, torch.float32), ("s_b", s_b, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if v_a.shape != v_b.shape or s_a.shape != s_b.shape or tuple(s_a.shape) != tuple(v_a.shape[:2]):
+        raise ValueError("shape mismatch between the two states")
+    if v_out is None:
+        v_out = torch.empty_like(v_a)
+    if s_out is None:
+        s_out = torch.empty_like(s_a)
+    n, H, D = v_a.shape
+    st = load().pkd_merge_states(ctypes.c_void_p(v_a.data_ptr()), ctypes.c_void_p(s_a.data_ptr()),
+                                 ctypes.c_void_p(v_b.data_ptr()), ctypes.c_void_p(s_b.data_ptr()),
+                                 ctypes.c_void_p(v_out.data_ptr()),
+                                 ctypes.c_void_p(s_out.data_ptr()), n, H, D, _stream_ptr(stream))
+    _check(st, "pkd_merge_states")
+    return v_out, s_out

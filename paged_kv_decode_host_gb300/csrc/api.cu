@@ -1,0 +1,419 @@
+// C ABI of libpkd: context, workspace, plan publication, run, merge_states,
+// CUDA-graph capture.  Host runtime only; the kernels live in
+// decode_kernel.cu and merge_kernels.cu, the scheduler in planner.cpp.
+//
+// Plan publication follows FlashInfer 完全拆解, 固定指针比固定内容更重要: the
+// schedule is written into page-locked host staging and copied with
+// cudaMemcpyAsync into fixed offsets of the caller's device workspace, so a
+// captured run sees new contents at the same addresses.  Staging is
+// double-buffered; an event per buffer keeps a pending copy from being
+// overwritten.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "pkd_internal.h"
+
+using namespace pkd;
+
+struct pkd_ctx {
+  pkd_config cfg;
+  int32_t n_cta = 0;
+  int32_t group = 0;
+  int smem_bytes = 0;
+  int merge_grid = 0;
+  int device = 0;
+  Layout layout{};
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  int32_t* staging[2] = {nullptr, nullptr};
+  cudaEvent_t staged[2] = {nullptr, nullptr};
+  bool staged_pending[2] = {false, false};
+  int next_staging = 0;
+  uint64_t epoch = 0;
+  pkd_plan_info info{};
+};
+
+struct pkd_graph {
+  pkd_ctx* ctx = nullptr;
+  int32_t layers = 0;
+  cudaGraphExec_t exec = nullptr;
+  std::vector<cudaEvent_t> ev;  // [2 * layers] when timing
+};
+
+namespace {
+
+bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+int check_config(const pkd_config* c) {
+  if (c == nullptr) return PKD_E_INVALID_ARG;
+  if (c->flags != 0) return PKD_E_INVALID_ARG;
+  if (c->max_batch < 0 || c->max_num_pages < 0 || c->num_pages < 1 || c->page_size < 1 ||
+      c->num_ctas < 0)
+    return PKD_E_INVALID_ARG;
+  if (c->head_dim != kHeadDim) return PKD_E_UNSUPPORTED_SHAPE;
+  if (c->num_kv_heads < 1 || c->num_kv_heads > kMaxKvHeads) return PKD_E_UNSUPPORTED_SHAPE;
+  if (c->num_qo_heads < 1 || c->num_qo_heads % c->num_kv_heads != 0)
+    return PKD_E_UNSUPPORTED_SHAPE;
+  if (!valid_group(c->num_qo_heads / c->num_kv_heads)) return PKD_E_UNSUPPORTED_SHAPE;
+  // a page must fit the copy-size and tx-count limits of one stage
+  if ((int64_t)c->page_size * c->num_kv_heads * kHeadDim * 2 * 2 > (int64_t)1 << 30)
+    return PKD_E_UNSUPPORTED_SHAPE;
+  return PKD_OK;
+}
+
+int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
+  const int g = c->num_qo_heads / c->num_kv_heads;
+  *smem_bytes = decode_smem_bytes(c->num_kv_heads, g);
+  if (c->num_ctas > 0) {
+    *n_cta = c->num_ctas;
+    return PKD_OK;
+  }
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKD_E_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (decode_prepare(g, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
+  if (decode_occupancy(g, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (per_sm < 1) return PKD_E_UNSUPPORTED_SHAPE;
+  *n_cta = sms * per_sm;
+  return PKD_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
+               cudaStream_t stream, cudaEvent_t ev_before, cudaEvent_t ev_after) {
+  const pkd_config& c = ctx->cfg;
+  DecodeArgs a{};
+  a.sched = reinterpret_cast<const int32_t*>(ctx->ws);
+  a.o_part = reinterpret_cast<float*>(ctx->ws + ctx->layout.o_part_byte);
+  a.l_part = reinterpret_cast<float*>(ctx->ws + ctx->layout.l_part_byte);
+  a.err = reinterpret_cast<int32_t*>(ctx->ws + ctx->layout.err_byte);
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv = static_cast<const uint8_t*>(kv);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.row_bytes = c.num_kv_heads * kHeadDim * 2;
+  a.page_bytes = (int64_t)2 * c.page_size * a.row_bytes;
+  a.off_cta = ctx->layout.cta_indptr;
+  a.off_items = ctx->layout.items;
+  a.off_pages = ctx->layout.page_list;
+  a.hq = c.num_qo_heads;
+  a.hkv = c.num_kv_heads;
+  a.page_size = c.page_size;
+  a.num_pages = c.num_pages;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (launch_decode(ctx->group, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
+      cudaSuccess)
+    return PKD_E_CUDA;
+  if (ev_after && cudaEventRecordWithFlags(ev_after, stream, cudaEventRecordExternal) != cudaSuccess)
+    return PKD_E_CUDA;
+  MergeArgs m{};
+  m.sched = a.sched;
+  m.o_part = a.o_part;
+  m.l_part = a.l_part;
+  m.out = a.out;
+  m.lse = lse;
+  m.off_units = ctx->layout.units;
+  m.off_merge = ctx->layout.merge_indptr;
+  m.hq = c.num_qo_heads;
+  if (launch_merge_partials(m, ctx->merge_grid, stream) != cudaSuccess) return PKD_E_CUDA;
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkd_version(void) { return 100; }
+
+const char* pkd_status_str(int s) {
+  switch (s) {
+    case PKD_OK: return "ok";
+    case PKD_E_INVALID_ARG: return "invalid argument";
+    case PKD_E_BAD_TABLE: return "bad page table (indptr / indices / last_page_len)";
+    case PKD_E_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case PKD_E_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKD_E_NO_PLAN: return "run before plan";
+    case PKD_E_STALE_PLAN: return "stale plan (epoch mismatch)";
+    case PKD_E_CAPACITY: return "batch or page count above the configured capacity";
+    case PKD_E_CUDA: return "CUDA runtime error";
+    case PKD_E_DEVICE: return "device error word set";
+    default: return "unknown status";
+  }
+}
+
+int pkd_schedule_layout(const pkd_config* cfg, int64_t off[6]) {
+  if (off == nullptr) return PKD_E_INVALID_ARG;
+  int st = check_config(cfg);
+  if (st != PKD_OK) return st;
+  if (cfg->num_ctas < 1) return PKD_E_INVALID_ARG;
+  Layout L = make_layout(*cfg, cfg->num_ctas);
+  off[0] = L.cta_indptr;
+  off[1] = L.items;
+  off[2] = L.units;
+  off[3] = L.merge_indptr;
+  off[4] = L.page_list;
+  off[5] = L.words;
+  return PKD_OK;
+}
+
+int pkd_plan_host(const pkd_config* cfg, const int32_t* indptr, const int32_t* indices,
+                  const int32_t* last_page_len, int32_t batch, int32_t* host_words,
+                  size_t max_words, pkd_plan_info* info) {
+  int st = check_config(cfg);
+  if (st != PKD_OK) return st;
+  if (cfg->num_ctas < 1 || host_words == nullptr) return PKD_E_INVALID_ARG;
+  Layout L = make_layout(*cfg, cfg->num_ctas);
+  if (max_words < (size_t)L.words) return PKD_E_INVALID_ARG;
+  return plan_schedule(*cfg, cfg->num_ctas, L, indptr, indices, last_page_len, batch,
+                       host_words, info);
+}
+
+size_t pkd_workspace_bytes(const pkd_config* cfg) {
+  if (check_config(cfg) != PKD_OK) return 0;
+  int32_t n_cta = 0;
+  int smem = 0;
+  if (resolve_ctas(cfg, &n_cta, &smem) != PKD_OK) return 0;
+  return make_layout(*cfg, n_cta).total_bytes;
+}
+
+int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
+               pkd_ctx** out) {
+  if (out == nullptr) return PKD_E_INVALID_ARG;
+  *out = nullptr;
+  int st = check_config(cfg);
+  if (st != PKD_OK) return st;
+  if (d_workspace == nullptr || !aligned(d_workspace, 256)) return PKD_E_INVALID_ARG;
+  pkd_ctx* ctx = new (std::nothrow) pkd_ctx();
+  if (!ctx) return PKD_E_INVALID_ARG;
+  ctx->cfg = *cfg;
+  ctx->group = cfg->num_qo_heads / cfg->num_kv_heads;
+  st = resolve_ctas(cfg, &ctx->n_cta, &ctx->smem_bytes);
+  if (st != PKD_OK) {
+    delete ctx;
+    return st;
+  }
+  if (decode_prepare(ctx->group, ctx->smem_bytes) != cudaSuccess) {
+    delete ctx;
+    return PKD_E_CUDA;
+  }
+  ctx->layout = make_layout(*cfg, ctx->n_cta);
+  if (workspace_bytes < ctx->layout.total_bytes) {
+    delete ctx;
+    return PKD_E_WORKSPACE_TOO_SMALL;
+  }
+  cudaGetDevice(&ctx->device);
+  ctx->merge_grid = ctx->n_cta;
+  ctx->ws = static_cast<uint8_t*>(d_workspace);
+  ctx->ws_bytes = workspace_bytes;
+  for (int k = 0; k < 2; ++k) {
+    if (cudaMallocHost(&ctx->staging[k], (size_t)ctx->layout.words * 4) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->staged[k], cudaEventDisableTiming) != cudaSuccess) {
+      pkd_destroy(ctx);
+      return PKD_E_CUDA;
+    }
+    std::memset(ctx->staging[k], 0, (size_t)ctx->layout.words * 4);
+  }
+  if (cudaMemset(ctx->ws + ctx->layout.err_byte, 0, 4) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    pkd_destroy(ctx);
+    return PKD_E_CUDA;
+  }
+  *out = ctx;
+  return PKD_OK;
+}
+
+void pkd_destroy(pkd_ctx* ctx) {
+  if (!ctx) return;
+  for (int k = 0; k < 2; ++k) {
+    if (ctx->staged[k]) {
+      cudaEventSynchronize(ctx->staged[k]);
+      cudaEventDestroy(ctx->staged[k]);
+    }
+    if (ctx->staging[k]) cudaFreeHost(ctx->staging[k]);
+  }
+  delete ctx;
+}
+
+int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
+             const int32_t* last_page_len, int32_t batch, void* stream, uint64_t* epoch) {
+  if (ctx == nullptr) return PKD_E_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int k = ctx->next_staging;
+  if (ctx->staged_pending[k]) {
+    if (cudaEventSynchronize(ctx->staged[k]) != cudaSuccess) return PKD_E_CUDA;
+    ctx->staged_pending[k] = false;
+  }
+  int32_t* words = ctx->staging[k];
+  pkd_plan_info info{};
+  int st = plan_schedule(ctx->cfg, ctx->n_cta, ctx->layout, indptr, indices, last_page_len,
+                         batch, words, &info);
+  if (st != PKD_OK) return st;
+  const Layout& L = ctx->layout;
+  // fixed-size part: header, cta queues, items, units, merge map
+  if (cudaMemcpyAsync(ctx->ws, words, (size_t)L.page_list * 4, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return PKD_E_CUDA;
+  if (info.nnz > 0 &&
+      cudaMemcpyAsync(ctx->ws + (size_t)L.page_list * 4, words + L.page_list,
+                      (size_t)info.nnz * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (cudaEventRecord(ctx->staged[k], s) != cudaSuccess) return PKD_E_CUDA;
+  ctx->staged_pending[k] = true;
+  ctx->next_staging = k ^ 1;
+  ctx->info = info;
+  ctx->epoch += 1;
+  if (epoch) *epoch = ctx->epoch;
+  return PKD_OK;
+}
+
+int pkd_get_plan_info(const pkd_ctx* ctx, pkd_plan_info* info) {
+  if (ctx == nullptr || info == nullptr) return PKD_E_INVALID_ARG;
+  if (ctx->epoch == 0) return PKD_E_NO_PLAN;
+  *info = ctx->info;
+  return PKD_OK;
+}
+
+int pkd_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
+            uint64_t expect_epoch, void* stream) {
+  if (ctx == nullptr) return PKD_E_INVALID_ARG;
+  if (ctx->epoch == 0) return PKD_E_NO_PLAN;
+  if (expect_epoch != 0 && expect_epoch != ctx->epoch) return PKD_E_STALE_PLAN;
+  if (ctx->info.batch > 0) {
+    if (q == nullptr || kv == nullptr || out == nullptr) return PKD_E_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(lse, 4))
+      return PKD_E_INVALID_ARG;
+  }
+  return launch_run(ctx, q, kv, out, lse, static_cast<cudaStream_t>(stream), nullptr, nullptr);
+}
+
+int pkd_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b,
+                     void* v_out, float* s_out, int32_t n, int32_t heads, int32_t head_dim,
+                     void* stream) {
+  if (n < 0 || heads < 0 || head_dim < 8 || head_dim % 8 != 0 || head_dim / 8 > 256)
+    return PKD_E_INVALID_ARG;
+  const int64_t rows = (int64_t)n * heads;
+  if (rows == 0) return PKD_OK;
+  if (!v_a || !s_a || !v_b || !s_b || !v_out || !s_out) return PKD_E_INVALID_ARG;
+  if (!aligned(v_a, 16) || !aligned(v_b, 16) || !aligned(v_out, 16) || !aligned(s_a, 4) ||
+      !aligned(s_b, 4) || !aligned(s_out, 4))
+    return PKD_E_INVALID_ARG;
+  if (launch_merge_states(v_a, s_a, v_b, s_b, v_out, s_out, rows, head_dim,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKD_E_CUDA;
+  return PKD_OK;
+}
+
+int pkd_last_device_error(pkd_ctx* ctx, void* stream, int32_t* dev_err) {
+  if (ctx == nullptr || dev_err == nullptr) return PKD_E_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKD_E_CUDA;
+  if (cudaMemcpy(&v, ctx->ws + ctx->layout.err_byte, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (cudaMemset(ctx->ws + ctx->layout.err_byte, 0, 4) != cudaSuccess) return PKD_E_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKD_E_CUDA;
+  *dev_err = v;
+  return PKD_OK;
+}
+
+int pkd_read_schedule(pkd_ctx* ctx, int32_t* host_words, size_t max_words, void* stream) {
+  if (ctx == nullptr || host_words == nullptr) return PKD_E_INVALID_ARG;
+  if (ctx->epoch == 0) return PKD_E_NO_PLAN;
+  const size_t words = (size_t)ctx->layout.page_list + (size_t)ctx->info.nnz;
+  if (max_words < words) return PKD_E_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKD_E_CUDA;
+  if (cudaMemcpy(host_words, ctx->ws, words * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKD_E_CUDA;
+  return PKD_OK;
+}
+
+int pkd_graph_capture(pkd_ctx* ctx, int32_t layers, const void* const* q, const void* const* kv,
+                      void* const* out, float* const* lse, uint32_t flags, pkd_graph** graph) {
+  if (ctx == nullptr || graph == nullptr || layers < 1 || q == nullptr || kv == nullptr ||
+      out == nullptr)
+    return PKD_E_INVALID_ARG;
+  if ((flags & ~PKD_GRAPH_TIMING) != 0) return PKD_E_INVALID_ARG;
+  *graph = nullptr;
+  if (ctx->epoch == 0) return PKD_E_NO_PLAN;
+  for (int l = 0; l < layers; ++l) {
+    if (!q[l] || !kv[l] || !out[l] || !aligned(q[l], 16) || !aligned(kv[l], 16) ||
+        !aligned(out[l], 16) || (lse && !aligned(lse[l], 4)))
+      return PKD_E_INVALID_ARG;
+  }
+  pkd_graph* g = new (std::nothrow) pkd_graph();
+  if (!g) return PKD_E_INVALID_ARG;
+  g->ctx = ctx;
+  g->layers = layers;
+  const bool timing = (flags & PKD_GRAPH_TIMING) != 0;
+  if (timing) {
+    g->ev.assign((size_t)2 * layers, nullptr);
+    for (auto& e : g->ev) {
+      if (cudaEventCreate(&e) != cudaSuccess) {
+        pkd_graph_destroy(g);
+        return PKD_E_CUDA;
+      }
+    }
+  }
+  cudaStream_t cs;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    pkd_graph_destroy(g);
+    return PKD_E_CUDA;
+  }
+  int st = PKD_OK;
+  cudaGraph_t graph_def = nullptr;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    st = PKD_E_CUDA;
+  } else {
+    for (int l = 0; l < layers && st == PKD_OK; ++l) {
+      st = launch_run(ctx, q[l], kv[l], out[l], lse ? lse[l] : nullptr, cs,
+                      timing ? g->ev[2 * l] : nullptr, timing ? g->ev[2 * l + 1] : nullptr);
+    }
+    if (cudaStreamEndCapture(cs, &graph_def) != cudaSuccess && st == PKD_OK) st = PKD_E_CUDA;
+  }
+  if (st == PKD_OK && cudaGraphInstantiate(&g->exec, graph_def, 0) != cudaSuccess)
+    st = PKD_E_CUDA;
+  if (graph_def) cudaGraphDestroy(graph_def);
+  cudaStreamDestroy(cs);
+  if (st != PKD_OK) {
+    pkd_graph_destroy(g);
+    return st;
+  }
+  *graph = g;
+  return PKD_OK;
+}
+
+int pkd_graph_launch(pkd_graph* g, void* stream) {
+  if (g == nullptr || g->exec == nullptr) return PKD_E_INVALID_ARG;
+  if (cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKD_E_CUDA;
+  return PKD_OK;
+}
+
+int pkd_graph_layer_times(pkd_graph* g, float* ms) {
+  if (g == nullptr || ms == nullptr || g->ev.empty()) return PKD_E_INVALID_ARG;
+  for (int l = 0; l < g->layers; ++l) {
+    if (cudaEventSynchronize(g->ev[2 * l + 1]) != cudaSuccess) return PKD_E_CUDA;
+    if (cudaEventElapsedTime(&ms[l], g->ev[2 * l], g->ev[2 * l + 1]) != cudaSuccess)
+      return PKD_E_CUDA;
+  }
+  return PKD_OK;
+}
+
+void pkd_graph_destroy(pkd_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  for (auto e : g->ev)
+    if (e) cudaEventDestroy(e);
+  delete g;
+}
+
+}  // extern "C"

@@ -1,0 +1,525 @@
+// Persistent paged-KV decode kernel for sm_103a.
+//
+// What it computes (FlashInfer 完全拆解, 从推理形状出发 and 在线 Softmax 为什么
+// 允许任意切块; FlashInfer, in depth, "GQA, tensor cores and MLA"): for each
+// work item (request, page-aligned token range) of this CTA's queue, the
+// attention state of every query head of the request over those tokens,
+//   s_t = q . k_t / sqrt(D),  O = sum_t exp(s_t - m) v_t / sum_t exp(s_t - m),
+//   L = m + log sum_t exp(s_t - m),
+// streamed with the online-softmax recurrence so scores never reach HBM.
+// Unsplit items write (O, L) straight to out / lse ("writethrough"); chunks
+// of split requests write (O, L) to their partial slot for the merge kernel.
+//
+// GB300 design:
+//  * Grid = the plan's fixed CTA count (persistent; only the queue contents
+//    change between plans, so launches can be captured in a CUDA graph).
+//  * One producer warp streams the item's pages into a 3-deep ring of
+//    shared-memory stages with TMA bulk copies (cp.async.bulk, completion on
+//    an mbarrier).  A stage holds 16 tokens x all KV heads of K and of V.
+//    In the NHD layout the K rows of one page are one contiguous block for
+//    all heads (and so are the V rows), so a full 16-token page is two 32 KiB
+//    copies; page size 1 gives 2 KiB copies per token.  Only valid slots are
+//    copied.
+//  * One consumer warp per KV head folds its GQA group of G query heads onto
+//    each K/V row it reads from shared memory (one read serves G heads).
+//    Lanes split D: half-warp hw takes tokens of parity hw, lane li owns
+//    dims [8 li, 8 li + 8).  Dot-product partials of 8 (or 4) token steps
+//    are reduce-scattered across the half-warp with shuffles, so each lane
+//    ends with whole scores for one head; the online-softmax update uses
+//    shuffles within the head's lane group; probabilities go through a small
+//    per-warp shared buffer to the P.V accumulation, which is lane-owned per
+//    dim.  All arithmetic is fp32 (bf16 inputs widened exactly).
+//  * Every wait is bounded (~2 s of %globaltimer); on timeout the kernel sets
+//    the device error word, stops issuing copies, waits (bounded) for the
+//    copies already in flight, and returns.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "pkd_internal.h"
+
+namespace pkd {
+namespace {
+
+constexpr int kTS = kWarpTokens;                 // tokens per stage
+constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns
+// false on timeout, or when `abort_flag` (if given) is raised.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (global_ns() - t0 > kTimeoutNs) return false;
+    }
+  }
+}
+
+// 1-D TMA bulk copy global -> shared, completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void raise_error(int32_t* err, volatile int* abort_flag, int code) {
+  atomicOr(err, code);
+  *abort_flag = 1;
+}
+
+// 8 bf16 (one uint4) -> 8 fp32, exact.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 r, float (&f)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs; NaN kept NaN).
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+// One reduce-scatter level across lanes `mask` apart: lanes with the mask
+// bit set keep the upper half of v, the others the lower half; each adds the
+// partner's copy of the half it keeps.
+template <int N>
+__device__ __forceinline__ void rs_level(const float (&v)[N], float (&o)[N / 2], int mask,
+                                         bool upper) {
+#pragma unroll
+  for (int t = 0; t < N / 2; ++t) {
+    const float keep = upper ? v[N / 2 + t] : v[t];
+    const float send = upper ? v[t] : v[N / 2 + t];
+    o[t] = keep + __shfl_xor_sync(kFull, send, mask);
+  }
+}
+
+// ---------------------------------------------------------------- producer
+__device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* stages,
+                             int stage_bytes, uint64_t* full, uint64_t* empty,
+                             volatile int* abort_flag, int lane) {
+  const int P = a.page_size;
+  const int row = a.row_bytes;
+  uint32_t stage = 0;
+  bool ok = true;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
+    const int tb = item[1], te = item[2], poff = item[4];
+    for (int t = tb; t < te; t += kTS) {
+      const int n = min(kTS, te - t);
+      const int slot = (int)(stage % kStages);
+      const uint32_t round = stage / kStages;
+      // Page ids of this stage's runs (a run = consecutive slots of one page).
+      int page = -1;
+      int cnt = 0;
+      const int j = lane;
+      if (j < n) {
+        const int tok = t + j;
+        const int pslot = tok % P;
+        if (j == 0 || pslot == 0) {
+          cnt = min(n - j, P - pslot);
+          page = a.sched[a.off_pages + poff + (tok - tb) / P];
+          if ((unsigned)page >= (unsigned)a.num_pages) {
+            atomicOr(a.err, PKD_DEV_ERR_BOUNDS);
+            page = 0;
+          }
+        }
+      }
+      if (round > 0) {
+        bool w = mbar_wait(&empty[slot], (round - 1) & 1u, abort_flag);
+        if (!__all_sync(kFull, w)) {
+          if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * n * row));
+      __syncwarp();
+      if (page >= 0) {
+        const int pslot = (t + j) % P;
+        const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)pslot * row;
+        uint8_t* dk = stages + (size_t)slot * stage_bytes + (size_t)j * row;
+        uint8_t* dv = dk + (size_t)kTS * row;
+        bulk_copy_g2s(dk, src, (uint32_t)(cnt * row), &full[slot]);
+        bulk_copy_g2s(dv, src + (int64_t)P * row, (uint32_t)(cnt * row), &full[slot]);
+      }
+      // pages longer than 32 runs per stage cannot occur: kTS <= 32
+      ++stage;
+    }
+  }
+  // Drain: wait for the last issued phase of every slot, so no copy is in
+  // flight into shared memory when the CTA exits.
+  if (lane == 0) {
+    for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+      if (stage > s) {
+        const uint32_t last_round = (stage - 1 - s) / kStages;
+        if (!mbar_wait(&full[s], last_round & 1u, nullptr)) atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- consumers
+template <int G>
+struct Shape {
+  static constexpr int J = (G == 8) ? 4 : 8;   // token steps per batch (per half-warp)
+  static constexpr int NB = (kTS / 2) / J;     // batches per stage
+  static constexpr int N0 = G * J;             // partials per lane before the reduce
+  static constexpr int E = (N0 >= 16) ? N0 / 16 : 1;  // scores per lane after it
+  // li bits that index tokens within a head's lane group (the others index
+  // the head).  For G = 1 the lowest bit is a duplicate, left out.
+  static constexpr int TOKBITS = (G == 1) ? 14 : (16 / G - 1);
+};
+
+template <int G>
+__device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
+                             int stage_bytes, uint64_t* full, uint64_t* empty,
+                             volatile int* abort_flag, float* pbuf, float* sbuf, int warp,
+                             int lane) {
+  using S = Shape<G>;
+  constexpr int J = S::J, NB = S::NB, N0 = S::N0, E = S::E;
+  const int hk = warp;
+  const int hw = lane >> 4;
+  const int li = lane & 15;
+  const int row = a.row_bytes;
+
+  // Which (head, step) values this lane holds after the reduce-scatter.
+  int vbase = 0;
+  {
+    int n = N0;
+    const int masks[4] = {8, 4, 2, 1};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (n > 1) {
+        n >>= 1;
+        if (li & masks[k]) vbase += n;
+      }
+    }
+  }
+  const int my_head = vbase / J;
+  const bool leader = ((li & S::TOKBITS) == 0) && hw == 0;
+
+  uint32_t stage = 0;
+  for (int it = it0; it < it1; ++it) {
+    const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
+    const int req = item[0], tb = item[1], te = item[2], dst = item[3];
+
+    // q of this KV head's group, pre-scaled by log2(e)/sqrt(D).
+    float qf[G][8];
+    {
+      const uint16_t* qp = a.q + ((int64_t)req * a.hq + (int64_t)hk * G) * kHeadDim + 8 * li;
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(qp + (int64_t)i * kHeadDim));
+        bf16x8_to_f32(r, qf[i]);
+#pragma unroll
+        for (int d = 0; d < 8; ++d) qf[i][d] *= a.scale_log2;
+      }
+    }
+    float acc[G][8];
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+#pragma unroll
+      for (int d = 0; d < 8; ++d) acc[i][d] = 0.f;
+    float m_run = -CUDART_INF_F;  // running max (log2 units) of my_head
+    float l_run = 0.f;            // this lane's share of the running sum
+
+    for (int t = tb; t < te; t += kTS) {
+      const int n = min(kTS, te - t);
+      const int slot = (int)(stage % kStages);
+      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      if (!__all_sync(kFull, got)) {
+        if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+        return;
+      }
+      const uint8_t* ks = stages + (size_t)slot * stage_bytes + hk * (kHeadDim * 2) + li * 16;
+      const uint8_t* vs = ks + (size_t)kTS * row;
+
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (2 * b * J >= n) break;
+        // ---- scores: partial dot products over this lane's 8 dims
+        float part[N0];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int tok = 2 * (b * J + j) + hw;
+          float k8[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(ks + (size_t)tok * row), k8);
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int d = 0; d < 8; ++d) s = fmaf(qf[i][d], k8[d], s);
+            part[i * J + j] = s;
+          }
+        }
+        // ---- reduce-scatter across the 16 lanes of the half-warp
+        float sv[E];
+        {
+          float r1[N0 / 2];
+          rs_level<N0>(part, r1, 8, (li & 8) != 0);
+          float r2[N0 / 4];
+          rs_level<N0 / 2>(r1, r2, 4, (li & 4) != 0);
+          float r3[N0 / 8];
+          rs_level<N0 / 4>(r2, r3, 2, (li & 2) != 0);
+          if constexpr (N0 >= 16) {
+            float r4[N0 / 16];
+            rs_level<N0 / 8>(r3, r4, 1, (li & 1) != 0);
+#pragma unroll
+            for (int e = 0; e < E; ++e) sv[e] = r4[e];
+          } else {
+            sv[0] = r3[0] + __shfl_xor_sync(kFull, r3[0], 1);
+          }
+        }
+        // ---- online softmax for my_head over this batch's tokens
+        float mx = -CUDART_INF_F;
+        int toks[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int j = (vbase + e) % J;
+          toks[e] = 2 * (b * J + j) + hw;
+          if (toks[e] >= n) sv[e] = -CUDART_INF_F;
+          mx = fmaxf(mx, sv[e]);
+        }
+#pragma unroll
+        for (int mask = 1; mask < 16; mask <<= 1)
+          if (S::TOKBITS & mask) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, mask));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+        const float alpha = exp2f(m_run - m_use);
+        float psum = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float p = exp2f(sv[e] - m_use);
+          psum += p;
+          pbuf[toks[e] * G + my_head] = p;
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if (leader) sbuf[my_head] = alpha;
+        __syncwarp();
+        // ---- rescale and accumulate P.V over this lane's dims
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const float al = sbuf[i];
+#pragma unroll
+          for (int d = 0; d < 8; ++d) acc[i][d] *= al;
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int tok = 2 * (b * J + j) + hw;
+          const int src_row = (tok < n) ? tok : 0;   // p = 0 there; row 0 is valid
+          float p[G];
+          if constexpr (G == 8) {
+            const float4 p0 = *reinterpret_cast<const float4*>(pbuf + tok * G);
+            const float4 p1 = *reinterpret_cast<const float4*>(pbuf + tok * G + 4);
+            p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
+            p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+          } else if constexpr (G == 4) {
+            const float4 p0 = *reinterpret_cast<const float4*>(pbuf + tok * G);
+            p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
+          } else if constexpr (G == 2) {
+            const float2 p0 = *reinterpret_cast<const float2*>(pbuf + tok * G);
+            p[0] = p0.x; p[1] = p0.y;
+          } else {
+            p[0] = pbuf[tok];
+          }
+          float v8[8];
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vs + (size_t)src_row * row), v8);
+#pragma unroll
+          for (int i = 0; i < G; ++i)
+#pragma unroll
+            for (int d = 0; d < 8; ++d) acc[i][d] = fmaf(p[i], v8[d], acc[i][d]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++stage;
+    }
+
+    // ---- epilogue: combine half-warps, normalise, write
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+#pragma unroll
+      for (int d = 0; d < 8; ++d) acc[i][d] += __shfl_xor_sync(kFull, acc[i][d], 16);
+    float l = l_run;
+#pragma unroll
+    for (int mask = 1; mask < 16; mask <<= 1)
+      if (S::TOKBITS & mask) l += __shfl_xor_sync(kFull, l, mask);
+    l += __shfl_xor_sync(kFull, l, 16);
+    if (leader) {
+      sbuf[8 + my_head] = m_run;
+      sbuf[16 + my_head] = l;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      if (G > 1 ? ((i & 1) != hw) : (hw != 0)) continue;
+      const float m = sbuf[8 + i];
+      const float lsum = sbuf[16 + i];
+      const float inv = 1.f / lsum;
+      const float lse_nat = (m + log2f(lsum)) * 0.69314718055994530942f;
+      const int64_t qrow = (int64_t)req * a.hq + (int64_t)hk * G + i;
+      if (dst < 0) {
+        uint32_t w[4];
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+          w[d] = f32_to_bf16_rne(acc[i][2 * d] * inv) |
+                 (f32_to_bf16_rne(acc[i][2 * d + 1] * inv) << 16);
+        *reinterpret_cast<uint4*>(a.out + qrow * kHeadDim + 8 * li) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+        if (a.lse != nullptr && li == 0) a.lse[qrow] = lse_nat;
+      } else {
+        const int64_t prow = (int64_t)dst * a.hq + (int64_t)hk * G + i;
+        float4* o = reinterpret_cast<float4*>(a.o_part + prow * kHeadDim + 8 * li);
+        o[0] = make_float4(acc[i][0] * inv, acc[i][1] * inv, acc[i][2] * inv, acc[i][3] * inv);
+        o[1] = make_float4(acc[i][4] * inv, acc[i][5] * inv, acc[i][6] * inv, acc[i][7] * inv);
+        if (li == 0) a.l_part[prow] = lse_nat;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int stage_bytes = 2 * kTS * a.row_bytes;
+  uint8_t* stages = smem;
+  float* pbuf_all = reinterpret_cast<float*>(smem + (size_t)kStages * stage_bytes);
+  float* sbuf_all = pbuf_all + kMaxKvHeads * kTS * G;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sbuf_all + kMaxKvHeads * 32);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_cons = a.hkv;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], (uint32_t)n_cons);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int it0 = a.sched[a.off_cta + blockIdx.x];
+  const int it1 = a.sched[a.off_cta + blockIdx.x + 1];
+  if (it0 >= it1) return;
+  if (warp == n_cons) {
+    run_producer(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
+  } else if (warp < n_cons) {
+    run_consumer<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+                    pbuf_all + warp * kTS * G, sbuf_all + warp * 32, warp, lane);
+  }
+}
+
+template <int G>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&decode_kernel<G>);
+}
+
+const void* kernel_for(int group) {
+  switch (group) {
+    case 1: return kernel_ptr<1>();
+    case 2: return kernel_ptr<2>();
+    case 4: return kernel_ptr<4>();
+    case 8: return kernel_ptr<8>();
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+int decode_threads(int hkv) { return (hkv + 1) * 32; }
+
+int decode_smem_bytes(int hkv, int group) {
+  const int row = hkv * kHeadDim * 2;
+  return kStages * 2 * kTS * row + kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 +
+         2 * kStages * 8 + 16;
+}
+
+cudaError_t decode_prepare(int group, int smem_bytes) {
+  const void* k = kernel_for(group);
+  if (!k) return cudaErrorInvalidValue;
+  // The attribute is per kernel, shared by every context: always allow the
+  // largest layout (8 KV heads) so a smaller context never lowers it.
+  const int most = decode_smem_bytes(kMaxKvHeads, group);
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes > most ? smem_bytes : most);
+}
+
+cudaError_t decode_occupancy(int group, int hkv, int smem_bytes, int* blocks_per_sm) {
+  const void* k = kernel_for(group);
+  if (!k) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, decode_threads(hkv),
+                                                       (size_t)smem_bytes);
+}
+
+cudaError_t launch_decode(int group, const DecodeArgs& a, int grid, int hkv, int smem_bytes,
+                          cudaStream_t stream) {
+  const void* k = kernel_for(group);
+  if (!k) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<DecodeArgs*>(&a)};
+  return cudaLaunchKernel(k, dim3(grid), dim3(decode_threads(hkv)), args, (size_t)smem_bytes,
+                          stream);
+}
+
+}  // namespace pkd

@@ -1,0 +1,156 @@
+// Attention-state merge kernels for sm_103a.
+//
+// The algebra (FlashInfer 完全拆解, 在线 Softmax 为什么允许任意切块; FlashInfer,
+// in depth, "Load balancing with split-KV"): states (O_I, L_I) over disjoint
+// key sets combine exactly as M = max L, w = exp(L - M), O = sum w O / sum w,
+// L = M + log sum w.  Both kernels are HBM/latency-bound elementwise passes;
+// neither uses atomics, and each output is produced by one fixed sequence of
+// floating-point operations, so results are bit-reproducible.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "pkd_internal.h"
+
+namespace pkd {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0u;
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+// Contraction of split chunks (the reduction map built by the planner): for
+// each split request u and query head h, fold the partial states in slots
+// merge_indptr[u] .. merge_indptr[u+1] (chunk order) into out / lse.
+// Block = 256 threads = 8 warps; a block takes (unit, head) tasks in a
+// grid-stride loop.  Warp w folds slots w, w+8, ... with a fixed maximum, so
+// every weight is independent of the others and the loads overlap; the 8
+// warp sums are then added in warp order.
+__global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float wacc[kMergeThreads / 32][kHeadDim];
+  __shared__ float wz[kMergeThreads / 32];
+  const int n_units = a.sched[H_NUNITS];
+  const int64_t tasks = (int64_t)n_units * a.hq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kMergeThreads / 32;
+  for (int64_t task = blockIdx.x; task < tasks; task += gridDim.x) {
+    const int u = (int)(task / a.hq);
+    const int h = (int)(task % a.hq);
+    const int req = a.sched[a.off_units + 2 * u];
+    const int s0 = a.sched[a.off_merge + u];
+    const int s1 = a.sched[a.off_merge + u + 1];
+    // maximum LSE over the chunks (log2 units)
+    float m = -CUDART_INF_F;
+    for (int s = s0 + threadIdx.x; s < s1; s += kMergeThreads)
+      m = fmaxf(m, a.l_part[(int64_t)s * a.hq + h] * kLog2e);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w]);
+    // weighted sums, warp w over slots w, w + 8, ...
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float z = 0.f;
+#pragma unroll 4
+    for (int s = s0 + warp; s < s1; s += kWarps) {
+      const float wgt = exp2f(a.l_part[(int64_t)s * a.hq + h] * kLog2e - m);
+      const float4 o = *reinterpret_cast<const float4*>(
+          a.o_part + ((int64_t)s * a.hq + h) * kHeadDim + 4 * lane);
+      acc.x = fmaf(wgt, o.x, acc.x);
+      acc.y = fmaf(wgt, o.y, acc.y);
+      acc.z = fmaf(wgt, o.z, acc.z);
+      acc.w = fmaf(wgt, o.w, acc.w);
+      z += wgt;
+    }
+    *reinterpret_cast<float4*>(&wacc[warp][4 * lane]) = acc;
+    if (lane == 0) wz[warp] = z;
+    __syncthreads();
+    if (threadIdx.x < kHeadDim) {
+      float o = 0.f, zt = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        o += wacc[w][threadIdx.x];
+        zt += wz[w];
+      }
+      const int64_t qrow = (int64_t)req * a.hq + h;
+      a.out[qrow * kHeadDim + threadIdx.x] = (uint16_t)f32_to_bf16_rne(o / zt);
+      if (threadIdx.x == 0 && a.lse != nullptr) a.lse[qrow] = (m + log2f(zt)) * kLn2;
+    }
+    __syncthreads();
+  }
+}
+
+// merge_states: two states per row, row = (n, head), rows_per_block rows of
+// head_dim / 8 threads each (one 16-byte chunk of 8 bf16 per thread).
+__global__ void __launch_bounds__(256) merge_states_kernel(
+    const uint16_t* __restrict__ va, const float* sa, const uint16_t* __restrict__ vb,
+    const float* sb, uint16_t* vo, float* so, int64_t rows, int chunks, int rows_per_block) {
+  const int r_local = threadIdx.x / chunks;
+  const int c = threadIdx.x % chunks;
+  const int64_t r = (int64_t)blockIdx.x * rows_per_block + r_local;
+  const bool active = r_local < rows_per_block && r < rows;
+  float la = 0.f, lb = 0.f;
+  uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+  if (active) {
+    la = sa[r];
+    lb = sb[r];
+    xa = *reinterpret_cast<const uint4*>(va + (r * chunks + c) * 8);
+    xb = *reinterpret_cast<const uint4*>(vb + (r * chunks + c) * 8);
+  }
+  __syncthreads();  // every read of s_a / s_b / v happens before any write (aliasing)
+  if (!active) return;
+  const float m = fmaxf(la, lb);
+  uint4 res = make_uint4(0, 0, 0, 0);
+  float lse = -CUDART_INF_F;
+  if (m != -CUDART_INF_F) {
+    const float wa = exp2f((la - m) * kLog2e);
+    const float wb = exp2f((lb - m) * kLog2e);
+    const float z = wa + wb;
+    const float inv = 1.f / z;
+    const uint32_t a4[4] = {xa.x, xa.y, xa.z, xa.w};
+    const uint32_t b4[4] = {xb.x, xb.y, xb.z, xb.w};
+    uint32_t o4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a0 = __uint_as_float(a4[k] << 16), a1 = __uint_as_float(a4[k] & 0xffff0000u);
+      const float b0 = __uint_as_float(b4[k] << 16), b1 = __uint_as_float(b4[k] & 0xffff0000u);
+      const float o0 = (wa * a0 + wb * b0) * inv;
+      const float o1 = (wa * a1 + wb * b1) * inv;
+      o4[k] = f32_to_bf16_rne(o0) | (f32_to_bf16_rne(o1) << 16);
+    }
+    res = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    lse = m + log2f(z) * kLn2;
+  }
+  *reinterpret_cast<uint4*>(vo + (r * chunks + c) * 8) = res;
+  if (c == 0) so[r] = lse;
+}
+
+}  // namespace
+
+cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t stream) {
+  merge_partials_kernel<<<grid, kMergeThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,
+                                const float* s_b, void* v_out, float* s_out, int64_t rows,
+                                int head_dim, cudaStream_t stream) {
+  const int chunks = head_dim / 8;
+  const int rows_per_block = 256 / chunks;
+  const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+  merge_states_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const uint16_t*>(v_a), s_a, static_cast<const uint16_t*>(v_b), s_b,
+      static_cast<uint16_t*>(v_out), s_out, rows, chunks, rows_per_block);
+  return cudaGetLastError();
+}
+
+}  // namespace pkd

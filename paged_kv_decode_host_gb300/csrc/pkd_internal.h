@@ -1,0 +1,124 @@
+// Internal definitions shared by the host runtime and the CUDA kernels of
+// libpkd: workspace layout, schedule header words, kernel argument blocks.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#include "pkd.h"
+
+namespace pkd {
+
+constexpr int32_t kMagic = 0x31444B50;  // "PKD1"
+constexpr int kHeadDim = 128;           // the decode kernel's D
+constexpr int kMaxKvHeads = 8;          // one consumer warp per KV head
+constexpr int kWarpTokens = 16;         // tokens per stage (each warp sees all 16)
+constexpr int kStages = 3;              // shared-memory ring depth
+constexpr int kDefaultAlpha = 32;
+constexpr int kDefaultMinChunk = 256;
+constexpr int kMergeThreads = 256;
+
+// Schedule header words (first 16 int32 of the workspace).
+enum HeaderWord {
+  H_MAGIC = 0, H_BATCH, H_HQ, H_HKV, H_D, H_P, H_NCTA, H_NITEMS, H_NUNITS,
+  H_NSLOTS, H_CHUNK, H_ALPHA, H_NNZ, H_MAKESPAN, H_MINCHUNK, H_RESERVED,
+  H_WORDS = 16
+};
+
+constexpr int kItemWords = 8;  // req, tok_begin, tok_end, dst_slot, page_off, 0,0,0
+
+// Fixed word offsets of the schedule arrays, all derived from capacities.
+struct Layout {
+  int64_t cta_indptr;    // [n_cta + 1]
+  int64_t items;         // [max_items][kItemWords]
+  int64_t units;         // [max_items][2]
+  int64_t merge_indptr;  // [max_items + 1]
+  int64_t page_list;     // [max_num_pages]
+  int64_t words;         // schedule words (end of page_list)
+  int64_t max_items;
+  // byte offsets inside the device workspace
+  size_t err_byte;       // int32 device error word (never written by plan)
+  size_t o_part_byte;    // fp32 [max_items][Hq][D]
+  size_t l_part_byte;    // fp32 [max_items][Hq]
+  size_t total_bytes;
+};
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Upper bound on work items of one plan: a split request of length l gives
+// ceil(l / c) <= l / c + 1 chunks and every chunk candidate is at least
+// ceil(L_kv / 4) with L_kv = ceil(sum l / n_cta), so sum_i ceil(l_i / c)
+// <= 4 n_cta + batch.
+inline int64_t max_items_for(int64_t max_batch, int64_t n_cta) {
+  return max_batch + 4 * n_cta + 8;
+}
+
+inline Layout make_layout(const pkd_config& c, int64_t n_cta) {
+  Layout L{};
+  L.max_items = max_items_for(c.max_batch, n_cta);
+  L.cta_indptr = H_WORDS;
+  L.items = align_up(L.cta_indptr + n_cta + 1, 8);
+  L.units = L.items + L.max_items * kItemWords;
+  L.merge_indptr = L.units + L.max_items * 2;
+  L.page_list = align_up(L.merge_indptr + L.max_items + 1, 4);
+  L.words = L.page_list + c.max_num_pages;
+  size_t sched_bytes = (size_t)L.words * 4;
+  L.err_byte = (size_t)align_up((int64_t)sched_bytes, 256);
+  L.o_part_byte = L.err_byte + 256;
+  L.l_part_byte = L.o_part_byte +
+                  (size_t)L.max_items * c.num_qo_heads * c.head_dim * sizeof(float);
+  L.l_part_byte = (size_t)align_up((int64_t)L.l_part_byte, 256);
+  L.total_bytes = L.l_part_byte + (size_t)L.max_items * c.num_qo_heads * sizeof(float);
+  L.total_bytes = (size_t)align_up((int64_t)L.total_bytes, 256);
+  return L;
+}
+
+// Decode kernel arguments (by value; fixed per launch so launches can be
+// captured -- the schedule itself is read from the workspace at run time).
+struct DecodeArgs {
+  const int32_t* sched;      // workspace base (schedule words)
+  float* o_part;             // partial outputs, fp32 [slot][Hq][D]
+  float* l_part;             // partial LSE, fp32 [slot][Hq] (natural log)
+  int32_t* err;              // device error word
+  const uint16_t* q;         // bf16 [B][Hq][D]
+  const uint8_t* kv;         // bf16 NHD cache, bytes
+  uint16_t* out;             // bf16 [B][Hq][D]
+  float* lse;                // fp32 [B][Hq] or null
+  int64_t page_bytes;        // 2 * P * row_bytes
+  int64_t off_cta, off_items, off_pages;
+  int32_t hq, hkv, page_size, num_pages;
+  int32_t row_bytes;         // Hkv * D * 2: one token of one page, all heads
+  float scale_log2;          // log2(e) / sqrt(D)
+};
+
+struct MergeArgs {
+  const int32_t* sched;
+  const float* o_part;
+  const float* l_part;
+  uint16_t* out;
+  float* lse;
+  int64_t off_units, off_merge;
+  int32_t hq;
+};
+
+// Kernel launchers (decode_kernel.cu / merge_kernels.cu).
+int decode_smem_bytes(int hkv, int group);
+int decode_threads(int hkv);
+cudaError_t decode_prepare(int group, int smem_bytes);
+cudaError_t decode_occupancy(int group, int hkv, int smem_bytes, int* blocks_per_sm);
+cudaError_t launch_decode(int group, const DecodeArgs& a, int grid, int hkv,
+                          int smem_bytes, cudaStream_t stream);
+cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,
+                                const float* s_b, void* v_out, float* s_out,
+                                int64_t rows, int head_dim, cudaStream_t stream);
+
+// Host planner (planner.cpp).  Writes the schedule words into `words`.
+int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                  const int32_t* indptr, const int32_t* indices,
+                  const int32_t* last, int32_t batch, int32_t* words,
+                  pkd_plan_info* info);
+
+}  // namespace pkd

@@ -1,0 +1,226 @@
+// Host scheduler ("inspector") for paged-KV decode.
+//
+// Runs once per decode step on the CPU and writes a flat int32 schedule that
+// the persistent decode kernel and the merge kernel read from a fixed-address
+// workspace.  Rules (FlashInfer 完全拆解, 先切长 KV，再做最长任务优先分配 and
+// 固定指针比固定内容更重要; FlashInfer, in depth, "Load balancing with
+// split-KV"):
+//
+//  * table check + lengths: l_i = P (n_i - 1) + r_i, 1 <= r_i <= P, every
+//    request owns >= 1 page, page ids inside the pool;
+//  * work bound L_kv = ceil(sum_i l_i / N_CTA) -- one query token per
+//    request, and one work item covers all KV heads of its tokens (the GQA
+//    group is folded in, and an NHD page is one contiguous block for all
+//    heads);
+//  * chunk = L_kv rounded up to whole pages and at least the split floor
+//    (short requests are not split); candidates L_kv, L_kv/2, L_kv/4 are each
+//    scheduled and the smallest predicted makespan wins (ties: larger chunk);
+//  * item cost alpha + tokens; items sorted by descending cost (ties: request,
+//    then chunk), each given to the least-loaded CTA (ties: lowest CTA id);
+//  * reduction map: split requests get contiguous partial slots in chunk
+//    order; unsplit items write straight to the output (slot -1), so no
+//    atomics and a fixed merge order.
+#include <algorithm>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "pkd_internal.h"
+
+namespace pkd {
+namespace {
+
+struct Item {
+  int64_t cost;
+  int32_t req;
+  int32_t chunk_idx;
+  int32_t tok_begin;
+  int32_t tok_end;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void split_items(const std::vector<int64_t>& lens, int64_t chunk, int64_t alpha,
+                 std::vector<Item>* out) {
+  out->clear();
+  for (size_t i = 0; i < lens.size(); ++i) {
+    int32_t k = 0;
+    for (int64_t t = 0; t < lens[i]; t += chunk, ++k) {
+      int64_t e = std::min(t + chunk, lens[i]);
+      out->push_back(Item{alpha + (e - t), (int32_t)i, k, (int32_t)t, (int32_t)e});
+    }
+  }
+}
+
+// Longest processing time first.  Returns the makespan; fills owner[] with
+// the CTA of each item (in the sorted order given by `order`).
+int64_t lpt(const std::vector<Item>& items, int32_t n_cta, std::vector<int32_t>* order,
+            std::vector<int32_t>* owner) {
+  order->resize(items.size());
+  for (size_t i = 0; i < items.size(); ++i) (*order)[i] = (int32_t)i;
+  std::sort(order->begin(), order->end(), [&](int32_t a, int32_t b) {
+    const Item& x = items[a];
+    const Item& y = items[b];
+    if (x.cost != y.cost) return x.cost > y.cost;
+    if (x.req != y.req) return x.req < y.req;
+    return x.chunk_idx < y.chunk_idx;
+  });
+  using Slot = std::pair<int64_t, int32_t>;  // (load, cta): min-heap order
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int32_t c = 0; c < n_cta; ++c) heap.push(Slot(0, c));
+  owner->assign(items.size(), -1);
+  int64_t makespan = 0;
+  for (int32_t idx : *order) {
+    Slot s = heap.top();
+    heap.pop();
+    (*owner)[idx] = s.second;
+    s.first += items[idx].cost;
+    makespan = std::max(makespan, s.first);
+    heap.push(s);
+  }
+  return makespan;
+}
+
+}  // namespace
+
+int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                  const int32_t* indptr, const int32_t* indices, const int32_t* last,
+                  int32_t batch, int32_t* words, pkd_plan_info* info) {
+  if (batch < 0 || n_cta < 1 || words == nullptr) return PKD_E_INVALID_ARG;
+  if (batch > 0 && (indptr == nullptr || last == nullptr)) return PKD_E_INVALID_ARG;
+  if (batch > cfg.max_batch) return PKD_E_CAPACITY;
+  const int64_t P = cfg.page_size;
+
+  // ---- P0: table check and lengths
+  std::vector<int64_t> lens((size_t)batch);
+  int64_t total = 0;
+  int64_t nnz = 0;
+  if (batch > 0) {
+    if (indptr[0] != 0) return PKD_E_BAD_TABLE;
+    for (int32_t i = 0; i < batch; ++i) {
+      int64_t n = (int64_t)indptr[i + 1] - indptr[i];
+      if (n < 1) return PKD_E_BAD_TABLE;
+      if (last[i] < 1 || last[i] > P) return PKD_E_BAD_TABLE;
+      lens[i] = P * (n - 1) + last[i];
+      if (lens[i] > 0x7fffffffLL) return PKD_E_CAPACITY;
+      total += lens[i];
+    }
+    nnz = indptr[batch];
+    if (nnz > cfg.max_num_pages) return PKD_E_CAPACITY;
+    if (nnz > 0 && indices == nullptr) return PKD_E_INVALID_ARG;
+    for (int64_t k = 0; k < nnz; ++k)
+      if (indices[k] < 0 || indices[k] >= cfg.num_pages) return PKD_E_BAD_TABLE;
+  }
+
+  // ---- P1 + P2 + P3: chunk candidates, split, LPT; keep the best
+  const int64_t alpha = cfg.alpha < 0 ? kDefaultAlpha : cfg.alpha;
+  const int64_t min_chunk = cfg.min_chunk_tokens < 0 ? kDefaultMinChunk : cfg.min_chunk_tokens;
+  const int64_t floor_c = ceil_div(std::max<int64_t>(min_chunk, 1), P) * P;
+  const int64_t work_bound = ceil_div(total, n_cta);
+  std::vector<int64_t> cands;
+  for (int64_t k : {1, 2, 4}) {
+    int64_t c = std::max(ceil_div(ceil_div(work_bound, k), P) * P, floor_c);
+    if (std::find(cands.begin(), cands.end(), c) == cands.end()) cands.push_back(c);
+  }
+  std::vector<Item> items, best_items;
+  std::vector<int32_t> order, owner, best_order, best_owner;
+  int64_t best_chunk = -1, best_span = 0;
+  for (int64_t c : cands) {
+    split_items(lens, c, alpha, &items);
+    int64_t span = lpt(items, n_cta, &order, &owner);
+    if (best_chunk < 0 || span < best_span) {
+      best_chunk = c;
+      best_span = span;
+      best_items.swap(items);
+      best_order.swap(order);
+      best_owner.swap(owner);
+    }
+  }
+  const int64_t n_items = (int64_t)best_items.size();
+  if (n_items > L.max_items) return PKD_E_CAPACITY;
+
+  // ---- P4: reduction map (split requests, ascending id; slots in chunk order)
+  std::vector<int32_t> first_slot((size_t)batch, -1);
+  std::vector<std::pair<int32_t, int32_t>> units;
+  int32_t n_slots = 0;
+  for (int32_t i = 0; i < batch; ++i) {
+    int64_t nc = ceil_div(lens[i], best_chunk);
+    if (nc > 1) {
+      first_slot[i] = n_slots;
+      units.emplace_back(i, (int32_t)nc);
+      n_slots += (int32_t)nc;
+    }
+  }
+
+  // ---- serialize: queues in CTA order, each in assignment (LPT) order
+  std::vector<int32_t> count((size_t)n_cta, 0);
+  for (int64_t j = 0; j < n_items; ++j) count[best_owner[j]]++;
+  int32_t* cta_indptr = words + L.cta_indptr;
+  cta_indptr[0] = 0;
+  for (int32_t c = 0; c < n_cta; ++c) cta_indptr[c + 1] = cta_indptr[c] + count[c];
+  std::vector<int32_t> fill(cta_indptr, cta_indptr + n_cta);
+  std::vector<int32_t> pos((size_t)n_items);
+  for (int32_t idx : best_order) pos[idx] = fill[best_owner[idx]]++;
+  std::vector<int32_t> by_pos((size_t)n_items);
+  for (int64_t j = 0; j < n_items; ++j) by_pos[pos[j]] = (int32_t)j;
+
+  int32_t* item_words = words + L.items;
+  int32_t* page_list = words + L.page_list;
+  int64_t page_off = 0;
+  for (int64_t p = 0; p < n_items; ++p) {
+    const Item& it = best_items[by_pos[p]];
+    int32_t* w = item_words + p * kItemWords;
+    w[0] = it.req;
+    w[1] = it.tok_begin;
+    w[2] = it.tok_end;
+    w[3] = first_slot[it.req] >= 0 ? first_slot[it.req] + it.chunk_idx : -1;
+    w[4] = (int32_t)page_off;
+    w[5] = w[6] = w[7] = 0;
+    int64_t p0 = it.tok_begin / P, p1 = ceil_div(it.tok_end, P);
+    for (int64_t pg = p0; pg < p1; ++pg) page_list[page_off++] = indices[indptr[it.req] + pg];
+  }
+  int32_t* unit_words = words + L.units;
+  int32_t* merge_indptr = words + L.merge_indptr;
+  merge_indptr[0] = 0;
+  for (size_t u = 0; u < units.size(); ++u) {
+    unit_words[2 * u] = units[u].first;
+    unit_words[2 * u + 1] = units[u].second;
+    merge_indptr[u + 1] = merge_indptr[u] + units[u].second;
+  }
+
+  int32_t* h = words;
+  std::memset(h, 0, sizeof(int32_t) * H_WORDS);
+  h[H_MAGIC] = kMagic;
+  h[H_BATCH] = batch;
+  h[H_HQ] = cfg.num_qo_heads;
+  h[H_HKV] = cfg.num_kv_heads;
+  h[H_D] = cfg.head_dim;
+  h[H_P] = cfg.page_size;
+  h[H_NCTA] = n_cta;
+  h[H_NITEMS] = (int32_t)n_items;
+  h[H_NUNITS] = (int32_t)units.size();
+  h[H_NSLOTS] = n_slots;
+  h[H_CHUNK] = (int32_t)best_chunk;
+  h[H_ALPHA] = (int32_t)alpha;
+  h[H_NNZ] = (int32_t)nnz;
+  h[H_MAKESPAN] = (int32_t)std::min<int64_t>(best_span, 0x7fffffff);
+  h[H_MINCHUNK] = (int32_t)floor_c;
+
+  if (info) {
+    info->batch = batch;
+    info->num_ctas = n_cta;
+    info->chunk_tokens = (int32_t)best_chunk;
+    info->num_items = (int32_t)n_items;
+    info->num_units = (int32_t)units.size();
+    info->num_slots = n_slots;
+    info->total_tokens = total;
+    info->makespan = best_span;
+    info->nnz = (int32_t)nnz;
+    info->schedule_words = (int32_t)(L.page_list + nnz);
+  }
+  return PKD_OK;
+}
+
+}  // namespace pkd

@@ -1,0 +1,146 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every
+entry point its header declares, and its host scheduler matches the plan
+restatement integer for integer.  No GPU work is issued here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_decode_host_gb300 as pkd
+import workloads
+from oracle import plan as oplan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkd.build()
+    return pkd.load()
+
+
+def _declared():
+    names = set()
+    with open(os.path.join(ROOT, "include", "pkd.h")) as f:
+        text = f.read()
+    for m in re.finditer(r"\b(pkd_[a-z_]+)\s*\(", text):
+        names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    assert declared == set(pkd.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.pkd_version() >= 100
+    assert lib.pkd_status_str(-2).decode().startswith("bad page table")
+    assert lib.pkd_status_str(12345).decode() == "unknown status"
+
+
+def _cfg(P, hq=32, hkv=8, max_batch=64, max_pages=4096, num_pages=4096, n_cta=152,
+         alpha=-1, min_chunk=-1, d=128):
+    return pkd.make_config(hq, hkv, d, P, max_batch, max_pages, num_pages, alpha, min_chunk,
+                           n_cta)
+
+
+def test_config_validation(lib):
+    off = (ctypes.c_int64 * 6)()
+    bad = [
+        _cfg(16, d=64),                 # head dim other than 128
+        _cfg(16, hq=12, hkv=8),         # Hq % Hkv != 0
+        _cfg(16, hq=48, hkv=8),         # group of 6
+        _cfg(16, hq=32, hkv=16),        # more than 8 KV heads
+    ]
+    for c in bad:
+        assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -3
+    c = _cfg(16)
+    c.flags = 1
+    assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
+    assert lib.pkd_schedule_layout(ctypes.byref(_cfg(16)), off) == 0
+    assert list(off)[5] > list(off)[4] > list(off)[3] > list(off)[2] > list(off)[1] > list(off)[0]
+
+
+def _compare(cfg, indptr, indices, last, alpha, min_chunk):
+    words, info, off = pkd.plan_host(cfg, indptr, indices, last)
+    got = pkd.decode_schedule(words, off, info)
+    ref = oplan.plan(indptr, indices, last, page_size=cfg.page_size, num_pages=cfg.num_pages,
+                     n_cta=cfg.num_ctas, alpha=alpha, min_chunk_tokens=min_chunk)
+    assert info["chunk_tokens"] == ref.chunk
+    assert info["makespan"] == ref.makespan
+    assert info["num_items"] == ref.n_items
+    assert info["num_slots"] == ref.n_slots
+    assert got["cta_indptr"] == ref.cta_indptr
+    assert got["items"] == [tuple(x) for x in ref.items]
+    assert got["units"] == [tuple(x) for x in ref.units]
+    assert got["merge_indptr"] == ref.merge_indptr
+    assert got["page_list"] == ref.page_list
+    assert got["header"][0] == 0x31444B50
+    return info
+
+
+@pytest.mark.parametrize("name", ["worked_example", "llama8b_step", "skewed",
+                                  "shared_prefix", "token_sparse"])
+def test_plan_bit_exact_on_workloads(lib, name):
+    w = workloads.workload(name)
+    t = workloads.make_tables(w)
+    views = [(t["indptr"], t["indices"], t["last"])]
+    if "prefix" in t:
+        views += [t["prefix"], t["suffix"]]
+    for indptr, indices, last in views:
+        nnz = int(indptr[-1])
+        cfg = _cfg(w.page_size, w.hq, w.hkv, max_batch=w.batch, max_pages=nnz,
+                   num_pages=w.pool_pages, n_cta=152, alpha=32, min_chunk=256)
+        _compare(cfg, indptr, indices, last, 32, 256)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_bit_exact_random(lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    P = int(rng.choice([1, 2, 3, 8, 16, 32]))
+    B = int(rng.integers(0 if seed == 0 else 1, 70))
+    lens = rng.integers(1, 5000, B).tolist()
+    if seed % 3 == 1 and B:
+        lens[-1] = int(rng.integers(20000, 120000))
+    pool = sum(-(-l // P) for l in lens) + 7
+    ids = rng.permutation(pool).astype(np.int32)
+    indptr, indices, last = workloads.page_table(lens, P, ids)
+    n_cta = int(rng.choice([1, 7, 64, 152, 304]))
+    alpha = int(rng.integers(0, 200))
+    min_chunk = int(rng.choice([1, 16, 256, 1000]))
+    cfg = _cfg(P, max_batch=max(B, 1), max_pages=max(int(indptr[-1]), 1), num_pages=pool,
+               n_cta=n_cta, alpha=alpha, min_chunk=min_chunk)
+    info = _compare(cfg, indptr, indices, last, alpha, min_chunk)
+    assert info["batch"] == B
+
+
+def test_plan_host_rejects_bad_tables(lib):
+    cfg = _cfg(16, max_batch=4, max_pages=8, num_pages=8, n_cta=4)
+    cases = [
+        ([0, 2], [0, 1], [0]),           # last_page_len 0 (multiple-of-P bug)
+        ([0, 2], [0, 1], [17]),          # longer than the page
+        ([0, 0], [], [1]),               # empty request
+        ([0, 1], [8], [1]),              # page outside the pool
+        ([0, 1], [-3], [1]),             # negative page
+        ([1, 2], [0, 1], [1]),           # indptr[0] != 0
+    ]
+    for indptr, indices, last in cases:
+        with pytest.raises(pkd.PkdError) as e:
+            pkd.plan_host(cfg, np.array(indptr, np.int32), np.array(indices, np.int32),
+                          np.array(last, np.int32))
+        assert e.value.status == -2, (indptr, indices, last)
+    # capacity: batch above max_batch, pages above max_num_pages
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.plan_host(cfg, np.arange(6, dtype=np.int32), np.arange(5, dtype=np.int32),
+                      np.ones(5, np.int32))
+    assert e.value.status == -7
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.plan_host(cfg, np.array([0, 9], np.int32), np.zeros(9, np.int32),
+                      np.ones(1, np.int32))
+    assert e.value.status == -7
+    # int64 tables are refused by the binding before reaching the library
+    with pytest.raises(TypeError):
+        pkd.plan_host(cfg, np.array([0, 1]), np.array([0]), np.array([1]))

@@ -1,0 +1,118 @@
+"""GPU-side API contract: the failure modes the pages list (stale plan,
+run before plan, dtype / layout mismatch, bad tables, workspace too small)
+come back as status codes or Python exceptions before any launch; no GPU
+fault is ever provoked."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_decode_host_gb300 as pkd
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkd.build()
+    pkd.load()
+
+
+def _setup(lens=(37, 16, 5)):
+    w = workloads.Workload("api", 1, 32, 8, 128, 16, 1, tuple(lens), 64)
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    dec = pkd.BatchDecodeWithPagedKVCache(32, 8, 128, 16, max_batch=8, max_num_pages=32,
+                                          num_pages=64)
+    return w, t, q, kv, dec
+
+
+def test_run_before_plan_and_stale_epoch():
+    w, t, q, kv, dec = _setup()
+    lib = pkd.load()
+    out = torch.empty_like(q)
+    st = lib.pkd_run(dec._h, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(kv.data_ptr()),
+                     ctypes.c_void_p(out.data_ptr()), None, 0, None)
+    assert st == -5                                       # PKD_E_NO_PLAN
+    e1 = dec.plan(t["indptr"], t["indices"], t["last"])
+    e2 = dec.plan(t["indptr"], t["indices"], t["last"])
+    assert e2 == e1 + 1
+    with pytest.raises(pkd.PkdError) as e:
+        dec.run(q, kv, expect_epoch=e1)
+    assert e.value.status == -6                           # PKD_E_STALE_PLAN
+    dec.run(q, kv, expect_epoch=e2)
+    torch.cuda.synchronize()
+
+
+def test_dtype_shape_layout_mismatch():
+    w, t, q, kv, dec = _setup()
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    with pytest.raises(TypeError):
+        dec.run(q.half(), kv)                             # planned bf16, got fp16
+    with pytest.raises(TypeError):
+        dec.run(q, kv.half())
+    with pytest.raises(ValueError):
+        dec.run(q[:2].contiguous(), kv)                   # batch differs from the plan
+    with pytest.raises(ValueError):
+        dec.run(q, kv.transpose(2, 3).contiguous())       # HND-shaped cache
+    with pytest.raises(ValueError):
+        pkd.BatchDecodeWithPagedKVCache(32, 8, 128, 16, max_batch=8, max_num_pages=32,
+                                        num_pages=64, kv_layout="HND")
+
+
+def test_bad_tables_and_capacity():
+    w, t, q, kv, dec = _setup()
+    for indptr, indices, last in [
+        ([0, 2], [0, 1], [0]), ([0, 2], [0, 1], [17]), ([0, 0], [], [1]),
+        ([0, 1], [64], [1]), ([0, 1], [-1], [1]),
+    ]:
+        with pytest.raises(pkd.PkdError) as e:
+            dec.plan(np.array(indptr, np.int32), np.array(indices, np.int32),
+                     np.array(last, np.int32))
+        assert e.value.status == -2
+    with pytest.raises(pkd.PkdError) as e:                # batch above capacity
+        dec.plan(np.arange(10, dtype=np.int32), np.arange(9, dtype=np.int32),
+                 np.ones(9, np.int32))
+    assert e.value.status == -7
+    with pytest.raises(TypeError):                        # int64 indices
+        dec.plan(t["indptr"].astype(np.int64), t["indices"], t["last"])
+    with pytest.raises(ValueError):                       # device-side table
+        dec.plan(torch.tensor(t["indptr"], device="cuda"), t["indices"], t["last"])
+    # a failed plan leaves the previous plan in force
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    ep = dec.epoch
+    with pytest.raises(pkd.PkdError):
+        dec.plan(np.array([0, 2], np.int32), np.array([0, 1], np.int32), np.array([0], np.int32))
+    assert dec.plan_info()["batch"] == 3
+    dec.run(q, kv, expect_epoch=ep)
+    torch.cuda.synchronize()
+    assert dec.device_error() == 0
+
+
+def test_workspace_too_small_and_misaligned():
+    lib = pkd.load()
+    cfg = pkd.make_config(32, 8, 128, 16, 64, 4096, 4096)
+    need = lib.pkd_workspace_bytes(ctypes.byref(cfg))
+    assert need > 0
+    small = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    h = ctypes.c_void_p()
+    assert lib.pkd_create(ctypes.byref(cfg), ctypes.c_void_p(small.data_ptr()), small.numel(),
+                          ctypes.byref(h)) == -4
+    big = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    assert lib.pkd_create(ctypes.byref(cfg), ctypes.c_void_p(big.data_ptr() + 8), need,
+                          ctypes.byref(h)) == -1
+    assert lib.pkd_create(ctypes.byref(cfg), ctypes.c_void_p(big.data_ptr()), need,
+                          ctypes.byref(h)) == 0
+    lib.pkd_destroy(h)
+
+
+def test_unsupported_shapes_rejected():
+    for hq, hkv, d in [(32, 8, 64), (48, 8, 128), (32, 16, 128)]:
+        with pytest.raises(pkd.PkdError):
+            pkd.BatchDecodeWithPagedKVCache(hq, hkv, d, 16, max_batch=4, max_num_pages=8,
+                                            num_pages=8)

@@ -54,6 +54,7 @@ extern "C" {
 #define PKD_E_CAPACITY -7           /* batch or page count above capacity  */
 #define PKD_E_CUDA -8               /* a CUDA runtime call failed          */
 #define PKD_E_DEVICE -9             /* the device reported an error word   */
+#define PKD_E_SCRATCH_LIMIT -10     /* needs more than the static scratch   */
 
 /* Device error word bits (pkd_last_device_error). */
 #define PKD_DEV_ERR_TIMEOUT 1       /* a bounded wait gave up               */
@@ -197,6 +198,37 @@ int pkd_graph_launch(pkd_graph *graph, void *stream);
  * (ms[layers]) of the most recent launch.  Errors: INVALID_ARG, CUDA. */
 int pkd_graph_layer_times(pkd_graph *graph, float *ms);
 void pkd_graph_destroy(pkd_graph *graph);
+
+/* ---- allocation-free variant ------------------------------------------- */
+/* No counterpart on the pages: this entry point exists for callers that may
+ * not allocate device memory at all -- an engine whose allocator owns every
+ * byte of the GPU and forbids libraries from calling cudaMalloc, a process
+ * under a hard memory cap, or a plugin given no allocator.  Such callers
+ * cannot provide the workspace that pkd_create needs.
+ *
+ * pkd_run_static_scratch runs one layer (decode kernel + merge of split
+ * chunks, the same kernels as pkd_run) with the schedule and the partial
+ * states in a static 32 MiB device array inside this library (held by every
+ * GPU that loads the library until the process exits).  It calls no
+ * allocator: no cudaMalloc / cudaFree / cudaMallocHost, no pkd_create.
+ *   cfg            : the configuration; cfg->num_ctas must be > 0 and equal
+ *                    the value the schedule was planned for
+ *   schedule_words : host buffer written by pkd_plan_host(cfg, ...) for this
+ *                    step (num_words = its length, >= page_list offset + nnz);
+ *                    copied with cudaMemcpyAsync on `stream`
+ *   q, kv, out, lse: as for pkd_run
+ * The whole layout for cfg (make sure max_batch / max_num_pages are not
+ * larger than needed) must fit the 32 MiB array, else PKD_E_SCRATCH_LIMIT.
+ * All calls share the array and it keeps the last call's contents (the
+ * device error word is cleared at the start of each call); calls whose GPU
+ * work overlaps race, so serialise them on one stream.  The first call on a
+ * device sets the device up (looks up the array's address and the kernel
+ * attribute) with that device current; make it before any stream capture.
+ * Errors: INVALID_ARG (null / misaligned pointer, schedule not matching cfg),
+ * UNSUPPORTED_SHAPE, SCRATCH_LIMIT, CUDA. */
+int pkd_run_static_scratch(const pkd_config *cfg, const int32_t *schedule_words,
+                           size_t num_words, const void *q, const void *kv,
+                           void *out, float *lse, void *stream);
 
 /* Human-readable name of a status code. */
 const char *pkd_status_str(int status);

@@ -34,7 +34,7 @@ STATUS = {
     0: "PKD_OK", -1: "PKD_E_INVALID_ARG", -2: "PKD_E_BAD_TABLE",
     -3: "PKD_E_UNSUPPORTED_SHAPE", -4: "PKD_E_WORKSPACE_TOO_SMALL",
     -5: "PKD_E_NO_PLAN", -6: "PKD_E_STALE_PLAN", -7: "PKD_E_CAPACITY",
-    -8: "PKD_E_CUDA", -9: "PKD_E_DEVICE",
+    -8: "PKD_E_CUDA", -9: "PKD_E_DEVICE", -10: "PKD_E_SCRATCH_LIMIT",
 }
 DEV_ERR_TIMEOUT = 1
 DEV_ERR_BOUNDS = 2
@@ -46,7 +46,7 @@ EXPORTS = (
     "pkd_get_plan_info", "pkd_run", "pkd_merge_states", "pkd_last_device_error",
     "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
     "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
-    "pkd_graph_destroy", "pkd_status_str", "pkd_version",
+    "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
 )
 
 
@@ -115,6 +115,7 @@ def load():
         "pkd_graph_destroy": (None, [vp]),
         "pkd_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pkd_version": (ctypes.c_int, []),
+        "pkd_run_static_scratch": (ctypes.c_int, [cfgp, vp, sz, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

@@ -146,6 +146,7 @@ const char* pkd_status_str(int s) {
     case PKD_E_CAPACITY: return "batch or page count above the configured capacity";
     case PKD_E_CUDA: return "CUDA runtime error";
     case PKD_E_DEVICE: return "device error word set";
+    case PKD_E_SCRATCH_LIMIT: return "layout larger than the static scratch array (32 MiB)";
     default: return "unknown status";
   }
 }

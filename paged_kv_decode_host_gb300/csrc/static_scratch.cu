@@ -1,0 +1,146 @@
+// Allocation-free decode entry point: pkd_run_static_scratch.
+//
+// Who needs it: callers that may not call cudaMalloc (or any allocator) at
+// the point where they run attention -- e.g. an engine whose memory manager
+// owns every byte of device memory and forbids libraries from allocating, a
+// process under a hard memory budget, or a plugin loaded into a host
+// framework that gives it no allocator.  Such a caller cannot hand the
+// regular path its workspace buffer (nor the pinned staging pkd_create makes).
+//
+// What it does instead: the schedule and the split-KV partial states live in
+// one file-scope device array of fixed size, kStaticScratchBytes, which every
+// GPU that loads this library keeps until the process exits.  The caller
+// passes only inputs and outputs: a schedule already built on the host by
+// pkd_plan_host (caller-owned host memory), q, the KV cache, out and lse.
+// The entry point copies the schedule into the array, clears the device
+// error word, and launches the same decode and merge kernels as pkd_run.
+//
+// Sharing: every call, from any thread or stream, uses the same array, which
+// keeps the previous call's contents.  Calls whose work overlaps on the GPU
+// race on it; callers must serialise them (one stream, or events).
+//
+// Set-up: the first call on each device (made with that device current)
+// looks up the array's device address with cudaGetSymbolAddress and sets the
+// decode kernel's shared-memory attribute.  Make that first call before any
+// stream capture.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "pkd_internal.h"
+
+namespace pkd {
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;  // 32 MiB per device
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+struct DeviceSlot {
+  std::atomic<int> ready{0};
+  uint8_t* addr = nullptr;
+};
+DeviceSlot g_slots[kMaxDevices];
+std::mutex g_setup_mu;
+
+// Device address of the scratch array on the current device (set-up once).
+int scratch_address(int group, uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKD_E_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PKD_E_UNSUPPORTED_SHAPE;
+  DeviceSlot& s = g_slots[dev];
+  if (s.ready.load(std::memory_order_acquire) & (1 << group)) {
+    *out = s.addr;
+    return PKD_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (s.addr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+      return PKD_E_CUDA;
+    s.addr = static_cast<uint8_t*>(p);
+  }
+  if (decode_prepare(group, decode_smem_bytes(kMaxKvHeads, group)) != cudaSuccess)
+    return PKD_E_CUDA;
+  s.ready.fetch_or(1 << group, std::memory_order_release);
+  *out = s.addr;
+  return PKD_OK;
+}
+
+}  // namespace
+}  // namespace pkd
+
+using namespace pkd;
+
+extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* schedule_words,
+                                      size_t num_words, const void* q, const void* kv, void* out,
+                                      float* lse, void* stream) {
+  if (cfg == nullptr || schedule_words == nullptr) return PKD_E_INVALID_ARG;
+  if (cfg->flags != 0 || cfg->num_ctas < 1 || cfg->head_dim != kHeadDim ||
+      cfg->num_kv_heads < 1 || cfg->num_kv_heads > kMaxKvHeads || cfg->num_qo_heads < 1 ||
+      cfg->num_qo_heads % cfg->num_kv_heads != 0 || cfg->page_size < 1 || cfg->num_pages < 1 ||
+      cfg->max_batch < 0 || cfg->max_num_pages < 0)
+    return PKD_E_INVALID_ARG;
+  const int group = cfg->num_qo_heads / cfg->num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PKD_E_UNSUPPORTED_SHAPE;
+  const Layout L = make_layout(*cfg, cfg->num_ctas);
+  if (L.total_bytes > kStaticScratchBytes) return PKD_E_SCRATCH_LIMIT;
+  // the schedule must be pkd_plan_host's output for this very configuration
+  if ((int64_t)num_words < L.page_list) return PKD_E_INVALID_ARG;
+  const int32_t* h = schedule_words;
+  if (h[H_MAGIC] != kMagic || h[H_HQ] != cfg->num_qo_heads || h[H_HKV] != cfg->num_kv_heads ||
+      h[H_D] != cfg->head_dim || h[H_P] != cfg->page_size || h[H_NCTA] != cfg->num_ctas ||
+      h[H_NITEMS] < 0 || h[H_NITEMS] > L.max_items || h[H_NNZ] < 0 ||
+      h[H_NNZ] > cfg->max_num_pages || (int64_t)num_words < L.page_list + h[H_NNZ])
+    return PKD_E_INVALID_ARG;
+  if (h[H_BATCH] > 0) {
+    if (q == nullptr || kv == nullptr || out == nullptr) return PKD_E_INVALID_ARG;
+    if (((uintptr_t)q | (uintptr_t)kv | (uintptr_t)out) % 16 != 0 || (uintptr_t)lse % 4 != 0)
+      return PKD_E_INVALID_ARG;
+  }
+  uint8_t* ws = nullptr;
+  int st = scratch_address(group, &ws);
+  if (st != PKD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t sched_bytes = ((size_t)L.page_list + (size_t)h[H_NNZ]) * 4;
+  if (cudaMemcpyAsync(ws, schedule_words, sched_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (cudaMemsetAsync(ws + L.err_byte, 0, 4, s) != cudaSuccess) return PKD_E_CUDA;
+
+  DecodeArgs a{};
+  a.sched = reinterpret_cast<const int32_t*>(ws);
+  a.o_part = reinterpret_cast<float*>(ws + L.o_part_byte);
+  a.l_part = reinterpret_cast<float*>(ws + L.l_part_byte);
+  a.err = reinterpret_cast<int32_t*>(ws + L.err_byte);
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv = static_cast<const uint8_t*>(kv);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.row_bytes = cfg->num_kv_heads * kHeadDim * 2;
+  a.page_bytes = (int64_t)2 * cfg->page_size * a.row_bytes;
+  a.off_cta = L.cta_indptr;
+  a.off_items = L.items;
+  a.off_pages = L.page_list;
+  a.hq = cfg->num_qo_heads;
+  a.hkv = cfg->num_kv_heads;
+  a.page_size = cfg->page_size;
+  a.num_pages = cfg->num_pages;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
+  if (launch_decode(group, a, cfg->num_ctas, cfg->num_kv_heads,
+                    decode_smem_bytes(cfg->num_kv_heads, group), s) != cudaSuccess)
+    return PKD_E_CUDA;
+  MergeArgs m{};
+  m.sched = a.sched;
+  m.o_part = a.o_part;
+  m.l_part = a.l_part;
+  m.out = a.out;
+  m.lse = lse;
+  m.off_units = L.units;
+  m.off_merge = L.merge_indptr;
+  m.hq = cfg->num_qo_heads;
+  if (launch_merge_partials(m, cfg->num_ctas, s) != cudaSuccess) return PKD_E_CUDA;
+  return PKD_OK;
+}

@@ -184,6 +184,8 @@ def run_ours(args, rank, world):
     for name, (ip, ix, la) in views:
         d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
                                             max_num_pages=int(ip[-1]), num_pages=w.pool_pages,
+                                            use_tensor_cores={"auto": None, "fma": False,
+                                                              "mma": True}[args.consumer],
                                             device=dev)
         d.plan(ip, ix, la)
         decs.append(d)
@@ -303,6 +305,7 @@ def run_ours(args, rank, world):
             "hkv": w.hkv, "head_dim": w.head_dim, "page_size": P,
             "total_tokens_per_layer": int(sum(lens)), "pages_per_layer": nnz,
             "alg_bytes_per_step": int(step_bytes),
+            "consumer": args.consumer,
             "l2": "inputs larger than L2 (each layer's cache >= 0.49 GB, distinct per replay)",
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
                                           "makespan")},
@@ -392,14 +395,14 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
         kv_bits = _bits(kvs[0])
     lens = _lens(t, w.page_size)
     order = list(range(w.batch))
-    # calibrate on one request, then size the sample to the budget
+    # calibrate on one request; the sample is requests 0, 1, ... of layer 0,
+    # cycling through the layer as many times as the time budget allows
     t_one = _oracle_sample(w, t, q_bits, kv_bits, [order[0]])
     per_tok = t_one / max(lens[order[0]], 1)
     n_tok_target = budget_s / max(per_tok, 1e-9)
     sample, acc = [], 0
-    for i in order:
-        if acc >= n_tok_target:
-            break
+    while acc < n_tok_target and len(sample) < 64 * w.batch:
+        i = order[len(sample) % w.batch]
         sample.append(i)
         acc += lens[i]
     secs = _oracle_sample(w, t, q_bits, kv_bits, sample)
@@ -407,10 +410,12 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
     bytes_ = alg_bytes_per_layer(
         workloads.Workload("s", 0, w.hq, w.hkv, w.head_dim, w.page_size, 1, tuple(s_lens), 1),
         s_lens, sum(-(-l // w.page_size) for l in s_lens))
+    passes = len(sample) / w.batch
     return {"value": round(bytes_ / secs / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": round(secs, 3),
-            "sample": f"layer 0, requests 0..{len(sample) - 1} ({sum(s_lens)} tokens) x "
-                      f"{w.hq} query heads, fp64, all host cores"}
+            "sample": f"layer 0: {len(sample)} request rows ({passes:.2f} passes over the "
+                      f"{w.batch} requests, {sum(s_lens)} tokens) x {w.hq} query heads, fp64, "
+                      f"all host cores"}
 
 
 def run_reference(args, rank, world):
@@ -463,6 +468,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_step",
                     choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix"])
+    ap.add_argument("--consumer", choices=["auto", "fma", "mma"], default="auto",
+                    help="decode-kernel consumer: the default, or forced CUDA-core (fma) / "
+                         "tensor-core (mma) folding of the GQA group")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -73,8 +73,15 @@ typedef struct pkd_config {
                                   tokens); < 0 selects the default (32)     */
     int32_t min_chunk_tokens;  /* split floor in tokens; < 0 -> 256          */
     int32_t num_ctas;          /* persistent grid; 0 -> SMs x CTAs per SM    */
-    uint32_t flags;            /* reserved, must be 0                        */
+    uint32_t flags;            /* PKD_FLAG_* (0 = defaults)                 */
 } pkd_config;
+
+/* Consumer variant of the decode kernel.  By default the GQA group is folded
+ * onto tensor cores (mma.sync m16n8k16, bf16 in / fp32 accumulate); the
+ * CUDA-core variant (fp32 FMA) is kept for comparison.  These flags force
+ * one; setting both is an error. */
+#define PKD_FLAG_FMA_CONSUMER 1u
+#define PKD_FLAG_MMA_CONSUMER 2u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;
@@ -171,14 +178,17 @@ int pkd_plan_host(const pkd_config *cfg, const int32_t *indptr,
 /* Word offsets of the schedule arrays (see pkd_plan_host):
  *   off[0] cta_indptr[num_ctas + 1]
  *   off[1] items[num_items][8] = {req, tok_begin, tok_end, dst_slot,
- *                                 page_off, 0, 0, 0}
+ *                                 first_page, 0, 0, 0}
+ *          (items of CTA c are items[cta_indptr[c] .. cta_indptr[c+1]) in
+ *          LPT order; dst_slot -1 = write through to out/lse; first_page =
+ *          indptr[req] + tok_begin / P, an index into page_list)
  *   off[2] units[num_units][2] = {req, num_chunks}
  *   off[3] merge_indptr[num_units + 1]
- *   off[4] page_list[nnz]
+ *   off[4] page_list[nnz]    (the CSR indices, unchanged)
  *   off[5] total words
  * Header words 0..15 hold: magic, batch, Hq, Hkv, D, P, num_ctas,
- * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (low 31
- * bits), 0, 0.  Errors: INVALID_ARG. */
+ * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (clamped to
+ * int32), split floor, 0.  Errors: INVALID_ARG. */
 int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 
 /* ---- CUDA-graph capture of a whole decode step ------------------------- */

@@ -30,7 +30,10 @@ P3  LPT: items in descending cost (ties: request, then chunk, ascending), each
 P4  reduction map: split requests get contiguous partial slots in chunk
     order; unsplit items write through to the output (slot -1)
     ("FlashInfer 完全拆解", sections 先切长 KV (fixed reduction map, no
-    atomics) and Split-KV 解决的是并行度 (writethrough)).
+    atomics) and Split-KV 解决的是并行度 (writethrough)).  Each item names its
+    pages by the index of its first page in the CSR indices array, which is
+    passed on unchanged ("FlashInfer, in depth", "The block-sparse page
+    table": request i owns indices[indptr[i]:indptr[i+1]]).
 """
 from __future__ import annotations
 
@@ -84,10 +87,10 @@ class Plan:
     chunk: int
     makespan: int
     cta_indptr: list          # [n_cta + 1]
-    items: list               # per item, queue order: (req, tok_begin, tok_end, dst_slot, page_off)
+    items: list               # per item, queue order: (req, tok_begin, tok_end, dst_slot, first page index)
     units: list               # per split request: (req, n_chunks)
     merge_indptr: list        # [n_units + 1]
-    page_list: list           # page ids in queue order
+    page_list: list           # the CSR page ids, as given
     lens: list
 
     @property
@@ -158,16 +161,13 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
 
     cta_indptr = [0]
     items = []
-    page_list = []
     indptr = [int(x) for x in indptr]
     for q in queues:
         for cost, req, k, tb, te in q:
             dst = first_slot[req] + k if req in first_slot else -1
-            items.append((req, tb, te, dst, len(page_list)))
-            p0 = tb // P
-            p1 = _ceil_div(te, P)
-            base = indptr[req]
-            page_list.extend(int(indices[base + p]) for p in range(p0, p1))
+            # page reference: index (into the CSR indices) of the item's first page
+            items.append((req, tb, te, dst, indptr[req] + tb // P))
         cta_indptr.append(len(items))
+    page_list = [int(x) for x in indices[: indptr[-1] if indptr else 0]]
     return Plan(chunk, makespan, cta_indptr, items, units, merge_indptr,
                 page_list, lens)

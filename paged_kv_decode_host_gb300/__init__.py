@@ -151,10 +151,14 @@ def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data) if a.size else ctypes.c_void_p(0)
 
 
+FLAG_FMA_CONSUMER = 1   # fold the GQA group onto CUDA cores (fp32 FMA)
+FLAG_MMA_CONSUMER = 2   # fold it onto tensor cores (mma.sync, bf16 in / fp32 acc)
+
+
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
-                num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0) -> Config:
+                num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0, flags=0) -> Config:
     return Config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
-                  num_pages, alpha, min_chunk_tokens, num_ctas, 0)
+                  num_pages, alpha, min_chunk_tokens, num_ctas, flags)
 
 
 def schedule_layout(cfg: Config):
@@ -239,7 +243,7 @@ class BatchDecodeWithPagedKVCache:
 
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
-                 kv_layout="NHD", device=None):
+                 use_tensor_cores=None, kv_layout="NHD", device=None):
         import torch
         if kv_layout != "NHD":
             raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
@@ -247,8 +251,10 @@ class BatchDecodeWithPagedKVCache:
         self.device = torch.device("cuda" if device is None else device)
         self.hq, self.hkv, self.d, self.p = num_qo_heads, num_kv_heads, head_dim, page_size
         self.num_pages = num_pages
+        flags = 0 if use_tensor_cores is None else (
+            FLAG_MMA_CONSUMER if use_tensor_cores else FLAG_FMA_CONSUMER)
         self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch,
-                               max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas)
+                               max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas, flags)
         with torch.cuda.device(self.device):
             nbytes = lib.pkd_workspace_bytes(ctypes.byref(self.cfg))
             if nbytes == 0:

@@ -23,6 +23,7 @@ struct pkd_ctx {
   pkd_config cfg;
   int32_t n_cta = 0;
   int32_t group = 0;
+  bool mma = false;
   int smem_bytes = 0;
   int merge_grid = 0;
   int device = 0;
@@ -50,7 +51,9 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 int check_config(const pkd_config* c) {
   if (c == nullptr) return PKD_E_INVALID_ARG;
-  if (c->flags != 0) return PKD_E_INVALID_ARG;
+  if ((c->flags & ~(PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER)) != 0 ||
+      c->flags == (PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER))
+    return PKD_E_INVALID_ARG;
   if (c->max_batch < 0 || c->max_num_pages < 0 || c->num_pages < 1 || c->page_size < 1 ||
       c->num_ctas < 0)
     return PKD_E_INVALID_ARG;
@@ -76,8 +79,9 @@ int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
   if (cudaGetDevice(&dev) != cudaSuccess) return PKD_E_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKD_E_CUDA;
-  if (decode_prepare(g, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
-  if (decode_occupancy(g, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
+  const bool mma = use_mma_consumer(g, c->flags);
+  if (decode_prepare(g, mma, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
+  if (decode_occupancy(g, mma, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
     return PKD_E_CUDA;
   if (per_sm < 1) return PKD_E_UNSUPPORTED_SHAPE;
   *n_cta = sms * per_sm;
@@ -110,8 +114,8 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
   if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
-  if (launch_decode(ctx->group, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
-      cudaSuccess)
+  if (launch_decode(ctx->group, ctx->mma, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes,
+                    stream) != cudaSuccess)
     return PKD_E_CUDA;
   if (ev_after && cudaEventRecordWithFlags(ev_after, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
@@ -197,12 +201,13 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
   if (!ctx) return PKD_E_INVALID_ARG;
   ctx->cfg = *cfg;
   ctx->group = cfg->num_qo_heads / cfg->num_kv_heads;
+  ctx->mma = use_mma_consumer(ctx->group, cfg->flags);
   st = resolve_ctas(cfg, &ctx->n_cta, &ctx->smem_bytes);
   if (st != PKD_OK) {
     delete ctx;
     return st;
   }
-  if (decode_prepare(ctx->group, ctx->smem_bytes) != cudaSuccess) {
+  if (decode_prepare(ctx->group, ctx->mma, ctx->smem_bytes) != cudaSuccess) {
     delete ctx;
     return PKD_E_CUDA;
   }
@@ -212,7 +217,7 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
     return PKD_E_WORKSPACE_TOO_SMALL;
   }
   cudaGetDevice(&ctx->device);
-  ctx->merge_grid = ctx->n_cta;
+  ctx->merge_grid = merge_grid_for(ctx->n_cta);
   ctx->ws = static_cast<uint8_t*>(d_workspace);
   ctx->ws_bytes = workspace_bytes;
   for (int k = 0; k < 2; ++k) {

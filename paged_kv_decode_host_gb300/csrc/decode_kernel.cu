@@ -101,15 +101,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// L2 policy for the KV stream: every byte is read once per layer, so mark it
+// evict-first and leave L2 to the schedule, queries and partial states.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // 1-D TMA bulk copy global -> shared, completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar) {
+                                              uint64_t* bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+
+// Shared-memory stride of one token row (all KV heads): 16 bytes of padding
+// shift consecutive rows across banks, so 8-row fragment loads of one head
+// are conflict-free.
+__host__ __device__ __forceinline__ int row_stride(int row_bytes) { return row_bytes + 16; }
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// launch early, and wait for the previous kernel before touching its data.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void raise_error(int32_t* err, volatile int* abort_flag, int code) {
   atomicOr(err, code);
@@ -154,6 +174,9 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
                              volatile int* abort_flag, int lane) {
   const int P = a.page_size;
   const int row = a.row_bytes;
+  const int rs = row_stride(row);
+  const uint64_t policy = l2_evict_first_policy();
+  bool waited = false;  // programmatic-launch wait, before the first KV read
   uint32_t stage = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
@@ -163,20 +186,15 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
       const int n = min(kTS, te - t);
       const int slot = (int)(stage % kStages);
       const uint32_t round = stage / kStages;
-      // Page ids of this stage's runs (a run = consecutive slots of one page).
+      // Page id of this lane's token: one K row and one V row per token (all
+      // KV heads), landing at a padded stride.
       int page = -1;
-      int cnt = 0;
       const int j = lane;
       if (j < n) {
-        const int tok = t + j;
-        const int pslot = tok % P;
-        if (j == 0 || pslot == 0) {
-          cnt = min(n - j, P - pslot);
-          page = a.sched[a.off_pages + poff + (tok - tb) / P];
-          if ((unsigned)page >= (unsigned)a.num_pages) {
-            atomicOr(a.err, PKD_DEV_ERR_BOUNDS);
-            page = 0;
-          }
+        page = a.sched[a.off_pages + poff + (t + j - tb) / P];
+        if ((unsigned)page >= (unsigned)a.num_pages) {
+          atomicOr(a.err, PKD_DEV_ERR_BOUNDS);
+          page = 0;
         }
       }
       if (round > 0) {
@@ -192,15 +210,19 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
       if (page >= 0) {
         const int pslot = (t + j) % P;
         const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)pslot * row;
-        uint8_t* dk = stages + (size_t)slot * stage_bytes + (size_t)j * row;
-        uint8_t* dv = dk + (size_t)kTS * row;
-        bulk_copy_g2s(dk, src, (uint32_t)(cnt * row), &full[slot]);
-        bulk_copy_g2s(dv, src + (int64_t)P * row, (uint32_t)(cnt * row), &full[slot]);
+        uint8_t* dk = stages + (size_t)slot * stage_bytes + (size_t)j * rs;
+        uint8_t* dv = dk + (size_t)kTS * rs;
+        if (!waited) {
+          pdl_wait();
+          waited = true;
+        }
+        bulk_copy_g2s(dk, src, (uint32_t)row, &full[slot], policy);
+        bulk_copy_g2s(dv, src + (int64_t)P * row, (uint32_t)row, &full[slot], policy);
       }
-      // pages longer than 32 runs per stage cannot occur: kTS <= 32
       ++stage;
     }
   }
+  if (!waited) pdl_wait();
   // Drain: wait for the last issued phase of every slot, so no copy is in
   // flight into shared memory when the CTA exits.
   if (lane == 0) {
@@ -226,7 +248,7 @@ struct Shape {
 };
 
 template <int G>
-__device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
+__device__ void run_consumer_fma(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                              int stage_bytes, uint64_t* full, uint64_t* empty,
                              volatile int* abort_flag, float* pbuf, float* sbuf, int warp,
                              int lane) {
@@ -235,7 +257,7 @@ __device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_
   const int hk = warp;
   const int hw = lane >> 4;
   const int li = lane & 15;
-  const int row = a.row_bytes;
+  const int rs = row_stride(a.row_bytes);
 
   // Which (head, step) values this lane holds after the reduce-scatter.
   int vbase = 0;
@@ -253,6 +275,7 @@ __device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_
   const int my_head = vbase / J;
   const bool leader = ((li & S::TOKBITS) == 0) && hw == 0;
 
+  pdl_wait();   // q may come from the previous kernel in the stream
   uint32_t stage = 0;
   for (int it = it0; it < it1; ++it) {
     const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
@@ -287,7 +310,7 @@ __device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_
         return;
       }
       const uint8_t* ks = stages + (size_t)slot * stage_bytes + hk * (kHeadDim * 2) + li * 16;
-      const uint8_t* vs = ks + (size_t)kTS * row;
+      const uint8_t* vs = ks + (size_t)kTS * rs;
 
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
@@ -298,7 +321,7 @@ __device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_
         for (int j = 0; j < J; ++j) {
           const int tok = 2 * (b * J + j) + hw;
           float k8[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(ks + (size_t)tok * row), k8);
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(ks + (size_t)tok * rs), k8);
 #pragma unroll
           for (int i = 0; i < G; ++i) {
             float s = 0.f;
@@ -380,7 +403,7 @@ __device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_
             p[0] = pbuf[tok];
           }
           float v8[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vs + (size_t)src_row * row), v8);
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(vs + (size_t)src_row * rs), v8);
 #pragma unroll
           for (int i = 0; i < G; ++i)
 #pragma unroll
@@ -436,10 +459,215 @@ __device__ void run_consumer(const DecodeArgs& a, int it0, int it1, const uint8_
   }
 }
 
+
+// ------------------------------------------------- tensor-core consumer (MMA)
+// The GQA group as a thin matrix: S = Q K^T with the group's G query heads
+// as the 16-row M dimension (rows >= G are zero), 8 tokens per N tile and 16
+// dims per K step (mma.sync m16n8k16, bf16 in, fp32 accumulate); then
+// O += P V with P taken straight from the S accumulators (converted to bf16)
+// and V fragments loaded transposed with ldmatrix.  One K/V read from shared
+// memory serves the whole group.  Softmax statistics stay in fp32.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A B + D with A 16x16 whose rows 8..15 are zero (a1 = a3 = 0), B 16x8,
+// fp32 accumulate.  Only rows 0..7 (d0, d1) are kept: the group has <= 8
+// query heads, so the other half of the tile is always zero.
+__device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+  float z0, z1;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%12};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
+}
+
+// A fragments of the group's queries: row = query head grp, two bf16 per
+// register (dims 16 ks + 2 tig, +1 and the same + 8).
 template <int G>
+__device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int req, int hk, int grp,
+                                             int tig, bool row_ok, uint32_t (&qa0)[8],
+                                             uint32_t (&qa2)[8]) {
+  const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+      a.q + ((int64_t)req * a.hq + (int64_t)hk * G + (row_ok ? grp : 0)) * kHeadDim);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    qa0[ks] = row_ok ? __ldg(qp + ks * 8 + tig) : 0u;
+    qa2[ks] = row_ok ? __ldg(qp + ks * 8 + 4 + tig) : 0u;
+  }
+}
+
+template <int G>
+__device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
+                                 int stage_bytes, uint64_t* full, uint64_t* empty,
+                                 volatile int* abort_flag, int warp, int lane) {
+  const int hk = warp;
+  const int grp = lane >> 2;   // fragment row: query head within the group
+  const int tig = lane & 3;    // fragment column pair
+  const bool row_ok = grp < G;
+  const int rs = row_stride(a.row_bytes);
+  const uint32_t stage0 = smem_u32(stages);
+  // ldmatrix row addresses (relative to a stage): lane L serves matrix L / 8,
+  // row L % 8.  K (no transpose): token = L % 8 (+ 8 per N tile), dim block =
+  // L / 8 (+ 4 per pair of K steps).  V (transpose): token = (L / 8 & 1) * 8
+  // + L % 8, dim block = L / 16 (+ 2 per pair of N tiles).
+  const uint32_t k_lane = (uint32_t)((lane & 7) * rs + hk * (kHeadDim * 2) + (lane >> 3) * 16);
+  const uint32_t v_lane = (uint32_t)(kTS * rs + (((lane >> 3) & 1) * 8 + (lane & 7)) * rs +
+                                     hk * (kHeadDim * 2) + (lane >> 4) * 16);
+
+  // the item and its queries are fetched one item ahead
+  const int32_t* item = a.sched + a.off_items + (int64_t)it0 * kItemWords;
+  int req = item[0], tb = item[1], te = item[2], dst = item[3];
+  pdl_wait();   // q may come from the previous kernel in the stream
+  uint32_t qa0[8], qa2[8];
+  load_q_frags<G>(a, req, hk, grp, tig, row_ok, qa0, qa2);
+
+  uint32_t stage = 0;
+  for (int it = it0; it < it1; ++it) {
+    int n_req = 0, n_tb = 0, n_te = 0, n_dst = -1;
+    uint32_t nq0[8], nq2[8];
+    if (it + 1 < it1) {
+      const int32_t* nx = a.sched + a.off_items + (int64_t)(it + 1) * kItemWords;
+      n_req = nx[0];
+      n_tb = nx[1];
+      n_te = nx[2];
+      n_dst = nx[3];
+      load_q_frags<G>(a, n_req, hk, grp, tig, row_ok, nq0, nq2);
+    }
+    float o[16][2];
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = 0.f;
+    float m_run = -CUDART_INF_F;
+    float l_run = 0.f;
+
+    for (int t = tb; t < te; t += kTS) {
+      const int n = min(kTS, te - t);
+      const int slot = (int)(stage % kStages);
+      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      if (!__all_sync(kFull, got)) {
+        if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+        return;
+      }
+      const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
+      if (n < kTS) {
+        // rows past the item's end hold stale bytes: zero this head's V rows
+        // there so P (= 0) x V cannot produce NaN
+        uint8_t* vrow = const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes +
+                        (size_t)kTS * rs + hk * (kHeadDim * 2) + (lane & 15) * 16;
+        for (int r = n + (lane >> 4); r < kTS; r += 2)
+          *reinterpret_cast<uint4*>(vrow + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+      }
+      // ---- S = Q K^T for two 8-token tiles
+      float sc[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sbase + k_lane + (uint32_t)(nt * 8 * rs + kp * 64), b0, b1, b2, b3);
+          mma_bf16(sc[nt], qa0[2 * kp], qa2[2 * kp], b0, b1);
+          mma_bf16(sc[nt], qa0[2 * kp + 1], qa2[2 * kp + 1], b2, b3);
+        }
+      }
+      // ---- online softmax on this lane's row (query head grp), 4 tokens
+      float s4[4];
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tok = nt * 8 + 2 * tig + c;
+          const float v = (tok < n) ? sc[nt][c] * a.scale_log2 : -CUDART_INF_F;
+          s4[nt * 2 + c] = v;
+          mx = fmaxf(mx, v);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+      const float alpha = exp2f(m_run - m_use);
+      float p4[4];
+      float psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        p4[k] = exp2f(s4[k] - m_use);
+        psum += p4[k];
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      const uint32_t pa0 = pack_bf16x2(p4[0], p4[1]);   // tokens 2 tig, 2 tig + 1
+      const uint32_t pa2 = pack_bf16x2(p4[2], p4[3]);   // tokens 8 + 2 tig, 9 + 2 tig
+      // ---- O = alpha O + P V over 16 dim tiles
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sbase + v_lane + (uint32_t)(dp * 32), b0, b1, b2, b3);
+        o[2 * dp][0] *= alpha;
+        o[2 * dp][1] *= alpha;
+        o[2 * dp + 1][0] *= alpha;
+        o[2 * dp + 1][1] *= alpha;
+        mma_bf16(o[2 * dp], pa0, pa2, b0, b1);
+        mma_bf16(o[2 * dp + 1], pa0, pa2, b2, b3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++stage;
+    }
+
+    // ---- epilogue: row sums over the quad, normalise, write
+    float l = l_run;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (row_ok) {
+      const float inv = 1.f / l;
+      const float lse_nat = (m_run + log2f(l)) * 0.69314718055994530942f;
+      const int64_t qrow = (int64_t)req * a.hq + (int64_t)hk * G + grp;
+      if (dst < 0) {
+        uint32_t* op = reinterpret_cast<uint32_t*>(a.out + qrow * kHeadDim) + tig;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) op[dt * 4] = pack_bf16x2(o[dt][0] * inv, o[dt][1] * inv);
+        if (a.lse != nullptr && tig == 0) a.lse[qrow] = lse_nat;
+      } else {
+        const int64_t prow = (int64_t)dst * a.hq + (int64_t)hk * G + grp;
+        float2* op = reinterpret_cast<float2*>(a.o_part + prow * kHeadDim) + tig;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) op[dt * 4] = make_float2(o[dt][0] * inv, o[dt][1] * inv);
+        if (tig == 0) a.l_part[prow] = lse_nat;
+      }
+    }
+    if (it + 1 < it1) {
+      req = n_req;
+      tb = n_tb;
+      te = n_te;
+      dst = n_dst;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qa0[ks] = nq0[ks];
+        qa2[ks] = nq2[ks];
+      }
+    }
+  }
+}
+
+template <int G, bool kMma>
 __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int stage_bytes = 2 * kTS * a.row_bytes;
+  const int stage_bytes = 2 * kTS * row_stride(a.row_bytes);
   uint8_t* stages = smem;
   float* pbuf_all = reinterpret_cast<float*>(smem + (size_t)kStages * stage_bytes);
   float* sbuf_all = pbuf_all + kMaxKvHeads * kTS * G;
@@ -450,6 +678,7 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_cons = a.hkv;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -459,29 +688,37 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
     fence_mbar_init();
   }
   __syncthreads();
-
+  // The schedule is only ever written by host-to-device copies, which order
+  // fully before this kernel, so it is read before the programmatic-launch
+  // wait.  q, the KV cache, the outputs and the partial states may belong to
+  // the previous kernel in the stream: each role waits (griddepcontrol.wait)
+  // before touching them.
   const int it0 = a.sched[a.off_cta + blockIdx.x];
   const int it1 = a.sched[a.off_cta + blockIdx.x + 1];
   if (it0 >= it1) return;
   if (warp == n_cons) {
     run_producer(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
   } else if (warp < n_cons) {
-    run_consumer<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
-                    pbuf_all + warp * kTS * G, sbuf_all + warp * 32, warp, lane);
+    if constexpr (kMma) {
+      run_consumer_mma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp, lane);
+    } else {
+      run_consumer_fma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+                          pbuf_all + warp * kTS * G, sbuf_all + warp * 32, warp, lane);
+    }
   }
 }
 
-template <int G>
+template <int G, bool kMma>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_kernel<G>);
+  return reinterpret_cast<const void*>(&decode_kernel<G, kMma>);
 }
 
-const void* kernel_for(int group) {
+const void* kernel_for(int group, bool mma) {
   switch (group) {
-    case 1: return kernel_ptr<1>();
-    case 2: return kernel_ptr<2>();
-    case 4: return kernel_ptr<4>();
-    case 8: return kernel_ptr<8>();
+    case 1: return mma ? kernel_ptr<1, true>() : kernel_ptr<1, false>();
+    case 2: return mma ? kernel_ptr<2, true>() : kernel_ptr<2, false>();
+    case 4: return mma ? kernel_ptr<4, true>() : kernel_ptr<4, false>();
+    case 8: return mma ? kernel_ptr<8, true>() : kernel_ptr<8, false>();
     default: return nullptr;
   }
 }
@@ -490,14 +727,21 @@ const void* kernel_for(int group) {
 
 int decode_threads(int hkv) { return (hkv + 1) * 32; }
 
+bool use_mma_consumer(int group, uint32_t flags) {
+  if (flags & PKD_FLAG_FMA_CONSUMER) return false;
+  if (flags & PKD_FLAG_MMA_CONSUMER) return true;
+  (void)group;
+  return true;   // measured faster than the CUDA-core consumer at every group size
+}
+
 int decode_smem_bytes(int hkv, int group) {
-  const int row = hkv * kHeadDim * 2;
-  return kStages * 2 * kTS * row + kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 +
+  const int rs = row_stride(hkv * kHeadDim * 2);
+  return kStages * 2 * kTS * rs + kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 +
          2 * kStages * 8 + 16;
 }
 
-cudaError_t decode_prepare(int group, int smem_bytes) {
-  const void* k = kernel_for(group);
+cudaError_t decode_prepare(int group, bool mma, int smem_bytes) {
+  const void* k = kernel_for(group, mma);
   if (!k) return cudaErrorInvalidValue;
   // The attribute is per kernel, shared by every context: always allow the
   // largest layout (8 KV heads) so a smaller context never lowers it.
@@ -506,20 +750,29 @@ cudaError_t decode_prepare(int group, int smem_bytes) {
                               smem_bytes > most ? smem_bytes : most);
 }
 
-cudaError_t decode_occupancy(int group, int hkv, int smem_bytes, int* blocks_per_sm) {
-  const void* k = kernel_for(group);
+cudaError_t decode_occupancy(int group, bool mma, int hkv, int smem_bytes, int* blocks_per_sm) {
+  const void* k = kernel_for(group, mma);
   if (!k) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, decode_threads(hkv),
                                                        (size_t)smem_bytes);
 }
 
-cudaError_t launch_decode(int group, const DecodeArgs& a, int grid, int hkv, int smem_bytes,
-                          cudaStream_t stream) {
-  const void* k = kernel_for(group);
+cudaError_t launch_decode(int group, bool mma, const DecodeArgs& a, int grid, int hkv,
+                          int smem_bytes, cudaStream_t stream) {
+  const void* k = kernel_for(group, mma);
   if (!k) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(decode_threads(hkv));
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void* args[] = {const_cast<DecodeArgs*>(&a)};
-  return cudaLaunchKernel(k, dim3(grid), dim3(decode_threads(hkv)), args, (size_t)smem_bytes,
-                          stream);
+  return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace pkd

@@ -25,65 +25,72 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float x) {
   return u >> 16;
 }
 
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Contraction of split chunks (the reduction map built by the planner): for
 // each split request u and query head h, fold the partial states in slots
-// merge_indptr[u] .. merge_indptr[u+1] (chunk order) into out / lse.
-// Block = 256 threads = 8 warps; a block takes (unit, head) tasks in a
-// grid-stride loop.  Warp w folds slots w, w+8, ... with a fixed maximum, so
-// every weight is independent of the others and the loads overlap; the 8
-// warp sums are then added in warp order.
+// merge_indptr[u] .. merge_indptr[u+1] into out / lse.
+// Block = 256 threads = 8 warps; blocks take (unit, head) tasks in a
+// grid-stride loop over a grid of 8 blocks per decode CTA, so every task of a
+// typical plan is in flight at once.  Warp w folds slots w, w + 8, ... with
+// the running-max recurrence (lane = 4 dims); the 8 warp states are then
+// combined in warp order.  Fixed assignment and order: bit-reproducible.
 __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
-  __shared__ float red[kMergeThreads / 32];
-  __shared__ float wacc[kMergeThreads / 32][kHeadDim];
-  __shared__ float wz[kMergeThreads / 32];
+  constexpr int kWarps = kMergeThreads / 32;
+  __shared__ float wm[kWarps];
+  __shared__ float wz[kWarps];
+  __shared__ __align__(16) float wacc[kWarps][kHeadDim];
+  pdl_launch_dependents();
+  pdl_wait();
   const int n_units = a.sched[H_NUNITS];
   const int64_t tasks = (int64_t)n_units * a.hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = kMergeThreads / 32;
   for (int64_t task = blockIdx.x; task < tasks; task += gridDim.x) {
     const int u = (int)(task / a.hq);
     const int h = (int)(task % a.hq);
     const int req = a.sched[a.off_units + 2 * u];
     const int s0 = a.sched[a.off_merge + u];
     const int s1 = a.sched[a.off_merge + u + 1];
-    // maximum LSE over the chunks (log2 units)
-    float m = -CUDART_INF_F;
-    for (int s = s0 + threadIdx.x; s < s1; s += kMergeThreads)
-      m = fmaxf(m, a.l_part[(int64_t)s * a.hq + h] * kLog2e);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    m = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w]);
-    // weighted sums, warp w over slots w, w + 8, ...
+    float m = -CUDART_INF_F, z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float z = 0.f;
 #pragma unroll 4
     for (int s = s0 + warp; s < s1; s += kWarps) {
-      const float wgt = exp2f(a.l_part[(int64_t)s * a.hq + h] * kLog2e - m);
+      const float l2 = a.l_part[(int64_t)s * a.hq + h] * kLog2e;
       const float4 o = *reinterpret_cast<const float4*>(
           a.o_part + ((int64_t)s * a.hq + h) * kHeadDim + 4 * lane);
-      acc.x = fmaf(wgt, o.x, acc.x);
-      acc.y = fmaf(wgt, o.y, acc.y);
-      acc.z = fmaf(wgt, o.z, acc.z);
-      acc.w = fmaf(wgt, o.w, acc.w);
-      z += wgt;
+      const float m_new = fmaxf(m, l2);
+      const float sc = exp2f(m - m_new);
+      const float w = exp2f(l2 - m_new);
+      acc.x = fmaf(w, o.x, acc.x * sc);
+      acc.y = fmaf(w, o.y, acc.y * sc);
+      acc.z = fmaf(w, o.z, acc.z * sc);
+      acc.w = fmaf(w, o.w, acc.w * sc);
+      z = fmaf(z, sc, w);
+      m = m_new;
     }
     *reinterpret_cast<float4*>(&wacc[warp][4 * lane]) = acc;
-    if (lane == 0) wz[warp] = z;
+    if (lane == 0) {
+      wm[warp] = m;
+      wz[warp] = z;
+    }
     __syncthreads();
     if (threadIdx.x < kHeadDim) {
+      float mm = wm[0];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, wm[w]);
       float o = 0.f, zt = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        o += wacc[w][threadIdx.x];
-        zt += wz[w];
+        const float sc = exp2f(wm[w] - mm);   // 0 for a warp that saw no slot
+        o = fmaf(wacc[w][threadIdx.x], sc, o);
+        zt = fmaf(wz[w], sc, zt);
       }
       const int64_t qrow = (int64_t)req * a.hq + h;
       a.out[qrow * kHeadDim + threadIdx.x] = (uint16_t)f32_to_bf16_rne(o / zt);
-      if (threadIdx.x == 0 && a.lse != nullptr) a.lse[qrow] = (m + log2f(zt)) * kLn2;
+      if (threadIdx.x == 0 && a.lse != nullptr) a.lse[qrow] = (mm + log2f(zt)) * kLn2;
     }
     __syncthreads();
   }
@@ -137,8 +144,17 @@ __global__ void __launch_bounds__(256) merge_states_kernel(
 }  // namespace
 
 cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t stream) {
-  merge_partials_kernel<<<grid, kMergeThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_partials_kernel, a);
 }
 
 cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,

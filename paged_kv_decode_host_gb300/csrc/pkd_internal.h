@@ -106,10 +106,14 @@ struct MergeArgs {
 // Kernel launchers (decode_kernel.cu / merge_kernels.cu).
 int decode_smem_bytes(int hkv, int group);
 int decode_threads(int hkv);
-cudaError_t decode_prepare(int group, int smem_bytes);
-cudaError_t decode_occupancy(int group, int hkv, int smem_bytes, int* blocks_per_sm);
-cudaError_t launch_decode(int group, const DecodeArgs& a, int grid, int hkv,
+cudaError_t decode_prepare(int group, bool mma, int smem_bytes);
+cudaError_t decode_occupancy(int group, bool mma, int hkv, int smem_bytes, int* blocks_per_sm);
+cudaError_t launch_decode(int group, bool mma, const DecodeArgs& a, int grid, int hkv,
                           int smem_bytes, cudaStream_t stream);
+// Consumer variant for a group size: tensor cores (mma.sync) or CUDA cores.
+bool use_mma_consumer(int group, uint32_t flags);
+// Merge grid for a persistent decode grid of n_cta CTAs.
+inline int merge_grid_for(int n_cta) { return 8 * n_cta; }
 cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,
                                 const float* s_b, void* v_out, float* s_out,

@@ -19,7 +19,9 @@
 //    then chunk), each given to the least-loaded CTA (ties: lowest CTA id);
 //  * reduction map: split requests get contiguous partial slots in chunk
 //    order; unsplit items write straight to the output (slot -1), so no
-//    atomics and a fixed merge order.
+//    atomics and a fixed merge order;
+//  * page ids go to the device as the CSR indices array itself; each item
+//    records the index of its first page (chunks start on page boundaries).
 #include <algorithm>
 #include <cstring>
 #include <functional>
@@ -42,43 +44,77 @@ struct Item {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-void split_items(const std::vector<int64_t>& lens, int64_t chunk, int64_t alpha,
-                 std::vector<Item>* out) {
-  out->clear();
+// Copy n page ids and check 0 <= id < num_pages, in one pass the compiler
+// can vectorise (no early exit).
+bool copy_checked(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int64_t n,
+                  int32_t num_pages) {
+  int32_t lo = 0, hi = 0;
+  for (int64_t k = 0; k < n; ++k) {
+    const int32_t v = src[k];
+    dst[k] = v;
+    lo = v < lo ? v : lo;
+    hi = v > hi ? v : hi;
+  }
+  return lo >= 0 && hi < num_pages;
+}
+
+// LPT visiting order: descending cost, then request, then chunk.
+bool lpt_before(const Item& x, const Item& y) {
+  if (x.cost != y.cost) return x.cost > y.cost;
+  if (x.req != y.req) return x.req < y.req;
+  return x.chunk_idx < y.chunk_idx;
+}
+
+// Split every request into chunks and return the items already in LPT
+// visiting order.  Whole chunks all cost alpha + chunk and come out of the
+// split in (request, chunk) order, which is their sorted order; only the
+// shorter items (one per request at most) need sorting, then one merge.
+void split_sorted(const std::vector<int64_t>& lens, int64_t chunk, int64_t alpha,
+                  std::vector<Item>* whole, std::vector<Item>* rest, std::vector<Item>* out) {
+  whole->clear();
+  rest->clear();
   for (size_t i = 0; i < lens.size(); ++i) {
     int32_t k = 0;
     for (int64_t t = 0; t < lens[i]; t += chunk, ++k) {
-      int64_t e = std::min(t + chunk, lens[i]);
-      out->push_back(Item{alpha + (e - t), (int32_t)i, k, (int32_t)t, (int32_t)e});
+      const int64_t e = std::min(t + chunk, lens[i]);
+      const Item it{alpha + (e - t), (int32_t)i, k, (int32_t)t, (int32_t)e};
+      (e - t == chunk ? whole : rest)->push_back(it);
     }
   }
+  std::sort(rest->begin(), rest->end(), lpt_before);
+  out->resize(whole->size() + rest->size());
+  std::merge(whole->begin(), whole->end(), rest->begin(), rest->end(), out->begin(), lpt_before);
 }
 
-// Longest processing time first.  Returns the makespan; fills owner[] with
-// the CTA of each item (in the sorted order given by `order`).
-int64_t lpt(const std::vector<Item>& items, int32_t n_cta, std::vector<int32_t>* order,
-            std::vector<int32_t>* owner) {
-  order->resize(items.size());
-  for (size_t i = 0; i < items.size(); ++i) (*order)[i] = (int32_t)i;
-  std::sort(order->begin(), order->end(), [&](int32_t a, int32_t b) {
-    const Item& x = items[a];
-    const Item& y = items[b];
-    if (x.cost != y.cost) return x.cost > y.cost;
-    if (x.req != y.req) return x.req < y.req;
-    return x.chunk_idx < y.chunk_idx;
-  });
-  using Slot = std::pair<int64_t, int32_t>;  // (load, cta): min-heap order
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int32_t c = 0; c < n_cta; ++c) heap.push(Slot(0, c));
-  owner->assign(items.size(), -1);
+// Longest processing time first over items given in visiting order.
+// Returns the makespan and the CTA of each item.  The CTA loads sit in a
+// flat binary min-heap keyed by (load, CTA id); giving an item to the top
+// CTA only grows its key, so one sift-down per item keeps the heap (the same
+// choice as pop + push, at half the work).
+int64_t lpt(const std::vector<Item>& items, int32_t n_cta, std::vector<int32_t>* owner,
+            std::vector<std::pair<int64_t, int32_t>>* heap) {
+  // all loads 0: the heap in CTA id order is already a valid min-heap
+  heap->resize((size_t)n_cta);
+  std::pair<int64_t, int32_t>* h = heap->data();
+  for (int32_t c = 0; c < n_cta; ++c) h[c] = std::make_pair((int64_t)0, c);
+  owner->resize(items.size());
   int64_t makespan = 0;
-  for (int32_t idx : *order) {
-    Slot s = heap.top();
-    heap.pop();
-    (*owner)[idx] = s.second;
-    s.first += items[idx].cost;
-    makespan = std::max(makespan, s.first);
-    heap.push(s);
+  const size_t n = (size_t)n_cta;
+  for (size_t idx = 0; idx < items.size(); ++idx) {
+    (*owner)[idx] = h[0].second;
+    h[0].first += items[idx].cost;
+    makespan = std::max(makespan, h[0].first);
+    size_t i = 0;
+    const std::pair<int64_t, int32_t> v = h[0];
+    for (;;) {
+      size_t c = 2 * i + 1;
+      if (c >= n) break;
+      if (c + 1 < n && h[c + 1] < h[c]) ++c;
+      if (!(h[c] < v)) break;
+      h[i] = h[c];
+      i = c;
+    }
+    h[i] = v;
   }
   return makespan;
 }
@@ -110,8 +146,9 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     nnz = indptr[batch];
     if (nnz > cfg.max_num_pages) return PKD_E_CAPACITY;
     if (nnz > 0 && indices == nullptr) return PKD_E_INVALID_ARG;
-    for (int64_t k = 0; k < nnz; ++k)
-      if (indices[k] < 0 || indices[k] >= cfg.num_pages) return PKD_E_BAD_TABLE;
+    // page ids go into the schedule verbatim (the kernel reads request i's
+    // pages at indptr[i] + t / P), range-checked in the same pass
+    if (!copy_checked(indices, words + L.page_list, nnz, cfg.num_pages)) return PKD_E_BAD_TABLE;
   }
 
   // ---- P1 + P2 + P3: chunk candidates, split, LPT; keep the best
@@ -124,17 +161,17 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     int64_t c = std::max(ceil_div(ceil_div(work_bound, k), P) * P, floor_c);
     if (std::find(cands.begin(), cands.end(), c) == cands.end()) cands.push_back(c);
   }
-  std::vector<Item> items, best_items;
-  std::vector<int32_t> order, owner, best_order, best_owner;
+  std::vector<Item> items, best_items, whole, rest;
+  std::vector<int32_t> owner, best_owner;
+  std::vector<std::pair<int64_t, int32_t>> heap;
   int64_t best_chunk = -1, best_span = 0;
   for (int64_t c : cands) {
-    split_items(lens, c, alpha, &items);
-    int64_t span = lpt(items, n_cta, &order, &owner);
+    split_sorted(lens, c, alpha, &whole, &rest, &items);
+    int64_t span = lpt(items, n_cta, &owner, &heap);
     if (best_chunk < 0 || span < best_span) {
       best_chunk = c;
       best_span = span;
       best_items.swap(items);
-      best_order.swap(order);
       best_owner.swap(owner);
     }
   }
@@ -161,14 +198,10 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   cta_indptr[0] = 0;
   for (int32_t c = 0; c < n_cta; ++c) cta_indptr[c + 1] = cta_indptr[c] + count[c];
   std::vector<int32_t> fill(cta_indptr, cta_indptr + n_cta);
-  std::vector<int32_t> pos((size_t)n_items);
-  for (int32_t idx : best_order) pos[idx] = fill[best_owner[idx]]++;
   std::vector<int32_t> by_pos((size_t)n_items);
-  for (int64_t j = 0; j < n_items; ++j) by_pos[pos[j]] = (int32_t)j;
+  for (int64_t j = 0; j < n_items; ++j) by_pos[fill[best_owner[j]]++] = (int32_t)j;
 
   int32_t* item_words = words + L.items;
-  int32_t* page_list = words + L.page_list;
-  int64_t page_off = 0;
   for (int64_t p = 0; p < n_items; ++p) {
     const Item& it = best_items[by_pos[p]];
     int32_t* w = item_words + p * kItemWords;
@@ -176,10 +209,8 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     w[1] = it.tok_begin;
     w[2] = it.tok_end;
     w[3] = first_slot[it.req] >= 0 ? first_slot[it.req] + it.chunk_idx : -1;
-    w[4] = (int32_t)page_off;
+    w[4] = (int32_t)(indptr[it.req] + it.tok_begin / P);  // index of the item's first page
     w[5] = w[6] = w[7] = 0;
-    int64_t p0 = it.tok_begin / P, p1 = ceil_div(it.tok_end, P);
-    for (int64_t pg = p0; pg < p1; ++pg) page_list[page_off++] = indices[indptr[it.req] + pg];
   }
   int32_t* unit_words = words + L.units;
   int32_t* merge_indptr = words + L.merge_indptr;

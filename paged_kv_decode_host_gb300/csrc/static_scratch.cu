@@ -47,12 +47,13 @@ DeviceSlot g_slots[kMaxDevices];
 std::mutex g_setup_mu;
 
 // Device address of the scratch array on the current device (set-up once).
-int scratch_address(int group, uint8_t** out) {
+int scratch_address(int group, bool mma, uint8_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKD_E_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PKD_E_UNSUPPORTED_SHAPE;
   DeviceSlot& s = g_slots[dev];
-  if (s.ready.load(std::memory_order_acquire) & (1 << group)) {
+  const int bit = 1 << (2 * group + (mma ? 1 : 0));
+  if (s.ready.load(std::memory_order_acquire) & bit) {
     *out = s.addr;
     return PKD_OK;
   }
@@ -63,9 +64,9 @@ int scratch_address(int group, uint8_t** out) {
       return PKD_E_CUDA;
     s.addr = static_cast<uint8_t*>(p);
   }
-  if (decode_prepare(group, decode_smem_bytes(kMaxKvHeads, group)) != cudaSuccess)
+  if (decode_prepare(group, mma, decode_smem_bytes(kMaxKvHeads, group)) != cudaSuccess)
     return PKD_E_CUDA;
-  s.ready.fetch_or(1 << group, std::memory_order_release);
+  s.ready.fetch_or(bit, std::memory_order_release);
   *out = s.addr;
   return PKD_OK;
 }
@@ -79,7 +80,8 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
                                       size_t num_words, const void* q, const void* kv, void* out,
                                       float* lse, void* stream) {
   if (cfg == nullptr || schedule_words == nullptr) return PKD_E_INVALID_ARG;
-  if (cfg->flags != 0 || cfg->num_ctas < 1 || cfg->head_dim != kHeadDim ||
+  if ((cfg->flags & ~(PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER)) != 0 ||
+      cfg->flags == (PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER) || cfg->num_ctas < 1 || cfg->head_dim != kHeadDim ||
       cfg->num_kv_heads < 1 || cfg->num_kv_heads > kMaxKvHeads || cfg->num_qo_heads < 1 ||
       cfg->num_qo_heads % cfg->num_kv_heads != 0 || cfg->page_size < 1 || cfg->num_pages < 1 ||
       cfg->max_batch < 0 || cfg->max_num_pages < 0)
@@ -101,8 +103,9 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
     if (((uintptr_t)q | (uintptr_t)kv | (uintptr_t)out) % 16 != 0 || (uintptr_t)lse % 4 != 0)
       return PKD_E_INVALID_ARG;
   }
+  const bool mma = use_mma_consumer(group, cfg->flags);
   uint8_t* ws = nullptr;
-  int st = scratch_address(group, &ws);
+  int st = scratch_address(group, mma, &ws);
   if (st != PKD_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t sched_bytes = ((size_t)L.page_list + (size_t)h[H_NNZ]) * 4;
@@ -129,7 +132,7 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
   a.page_size = cfg->page_size;
   a.num_pages = cfg->num_pages;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
-  if (launch_decode(group, a, cfg->num_ctas, cfg->num_kv_heads,
+  if (launch_decode(group, mma, a, cfg->num_ctas, cfg->num_kv_heads,
                     decode_smem_bytes(cfg->num_kv_heads, group), s) != cudaSuccess)
     return PKD_E_CUDA;
   MergeArgs m{};
@@ -141,6 +144,7 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
   m.off_units = L.units;
   m.off_merge = L.merge_indptr;
   m.hq = cfg->num_qo_heads;
-  if (launch_merge_partials(m, cfg->num_ctas, s) != cudaSuccess) return PKD_E_CUDA;
+  if (launch_merge_partials(m, merge_grid_for(cfg->num_ctas), s) != cudaSuccess)
+    return PKD_E_CUDA;
   return PKD_OK;
 }

@@ -57,9 +57,14 @@ def test_config_validation(lib):
     ]
     for c in bad:
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -3
-    c = _cfg(16)
-    c.flags = 1
-    assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
+    for bad_flags in (3, 4, 0x80000000):
+        c = _cfg(16)
+        c.flags = bad_flags
+        assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
+    for ok_flags in (0, 1, 2):
+        c = _cfg(16)
+        c.flags = ok_flags
+        assert lib.pkd_schedule_layout(ctypes.byref(c), off) == 0
     assert lib.pkd_schedule_layout(ctypes.byref(_cfg(16)), off) == 0
     assert list(off)[5] > list(off)[4] > list(off)[3] > list(off)[2] > list(off)[1] > list(off)[0]
 

@@ -30,12 +30,14 @@ def _lib():
     pkd.load()
 
 
-def _decoder(w, indptr, *, num_ctas=0, alpha=-1, min_chunk=-1, max_batch=None, max_pages=None):
+def _decoder(w, indptr, *, num_ctas=0, alpha=-1, min_chunk=-1, max_batch=None, max_pages=None,
+             tc=None):
     return pkd.BatchDecodeWithPagedKVCache(
         w.hq, w.hkv, w.head_dim, w.page_size,
         max_batch=max_batch or max(w.batch, 1),
         max_num_pages=max_pages or max(int(indptr[-1]), 1),
-        num_pages=w.pool_pages, num_ctas=num_ctas, alpha=alpha, min_chunk_tokens=min_chunk)
+        num_pages=w.pool_pages, num_ctas=num_ctas, alpha=alpha, min_chunk_tokens=min_chunk,
+        use_tensor_cores=tc)
 
 
 def _check(out, lse, ref_o, ref_l, rows=None):
@@ -78,12 +80,15 @@ SMALL = [
 
 @pytest.mark.parametrize("case", SMALL, ids=[f"case{c[0]}" for c in SMALL])
 @pytest.mark.parametrize("split", ["writethrough", "split"])
-def test_small_parity_every_element(case, split):
+@pytest.mark.parametrize("tc", [False, True], ids=["fma", "mma"])
+def test_small_parity_every_element(case, split, tc):
+    """Every element, both consumer variants (CUDA-core FMA and tensor-core
+    MMA folding of the GQA group), with and without split-KV."""
     seed, lens, P, hq, hkv = case
     w, t, q, kv = _small_case(seed, lens, P, hq, hkv)
     kw = dict(num_ctas=1, min_chunk=1 << 30) if split == "writethrough" else \
         dict(num_ctas=5, alpha=0, min_chunk=1)
-    dec = _decoder(w, t["indptr"], **kw)
+    dec = _decoder(w, t["indptr"], tc=tc, **kw)
     dec.plan(t["indptr"], t["indices"], t["last"])
     info = dec.plan_info()
     if split == "split" and max(lens) > 64:
@@ -95,9 +100,10 @@ def test_small_parity_every_element(case, split):
     assert dec.device_error() == 0
 
 
-def test_peaky_scores_parity():
+@pytest.mark.parametrize("tc", [False, True], ids=["fma", "mma"])
+def test_peaky_scores_parity(tc):
     w, t, q, kv = _small_case(11, [640, 77, 1500], 16, 32, 8, scale_q=8.0)
-    dec = _decoder(w, t["indptr"], num_ctas=6, alpha=0, min_chunk=1)
+    dec = _decoder(w, t["indptr"], num_ctas=6, alpha=0, min_chunk=1, tc=tc)
     dec.plan(t["indptr"], t["indices"], t["last"])
     out, lse = dec.run(q, kv)
     ref_o, ref_l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=32, hkv=8)
@@ -165,13 +171,14 @@ def _sample_rows(rng, B, hq, per_req):
     return np.array(rows, dtype=np.int32)
 
 
-def test_skewed_full_parity():
+@pytest.mark.parametrize("tc", [None, False], ids=["default", "fma"])
+def test_skewed_full_parity(tc):
     """63 short requests + one 100,000-token request, default grid."""
     w = workloads.workload("skewed")
     t = workloads.make_tables(w)
     q = workloads.make_q(w, device="cuda")[0]
     kv = workloads.make_kv(w, device="cuda")[0]
-    dec = _decoder(w, t["indptr"])
+    dec = _decoder(w, t["indptr"], tc=tc)
     dec.plan(t["indptr"], t["indices"], t["last"])
     assert dec.plan_info()["num_units"] >= 1
     out, lse = dec.run(q, kv)
@@ -228,12 +235,13 @@ def test_shared_prefix_merge_states_parity():
     _check(out, lse, ref_o, ref_l)
 
 
-def test_token_sparse_sampled_parity():
+@pytest.mark.parametrize("tc", [None, False], ids=["default", "fma"])
+def test_token_sparse_sampled_parity(tc):
     w = workloads.workload("token_sparse")
     t = workloads.make_tables(w)
     q = workloads.make_q(w, device="cuda")[0]
     kv = workloads.make_kv(w, device="cuda")[0]
-    dec = _decoder(w, t["indptr"])
+    dec = _decoder(w, t["indptr"], tc=tc)
     dec.plan(t["indptr"], t["indices"], t["last"])
     out, lse = dec.run(q, kv)
     torch.cuda.synchronize()

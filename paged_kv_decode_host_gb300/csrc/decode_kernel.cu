@@ -13,22 +13,21 @@
 // GB300 design:
 //  * Grid = the plan's fixed CTA count (persistent; only the queue contents
 //    change between plans, so launches can be captured in a CUDA graph).
-//  * One producer warp streams the item's pages into a 3-deep ring of
+//  * One producer warp streams the item's tokens into a 3-deep ring of
 //    shared-memory stages with TMA bulk copies (cp.async.bulk, completion on
-//    an mbarrier).  A stage holds 16 tokens x all KV heads of K and of V.
-//    In the NHD layout the K rows of one page are one contiguous block for
-//    all heads (and so are the V rows), so a full 16-token page is two 32 KiB
-//    copies; page size 1 gives 2 KiB copies per token.  Only valid slots are
-//    copied.
+//    an mbarrier, L2 evict-first).  A stage holds 16 tokens; in the NHD
+//    layout one token row of all KV heads is contiguous, so each token costs
+//    one K-row and one V-row copy (2 KiB each at 8 KV heads), landing at a
+//    padded row stride so that 8-row fragment loads of one head are
+//    conflict-free.  Only valid rows are copied.
 //  * One consumer warp per KV head folds its GQA group of G query heads onto
-//    each K/V row it reads from shared memory (one read serves G heads).
-//    Lanes split D: half-warp hw takes tokens of parity hw, lane li owns
-//    dims [8 li, 8 li + 8).  Dot-product partials of 8 (or 4) token steps
-//    are reduce-scattered across the half-warp with shuffles, so each lane
-//    ends with whole scores for one head; the online-softmax update uses
-//    shuffles within the head's lane group; probabilities go through a small
-//    per-warp shared buffer to the P.V accumulation, which is lane-owned per
-//    dim.  All arithmetic is fp32 (bf16 inputs widened exactly).
+//    each K/V row it reads from shared memory (one read serves G heads).  The
+//    default consumer runs the group as a thin matrix on tensor cores
+//    (mma.sync m16n8k16, bf16 in, fp32 accumulate); the CUDA-core consumer
+//    (fp32 FMA, lanes split D, reduce-scatter of the dot products across a
+//    half-warp) is kept as an option.  Softmax statistics are fp32.
+//  * Programmatic dependent launch: CTAs trigger the next kernel at start and
+//    wait for the previous one only before touching q / KV / outputs.
 //  * Every wait is bounded (~2 s of %globaltimer); on timeout the kernel sets
 //    the device error word, stops issuing copies, waits (bounded) for the
 //    copies already in flight, and returns.

@@ -180,44 +180,68 @@ def run_ours(args, rank, world):
     outs = [torch.empty_like(x) for x in qs]
     lses = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in qs]
     views = _views(w, t)
-    decs = []
-    for name, (ip, ix, la) in views:
-        d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
-                                            max_num_pages=int(ip[-1]), num_pages=w.pool_pages,
-                                            use_tensor_cores={"auto": None, "fma": False,
-                                                              "mma": True}[args.consumer],
-                                            device=dev)
-        d.plan(ip, ix, la)
-        decs.append(d)
-    # graphs: one per cache copy; each captures the layers of a step
-    graphs = []
+    # Two planning contexts used on alternate steps: the schedule of step k+1
+    # is uploaded on a copy stream while step k's kernels run (each context's
+    # workspace is rewritten only after the step that last read it is done).
+    n_sets = 2
+    sets = []
+    for _ in range(n_sets):
+        decs = []
+        for name, (ip, ix, la) in views:
+            d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
+                                                max_num_pages=int(ip[-1]),
+                                                num_pages=w.pool_pages,
+                                                use_tensor_cores={"auto": None, "fma": False,
+                                                                  "mma": True}[args.consumer],
+                                                device=dev)
+            d.plan(ip, ix, la)
+            decs.append(d)
+        sets.append(decs)
+    decs = sets[0]
+    # graphs: per context, one per cache copy; each captures the layers of a step
+    graphs = [[] for _ in range(n_sets)]
     if w.prefix_tokens:
         # prefix run + suffix run + merge_states, per cache copy
         po = [torch.empty_like(qs[0]) for _ in range(copies)]
         pl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
         so = [torch.empty_like(qs[0]) for _ in range(copies)]
         sl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
-        for c in range(copies):
-            gp = decs[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=True)
-            gs = decs[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=True)
-            graphs.append((gp, gs, c))
+        for si, ds in enumerate(sets):
+            for c in range(copies):
+                gp = ds[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=True)
+                gs = ds[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=True)
+                graphs[si].append((gp, gs, c))
     else:
-        for c in range(copies):
-            kv_c = kvs[c * layers:(c + 1) * layers]
-            graphs.append((decs[0].capture(qs, kv_c, outs, lses, timing=True), None, c))
+        for si, ds in enumerate(sets):
+            for c in range(copies):
+                kv_c = kvs[c * layers:(c + 1) * layers]
+                graphs[si].append((ds[0].capture(qs, kv_c, outs, lses, timing=True), None, c))
 
     stream = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(n_sets)]
+    done = [torch.cuda.Event() for _ in range(n_sets)]
+    for e in done:
+        e.record(stream)
     host = {}
+
+    def graph_of(k):
+        return graphs[k % n_sets][(k // n_sets) % copies]
 
     def step(k):
         """One decode step.  With host buffers (e2e): q comes from pinned host
         memory and out / lse go back to it, inside the step."""
+        si = k % n_sets
+        copy_stream.wait_event(done[si])
+        with torch.cuda.stream(copy_stream):
+            for (name, (ip, ix, la)), d in zip(views, sets[si]):
+                d.plan(ip, ix, la)
+            copied[si].record(copy_stream)
         if host:
             for x, h in zip(qs, host["q"]):
                 x.copy_(h, non_blocking=True)
-        gp, gs, c = graphs[k % len(graphs)]
-        for (name, (ip, ix, la)), d in zip(views, decs):
-            d.plan(ip, ix, la)
+        stream.wait_event(copied[si])
+        gp, gs, c = graph_of(k)
         gp.launch()
         if gs is not None:
             gs.launch()
@@ -227,6 +251,7 @@ def run_ours(args, rank, world):
                 h.copy_(x, non_blocking=True)
             for x, h in zip(lses, host["lse"]):
                 h.copy_(x, non_blocking=True)
+        done[si].record(stream)
 
     for k in range(args.warmup):
         step(k)
@@ -247,7 +272,7 @@ def run_ours(args, rank, world):
         e1.record(stream)
         torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)
-    last = graphs[(args.warmup + args.steps - 1) % len(graphs)]
+    last = graph_of(args.warmup + args.steps - 1)
     k1_ms = last[0].layer_times() + (last[1].layer_times() if last[1] is not None else [])
     if world > 1:
         import torch.distributed as dist
@@ -282,8 +307,8 @@ def run_ours(args, rank, world):
     e2e = run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, dev)
 
     clocks = sampler.summary()
-    launches_per_step = sum(g.layers for gg in graphs[:1] for g in gg[:2] if g is not None) * 2 + \
-        (1 if w.prefix_tokens else 0)
+    gp0, gs0, _ = graphs[0][0]
+    launches_per_step = 2 * gp0.layers + (2 * gs0.layers + 1 if gs0 is not None else 0)
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),

@@ -489,6 +489,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2
       "{%8,%9}, {%10,%11,%12,%12};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
+  (void)z0;
+  (void)z1;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
@@ -694,7 +696,12 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
   // before touching them.
   const int it0 = a.sched[a.off_cta + blockIdx.x];
   const int it1 = a.sched[a.off_cta + blockIdx.x + 1];
-  if (it0 >= it1) return;
+  if (it0 >= it1) {
+    // no work, but still complete only after the previous kernel does, so
+    // that "this grid finished" keeps implying "every earlier grid finished"
+    pdl_wait();
+    return;
+  }
   if (warp == n_cons) {
     run_producer(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
   } else if (warp < n_cons) {

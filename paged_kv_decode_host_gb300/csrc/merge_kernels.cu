@@ -44,16 +44,22 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   __shared__ float wz[kWarps];
   __shared__ __align__(16) float wacc[kWarps][kHeadDim];
   pdl_launch_dependents();
-  pdl_wait();
+  // The schedule is only written by host-to-device copies (ordered before
+  // this kernel): read it before waiting for the decode kernel.
   const int n_units = a.sched[H_NUNITS];
   const int64_t tasks = (int64_t)n_units * a.hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool waited = false;
   for (int64_t task = blockIdx.x; task < tasks; task += gridDim.x) {
     const int u = (int)(task / a.hq);
     const int h = (int)(task % a.hq);
     const int req = a.sched[a.off_units + 2 * u];
     const int s0 = a.sched[a.off_merge + u];
     const int s1 = a.sched[a.off_merge + u + 1];
+    if (!waited) {
+      pdl_wait();   // partial states and outputs belong to the decode kernel
+      waited = true;
+    }
     float m = -CUDART_INF_F, z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
@@ -94,6 +100,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
     }
     __syncthreads();
   }
+  if (!waited) pdl_wait();
 }
 
 // merge_states: two states per row, row = (n, head), rows_per_block rows of

@@ -198,8 +198,13 @@ def run_ours(args, rank, world):
             decs.append(d)
         sets.append(decs)
     decs = sets[0]
-    # graphs: per context, one per cache copy; each captures the layers of a step
+    # graphs: per context, one per cache copy; each captures the layers of a
+    # step.  `graphs` are the plain graphs of the timed steps; `tgraphs` carry
+    # CUDA event nodes around every decode launch for the per-kernel roofline
+    # (event nodes break the kernel-to-kernel programmatic launch overlap, so
+    # they are kept out of the step timing).
     graphs = [[] for _ in range(n_sets)]
+    tgraphs = [[] for _ in range(n_sets)]
     if w.prefix_tokens:
         # prefix run + suffix run + merge_states, per cache copy
         po = [torch.empty_like(qs[0]) for _ in range(copies)]
@@ -208,14 +213,16 @@ def run_ours(args, rank, world):
         sl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
         for si, ds in enumerate(sets):
             for c in range(copies):
-                gp = ds[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=True)
-                gs = ds[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=True)
-                graphs[si].append((gp, gs, c))
+                for timing, dst in ((False, graphs), (True, tgraphs)):
+                    gp = ds[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=timing)
+                    gs = ds[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=timing)
+                    dst[si].append((gp, gs, c))
     else:
         for si, ds in enumerate(sets):
             for c in range(copies):
                 kv_c = kvs[c * layers:(c + 1) * layers]
-                graphs[si].append((ds[0].capture(qs, kv_c, outs, lses, timing=True), None, c))
+                for timing, dst in ((False, graphs), (True, tgraphs)):
+                    dst[si].append((ds[0].capture(qs, kv_c, outs, lses, timing=timing), None, c))
 
     stream = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream(device=dev)
@@ -225,8 +232,10 @@ def run_ours(args, rank, world):
         e.record(stream)
     host = {}
 
+    use = {"graphs": graphs}
+
     def graph_of(k):
-        return graphs[k % n_sets][(k // n_sets) % copies]
+        return use["graphs"][k % n_sets][(k // n_sets) % copies]
 
     def step(k):
         """One decode step.  With host buffers (e2e): q comes from pinned host
@@ -272,8 +281,16 @@ def run_ours(args, rank, world):
         e1.record(stream)
         torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)
-    last = graph_of(args.warmup + args.steps - 1)
+    # second timed loop, same steps with the event-node graphs: decode-kernel
+    # duration of every launch of the last step
+    use["graphs"] = tgraphs
+    k_roof = max(3, min(args.steps, 10))
+    for k in range(k_roof):
+        step(args.warmup + args.steps + k)
+    torch.cuda.synchronize()
+    last = graph_of(args.warmup + args.steps + k_roof - 1)
     k1_ms = last[0].layer_times() + (last[1].layer_times() if last[1] is not None else [])
+    use["graphs"] = graphs
     if world > 1:
         import torch.distributed as dist
         tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
@@ -341,12 +358,13 @@ def run_ours(args, rank, world):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback",
             "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": traffic_from_profile(),
+            "traffic": traffic_from_profile() if args.workload == "llama8b_step" else None,
             "kernel": "decode_kernel", "launch_ms_mean": round(k1_mean_ms, 5),
             "launch_gbs_min": round(min(k1_gbs), 1) if k1_gbs else None,
             "launch_gbs_max": round(max(k1_gbs), 1) if k1_gbs else None,
-            "timing": "CUDA event nodes around each decode launch inside the replayed graph "
-                      "(last timed step)",
+            "timing": "CUDA event nodes around each decode launch inside a replayed copy of "
+                      "the step graph, in a second timed loop of the same steps (last step); "
+                      "the step time comes from the plain graph",
         },
         "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
@@ -443,9 +461,119 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
                       f"all host cores"}
 
 
+def run_append(args, rank, world):
+    """append_paged_kv_cache for the Llama-shaped step: each of the 64
+    requests appends its new token (K and V rows, all 8 KV heads) into its
+    page slot, in each of the 32 layer caches; one step = one CUDA-graph
+    replay of the 32 append launches.  Bytes: the new rows read + written
+    and the table words read."""
+    import torch
+
+    import paged_kv_decode_host_gb300 as pkd
+
+    pkd.build()
+    pkd.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = workloads.workload("llama8b_step")
+    t = workloads.make_tables(w)
+    lens = _lens(t, w.page_size)
+    B, L = w.batch, w.layers
+    kvs = workloads.make_kv(w, device=dev, layers=L)
+    g = torch.Generator(device=dev).manual_seed(77)
+    k_new = [torch.randn(B, w.hkv, w.head_dim, generator=g, device=dev).to(torch.bfloat16)
+             for _ in range(L)]
+    v_new = [torch.randn(B, w.hkv, w.head_dim, generator=g, device=dev).to(torch.bfloat16)
+             for _ in range(L)]
+    as_dev = lambda a: torch.tensor(np.asarray(a, dtype=np.int32), device=dev)
+    bidx, pos = as_dev(range(B)), as_dev([l - 1 for l in lens])
+    ip, ix, la = as_dev(t["indptr"]), as_dev(t["indices"]), as_dev(t["last"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        for l in range(L):
+            pkd.append_kv(k_new[l], v_new[l], bidx, pos, ip, ix, la, kvs[l], err=err)
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    sampler = ClockSampler(f"GPU-{gpu_uuid}" if gpu_uuid else dev.index)
+    with sampler:
+        time.sleep(0.3)
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert int(err.item()) == 0
+    row = w.hkv * w.head_dim * 2
+    step_bytes = L * (B * 2 * row * 2 + 4 * (2 * B + 2 * B + 1 + B))
+    peak, peak_kind = measured_peak()
+    gbs = world * step_bytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": "append_paged_kv_cache throughput (new K/V rows into page slots)",
+        "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "us_per_launch": round(1e3 * ms / L, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "append", "layers": L, "batch": B, "hkv": w.hkv,
+                   "head_dim": w.head_dim, "page_size": w.page_size,
+                   "bytes_per_step": int(step_bytes)},
+        "roofline": {"bound": "latency (0.5 MB per launch)", "achieved": round(gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "traffic": None},
+        "gpu_launches": L * args.steps, "clocks": sampler.summary(),
+    }
+
+
+def run_reference_append(args, world):
+    """Reference arm for the append workload: the numpy append oracle on one
+    layer of the Llama-shaped step (64 new tokens)."""
+    import torch
+    from oracle import _bits
+    from oracle import append as oappend
+    w = workloads.workload("llama8b_step")
+    t = workloads.make_tables(w)
+    lens = _lens(t, w.page_size)
+    kv = _bits(workloads.make_kv(w, device="cpu", layers=1)[0])
+    g = torch.Generator().manual_seed(77)
+    k_new = _bits(torch.randn(w.batch, w.hkv, w.head_dim, generator=g).to(torch.bfloat16))
+    row = w.hkv * w.head_dim * 2
+    layer_bytes = w.batch * 2 * row * 2 + 4 * (5 * w.batch + 1)
+    secs = []
+    for k in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oappend.append_kv(kv, k_new, k_new, range(w.batch), [l - 1 for l in lens], t["indptr"],
+                          t["indices"], t["last"], w.page_size)
+        if k >= args.warmup:
+            secs.append(time.perf_counter() - t0)
+    v = layer_bytes / float(np.mean(secs)) / 1e9
+    return {"impl": "reference", "metric": "append_paged_kv_cache throughput (new K/V rows into "
+            "page slots)", "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * float(np.mean(secs)), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 bits", "data": "synthetic",
+            "config": {"workload": "append", "sample_per_step": "one layer (64 tokens)"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one layer (64 tokens), numpy, one core"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
 def run_reference(args, rank, world):
     """Reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
     import torch
+    if args.workload == "append":
+        return run_reference_append(args, world)
     w = workloads.workload(args.workload)
     t = workloads.make_tables(w)
     from oracle import _bits
@@ -492,7 +620,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_step",
-                    choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix"])
+                    choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix",
+                             "append"])
     ap.add_argument("--consumer", choices=["auto", "fma", "mma"], default="auto",
                     help="decode-kernel consumer: the default, or forced CUDA-core (fma) / "
                          "tensor-core (mma) folding of the GQA group")
@@ -513,7 +642,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    line = run_ours(args, rank, world)
+    line = run_append(args, rank, world) if args.workload == "append" else \
+        run_ours(args, rank, world)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

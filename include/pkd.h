@@ -157,6 +157,28 @@ int pkd_merge_states(const void *v_a, const float *s_a, const void *v_b,
                      const float *s_b, void *v_out, float *s_out, int32_t n,
                      int32_t heads, int32_t head_dim, void *stream);
 
+/* append_paged_kv_cache: write n new tokens' K and V rows into their page
+ * slots (pyshine FlashInfer tour, "The Paged KV Cache Layer"; the slot rule is
+ * the page table's, FlashInfer, in depth, "The block-sparse page table").
+ * Token i belongs to request b = batch_indices[i] at 0-based position
+ * pos = positions[i] of the request's length after the append; its K row goes
+ * to kv[indices[indptr[b] + pos / P]][0][pos % P] and its V row to [...][1][...].
+ *   k_new, v_new         : device bf16 [n][Hkv][D], 16-byte aligned
+ *   batch_indices, positions : device int32 [n]
+ *   indptr [batch + 1], indices [indptr[batch]], last_page_len [batch] :
+ *                          device int32, the table after the append
+ *   kv                   : device bf16 [num_pages][2][P][Hkv][D] (NHD)
+ *   err                  : device int32 word or NULL
+ * A token whose request, position (outside 0..len-1) or page id (outside the
+ * pool) is out of range is skipped and PKD_DEV_ERR_BOUNDS is OR-ed into *err;
+ * nothing is written outside the cache.  Stream-ordered, no host sync.
+ * Errors: INVALID_ARG, CUDA. */
+int pkd_append_kv(const void *k_new, const void *v_new, const int32_t *batch_indices,
+                  const int32_t *positions, int32_t n, const int32_t *indptr,
+                  const int32_t *indices, const int32_t *last_page_len, int32_t batch,
+                  void *kv, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                  int32_t head_dim, int32_t *err, void *stream);
+
 /* Read and clear the device error word (synchronizes `stream`).
  * *dev_err receives PKD_DEV_ERR_* bits (0 = none). */
 int pkd_last_device_error(pkd_ctx *ctx, void *stream, int32_t *dev_err);

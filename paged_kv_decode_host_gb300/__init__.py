@@ -23,7 +23,7 @@ import os
 import numpy as np
 
 __all__ = [
-    "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states",
+    "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states", "append_kv",
     "plan_host", "schedule_layout", "Graph", "STATUS",
 ]
 
@@ -47,6 +47,7 @@ EXPORTS = (
     "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
     "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
+    "pkd_append_kv",
 )
 
 
@@ -116,6 +117,8 @@ def load():
         "pkd_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pkd_version": (ctypes.c_int, []),
         "pkd_run_static_scratch": (ctypes.c_int, [cfgp, vp, sz, vp, vp, vp, vp, vp]),
+        "pkd_append_kv": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
+                                         i32, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -400,3 +403,44 @@ def merge_states(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):
                                  ctypes.c_void_p(s_out.data_ptr()), n, H, D, _stream_ptr(stream))
     _check(st, "pkd_merge_states")
     return v_out, s_out
+
+
+def append_kv(k_new, v_new, batch_indices, positions, indptr, indices, last_page_len, kv_cache,
+              err=None, stream=None):
+    """append_paged_kv_cache: write new tokens' K / V rows into their page slots.
+
+    k_new, v_new: bf16 [n, Hkv, D]; batch_indices, positions: int32 [n]
+    (position = 0-based index of the token in its request after the append);
+    indptr / indices / last_page_len: int32 CUDA tensors, the table after the
+    append; kv_cache: bf16 NHD [pages, 2, P, Hkv, D], written in place.
+    err: optional int32 CUDA tensor of one element; tokens outside the table
+    are skipped and flagged there."""
+    import torch
+    for name, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
+                        ("kv_cache", kv_cache, torch.bfloat16),
+                        ("batch_indices", batch_indices, torch.int32),
+                        ("positions", positions, torch.int32), ("indptr", indptr, torch.int32),
+                        ("indices", indices, torch.int32),
+                        ("last_page_len", last_page_len, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA {dt} tensor")
+    n = int(k_new.shape[0])
+    pages, two, P, hkv, D = kv_cache.shape
+    if two != 2 or tuple(k_new.shape) != (n, hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [n, Hkv, D] matching the NHD cache")
+    if batch_indices.numel() != n or positions.numel() != n:
+        raise ValueError("batch_indices and positions need one entry per new token")
+    batch = int(last_page_len.numel())
+    if indptr.numel() != batch + 1:
+        raise ValueError("indptr must have batch + 1 entries")
+    if err is not None and (err.dtype != torch.int32 or not err.is_cuda):
+        raise TypeError("err must be an int32 CUDA tensor")
+    st = load().pkd_append_kv(
+        ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+        ctypes.c_void_p(batch_indices.data_ptr()), ctypes.c_void_p(positions.data_ptr()), n,
+        ctypes.c_void_p(indptr.data_ptr()), ctypes.c_void_p(indices.data_ptr()),
+        ctypes.c_void_p(last_page_len.data_ptr()), batch, ctypes.c_void_p(kv_cache.data_ptr()),
+        int(pages), int(P), int(hkv), int(D),
+        ctypes.c_void_p(err.data_ptr() if err is not None else 0), _stream_ptr(stream))
+    _check(st, "pkd_append_kv")
+    return kv_cache

@@ -318,6 +318,29 @@ int pkd_merge_states(const void* v_a, const float* s_a, const void* v_b, const f
   return PKD_OK;
 }
 
+int pkd_append_kv(const void* k_new, const void* v_new, const int32_t* batch_indices,
+                  const int32_t* positions, int32_t n, const int32_t* indptr,
+                  const int32_t* indices, const int32_t* last_page_len, int32_t batch, void* kv,
+                  int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t* err, void* stream) {
+  if (n < 0 || batch < 0 || num_pages < 1 || page_size < 1 || num_kv_heads < 1 ||
+      head_dim < 8 || head_dim % 8 != 0)
+    return PKD_E_INVALID_ARG;
+  if (n == 0) return PKD_OK;
+  if (!k_new || !v_new || !batch_indices || !positions || !indptr || !indices ||
+      !last_page_len || !kv)
+    return PKD_E_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv, 16) || !aligned(err, 4))
+    return PKD_E_INVALID_ARG;
+  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
+  if (row_bytes > (1 << 24)) return PKD_E_INVALID_ARG;
+  if (launch_append(k_new, v_new, batch_indices, positions, n, indptr, indices, last_page_len,
+                    batch, kv, num_pages, page_size, (int32_t)row_bytes, err,
+                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKD_E_CUDA;
+  return PKD_OK;
+}
+
 int pkd_last_device_error(pkd_ctx* ctx, void* stream, int32_t* dev_err) {
   if (ctx == nullptr || dev_err == nullptr) return PKD_E_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -119,6 +119,12 @@ cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v
                                 const float* s_b, void* v_out, float* s_out,
                                 int64_t rows, int head_dim, cudaStream_t stream);
 
+cudaError_t launch_append(const void* k_new, const void* v_new, const int32_t* batch_indices,
+                          const int32_t* positions, int32_t n, const int32_t* indptr,
+                          const int32_t* indices, const int32_t* last_page_len, int32_t batch,
+                          void* kv, int32_t num_pages, int32_t page_size, int32_t row_bytes,
+                          int32_t* err, cudaStream_t stream);
+
 // Host planner (planner.cpp).  Writes the schedule words into `words`.
 int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
                   const int32_t* indptr, const int32_t* indices,

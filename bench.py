@@ -151,9 +151,23 @@ class ClockSampler:
 # ---------------------------------------------------------------- our arm
 
 def _views(w, t):
+    """(name, group_indptr or None, (indptr, indices, last)) per planned level.
+    The shared prefix is one group: every request over the 512 prefix pages,
+    planned as a shared-prefix level (FlashInfer 完全拆解, Composable Format)."""
     if w.prefix_tokens:
-        return [("prefix", t["prefix"]), ("suffix", t["suffix"])]
-    return [("full", (t["indptr"], t["indices"], t["last"]))]
+        n_pre = w.prefix_tokens // w.page_size
+        prefix = (np.array([0, n_pre], np.int32), np.asarray(t["prefix"][1][:n_pre], np.int32),
+                  np.array([w.page_size], np.int32))
+        return [("prefix", np.array([0, w.batch], np.int32), prefix),
+                ("suffix", None, t["suffix"])]
+    return [("full", None, (t["indptr"], t["indices"], t["last"]))]
+
+
+def _plan(d, group_indptr, table):
+    if group_indptr is None:
+        d.plan(*table)
+    else:
+        d.plan_shared(group_indptr, *table)
 
 
 def run_ours(args, rank, world):
@@ -187,14 +201,15 @@ def run_ours(args, rank, world):
     sets = []
     for _ in range(n_sets):
         decs = []
-        for name, (ip, ix, la) in views:
+        for name, gi, (ip, ix, la) in views:
             d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
                                                 max_num_pages=int(ip[-1]),
+                                                shared_prefix=gi is not None,
                                                 num_pages=w.pool_pages,
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
                                                 device=dev)
-            d.plan(ip, ix, la)
+            _plan(d, gi, (ip, ix, la))
             decs.append(d)
         sets.append(decs)
     decs = sets[0]
@@ -243,8 +258,8 @@ def run_ours(args, rank, world):
         si = k % n_sets
         copy_stream.wait_event(done[si])
         with torch.cuda.stream(copy_stream):
-            for (name, (ip, ix, la)), d in zip(views, sets[si]):
-                d.plan(ip, ix, la)
+            for (name, gi, table), d in zip(views, sets[si]):
+                _plan(d, gi, table)
             copied[si].record(copy_stream)
         if host:
             for x, h in zip(qs, host["q"]):
@@ -300,13 +315,14 @@ def run_ours(args, rank, world):
 
     # algorithmic bytes of one step
     if w.prefix_tokens:
-        pre_lens = [w.prefix_tokens] * w.batch
+        n_pre = w.prefix_tokens // w.page_size
         suf_lens = list(w.suffix_lens)
         kv_bytes = (w.prefix_tokens + sum(suf_lens)) * 2 * w.hkv * w.head_dim * 2  # prefix once
         io = w.batch * w.hq * (w.head_dim * 2 * 2 + 4)
-        table = 4 * (int(t["prefix"][0][-1]) + int(t["suffix"][0][-1]) + 4 * w.batch + 2)
+        table = 4 * (n_pre + 3 + 2 + int(t["suffix"][0][-1]) + 2 * w.batch + 1)
         step_bytes = kv_bytes + io + table
-        layer_bytes = [alg_bytes_per_layer(w, pre_lens, int(t["prefix"][0][-1])),
+        # per launch: the prefix level reads the shared pages once for all requests
+        layer_bytes = [alg_bytes_per_layer(w, [w.prefix_tokens], n_pre),
                        alg_bytes_per_layer(w, suf_lens, int(t["suffix"][0][-1]))]
     else:
         lb = alg_bytes_per_layer(w, lens, nnz)

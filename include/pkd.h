@@ -82,6 +82,13 @@ typedef struct pkd_config {
  * one; setting both is an error. */
 #define PKD_FLAG_FMA_CONSUMER 1u
 #define PKD_FLAG_MMA_CONSUMER 2u
+/* Shared-prefix context (FlashInfer 完全拆解, Composable Format: a shared
+ * prefix as an (R, 1) block so R queries reuse one read of its KV): plans made
+ * with pkd_plan_shared give work items over blocks of R = 16 / g requests of
+ * one group, run by a decode kernel whose tensor-core tile holds all R x g
+ * query rows of a KV head.  Not combinable with PKD_FLAG_FMA_CONSUMER.  The
+ * workspace then holds R partial-state slots per item. */
+#define PKD_FLAG_SHARED_PREFIX 4u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;
@@ -127,6 +134,19 @@ void pkd_destroy(pkd_ctx *ctx);
 int pkd_plan(pkd_ctx *ctx, const int32_t *indptr, const int32_t *indices,
              const int32_t *last_page_len, int32_t batch, void *stream,
              uint64_t *epoch);
+
+/* Plan a shared-prefix level (needs a context created with
+ * PKD_FLAG_SHARED_PREFIX).  Requests group_indptr[j] .. group_indptr[j+1]-1
+ * (group_indptr[0] = 0, strictly increasing, batch = group_indptr[num_groups])
+ * all attend over group j's pages indices[indptr[j] .. indptr[j+1]) with
+ * last_page_len[j] -- a CSR table over groups.  pkd_run then returns, for
+ * every request and query head, the attention state (out, lse) over its
+ * group's pages, to be combined with the request's own suffix state by
+ * pkd_merge_states (FlashInfer 完全拆解, Composable Format; FlashInfer, in
+ * depth, "Prefill, masks and shared prefixes").  Errors: as pkd_plan. */
+int pkd_plan_shared(pkd_ctx *ctx, const int32_t *group_indptr, int32_t num_groups,
+                    const int32_t *indptr, const int32_t *indices,
+                    const int32_t *last_page_len, void *stream, uint64_t *epoch);
 
 /* Summary of the current plan.  Errors: INVALID_ARG, NO_PLAN. */
 int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
@@ -197,20 +217,30 @@ int pkd_plan_host(const pkd_config *cfg, const int32_t *indptr,
                   int32_t batch, int32_t *host_words, size_t max_words,
                   pkd_plan_info *info);
 
+/* pkd_plan_host for a shared-prefix plan (cfg->flags has
+ * PKD_FLAG_SHARED_PREFIX; arguments as pkd_plan_shared). */
+int pkd_plan_host_shared(const pkd_config *cfg, const int32_t *group_indptr,
+                         int32_t num_groups, const int32_t *indptr, const int32_t *indices,
+                         const int32_t *last_page_len, int32_t *host_words,
+                         size_t max_words, pkd_plan_info *info);
+
 /* Word offsets of the schedule arrays (see pkd_plan_host):
  *   off[0] cta_indptr[num_ctas + 1]
  *   off[1] items[num_items][8] = {req, tok_begin, tok_end, dst_slot,
- *                                 first_page, 0, 0, 0}
+ *                                 first_page, n_req, slot_stride, 0}
  *          (items of CTA c are items[cta_indptr[c] .. cta_indptr[c+1]) in
- *          LPT order; dst_slot -1 = write through to out/lse; first_page =
- *          indptr[req] + tok_begin / P, an index into page_list)
+ *          LPT order; the item covers requests req .. req + n_req - 1 (1
+ *          without grouping); dst_slot -1 = write through to out/lse, else
+ *          request req + i writes slot dst_slot + i * slot_stride;
+ *          first_page = indptr[table row] + tok_begin / P, an index into
+ *          page_list)
  *   off[2] units[num_units][2] = {req, num_chunks}
  *   off[3] merge_indptr[num_units + 1]
  *   off[4] page_list[nnz]    (the CSR indices, unchanged)
  *   off[5] total words
  * Header words 0..15 hold: magic, batch, Hq, Hkv, D, P, num_ctas,
  * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (clamped to
- * int32), split floor, 0.  Errors: INVALID_ARG. */
+ * int32), split floor, requests per block.  Errors: INVALID_ARG. */
 int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 
 /* ---- CUDA-graph capture of a whole decode step ------------------------- */

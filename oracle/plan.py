@@ -87,11 +87,12 @@ class Plan:
     chunk: int
     makespan: int
     cta_indptr: list          # [n_cta + 1]
-    items: list               # per item, queue order: (req, tok_begin, tok_end, dst_slot, first page index)
+    items: list               # per item, queue order: (first request, tok_begin, tok_end,
+    #                           dst_slot, first page index, requests, slot stride)
     units: list               # per split request: (req, n_chunks)
     merge_indptr: list        # [n_units + 1]
     page_list: list           # the CSR page ids, as given
-    lens: list
+    lens: list                # per block (per request without grouping)
 
     @property
     def n_items(self):
@@ -132,9 +133,29 @@ def _lpt(items, n_cta):
 
 
 def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
-         alpha: int, min_chunk_tokens: int, chunk_divisors=(1, 2, 4)) -> Plan:
-    lens = lengths(indptr, last, indices, page_size, num_pages)
+         alpha: int, min_chunk_tokens: int, chunk_divisors=(1, 2, 4), group_indptr=None,
+         rows: int = 1) -> Plan:
+    """Schedule a decode step.  Without ``group_indptr`` the table has one row
+    per request.  With it (a shared-prefix level, "FlashInfer 完全拆解",
+    section Composable Format) the table has one row per group, requests
+    group_indptr[j] .. group_indptr[j+1]-1 share group j's pages, and each
+    group's requests are cut into blocks of ``rows`` consecutive requests; a
+    work item covers one block."""
+    row_lens = lengths(indptr, last, indices, page_size, num_pages)
     P = page_size
+    if group_indptr is None:
+        blocks = [(i, 1, i) for i in range(len(row_lens))]     # (first request, n, table row)
+    else:
+        gi = [int(x) for x in group_indptr]
+        if len(gi) != len(row_lens) + 1 or (gi and gi[0] != 0):
+            raise TableError("group_indptr must have one entry per group + 1, starting at 0")
+        blocks = []
+        for j in range(len(row_lens)):
+            if gi[j + 1] <= gi[j]:
+                raise TableError(f"group {j} has no request")
+            for r in range(gi[j], gi[j + 1], rows):
+                blocks.append((r, min(rows, gi[j + 1] - r), j))
+    lens = [row_lens[b[2]] for b in blocks]
     W = sum(lens)
     L = _ceil_div(W, n_cta)
     floor = _round_up(max(min_chunk_tokens, 1), P)
@@ -150,23 +171,31 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
             best = (c, makespan, queues)
     chunk, makespan, queues = best
 
-    # P4: reduction map over split requests, ascending request id
+    # P4: reduction map: each request of a split block is a unit with one
+    # partial slot per chunk; units in ascending request order
     n_chunks = [_ceil_div(l, chunk) for l in lens]
-    units = [(i, n_chunks[i]) for i in range(len(lens)) if n_chunks[i] > 1]
+    units = []
     merge_indptr = [0]
-    first_slot = {}
-    for req, nc in units:
-        first_slot[req] = merge_indptr[-1]
-        merge_indptr.append(merge_indptr[-1] + nc)
+    block_slot = {}
+    for bi, (r0, n, row) in enumerate(blocks):
+        if n_chunks[bi] > 1:
+            block_slot[bi] = merge_indptr[-1]
+            for r in range(r0, r0 + n):
+                units.append((r, n_chunks[bi]))
+                merge_indptr.append(merge_indptr[-1] + n_chunks[bi])
 
     cta_indptr = [0]
     items = []
     indptr = [int(x) for x in indptr]
     for q in queues:
-        for cost, req, k, tb, te in q:
-            dst = first_slot[req] + k if req in first_slot else -1
-            # page reference: index (into the CSR indices) of the item's first page
-            items.append((req, tb, te, dst, indptr[req] + tb // P))
+        for cost, bi, k, tb, te in q:
+            r0, n, row = blocks[bi]
+            split = bi in block_slot
+            dst = block_slot[bi] + k if split else -1
+            # page reference: index (into the CSR indices) of the item's first
+            # page; request r0 + i of the block writes slot dst + i * stride
+            items.append((r0, tb, te, dst, indptr[row] + tb // P, n,
+                          n_chunks[bi] if split else 0))
         cta_indptr.append(len(items))
     page_list = [int(x) for x in indices[: indptr[-1] if indptr else 0]]
     return Plan(chunk, makespan, cta_indptr, items, units, merge_indptr,

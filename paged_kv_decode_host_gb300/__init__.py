@@ -47,7 +47,7 @@ EXPORTS = (
     "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
     "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
-    "pkd_append_kv",
+    "pkd_append_kv", "pkd_plan_shared", "pkd_plan_host_shared",
 )
 
 
@@ -119,6 +119,9 @@ def load():
         "pkd_run_static_scratch": (ctypes.c_int, [cfgp, vp, sz, vp, vp, vp, vp, vp]),
         "pkd_append_kv": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
                                          i32, i32, vp, vp]),
+        "pkd_plan_shared": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(u64)]),
+        "pkd_plan_host_shared": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp, sz,
+                                                ctypes.POINTER(PlanInfo)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -156,6 +159,7 @@ def _ptr(a: np.ndarray):
 
 FLAG_FMA_CONSUMER = 1   # fold the GQA group onto CUDA cores (fp32 FMA)
 FLAG_MMA_CONSUMER = 2   # fold it onto tensor cores (mma.sync, bf16 in / fp32 acc)
+FLAG_SHARED_PREFIX = 4  # shared-prefix context: plans over groups of requests
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -184,6 +188,21 @@ def plan_host(cfg: Config, indptr, indices, last_page_len):
     return words, info.as_dict(), off
 
 
+def plan_host_shared(cfg: Config, group_indptr, indptr, indices, last_page_len):
+    """The C++ scheduler for a shared-prefix level, on the host."""
+    lib = load()
+    gi = _host_i32(group_indptr)
+    indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
+    off = schedule_layout(cfg)
+    words = np.zeros(off[5], dtype=np.int32)
+    info = PlanInfo()
+    st = lib.pkd_plan_host_shared(ctypes.byref(cfg), _ptr(gi), int(last.shape[0]), _ptr(indptr),
+                                  _ptr(indices), _ptr(last), _ptr(words), words.size,
+                                  ctypes.byref(info))
+    _check(st, "pkd_plan_host_shared")
+    return words, info.as_dict(), off
+
+
 def decode_schedule(words, off, info):
     """Unpack schedule words into python lists (same shape as the plan
     restatement's fields)."""
@@ -191,7 +210,7 @@ def decode_schedule(words, off, info):
                                     info["nnz"])
     cta_indptr = words[off[0]:off[0] + n_cta + 1].tolist()
     it = words[off[1]:off[1] + 8 * n_items].reshape(n_items, 8)
-    items = [tuple(int(x) for x in r[:5]) for r in it]
+    items = [tuple(int(x) for x in r[:7]) for r in it]
     un = words[off[2]:off[2] + 2 * n_units].reshape(n_units, 2)
     units = [tuple(int(x) for x in r) for r in un]
     merge_indptr = words[off[3]:off[3] + n_units + 1].tolist()
@@ -246,7 +265,7 @@ class BatchDecodeWithPagedKVCache:
 
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
-                 use_tensor_cores=None, kv_layout="NHD", device=None):
+                 use_tensor_cores=None, shared_prefix=False, kv_layout="NHD", device=None):
         import torch
         if kv_layout != "NHD":
             raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
@@ -256,6 +275,8 @@ class BatchDecodeWithPagedKVCache:
         self.num_pages = num_pages
         flags = 0 if use_tensor_cores is None else (
             FLAG_MMA_CONSUMER if use_tensor_cores else FLAG_FMA_CONSUMER)
+        if shared_prefix:
+            flags |= FLAG_SHARED_PREFIX
         self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch,
                                max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas, flags)
         with torch.cuda.device(self.device):
@@ -285,6 +306,24 @@ class BatchDecodeWithPagedKVCache:
                             _stream_ptr(stream), ctypes.byref(ep)), "pkd_plan")
         self.epoch = ep.value
         self.batch = batch
+        return self.epoch
+
+    def plan_shared(self, group_indptr, indptr, indices, last_page_len, stream=None):
+        """Plan a shared-prefix level: requests group_indptr[j] ..
+        group_indptr[j+1]-1 attend over group j's pages (CSR over groups).
+        Needs ``shared_prefix=True``.  Returns the epoch."""
+        lib = load()
+        gi = _host_i32(group_indptr)
+        indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
+        n_groups = int(last.shape[0])
+        if gi.shape[0] != n_groups + 1 or indptr.shape[0] != n_groups + 1:
+            raise PkdError(-2, "group_indptr and indptr need one entry per group + 1")
+        ep = ctypes.c_uint64()
+        _check(lib.pkd_plan_shared(self._h, _ptr(gi), n_groups, _ptr(indptr), _ptr(indices),
+                                   _ptr(last), _stream_ptr(stream), ctypes.byref(ep)),
+               "pkd_plan_shared")
+        self.epoch = ep.value
+        self.batch = int(gi[-1]) if n_groups else 0
         return self.epoch
 
     def plan_info(self):

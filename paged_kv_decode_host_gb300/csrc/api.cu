@@ -24,6 +24,7 @@ struct pkd_ctx {
   int32_t n_cta = 0;
   int32_t group = 0;
   bool mma = false;
+  bool block = false;  // shared-prefix row-block kernel
   int smem_bytes = 0;
   int merge_grid = 0;
   int device = 0;
@@ -49,11 +50,19 @@ namespace {
 
 bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
+// The consumer flags exclude each other; the shared-prefix kernel exists for
+// the tensor-core consumer only.
+bool valid_flags(uint32_t f) {
+  const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX;
+  if (f & ~known) return false;
+  if ((f & PKD_FLAG_FMA_CONSUMER) && (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX)))
+    return false;
+  return true;
+}
+
 int check_config(const pkd_config* c) {
   if (c == nullptr) return PKD_E_INVALID_ARG;
-  if ((c->flags & ~(PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER)) != 0 ||
-      c->flags == (PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER))
-    return PKD_E_INVALID_ARG;
+  if (!valid_flags(c->flags)) return PKD_E_INVALID_ARG;
   if (c->max_batch < 0 || c->max_num_pages < 0 || c->num_pages < 1 || c->page_size < 1 ||
       c->num_ctas < 0)
     return PKD_E_INVALID_ARG;
@@ -80,8 +89,9 @@ int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKD_E_CUDA;
   const bool mma = use_mma_consumer(g, c->flags);
-  if (decode_prepare(g, mma, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
-  if (decode_occupancy(g, mma, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
+  const bool block = (c->flags & PKD_FLAG_SHARED_PREFIX) != 0;
+  if (decode_prepare(g, mma, block, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
+  if (decode_occupancy(g, mma, block, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
     return PKD_E_CUDA;
   if (per_sm < 1) return PKD_E_UNSUPPORTED_SHAPE;
   *n_cta = sms * per_sm;
@@ -114,8 +124,8 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
   if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
-  if (launch_decode(ctx->group, ctx->mma, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes,
-                    stream) != cudaSuccess)
+  if (launch_decode(ctx->group, ctx->mma, ctx->block, a, ctx->n_cta, c.num_kv_heads,
+                    ctx->smem_bytes, stream) != cudaSuccess)
     return PKD_E_CUDA;
   if (ev_after && cudaEventRecordWithFlags(ev_after, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
@@ -170,6 +180,21 @@ int pkd_schedule_layout(const pkd_config* cfg, int64_t off[6]) {
   return PKD_OK;
 }
 
+int pkd_plan_host_shared(const pkd_config* cfg, const int32_t* group_indptr, int32_t num_groups,
+                         const int32_t* indptr, const int32_t* indices,
+                         const int32_t* last_page_len, int32_t* host_words, size_t max_words,
+                         pkd_plan_info* info) {
+  int st = check_config(cfg);
+  if (st != PKD_OK) return st;
+  if (cfg->num_ctas < 1 || host_words == nullptr || !(cfg->flags & PKD_FLAG_SHARED_PREFIX))
+    return PKD_E_INVALID_ARG;
+  if (num_groups > 0 && group_indptr == nullptr) return PKD_E_INVALID_ARG;
+  Layout L = make_layout(*cfg, cfg->num_ctas);
+  if (max_words < (size_t)L.words) return PKD_E_INVALID_ARG;
+  return plan_schedule_grouped(*cfg, cfg->num_ctas, L, group_indptr, num_groups, indptr, indices,
+                               last_page_len, host_words, info);
+}
+
 int pkd_plan_host(const pkd_config* cfg, const int32_t* indptr, const int32_t* indices,
                   const int32_t* last_page_len, int32_t batch, int32_t* host_words,
                   size_t max_words, pkd_plan_info* info) {
@@ -202,12 +227,13 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
   ctx->cfg = *cfg;
   ctx->group = cfg->num_qo_heads / cfg->num_kv_heads;
   ctx->mma = use_mma_consumer(ctx->group, cfg->flags);
+  ctx->block = (cfg->flags & PKD_FLAG_SHARED_PREFIX) != 0;
   st = resolve_ctas(cfg, &ctx->n_cta, &ctx->smem_bytes);
   if (st != PKD_OK) {
     delete ctx;
     return st;
   }
-  if (decode_prepare(ctx->group, ctx->mma, ctx->smem_bytes) != cudaSuccess) {
+  if (decode_prepare(ctx->group, ctx->mma, ctx->block, ctx->smem_bytes) != cudaSuccess) {
     delete ctx;
     return PKD_E_CUDA;
   }
@@ -249,8 +275,10 @@ void pkd_destroy(pkd_ctx* ctx) {
   delete ctx;
 }
 
-int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
-             const int32_t* last_page_len, int32_t batch, void* stream, uint64_t* epoch) {
+// Plan (grouped or not) into the next staging buffer and publish it.
+static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n_rows,
+                            const int32_t* indptr, const int32_t* indices,
+                            const int32_t* last_page_len, void* stream, uint64_t* epoch) {
   if (ctx == nullptr) return PKD_E_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int k = ctx->next_staging;
@@ -260,8 +288,8 @@ int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
   }
   int32_t* words = ctx->staging[k];
   pkd_plan_info info{};
-  int st = plan_schedule(ctx->cfg, ctx->n_cta, ctx->layout, indptr, indices, last_page_len,
-                         batch, words, &info);
+  int st = plan_schedule_grouped(ctx->cfg, ctx->n_cta, ctx->layout, group_indptr, n_rows,
+                                 indptr, indices, last_page_len, words, &info);
   if (st != PKD_OK) return st;
   const Layout& L = ctx->layout;
   // fixed-size part: header, cta queues, items, units, merge map
@@ -279,6 +307,20 @@ int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
   ctx->epoch += 1;
   if (epoch) *epoch = ctx->epoch;
   return PKD_OK;
+}
+
+int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
+             const int32_t* last_page_len, int32_t batch, void* stream, uint64_t* epoch) {
+  return plan_and_publish(ctx, nullptr, batch, indptr, indices, last_page_len, stream, epoch);
+}
+
+int pkd_plan_shared(pkd_ctx* ctx, const int32_t* group_indptr, int32_t num_groups,
+                    const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
+                    void* stream, uint64_t* epoch) {
+  if (ctx == nullptr || !ctx->block) return PKD_E_INVALID_ARG;
+  if (num_groups > 0 && group_indptr == nullptr) return PKD_E_INVALID_ARG;
+  return plan_and_publish(ctx, group_indptr, num_groups, indptr, indices, last_page_len, stream,
+                          epoch);
 }
 
 int pkd_get_plan_info(const pkd_ctx* ctx, pkd_plan_info* info) {

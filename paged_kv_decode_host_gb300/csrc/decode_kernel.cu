@@ -665,7 +665,185 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
   }
 }
 
-template <int G, bool kMma>
+
+// --------------------------------------- shared-prefix row-block consumer (MMA)
+// A work item covers a block of n_req <= 16 / G consecutive requests that
+// attend over the same pages (a shared prefix: FlashInfer 完全拆解, Composable
+// Format, the (R, 1) block).  All 16 rows of the m16n8k16 tile are used:
+// row r is request r / G of the block and query head hk * G + r % G, so one
+// K/V read from shared memory serves n_req * G query rows.
+__device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One tile row's online-softmax update over this lane's 4 scores (tokens
+// 2 tig, 2 tig + 1, 8 + 2 tig, 9 + 2 tig); returns the rescale factor.
+__device__ __forceinline__ float softmax_row(float (&s4)[4], float& m_run, float& l_run) {
+  float mx = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+  const float alpha = exp2f(m_run - m_use);
+  float psum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    s4[k] = exp2f(s4[k] - m_use);
+    psum += s4[k];
+  }
+  l_run = l_run * alpha + psum;
+  m_run = m_new;
+  return alpha;
+}
+
+template <int G>
+__device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
+                                       const uint8_t* stages, int stage_bytes, uint64_t* full,
+                                       uint64_t* empty, volatile int* abort_flag, int warp,
+                                       int lane) {
+  const int hk = warp;
+  const int grp = lane >> 2;
+  const int tig = lane & 3;
+  // the lane's two tile rows: grp and grp + 8
+  const int rq0 = grp / G, hd0 = grp % G;
+  const int rq1 = (grp + 8) / G, hd1 = (grp + 8) % G;
+  const int rs = row_stride(a.row_bytes);
+  const uint32_t stage0 = smem_u32(stages);
+  const uint32_t k_lane = (uint32_t)((lane & 7) * rs + hk * (kHeadDim * 2) + (lane >> 3) * 16);
+  const uint32_t v_lane = (uint32_t)(kTS * rs + (((lane >> 3) & 1) * 8 + (lane & 7)) * rs +
+                                     hk * (kHeadDim * 2) + (lane >> 4) * 16);
+  pdl_wait();   // q may come from the previous kernel in the stream
+  uint32_t stage = 0;
+  for (int it = it0; it < it1; ++it) {
+    const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
+    const int req = item[0], tb = item[1], te = item[2], dst = item[3];
+    const int n_req = item[5], stride = item[6];
+    const bool ok0 = rq0 < n_req, ok1 = rq1 < n_req;
+    uint32_t qa0[8], qa1[8], qa2[8], qa3[8];
+    {
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+          a.q + ((int64_t)(req + (ok0 ? rq0 : 0)) * a.hq + (int64_t)hk * G + hd0) * kHeadDim);
+      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+          a.q + ((int64_t)(req + (ok1 ? rq1 : 0)) * a.hq + (int64_t)hk * G + hd1) * kHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qa0[ks] = ok0 ? __ldg(q0 + ks * 8 + tig) : 0u;
+        qa2[ks] = ok0 ? __ldg(q0 + ks * 8 + 4 + tig) : 0u;
+        qa1[ks] = ok1 ? __ldg(q1 + ks * 8 + tig) : 0u;
+        qa3[ks] = ok1 ? __ldg(q1 + ks * 8 + 4 + tig) : 0u;
+      }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[dt][c] = 0.f;
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+
+    for (int t = tb; t < te; t += kTS) {
+      const int n = min(kTS, te - t);
+      const int slot = (int)(stage % kStages);
+      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      if (!__all_sync(kFull, got)) {
+        if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+        return;
+      }
+      const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
+      if (n < kTS) {
+        uint8_t* vrow = const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes +
+                        (size_t)kTS * rs + hk * (kHeadDim * 2) + (lane & 15) * 16;
+        for (int r = n + (lane >> 4); r < kTS; r += 2)
+          *reinterpret_cast<uint4*>(vrow + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+      }
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[nt][c] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sbase + k_lane + (uint32_t)(nt * 8 * rs + kp * 64), b0, b1, b2, b3);
+          mma_bf16_full(sc[nt], qa0[2 * kp], qa1[2 * kp], qa2[2 * kp], qa3[2 * kp], b0, b1);
+          mma_bf16_full(sc[nt], qa0[2 * kp + 1], qa1[2 * kp + 1], qa2[2 * kp + 1],
+                        qa3[2 * kp + 1], b2, b3);
+        }
+      }
+      float s0[4], s1[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const bool v = nt * 8 + 2 * tig + c < n;
+          s0[nt * 2 + c] = v ? sc[nt][c] * a.scale_log2 : -CUDART_INF_F;
+          s1[nt * 2 + c] = v ? sc[nt][2 + c] * a.scale_log2 : -CUDART_INF_F;
+        }
+      const float al0 = softmax_row(s0, m0, l0);
+      const float al1 = softmax_row(s1, m1, l1);
+      const uint32_t pa0 = pack_bf16x2(s0[0], s0[1]);   // row grp, tokens 2 tig, +1
+      const uint32_t pa1 = pack_bf16x2(s1[0], s1[1]);   // row grp + 8
+      const uint32_t pa2 = pack_bf16x2(s0[2], s0[3]);   // row grp, tokens 8 + 2 tig, +1
+      const uint32_t pa3 = pack_bf16x2(s1[2], s1[3]);   // row grp + 8
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sbase + v_lane + (uint32_t)(dp * 32), b0, b1, b2, b3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          o[2 * dp + h][0] *= al0;
+          o[2 * dp + h][1] *= al0;
+          o[2 * dp + h][2] *= al1;
+          o[2 * dp + h][3] *= al1;
+        }
+        mma_bf16_full(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+        mma_bf16_full(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++stage;
+    }
+
+    l0 += __shfl_xor_sync(kFull, l0, 1);
+    l0 += __shfl_xor_sync(kFull, l0, 2);
+    l1 += __shfl_xor_sync(kFull, l1, 1);
+    l1 += __shfl_xor_sync(kFull, l1, 2);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const bool ok = rr ? ok1 : ok0;
+      if (!ok) continue;
+      const int rq = rr ? rq1 : rq0;
+      const int head = hk * G + (rr ? hd1 : hd0);
+      const float l = rr ? l1 : l0;
+      const float m = rr ? m1 : m0;
+      const float inv = 1.f / l;
+      const float lse_nat = (m + log2f(l)) * 0.69314718055994530942f;
+      if (dst < 0) {
+        const int64_t qrow = (int64_t)(req + rq) * a.hq + head;
+        uint32_t* op = reinterpret_cast<uint32_t*>(a.out + qrow * kHeadDim) + tig;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt)
+          op[dt * 4] = pack_bf16x2(o[dt][2 * rr] * inv, o[dt][2 * rr + 1] * inv);
+        if (a.lse != nullptr && tig == 0) a.lse[qrow] = lse_nat;
+      } else {
+        const int64_t prow = (int64_t)(dst + rq * stride) * a.hq + head;
+        float2* op = reinterpret_cast<float2*>(a.o_part + prow * kHeadDim) + tig;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt)
+          op[dt * 4] = make_float2(o[dt][2 * rr] * inv, o[dt][2 * rr + 1] * inv);
+        if (tig == 0) a.l_part[prow] = lse_nat;
+      }
+    }
+  }
+}
+
+template <int G, bool kMma, bool kBlock>
 __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int stage_bytes = 2 * kTS * row_stride(a.row_bytes);
@@ -705,7 +883,10 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
   if (warp == n_cons) {
     run_producer(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
   } else if (warp < n_cons) {
-    if constexpr (kMma) {
+    if constexpr (kBlock) {
+      run_consumer_mma_block<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
+                                lane);
+    } else if constexpr (kMma) {
       run_consumer_mma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp, lane);
     } else {
       run_consumer_fma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
@@ -714,17 +895,20 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
   }
 }
 
-template <int G, bool kMma>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_kernel<G, kMma>);
+template <int G>
+const void* kernel_ptr(bool mma, bool block) {
+  if (block) return reinterpret_cast<const void*>(&decode_kernel<G, true, true>);
+  return mma ? reinterpret_cast<const void*>(&decode_kernel<G, true, false>)
+             : reinterpret_cast<const void*>(&decode_kernel<G, false, false>);
 }
 
-const void* kernel_for(int group, bool mma) {
+const void* kernel_for(int group, bool mma, bool block) {
+  if (block && !mma) return nullptr;
   switch (group) {
-    case 1: return mma ? kernel_ptr<1, true>() : kernel_ptr<1, false>();
-    case 2: return mma ? kernel_ptr<2, true>() : kernel_ptr<2, false>();
-    case 4: return mma ? kernel_ptr<4, true>() : kernel_ptr<4, false>();
-    case 8: return mma ? kernel_ptr<8, true>() : kernel_ptr<8, false>();
+    case 1: return kernel_ptr<1>(mma, block);
+    case 2: return kernel_ptr<2>(mma, block);
+    case 4: return kernel_ptr<4>(mma, block);
+    case 8: return kernel_ptr<8>(mma, block);
     default: return nullptr;
   }
 }
@@ -746,8 +930,8 @@ int decode_smem_bytes(int hkv, int group) {
          2 * kStages * 8 + 16;
 }
 
-cudaError_t decode_prepare(int group, bool mma, int smem_bytes) {
-  const void* k = kernel_for(group, mma);
+cudaError_t decode_prepare(int group, bool mma, bool block, int smem_bytes) {
+  const void* k = kernel_for(group, mma, block);
   if (!k) return cudaErrorInvalidValue;
   // The attribute is per kernel, shared by every context: always allow the
   // largest layout (8 KV heads) so a smaller context never lowers it.
@@ -756,16 +940,17 @@ cudaError_t decode_prepare(int group, bool mma, int smem_bytes) {
                               smem_bytes > most ? smem_bytes : most);
 }
 
-cudaError_t decode_occupancy(int group, bool mma, int hkv, int smem_bytes, int* blocks_per_sm) {
-  const void* k = kernel_for(group, mma);
+cudaError_t decode_occupancy(int group, bool mma, bool block, int hkv, int smem_bytes,
+                             int* blocks_per_sm) {
+  const void* k = kernel_for(group, mma, block);
   if (!k) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, decode_threads(hkv),
                                                        (size_t)smem_bytes);
 }
 
-cudaError_t launch_decode(int group, bool mma, const DecodeArgs& a, int grid, int hkv,
-                          int smem_bytes, cudaStream_t stream) {
-  const void* k = kernel_for(group, mma);
+cudaError_t launch_decode(int group, bool mma, bool block, const DecodeArgs& a, int grid,
+                          int hkv, int smem_bytes, cudaStream_t stream) {
+  const void* k = kernel_for(group, mma, block);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -23,11 +23,13 @@ constexpr int kMergeThreads = 256;
 // Schedule header words (first 16 int32 of the workspace).
 enum HeaderWord {
   H_MAGIC = 0, H_BATCH, H_HQ, H_HKV, H_D, H_P, H_NCTA, H_NITEMS, H_NUNITS,
-  H_NSLOTS, H_CHUNK, H_ALPHA, H_NNZ, H_MAKESPAN, H_MINCHUNK, H_RESERVED,
+  H_NSLOTS, H_CHUNK, H_ALPHA, H_NNZ, H_MAKESPAN, H_MINCHUNK, H_BLOCK,
   H_WORDS = 16
 };
 
-constexpr int kItemWords = 8;  // req, tok_begin, tok_end, dst_slot, page_off, 0,0,0
+// req (first of the block), tok_begin, tok_end, dst_slot, first page index,
+// requests in the block, slot stride per request, 0
+constexpr int kItemWords = 8;
 
 // Fixed word offsets of the schedule arrays, all derived from capacities.
 struct Layout {
@@ -38,10 +40,11 @@ struct Layout {
   int64_t page_list;     // [max_num_pages]
   int64_t words;         // schedule words (end of page_list)
   int64_t max_items;
+  int64_t max_slots;     // partial-state slots
   // byte offsets inside the device workspace
   size_t err_byte;       // int32 device error word (never written by plan)
-  size_t o_part_byte;    // fp32 [max_items][Hq][D]
-  size_t l_part_byte;    // fp32 [max_items][Hq]
+  size_t o_part_byte;    // fp32 [max_slots][Hq][D]
+  size_t l_part_byte;    // fp32 [max_slots][Hq]
   size_t total_bytes;
 };
 
@@ -58,6 +61,9 @@ inline int64_t max_items_for(int64_t max_batch, int64_t n_cta) {
 inline Layout make_layout(const pkd_config& c, int64_t n_cta) {
   Layout L{};
   L.max_items = max_items_for(c.max_batch, n_cta);
+  // a shared-prefix block of 16 / g requests writes one slot per request
+  L.max_slots = L.max_items * ((c.flags & PKD_FLAG_SHARED_PREFIX)
+                                   ? 16 / (c.num_qo_heads / c.num_kv_heads) : 1);
   L.cta_indptr = H_WORDS;
   L.items = align_up(L.cta_indptr + n_cta + 1, 8);
   L.units = L.items + L.max_items * kItemWords;
@@ -68,9 +74,9 @@ inline Layout make_layout(const pkd_config& c, int64_t n_cta) {
   L.err_byte = (size_t)align_up((int64_t)sched_bytes, 256);
   L.o_part_byte = L.err_byte + 256;
   L.l_part_byte = L.o_part_byte +
-                  (size_t)L.max_items * c.num_qo_heads * c.head_dim * sizeof(float);
+                  (size_t)L.max_slots * c.num_qo_heads * c.head_dim * sizeof(float);
   L.l_part_byte = (size_t)align_up((int64_t)L.l_part_byte, 256);
-  L.total_bytes = L.l_part_byte + (size_t)L.max_items * c.num_qo_heads * sizeof(float);
+  L.total_bytes = L.l_part_byte + (size_t)L.max_slots * c.num_qo_heads * sizeof(float);
   L.total_bytes = (size_t)align_up((int64_t)L.total_bytes, 256);
   return L;
 }
@@ -106,10 +112,12 @@ struct MergeArgs {
 // Kernel launchers (decode_kernel.cu / merge_kernels.cu).
 int decode_smem_bytes(int hkv, int group);
 int decode_threads(int hkv);
-cudaError_t decode_prepare(int group, bool mma, int smem_bytes);
-cudaError_t decode_occupancy(int group, bool mma, int hkv, int smem_bytes, int* blocks_per_sm);
-cudaError_t launch_decode(int group, bool mma, const DecodeArgs& a, int grid, int hkv,
-                          int smem_bytes, cudaStream_t stream);
+// block: the shared-prefix variant (work items over row blocks of requests)
+cudaError_t decode_prepare(int group, bool mma, bool block, int smem_bytes);
+cudaError_t decode_occupancy(int group, bool mma, bool block, int hkv, int smem_bytes,
+                             int* blocks_per_sm);
+cudaError_t launch_decode(int group, bool mma, bool block, const DecodeArgs& a, int grid,
+                          int hkv, int smem_bytes, cudaStream_t stream);
 // Consumer variant for a group size: tensor cores (mma.sync) or CUDA cores.
 bool use_mma_consumer(int group, uint32_t flags);
 // Merge grid for a persistent decode grid of n_cta CTAs.
@@ -130,5 +138,11 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
                   const int32_t* indptr, const int32_t* indices,
                   const int32_t* last, int32_t batch, int32_t* words,
                   pkd_plan_info* info);
+// Same over groups of requests sharing one table row each (group_indptr over
+// requests, n_rows groups); group_indptr == nullptr gives plan_schedule.
+int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                          const int32_t* group_indptr, int32_t n_rows, const int32_t* indptr,
+                          const int32_t* indices, const int32_t* last, int32_t* words,
+                          pkd_plan_info* info);
 
 }  // namespace pkd

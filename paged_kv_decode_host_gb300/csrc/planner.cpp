@@ -124,32 +124,76 @@ int64_t lpt(const std::vector<Item>& items, int32_t n_cta, std::vector<int32_t>*
 int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
                   const int32_t* indptr, const int32_t* indices, const int32_t* last,
                   int32_t batch, int32_t* words, pkd_plan_info* info) {
-  if (batch < 0 || n_cta < 1 || words == nullptr) return PKD_E_INVALID_ARG;
-  if (batch > 0 && (indptr == nullptr || last == nullptr)) return PKD_E_INVALID_ARG;
-  if (batch > cfg.max_batch) return PKD_E_CAPACITY;
-  const int64_t P = cfg.page_size;
+  return plan_schedule_grouped(cfg, n_cta, L, nullptr, batch, indptr, indices, last, words,
+                               info);
+}
 
-  // ---- P0: table check and lengths
-  std::vector<int64_t> lens((size_t)batch);
-  int64_t total = 0;
+// Row blocks: a block is a run of consecutive requests that attend over the
+// same pages (table row).  Without grouping every request is its own block;
+// with grouping (a shared prefix, FlashInfer 完全拆解, Composable Format) the
+// requests of a group are cut into blocks of `rows` = 16 / g requests, the
+// query rows one tensor-core tile holds per KV head, so one read of the
+// group's pages serves the whole block.
+int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                          const int32_t* group_indptr, int32_t n_rows, const int32_t* indptr,
+                          const int32_t* indices, const int32_t* last, int32_t* words,
+                          pkd_plan_info* info) {
+  // n_rows: table rows (= requests without grouping, = groups with it)
+  if (n_rows < 0 || n_cta < 1 || words == nullptr) return PKD_E_INVALID_ARG;
+  if (n_rows > 0 && (indptr == nullptr || last == nullptr)) return PKD_E_INVALID_ARG;
+  const int64_t P = cfg.page_size;
+  const int32_t group = cfg.num_qo_heads / cfg.num_kv_heads;
+  const int32_t rows = group_indptr ? 16 / group : 1;
+
+  // requests
+  int32_t batch = n_rows;
+  if (group_indptr) {
+    if (group_indptr[0] != 0) return PKD_E_BAD_TABLE;
+    for (int32_t j = 0; j < n_rows; ++j)
+      if (group_indptr[j + 1] <= group_indptr[j]) return PKD_E_BAD_TABLE;
+    batch = n_rows > 0 ? group_indptr[n_rows] : 0;
+  }
+  if (batch > cfg.max_batch) return PKD_E_CAPACITY;
+
+  // ---- P0: table check and lengths (per table row)
+  std::vector<int64_t> row_len((size_t)n_rows);
   int64_t nnz = 0;
-  if (batch > 0) {
+  if (n_rows > 0) {
     if (indptr[0] != 0) return PKD_E_BAD_TABLE;
-    for (int32_t i = 0; i < batch; ++i) {
+    for (int32_t i = 0; i < n_rows; ++i) {
       int64_t n = (int64_t)indptr[i + 1] - indptr[i];
       if (n < 1) return PKD_E_BAD_TABLE;
       if (last[i] < 1 || last[i] > P) return PKD_E_BAD_TABLE;
-      lens[i] = P * (n - 1) + last[i];
-      if (lens[i] > 0x7fffffffLL) return PKD_E_CAPACITY;
-      total += lens[i];
+      row_len[i] = P * (n - 1) + last[i];
+      if (row_len[i] > 0x7fffffffLL) return PKD_E_CAPACITY;
     }
-    nnz = indptr[batch];
+    nnz = indptr[n_rows];
     if (nnz > cfg.max_num_pages) return PKD_E_CAPACITY;
     if (nnz > 0 && indices == nullptr) return PKD_E_INVALID_ARG;
-    // page ids go into the schedule verbatim (the kernel reads request i's
-    // pages at indptr[i] + t / P), range-checked in the same pass
+    // page ids go into the schedule verbatim (the kernel reads a table row's
+    // pages at indptr[row] + t / P), range-checked in the same pass
     if (!copy_checked(indices, words + L.page_list, nnz, cfg.num_pages)) return PKD_E_BAD_TABLE;
   }
+
+  // ---- row blocks
+  struct Block {
+    int32_t req_first, n_req, table_row;
+  };
+  std::vector<Block> blocks;
+  std::vector<int64_t> lens;  // per block: tokens of its table row
+  if (group_indptr) {
+    for (int32_t j = 0; j < n_rows; ++j)
+      for (int32_t r = group_indptr[j]; r < group_indptr[j + 1]; r += rows) {
+        blocks.push_back(Block{r, std::min(rows, group_indptr[j + 1] - r), j});
+        lens.push_back(row_len[j]);
+      }
+  } else {
+    for (int32_t i = 0; i < n_rows; ++i) blocks.push_back(Block{i, 1, i});
+    lens = row_len;
+  }
+  const int32_t n_blocks = (int32_t)blocks.size();
+  int64_t total = 0;
+  for (int64_t l : lens) total += l;
 
   // ---- P1 + P2 + P3: chunk candidates, split, LPT; keep the best
   const int64_t alpha = cfg.alpha < 0 ? kDefaultAlpha : cfg.alpha;
@@ -178,18 +222,24 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   const int64_t n_items = (int64_t)best_items.size();
   if (n_items > L.max_items) return PKD_E_CAPACITY;
 
-  // ---- P4: reduction map (split requests, ascending id; slots in chunk order)
-  std::vector<int32_t> first_slot((size_t)batch, -1);
+  // ---- P4: reduction map: every request of a split block is a unit with
+  // one slot per chunk, units in ascending request order, slots in chunk order
+  std::vector<int32_t> first_slot((size_t)n_blocks, -1);  // slot of the block's first request
+  std::vector<int32_t> n_chunks((size_t)n_blocks, 1);
   std::vector<std::pair<int32_t, int32_t>> units;
-  int32_t n_slots = 0;
-  for (int32_t i = 0; i < batch; ++i) {
-    int64_t nc = ceil_div(lens[i], best_chunk);
+  int64_t n_slots = 0;
+  for (int32_t b = 0; b < n_blocks; ++b) {
+    const int64_t nc = ceil_div(lens[b], best_chunk);
+    n_chunks[b] = (int32_t)nc;
     if (nc > 1) {
-      first_slot[i] = n_slots;
-      units.emplace_back(i, (int32_t)nc);
-      n_slots += (int32_t)nc;
+      first_slot[b] = (int32_t)n_slots;
+      for (int32_t r = 0; r < blocks[b].n_req; ++r) {
+        units.emplace_back(blocks[b].req_first + r, (int32_t)nc);
+        n_slots += nc;
+      }
     }
   }
+  if (n_slots > L.max_slots || (int64_t)units.size() > L.max_items) return PKD_E_CAPACITY;
 
   // ---- serialize: queues in CTA order, each in assignment (LPT) order
   std::vector<int32_t> count((size_t)n_cta, 0);
@@ -204,13 +254,16 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   int32_t* item_words = words + L.items;
   for (int64_t p = 0; p < n_items; ++p) {
     const Item& it = best_items[by_pos[p]];
+    const Block& bk = blocks[it.req];
     int32_t* w = item_words + p * kItemWords;
-    w[0] = it.req;
+    w[0] = bk.req_first;
     w[1] = it.tok_begin;
     w[2] = it.tok_end;
     w[3] = first_slot[it.req] >= 0 ? first_slot[it.req] + it.chunk_idx : -1;
-    w[4] = (int32_t)(indptr[it.req] + it.tok_begin / P);  // index of the item's first page
-    w[5] = w[6] = w[7] = 0;
+    w[4] = (int32_t)(indptr[bk.table_row] + it.tok_begin / P);  // index of the first page
+    w[5] = bk.n_req;
+    w[6] = first_slot[it.req] >= 0 ? n_chunks[it.req] : 0;     // slot stride per request
+    w[7] = 0;
   }
   int32_t* unit_words = words + L.units;
   int32_t* merge_indptr = words + L.merge_indptr;
@@ -232,12 +285,13 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   h[H_NCTA] = n_cta;
   h[H_NITEMS] = (int32_t)n_items;
   h[H_NUNITS] = (int32_t)units.size();
-  h[H_NSLOTS] = n_slots;
+  h[H_NSLOTS] = (int32_t)n_slots;
   h[H_CHUNK] = (int32_t)best_chunk;
   h[H_ALPHA] = (int32_t)alpha;
   h[H_NNZ] = (int32_t)nnz;
   h[H_MAKESPAN] = (int32_t)std::min<int64_t>(best_span, 0x7fffffff);
   h[H_MINCHUNK] = (int32_t)floor_c;
+  h[H_BLOCK] = rows;
 
   if (info) {
     info->batch = batch;
@@ -245,7 +299,7 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     info->chunk_tokens = (int32_t)best_chunk;
     info->num_items = (int32_t)n_items;
     info->num_units = (int32_t)units.size();
-    info->num_slots = n_slots;
+    info->num_slots = (int32_t)n_slots;
     info->total_tokens = total;
     info->makespan = best_span;
     info->nnz = (int32_t)nnz;

@@ -57,11 +57,11 @@ def test_config_validation(lib):
     ]
     for c in bad:
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -3
-    for bad_flags in (3, 4, 0x80000000):
+    for bad_flags in (3, 5, 7, 8, 0x80000000):
         c = _cfg(16)
         c.flags = bad_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
-    for ok_flags in (0, 1, 2):
+    for ok_flags in (0, 1, 2, 4, 6):
         c = _cfg(16)
         c.flags = ok_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == 0
@@ -149,3 +149,31 @@ def test_plan_host_rejects_bad_tables(lib):
     # int64 tables are refused by the binding before reaching the library
     with pytest.raises(TypeError):
         pkd.plan_host(cfg, np.array([0, 1]), np.array([0]), np.array([1]))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_grouped_plan_bit_exact_random(lib, seed):
+    rng = np.random.default_rng(300 + seed)
+    P = int(rng.choice([1, 3, 16]))
+    hkv = 8
+    g = int(rng.choice([1, 2, 4, 8]))
+    n_groups = int(rng.integers(1, 5))
+    sizes = rng.integers(1, 35, n_groups).tolist()
+    group_indptr = np.array([0] + np.cumsum(sizes).tolist(), dtype=np.int32)
+    lens = rng.integers(1, 12000, n_groups).tolist()
+    pool = sum(-(-l // P) for l in lens) + 4
+    indptr, indices, last = workloads.page_table(lens, P, rng.permutation(pool).astype(np.int32))
+    n_cta = int(rng.choice([3, 64, 152]))
+    cfg = pkd.make_config(g * hkv, hkv, 128, P, int(group_indptr[-1]), int(indptr[-1]), pool,
+                          32, 256, n_cta, pkd.FLAG_SHARED_PREFIX)
+    words, info, off = pkd.plan_host_shared(cfg, group_indptr, indptr, indices, last)
+    got = pkd.decode_schedule(words, off, info)
+    ref = oplan.plan(indptr, indices, last, page_size=P, num_pages=pool, n_cta=n_cta, alpha=32,
+                     min_chunk_tokens=256, group_indptr=group_indptr, rows=16 // g)
+    assert info["chunk_tokens"] == ref.chunk and info["makespan"] == ref.makespan
+    assert got["cta_indptr"] == ref.cta_indptr
+    assert got["items"] == [tuple(x) for x in ref.items]
+    assert got["units"] == [tuple(x) for x in ref.units]
+    assert got["merge_indptr"] == ref.merge_indptr
+    assert got["page_list"] == ref.page_list
+    assert got["header"][15] == 16 // g

@@ -266,23 +266,32 @@ def test_plan_hand_worked(idx):
     _check_plan_case(_golden("plan_hand.json")["cases"][idx])
 
 
-def coverage_check(p, indptr, indices, last, page_size):
-    """Independent check of a schedule: every valid token exactly once,
-    page_list consistent with the table, merge map in chunk order."""
+def coverage_check(p, indptr, indices, last, page_size, group_indptr=None):
+    """Independent check of a schedule: every (request, token of its table
+    row) covered exactly once, page references consistent with the table,
+    partial slots of each split request contiguous in chunk order."""
     P = page_size
-    lens = [P * (indptr[i + 1] - indptr[i] - 1) + last[i] for i in range(len(last))]
-    seen = [np.zeros(l, dtype=np.int32) for l in lens]
+    n_rows = len(last)
+    row_lens = [P * (indptr[i + 1] - indptr[i] - 1) + last[i] for i in range(n_rows)]
+    if group_indptr is None:
+        req_row = list(range(n_rows))
+    else:
+        req_row = [j for j in range(n_rows) for _ in range(group_indptr[j], group_indptr[j + 1])]
+    seen = [np.zeros(row_lens[req_row[r]], dtype=np.int32) for r in range(len(req_row))]
     slots_of = {}
-    for n, (req, tb, te, dst, poff) in enumerate(p.items):
-        assert 0 <= tb < te <= lens[req]
-        assert tb % P == 0
-        seen[req][tb:te] += 1
+    for (r0, tb, te, dst, fp, n, stride) in p.items:
+        row = req_row[r0]
+        assert n >= 1 and all(req_row[r] == row for r in range(r0, r0 + n))
+        assert 0 <= tb < te <= row_lens[row] and tb % P == 0
+        assert fp == indptr[row] + tb // P
         for t in range(tb, te):
-            assert p.page_list[poff + (t - tb) // P] == indices[indptr[req] + t // P]
-        if dst >= 0:
-            slots_of.setdefault(req, []).append((tb, dst))
-    for s in seen:
-        assert np.all(s == 1)
+            assert p.page_list[fp + (t - tb) // P] == indices[indptr[row] + t // P]
+        for i in range(n):
+            seen[r0 + i][tb:te] += 1
+            if dst >= 0:
+                slots_of.setdefault(r0 + i, []).append((tb, dst + i * stride))
+    for s_ in seen:
+        assert np.all(s_ == 1)
     assert p.cta_indptr[0] == 0 and p.cta_indptr[-1] == len(p.items)
     assert all(a <= b for a, b in zip(p.cta_indptr, p.cta_indptr[1:]))
     for u, (req, nc) in enumerate(p.units):
@@ -311,3 +320,39 @@ def test_plan_coverage_random(seed):
     W = sum(lens)
     assert len(p.items) <= B + 4 * n_cta + 4
     assert p.makespan * n_cta >= W                   # a makespan is at least the mean
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_plan_coverage_random(seed):
+    """Shared-prefix plans: groups of requests over one table row each, cut
+    into blocks of `rows` requests."""
+    rng = np.random.default_rng(40 + seed)
+    P = int(rng.choice([1, 16]))
+    n_groups = int(rng.integers(1, 6))
+    sizes = rng.integers(1, 40, n_groups).tolist()
+    group_indptr = [0] + np.cumsum(sizes).tolist()
+    lens = rng.integers(1, 9000, n_groups).tolist()
+    pool = sum(-(-l // P) for l in lens) + 2
+    indptr, indices, last = workloads.page_table(lens, P, rng.permutation(pool).astype(np.int32))
+    rows = int(rng.choice([2, 4, 8, 16]))
+    n_cta = int(rng.choice([5, 64, 152]))
+    p = oplan.plan(indptr, indices, last, page_size=P, num_pages=pool, n_cta=n_cta, alpha=32,
+                   min_chunk_tokens=256, group_indptr=group_indptr, rows=rows)
+    coverage_check(p, indptr.tolist(), indices.tolist(), last.tolist(), P, group_indptr)
+    assert all(n <= rows for (_, _, _, _, _, n, _) in p.items)
+
+
+def test_grouped_plan_hand_worked():
+    """One group of 5 requests sharing 40 tokens (P 16), blocks of 2, 3 CTAs,
+    alpha 0, floor 16.  Blocks: requests {0,1}, {2,3}, {4}, each 40 tokens:
+    W = 120, L = 40 -> chunk 48 (page-rounded): three whole-row items of cost
+    40 (makespan 40); L/2 = 20 -> chunk 32: six items 32, 32, 32, 8, 8, 8 ->
+    loads 40, 40, 40 (tie, larger chunk kept).  No split, so every item writes
+    through; CTA c takes block c."""
+    indptr, indices, last = workloads.page_table([40], 16)
+    p = oplan.plan(indptr, indices, last, page_size=16, num_pages=3, n_cta=3, alpha=0,
+                   min_chunk_tokens=16, group_indptr=[0, 5], rows=2)
+    assert p.chunk == 48 and p.makespan == 40
+    assert p.cta_indptr == [0, 1, 2, 3]
+    assert p.items == [(0, 0, 40, -1, 0, 2, 0), (2, 0, 40, -1, 0, 2, 0), (4, 0, 40, -1, 0, 1, 0)]
+    assert p.units == [] and p.merge_indptr == [0]

@@ -148,6 +148,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------- multi-rank
+
+def max_over_ranks(ms, world, device):
+    """Whole-job time = the slowest rank's (replicas run independent shards,
+    no data-path collective; this is the only exchange, timing metadata)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def aggregate_throughput(bytes_per_rank_step, ms_per_step, world):
+    """GB/s of the whole job: every rank moved bytes_per_rank_step per step,
+    in the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- our arm
 
 def _views(w, t):
@@ -306,11 +326,7 @@ def run_ours(args, rank, world):
     last = graph_of(args.warmup + args.steps + k_roof - 1)
     k1_ms = last[0].layer_times() + (last[1].layer_times() if last[1] is not None else [])
     use["graphs"] = graphs
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
 
     # algorithmic bytes of one step
@@ -328,7 +344,7 @@ def run_ours(args, rank, world):
         lb = alg_bytes_per_layer(w, lens, nnz)
         step_bytes = lb * layers
         layer_bytes = [lb] * layers
-    gbs = world * step_bytes / (ms_step * 1e-3) / 1e9
+    gbs = aggregate_throughput(step_bytes, ms_step, world)
     peak, peak_kind = measured_peak()
     # roofline of the dominant kernel (decode), per launch
     k1_gbs = [b / (ms * 1e-3) / 1e9 for b, ms in zip(layer_bytes, k1_ms) if ms > 0]
@@ -420,11 +436,7 @@ def run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, d
         ms = max(e0.elapsed_time(e1) / steps, wall)
     finally:
         host.clear()
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d + sched),
             "d2h_bytes_per_step": int(d2h),

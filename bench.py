@@ -46,7 +46,7 @@ KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_decode_host_gb300", "csrc", "decode
 # --------------------------------------------------------------------- bytes
 
 def alg_bytes_per_layer(w, lens, nnz):
-    kv = sum(lens) * 2 * w.hkv * w.head_dim * 2
+    kv = sum(lens) * 2 * w.hkv * w.head_dim * w.kv_elem_bytes
     q = w.batch * w.hq * w.head_dim * 2
     out = w.batch * w.hq * w.head_dim * 2
     lse = w.batch * w.hq * 4
@@ -207,9 +207,15 @@ def run_ours(args, rank, world):
     layers = w.layers
     # distinct caches per replay for single-layer workloads so no step reads
     # another step's bytes out of L2
-    copies = 1 if layers > 1 else max(1, int(np.ceil(1.2e9 / (w.pool_pages * 2 * P * w.hkv * 256))))
+    copies = 1 if layers > 1 else max(1, int(np.ceil(
+        1.2e9 / (w.pool_pages * 2 * P * w.hkv * w.head_dim * w.kv_elem_bytes))))
     n_kv = layers * copies
-    kvs = workloads.make_kv(w, device=dev, layers=n_kv)
+    if w.kv_dtype == "e4m3":
+        kvs, kv_scale = workloads.make_kv_fp8(w, device=dev, layers=n_kv)
+        kv_scales = [(kv_scale, kv_scale)] * layers
+    else:
+        kvs = workloads.make_kv(w, device=dev, layers=n_kv)
+        kv_scales = None
     qs = workloads.make_q(w, device=dev, layers=layers)
     outs = [torch.empty_like(x) for x in qs]
     lses = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in qs]
@@ -225,6 +231,7 @@ def run_ours(args, rank, world):
             d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
                                                 max_num_pages=int(ip[-1]),
                                                 shared_prefix=gi is not None,
+                                                kv_dtype=w.kv_dtype,
                                                 num_pages=w.pool_pages,
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
@@ -257,7 +264,8 @@ def run_ours(args, rank, world):
             for c in range(copies):
                 kv_c = kvs[c * layers:(c + 1) * layers]
                 for timing, dst in ((False, graphs), (True, tgraphs)):
-                    dst[si].append((ds[0].capture(qs, kv_c, outs, lses, timing=timing), None, c))
+                    dst[si].append((ds[0].capture(qs, kv_c, outs, lses, timing=timing,
+                                                  kv_scales=kv_scales), None, c))
 
     stream = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream(device=dev)
@@ -371,11 +379,12 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 KV (f16 MMA)",
         "accum_dtype": "fp32",
         "data": "synthetic (seeded N(0,1) bf16 q/KV, seeded lengths and page permutation)",
         "config": {
-            "workload": args.workload, "layers": layers, "batch": w.batch, "hq": w.hq,
+            "workload": args.workload, "kv_dtype": w.kv_dtype, "layers": layers,
+            "batch": w.batch, "hq": w.hq,
             "hkv": w.hkv, "head_dim": w.head_dim, "page_size": P,
             "total_tokens_per_layer": int(sum(lens)), "pages_per_layer": nnz,
             "alg_bytes_per_step": int(step_bytes),
@@ -402,7 +411,7 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and w.kv_dtype == "bf16":
         line["cpu_baseline"] = cpu_baseline(w, t, qs, kvs, budget_s=args.cpu_seconds)
     return line
 
@@ -649,7 +658,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_step",
                     choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix",
-                             "append"])
+                             "llama8b_step_fp8", "append"])
     ap.add_argument("--consumer", choices=["auto", "fma", "mma"], default="auto",
                     help="decode-kernel consumer: the default, or forced CUDA-core (fma) / "
                          "tensor-core (mma) folding of the GQA group")

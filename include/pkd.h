@@ -89,6 +89,13 @@ typedef struct pkd_config {
  * query rows of a KV head.  Not combinable with PKD_FLAG_FMA_CONSUMER.  The
  * workspace then holds R partial-state slots per item. */
 #define PKD_FLAG_SHARED_PREFIX 4u
+/* FP8 cache: the KV cache holds E4M3 values (one byte per element, same NHD
+ * shape) with a per-call scale for K and one for V (pkd_run_scaled): the
+ * attended key is k_scale * K and the value v_scale * V ("FlashInfer 完全拆解",
+ * performance section: E4M3 KV in vLLM; applicability table: low-precision KV
+ * needs a scale contract).  Tensor-core consumer only; not combinable with
+ * PKD_FLAG_SHARED_PREFIX. */
+#define PKD_FLAG_KV_FP8 8u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;
@@ -162,6 +169,14 @@ int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
  * kernel on `stream`.  Errors: INVALID_ARG, NO_PLAN, STALE_PLAN, CUDA. */
 int pkd_run(pkd_ctx *ctx, const void *q, const void *kv, void *out, float *lse,
             uint64_t expect_epoch, void *stream);
+
+/* pkd_run with scales: scores use k_scale * K and the output v_scale * V
+ * (lse is the log-sum-exp of the scaled scores).  Required for an FP8 cache
+ * (PKD_FLAG_KV_FP8; kv then holds E4M3 bytes, [num_pages][2][P][Hkv][D]);
+ * for bf16 any finite scales are allowed, pkd_run is (1, 1).
+ * Errors: as pkd_run; INVALID_ARG for a non-finite scale. */
+int pkd_run_scaled(pkd_ctx *ctx, const void *q, const void *kv, void *out, float *lse,
+                   float k_scale, float v_scale, uint64_t expect_epoch, void *stream);
 
 /* merge_states: for each of n x heads rows,
  *   m = max(s_a, s_b), w_a = exp(s_a - m), w_b = exp(s_b - m),
@@ -247,13 +262,14 @@ int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 /* Capture `layers` pkd_run calls (the current plan's workspace is read at
  * replay time, so re-planning between replays is allowed as long as batch
  * and capacities fit) into a graph.  Arrays of device pointers, one per
- * layer.  flags: PKD_GRAPH_TIMING records an event before and after each
+ * layer; kv_scales: NULL or host floats {k_scale, v_scale} per layer.  flags: PKD_GRAPH_TIMING records an event before and after each
  * layer's decode kernel, readable with pkd_graph_layer_times.
  * Errors: INVALID_ARG, NO_PLAN, CUDA. */
 #define PKD_GRAPH_TIMING 1u
 int pkd_graph_capture(pkd_ctx *ctx, int32_t layers, const void *const *q,
                       const void *const *kv, void *const *out,
-                      float *const *lse, uint32_t flags, pkd_graph **graph);
+                      float *const *lse, const float *kv_scales, uint32_t flags,
+                      pkd_graph **graph);
 /* Launch the captured step on `stream`.  Errors: INVALID_ARG, CUDA. */
 int pkd_graph_launch(pkd_graph *graph, void *stream);
 /* After the launch has completed: decode-kernel milliseconds per layer

@@ -54,7 +54,11 @@ def _load():
         lib.oracle_lengths.argtypes = [p, p, p, i, i, i, p]
         lib.oracle_attend.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, p, i]
         lib.oracle_merge.argtypes = [p, p, p, p, i, i, p, p]
-        for f in (lib.oracle_lengths, lib.oracle_attend, lib.oracle_merge):
+        d = ctypes.c_double
+        lib.oracle_attend_ex.argtypes = [p, p, i, d, d, p, p, p, i, i, i, i, i, i, p, i, p, p, i]
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = d
+        for f in (lib.oracle_lengths, lib.oracle_attend, lib.oracle_merge, lib.oracle_attend_ex):
             f.restype = i
         _lib = lib
     return _lib
@@ -124,6 +128,59 @@ def attend(q, kv, indptr, indices, last, rows, *, hq: int, hkv: int,
     if st != OK:
         raise OracleError(f"oracle_attend: status {st}")
     return out[:n], lse[:n]
+
+
+def e4m3_to_float(byte: int) -> float:
+    """Decode one E4M3 byte (the oracle's own decoder)."""
+    return float(_load().oracle_e4m3_to_double(int(byte)))
+
+
+def _u8(t) -> np.ndarray:
+    """E4M3 cache (torch float8_e4m3fn / uint8 tensor or numpy uint8) -> uint8 numpy."""
+    import torch
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint8
+        return np.ascontiguousarray(t)
+    return t.detach().cpu().contiguous().view(torch.uint8).numpy()
+
+
+def attend_fp8(q, kv8, indptr, indices, last, rows, *, hq: int, hkv: int, k_scale: float,
+               v_scale: float, nthreads: int | None = None):
+    """attend() for an E4M3 cache with K / V scales (bytes [pages, 2, P, Hkv, D])."""
+    lib = _load()
+    qb, kvb = _bits(q), _u8(kv8)
+    B, hq_, D = qb.shape
+    pages, two, P, hkv_, D2 = kvb.shape
+    assert hq_ == hq and hkv_ == hkv and D2 == D and two == 2
+    rows = np.asarray(rows, dtype=np.int32)
+    if rows.ndim == 1:
+        rows = rows.reshape(-1, 2)
+    if rows.shape[1] == 2:
+        rows = np.concatenate([rows, np.zeros((rows.shape[0], 1), np.int32),
+                               -np.ones((rows.shape[0], 1), np.int32)], axis=1)
+    rows = np.ascontiguousarray(rows)
+    n = rows.shape[0]
+    out = np.zeros((max(n, 1), D), dtype=np.float64)
+    lse = np.zeros(max(n, 1), dtype=np.float64)
+    indptr, indices, last = _i32(indptr), _i32(indices), _i32(last)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    st = lib.oracle_attend_ex(_ptr(qb), _ptr(kvb), 1, float(k_scale), float(v_scale), _ptr(indptr),
+                              _ptr(indices), _ptr(last), B, hq, hkv, D, P, pages, _ptr(rows), n,
+                              _ptr(out), _ptr(lse), int(nthreads))
+    if st != OK:
+        raise OracleError(f"oracle_attend_ex: status {st}")
+    return out[:n], lse[:n]
+
+
+def decode_fp8(q, kv8, indptr, indices, last, *, hq: int, hkv: int, k_scale: float,
+               v_scale: float, nthreads=None):
+    """Full decode attention over an E4M3 cache: out [B, Hq, D], lse [B, Hq]."""
+    B = int(np.asarray(last).shape[0])
+    rows = np.array([(i, h) for i in range(B) for h in range(hq)], dtype=np.int32)
+    out, lse = attend_fp8(q, kv8, indptr, indices, last, rows.reshape(-1, 2), hq=hq, hkv=hkv,
+                          k_scale=k_scale, v_scale=v_scale, nthreads=nthreads)
+    return out.reshape(B, hq, -1), lse.reshape(B, hq)
 
 
 def decode(q, kv, indptr, indices, last, *, hq: int, hkv: int, nthreads=None):

@@ -38,7 +38,13 @@
  * say a group of g query heads shares one KV head but not which ones).
  *
  * Inputs are the same bf16 bit patterns the GPU consumes, widened exactly to
- * double.
+ * double.  An FP8 cache (oracle_attend_ex, kv_type 1) holds E4M3 bytes --
+ * 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, subnormals at
+ * exponent 0, the all-ones pattern (S.1111.111) NaN, no infinities -- each
+ * decoded exactly and multiplied by its tensor's scale: the attended key is
+ * k_scale * K and the value v_scale * V ("FlashInfer 完全拆解", performance
+ * section: E4M3 KV cache; applicability table: low-precision KV needs a
+ * scale contract).
  */
 #include <math.h>
 #include <pthread.h>
@@ -56,6 +62,16 @@ static double bf16_to_double(uint16_t b) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* E4M3 byte -> double, from the format definition. */
+double oracle_e4m3_to_double(uint8_t b) {
+    int sign = b >> 7, e = (b >> 3) & 0xF, m = b & 7;
+    double v;
+    if (e == 0xF && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, 1 - 7);        /* subnormal */
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
 }
 
 /* Table check and lengths.  Returns ORACLE_OK or ORACLE_E_TABLE. */
@@ -78,7 +94,9 @@ int oracle_lengths(const int32_t *indptr, const int32_t *indices,
 
 typedef struct {
     const uint16_t *q;     /* [B][Hq][D] bf16 bits */
-    const uint16_t *kv;    /* [pages][2][P][Hkv][D] bf16 bits */
+    const void *kv;        /* [pages][2][P][Hkv][D] bf16 bits or E4M3 bytes */
+    int kv_type;           /* 0 bf16, 1 E4M3 */
+    double k_scale, v_scale;
     const int32_t *indptr, *indices, *last;
     int batch, hq, hkv, d, p, num_pages;
     const int32_t *rows;   /* n_rows x 4: req, head, t0, t1 (t1 < 0: to end) */
@@ -90,11 +108,16 @@ typedef struct {
     pthread_mutex_t mu;
 } job_t;
 
-static const uint16_t *row_ptr(const job_t *j, int page, int kv, int slot,
-                               int kvh) {
+/* Element c of the K (kv = 0) or V (kv = 1) row of a page slot, decoded and
+ * scaled. */
+static double kv_elem(const job_t *j, int page, int kv, int slot, int kvh, int c) {
     size_t off = ((((size_t)page * 2 + kv) * j->p + slot) * j->hkv + kvh) *
-                 (size_t)j->d;
-    return j->kv + off;
+                 (size_t)j->d + (size_t)c;
+    if (j->kv_type == 1) {
+        double s = kv ? j->v_scale : j->k_scale;
+        return s * oracle_e4m3_to_double(((const uint8_t *)j->kv)[off]);
+    }
+    return (kv ? j->v_scale : j->k_scale) * bf16_to_double(((const uint16_t *)j->kv)[off]);
 }
 
 /* One query row over tokens [t0, t1).  Two passes over the keys (max, then
@@ -114,9 +137,9 @@ static int attend_row(const job_t *j, int r, double *scores) {
     double m = -INFINITY;
     for (int t = t0; t < t1; ++t) {
         int page = j->indices[j->indptr[i] + t / j->p];
-        const uint16_t *k = row_ptr(j, page, 0, t % j->p, kvh);
         double s = 0.0;
-        for (int c = 0; c < j->d; ++c) s += bf16_to_double(q[c]) * bf16_to_double(k[c]);
+        for (int c = 0; c < j->d; ++c)
+            s += bf16_to_double(q[c]) * kv_elem(j, page, 0, t % j->p, kvh, c);
         s *= inv_sqrt_d;
         scores[t - t0] = s;
         if (s > m) m = s;
@@ -130,8 +153,7 @@ static int attend_row(const job_t *j, int r, double *scores) {
         double w = exp(scores[t - t0] - m) / z;   /* softmax weight */
         psum += w;
         int page = j->indices[j->indptr[i] + t / j->p];
-        const uint16_t *v = row_ptr(j, page, 1, t % j->p, kvh);
-        for (int c = 0; c < j->d; ++c) o[c] += w * bf16_to_double(v[c]);
+        for (int c = 0; c < j->d; ++c) o[c] += w * kv_elem(j, page, 1, t % j->p, kvh, c);
     }
     /* self-check: the softmax weights of a row sum to one */
     if (fabs(psum - 1.0) > 1e-12 * (double)(t1 - t0)) return ORACLE_E_SELFCHECK;
@@ -173,11 +195,28 @@ static void *worker(void *arg) {
 /* Attention for a list of query rows (req, head, t0, t1).
  * q: [batch][hq][d] bf16 bits; kv: [num_pages][2][p][hkv][d] bf16 bits.
  * out: n_rows x d doubles; lse: n_rows doubles (natural log). */
+int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, double k_scale,
+                     double v_scale, const int32_t *indptr, const int32_t *indices,
+                     const int32_t *last, int batch, int hq, int hkv, int d, int p,
+                     int num_pages, const int32_t *rows, int n_rows, double *out,
+                     double *lse, int nthreads);
+
 int oracle_attend(const uint16_t *q, const uint16_t *kv, const int32_t *indptr,
                   const int32_t *indices, const int32_t *last, int batch,
                   int hq, int hkv, int d, int p, int num_pages,
                   const int32_t *rows, int n_rows, double *out, double *lse,
                   int nthreads) {
+    return oracle_attend_ex(q, kv, 0, 1.0, 1.0, indptr, indices, last, batch, hq, hkv, d, p,
+                            num_pages, rows, n_rows, out, lse, nthreads);
+}
+
+/* As oracle_attend, for a cache of kv_type (0 bf16, 1 E4M3) with scales. */
+int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, double k_scale,
+                     double v_scale, const int32_t *indptr, const int32_t *indices,
+                     const int32_t *last, int batch, int hq, int hkv, int d, int p,
+                     int num_pages, const int32_t *rows, int n_rows, double *out,
+                     double *lse, int nthreads) {
+    if (kv_type != 0 && kv_type != 1) return ORACLE_E_ARG;
     if (hq < 1 || hkv < 1 || hq % hkv != 0 || d < 1 || p < 1) return ORACLE_E_ARG;
     int64_t *lens = (int64_t *)malloc(sizeof(int64_t) * (size_t)(batch > 0 ? batch : 1));
     if (!lens) return ORACLE_E_ARG;
@@ -190,7 +229,8 @@ int oracle_attend(const uint16_t *q, const uint16_t *kv, const int32_t *indptr,
     }
     job_t j;
     memset(&j, 0, sizeof j);
-    j.q = q; j.kv = kv; j.indptr = indptr; j.indices = indices; j.last = last;
+    j.q = q; j.kv = kv; j.kv_type = kv_type; j.k_scale = k_scale; j.v_scale = v_scale;
+    j.indptr = indptr; j.indices = indices; j.last = last;
     j.batch = batch; j.hq = hq; j.hkv = hkv; j.d = d; j.p = p;
     j.num_pages = num_pages; j.rows = rows; j.n_rows = n_rows;
     j.out = out; j.lse = lse; j.next = 0; j.status = ORACLE_OK;

@@ -47,7 +47,7 @@ EXPORTS = (
     "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
     "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
-    "pkd_append_kv", "pkd_plan_shared", "pkd_plan_host_shared",
+    "pkd_append_kv", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
 )
 
 
@@ -104,13 +104,16 @@ def load():
         "pkd_plan": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, ctypes.POINTER(u64)]),
         "pkd_get_plan_info": (ctypes.c_int, [vp, ctypes.POINTER(PlanInfo)]),
         "pkd_run": (ctypes.c_int, [vp, vp, vp, vp, vp, u64, vp]),
+        "pkd_run_scaled": (ctypes.c_int, [vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float,
+                                          u64, vp]),
         "pkd_merge_states": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]),
         "pkd_last_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
         "pkd_read_schedule": (ctypes.c_int, [vp, vp, sz, vp]),
         "pkd_plan_host": (ctypes.c_int, [cfgp, vp, vp, vp, i32, vp, sz,
                                          ctypes.POINTER(PlanInfo)]),
         "pkd_schedule_layout": (ctypes.c_int, [cfgp, vp]),
-        "pkd_graph_capture": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, u32, ctypes.POINTER(vp)]),
+        "pkd_graph_capture": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, u32,
+                                             ctypes.POINTER(vp)]),
         "pkd_graph_launch": (ctypes.c_int, [vp, vp]),
         "pkd_graph_layer_times": (ctypes.c_int, [vp, vp]),
         "pkd_graph_destroy": (None, [vp]),
@@ -160,6 +163,7 @@ def _ptr(a: np.ndarray):
 FLAG_FMA_CONSUMER = 1   # fold the GQA group onto CUDA cores (fp32 FMA)
 FLAG_MMA_CONSUMER = 2   # fold it onto tensor cores (mma.sync, bf16 in / fp32 acc)
 FLAG_SHARED_PREFIX = 4  # shared-prefix context: plans over groups of requests
+FLAG_KV_FP8 = 8         # E4M3 cache with per-call K / V scales
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -265,7 +269,8 @@ class BatchDecodeWithPagedKVCache:
 
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
-                 use_tensor_cores=None, shared_prefix=False, kv_layout="NHD", device=None):
+                 use_tensor_cores=None, shared_prefix=False, kv_dtype="bf16", kv_layout="NHD",
+                 device=None):
         import torch
         if kv_layout != "NHD":
             raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
@@ -277,6 +282,11 @@ class BatchDecodeWithPagedKVCache:
             FLAG_MMA_CONSUMER if use_tensor_cores else FLAG_FMA_CONSUMER)
         if shared_prefix:
             flags |= FLAG_SHARED_PREFIX
+        if kv_dtype not in ("bf16", "e4m3"):
+            raise ValueError("kv_dtype must be 'bf16' or 'e4m3'")
+        self.kv_dtype = kv_dtype
+        if kv_dtype == "e4m3":
+            flags |= FLAG_KV_FP8
         self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch,
                                max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas, flags)
         with torch.cuda.device(self.device):
@@ -351,10 +361,13 @@ class BatchDecodeWithPagedKVCache:
         if self.batch is None:
             raise PkdError(-5, "run before plan")
         B = self.batch
-        for name, t, dt in (("q", q, torch.bfloat16), ("kv_cache", kv_cache, torch.bfloat16),
+        kv_dt = torch.bfloat16 if self.kv_dtype == "bf16" else torch.float8_e4m3fn
+        for name, t, dt in (("q", q, torch.bfloat16), ("kv_cache", kv_cache, kv_dt),
                             ("out", out, torch.bfloat16)):
-            if t.dtype != dt:
-                raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+            if t.dtype != dt and not (name == "kv_cache" and self.kv_dtype == "e4m3"
+                                      and t.dtype == torch.uint8):
+                raise TypeError(f"{name} must be {dt} (planned kv_dtype "
+                                f"{self.kv_dtype!r}), got {t.dtype}")
             if t.device != self.device and not (t.is_cuda and self.device.index is None):
                 raise ValueError(f"{name} is on {t.device}, the plan on {self.device}")
             if not t.is_contiguous():
@@ -371,22 +384,26 @@ class BatchDecodeWithPagedKVCache:
                 raise ValueError("lse must be contiguous float32 [batch, Hq]")
 
     def run(self, q, kv_cache, out=None, lse=None, return_lse=True, expect_epoch=0,
-            stream=None):
-        """Attention for one layer.  Returns (out, lse) or out."""
+            stream=None, k_scale=1.0, v_scale=1.0):
+        """Attention for one layer.  Returns (out, lse) or out.  With scales
+        the attended key is k_scale * K and the value v_scale * V (an E4M3
+        cache needs them)."""
         import torch
         if out is None:
             out = torch.empty_like(q)
         if lse is None and return_lse:
             lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
         self._check_run_args(q, kv_cache, out, lse)
-        st = load().pkd_run(self._h, ctypes.c_void_p(q.data_ptr()),
-                            ctypes.c_void_p(kv_cache.data_ptr()), ctypes.c_void_p(out.data_ptr()),
-                            ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
-                            int(expect_epoch), _stream_ptr(stream))
+        st = load().pkd_run_scaled(self._h, ctypes.c_void_p(q.data_ptr()),
+                                   ctypes.c_void_p(kv_cache.data_ptr()),
+                                   ctypes.c_void_p(out.data_ptr()),
+                                   ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                                   float(k_scale), float(v_scale), int(expect_epoch),
+                                   _stream_ptr(stream))
         _check(st, "pkd_run")
         return (out, lse) if return_lse else out
 
-    def capture(self, qs, kvs, outs, lses=None, timing=False) -> Graph:
+    def capture(self, qs, kvs, outs, lses=None, timing=False, kv_scales=None) -> Graph:
         """Capture len(qs) runs (one decode step over all layers) in a graph."""
         n = len(qs)
         for l in range(n):
@@ -398,8 +415,11 @@ class BatchDecodeWithPagedKVCache:
         l_arr = P(*[t.data_ptr() for t in lses]) if lses else None
         h = ctypes.c_void_p()
         as_vp = lambda a: ctypes.cast(a, ctypes.c_void_p) if a is not None else None
+        sc = None
+        if kv_scales is not None:
+            sc = (ctypes.c_float * (2 * n))(*[float(x) for pair in kv_scales for x in pair])
         st = load().pkd_graph_capture(self._h, n, as_vp(q_arr), as_vp(kv_arr), as_vp(o_arr),
-                                      as_vp(l_arr),
+                                      as_vp(l_arr), as_vp(sc),
                                       GRAPH_TIMING if timing else 0, ctypes.byref(h))
         _check(st, "pkd_graph_capture")
         return Graph(self, h, n, (list(qs), list(kvs), list(outs), list(lses or [])))

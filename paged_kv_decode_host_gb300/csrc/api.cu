@@ -25,6 +25,7 @@ struct pkd_ctx {
   int32_t group = 0;
   bool mma = false;
   bool block = false;  // shared-prefix row-block kernel
+  bool fp8 = false;    // e4m3 cache
   int smem_bytes = 0;
   int merge_grid = 0;
   int device = 0;
@@ -53,10 +54,13 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 // The consumer flags exclude each other; the shared-prefix kernel exists for
 // the tensor-core consumer only.
 bool valid_flags(uint32_t f) {
-  const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX;
+  const uint32_t known =
+      PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8;
   if (f & ~known) return false;
-  if ((f & PKD_FLAG_FMA_CONSUMER) && (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX)))
+  if ((f & PKD_FLAG_FMA_CONSUMER) &&
+      (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8)))
     return false;
+  if ((f & PKD_FLAG_SHARED_PREFIX) && (f & PKD_FLAG_KV_FP8)) return false;
   return true;
 }
 
@@ -79,7 +83,8 @@ int check_config(const pkd_config* c) {
 
 int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
   const int g = c->num_qo_heads / c->num_kv_heads;
-  *smem_bytes = decode_smem_bytes(c->num_kv_heads, g);
+  const bool fp8 = (c->flags & PKD_FLAG_KV_FP8) != 0;
+  *smem_bytes = decode_smem_bytes(c->num_kv_heads, g, fp8);
   if (c->num_ctas > 0) {
     *n_cta = c->num_ctas;
     return PKD_OK;
@@ -90,8 +95,8 @@ int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
     return PKD_E_CUDA;
   const bool mma = use_mma_consumer(g, c->flags);
   const bool block = (c->flags & PKD_FLAG_SHARED_PREFIX) != 0;
-  if (decode_prepare(g, mma, block, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
-  if (decode_occupancy(g, mma, block, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
+  if (decode_prepare(g, mma, block, fp8, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
+  if (decode_occupancy(g, mma, block, fp8, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
     return PKD_E_CUDA;
   if (per_sm < 1) return PKD_E_UNSUPPORTED_SHAPE;
   *n_cta = sms * per_sm;
@@ -101,7 +106,8 @@ int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
-               cudaStream_t stream, cudaEvent_t ev_before, cudaEvent_t ev_after) {
+               float k_scale, float v_scale, cudaStream_t stream, cudaEvent_t ev_before,
+               cudaEvent_t ev_after) {
   const pkd_config& c = ctx->cfg;
   DecodeArgs a{};
   a.sched = reinterpret_cast<const int32_t*>(ctx->ws);
@@ -112,7 +118,7 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.kv = static_cast<const uint8_t*>(kv);
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
-  a.row_bytes = c.num_kv_heads * kHeadDim * 2;
+  a.row_bytes = c.num_kv_heads * kHeadDim * (ctx->fp8 ? 1 : 2);
   a.page_bytes = (int64_t)2 * c.page_size * a.row_bytes;
   a.off_cta = ctx->layout.cta_indptr;
   a.off_items = ctx->layout.items;
@@ -121,10 +127,11 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.hkv = c.num_kv_heads;
   a.page_size = c.page_size;
   a.num_pages = c.num_pages;
-  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim) * (double)k_scale);
+  a.v_scale = v_scale;
   if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
-  if (launch_decode(ctx->group, ctx->mma, ctx->block, a, ctx->n_cta, c.num_kv_heads,
+  if (launch_decode(ctx->group, ctx->mma, ctx->block, ctx->fp8, a, ctx->n_cta, c.num_kv_heads,
                     ctx->smem_bytes, stream) != cudaSuccess)
     return PKD_E_CUDA;
   if (ev_after && cudaEventRecordWithFlags(ev_after, stream, cudaEventRecordExternal) != cudaSuccess)
@@ -228,12 +235,13 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
   ctx->group = cfg->num_qo_heads / cfg->num_kv_heads;
   ctx->mma = use_mma_consumer(ctx->group, cfg->flags);
   ctx->block = (cfg->flags & PKD_FLAG_SHARED_PREFIX) != 0;
+  ctx->fp8 = (cfg->flags & PKD_FLAG_KV_FP8) != 0;
   st = resolve_ctas(cfg, &ctx->n_cta, &ctx->smem_bytes);
   if (st != PKD_OK) {
     delete ctx;
     return st;
   }
-  if (decode_prepare(ctx->group, ctx->mma, ctx->block, ctx->smem_bytes) != cudaSuccess) {
+  if (decode_prepare(ctx->group, ctx->mma, ctx->block, ctx->fp8, ctx->smem_bytes) != cudaSuccess) {
     delete ctx;
     return PKD_E_CUDA;
   }
@@ -332,6 +340,12 @@ int pkd_get_plan_info(const pkd_ctx* ctx, pkd_plan_info* info) {
 
 int pkd_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
             uint64_t expect_epoch, void* stream) {
+  return pkd_run_scaled(ctx, q, kv, out, lse, 1.f, 1.f, expect_epoch, stream);
+}
+
+int pkd_run_scaled(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
+                   float k_scale, float v_scale, uint64_t expect_epoch, void* stream) {
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return PKD_E_INVALID_ARG;
   if (ctx == nullptr) return PKD_E_INVALID_ARG;
   if (ctx->epoch == 0) return PKD_E_NO_PLAN;
   if (expect_epoch != 0 && expect_epoch != ctx->epoch) return PKD_E_STALE_PLAN;
@@ -340,7 +354,8 @@ int pkd_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
     if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(lse, 4))
       return PKD_E_INVALID_ARG;
   }
-  return launch_run(ctx, q, kv, out, lse, static_cast<cudaStream_t>(stream), nullptr, nullptr);
+  return launch_run(ctx, q, kv, out, lse, k_scale, v_scale, static_cast<cudaStream_t>(stream),
+                    nullptr, nullptr);
 }
 
 int pkd_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b,
@@ -408,7 +423,8 @@ int pkd_read_schedule(pkd_ctx* ctx, int32_t* host_words, size_t max_words, void*
 }
 
 int pkd_graph_capture(pkd_ctx* ctx, int32_t layers, const void* const* q, const void* const* kv,
-                      void* const* out, float* const* lse, uint32_t flags, pkd_graph** graph) {
+                      void* const* out, float* const* lse, const float* kv_scales,
+                      uint32_t flags, pkd_graph** graph) {
   if (ctx == nullptr || graph == nullptr || layers < 1 || q == nullptr || kv == nullptr ||
       out == nullptr)
     return PKD_E_INVALID_ARG;
@@ -445,7 +461,9 @@ int pkd_graph_capture(pkd_ctx* ctx, int32_t layers, const void* const* q, const 
     st = PKD_E_CUDA;
   } else {
     for (int l = 0; l < layers && st == PKD_OK; ++l) {
-      st = launch_run(ctx, q[l], kv[l], out[l], lse ? lse[l] : nullptr, cs,
+      const float ks = kv_scales ? kv_scales[2 * l] : 1.f;
+      const float vs = kv_scales ? kv_scales[2 * l + 1] : 1.f;
+      st = launch_run(ctx, q[l], kv[l], out[l], lse ? lse[l] : nullptr, ks, vs, cs,
                       timing ? g->ev[2 * l] : nullptr, timing ? g->ev[2 * l + 1] : nullptr);
     }
     if (cudaStreamEndCapture(cs, &graph_def) != cudaSuccess && st == PKD_OK) st = PKD_E_CUDA;

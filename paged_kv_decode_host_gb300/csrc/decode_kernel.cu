@@ -32,6 +32,7 @@
 //    the device error word, stops issuing copies, waits (bounded) for the
 //    copies already in flight, and returns.
 #include <cuda_runtime.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 #include <stdint.h>
 
@@ -434,7 +435,7 @@ __device__ void run_consumer_fma(const DecodeArgs& a, int it0, int it1, const ui
       if (G > 1 ? ((i & 1) != hw) : (hw != 0)) continue;
       const float m = sbuf[8 + i];
       const float lsum = sbuf[16 + i];
-      const float inv = 1.f / lsum;
+      const float inv = a.v_scale / lsum;
       const float lse_nat = (m + log2f(lsum)) * 0.69314718055994530942f;
       const int64_t qrow = (int64_t)req * a.hq + (int64_t)hk * G + i;
       if (dst < 0) {
@@ -635,7 +636,7 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
     l += __shfl_xor_sync(kFull, l, 1);
     l += __shfl_xor_sync(kFull, l, 2);
     if (row_ok) {
-      const float inv = 1.f / l;
+      const float inv = a.v_scale / l;
       const float lse_nat = (m_run + log2f(l)) * 0.69314718055994530942f;
       const int64_t qrow = (int64_t)req * a.hq + (int64_t)hk * G + grp;
       if (dst < 0) {
@@ -822,7 +823,7 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
       const int head = hk * G + (rr ? hd1 : hd0);
       const float l = rr ? l1 : l0;
       const float m = rr ? m1 : m0;
-      const float inv = 1.f / l;
+      const float inv = a.v_scale / l;
       const float lse_nat = (m + log2f(l)) * 0.69314718055994530942f;
       if (dst < 0) {
         const int64_t qrow = (int64_t)(req + rq) * a.hq + head;
@@ -843,12 +844,199 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
   }
 }
 
-template <int G, bool kMma, bool kBlock>
+
+// ------------------------------------------------------ FP8-E4M3 KV consumer
+// The cache holds e4m3 (one byte per element, half the bytes per token);
+// k_scale and v_scale are folded into the score scale and the output.  Each
+// stage, the warp converts its KV head's K and V slices to f16 -- exact, every
+// e4m3 value is an f16 -- into a per-warp shared buffer at a padded row
+// stride, releases the stage, and runs the same fragment code as the bf16
+// consumer with f16 operands.  q is scaled per row into [-1, 1] (no f16
+// overflow whatever the bf16 range) and the factor folded into the score
+// scale; P is f16.
+constexpr int kF16Row = kHeadDim * 2 + 16;        // scratch row stride (bytes)
+constexpr int kFp8ScratchBytes = 2 * kTS * kF16Row;  // per warp: K and V of one stage
+
+__device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
+                                        uint32_t b1) {
+  float z0, z1;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%12};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
+  (void)z0;
+  (void)z1;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 4 e4m3 (one word, ascending address) -> 4 f16 (two words).
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  return make_uint2((uint32_t)lo.x | ((uint32_t)lo.y << 16), (uint32_t)hi.x | ((uint32_t)hi.y << 16));
+}
+
+template <int G>
+__device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
+                                     int stage_bytes, uint64_t* full, uint64_t* empty,
+                                     volatile int* abort_flag, uint8_t* scratch, int warp,
+                                     int lane) {
+  const int hk = warp;
+  const int grp = lane >> 2;
+  const int tig = lane & 3;
+  const bool row_ok = grp < G;
+  const int rs = row_stride(a.row_bytes);
+  const uint32_t s0 = smem_u32(scratch);
+  const uint32_t k_lane = (uint32_t)((lane & 7) * kF16Row + (lane >> 3) * 16);
+  const uint32_t v_lane =
+      (uint32_t)(kTS * kF16Row + (((lane >> 3) & 1) * 8 + (lane & 7)) * kF16Row + (lane >> 4) * 16);
+  // conversion: lane converts token ct = lane / 2, bytes [64 ch, 64 ch + 64) of the head's row
+  const int ct = lane >> 1, ch = lane & 1;
+  pdl_wait();
+  uint32_t stage = 0;
+  for (int it = it0; it < it1; ++it) {
+    const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
+    const int req = item[0], tb = item[1], te = item[2], dst = item[3];
+    uint32_t qa0[8], qa2[8];
+    float s_scale;
+    {
+      uint32_t raw0[8], raw2[8];
+      load_q_frags<G>(a, req, hk, grp, tig, row_ok, raw0, raw2);
+      float amax = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw0[ks] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw0[ks] & 0xffff0000u)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw2[ks] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw2[ks] & 0xffff0000u)));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      const float inv = amax > 0.f ? 1.f / amax : 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qa0[ks] = pack_f16x2(__uint_as_float(raw0[ks] << 16) * inv,
+                             __uint_as_float(raw0[ks] & 0xffff0000u) * inv);
+        qa2[ks] = pack_f16x2(__uint_as_float(raw2[ks] << 16) * inv,
+                             __uint_as_float(raw2[ks] & 0xffff0000u) * inv);
+      }
+      s_scale = a.scale_log2 * amax;
+    }
+    float o[16][2];
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = 0.f;
+    float m_run = -CUDART_INF_F;
+    float l_run = 0.f;
+
+    for (int t = tb; t < te; t += kTS) {
+      const int n = min(kTS, te - t);
+      const int slot = (int)(stage % kStages);
+      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      if (!__all_sync(kFull, got)) {
+        if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+        return;
+      }
+      // ---- e4m3 -> f16 into the warp's scratch (K, then V); V rows past
+      // the item's end are zeroed (stale bytes could decode to NaN)
+      {
+        const uint8_t* src = stages + (size_t)slot * stage_bytes + (size_t)ct * rs +
+                             hk * kHeadDim + ch * 64;
+        uint8_t* kd = scratch + ct * kF16Row + ch * 128;
+        uint8_t* vd = kd + kTS * kF16Row;
+        __syncwarp();   // the previous stage's fragment loads are done
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src + c * 16);
+          const uint2 h0 = e4m3x4_to_f16x4(w.x), h1 = e4m3x4_to_f16x4(w.y);
+          const uint2 h2 = e4m3x4_to_f16x4(w.z), h3 = e4m3x4_to_f16x4(w.w);
+          *reinterpret_cast<uint4*>(kd + c * 32) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+          *reinterpret_cast<uint4*>(kd + c * 32 + 16) = make_uint4(h2.x, h2.y, h3.x, h3.y);
+        }
+        const uint8_t* vsrc = src + (size_t)kTS * rs;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 w = *reinterpret_cast<const uint4*>(vsrc + c * 16);
+          if (ct >= n) w = make_uint4(0, 0, 0, 0);
+          const uint2 h0 = e4m3x4_to_f16x4(w.x), h1 = e4m3x4_to_f16x4(w.y);
+          const uint2 h2 = e4m3x4_to_f16x4(w.z), h3 = e4m3x4_to_f16x4(w.w);
+          *reinterpret_cast<uint4*>(vd + c * 32) = make_uint4(h0.x, h0.y, h1.x, h1.y);
+          *reinterpret_cast<uint4*>(vd + c * 32 + 16) = make_uint4(h2.x, h2.y, h3.x, h3.y);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);   // the stage is free again
+      }
+      float sc[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(s0 + k_lane + (uint32_t)(nt * 8 * kF16Row + kp * 64), b0, b1, b2, b3);
+          mma_f16(sc[nt], qa0[2 * kp], qa2[2 * kp], b0, b1);
+          mma_f16(sc[nt], qa0[2 * kp + 1], qa2[2 * kp + 1], b2, b3);
+        }
+      }
+      float s4[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tok = nt * 8 + 2 * tig + c;
+          s4[nt * 2 + c] = (tok < n) ? sc[nt][c] * s_scale : -CUDART_INF_F;
+        }
+      const float alpha = softmax_row(s4, m_run, l_run);
+      const uint32_t pa0 = pack_f16x2(s4[0], s4[1]);
+      const uint32_t pa2 = pack_f16x2(s4[2], s4[3]);
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(s0 + v_lane + (uint32_t)(dp * 32), b0, b1, b2, b3);
+        o[2 * dp][0] *= alpha;
+        o[2 * dp][1] *= alpha;
+        o[2 * dp + 1][0] *= alpha;
+        o[2 * dp + 1][1] *= alpha;
+        mma_f16(o[2 * dp], pa0, pa2, b0, b1);
+        mma_f16(o[2 * dp + 1], pa0, pa2, b2, b3);
+      }
+      ++stage;
+    }
+
+    float l = l_run;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (row_ok) {
+      const float inv = a.v_scale / l;
+      const float lse_nat = (m_run + log2f(l)) * 0.69314718055994530942f;
+      const int64_t qrow = (int64_t)req * a.hq + (int64_t)hk * G + grp;
+      if (dst < 0) {
+        uint32_t* op = reinterpret_cast<uint32_t*>(a.out + qrow * kHeadDim) + tig;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) op[dt * 4] = pack_bf16x2(o[dt][0] * inv, o[dt][1] * inv);
+        if (a.lse != nullptr && tig == 0) a.lse[qrow] = lse_nat;
+      } else {
+        const int64_t prow = (int64_t)dst * a.hq + (int64_t)hk * G + grp;
+        float2* op = reinterpret_cast<float2*>(a.o_part + prow * kHeadDim) + tig;
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) op[dt * 4] = make_float2(o[dt][0] * inv, o[dt][1] * inv);
+        if (tig == 0) a.l_part[prow] = lse_nat;
+      }
+    }
+  }
+}
+
+template <int G, bool kMma, bool kBlock, bool kFp8>
 __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int stage_bytes = 2 * kTS * row_stride(a.row_bytes);
   uint8_t* stages = smem;
-  float* pbuf_all = reinterpret_cast<float*>(smem + (size_t)kStages * stage_bytes);
+  uint8_t* scratch = smem + (size_t)kStages * stage_bytes;   // fp8 only
+  float* pbuf_all = reinterpret_cast<float*>(scratch + (kFp8 ? kMaxKvHeads * kFp8ScratchBytes : 0));
   float* sbuf_all = pbuf_all + kMaxKvHeads * kTS * G;
   uint64_t* full = reinterpret_cast<uint64_t*>(sbuf_all + kMaxKvHeads * 32);
   uint64_t* empty = full + kStages;
@@ -883,7 +1071,10 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
   if (warp == n_cons) {
     run_producer(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
   } else if (warp < n_cons) {
-    if constexpr (kBlock) {
+    if constexpr (kFp8) {
+      run_consumer_mma_fp8<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+                              scratch + warp * kFp8ScratchBytes, warp, lane);
+    } else if constexpr (kBlock) {
       run_consumer_mma_block<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
                                 lane);
     } else if constexpr (kMma) {
@@ -896,19 +1087,21 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
 }
 
 template <int G>
-const void* kernel_ptr(bool mma, bool block) {
-  if (block) return reinterpret_cast<const void*>(&decode_kernel<G, true, true>);
-  return mma ? reinterpret_cast<const void*>(&decode_kernel<G, true, false>)
-             : reinterpret_cast<const void*>(&decode_kernel<G, false, false>);
+const void* kernel_ptr(bool mma, bool block, bool fp8) {
+  if (fp8) return reinterpret_cast<const void*>(&decode_kernel<G, true, false, true>);
+  if (block) return reinterpret_cast<const void*>(&decode_kernel<G, true, true, false>);
+  return mma ? reinterpret_cast<const void*>(&decode_kernel<G, true, false, false>)
+             : reinterpret_cast<const void*>(&decode_kernel<G, false, false, false>);
 }
 
-const void* kernel_for(int group, bool mma, bool block) {
-  if (block && !mma) return nullptr;
+const void* kernel_for(int group, bool mma, bool block, bool fp8) {
+  if ((block || fp8) && !mma) return nullptr;
+  if (block && fp8) return nullptr;
   switch (group) {
-    case 1: return kernel_ptr<1>(mma, block);
-    case 2: return kernel_ptr<2>(mma, block);
-    case 4: return kernel_ptr<4>(mma, block);
-    case 8: return kernel_ptr<8>(mma, block);
+    case 1: return kernel_ptr<1>(mma, block, fp8);
+    case 2: return kernel_ptr<2>(mma, block, fp8);
+    case 4: return kernel_ptr<4>(mma, block, fp8);
+    case 8: return kernel_ptr<8>(mma, block, fp8);
     default: return nullptr;
   }
 }
@@ -924,33 +1117,33 @@ bool use_mma_consumer(int group, uint32_t flags) {
   return true;   // measured faster than the CUDA-core consumer at every group size
 }
 
-int decode_smem_bytes(int hkv, int group) {
-  const int rs = row_stride(hkv * kHeadDim * 2);
-  return kStages * 2 * kTS * rs + kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 +
-         2 * kStages * 8 + 16;
+int decode_smem_bytes(int hkv, int group, bool fp8) {
+  const int rs = row_stride(hkv * kHeadDim * (fp8 ? 1 : 2));
+  return kStages * 2 * kTS * rs + (fp8 ? kMaxKvHeads * kFp8ScratchBytes : 0) +
+         kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 + 2 * kStages * 8 + 16;
 }
 
-cudaError_t decode_prepare(int group, bool mma, bool block, int smem_bytes) {
-  const void* k = kernel_for(group, mma, block);
+cudaError_t decode_prepare(int group, bool mma, bool block, bool fp8, int smem_bytes) {
+  const void* k = kernel_for(group, mma, block, fp8);
   if (!k) return cudaErrorInvalidValue;
   // The attribute is per kernel, shared by every context: always allow the
   // largest layout (8 KV heads) so a smaller context never lowers it.
-  const int most = decode_smem_bytes(kMaxKvHeads, group);
+  const int most = decode_smem_bytes(kMaxKvHeads, group, fp8);
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_bytes > most ? smem_bytes : most);
 }
 
-cudaError_t decode_occupancy(int group, bool mma, bool block, int hkv, int smem_bytes,
+cudaError_t decode_occupancy(int group, bool mma, bool block, bool fp8, int hkv, int smem_bytes,
                              int* blocks_per_sm) {
-  const void* k = kernel_for(group, mma, block);
+  const void* k = kernel_for(group, mma, block, fp8);
   if (!k) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, decode_threads(hkv),
                                                        (size_t)smem_bytes);
 }
 
-cudaError_t launch_decode(int group, bool mma, bool block, const DecodeArgs& a, int grid,
-                          int hkv, int smem_bytes, cudaStream_t stream) {
-  const void* k = kernel_for(group, mma, block);
+cudaError_t launch_decode(int group, bool mma, bool block, bool fp8, const DecodeArgs& a,
+                          int grid, int hkv, int smem_bytes, cudaStream_t stream) {
+  const void* k = kernel_for(group, mma, block, fp8);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

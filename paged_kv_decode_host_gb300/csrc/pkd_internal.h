@@ -89,14 +89,15 @@ struct DecodeArgs {
   float* l_part;             // partial LSE, fp32 [slot][Hq] (natural log)
   int32_t* err;              // device error word
   const uint16_t* q;         // bf16 [B][Hq][D]
-  const uint8_t* kv;         // bf16 NHD cache, bytes
+  const uint8_t* kv;         // NHD cache (bf16 or e4m3), bytes
   uint16_t* out;             // bf16 [B][Hq][D]
   float* lse;                // fp32 [B][Hq] or null
   int64_t page_bytes;        // 2 * P * row_bytes
   int64_t off_cta, off_items, off_pages;
   int32_t hq, hkv, page_size, num_pages;
-  int32_t row_bytes;         // Hkv * D * 2: one token of one page, all heads
-  float scale_log2;          // log2(e) / sqrt(D)
+  int32_t row_bytes;         // Hkv * D * element bytes: one token of one page, all heads
+  float scale_log2;          // k_scale * log2(e) / sqrt(D)
+  float v_scale;             // multiplies the output (1 for an unscaled cache)
 };
 
 struct MergeArgs {
@@ -110,14 +111,15 @@ struct MergeArgs {
 };
 
 // Kernel launchers (decode_kernel.cu / merge_kernels.cu).
-int decode_smem_bytes(int hkv, int group);
+int decode_smem_bytes(int hkv, int group, bool fp8);
 int decode_threads(int hkv);
 // block: the shared-prefix variant (work items over row blocks of requests)
-cudaError_t decode_prepare(int group, bool mma, bool block, int smem_bytes);
-cudaError_t decode_occupancy(int group, bool mma, bool block, int hkv, int smem_bytes,
+// fp8: the cache holds e4m3 (tensor-core consumer only)
+cudaError_t decode_prepare(int group, bool mma, bool block, bool fp8, int smem_bytes);
+cudaError_t decode_occupancy(int group, bool mma, bool block, bool fp8, int hkv, int smem_bytes,
                              int* blocks_per_sm);
-cudaError_t launch_decode(int group, bool mma, bool block, const DecodeArgs& a, int grid,
-                          int hkv, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_decode(int group, bool mma, bool block, bool fp8, const DecodeArgs& a,
+                          int grid, int hkv, int smem_bytes, cudaStream_t stream);
 // Consumer variant for a group size: tensor cores (mma.sync) or CUDA cores.
 bool use_mma_consumer(int group, uint32_t flags);
 // Merge grid for a persistent decode grid of n_cta CTAs.

@@ -39,6 +39,7 @@ __all__ = [
     "make_tables",
     "make_q",
     "make_kv",
+    "make_kv_fp8",
     "workload",
 ]
 
@@ -58,6 +59,11 @@ class Workload:
     pool_pages: int  # pages in the pool (>= pages referenced)
     prefix_tokens: int = 0  # shared-prefix workload only
     suffix_lens: tuple = field(default_factory=tuple)
+    kv_dtype: str = "bf16"  # "bf16" or "e4m3" (FP8 cache with K / V scales)
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == "e4m3" else 2
 
     @property
     def batch(self) -> int:
@@ -84,6 +90,10 @@ def workload(name: str) -> Workload:
         g = torch.Generator().manual_seed(2)
         lens = tuple(_randint(g, 1, 8192, 64))
         return Workload(name, 2, 32, 8, 128, 16, 32, lens, _pages_for(lens, 16))
+    if name == "llama8b_step_fp8":
+        w = workload("llama8b_step")
+        return Workload(name, w.seed, w.hq, w.hkv, w.head_dim, w.page_size, w.layers, w.lens,
+                        w.pool_pages, kv_dtype="e4m3")
     if name == "skewed":
         g = torch.Generator().manual_seed(3)
         lens = tuple(_randint(g, 128, 512, 63) + [100_000])
@@ -104,6 +114,8 @@ def workload(name: str) -> Workload:
 
 
 WORKLOADS = ("worked_example", "llama8b_step", "skewed", "shared_prefix", "token_sparse")
+# the same Llama-shaped step over an E4M3 cache
+EXTRA_WORKLOADS = ("llama8b_step_fp8",)
 
 
 def page_table(kv_lens, page_size, page_ids=None):
@@ -199,6 +211,21 @@ def make_kv(w: Workload, device="cpu", layers=None, seed_offset=0):
     shape = (w.pool_pages, 2, w.page_size, w.hkv, w.head_dim)
     return [torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device)
             for _ in range(layers)]
+
+
+def make_kv_fp8(w: Workload, device="cpu", layers=None, seed_offset=0, amax=4.0):
+    """E4M3 paged caches (torch.float8_e4m3fn, NHD) holding N(0, 1) / scale
+    values, scale = amax / 448 so that amax maps to the largest E4M3 value;
+    returns (caches, scale) -- the attended K and V are scale * cache."""
+    layers = w.layers if layers is None else layers
+    scale = amax / 448.0
+    g = _generator(10_000 * w.seed + 31 + seed_offset, device)
+    shape = (w.pool_pages, 2, w.page_size, w.hkv, w.head_dim)
+    caches = []
+    for _ in range(layers):
+        x = torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device)
+        caches.append((x.float() / scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn))
+    return caches, scale
 
 
 def random_small(seed: int, batch: int, max_len: int, page_size: int,

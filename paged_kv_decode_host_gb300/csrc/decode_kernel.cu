@@ -169,6 +169,7 @@ __device__ __forceinline__ void rs_level(const float (&v)[N], float (&o)[N / 2],
 }
 
 // ---------------------------------------------------------------- producer
+template <int kTokens>
 __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* stages,
                              int stage_bytes, uint64_t* full, uint64_t* empty,
                              volatile int* abort_flag, int lane) {
@@ -182,8 +183,8 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
   for (int it = it0; it < it1 && ok; ++it) {
     const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
     const int tb = item[1], te = item[2], poff = item[4];
-    for (int t = tb; t < te; t += kTS) {
-      const int n = min(kTS, te - t);
+    for (int t = tb; t < te; t += kTokens) {
+      const int n = min(kTokens, te - t);
       const int slot = (int)(stage % kStages);
       const uint32_t round = stage / kStages;
       // Page id of this lane's token: one K row and one V row per token (all
@@ -211,7 +212,7 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
         const int pslot = (t + j) % P;
         const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)pslot * row;
         uint8_t* dk = stages + (size_t)slot * stage_bytes + (size_t)j * rs;
-        uint8_t* dv = dk + (size_t)kTS * rs;
+        uint8_t* dv = dk + (size_t)kTokens * rs;
         if (!waited) {
           pdl_wait();
           waited = true;
@@ -846,16 +847,22 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
 
 
 // ------------------------------------------------------ FP8-E4M3 KV consumer
-// The cache holds e4m3 (one byte per element, half the bytes per token);
-// k_scale and v_scale are folded into the score scale and the output.  Each
-// stage, the warp converts its KV head's K and V slices to f16 -- exact, every
-// e4m3 value is an f16 -- into a per-warp shared buffer at a padded row
-// stride, releases the stage, and runs the same fragment code as the bf16
-// consumer with f16 operands.  q is scaled per row into [-1, 1] (no f16
-// overflow whatever the bf16 range) and the factor folded into the score
-// scale; P is f16.
-constexpr int kF16Row = kHeadDim * 2 + 16;        // scratch row stride (bytes)
-constexpr int kFp8ScratchBytes = 2 * kTS * kF16Row;  // per warp: K and V of one stage
+// The cache holds e4m3 (one byte per element: half the bytes per token);
+// k_scale and v_scale are folded into the score scale and the output.  The
+// e4m3 bytes go straight from the shared-memory stage into f16 MMA
+// fragments -- every e4m3 value is an f16, cvt.f16x2.e4m3x2 is exact:
+//  * K: ldmatrix on the byte rows gives each lane 4 consecutive dims of one
+//    token; in the MMA's K (dims) order, k = 2t, 2t+1, 2t+8, 2t+9 stand for
+//    dims 4t .. 4t+3 of each 16-dim block, and q's A fragments are loaded in
+//    the same order, so the dot products are unchanged;
+//  * V: ldmatrix.trans on the byte rows gives each lane 2 tokens x 2 adjacent
+//    dims; one byte permute and two converts make the B fragments of two
+//    N tiles (even and odd dims of the block), so the lane ends with 4
+//    consecutive output dims per block.
+// q is scaled per row into [-1, 1] (no f16 overflow whatever the bf16 range)
+// and the factor folded into the score scale; P is f16.  A stage holds 32
+// tokens (the same bytes as 16 bf16 tokens), processed as two 16-token tiles.
+constexpr int kFp8Tokens = 32;
 
 __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
                                         uint32_t b1) {
@@ -874,136 +881,142 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// 4 e4m3 (one word, ascending address) -> 4 f16 (two words).
-__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
-  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
-  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-  return make_uint2((uint32_t)lo.x | ((uint32_t)lo.y << 16), (uint32_t)hi.x | ((uint32_t)hi.y << 16));
+// two e4m3 (low byte first) -> f16x2
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_bytes, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 template <int G>
 __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                                      int stage_bytes, uint64_t* full, uint64_t* empty,
-                                     volatile int* abort_flag, uint8_t* scratch, int warp,
-                                     int lane) {
+                                     volatile int* abort_flag, int warp, int lane) {
+  constexpr int T = kFp8Tokens;
   const int hk = warp;
   const int grp = lane >> 2;
   const int tig = lane & 3;
   const bool row_ok = grp < G;
   const int rs = row_stride(a.row_bytes);
-  const uint32_t s0 = smem_u32(scratch);
-  const uint32_t k_lane = (uint32_t)((lane & 7) * kF16Row + (lane >> 3) * 16);
-  const uint32_t v_lane =
-      (uint32_t)(kTS * kF16Row + (((lane >> 3) & 1) * 8 + (lane & 7)) * kF16Row + (lane >> 4) * 16);
-  // conversion: lane converts token ct = lane / 2, bytes [64 ch, 64 ch + 64) of the head's row
-  const int ct = lane >> 1, ch = lane & 1;
+  const uint32_t stage0 = smem_u32(stages);
+  // ldmatrix row addresses: K: token L % 8 (+ 8 per N tile, + 16 per tile),
+  // dim block L / 8 (+ 4 per x4); V (trans): token (L / 8 & 1) * 8 + L % 8,
+  // dim block L / 16 (+ 2 per x4)
+  const uint32_t k_lane = (uint32_t)((lane & 7) * rs + hk * kHeadDim + (lane >> 3) * 16);
+  const uint32_t v_lane = (uint32_t)(T * rs + (((lane >> 3) & 1) * 8 + (lane & 7)) * rs +
+                                     hk * kHeadDim + (lane >> 4) * 16);
   pdl_wait();
   uint32_t stage = 0;
   for (int it = it0; it < it1; ++it) {
     const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
     const int req = item[0], tb = item[1], te = item[2], dst = item[3];
+    // q in the permuted K order: a0 = dims 16 kb + 4 tig, +1; a2 = +2, +3
     uint32_t qa0[8], qa2[8];
     float s_scale;
     {
-      uint32_t raw0[8], raw2[8];
-      load_q_frags<G>(a, req, hk, grp, tig, row_ok, raw0, raw2);
+      const uint2* qp = reinterpret_cast<const uint2*>(
+          a.q + ((int64_t)req * a.hq + (int64_t)hk * G + (row_ok ? grp : 0)) * kHeadDim);
+      uint2 raw[8];
       float amax = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        amax = fmaxf(amax, fabsf(__uint_as_float(raw0[ks] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(raw0[ks] & 0xffff0000u)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(raw2[ks] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(raw2[ks] & 0xffff0000u)));
+      for (int kb = 0; kb < 8; ++kb) {
+        raw[kb] = row_ok ? __ldg(qp + kb * 4 + tig) : make_uint2(0u, 0u);
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw[kb].x << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw[kb].x & 0xffff0000u)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw[kb].y << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(raw[kb].y & 0xffff0000u)));
       }
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
       const float inv = amax > 0.f ? 1.f / amax : 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qa0[ks] = pack_f16x2(__uint_as_float(raw0[ks] << 16) * inv,
-                             __uint_as_float(raw0[ks] & 0xffff0000u) * inv);
-        qa2[ks] = pack_f16x2(__uint_as_float(raw2[ks] << 16) * inv,
-                             __uint_as_float(raw2[ks] & 0xffff0000u) * inv);
+      for (int kb = 0; kb < 8; ++kb) {
+        qa0[kb] = pack_f16x2(__uint_as_float(raw[kb].x << 16) * inv,
+                             __uint_as_float(raw[kb].x & 0xffff0000u) * inv);
+        qa2[kb] = pack_f16x2(__uint_as_float(raw[kb].y << 16) * inv,
+                             __uint_as_float(raw[kb].y & 0xffff0000u) * inv);
       }
       s_scale = a.scale_log2 * amax;
     }
-    float o[16][2];
+    // accumulators per 16-dim block vb: [vb][0] even-dim tile, [vb][1] odd
+    float oe[8][2], oo[8][2];
 #pragma unroll
-    for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = 0.f;
+    for (int vb = 0; vb < 8; ++vb) oe[vb][0] = oe[vb][1] = oo[vb][0] = oo[vb][1] = 0.f;
     float m_run = -CUDART_INF_F;
     float l_run = 0.f;
 
-    for (int t = tb; t < te; t += kTS) {
-      const int n = min(kTS, te - t);
+    for (int t = tb; t < te; t += T) {
+      const int n = min(T, te - t);
       const int slot = (int)(stage % kStages);
       const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
         return;
       }
-      // ---- e4m3 -> f16 into the warp's scratch (K, then V); V rows past
-      // the item's end are zeroed (stale bytes could decode to NaN)
-      {
-        const uint8_t* src = stages + (size_t)slot * stage_bytes + (size_t)ct * rs +
-                             hk * kHeadDim + ch * 64;
-        uint8_t* kd = scratch + ct * kF16Row + ch * 128;
-        uint8_t* vd = kd + kTS * kF16Row;
-        __syncwarp();   // the previous stage's fragment loads are done
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src + c * 16);
-          const uint2 h0 = e4m3x4_to_f16x4(w.x), h1 = e4m3x4_to_f16x4(w.y);
-          const uint2 h2 = e4m3x4_to_f16x4(w.z), h3 = e4m3x4_to_f16x4(w.w);
-          *reinterpret_cast<uint4*>(kd + c * 32) = make_uint4(h0.x, h0.y, h1.x, h1.y);
-          *reinterpret_cast<uint4*>(kd + c * 32 + 16) = make_uint4(h2.x, h2.y, h3.x, h3.y);
-        }
-        const uint8_t* vsrc = src + (size_t)kTS * rs;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 w = *reinterpret_cast<const uint4*>(vsrc + c * 16);
-          if (ct >= n) w = make_uint4(0, 0, 0, 0);
-          const uint2 h0 = e4m3x4_to_f16x4(w.x), h1 = e4m3x4_to_f16x4(w.y);
-          const uint2 h2 = e4m3x4_to_f16x4(w.z), h3 = e4m3x4_to_f16x4(w.w);
-          *reinterpret_cast<uint4*>(vd + c * 32) = make_uint4(h0.x, h0.y, h1.x, h1.y);
-          *reinterpret_cast<uint4*>(vd + c * 32 + 16) = make_uint4(h2.x, h2.y, h3.x, h3.y);
-        }
+      const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
+      if (n < T) {
+        // V rows past the item's end hold stale bytes (0x7f/0xff are NaN):
+        // zero this head's slice there
+        uint8_t* vrow = const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes +
+                        (size_t)T * rs + hk * kHeadDim + (lane & 7) * 16;
+        for (int r = n + (lane >> 3); r < T; r += 4)
+          *reinterpret_cast<uint4*>(vrow + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);   // the stage is free again
       }
-      float sc[2][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sc[nt][0] = sc[nt][1] = 0.f;
+      for (int st = 0; st < T / 16; ++st) {
+        if (st * 16 >= n) break;
+        const uint32_t tbase = sbase + (uint32_t)(st * 16 * rs);
+        // ---- S = Q K^T, two 8-token tiles
+        float sc[2][2];
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(s0 + k_lane + (uint32_t)(nt * 8 * kF16Row + kp * 64), b0, b1, b2, b3);
-          mma_f16(sc[nt], qa0[2 * kp], qa2[2 * kp], b0, b1);
-          mma_f16(sc[nt], qa0[2 * kp + 1], qa2[2 * kp + 1], b2, b3);
+        for (int nt = 0; nt < 2; ++nt) {
+          sc[nt][0] = sc[nt][1] = 0.f;
+#pragma unroll
+          for (int kq = 0; kq < 2; ++kq) {
+            uint32_t r[4];
+            ldsm_x4(tbase + k_lane + (uint32_t)(nt * 8 * rs + kq * 64), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int kb = kq * 4 + j;
+              mma_f16(sc[nt], qa0[kb], qa2[kb], e4m3x2_to_f16x2(r[j] & 0xffffu),
+                      e4m3x2_to_f16x2(r[j] >> 16));
+            }
+          }
+        }
+        float s4[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int tok = st * 16 + nt * 8 + 2 * tig + c;
+            s4[nt * 2 + c] = (tok < n) ? sc[nt][c] * s_scale : -CUDART_INF_F;
+          }
+        const float alpha = softmax_row(s4, m_run, l_run);
+        const uint32_t pa0 = pack_f16x2(s4[0], s4[1]);
+        const uint32_t pa2 = pack_f16x2(s4[2], s4[3]);
+        // ---- O = alpha O + P V: per x4.trans, dim blocks 2 vp and 2 vp + 1
+#pragma unroll
+        for (int vp = 0; vp < 4; ++vp) {
+          uint32_t r[4];
+          ldsm_x4_t(tbase + v_lane + (uint32_t)(vp * 32), r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int vb = 2 * vp + h;
+            // r[2h]: tokens 2 tig, 2 tig + 1; r[2h + 1]: tokens 8 + 2 tig, 9 + 2 tig
+            const uint32_t x0 = __byte_perm(r[2 * h], 0u, 0x3120);
+            const uint32_t x1 = __byte_perm(r[2 * h + 1], 0u, 0x3120);
+            oe[vb][0] *= alpha;
+            oe[vb][1] *= alpha;
+            oo[vb][0] *= alpha;
+            oo[vb][1] *= alpha;
+            mma_f16(oe[vb], pa0, pa2, e4m3x2_to_f16x2(x0 & 0xffffu),
+                    e4m3x2_to_f16x2(x1 & 0xffffu));
+            mma_f16(oo[vb], pa0, pa2, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
+          }
         }
       }
-      float s4[4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int tok = nt * 8 + 2 * tig + c;
-          s4[nt * 2 + c] = (tok < n) ? sc[nt][c] * s_scale : -CUDART_INF_F;
-        }
-      const float alpha = softmax_row(s4, m_run, l_run);
-      const uint32_t pa0 = pack_f16x2(s4[0], s4[1]);
-      const uint32_t pa2 = pack_f16x2(s4[2], s4[3]);
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(s0 + v_lane + (uint32_t)(dp * 32), b0, b1, b2, b3);
-        o[2 * dp][0] *= alpha;
-        o[2 * dp][1] *= alpha;
-        o[2 * dp + 1][0] *= alpha;
-        o[2 * dp + 1][1] *= alpha;
-        mma_f16(o[2 * dp], pa0, pa2, b0, b1);
-        mma_f16(o[2 * dp + 1], pa0, pa2, b2, b3);
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
       ++stage;
     }
 
@@ -1014,16 +1027,21 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
       const float inv = a.v_scale / l;
       const float lse_nat = (m_run + log2f(l)) * 0.69314718055994530942f;
       const int64_t qrow = (int64_t)req * a.hq + (int64_t)hk * G + grp;
+      // lane holds dims 16 vb + 4 tig + {0, 1, 2, 3} = {oe.c0, oo.c0, oe.c1, oo.c1}
       if (dst < 0) {
-        uint32_t* op = reinterpret_cast<uint32_t*>(a.out + qrow * kHeadDim) + tig;
+        uint2* op = reinterpret_cast<uint2*>(a.out + qrow * kHeadDim) + tig;
 #pragma unroll
-        for (int dt = 0; dt < 16; ++dt) op[dt * 4] = pack_bf16x2(o[dt][0] * inv, o[dt][1] * inv);
+        for (int vb = 0; vb < 8; ++vb)
+          op[vb * 4] = make_uint2(pack_bf16x2(oe[vb][0] * inv, oo[vb][0] * inv),
+                                  pack_bf16x2(oe[vb][1] * inv, oo[vb][1] * inv));
         if (a.lse != nullptr && tig == 0) a.lse[qrow] = lse_nat;
       } else {
         const int64_t prow = (int64_t)dst * a.hq + (int64_t)hk * G + grp;
-        float2* op = reinterpret_cast<float2*>(a.o_part + prow * kHeadDim) + tig;
+        float4* op = reinterpret_cast<float4*>(a.o_part + prow * kHeadDim) + tig;
 #pragma unroll
-        for (int dt = 0; dt < 16; ++dt) op[dt * 4] = make_float2(o[dt][0] * inv, o[dt][1] * inv);
+        for (int vb = 0; vb < 8; ++vb)
+          op[vb * 4] = make_float4(oe[vb][0] * inv, oo[vb][0] * inv, oe[vb][1] * inv,
+                                   oo[vb][1] * inv);
         if (tig == 0) a.l_part[prow] = lse_nat;
       }
     }
@@ -1033,10 +1051,10 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
 template <int G, bool kMma, bool kBlock, bool kFp8>
 __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int stage_bytes = 2 * kTS * row_stride(a.row_bytes);
+  constexpr int kStageTokens = kFp8 ? kFp8Tokens : kTS;
+  const int stage_bytes = 2 * kStageTokens * row_stride(a.row_bytes);
   uint8_t* stages = smem;
-  uint8_t* scratch = smem + (size_t)kStages * stage_bytes;   // fp8 only
-  float* pbuf_all = reinterpret_cast<float*>(scratch + (kFp8 ? kMaxKvHeads * kFp8ScratchBytes : 0));
+  float* pbuf_all = reinterpret_cast<float*>(smem + (size_t)kStages * stage_bytes);
   float* sbuf_all = pbuf_all + kMaxKvHeads * kTS * G;
   uint64_t* full = reinterpret_cast<uint64_t*>(sbuf_all + kMaxKvHeads * 32);
   uint64_t* empty = full + kStages;
@@ -1069,11 +1087,11 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
     return;
   }
   if (warp == n_cons) {
-    run_producer(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
+    run_producer<kStageTokens>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
   } else if (warp < n_cons) {
     if constexpr (kFp8) {
-      run_consumer_mma_fp8<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
-                              scratch + warp * kFp8ScratchBytes, warp, lane);
+      run_consumer_mma_fp8<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
+                              lane);
     } else if constexpr (kBlock) {
       run_consumer_mma_block<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
                                 lane);
@@ -1119,8 +1137,9 @@ bool use_mma_consumer(int group, uint32_t flags) {
 
 int decode_smem_bytes(int hkv, int group, bool fp8) {
   const int rs = row_stride(hkv * kHeadDim * (fp8 ? 1 : 2));
-  return kStages * 2 * kTS * rs + (fp8 ? kMaxKvHeads * kFp8ScratchBytes : 0) +
-         kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 + 2 * kStages * 8 + 16;
+  const int tokens = fp8 ? kFp8Tokens : kTS;
+  return kStages * 2 * tokens * rs + kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 +
+         2 * kStages * 8 + 16;
 }
 
 cudaError_t decode_prepare(int group, bool mma, bool block, bool fp8, int smem_bytes) {

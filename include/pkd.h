@@ -96,6 +96,13 @@ typedef struct pkd_config {
  * needs a scale contract).  Tensor-core consumer only; not combinable with
  * PKD_FLAG_SHARED_PREFIX. */
 #define PKD_FLAG_KV_FP8 8u
+/* KV producer.  When the page size is a multiple of 16 and the consumer is
+ * the tensor-core one, the decode kernel copies 16 tokens of K (or V) of all
+ * KV heads per TMA tensor copy (a 5-D tensor map over the NHD cache, 128-byte
+ * shared-memory swizzle); otherwise it copies one token row (all KV heads) per
+ * bulk copy.  This flag forces the token-row copies.  Combinable with every
+ * other flag. */
+#define PKD_FLAG_ROW_COPIES 16u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;
@@ -112,6 +119,11 @@ typedef struct pkd_plan_info {
     int64_t makespan;          /* predicted max per-CTA cost                */
     int32_t nnz;               /* pages referenced                          */
     int32_t schedule_words;    /* int32 words pkd_plan_host writes          */
+    int32_t page_tiles;        /* 1: the context's decode kernel copies KV in
+                                  16-token page tiles (tensor map); 0: one
+                                  copy per token row (pkd_plan /
+                                  pkd_plan_shared fill it; pkd_plan_host
+                                  leaves it 0)                              */
 } pkd_plan_info;
 
 /* Bytes of device workspace needed for this configuration.  With

@@ -70,7 +70,8 @@ class PlanInfo(ctypes.Structure):
                 ("chunk_tokens", ctypes.c_int32), ("num_items", ctypes.c_int32),
                 ("num_units", ctypes.c_int32), ("num_slots", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("makespan", ctypes.c_int64),
-                ("nnz", ctypes.c_int32), ("schedule_words", ctypes.c_int32)]
+                ("nnz", ctypes.c_int32), ("schedule_words", ctypes.c_int32),
+                ("page_tiles", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -164,6 +165,7 @@ FLAG_FMA_CONSUMER = 1   # fold the GQA group onto CUDA cores (fp32 FMA)
 FLAG_MMA_CONSUMER = 2   # fold it onto tensor cores (mma.sync, bf16 in / fp32 acc)
 FLAG_SHARED_PREFIX = 4  # shared-prefix context: plans over groups of requests
 FLAG_KV_FP8 = 8         # E4M3 cache with per-call K / V scales
+FLAG_ROW_COPIES = 16    # force one KV copy per token row (no page-tile tensor map)
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -270,7 +272,7 @@ class BatchDecodeWithPagedKVCache:
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
                  use_tensor_cores=None, shared_prefix=False, kv_dtype="bf16", kv_layout="NHD",
-                 device=None):
+                 row_copies=False, device=None):
         import torch
         if kv_layout != "NHD":
             raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
@@ -287,6 +289,8 @@ class BatchDecodeWithPagedKVCache:
         self.kv_dtype = kv_dtype
         if kv_dtype == "e4m3":
             flags |= FLAG_KV_FP8
+        if row_copies:
+            flags |= FLAG_ROW_COPIES
         self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch,
                                max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas, flags)
         with torch.cuda.device(self.device):

@@ -19,14 +19,20 @@
 
 using namespace pkd;
 
+struct KvMapEntry {
+  const void* kv = nullptr;
+  CUtensorMap map{};
+};
+
 struct pkd_ctx {
   pkd_config cfg;
   int32_t n_cta = 0;
-  int32_t group = 0;
-  bool mma = false;
-  bool block = false;  // shared-prefix row-block kernel
-  bool fp8 = false;    // e4m3 cache
+  DecodeKind kind{};   // which decode kernel (consumer, cache type, producer)
   int smem_bytes = 0;
+  // page-tile maps by cache address (the map holds only the address and the
+  // context's fixed shape), replaced round-robin
+  std::vector<KvMapEntry> kv_maps;
+  size_t next_map = 0;
   int merge_grid = 0;
   int device = 0;
   Layout layout{};
@@ -54,8 +60,8 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 // The consumer flags exclude each other; the shared-prefix kernel exists for
 // the tensor-core consumer only.
 bool valid_flags(uint32_t f) {
-  const uint32_t known =
-      PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8;
+  const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX |
+                         PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES;
   if (f & ~known) return false;
   if ((f & PKD_FLAG_FMA_CONSUMER) &&
       (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8)))
@@ -81,10 +87,28 @@ int check_config(const pkd_config* c) {
   return PKD_OK;
 }
 
-int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
-  const int g = c->num_qo_heads / c->num_kv_heads;
-  const bool fp8 = (c->flags & PKD_FLAG_KV_FP8) != 0;
-  *smem_bytes = decode_smem_bytes(c->num_kv_heads, g, fp8);
+// The decode kernel a configuration selects.  Page tiles need a page size
+// that is a multiple of the 16-token box, a tensor-core consumer, and a
+// driver that encodes the map (checked on `probe_address`, a device address
+// standing in for the cache -- encoding records the address and checks the
+// shape; with a null probe the check is skipped).
+DecodeKind kind_for(const pkd_config* c, const void* probe_address) {
+  DecodeKind k;
+  k.group = c->num_qo_heads / c->num_kv_heads;
+  k.mma = use_mma_consumer(k.group, c->flags);
+  k.block = (c->flags & PKD_FLAG_SHARED_PREFIX) != 0;
+  k.fp8 = (c->flags & PKD_FLAG_KV_FP8) != 0;
+  k.tmap = k.mma && c->page_size % 16 == 0 && !(c->flags & PKD_FLAG_ROW_COPIES);
+  if (k.tmap && probe_address != nullptr) {
+    CUtensorMap m;
+    k.tmap = encode_kv_map(probe_address, c->num_pages, c->page_size, c->num_kv_heads, k.fp8,
+                           &m) == cudaSuccess;
+  }
+  return k;
+}
+
+int resolve_ctas(const pkd_config* c, const DecodeKind& k, int32_t* n_cta, int* smem_bytes) {
+  *smem_bytes = decode_smem_bytes(c->num_kv_heads, k);
   if (c->num_ctas > 0) {
     *n_cta = c->num_ctas;
     return PKD_OK;
@@ -93,10 +117,8 @@ int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
   if (cudaGetDevice(&dev) != cudaSuccess) return PKD_E_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKD_E_CUDA;
-  const bool mma = use_mma_consumer(g, c->flags);
-  const bool block = (c->flags & PKD_FLAG_SHARED_PREFIX) != 0;
-  if (decode_prepare(g, mma, block, fp8, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
-  if (decode_occupancy(g, mma, block, fp8, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
+  if (decode_prepare(k, *smem_bytes) != cudaSuccess) return PKD_E_CUDA;
+  if (decode_occupancy(k, c->num_kv_heads, *smem_bytes, &per_sm) != cudaSuccess)
     return PKD_E_CUDA;
   if (per_sm < 1) return PKD_E_UNSUPPORTED_SHAPE;
   *n_cta = sms * per_sm;
@@ -104,6 +126,30 @@ int resolve_ctas(const pkd_config* c, int32_t* n_cta, int* smem_bytes) {
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// The page-tile map of the cache at kv (cached per address).
+int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out) {
+  for (const KvMapEntry& e : ctx->kv_maps)
+    if (e.kv == kv) {
+      *out = e.map;
+      return PKD_OK;
+    }
+  KvMapEntry e;
+  e.kv = kv;
+  const pkd_config& c = ctx->cfg;
+  if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8, &e.map) !=
+      cudaSuccess)
+    return PKD_E_CUDA;
+  constexpr size_t kMaxMaps = 128;
+  if (ctx->kv_maps.size() < kMaxMaps) {
+    ctx->kv_maps.push_back(e);
+  } else {
+    ctx->kv_maps[ctx->next_map] = e;
+    ctx->next_map = (ctx->next_map + 1) % kMaxMaps;
+  }
+  *out = e.map;
+  return PKD_OK;
+}
 
 int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
                float k_scale, float v_scale, cudaStream_t stream, cudaEvent_t ev_before,
@@ -118,7 +164,7 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.kv = static_cast<const uint8_t*>(kv);
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
-  a.row_bytes = c.num_kv_heads * kHeadDim * (ctx->fp8 ? 1 : 2);
+  a.row_bytes = c.num_kv_heads * kHeadDim * (ctx->kind.fp8 ? 1 : 2);
   a.page_bytes = (int64_t)2 * c.page_size * a.row_bytes;
   a.off_cta = ctx->layout.cta_indptr;
   a.off_items = ctx->layout.items;
@@ -129,10 +175,14 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.num_pages = c.num_pages;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim) * (double)k_scale);
   a.v_scale = v_scale;
+  if (ctx->kind.tmap && kv != nullptr) {
+    const int st = kv_map_for(ctx, kv, &a.kv_map);
+    if (st != PKD_OK) return st;
+  }
   if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
-  if (launch_decode(ctx->group, ctx->mma, ctx->block, ctx->fp8, a, ctx->n_cta, c.num_kv_heads,
-                    ctx->smem_bytes, stream) != cudaSuccess)
+  if (launch_decode(ctx->kind, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
+      cudaSuccess)
     return PKD_E_CUDA;
   if (ev_after && cudaEventRecordWithFlags(ev_after, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
@@ -218,7 +268,8 @@ size_t pkd_workspace_bytes(const pkd_config* cfg) {
   if (check_config(cfg) != PKD_OK) return 0;
   int32_t n_cta = 0;
   int smem = 0;
-  if (resolve_ctas(cfg, &n_cta, &smem) != PKD_OK) return 0;
+  // the workspace layout does not depend on the producer
+  if (resolve_ctas(cfg, kind_for(cfg, nullptr), &n_cta, &smem) != PKD_OK) return 0;
   return make_layout(*cfg, n_cta).total_bytes;
 }
 
@@ -232,16 +283,13 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
   pkd_ctx* ctx = new (std::nothrow) pkd_ctx();
   if (!ctx) return PKD_E_INVALID_ARG;
   ctx->cfg = *cfg;
-  ctx->group = cfg->num_qo_heads / cfg->num_kv_heads;
-  ctx->mma = use_mma_consumer(ctx->group, cfg->flags);
-  ctx->block = (cfg->flags & PKD_FLAG_SHARED_PREFIX) != 0;
-  ctx->fp8 = (cfg->flags & PKD_FLAG_KV_FP8) != 0;
-  st = resolve_ctas(cfg, &ctx->n_cta, &ctx->smem_bytes);
+  ctx->kind = kind_for(cfg, d_workspace);
+  st = resolve_ctas(cfg, ctx->kind, &ctx->n_cta, &ctx->smem_bytes);
   if (st != PKD_OK) {
     delete ctx;
     return st;
   }
-  if (decode_prepare(ctx->group, ctx->mma, ctx->block, ctx->fp8, ctx->smem_bytes) != cudaSuccess) {
+  if (decode_prepare(ctx->kind, ctx->smem_bytes) != cudaSuccess) {
     delete ctx;
     return PKD_E_CUDA;
   }
@@ -311,6 +359,7 @@ static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n
   if (cudaEventRecord(ctx->staged[k], s) != cudaSuccess) return PKD_E_CUDA;
   ctx->staged_pending[k] = true;
   ctx->next_staging = k ^ 1;
+  info.page_tiles = ctx->kind.tmap ? 1 : 0;
   ctx->info = info;
   ctx->epoch += 1;
   if (epoch) *epoch = ctx->epoch;
@@ -325,7 +374,7 @@ int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
 int pkd_plan_shared(pkd_ctx* ctx, const int32_t* group_indptr, int32_t num_groups,
                     const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                     void* stream, uint64_t* epoch) {
-  if (ctx == nullptr || !ctx->block) return PKD_E_INVALID_ARG;
+  if (ctx == nullptr || !ctx->kind.block) return PKD_E_INVALID_ARG;
   if (num_groups > 0 && group_indptr == nullptr) return PKD_E_INVALID_ARG;
   return plan_and_publish(ctx, group_indptr, num_groups, indptr, indices, last_page_len, stream,
                           epoch);

@@ -14,12 +14,17 @@
 //  * Grid = the plan's fixed CTA count (persistent; only the queue contents
 //    change between plans, so launches can be captured in a CUDA graph).
 //  * One producer warp streams the item's tokens into a 3-deep ring of
-//    shared-memory stages with TMA bulk copies (cp.async.bulk, completion on
-//    an mbarrier, L2 evict-first).  A stage holds 16 tokens; in the NHD
-//    layout one token row of all KV heads is contiguous, so each token costs
-//    one K-row and one V-row copy (2 KiB each at 8 KV heads), landing at a
-//    padded row stride so that 8-row fragment loads of one head are
-//    conflict-free.  Only valid rows are copied.
+//    shared-memory stages with TMA (completion on an mbarrier, L2
+//    evict-first).  A stage holds 16 tokens (32 for an e4m3 cache).  Two
+//    producers:
+//      - page tiles (page size a multiple of 16): one tensor-map copy
+//        (cp.async.bulk.tensor, 5-D) moves 16 tokens of K (or V) of all KV
+//        heads, re-ordered to [head][128-byte half][token] with the 128-byte
+//        swizzle, so 8-token fragment loads of one head are conflict-free;
+//      - token rows (any page size): in the NHD layout one token row of all
+//        KV heads is contiguous, so each token costs one K-row and one V-row
+//        bulk copy (cp.async.bulk, 2 KiB each at 8 KV heads), landing at a
+//        padded row stride for the same reason.  Only valid rows are copied.
 //  * One consumer warp per KV head folds its GQA group of G query heads onto
 //    each K/V row it reads from shared memory (one read serves G heads).  The
 //    default consumer runs the group as a thin matrix on tensor cores
@@ -32,9 +37,12 @@
 //    the device error word, stops issuing copies, waits (bounded) for the
 //    copies already in flight, and returns.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp8.h>
 #include <math_constants.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "pkd_internal.h"
 
@@ -119,6 +127,25 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 5-D tensor-map copy global -> shared (box of the map at the given
+// coordinates, innermost first), completion counted in bytes on `bar`.
+__device__ __forceinline__ void tensor_copy_g2s(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                int c2, int c3, int c4, uint64_t* bar,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory stride of one token row (all KV heads): 16 bytes of padding
 // shift consecutive rows across banks, so 8-row fragment loads of one head
 // are conflict-free.
@@ -169,13 +196,22 @@ __device__ __forceinline__ void rs_level(const float (&v)[N], float (&o)[N / 2],
 }
 
 // ---------------------------------------------------------------- producer
-template <int kTokens>
+// Page tiles (kTiles): stage = [K box 0 .. kBoxes-1][V box 0 .. kBoxes-1],
+// box b holding tokens 16 b .. 16 b + 15 of the stage as [head][half][token]
+// lines of 128 bytes; lane 2 b + c copies box b of K (c = 0) or V (c = 1).
+// A box always moves 16 token slots of its page; slots past the item's end
+// are in-page bytes the consumers mask (scores) or zero (V).
+// Token rows: stage = [K rows][V rows] at the padded row stride; lane j
+// copies token j's K row and V row (valid tokens only).
+template <int kTokens, bool kTiles>
 __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* stages,
                              int stage_bytes, uint64_t* full, uint64_t* empty,
                              volatile int* abort_flag, int lane) {
+  constexpr int kBoxes = kTokens / 16;
   const int P = a.page_size;
   const int row = a.row_bytes;
   const int rs = row_stride(row);
+  const uint32_t box = (uint32_t)(16 * row);
   const uint64_t policy = l2_evict_first_policy();
   bool waited = false;  // programmatic-launch wait, before the first KV read
   uint32_t stage = 0;
@@ -187,12 +223,12 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
       const int n = min(kTokens, te - t);
       const int slot = (int)(stage % kStages);
       const uint32_t round = stage / kStages;
-      // Page id of this lane's token: one K row and one V row per token (all
-      // KV heads), landing at a padded stride.
+      // this lane's token (rows) or box (tiles), and its page id
+      const int nbox = (n + 15) >> 4;
+      const int tok = kTiles ? t + 16 * (lane >> 1) : t + lane;
       int page = -1;
-      const int j = lane;
-      if (j < n) {
-        page = a.sched[a.off_pages + poff + (t + j - tb) / P];
+      if (kTiles ? (lane >> 1) < nbox : lane < n) {
+        page = a.sched[a.off_pages + poff + (tok - tb) / P];
         if ((unsigned)page >= (unsigned)a.num_pages) {
           atomicOr(a.err, PKD_DEV_ERR_BOUNDS);
           page = 0;
@@ -206,19 +242,27 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
           break;
         }
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * n * row));
+      if (lane == 0)
+        mbar_arrive_expect_tx(&full[slot], kTiles ? 2u * (uint32_t)nbox * box
+                                                  : (uint32_t)(2 * n * row));
       __syncwarp();
       if (page >= 0) {
-        const int pslot = (t + j) % P;
-        const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)pslot * row;
-        uint8_t* dk = stages + (size_t)slot * stage_bytes + (size_t)j * rs;
-        uint8_t* dv = dk + (size_t)kTokens * rs;
         if (!waited) {
           pdl_wait();
           waited = true;
         }
-        bulk_copy_g2s(dk, src, (uint32_t)row, &full[slot], policy);
-        bulk_copy_g2s(dv, src + (int64_t)P * row, (uint32_t)row, &full[slot], policy);
+        uint8_t* st = stages + (size_t)slot * stage_bytes;
+        if constexpr (kTiles) {
+          const int c = lane & 1;
+          tensor_copy_g2s(st + (size_t)(c * kBoxes + (lane >> 1)) * box, &a.kv_map, 0, tok % P, 0,
+                          0, 2 * page + c, &full[slot], policy);
+        } else {
+          const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)(tok % P) * row;
+          uint8_t* dk = st + (size_t)lane * rs;
+          bulk_copy_g2s(dk, src, (uint32_t)row, &full[slot], policy);
+          bulk_copy_g2s(dk + (size_t)kTokens * rs, src + (int64_t)P * row, (uint32_t)row,
+                        &full[slot], policy);
+        }
       }
       ++stage;
     }
@@ -485,18 +529,74 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 // query heads, so the other half of the tile is always zero.
 __device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
                                          uint32_t b1) {
-  float z0, z1;
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%11,%12,%12};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
+      "{\n\t.reg .f32 z0, z1;\n\t"
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,z0,z1}, {%2,%3,%4,%5}, "
+      "{%6,%7}, {%8,%9,%10,%10};\n\t}"
+      : "=f"(d[0]), "=f"(d[1])
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
-  (void)z0;
-  (void)z1;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
 }
+
+// Shared-memory addresses of KV head hk's ldmatrix rows in a 16-token bf16
+// stage.  K (no transpose), for N tile nt and K-step pair kp: lane L gives
+// token 8 nt + L % 8, 16-byte chunk 4 kp + L / 8 of the head's 256 bytes.
+// V (transposed), for dim pair dp: token (L / 8 & 1) * 8 + L % 8, chunk
+// 2 dp + L / 16.
+//  * token rows: token t at t * rs (K rows, then V rows), head at hk * 256;
+//  * page tiles: K box at 0, V box at 16 * row_bytes; inside a box the
+//    128-byte line (2 hk + chunk / 8) * 16 + t holds the chunk at position
+//    (chunk % 8) ^ (t % 8).
+template <bool kTiles>
+struct Bf16Frags {
+  uint32_t k, v, kx, vx;
+  int rs;
+  __device__ __forceinline__ Bf16Frags(const DecodeArgs& a, int hk, int lane) {
+    rs = row_stride(a.row_bytes);
+    const int r = lane & 7;
+    if constexpr (kTiles) {
+      k = (uint32_t)((hk * 32 + r) * 128);
+      kx = (uint32_t)(((lane >> 3) ^ r) << 4);
+      v = (uint32_t)(16 * a.row_bytes + (hk * 32 + ((lane >> 3) & 1) * 8 + r) * 128);
+      vx = (uint32_t)(((lane >> 4) ^ r) << 4);
+    } else {
+      k = (uint32_t)(r * rs + hk * (kHeadDim * 2) + (lane >> 3) * 16);
+      v = (uint32_t)(kTS * rs + (((lane >> 3) & 1) * 8 + r) * rs + hk * (kHeadDim * 2) +
+                     (lane >> 4) * 16);
+      kx = vx = 0;
+    }
+  }
+  __device__ __forceinline__ uint32_t kaddr(uint32_t sbase, int nt, int kp) const {
+    if constexpr (kTiles)
+      return sbase + k + (uint32_t)((kp >> 1) * 2048 + nt * 1024) + (kx ^ (uint32_t)((kp & 1) << 6));
+    else
+      return sbase + k + (uint32_t)(nt * 8 * rs + kp * 64);
+  }
+  __device__ __forceinline__ uint32_t vaddr(uint32_t sbase, int dp) const {
+    if constexpr (kTiles)
+      return sbase + v + (uint32_t)((dp >> 2) * 2048) + (vx ^ (uint32_t)((dp & 3) << 5));
+    else
+      return sbase + v + (uint32_t)(dp * 32);
+  }
+  // Zero head hk's V tokens n .. 15 of the stage (stale or past-the-end
+  // bytes: P = 0 there, but 0 x NaN would poison O).
+  __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int row_bytes, int hk, int lane,
+                                              int n) const {
+    if constexpr (kTiles) {
+      uint8_t* z = stage + 16 * row_bytes + (hk * 32 + ((lane >> 3) & 1) * 16) * 128 + (lane & 7) * 16;
+      for (int r = n + (lane >> 4); r < kTS; r += 2)
+        *reinterpret_cast<uint4*>(z + r * 128) = make_uint4(0, 0, 0, 0);
+    } else {
+      uint8_t* z = stage + (size_t)kTS * rs + hk * (kHeadDim * 2) + (lane & 15) * 16;
+      for (int r = n + (lane >> 4); r < kTS; r += 2)
+        *reinterpret_cast<uint4*>(z + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+};
 
 // A fragments of the group's queries: row = query head grp, two bf16 per
 // register (dims 16 ks + 2 tig, +1 and the same + 8).
@@ -513,7 +613,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int req, int h
   }
 }
 
-template <int G>
+template <int G, bool kTiles>
 __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                                  int stage_bytes, uint64_t* full, uint64_t* empty,
                                  volatile int* abort_flag, int warp, int lane) {
@@ -521,15 +621,8 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
   const int grp = lane >> 2;   // fragment row: query head within the group
   const int tig = lane & 3;    // fragment column pair
   const bool row_ok = grp < G;
-  const int rs = row_stride(a.row_bytes);
   const uint32_t stage0 = smem_u32(stages);
-  // ldmatrix row addresses (relative to a stage): lane L serves matrix L / 8,
-  // row L % 8.  K (no transpose): token = L % 8 (+ 8 per N tile), dim block =
-  // L / 8 (+ 4 per pair of K steps).  V (transpose): token = (L / 8 & 1) * 8
-  // + L % 8, dim block = L / 16 (+ 2 per pair of N tiles).
-  const uint32_t k_lane = (uint32_t)((lane & 7) * rs + hk * (kHeadDim * 2) + (lane >> 3) * 16);
-  const uint32_t v_lane = (uint32_t)(kTS * rs + (((lane >> 3) & 1) * 8 + (lane & 7)) * rs +
-                                     hk * (kHeadDim * 2) + (lane >> 4) * 16);
+  const Bf16Frags<kTiles> fr(a, hk, lane);
 
   // the item and its queries are fetched one item ahead
   const int32_t* item = a.sched + a.off_items + (int64_t)it0 * kItemWords;
@@ -565,15 +658,9 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
         return;
       }
       const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
-      if (n < kTS) {
-        // rows past the item's end hold stale bytes: zero this head's V rows
-        // there so P (= 0) x V cannot produce NaN
-        uint8_t* vrow = const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes +
-                        (size_t)kTS * rs + hk * (kHeadDim * 2) + (lane & 15) * 16;
-        for (int r = n + (lane >> 4); r < kTS; r += 2)
-          *reinterpret_cast<uint4*>(vrow + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-      }
+      if (n < kTS)
+        fr.zero_v_tail(const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes, a.row_bytes, hk,
+                       lane, n);
       // ---- S = Q K^T for two 8-token tiles
       float sc[2][2];
 #pragma unroll
@@ -582,7 +669,7 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(sbase + k_lane + (uint32_t)(nt * 8 * rs + kp * 64), b0, b1, b2, b3);
+          ldsm_x4(fr.kaddr(sbase, nt, kp), b0, b1, b2, b3);
           mma_bf16(sc[nt], qa0[2 * kp], qa2[2 * kp], b0, b1);
           mma_bf16(sc[nt], qa0[2 * kp + 1], qa2[2 * kp + 1], b2, b3);
         }
@@ -619,7 +706,7 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
 #pragma unroll
       for (int dp = 0; dp < 8; ++dp) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sbase + v_lane + (uint32_t)(dp * 32), b0, b1, b2, b3);
+        ldsm_x4_t(fr.vaddr(sbase, dp), b0, b1, b2, b3);
         o[2 * dp][0] *= alpha;
         o[2 * dp][1] *= alpha;
         o[2 * dp + 1][0] *= alpha;
@@ -704,7 +791,7 @@ __device__ __forceinline__ float softmax_row(float (&s4)[4], float& m_run, float
   return alpha;
 }
 
-template <int G>
+template <int G, bool kTiles>
 __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
                                        const uint8_t* stages, int stage_bytes, uint64_t* full,
                                        uint64_t* empty, volatile int* abort_flag, int warp,
@@ -715,11 +802,8 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
   // the lane's two tile rows: grp and grp + 8
   const int rq0 = grp / G, hd0 = grp % G;
   const int rq1 = (grp + 8) / G, hd1 = (grp + 8) % G;
-  const int rs = row_stride(a.row_bytes);
   const uint32_t stage0 = smem_u32(stages);
-  const uint32_t k_lane = (uint32_t)((lane & 7) * rs + hk * (kHeadDim * 2) + (lane >> 3) * 16);
-  const uint32_t v_lane = (uint32_t)(kTS * rs + (((lane >> 3) & 1) * 8 + (lane & 7)) * rs +
-                                     hk * (kHeadDim * 2) + (lane >> 4) * 16);
+  const Bf16Frags<kTiles> fr(a, hk, lane);
   pdl_wait();   // q may come from the previous kernel in the stream
   uint32_t stage = 0;
   for (int it = it0; it < it1; ++it) {
@@ -757,13 +841,9 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
         return;
       }
       const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
-      if (n < kTS) {
-        uint8_t* vrow = const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes +
-                        (size_t)kTS * rs + hk * (kHeadDim * 2) + (lane & 15) * 16;
-        for (int r = n + (lane >> 4); r < kTS; r += 2)
-          *reinterpret_cast<uint4*>(vrow + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-      }
+      if (n < kTS)
+        fr.zero_v_tail(const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes, a.row_bytes, hk,
+                       lane, n);
       float sc[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -772,7 +852,7 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(sbase + k_lane + (uint32_t)(nt * 8 * rs + kp * 64), b0, b1, b2, b3);
+          ldsm_x4(fr.kaddr(sbase, nt, kp), b0, b1, b2, b3);
           mma_bf16_full(sc[nt], qa0[2 * kp], qa1[2 * kp], qa2[2 * kp], qa3[2 * kp], b0, b1);
           mma_bf16_full(sc[nt], qa0[2 * kp + 1], qa1[2 * kp + 1], qa2[2 * kp + 1],
                         qa3[2 * kp + 1], b2, b3);
@@ -796,7 +876,7 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
 #pragma unroll
       for (int dp = 0; dp < 8; ++dp) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sbase + v_lane + (uint32_t)(dp * 32), b0, b1, b2, b3);
+        ldsm_x4_t(fr.vaddr(sbase, dp), b0, b1, b2, b3);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           o[2 * dp + h][0] *= al0;
@@ -866,14 +946,12 @@ constexpr int kFp8Tokens = 32;
 
 __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
                                         uint32_t b1) {
-  float z0, z1;
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%11,%12,%12};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(z0), "=f"(z1)
+      "{\n\t.reg .f32 z0, z1;\n\t"
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,z0,z1}, {%2,%3,%4,%5}, "
+      "{%6,%7}, {%8,%9,%10,%10};\n\t}"
+      : "=f"(d[0]), "=f"(d[1])
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d[0]), "f"(d[1]), "f"(0.f));
-  (void)z0;
-  (void)z1;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -887,7 +965,66 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
-template <int G>
+// Shared-memory addresses of KV head hk's ldmatrix rows in a 32-token e4m3
+// stage (16-token tile st).  K, for N tile nt and x4 kq: lane L gives token
+// 16 st + 8 nt + L % 8, 16-byte chunk 4 kq + L / 8 of the head's 128 bytes.
+// V (trans), for x4 vp: token 16 st + (L / 8 & 1) * 8 + L % 8, chunk
+// 2 vp + L / 16.
+//  * token rows: token t at t * rs (K rows, then V rows), head at hk * 128;
+//  * page tiles: K box st at st * box, V box st at (2 + st) * box (box =
+//    16 * row_bytes); inside a box the line hk * 16 + t holds chunk c at
+//    position c ^ (t % 8).
+template <bool kTiles>
+struct Fp8Frags {
+  uint32_t k, v, kx, vx, box;
+  int rs;
+  __device__ __forceinline__ Fp8Frags(const DecodeArgs& a, int hk, int lane) {
+    rs = row_stride(a.row_bytes);
+    box = (uint32_t)(16 * a.row_bytes);
+    const int r = lane & 7;
+    if constexpr (kTiles) {
+      k = (uint32_t)((hk * 16 + r) * 128);
+      kx = (uint32_t)(((lane >> 3) ^ r) << 4);
+      v = 2 * box + (uint32_t)((hk * 16 + ((lane >> 3) & 1) * 8 + r) * 128);
+      vx = (uint32_t)(((lane >> 4) ^ r) << 4);
+    } else {
+      k = (uint32_t)(r * rs + hk * kHeadDim + (lane >> 3) * 16);
+      v = (uint32_t)(kFp8Tokens * rs + (((lane >> 3) & 1) * 8 + r) * rs + hk * kHeadDim +
+                     (lane >> 4) * 16);
+      kx = vx = 0;
+    }
+  }
+  __device__ __forceinline__ uint32_t kaddr(uint32_t sbase, int st, int nt, int kq) const {
+    if constexpr (kTiles)
+      return sbase + (uint32_t)st * box + k + (uint32_t)(nt * 1024) + (kx ^ (uint32_t)(kq << 6));
+    else
+      return sbase + k + (uint32_t)((st * 16 + nt * 8) * rs + kq * 64);
+  }
+  __device__ __forceinline__ uint32_t vaddr(uint32_t sbase, int st, int vp) const {
+    if constexpr (kTiles)
+      return sbase + (uint32_t)st * box + v + (vx ^ (uint32_t)(vp << 5));
+    else
+      return sbase + v + (uint32_t)(st * 16 * rs + vp * 32);
+  }
+  // Zero head hk's V tokens n .. (end of the copied rows) of the stage
+  // (0x7f / 0xff bytes are NaN in e4m3).
+  __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int hk, int lane, int n) const {
+    if constexpr (kTiles) {
+      const int end = (n + 15) & ~15;   // the copied boxes
+      uint8_t* z = stage + 2 * box + hk * 16 * 128 + (lane & 7) * 16;
+      for (int r = n + (lane >> 3); r < end; r += 4)
+        *reinterpret_cast<uint4*>(z + (r >> 4) * box + (r & 15) * 128) = make_uint4(0, 0, 0, 0);
+    } else {
+      uint8_t* z = stage + (size_t)kFp8Tokens * rs + hk * kHeadDim + (lane & 7) * 16;
+      for (int r = n + (lane >> 3); r < kFp8Tokens; r += 4)
+        *reinterpret_cast<uint4*>(z + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+};
+
+template <int G, bool kTiles>
 __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                                      int stage_bytes, uint64_t* full, uint64_t* empty,
                                      volatile int* abort_flag, int warp, int lane) {
@@ -896,14 +1033,8 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
   const int grp = lane >> 2;
   const int tig = lane & 3;
   const bool row_ok = grp < G;
-  const int rs = row_stride(a.row_bytes);
   const uint32_t stage0 = smem_u32(stages);
-  // ldmatrix row addresses: K: token L % 8 (+ 8 per N tile, + 16 per tile),
-  // dim block L / 8 (+ 4 per x4); V (trans): token (L / 8 & 1) * 8 + L % 8,
-  // dim block L / 16 (+ 2 per x4)
-  const uint32_t k_lane = (uint32_t)((lane & 7) * rs + hk * kHeadDim + (lane >> 3) * 16);
-  const uint32_t v_lane = (uint32_t)(T * rs + (((lane >> 3) & 1) * 8 + (lane & 7)) * rs +
-                                     hk * kHeadDim + (lane >> 4) * 16);
+  const Fp8Frags<kTiles> fr(a, hk, lane);
   pdl_wait();
   uint32_t stage = 0;
   for (int it = it0; it < it1; ++it) {
@@ -953,19 +1084,11 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
         return;
       }
       const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
-      if (n < T) {
-        // V rows past the item's end hold stale bytes (0x7f/0xff are NaN):
-        // zero this head's slice there
-        uint8_t* vrow = const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes +
-                        (size_t)T * rs + hk * kHeadDim + (lane & 7) * 16;
-        for (int r = n + (lane >> 3); r < T; r += 4)
-          *reinterpret_cast<uint4*>(vrow + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-      }
+      if (n < T)
+        fr.zero_v_tail(const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes, hk, lane, n);
 #pragma unroll
       for (int st = 0; st < T / 16; ++st) {
         if (st * 16 >= n) break;
-        const uint32_t tbase = sbase + (uint32_t)(st * 16 * rs);
         // ---- S = Q K^T, two 8-token tiles
         float sc[2][2];
 #pragma unroll
@@ -974,7 +1097,7 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
 #pragma unroll
           for (int kq = 0; kq < 2; ++kq) {
             uint32_t r[4];
-            ldsm_x4(tbase + k_lane + (uint32_t)(nt * 8 * rs + kq * 64), r[0], r[1], r[2], r[3]);
+            ldsm_x4(fr.kaddr(sbase, st, nt, kq), r[0], r[1], r[2], r[3]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int kb = kq * 4 + j;
@@ -998,7 +1121,7 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
 #pragma unroll
         for (int vp = 0; vp < 4; ++vp) {
           uint32_t r[4];
-          ldsm_x4_t(tbase + v_lane + (uint32_t)(vp * 32), r[0], r[1], r[2], r[3]);
+          ldsm_x4_t(fr.vaddr(sbase, st, vp), r[0], r[1], r[2], r[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int vb = 2 * vp + h;
@@ -1048,13 +1171,24 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
   }
 }
 
-template <int G, bool kMma, bool kBlock, bool kFp8>
-__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const DecodeArgs a) {
+// Stage bytes: token rows keep a padded row stride; page tiles are dense
+// (16 * row_bytes per box, a multiple of 1024, so every box stays aligned for
+// the 128-byte swizzle).
+__host__ __device__ __forceinline__ int stage_bytes_for(int row_bytes, int tokens, bool tiles) {
+  return 2 * tokens * (tiles ? row_bytes : row_stride(row_bytes));
+}
+
+template <int G, bool kMma, bool kBlock, bool kFp8, bool kTiles>
+__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
+    decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kStageTokens = kFp8 ? kFp8Tokens : kTS;
-  const int stage_bytes = 2 * kStageTokens * row_stride(a.row_bytes);
+  const int stage_bytes = stage_bytes_for(a.row_bytes, kStageTokens, kTiles);
+  // the 128-byte swizzle repeats every 1024 bytes: page-tile stages start on
+  // a 1024-byte boundary (the launch reserves the slack)
   uint8_t* stages = smem;
-  float* pbuf_all = reinterpret_cast<float*>(smem + (size_t)kStages * stage_bytes);
+  if constexpr (kTiles) stages += (1024u - (smem_u32(smem) & 1023u)) & 1023u;
+  float* pbuf_all = reinterpret_cast<float*>(stages + (size_t)kStages * stage_bytes);
   float* sbuf_all = pbuf_all + kMaxKvHeads * kTS * G;
   uint64_t* full = reinterpret_cast<uint64_t*>(sbuf_all + kMaxKvHeads * 32);
   uint64_t* empty = full + kStages;
@@ -1087,16 +1221,18 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
     return;
   }
   if (warp == n_cons) {
-    run_producer<kStageTokens>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, lane);
+    run_producer<kStageTokens, kTiles>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+                                       lane);
   } else if (warp < n_cons) {
     if constexpr (kFp8) {
-      run_consumer_mma_fp8<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
-                              lane);
+      run_consumer_mma_fp8<G, kTiles>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+                                      warp, lane);
     } else if constexpr (kBlock) {
-      run_consumer_mma_block<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
-                                lane);
+      run_consumer_mma_block<G, kTiles>(a, it0, it1, stages, stage_bytes, full, empty,
+                                        abort_flag, warp, lane);
     } else if constexpr (kMma) {
-      run_consumer_mma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp, lane);
+      run_consumer_mma<G, kTiles>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
+                                  lane);
     } else {
       run_consumer_fma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
                           pbuf_all + warp * kTS * G, sbuf_all + warp * 32, warp, lane);
@@ -1104,22 +1240,28 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1) decode_kernel(const
   }
 }
 
-template <int G>
-const void* kernel_ptr(bool mma, bool block, bool fp8) {
-  if (fp8) return reinterpret_cast<const void*>(&decode_kernel<G, true, false, true>);
-  if (block) return reinterpret_cast<const void*>(&decode_kernel<G, true, true, false>);
-  return mma ? reinterpret_cast<const void*>(&decode_kernel<G, true, false, false>)
-             : reinterpret_cast<const void*>(&decode_kernel<G, false, false, false>);
+template <int G, bool kTiles>
+const void* kernel_ptr(const DecodeKind& k) {
+  if (k.fp8) return reinterpret_cast<const void*>(&decode_kernel<G, true, false, true, kTiles>);
+  if (k.block) return reinterpret_cast<const void*>(&decode_kernel<G, true, true, false, kTiles>);
+  if (k.mma) return reinterpret_cast<const void*>(&decode_kernel<G, true, false, false, kTiles>);
+  if constexpr (kTiles) return nullptr;   // the CUDA-core consumer reads token rows only
+  return reinterpret_cast<const void*>(&decode_kernel<G, false, false, false, false>);
 }
 
-const void* kernel_for(int group, bool mma, bool block, bool fp8) {
-  if ((block || fp8) && !mma) return nullptr;
-  if (block && fp8) return nullptr;
-  switch (group) {
-    case 1: return kernel_ptr<1>(mma, block, fp8);
-    case 2: return kernel_ptr<2>(mma, block, fp8);
-    case 4: return kernel_ptr<4>(mma, block, fp8);
-    case 8: return kernel_ptr<8>(mma, block, fp8);
+template <int G>
+const void* kernel_ptr_g(const DecodeKind& k) {
+  return k.tmap ? kernel_ptr<G, true>(k) : kernel_ptr<G, false>(k);
+}
+
+const void* kernel_for(const DecodeKind& k) {
+  if ((k.block || k.fp8) && !k.mma) return nullptr;
+  if (k.block && k.fp8) return nullptr;
+  switch (k.group) {
+    case 1: return kernel_ptr_g<1>(k);
+    case 2: return kernel_ptr_g<2>(k);
+    case 4: return kernel_ptr_g<4>(k);
+    case 8: return kernel_ptr_g<8>(k);
     default: return nullptr;
   }
 }
@@ -1135,35 +1277,34 @@ bool use_mma_consumer(int group, uint32_t flags) {
   return true;   // measured faster than the CUDA-core consumer at every group size
 }
 
-int decode_smem_bytes(int hkv, int group, bool fp8) {
-  const int rs = row_stride(hkv * kHeadDim * (fp8 ? 1 : 2));
-  const int tokens = fp8 ? kFp8Tokens : kTS;
-  return kStages * 2 * tokens * rs + kMaxKvHeads * kTS * group * 4 + kMaxKvHeads * 32 * 4 +
-         2 * kStages * 8 + 16;
+int decode_smem_bytes(int hkv, const DecodeKind& k) {
+  const int row = hkv * kHeadDim * (k.fp8 ? 1 : 2);
+  const int tokens = k.fp8 ? kFp8Tokens : kTS;
+  return kStages * stage_bytes_for(row, tokens, k.tmap) + (k.tmap ? 1024 : 0) +
+         kMaxKvHeads * kTS * k.group * 4 + kMaxKvHeads * 32 * 4 + 2 * kStages * 8 + 16;
 }
 
-cudaError_t decode_prepare(int group, bool mma, bool block, bool fp8, int smem_bytes) {
-  const void* k = kernel_for(group, mma, block, fp8);
-  if (!k) return cudaErrorInvalidValue;
+cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes) {
+  const void* f = kernel_for(k);
+  if (!f) return cudaErrorInvalidValue;
   // The attribute is per kernel, shared by every context: always allow the
   // largest layout (8 KV heads) so a smaller context never lowers it.
-  const int most = decode_smem_bytes(kMaxKvHeads, group, fp8);
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int most = decode_smem_bytes(kMaxKvHeads, k);
+  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_bytes > most ? smem_bytes : most);
 }
 
-cudaError_t decode_occupancy(int group, bool mma, bool block, bool fp8, int hkv, int smem_bytes,
-                             int* blocks_per_sm) {
-  const void* k = kernel_for(group, mma, block, fp8);
-  if (!k) return cudaErrorInvalidValue;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, decode_threads(hkv),
+cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* blocks_per_sm) {
+  const void* f = kernel_for(k);
+  if (!f) return cudaErrorInvalidValue;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, decode_threads(hkv),
                                                        (size_t)smem_bytes);
 }
 
-cudaError_t launch_decode(int group, bool mma, bool block, bool fp8, const DecodeArgs& a,
-                          int grid, int hkv, int smem_bytes, cudaStream_t stream) {
-  const void* k = kernel_for(group, mma, block, fp8);
-  if (!k) return cudaErrorInvalidValue;
+cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, int hkv,
+                          int smem_bytes, cudaStream_t stream) {
+  const void* f = kernel_for(k);
+  if (!f) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(decode_threads(hkv));
@@ -1175,7 +1316,44 @@ cudaError_t launch_decode(int group, bool mma, bool block, bool fp8, const Decod
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {const_cast<DecodeArgs*>(&a)};
-  return cudaLaunchKernelExC(&cfg, k, args);
+  return cudaLaunchKernelExC(&cfg, f, args);
+}
+
+// The map: dims (innermost first) {128-byte chunk of elements, token slot,
+// 128-byte half of a head, KV head, 2 * page + (0 K, 1 V)} with byte strides
+// {row, 128, D * E, P * row}; box {chunk, 16 tokens, all halves, all heads,
+// one K or V page}, which lands as [head][half][token][128 B] with the
+// 128-byte swizzle.
+cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
+                          bool fp8, CUtensorMap* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (encode == nullptr) return cudaErrorNotSupported;
+  if (kv == nullptr || (uintptr_t)kv % 16 != 0 || page_size % 16 != 0 || num_pages < 1 ||
+      hkv < 1 || hkv > kMaxKvHeads)
+    return cudaErrorInvalidValue;
+  const int E = fp8 ? 1 : 2;
+  const cuuint64_t row = (cuuint64_t)hkv * kHeadDim * E;
+  const cuuint64_t dims[5] = {(cuuint64_t)(128 / E), (cuuint64_t)page_size,
+                              (cuuint64_t)(kHeadDim * E / 128), (cuuint64_t)hkv,
+                              2 * (cuuint64_t)num_pages};
+  const cuuint64_t strides[4] = {row, 128, (cuuint64_t)(kHeadDim * E), (cuuint64_t)page_size * row};
+  const cuuint32_t box[5] = {(cuuint32_t)(128 / E), 16, (cuuint32_t)(kHeadDim * E / 128),
+                             (cuuint32_t)hkv, 1};
+  const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  const CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            5, const_cast<void*>(kv), dims, strides, box, elem_strides,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace pkd

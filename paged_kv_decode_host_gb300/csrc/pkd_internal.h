@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>   // CUtensorMap (encoded through the runtime's driver entry point)
 #include <cuda_runtime_api.h>
 
 #include "pkd.h"
@@ -98,6 +99,10 @@ struct DecodeArgs {
   int32_t row_bytes;         // Hkv * D * element bytes: one token of one page, all heads
   float scale_log2;          // k_scale * log2(e) / sqrt(D)
   float v_scale;             // multiplies the output (1 for an unscaled cache)
+  // Page-tile producer only: 5-D map over the cache (128-byte chunk, token
+  // slot, 128-byte half of a head, KV head, 2 * page + {0 K, 1 V}) whose
+  // 16-token box lands in shared memory with the 128-byte swizzle.
+  CUtensorMap kv_map;
 };
 
 struct MergeArgs {
@@ -111,15 +116,24 @@ struct MergeArgs {
 };
 
 // Kernel launchers (decode_kernel.cu / merge_kernels.cu).
-int decode_smem_bytes(int hkv, int group, bool fp8);
+// Which decode kernel runs.
+struct DecodeKind {
+  int group = 1;       // query heads per KV head (1, 2, 4, 8)
+  bool mma = true;     // tensor-core consumer (false: CUDA-core FMA)
+  bool block = false;  // shared-prefix variant (work items over row blocks of requests)
+  bool fp8 = false;    // the cache holds e4m3 (tensor-core consumer only)
+  bool tmap = false;   // page-tile producer: one tensor-map copy per 16 tokens of K or V
+                       // (P % 16 == 0, tensor-core consumers); else one copy per token row
+};
+int decode_smem_bytes(int hkv, const DecodeKind& k);
 int decode_threads(int hkv);
-// block: the shared-prefix variant (work items over row blocks of requests)
-// fp8: the cache holds e4m3 (tensor-core consumer only)
-cudaError_t decode_prepare(int group, bool mma, bool block, bool fp8, int smem_bytes);
-cudaError_t decode_occupancy(int group, bool mma, bool block, bool fp8, int hkv, int smem_bytes,
-                             int* blocks_per_sm);
-cudaError_t launch_decode(int group, bool mma, bool block, bool fp8, const DecodeArgs& a,
-                          int grid, int hkv, int smem_bytes, cudaStream_t stream);
+cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes);
+cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* blocks_per_sm);
+cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, int hkv,
+                          int smem_bytes, cudaStream_t stream);
+// Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`.
+cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
+                          bool fp8, CUtensorMap* map);
 // Consumer variant for a group size: tensor cores (mma.sync) or CUDA cores.
 bool use_mma_consumer(int group, uint32_t flags);
 // Merge grid for a persistent decode grid of n_cta CTAs.

@@ -64,9 +64,10 @@ int scratch_address(int group, bool mma, uint8_t** out) {
       return PKD_E_CUDA;
     s.addr = static_cast<uint8_t*>(p);
   }
-  if (decode_prepare(group, mma, false, false, decode_smem_bytes(kMaxKvHeads, group, false)) !=
-      cudaSuccess)
-    return PKD_E_CUDA;
+  DecodeKind k;
+  k.group = group;
+  k.mma = mma;
+  if (decode_prepare(k, decode_smem_bytes(kMaxKvHeads, k)) != cudaSuccess) return PKD_E_CUDA;
   s.ready.fetch_or(bit, std::memory_order_release);
   *out = s.addr;
   return PKD_OK;
@@ -134,8 +135,11 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
   a.num_pages = cfg->num_pages;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cfg->head_dim));
   a.v_scale = 1.f;
-  if (launch_decode(group, mma, false, false, a, cfg->num_ctas, cfg->num_kv_heads,
-                    decode_smem_bytes(cfg->num_kv_heads, group, false), s) != cudaSuccess)
+  DecodeKind k;   // token-row producer
+  k.group = group;
+  k.mma = mma;
+  if (launch_decode(k, a, cfg->num_ctas, cfg->num_kv_heads, decode_smem_bytes(cfg->num_kv_heads, k),
+                    s) != cudaSuccess)
     return PKD_E_CUDA;
   MergeArgs m{};
   m.sched = a.sched;

@@ -39,7 +39,7 @@ import workloads  # noqa: E402
 
 METRIC = "decode-step KV throughput: achieved HBM GB/s (% of GB300 peak) and steps/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_kernel_llama8b_step.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_decode_host_gb300", "csrc", "decode_kernel.cu")
 
 
@@ -71,11 +71,12 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profile():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+def traffic_from_profile(workload):
+    """DRAM bytes per decode launch of this workload from the committed ncu
+    summary (profiles/decode_kernel_<workload>.md), if it was taken on the
+    current kernel source (else None)."""
     try:
-        with open(PROFILE_SUMMARY) as f:
+        with open(os.path.join(PROFILE_DIR, f"decode_kernel_{workload}.md")) as f:
             text = f.read()
         with open(KERNEL_SOURCE, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
@@ -204,7 +205,7 @@ def run_ours(args, rank, world):
     P = w.page_size
     lens = _lens(t, P)
     nnz = int(t["indptr"][-1])
-    layers = w.layers
+    layers = args.layers if args.layers > 0 else w.layers
     # distinct caches per replay for single-layer workloads so no step reads
     # another step's bytes out of L2
     copies = 1 if layers > 1 else max(1, int(np.ceil(
@@ -399,7 +400,7 @@ def run_ours(args, rank, world):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback",
             "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": traffic_from_profile() if args.workload == "llama8b_step" else None,
+            "traffic": traffic_from_profile(args.workload),
             "kernel": "decode_kernel", "launch_ms_mean": round(k1_mean_ms, 5),
             "launch_gbs_min": round(min(k1_gbs), 1) if k1_gbs else None,
             "launch_gbs_max": round(max(k1_gbs), 1) if k1_gbs else None,
@@ -664,6 +665,8 @@ def main():
                          "tensor-core (mma) folding of the GQA group")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers per step (0: the workload's own); smaller for profiling captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -941,7 +941,7 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
 //    consecutive output dims per block.
 // q is scaled per row into [-1, 1] (no f16 overflow whatever the bf16 range)
 // and the factor folded into the score scale; P is f16.  A stage holds 32
-// tokens (the same bytes as 16 bf16 tokens), processed as two 16-token tiles.
+// tokens (the same bytes as 16 bf16 tokens), folded in one softmax update.
 constexpr int kFp8Tokens = 32;
 
 __device__ __forceinline__ void mma_f16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0,
@@ -959,10 +959,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// two e4m3 (low byte first) -> f16x2
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_bytes, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four e4m3 bytes -> two f16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi); every
+// e4m3 value is exact in f16.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t r, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(r));
 }
 
 // Shared-memory addresses of KV head hk's ldmatrix rows in a 32-token e4m3
@@ -1023,6 +1026,96 @@ struct Fp8Frags {
     __syncwarp();
   }
 };
+
+// One stage folded into the running state: kNt 8-token N tiles (4: both
+// 16-token halves of the stage; 2: the first half only, when the stage holds
+// <= 16 tokens -- the second half was not copied).  The S accumulators form kNt
+// independent MMA chains; one softmax update and one rescale of O per stage.
+template <int kNt, bool kTiles>
+__device__ __forceinline__ void fp8_stage(const Fp8Frags<kTiles>& fr, uint32_t sbase, int n,
+                                          int tig, const uint32_t (&qa0)[8],
+                                          const uint32_t (&qa2)[8], float s_scale,
+                                          float (&oe)[8][2], float (&oo)[8][2], float& m_run,
+                                          float& l_run) {
+  // ---- S = Q K^T
+  float sc[kNt][2];
+#pragma unroll
+  for (int nt = 0; nt < kNt; ++nt) sc[nt][0] = sc[nt][1] = 0.f;
+#pragma unroll
+  for (int kq = 0; kq < 2; ++kq) {
+    uint32_t r[kNt][4];
+#pragma unroll
+    for (int nt = 0; nt < kNt; ++nt)
+      ldsm_x4(fr.kaddr(sbase, nt >> 1, nt & 1, kq), r[nt][0], r[nt][1], r[nt][2], r[nt][3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int nt = 0; nt < kNt; ++nt) {
+        uint32_t b0, b1;
+        e4m3x4_to_f16x2x2(r[nt][j], b0, b1);
+        mma_f16(sc[nt], qa0[kq * 4 + j], qa2[kq * 4 + j], b0, b1);
+      }
+    }
+  }
+  // ---- online softmax over this lane's 2 kNt scores (query head grp)
+  float mx = -CUDART_INF_F;
+#pragma unroll
+  for (int nt = 0; nt < kNt; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int tok = nt * 8 + 2 * tig + c;
+      sc[nt][c] = (tok < n) ? sc[nt][c] * s_scale : -CUDART_INF_F;
+      mx = fmaxf(mx, sc[nt][c]);
+    }
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+  const float alpha = exp2f(m_run - m_use);
+  float psum = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < kNt; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      sc[nt][c] = exp2f(sc[nt][c] - m_use);
+      psum += sc[nt][c];
+    }
+  l_run = l_run * alpha + psum;
+  m_run = m_new;
+  // P as A fragments, one pair per 16-token K step st
+  uint32_t pa0[kNt / 2], pa2[kNt / 2];
+#pragma unroll
+  for (int st = 0; st < kNt / 2; ++st) {
+    pa0[st] = pack_f16x2(sc[2 * st][0], sc[2 * st][1]);          // tokens 16 st + 2 tig, +1
+    pa2[st] = pack_f16x2(sc[2 * st + 1][0], sc[2 * st + 1][1]);  // 16 st + 8 + 2 tig, +1
+  }
+#pragma unroll
+  for (int vb = 0; vb < 8; ++vb) {
+    oe[vb][0] *= alpha;
+    oe[vb][1] *= alpha;
+    oo[vb][0] *= alpha;
+    oo[vb][1] *= alpha;
+  }
+  // ---- O += P V: per x4.trans, dim blocks 2 vp and 2 vp + 1
+#pragma unroll
+  for (int vp = 0; vp < 4; ++vp) {
+#pragma unroll
+    for (int st = 0; st < kNt / 2; ++st) {
+      uint32_t r[4];
+      ldsm_x4_t(fr.vaddr(sbase, st, vp), r[0], r[1], r[2], r[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int vb = 2 * vp + h;
+        // r[2h]: tokens 2 tig, 2 tig + 1; r[2h + 1]: tokens 8 + 2 tig, 9 + 2 tig
+        uint32_t e0, o0, e1, o1;
+        e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0u, 0x3120), e0, o0);
+        e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0u, 0x3120), e1, o1);
+        mma_f16(oe[vb], pa0[st], pa2[st], e0, e1);
+        mma_f16(oo[vb], pa0[st], pa2[st], o0, o1);
+      }
+    }
+  }
+}
 
 template <int G, bool kTiles>
 __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
@@ -1086,58 +1179,10 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
       const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
       if (n < T)
         fr.zero_v_tail(const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes, hk, lane, n);
-#pragma unroll
-      for (int st = 0; st < T / 16; ++st) {
-        if (st * 16 >= n) break;
-        // ---- S = Q K^T, two 8-token tiles
-        float sc[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          sc[nt][0] = sc[nt][1] = 0.f;
-#pragma unroll
-          for (int kq = 0; kq < 2; ++kq) {
-            uint32_t r[4];
-            ldsm_x4(fr.kaddr(sbase, st, nt, kq), r[0], r[1], r[2], r[3]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int kb = kq * 4 + j;
-              mma_f16(sc[nt], qa0[kb], qa2[kb], e4m3x2_to_f16x2(r[j] & 0xffffu),
-                      e4m3x2_to_f16x2(r[j] >> 16));
-            }
-          }
-        }
-        float s4[4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int tok = st * 16 + nt * 8 + 2 * tig + c;
-            s4[nt * 2 + c] = (tok < n) ? sc[nt][c] * s_scale : -CUDART_INF_F;
-          }
-        const float alpha = softmax_row(s4, m_run, l_run);
-        const uint32_t pa0 = pack_f16x2(s4[0], s4[1]);
-        const uint32_t pa2 = pack_f16x2(s4[2], s4[3]);
-        // ---- O = alpha O + P V: per x4.trans, dim blocks 2 vp and 2 vp + 1
-#pragma unroll
-        for (int vp = 0; vp < 4; ++vp) {
-          uint32_t r[4];
-          ldsm_x4_t(fr.vaddr(sbase, st, vp), r[0], r[1], r[2], r[3]);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int vb = 2 * vp + h;
-            // r[2h]: tokens 2 tig, 2 tig + 1; r[2h + 1]: tokens 8 + 2 tig, 9 + 2 tig
-            const uint32_t x0 = __byte_perm(r[2 * h], 0u, 0x3120);
-            const uint32_t x1 = __byte_perm(r[2 * h + 1], 0u, 0x3120);
-            oe[vb][0] *= alpha;
-            oe[vb][1] *= alpha;
-            oo[vb][0] *= alpha;
-            oo[vb][1] *= alpha;
-            mma_f16(oe[vb], pa0, pa2, e4m3x2_to_f16x2(x0 & 0xffffu),
-                    e4m3x2_to_f16x2(x1 & 0xffffu));
-            mma_f16(oo[vb], pa0, pa2, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
-          }
-        }
-      }
+      if (n > 16)
+        fp8_stage<4, kTiles>(fr, sbase, n, tig, qa0, qa2, s_scale, oe, oo, m_run, l_run);
+      else
+        fp8_stage<2, kTiles>(fr, sbase, n, tig, qa0, qa2, s_scale, oe, oo, m_run, l_run);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       ++stage;

@@ -236,6 +236,7 @@ def run_ours(args, rank, world):
                                                 num_pages=w.pool_pages,
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
+                                                chunk_rule=args.chunk_rule,
                                                 device=dev)
             _plan(d, gi, (ip, ix, la))
             decs.append(d)
@@ -390,6 +391,7 @@ def run_ours(args, rank, world):
             "total_tokens_per_layer": int(sum(lens)), "pages_per_layer": nnz,
             "alg_bytes_per_step": int(step_bytes),
             "consumer": args.consumer,
+            "chunk_rule": args.chunk_rule,
             "l2": "inputs larger than L2 (each layer's cache >= 0.49 GB, distinct per replay)",
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
                                           "makespan")},
@@ -665,6 +667,9 @@ def main():
                          "tensor-core (mma) folding of the GQA group")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk-rule", choices=["closed", "search"], default="closed",
+                    help="split chunk: closed-form work bound (default) or the largest chunk "
+                         "that still gives every CTA an item (binary search)")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per step (0: the workload's own); smaller for profiling captures")
     args = ap.parse_args()

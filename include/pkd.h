@@ -103,6 +103,14 @@ typedef struct pkd_config {
  * bulk copy.  This flag forces the token-row copies.  Combinable with every
  * other flag. */
 #define PKD_FLAG_ROW_COPIES 16u
+/* Chunk rule.  By default the split chunk is the closed-form work bound
+ * ceil(sum_i l_i / N_CTA) rounded up to whole pages (its half and quarter
+ * are tried too, the smallest predicted makespan wins).  With this flag the
+ * chunk is the largest page multiple, not below min_chunk_tokens, whose split
+ * still gives at least N_CTA work items (binary search; pyshine FlashInfer
+ * tour, "Planning on the Host, Executing on the Device", where the prefill
+ * planner searches the KV chunk this way). */
+#define PKD_FLAG_CHUNK_SEARCH 64u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;

@@ -55,7 +55,8 @@ def _load():
         lib.oracle_attend.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, p, i]
         lib.oracle_merge.argtypes = [p, p, p, p, i, i, p, p]
         d = ctypes.c_double
-        lib.oracle_attend_ex.argtypes = [p, p, i, d, d, p, p, p, i, i, i, i, i, i, p, i, p, p, i]
+        lib.oracle_attend_ex.argtypes = [p, p, i, i, d, d, p, p, p, i, i, i, i, i, i, p, i, p,
+                                         p, i]
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = d
         for f in (lib.oracle_lengths, lib.oracle_attend, lib.oracle_merge, lib.oracle_attend_ex):
@@ -95,39 +96,65 @@ def lengths(indptr, indices, last, page_size: int, num_pages: int) -> np.ndarray
     return out[:batch]
 
 
-def attend(q, kv, indptr, indices, last, rows, *, hq: int, hkv: int,
-           nthreads: int | None = None):
-    """Attention states for query rows.
+_LAYOUTS = {"NHD": 0, "HND": 1}
 
-    q: bf16 [B, Hq, D]; kv: bf16 [pages, 2, P, Hkv, D] (NHD).
-    rows: int array (n, 2) of (request, query head) -- the full KV range -- or
-    (n, 4) of (request, query head, t0, t1) for the partial state of tokens
-    [t0, t1).  Returns (out [n, D] float64, lse [n] float64, natural log).
-    """
-    lib = _load()
-    qb, kvb = _bits(q), _bits(kv)
-    B, hq_, D = qb.shape
-    pages, two, P, hkv_, D2 = kvb.shape
-    assert hq_ == hq and hkv_ == hkv and D2 == D and two == 2
+
+def _rows4(rows):
     rows = np.asarray(rows, dtype=np.int32)
     if rows.ndim == 1:
         rows = rows.reshape(-1, 2)
     if rows.shape[1] == 2:
         rows = np.concatenate([rows, np.zeros((rows.shape[0], 1), np.int32),
                                -np.ones((rows.shape[0], 1), np.int32)], axis=1)
-    rows = np.ascontiguousarray(rows)
+    return np.ascontiguousarray(rows)
+
+
+def _cache_dims(shape, layout):
+    """(pages, P, Hkv, D) of a cache shape in the given layout."""
+    if layout == "NHD":
+        pages, two, P, hkv, D = shape
+    elif layout == "HND":
+        pages, two, hkv, P, D = shape
+    else:
+        raise ValueError("layout must be 'NHD' or 'HND'")
+    assert two == 2
+    return pages, P, hkv, D
+
+
+def _attend(qb, kvb, kv_type, layout, k_scale, v_scale, indptr, indices, last, rows, hq, hkv,
+            nthreads):
+    lib = _load()
+    B, hq_, D = qb.shape
+    pages, P, hkv_, D2 = _cache_dims(kvb.shape, layout)
+    assert hq_ == hq and hkv_ == hkv and D2 == D
+    rows = _rows4(rows)
     n = rows.shape[0]
     out = np.zeros((max(n, 1), D), dtype=np.float64)
     lse = np.zeros(max(n, 1), dtype=np.float64)
     indptr, indices, last = _i32(indptr), _i32(indices), _i32(last)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    st = lib.oracle_attend(_ptr(qb), _ptr(kvb), _ptr(indptr), _ptr(indices),
-                           _ptr(last), B, hq, hkv, D, P, pages, _ptr(rows), n,
-                           _ptr(out), _ptr(lse), int(nthreads))
+    st = lib.oracle_attend_ex(_ptr(qb), _ptr(kvb), kv_type, _LAYOUTS[layout], float(k_scale),
+                              float(v_scale), _ptr(indptr), _ptr(indices), _ptr(last), B, hq,
+                              hkv, D, P, pages, _ptr(rows), n, _ptr(out), _ptr(lse),
+                              int(nthreads))
     if st != OK:
-        raise OracleError(f"oracle_attend: status {st}")
+        raise OracleError(f"oracle_attend_ex: status {st}")
     return out[:n], lse[:n]
+
+
+def attend(q, kv, indptr, indices, last, rows, *, hq: int, hkv: int,
+           nthreads: int | None = None, layout: str = "NHD"):
+    """Attention states for query rows.
+
+    q: bf16 [B, Hq, D]; kv: bf16 [pages, 2, P, Hkv, D] (NHD) or
+    [pages, 2, Hkv, P, D] (HND).
+    rows: int array (n, 2) of (request, query head) -- the full KV range -- or
+    (n, 4) of (request, query head, t0, t1) for the partial state of tokens
+    [t0, t1).  Returns (out [n, D] float64, lse [n] float64, natural log).
+    """
+    return _attend(_bits(q), _bits(kv), 0, layout, 1.0, 1.0, indptr, indices, last, rows, hq,
+                   hkv, nthreads)
 
 
 def e4m3_to_float(byte: int) -> float:
@@ -145,50 +172,29 @@ def _u8(t) -> np.ndarray:
 
 
 def attend_fp8(q, kv8, indptr, indices, last, rows, *, hq: int, hkv: int, k_scale: float,
-               v_scale: float, nthreads: int | None = None):
-    """attend() for an E4M3 cache with K / V scales (bytes [pages, 2, P, Hkv, D])."""
-    lib = _load()
-    qb, kvb = _bits(q), _u8(kv8)
-    B, hq_, D = qb.shape
-    pages, two, P, hkv_, D2 = kvb.shape
-    assert hq_ == hq and hkv_ == hkv and D2 == D and two == 2
-    rows = np.asarray(rows, dtype=np.int32)
-    if rows.ndim == 1:
-        rows = rows.reshape(-1, 2)
-    if rows.shape[1] == 2:
-        rows = np.concatenate([rows, np.zeros((rows.shape[0], 1), np.int32),
-                               -np.ones((rows.shape[0], 1), np.int32)], axis=1)
-    rows = np.ascontiguousarray(rows)
-    n = rows.shape[0]
-    out = np.zeros((max(n, 1), D), dtype=np.float64)
-    lse = np.zeros(max(n, 1), dtype=np.float64)
-    indptr, indices, last = _i32(indptr), _i32(indices), _i32(last)
-    if nthreads is None:
-        nthreads = os.cpu_count() or 1
-    st = lib.oracle_attend_ex(_ptr(qb), _ptr(kvb), 1, float(k_scale), float(v_scale), _ptr(indptr),
-                              _ptr(indices), _ptr(last), B, hq, hkv, D, P, pages, _ptr(rows), n,
-                              _ptr(out), _ptr(lse), int(nthreads))
-    if st != OK:
-        raise OracleError(f"oracle_attend_ex: status {st}")
-    return out[:n], lse[:n]
+               v_scale: float, nthreads: int | None = None, layout: str = "NHD"):
+    """attend() for an E4M3 cache with K / V scales (bytes, NHD or HND)."""
+    return _attend(_bits(q), _u8(kv8), 1, layout, k_scale, v_scale, indptr, indices, last, rows,
+                   hq, hkv, nthreads)
 
 
 def decode_fp8(q, kv8, indptr, indices, last, *, hq: int, hkv: int, k_scale: float,
-               v_scale: float, nthreads=None):
+               v_scale: float, nthreads=None, layout: str = "NHD"):
     """Full decode attention over an E4M3 cache: out [B, Hq, D], lse [B, Hq]."""
     B = int(np.asarray(last).shape[0])
     rows = np.array([(i, h) for i in range(B) for h in range(hq)], dtype=np.int32)
     out, lse = attend_fp8(q, kv8, indptr, indices, last, rows.reshape(-1, 2), hq=hq, hkv=hkv,
-                          k_scale=k_scale, v_scale=v_scale, nthreads=nthreads)
+                          k_scale=k_scale, v_scale=v_scale, nthreads=nthreads, layout=layout)
     return out.reshape(B, hq, -1), lse.reshape(B, hq)
 
 
-def decode(q, kv, indptr, indices, last, *, hq: int, hkv: int, nthreads=None):
+def decode(q, kv, indptr, indices, last, *, hq: int, hkv: int, nthreads=None,
+           layout: str = "NHD"):
     """Full decode attention: out [B, Hq, D] and lse [B, Hq] (float64)."""
     B = int(np.asarray(last).shape[0])
     rows = np.array([(i, h) for i in range(B) for h in range(hq)], dtype=np.int32)
     out, lse = attend(q, kv, indptr, indices, last, rows.reshape(-1, 2),
-                      hq=hq, hkv=hkv, nthreads=nthreads)
+                      hq=hq, hkv=hkv, nthreads=nthreads, layout=layout)
     D = out.shape[1] if out.size else (_bits(q).shape[2])
     return out.reshape(B, hq, D), lse.reshape(B, hq)
 

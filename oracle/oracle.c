@@ -36,6 +36,10 @@
  * "The block-sparse page table").  Query head h reads KV head h / g with
  * g = Hq / Hkv: consecutive query heads form a group (a reading; the pages
  * say a group of g query heads shares one KV head but not which ones).
+ * The HND layout (layout 1 of oracle_attend_ex) swaps the last three
+ * dimensions' first two: [pages][2][Hkv][P][D] ("FlashInfer 完全拆解",
+ * section 接口层最容易踩的四个坑: NHD and HND differ in the order of the last
+ * three dimensions); the same token, head and element are read.
  *
  * Inputs are the same bf16 bit patterns the GPU consumes, widened exactly to
  * double.  An FP8 cache (oracle_attend_ex, kv_type 1) holds E4M3 bytes --
@@ -96,6 +100,7 @@ typedef struct {
     const uint16_t *q;     /* [B][Hq][D] bf16 bits */
     const void *kv;        /* [pages][2][P][Hkv][D] bf16 bits or E4M3 bytes */
     int kv_type;           /* 0 bf16, 1 E4M3 */
+    int layout;            /* 0 NHD [pages][2][P][Hkv][D], 1 HND [pages][2][Hkv][P][D] */
     double k_scale, v_scale;
     const int32_t *indptr, *indices, *last;
     int batch, hq, hkv, d, p, num_pages;
@@ -111,8 +116,9 @@ typedef struct {
 /* Element c of the K (kv = 0) or V (kv = 1) row of a page slot, decoded and
  * scaled. */
 static double kv_elem(const job_t *j, int page, int kv, int slot, int kvh, int c) {
-    size_t off = ((((size_t)page * 2 + kv) * j->p + slot) * j->hkv + kvh) *
-                 (size_t)j->d + (size_t)c;
+    size_t off = j->layout == 0
+        ? ((((size_t)page * 2 + kv) * j->p + slot) * j->hkv + kvh) * (size_t)j->d + (size_t)c
+        : ((((size_t)page * 2 + kv) * j->hkv + kvh) * j->p + slot) * (size_t)j->d + (size_t)c;
     if (j->kv_type == 1) {
         double s = kv ? j->v_scale : j->k_scale;
         return s * oracle_e4m3_to_double(((const uint8_t *)j->kv)[off]);
@@ -195,10 +201,10 @@ static void *worker(void *arg) {
 /* Attention for a list of query rows (req, head, t0, t1).
  * q: [batch][hq][d] bf16 bits; kv: [num_pages][2][p][hkv][d] bf16 bits.
  * out: n_rows x d doubles; lse: n_rows doubles (natural log). */
-int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, double k_scale,
-                     double v_scale, const int32_t *indptr, const int32_t *indices,
-                     const int32_t *last, int batch, int hq, int hkv, int d, int p,
-                     int num_pages, const int32_t *rows, int n_rows, double *out,
+int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, int layout,
+                     double k_scale, double v_scale, const int32_t *indptr,
+                     const int32_t *indices, const int32_t *last, int batch, int hq, int hkv,
+                     int d, int p, int num_pages, const int32_t *rows, int n_rows, double *out,
                      double *lse, int nthreads);
 
 int oracle_attend(const uint16_t *q, const uint16_t *kv, const int32_t *indptr,
@@ -206,17 +212,19 @@ int oracle_attend(const uint16_t *q, const uint16_t *kv, const int32_t *indptr,
                   int hq, int hkv, int d, int p, int num_pages,
                   const int32_t *rows, int n_rows, double *out, double *lse,
                   int nthreads) {
-    return oracle_attend_ex(q, kv, 0, 1.0, 1.0, indptr, indices, last, batch, hq, hkv, d, p,
+    return oracle_attend_ex(q, kv, 0, 0, 1.0, 1.0, indptr, indices, last, batch, hq, hkv, d, p,
                             num_pages, rows, n_rows, out, lse, nthreads);
 }
 
-/* As oracle_attend, for a cache of kv_type (0 bf16, 1 E4M3) with scales. */
-int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, double k_scale,
-                     double v_scale, const int32_t *indptr, const int32_t *indices,
-                     const int32_t *last, int batch, int hq, int hkv, int d, int p,
-                     int num_pages, const int32_t *rows, int n_rows, double *out,
+/* As oracle_attend, for a cache of kv_type (0 bf16, 1 E4M3) with scales, in
+ * layout 0 (NHD) or 1 (HND). */
+int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, int layout,
+                     double k_scale, double v_scale, const int32_t *indptr,
+                     const int32_t *indices, const int32_t *last, int batch, int hq, int hkv,
+                     int d, int p, int num_pages, const int32_t *rows, int n_rows, double *out,
                      double *lse, int nthreads) {
     if (kv_type != 0 && kv_type != 1) return ORACLE_E_ARG;
+    if (layout != 0 && layout != 1) return ORACLE_E_ARG;
     if (hq < 1 || hkv < 1 || hq % hkv != 0 || d < 1 || p < 1) return ORACLE_E_ARG;
     int64_t *lens = (int64_t *)malloc(sizeof(int64_t) * (size_t)(batch > 0 ? batch : 1));
     if (!lens) return ORACLE_E_ARG;
@@ -229,7 +237,8 @@ int oracle_attend_ex(const uint16_t *q, const void *kv, int kv_type, double k_sc
     }
     job_t j;
     memset(&j, 0, sizeof j);
-    j.q = q; j.kv = kv; j.kv_type = kv_type; j.k_scale = k_scale; j.v_scale = v_scale;
+    j.q = q; j.kv = kv; j.kv_type = kv_type; j.layout = layout;
+    j.k_scale = k_scale; j.v_scale = v_scale;
     j.indptr = indptr; j.indices = indices; j.last = last;
     j.batch = batch; j.hq = hq; j.hkv = hkv; j.d = d; j.p = p;
     j.num_pages = num_pages; j.rows = rows; j.n_rows = n_rows;

@@ -21,6 +21,14 @@ P1  chunk size: with one query token per request and the GQA group folded
     section Split-KV 解决的是并行度).  Reading taken where the pages leave it
     open: the candidates L_kv, L_kv/2 and L_kv/4 are each scheduled and the
     one with the smallest predicted makespan wins (ties: the larger chunk).
+P1' chunk size by search (variant): the largest chunk that still fills the
+    GPU (pyshine FlashInfer tour, "Planning on the Host, Executing on the
+    Device", where the prefill planner binary-searches it).  Reading
+    taken: "fills the GPU" = the split gives at least N_CTA work items; the
+    chunk is a whole number of pages and never below the floor (the floor
+    when even it gives fewer items).  Stated here as a scan down from the
+    longest request; the library binary-searches the same predicate, which
+    only falls as the chunk grows.
 P2  split and cost: a request longer than the chunk becomes chunks
     [k c, min((k+1) c, l)); cost C = alpha * l_q + beta * l_kv with l_q = 1
     and beta = 1, so C = alpha + len (same section, the cost model).
@@ -132,9 +140,27 @@ def _lpt(items, n_cta):
     return queues, max(loads) if loads else 0
 
 
+def n_split_items(lens, chunk):
+    """Number of work items the split at ``chunk`` tokens gives."""
+    return sum(_ceil_div(l, chunk) for l in lens)
+
+
+def search_chunk(lens, *, page_size: int, n_cta: int, floor: int) -> int:
+    """P1': the largest multiple of the page size, not below ``floor`` (a page
+    multiple), whose split gives at least n_cta items; ``floor`` when none
+    does."""
+    top = max(_round_up(max(lens), page_size), floor) if lens else floor
+    c = top
+    while c > floor:
+        if n_split_items(lens, c) >= n_cta:
+            return c
+        c -= page_size
+    return floor
+
+
 def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
          alpha: int, min_chunk_tokens: int, chunk_divisors=(1, 2, 4), group_indptr=None,
-         rows: int = 1) -> Plan:
+         rows: int = 1, chunk_rule: str = "closed") -> Plan:
     """Schedule a decode step.  Without ``group_indptr`` the table has one row
     per request.  With it (a shared-prefix level, "FlashInfer 完全拆解",
     section Composable Format) the table has one row per group, requests
@@ -160,10 +186,15 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
     L = _ceil_div(W, n_cta)
     floor = _round_up(max(min_chunk_tokens, 1), P)
     cands = []
-    for k in chunk_divisors:
-        c = max(_round_up(_ceil_div(L, k), P), floor)
-        if c not in cands:
-            cands.append(c)
+    if chunk_rule == "search":
+        cands.append(search_chunk(lens, page_size=P, n_cta=n_cta, floor=floor))
+    elif chunk_rule == "closed":
+        for k in chunk_divisors:
+            c = max(_round_up(_ceil_div(L, k), P), floor)
+            if c not in cands:
+                cands.append(c)
+    else:
+        raise ValueError("chunk_rule must be 'closed' or 'search'")
     best = None
     for c in cands:
         queues, makespan = _lpt(_split(lens, c, alpha), n_cta)

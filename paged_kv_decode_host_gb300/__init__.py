@@ -166,6 +166,7 @@ FLAG_MMA_CONSUMER = 2   # fold it onto tensor cores (mma.sync, bf16 in / fp32 ac
 FLAG_SHARED_PREFIX = 4  # shared-prefix context: plans over groups of requests
 FLAG_KV_FP8 = 8         # E4M3 cache with per-call K / V scales
 FLAG_ROW_COPIES = 16    # force one KV copy per token row (no page-tile tensor map)
+FLAG_CHUNK_SEARCH = 64  # chunk = largest page multiple still giving >= N_CTA items
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -272,7 +273,7 @@ class BatchDecodeWithPagedKVCache:
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
                  use_tensor_cores=None, shared_prefix=False, kv_dtype="bf16", kv_layout="NHD",
-                 row_copies=False, device=None):
+                 row_copies=False, chunk_rule="closed", device=None):
         import torch
         if kv_layout != "NHD":
             raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
@@ -291,6 +292,10 @@ class BatchDecodeWithPagedKVCache:
             flags |= FLAG_KV_FP8
         if row_copies:
             flags |= FLAG_ROW_COPIES
+        if chunk_rule not in ("closed", "search"):
+            raise ValueError("chunk_rule must be 'closed' or 'search'")
+        if chunk_rule == "search":
+            flags |= FLAG_CHUNK_SEARCH
         self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch,
                                max_num_pages, num_pages, alpha, min_chunk_tokens, num_ctas, flags)
         with torch.cuda.device(self.device):

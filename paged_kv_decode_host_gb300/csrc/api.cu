@@ -61,7 +61,7 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 // the tensor-core consumer only.
 bool valid_flags(uint32_t f) {
   const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX |
-                         PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES;
+                         PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES | PKD_FLAG_CHUNK_SEARCH;
   if (f & ~known) return false;
   if ((f & PKD_FLAG_FMA_CONSUMER) &&
       (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8)))

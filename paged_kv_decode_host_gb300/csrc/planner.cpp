@@ -15,6 +15,10 @@
 //  * chunk = L_kv rounded up to whole pages and at least the split floor
 //    (short requests are not split); candidates L_kv, L_kv/2, L_kv/4 are each
 //    scheduled and the smallest predicted makespan wins (ties: larger chunk);
+//    with PKD_FLAG_CHUNK_SEARCH instead the largest page-multiple chunk (not
+//    below the floor) whose split still gives at least N_CTA items, found by
+//    binary search (pyshine FlashInfer tour, "Planning on the Host, Executing
+//    on the Device": the prefill planner's search, here applied to decode);
 //  * item cost alpha + tokens; items sorted by descending cost (ties: request,
 //    then chunk), each given to the least-loaded CTA (ties: lowest CTA id);
 //  * reduction map: split requests get contiguous partial slots in chunk
@@ -43,6 +47,35 @@ struct Item {
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Largest multiple of P, at least floor_c (itself a multiple of P), whose
+// split gives >= n_cta items; floor_c when none does.  The item count only
+// falls as the chunk grows, so the largest such chunk is a binary search
+// over whole pages.  Up to the longest request rounded up: beyond it nothing
+// splits.
+int64_t search_chunk(const std::vector<int64_t>& lens, int64_t n_cta, int64_t P, int64_t floor_c) {
+  int64_t max_l = 0;
+  for (int64_t l : lens) max_l = std::max(max_l, l);
+  auto fills = [&](int64_t pages) {
+    const int64_t c = pages * P;
+    int64_t n = 0;
+    for (int64_t l : lens) {
+      n += ceil_div(l, c);
+      if (n >= n_cta) return true;
+    }
+    return false;
+  };
+  int64_t lo = floor_c / P, hi = std::max(ceil_div(max_l, P), lo);
+  if (!fills(lo)) return floor_c;
+  while (lo < hi) {   // fills(lo) holds
+    const int64_t mid = lo + (hi - lo + 1) / 2;
+    if (fills(mid))
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo * P;
+}
 
 // Copy n page ids and check 0 <= id < num_pages, in one pass the compiler
 // can vectorise (no early exit).
@@ -201,9 +234,13 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   const int64_t floor_c = ceil_div(std::max<int64_t>(min_chunk, 1), P) * P;
   const int64_t work_bound = ceil_div(total, n_cta);
   std::vector<int64_t> cands;
-  for (int64_t k : {1, 2, 4}) {
-    int64_t c = std::max(ceil_div(ceil_div(work_bound, k), P) * P, floor_c);
-    if (std::find(cands.begin(), cands.end(), c) == cands.end()) cands.push_back(c);
+  if (cfg.flags & PKD_FLAG_CHUNK_SEARCH) {
+    cands.push_back(search_chunk(lens, n_cta, P, floor_c));
+  } else {
+    for (int64_t k : {1, 2, 4}) {
+      int64_t c = std::max(ceil_div(ceil_div(work_bound, k), P) * P, floor_c);
+      if (std::find(cands.begin(), cands.end(), c) == cands.end()) cands.push_back(c);
+    }
   }
   std::vector<Item> items, best_items, whole, rest;
   std::vector<int32_t> owner, best_owner;

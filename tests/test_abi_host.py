@@ -57,11 +57,11 @@ def test_config_validation(lib):
     ]
     for c in bad:
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -3
-    for bad_flags in (3, 5, 7, 9, 12, 28, 32, 0x80000000):
+    for bad_flags in (3, 5, 7, 9, 12, 28, 32, 128, 0x80000000):
         c = _cfg(16)
         c.flags = bad_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
-    for ok_flags in (0, 1, 2, 4, 6, 8, 10, 16, 17, 18, 20, 24):
+    for ok_flags in (0, 1, 2, 4, 6, 8, 10, 16, 17, 18, 20, 24, 64, 65, 66, 68, 72, 88):
         c = _cfg(16)
         c.flags = ok_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == 0
@@ -69,11 +69,12 @@ def test_config_validation(lib):
     assert list(off)[5] > list(off)[4] > list(off)[3] > list(off)[2] > list(off)[1] > list(off)[0]
 
 
-def _compare(cfg, indptr, indices, last, alpha, min_chunk):
+def _compare(cfg, indptr, indices, last, alpha, min_chunk, chunk_rule="closed"):
     words, info, off = pkd.plan_host(cfg, indptr, indices, last)
     got = pkd.decode_schedule(words, off, info)
     ref = oplan.plan(indptr, indices, last, page_size=cfg.page_size, num_pages=cfg.num_pages,
-                     n_cta=cfg.num_ctas, alpha=alpha, min_chunk_tokens=min_chunk)
+                     n_cta=cfg.num_ctas, alpha=alpha, min_chunk_tokens=min_chunk,
+                     chunk_rule=chunk_rule)
     assert info["chunk_tokens"] == ref.chunk
     assert info["makespan"] == ref.makespan
     assert info["num_items"] == ref.n_items
@@ -120,6 +121,38 @@ def test_plan_bit_exact_random(lib, seed):
                n_cta=n_cta, alpha=alpha, min_chunk=min_chunk)
     info = _compare(cfg, indptr, indices, last, alpha, min_chunk)
     assert info["batch"] == B
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_search_rule_plan_bit_exact_random(lib, seed):
+    """Binary-search chunk rule (PKD_FLAG_CHUNK_SEARCH) against the oracle's
+    scan, schedule word for word."""
+    rng = np.random.default_rng(300 + seed)
+    P = int(rng.choice([1, 3, 16, 32]))
+    B = int(rng.integers(0 if seed == 0 else 1, 300))
+    lens = rng.integers(1, 6000, B).tolist()
+    if seed % 3 == 1 and B:
+        lens[-1] = int(rng.integers(20000, 120000))
+    pool = sum(-(-l // P) for l in lens) + 7
+    indptr, indices, last = workloads.page_table(lens, P, rng.permutation(pool).astype(np.int32))
+    n_cta = int(rng.choice([1, 7, 64, 152, 304]))
+    alpha = int(rng.integers(0, 200))
+    min_chunk = int(rng.choice([1, 16, 256, 1000]))
+    cfg = _cfg(P, max_batch=max(B, 1), max_pages=max(int(indptr[-1]), 1), num_pages=pool,
+               n_cta=n_cta, alpha=alpha, min_chunk=min_chunk)
+    cfg.flags = pkd.FLAG_CHUNK_SEARCH
+    _compare(cfg, indptr, indices, last, alpha, min_chunk, chunk_rule="search")
+
+
+@pytest.mark.parametrize("name", ["llama8b_step", "skewed", "token_sparse"])
+def test_search_rule_plan_bit_exact_on_workloads(lib, name):
+    w = workloads.workload(name)
+    t = workloads.make_tables(w)
+    nnz = int(t["indptr"][-1])
+    cfg = _cfg(w.page_size, w.hq, w.hkv, max_batch=w.batch, max_pages=nnz,
+               num_pages=w.pool_pages, n_cta=152, alpha=32, min_chunk=256)
+    cfg.flags = pkd.FLAG_CHUNK_SEARCH
+    _compare(cfg, t["indptr"], t["indices"], t["last"], 32, 256, chunk_rule="search")
 
 
 def test_plan_host_rejects_bad_tables(lib):

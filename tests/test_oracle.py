@@ -133,6 +133,54 @@ def test_brute_force_dense(P, lens, hq, hkv):
     np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
 
 
+def _to_hnd(kv):
+    """[pages, 2, P, Hkv, D] -> [pages, 2, Hkv, P, D] by explicit element
+    moves (no library permute), for tiny caches."""
+    pages, two, P, hkv, D = kv.shape
+    out = torch.empty(pages, two, hkv, P, D, dtype=kv.dtype)
+    for pg in range(pages):
+        for c in range(two):
+            for s in range(P):
+                for h in range(hkv):
+                    out[pg, c, h, s, :] = kv[pg, c, s, h, :]
+    return out
+
+
+@pytest.mark.parametrize("P,lens,hq,hkv", [
+    (16, [37, 16, 5], 8, 2),
+    (4, [1, 9, 12, 3], 4, 4),
+    (3, [10, 3, 4], 6, 3),
+])
+def test_brute_force_dense_hnd(P, lens, hq, hkv):
+    """HND cache ("FlashInfer 完全拆解", 接口层最容易踩的四个坑: the last three
+    dimensions ordered head, token, dim): the oracle reading the HND copy
+    equals the dense reference gathered from the NHD original."""
+    w, t, q, kv = _tiny(17 + P, lens, P, hq, hkv)
+    ref_o, ref_l = _dense_reference(w, t, q, kv)
+    o, l = oracle.decode(q, _to_hnd(kv), t["indptr"], t["indices"], t["last"], hq=hq, hkv=hkv,
+                         layout="HND")
+    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+    # the same bytes read with the NHD strides give a different answer, so the
+    # check above does see the layout
+    if hkv > 1 and P > 1:
+        bad = _to_hnd(kv).reshape(kv.shape)
+        o2, _ = oracle.decode(q, bad, t["indptr"], t["indices"], t["last"], hq=hq, hkv=hkv)
+        assert np.abs(o2 - ref_o).max() > 1e-3
+
+
+def test_fp8_hnd_equals_nhd():
+    w, t, q, _ = _tiny(29, [33, 7, 50], 16, 8, 2)
+    kv8, scale = workloads.make_kv_fp8(w)
+    kv8 = kv8[0]
+    a = oracle.decode_fp8(q, kv8, t["indptr"], t["indices"], t["last"], hq=8, hkv=2,
+                          k_scale=scale, v_scale=2 * scale)
+    hnd = _to_hnd(kv8.view(torch.uint8)).view(torch.float8_e4m3fn)
+    b = oracle.decode_fp8(q, hnd, t["indptr"], t["indices"], t["last"], hq=8, hkv=2,
+                          k_scale=scale, v_scale=2 * scale, layout="HND")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 def test_peaky_scores_brute_force():
     w, t, q, kv = _tiny(3, [40, 17], 16, 4, 2, scale_q=8.0)
     ref_o, ref_l = _dense_reference(w, t, q, kv)
@@ -356,3 +404,61 @@ def test_grouped_plan_hand_worked():
     assert p.cta_indptr == [0, 1, 2, 3]
     assert p.items == [(0, 0, 40, -1, 0, 2, 0), (2, 0, 40, -1, 0, 2, 0), (4, 0, 40, -1, 0, 1, 0)]
     assert p.units == [] and p.merge_indptr == [0]
+
+
+# ---- chunk size by search (variant of P1)
+
+def test_search_chunk_hand_worked():
+    """lens [100, 50, 30], P 16, floor 16.  Items at chunk c: c=16 -> 7+4+2 =
+    13; c=32 -> 4+2+1 = 7; c=48 -> 3+2+1 = 6; c=64 -> 2+1+1 = 4; c=80, 96 ->
+    4; c=112 -> 3.  Need 8 items: 16.  Need 4: 96 (the largest with 4).
+    Need 3: 112 = the longest request rounded up (no split).  Need 14: even
+    the floor gives 13 -> the floor."""
+    lens = [100, 50, 30]
+    assert oplan.search_chunk(lens, page_size=16, n_cta=8, floor=16) == 16
+    assert oplan.search_chunk(lens, page_size=16, n_cta=4, floor=16) == 96
+    assert oplan.search_chunk(lens, page_size=16, n_cta=3, floor=16) == 112
+    assert oplan.search_chunk(lens, page_size=16, n_cta=14, floor=16) == 16
+    assert oplan.search_chunk(lens, page_size=16, n_cta=4, floor=256) == 256
+    assert oplan.search_chunk([], page_size=16, n_cta=4, floor=256) == 256
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_search_chunk_defining_property(seed):
+    """The chosen chunk c fills the GPU (>= n_cta items) and c + P does not,
+    unless c is the floor or the longest request (no split)."""
+    rng = np.random.default_rng(70 + seed)
+    P = int(rng.choice([1, 4, 16]))
+    lens = rng.integers(1, 5000, int(rng.integers(1, 60))).tolist()
+    n_cta = int(rng.choice([4, 37, 152]))
+    floor = P * int(rng.integers(1, 20))
+    c = oplan.search_chunk(lens, page_size=P, n_cta=n_cta, floor=floor)
+    assert c % P == 0 and c >= floor
+    top = max(-(-max(lens) // P) * P, floor)
+    if c == floor:
+        assert oplan.n_split_items(lens, c) < n_cta or c == top or \
+            oplan.n_split_items(lens, c + P) < n_cta
+    else:
+        assert oplan.n_split_items(lens, c) >= n_cta
+        assert c == top or oplan.n_split_items(lens, c + P) < n_cta
+    # brute force over every page multiple
+    ok = [k for k in range(floor, top + 1, P) if oplan.n_split_items(lens, k) >= n_cta]
+    assert c == (max(ok) if ok else floor)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_search_rule_plan_coverage(seed):
+    rng = np.random.default_rng(90 + seed)
+    P = int(rng.choice([1, 16]))
+    lens = rng.integers(1, 6000, int(rng.integers(1, 50))).tolist()
+    if seed % 2:
+        lens[-1] = 30000
+    pool = sum(-(-l // P) for l in lens) + 2
+    indptr, indices, last = workloads.page_table(lens, P, rng.permutation(pool).astype(np.int32))
+    n_cta = int(rng.choice([8, 152]))
+    p = oplan.plan(indptr, indices, last, page_size=P, num_pages=pool, n_cta=n_cta, alpha=32,
+                   min_chunk_tokens=256, chunk_rule="search")
+    coverage_check(p, indptr.tolist(), indices.tolist(), last.tolist(), P)
+    floor = -(-256 // P) * P
+    assert p.chunk == oplan.search_chunk(lens, page_size=P, n_cta=n_cta, floor=floor)
+    assert len(p.items) <= len(lens) + 4 * n_cta + 8

@@ -83,3 +83,34 @@ def test_out_of_range_tokens_skipped():
     changed = np.argwhere((out != _bits(kv)).any(axis=(-1, -2)))
     pages = {int(indices[indptr[1] + 19 // 16])}
     assert {int(c[0]) for c in changed} == pages
+
+
+def test_hnd_read_back_through_attention_oracle():
+    """HND cache: the appended rows read back through the attention oracle's
+    HND gather, and the HND result is the NHD result with head and slot
+    swapped."""
+    lens, P, hkv, D = [23, 9, 40], 4, 2, 16
+    indptr, indices, last, kv, g = _setup(lens, P, hkv=hkv, D=D, seed=5)
+    kv_hnd = kv.permute(0, 1, 3, 2, 4).contiguous()
+    batch_idx, pos = [0, 1, 2], [22, 3, 17]
+    n = len(batch_idx)
+    k_new = torch.randn(n, hkv, D, generator=g).to(torch.bfloat16)
+    v_new = torch.randn(n, hkv, D, generator=g).to(torch.bfloat16)
+    out_h, sk_h = oappend.append_kv(_bits(kv_hnd), _bits(k_new), _bits(v_new), batch_idx, pos,
+                                    indptr, indices, last, P, layout="HND")
+    out_n, sk_n = oappend.append_kv(_bits(kv), _bits(k_new), _bits(v_new), batch_idx, pos,
+                                    indptr, indices, last, P)
+    assert sk_h == sk_n == []
+    for pg in range(out_n.shape[0]):
+        for c in range(2):
+            for s in range(P):
+                for h in range(hkv):
+                    assert np.array_equal(out_h[pg, c, h, s], out_n[pg, c, s, h])
+    hq = 2 * hkv
+    q = torch.randn(len(lens), hq, D, generator=g).to(torch.bfloat16)
+    for i, (b, p) in enumerate(zip(batch_idx, pos)):
+        rows = [(b, h, p, p + 1) for h in range(hq)]
+        o, _ = oracle.attend(_bits(q), out_h, indptr, indices, last, rows, hq=hq, hkv=hkv,
+                             layout="HND")
+        for h in range(hq):
+            np.testing.assert_array_equal(o[h], v_new[i, h // 2].double().numpy())

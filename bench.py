@@ -233,6 +233,7 @@ def run_ours(args, rank, world):
                                                 max_num_pages=int(ip[-1]),
                                                 shared_prefix=gi is not None,
                                                 kv_dtype=w.kv_dtype,
+                                                kv_layout=w.kv_layout,
                                                 num_pages=w.pool_pages,
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
@@ -385,7 +386,8 @@ def run_ours(args, rank, world):
         "accum_dtype": "fp32",
         "data": "synthetic (seeded N(0,1) bf16 q/KV, seeded lengths and page permutation)",
         "config": {
-            "workload": args.workload, "kv_dtype": w.kv_dtype, "layers": layers,
+            "workload": args.workload, "kv_dtype": w.kv_dtype, "kv_layout": w.kv_layout,
+            "layers": layers,
             "batch": w.batch, "hq": w.hq,
             "hkv": w.hkv, "head_dim": w.head_dim, "page_size": P,
             "total_tokens_per_layer": int(sum(lens)), "pages_per_layer": nnz,
@@ -414,7 +416,7 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_cpu_baseline and w.kv_dtype == "bf16":
+    if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, t, qs, kvs, budget_s=args.cpu_seconds)
     return line
 
@@ -462,8 +464,13 @@ def _oracle_sample(w, t, q_bits, kv_bits, rows_req):
     import oracle
     rows = np.array([(i, h) for i in rows_req for h in range(w.hq)], dtype=np.int32)
     t0 = time.perf_counter()
-    oracle.attend(q_bits, kv_bits, t["indptr"], t["indices"], t["last"], rows,
-                  hq=w.hq, hkv=w.hkv)
+    if w.kv_dtype == "e4m3":
+        s = workloads.FP8_AMAX / 448.0
+        oracle.attend_fp8(q_bits, kv_bits, t["indptr"], t["indices"], t["last"], rows,
+                          hq=w.hq, hkv=w.hkv, k_scale=s, v_scale=s, layout=w.kv_layout)
+    else:
+        oracle.attend(q_bits, kv_bits, t["indptr"], t["indices"], t["last"], rows,
+                      hq=w.hq, hkv=w.hkv, layout=w.kv_layout)
     return time.perf_counter() - t0
 
 
@@ -471,11 +478,11 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
     """The fp64 oracle on the host cores, on a bounded sample of the same
     workload (requests of layer 0, all query heads), in the metric's unit."""
     import oracle
-    from oracle import _bits
+    from oracle import _bits, _u8
     oracle.build()
     if q_bits is None:
         q_bits = _bits(qs[0])
-        kv_bits = _bits(kvs[0])
+        kv_bits = _u8(kvs[0]) if w.kv_dtype == "e4m3" else _bits(kvs[0])
     lens = _lens(t, w.page_size)
     order = list(range(w.batch))
     # calibrate on one request; the sample is requests 0, 1, ... of layer 0,
@@ -491,7 +498,8 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
     secs = _oracle_sample(w, t, q_bits, kv_bits, sample)
     s_lens = [lens[i] for i in sample]
     bytes_ = alg_bytes_per_layer(
-        workloads.Workload("s", 0, w.hq, w.hkv, w.head_dim, w.page_size, 1, tuple(s_lens), 1),
+        workloads.Workload("s", 0, w.hq, w.hkv, w.head_dim, w.page_size, 1, tuple(s_lens), 1,
+                           kv_dtype=w.kv_dtype),
         s_lens, sum(-(-l // w.page_size) for l in s_lens))
     passes = len(sample) / w.batch
     return {"value": round(bytes_ / secs / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
@@ -616,11 +624,16 @@ def run_reference(args, rank, world):
         return run_reference_append(args, world)
     w = workloads.workload(args.workload)
     t = workloads.make_tables(w)
-    from oracle import _bits
+    from oracle import _bits, _u8
     q = workloads.make_q(w, device="cpu", layers=1)[0]
     # only the pages the sample touches need values; build the whole layer
-    kv = workloads.make_kv(w, device="cpu", layers=1)[0]
-    q_bits, kv_bits = _bits(q), _bits(kv)
+    if w.kv_dtype == "e4m3":
+        kv = workloads.make_kv_fp8(w, device="cpu", layers=1)[0][0]
+        kv_bits = _u8(kv)
+    else:
+        kv = workloads.make_kv(w, device="cpu", layers=1)[0]
+        kv_bits = _bits(kv)
+    q_bits = _bits(q)
     del kv
     per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     lens = _lens(t, w.page_size)
@@ -661,7 +674,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_step",
                     choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix",
-                             "llama8b_step_fp8", "append"])
+                             "llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd",
+                             "append"])
     ap.add_argument("--consumer", choices=["auto", "fma", "mma"], default="auto",
                     help="decode-kernel consumer: the default, or forced CUDA-core (fma) / "
                          "tensor-core (mma) folding of the GQA group")

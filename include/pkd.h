@@ -111,6 +111,14 @@ typedef struct pkd_config {
  * tour, "Planning on the Host, Executing on the Device", where the prefill
  * planner searches the KV chunk this way). */
 #define PKD_FLAG_CHUNK_SEARCH 64u
+/* HND cache layout: kv is [num_pages][2][Hkv][P][D] -- within a page, each KV
+ * head's P token rows are contiguous -- instead of NHD [num_pages][2][P][Hkv][D]
+ * ("FlashInfer 完全拆解", section 接口层最容易踩的四个坑: NHD and HND order the
+ * last three dimensions differently; low-precision KV may prefer HND).  Same
+ * results as NHD for the same values.  With page tiles (page size a multiple
+ * of 16) only the tensor map changes; token-row copies become one copy per
+ * token and KV head.  Combinable with every other flag. */
+#define PKD_FLAG_HND 32u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;
@@ -233,6 +241,18 @@ int pkd_append_kv(const void *k_new, const void *v_new, const int32_t *batch_ind
                   const int32_t *indices, const int32_t *last_page_len, int32_t batch,
                   void *kv, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
                   int32_t head_dim, int32_t *err, void *stream);
+
+/* pkd_append_kv for other caches.  flags: PKD_FLAG_HND (kv is
+ * [num_pages][2][Hkv][P][D]; the token's row of head h goes to
+ * kv[page][0 or 1][h][pos % P]) and/or PKD_FLAG_KV_FP8 (one byte per element:
+ * k_new, v_new and kv hold E4M3 bytes, copied as given -- quantising is the
+ * caller's).  head_dim * element bytes must be a multiple of 16.  Other flags:
+ * INVALID_ARG.  pkd_append_kv is this with flags 0. */
+int pkd_append_kv_ex(const void *k_new, const void *v_new, const int32_t *batch_indices,
+                     const int32_t *positions, int32_t n, const int32_t *indptr,
+                     const int32_t *indices, const int32_t *last_page_len, int32_t batch,
+                     void *kv, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                     int32_t head_dim, uint32_t flags, int32_t *err, void *stream);
 
 /* Read and clear the device error word (synchronizes `stream`).
  * *dev_err receives PKD_DEV_ERR_* bits (0 = none). */

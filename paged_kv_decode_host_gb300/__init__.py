@@ -47,7 +47,7 @@ EXPORTS = (
     "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
     "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
-    "pkd_append_kv", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
+    "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
 )
 
 
@@ -123,6 +123,8 @@ def load():
         "pkd_run_static_scratch": (ctypes.c_int, [cfgp, vp, sz, vp, vp, vp, vp, vp]),
         "pkd_append_kv": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
                                          i32, i32, vp, vp]),
+        "pkd_append_kv_ex": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
+                                            i32, i32, ctypes.c_uint32, vp, vp]),
         "pkd_plan_shared": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(u64)]),
         "pkd_plan_host_shared": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp, sz,
                                                 ctypes.POINTER(PlanInfo)]),
@@ -167,6 +169,7 @@ FLAG_SHARED_PREFIX = 4  # shared-prefix context: plans over groups of requests
 FLAG_KV_FP8 = 8         # E4M3 cache with per-call K / V scales
 FLAG_ROW_COPIES = 16    # force one KV copy per token row (no page-tile tensor map)
 FLAG_CHUNK_SEARCH = 64  # chunk = largest page multiple still giving >= N_CTA items
+FLAG_HND = 32           # cache layout [pages, 2, Hkv, P, D] instead of NHD [pages, 2, P, Hkv, D]
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -267,7 +270,8 @@ class BatchDecodeWithPagedKVCache:
 
     The workspace is one device tensor allocated here with torch (its size
     and layout come from the library) and kept at a fixed address for the
-    object's life.  bf16 only; KV layout NHD ``[pages, 2, P, Hkv, D]``.
+    object's life.  q / out bf16; KV bf16 or e4m3, layout NHD
+    ``[pages, 2, P, Hkv, D]`` or HND ``[pages, 2, Hkv, P, D]``.
     """
 
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
@@ -275,8 +279,10 @@ class BatchDecodeWithPagedKVCache:
                  use_tensor_cores=None, shared_prefix=False, kv_dtype="bf16", kv_layout="NHD",
                  row_copies=False, chunk_rule="closed", device=None):
         import torch
-        if kv_layout != "NHD":
-            raise ValueError("only the NHD layout [pages, 2, P, Hkv, D] is supported")
+        if kv_layout not in ("NHD", "HND"):
+            raise ValueError("kv_layout must be 'NHD' [pages, 2, P, Hkv, D] or "
+                             "'HND' [pages, 2, Hkv, P, D]")
+        self.kv_layout = kv_layout
         lib = load()
         self.device = torch.device("cuda" if device is None else device)
         self.hq, self.hkv, self.d, self.p = num_qo_heads, num_kv_heads, head_dim, page_size
@@ -292,6 +298,8 @@ class BatchDecodeWithPagedKVCache:
             flags |= FLAG_KV_FP8
         if row_copies:
             flags |= FLAG_ROW_COPIES
+        if kv_layout == "HND":
+            flags |= FLAG_HND
         if chunk_rule not in ("closed", "search"):
             raise ValueError("chunk_rule must be 'closed' or 'search'")
         if chunk_rule == "search":
@@ -385,9 +393,11 @@ class BatchDecodeWithPagedKVCache:
             raise ValueError(f"q shape {tuple(q.shape)} != planned {(B, self.hq, self.d)}")
         if tuple(out.shape) != (B, self.hq, self.d):
             raise ValueError(f"out shape {tuple(out.shape)} != {(B, self.hq, self.d)}")
-        if tuple(kv_cache.shape) != (self.num_pages, 2, self.p, self.hkv, self.d):
-            raise ValueError(f"kv_cache shape {tuple(kv_cache.shape)} is not NHD "
-                             f"{(self.num_pages, 2, self.p, self.hkv, self.d)}")
+        want = ((self.num_pages, 2, self.p, self.hkv, self.d) if self.kv_layout == "NHD" else
+                (self.num_pages, 2, self.hkv, self.p, self.d))
+        if tuple(kv_cache.shape) != want:
+            raise ValueError(f"kv_cache shape {tuple(kv_cache.shape)} is not "
+                             f"{self.kv_layout} {want}")
         if lse is not None:
             if lse.dtype != torch.float32 or tuple(lse.shape) != (B, self.hq) or not lse.is_contiguous():
                 raise ValueError("lse must be contiguous float32 [batch, Hq]")
@@ -474,28 +484,36 @@ def merge_states(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):
 
 
 def append_kv(k_new, v_new, batch_indices, positions, indptr, indices, last_page_len, kv_cache,
-              err=None, stream=None):
+              err=None, stream=None, kv_layout="NHD"):
     """append_paged_kv_cache: write new tokens' K / V rows into their page slots.
 
-    k_new, v_new: bf16 [n, Hkv, D]; batch_indices, positions: int32 [n]
-    (position = 0-based index of the token in its request after the append);
-    indptr / indices / last_page_len: int32 CUDA tensors, the table after the
-    append; kv_cache: bf16 NHD [pages, 2, P, Hkv, D], written in place.
+    k_new, v_new: [n, Hkv, D], the cache's dtype (bf16, or e4m3 bytes);
+    batch_indices, positions: int32 [n] (position = 0-based index of the
+    token in its request after the append); indptr / indices / last_page_len:
+    int32 CUDA tensors, the table after the append; kv_cache: NHD
+    [pages, 2, P, Hkv, D] or HND [pages, 2, Hkv, P, D], written in place.
     err: optional int32 CUDA tensor of one element; tokens outside the table
     are skipped and flagged there."""
     import torch
-    for name, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
-                        ("kv_cache", kv_cache, torch.bfloat16),
+    fp8 = kv_cache.dtype in (torch.float8_e4m3fn, torch.uint8)
+    kv_dt = kv_cache.dtype if fp8 else torch.bfloat16
+    for name, t, dt in (("k_new", k_new, kv_dt), ("v_new", v_new, kv_dt),
+                        ("kv_cache", kv_cache, kv_dt),
                         ("batch_indices", batch_indices, torch.int32),
                         ("positions", positions, torch.int32), ("indptr", indptr, torch.int32),
                         ("indices", indices, torch.int32),
                         ("last_page_len", last_page_len, torch.int32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if kv_layout not in ("NHD", "HND"):
+        raise ValueError("kv_layout must be 'NHD' or 'HND'")
     n = int(k_new.shape[0])
-    pages, two, P, hkv, D = kv_cache.shape
+    if kv_layout == "NHD":
+        pages, two, P, hkv, D = kv_cache.shape
+    else:
+        pages, two, hkv, P, D = kv_cache.shape
     if two != 2 or tuple(k_new.shape) != (n, hkv, D) or v_new.shape != k_new.shape:
-        raise ValueError("k_new / v_new must be [n, Hkv, D] matching the NHD cache")
+        raise ValueError(f"k_new / v_new must be [n, Hkv, D] matching the {kv_layout} cache")
     if batch_indices.numel() != n or positions.numel() != n:
         raise ValueError("batch_indices and positions need one entry per new token")
     batch = int(last_page_len.numel())
@@ -503,12 +521,13 @@ def append_kv(k_new, v_new, batch_indices, positions, indptr, indices, last_page
         raise ValueError("indptr must have batch + 1 entries")
     if err is not None and (err.dtype != torch.int32 or not err.is_cuda):
         raise TypeError("err must be an int32 CUDA tensor")
-    st = load().pkd_append_kv(
+    flags = (FLAG_HND if kv_layout == "HND" else 0) | (FLAG_KV_FP8 if fp8 else 0)
+    st = load().pkd_append_kv_ex(
         ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
         ctypes.c_void_p(batch_indices.data_ptr()), ctypes.c_void_p(positions.data_ptr()), n,
         ctypes.c_void_p(indptr.data_ptr()), ctypes.c_void_p(indices.data_ptr()),
         ctypes.c_void_p(last_page_len.data_ptr()), batch, ctypes.c_void_p(kv_cache.data_ptr()),
-        int(pages), int(P), int(hkv), int(D),
+        int(pages), int(P), int(hkv), int(D), flags,
         ctypes.c_void_p(err.data_ptr() if err is not None else 0), _stream_ptr(stream))
-    _check(st, "pkd_append_kv")
+    _check(st, "pkd_append_kv_ex")
     return kv_cache

@@ -61,7 +61,8 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 // the tensor-core consumer only.
 bool valid_flags(uint32_t f) {
   const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX |
-                         PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES | PKD_FLAG_CHUNK_SEARCH;
+                         PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES | PKD_FLAG_CHUNK_SEARCH |
+                         PKD_FLAG_HND;
   if (f & ~known) return false;
   if ((f & PKD_FLAG_FMA_CONSUMER) &&
       (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8)))
@@ -102,7 +103,7 @@ DecodeKind kind_for(const pkd_config* c, const void* probe_address) {
   if (k.tmap && probe_address != nullptr) {
     CUtensorMap m;
     k.tmap = encode_kv_map(probe_address, c->num_pages, c->page_size, c->num_kv_heads, k.fp8,
-                           &m) == cudaSuccess;
+                           (c->flags & PKD_FLAG_HND) != 0, &m) == cudaSuccess;
   }
   return k;
 }
@@ -137,8 +138,8 @@ int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out) {
   KvMapEntry e;
   e.kv = kv;
   const pkd_config& c = ctx->cfg;
-  if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8, &e.map) !=
-      cudaSuccess)
+  if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8,
+                    (c.flags & PKD_FLAG_HND) != 0, &e.map) != cudaSuccess)
     return PKD_E_CUDA;
   constexpr size_t kMaxMaps = 128;
   if (ctx->kv_maps.size() < kMaxMaps) {
@@ -175,6 +176,7 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.num_pages = c.num_pages;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim) * (double)k_scale);
   a.v_scale = v_scale;
+  a.hnd = (c.flags & PKD_FLAG_HND) ? 1 : 0;
   if (ctx->kind.tmap && kv != nullptr) {
     const int st = kv_map_for(ctx, kv, &a.kv_map);
     if (st != PKD_OK) return st;
@@ -429,8 +431,20 @@ int pkd_append_kv(const void* k_new, const void* v_new, const int32_t* batch_ind
                   const int32_t* indices, const int32_t* last_page_len, int32_t batch, void* kv,
                   int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
                   int32_t* err, void* stream) {
+  return pkd_append_kv_ex(k_new, v_new, batch_indices, positions, n, indptr, indices,
+                          last_page_len, batch, kv, num_pages, page_size, num_kv_heads, head_dim,
+                          0u, err, stream);
+}
+
+int pkd_append_kv_ex(const void* k_new, const void* v_new, const int32_t* batch_indices,
+                     const int32_t* positions, int32_t n, const int32_t* indptr,
+                     const int32_t* indices, const int32_t* last_page_len, int32_t batch,
+                     void* kv, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                     int32_t head_dim, uint32_t flags, int32_t* err, void* stream) {
+  if ((flags & ~(PKD_FLAG_HND | PKD_FLAG_KV_FP8)) != 0) return PKD_E_INVALID_ARG;
+  const int elem = (flags & PKD_FLAG_KV_FP8) ? 1 : 2;
   if (n < 0 || batch < 0 || num_pages < 1 || page_size < 1 || num_kv_heads < 1 ||
-      head_dim < 8 || head_dim % 8 != 0)
+      head_dim < 1 || ((int64_t)head_dim * elem) % 16 != 0)
     return PKD_E_INVALID_ARG;
   if (n == 0) return PKD_OK;
   if (!k_new || !v_new || !batch_indices || !positions || !indptr || !indices ||
@@ -438,10 +452,11 @@ int pkd_append_kv(const void* k_new, const void* v_new, const int32_t* batch_ind
     return PKD_E_INVALID_ARG;
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv, 16) || !aligned(err, 4))
     return PKD_E_INVALID_ARG;
-  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
-  if (row_bytes > (1 << 24)) return PKD_E_INVALID_ARG;
+  const int64_t head_bytes = (int64_t)head_dim * elem;
+  if (head_bytes * num_kv_heads > (1 << 24)) return PKD_E_INVALID_ARG;
   if (launch_append(k_new, v_new, batch_indices, positions, n, indptr, indices, last_page_len,
-                    batch, kv, num_pages, page_size, (int32_t)row_bytes, err,
+                    batch, kv, num_pages, page_size, num_kv_heads, (int32_t)head_bytes,
+                    (flags & PKD_FLAG_HND) != 0, err,
                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKD_E_CUDA;
   return PKD_OK;

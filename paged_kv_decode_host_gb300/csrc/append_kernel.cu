@@ -7,10 +7,12 @@
 // positions[i] (0-based within the request's length after the append); its
 // K row goes to cache[indices[indptr[b] + pos / P]][0][pos % P][:][:] and its
 // V row to [...][1][pos % P][:][:] (NHD, FlashInfer, in depth, "The
-// block-sparse page table").  One warp per token, 16-byte vector copies; the
-// table is read on the device.  A token whose request, position or page id
-// falls outside the table is skipped and flagged in the error word -- the
-// kernel never writes outside the cache.
+// block-sparse page table"); in the HND layout head h's part goes to
+// [page][0 or 1][h][pos % P][:] ("FlashInfer 完全拆解", 接口层最容易踩的四个坑).
+// One warp per token, 16-byte vector copies; the table is read on the device.
+// Elements are moved as bytes (bf16 or e4m3 alike).  A token whose request,
+// position or page id falls outside the table is skipped and flagged in the
+// error word -- the kernel never writes outside the cache.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,11 +28,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(
     const int32_t* __restrict__ batch_indices, const int32_t* __restrict__ positions, int32_t n,
     const int32_t* __restrict__ indptr, const int32_t* __restrict__ indices,
     const int32_t* __restrict__ last_page_len, int32_t batch, uint4* __restrict__ kv,
-    int32_t num_pages, int32_t page_size, int32_t row_chunks, int32_t* err) {
+    int32_t num_pages, int32_t page_size, int32_t hkv, int32_t head_chunks, int32_t hnd,
+    int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int64_t i = (int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   if (i >= n) return;
-  int64_t dst = -1;  // chunk index of the K row's first 16 bytes
+  int page = -1, slot = 0;
   if (lane == 0) {
     const int b = batch_indices[i];
     const int pos = positions[i];
@@ -39,21 +42,35 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(
       const int last = last_page_len[b];
       const int64_t len = (int64_t)page_size * (p1 - p0 - 1) + last;
       if (p1 > p0 && last >= 1 && last <= page_size && pos >= 0 && pos < len) {
-        const int page = indices[p0 + pos / page_size];
-        if (page >= 0 && page < num_pages)
-          dst = (((int64_t)page * 2) * page_size + pos % page_size) * row_chunks;
+        const int pg = indices[p0 + pos / page_size];
+        if (pg >= 0 && pg < num_pages) {
+          page = pg;
+          slot = pos % page_size;
+        }
       }
     }
-    if (dst < 0 && err != nullptr) atomicOr(err, PKD_DEV_ERR_BOUNDS);
+    if (page < 0 && err != nullptr) atomicOr(err, PKD_DEV_ERR_BOUNDS);
   }
-  dst = __shfl_sync(0xffffffffu, dst, 0);
-  if (dst < 0) return;
-  const int64_t v_off = (int64_t)page_size * row_chunks;  // V rows follow the P K rows
+  page = __shfl_sync(0xffffffffu, page, 0);
+  slot = __shfl_sync(0xffffffffu, slot, 0);
+  if (page < 0) return;
+  // in 16-byte chunks: a token row is hkv * head_chunks; one K (or V) page
+  // block is page_size rows
+  const int64_t row_chunks = (int64_t)hkv * head_chunks;
+  const int64_t kv_block = (int64_t)page_size * row_chunks;    // K -> V
+  const int64_t page_base = (int64_t)page * 2 * kv_block;
   const uint4* ks = k_new + i * row_chunks;
   const uint4* vs = v_new + i * row_chunks;
   for (int c = lane; c < row_chunks; c += 32) {
-    kv[dst + c] = ks[c];
-    kv[dst + v_off + c] = vs[c];
+    int64_t dst;
+    if (hnd) {
+      const int h = c / head_chunks, cc = c % head_chunks;
+      dst = page_base + ((int64_t)h * page_size + slot) * head_chunks + cc;
+    } else {
+      dst = page_base + (int64_t)slot * row_chunks + c;
+    }
+    kv[dst] = ks[c];
+    kv[dst + kv_block] = vs[c];
   }
 }
 
@@ -62,13 +79,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(
 cudaError_t launch_append(const void* k_new, const void* v_new, const int32_t* batch_indices,
                           const int32_t* positions, int32_t n, const int32_t* indptr,
                           const int32_t* indices, const int32_t* last_page_len, int32_t batch,
-                          void* kv, int32_t num_pages, int32_t page_size, int32_t row_bytes,
-                          int32_t* err, cudaStream_t stream) {
+                          void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
+                          int32_t head_bytes, bool hnd, int32_t* err, cudaStream_t stream) {
   const int64_t blocks = ((int64_t)n + kAppendWarps - 1) / kAppendWarps;
   append_kernel<<<(unsigned)blocks, kAppendWarps * 32, 0, stream>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), batch_indices,
       positions, n, indptr, indices, last_page_len, batch, static_cast<uint4*>(kv), num_pages,
-      page_size, row_bytes / 16, err);
+      page_size, hkv, head_bytes / 16, hnd ? 1 : 0, err);
   return cudaGetLastError();
 }
 

@@ -24,7 +24,11 @@
 //      - token rows (any page size): in the NHD layout one token row of all
 //        KV heads is contiguous, so each token costs one K-row and one V-row
 //        bulk copy (cp.async.bulk, 2 KiB each at 8 KV heads), landing at a
-//        padded row stride for the same reason.  Only valid rows are copied.
+//        padded row stride for the same reason (HND: one copy per token and
+//        KV head).  Only valid rows are copied.
+//    Both producers read either cache layout (NHD [pages][2][P][Hkv][D] or
+//    HND [pages][2][Hkv][P][D]) into the same shared-memory layout, so the
+//    consumers do not depend on it.
 //  * One consumer warp per KV head folds its GQA group of G query heads onto
 //    each K/V row it reads from shared memory (one read serves G heads).  The
 //    default consumer runs the group as a thin matrix on tensor cores
@@ -257,11 +261,23 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
           tensor_copy_g2s(st + (size_t)(c * kBoxes + (lane >> 1)) * box, &a.kv_map, 0, tok % P, 0,
                           0, 2 * page + c, &full[slot], policy);
         } else {
-          const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)(tok % P) * row;
           uint8_t* dk = st + (size_t)lane * rs;
-          bulk_copy_g2s(dk, src, (uint32_t)row, &full[slot], policy);
-          bulk_copy_g2s(dk + (size_t)kTokens * rs, src + (int64_t)P * row, (uint32_t)row,
-                        &full[slot], policy);
+          if (!a.hnd) {
+            const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)(tok % P) * row;
+            bulk_copy_g2s(dk, src, (uint32_t)row, &full[slot], policy);
+            bulk_copy_g2s(dk + (size_t)kTokens * rs, src + (int64_t)P * row, (uint32_t)row,
+                          &full[slot], policy);
+          } else {
+            // HND: the token's KV heads sit P rows of one head apart
+            const int hb = row / a.hkv;
+            const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)(tok % P) * hb;
+            for (int h = 0; h < a.hkv; ++h) {
+              const uint8_t* sk = src + (int64_t)h * P * hb;
+              bulk_copy_g2s(dk + h * hb, sk, (uint32_t)hb, &full[slot], policy);
+              bulk_copy_g2s(dk + (size_t)kTokens * rs + h * hb, sk + (int64_t)P * row,
+                            (uint32_t)hb, &full[slot], policy);
+            }
+          }
         }
       }
       ++stage;
@@ -1366,11 +1382,11 @@ cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, in
 
 // The map: dims (innermost first) {128-byte chunk of elements, token slot,
 // 128-byte half of a head, KV head, 2 * page + (0 K, 1 V)} with byte strides
-// {row, 128, D * E, P * row}; box {chunk, 16 tokens, all halves, all heads,
-// one K or V page}, which lands as [head][half][token][128 B] with the
-// 128-byte swizzle.
+// {row, 128, D * E, P * row} (NHD) or {D * E, 128, P * D * E, P * row} (HND);
+// box {chunk, 16 tokens, all halves, all heads, one K or V page}, which lands
+// as [head][half][token][128 B] with the 128-byte swizzle in either layout.
 cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
-                          bool fp8, CUtensorMap* map) {
+                          bool fp8, bool hnd, CUtensorMap* map) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -1390,7 +1406,9 @@ cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, 
   const cuuint64_t dims[5] = {(cuuint64_t)(128 / E), (cuuint64_t)page_size,
                               (cuuint64_t)(kHeadDim * E / 128), (cuuint64_t)hkv,
                               2 * (cuuint64_t)num_pages};
-  const cuuint64_t strides[4] = {row, 128, (cuuint64_t)(kHeadDim * E), (cuuint64_t)page_size * row};
+  const cuuint64_t head = (cuuint64_t)kHeadDim * E;
+  const cuuint64_t strides[4] = {hnd ? head : row, 128, hnd ? (cuuint64_t)page_size * head : head,
+                                 (cuuint64_t)page_size * row};
   const cuuint32_t box[5] = {(cuuint32_t)(128 / E), 16, (cuuint32_t)(kHeadDim * E / 128),
                              (cuuint32_t)hkv, 1};
   const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};

@@ -99,6 +99,7 @@ struct DecodeArgs {
   int32_t row_bytes;         // Hkv * D * element bytes: one token of one page, all heads
   float scale_log2;          // k_scale * log2(e) / sqrt(D)
   float v_scale;             // multiplies the output (1 for an unscaled cache)
+  int32_t hnd;               // 1: cache is HND [pages][2][Hkv][P][D] (else NHD)
   // Page-tile producer only: 5-D map over the cache (128-byte chunk, token
   // slot, 128-byte half of a head, KV head, 2 * page + {0 K, 1 V}) whose
   // 16-token box lands in shared memory with the 128-byte swizzle.
@@ -133,7 +134,7 @@ cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, in
                           int smem_bytes, cudaStream_t stream);
 // Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`.
 cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
-                          bool fp8, CUtensorMap* map);
+                          bool fp8, bool hnd, CUtensorMap* map);
 // Consumer variant for a group size: tensor cores (mma.sync) or CUDA cores.
 bool use_mma_consumer(int group, uint32_t flags);
 // Merge grid for a persistent decode grid of n_cta CTAs.
@@ -146,8 +147,8 @@ cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v
 cudaError_t launch_append(const void* k_new, const void* v_new, const int32_t* batch_indices,
                           const int32_t* positions, int32_t n, const int32_t* indptr,
                           const int32_t* indices, const int32_t* last_page_len, int32_t batch,
-                          void* kv, int32_t num_pages, int32_t page_size, int32_t row_bytes,
-                          int32_t* err, cudaStream_t stream);
+                          void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
+                          int32_t head_bytes, bool hnd, int32_t* err, cudaStream_t stream);
 
 // Host planner (planner.cpp).  Writes the schedule words into `words`.
 int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,

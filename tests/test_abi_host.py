@@ -57,11 +57,12 @@ def test_config_validation(lib):
     ]
     for c in bad:
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -3
-    for bad_flags in (3, 5, 7, 9, 12, 28, 32, 128, 0x80000000):
+    for bad_flags in (3, 5, 7, 9, 12, 28, 33 | 4 | 8, 128, 256, 0x80000000):
         c = _cfg(16)
         c.flags = bad_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
-    for ok_flags in (0, 1, 2, 4, 6, 8, 10, 16, 17, 18, 20, 24, 64, 65, 66, 68, 72, 88):
+    for ok_flags in (0, 1, 2, 4, 6, 8, 10, 16, 17, 18, 20, 24, 32, 33, 36, 40, 56, 64, 65, 66,
+                     68, 72, 88, 120):
         c = _cfg(16)
         c.flags = ok_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == 0

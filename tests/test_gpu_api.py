@@ -59,10 +59,16 @@ def test_dtype_shape_layout_mismatch():
     with pytest.raises(ValueError):
         dec.run(q[:2].contiguous(), kv)                   # batch differs from the plan
     with pytest.raises(ValueError):
-        dec.run(q, kv.transpose(2, 3).contiguous())       # HND-shaped cache
+        dec.run(q, kv.transpose(2, 3).contiguous())       # HND-shaped cache, NHD plan
     with pytest.raises(ValueError):
         pkd.BatchDecodeWithPagedKVCache(32, 8, 128, 16, max_batch=8, max_num_pages=32,
-                                        num_pages=64, kv_layout="HND")
+                                        num_pages=64, kv_layout="NDH")
+    hnd = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, w.page_size, max_batch=w.batch,
+                                          max_num_pages=int(t["indptr"][-1]),
+                                          num_pages=w.pool_pages, kv_layout="HND")
+    hnd.plan(t["indptr"], t["indices"], t["last"])
+    with pytest.raises(ValueError):
+        hnd.run(q, kv)                                    # NHD-shaped cache, HND plan
 
 
 def test_bad_tables_and_capacity():

@@ -19,7 +19,10 @@ Shapes and distributions follow the workloads named on the pages:
 * a shared prefix plus per-request suffixes
   ("FlashInfer 完全拆解", section "Composable Format");
 * page size 1, token-level sparse layout
-  ("FlashInfer, in depth", section "The block-sparse page table").
+  ("FlashInfer, in depth", section "The block-sparse page table");
+* the Llama-shaped step with an E4M3 cache, and either step with the cache in
+  the HND layout [pages, 2, Hkv, P, D] ("FlashInfer 完全拆解", section
+  接口层最容易踩的四个坑) -- the same values as the NHD cache, moved.
 
 Values are N(0, 1) in bf16.  Pages are placed by a seeded permutation of the
 pool, so consecutive logical pages are scattered in memory.
@@ -60,6 +63,7 @@ class Workload:
     prefix_tokens: int = 0  # shared-prefix workload only
     suffix_lens: tuple = field(default_factory=tuple)
     kv_dtype: str = "bf16"  # "bf16" or "e4m3" (FP8 cache with K / V scales)
+    kv_layout: str = "NHD"  # "NHD" [pages, 2, P, Hkv, D] or "HND" [pages, 2, Hkv, P, D]
 
     @property
     def kv_elem_bytes(self) -> int:
@@ -90,10 +94,11 @@ def workload(name: str) -> Workload:
         g = torch.Generator().manual_seed(2)
         lens = tuple(_randint(g, 1, 8192, 64))
         return Workload(name, 2, 32, 8, 128, 16, 32, lens, _pages_for(lens, 16))
-    if name == "llama8b_step_fp8":
+    if name in ("llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd"):
         w = workload("llama8b_step")
         return Workload(name, w.seed, w.hq, w.hkv, w.head_dim, w.page_size, w.layers, w.lens,
-                        w.pool_pages, kv_dtype="e4m3")
+                        w.pool_pages, kv_dtype="e4m3" if "fp8" in name else "bf16",
+                        kv_layout="HND" if name.endswith("hnd") else "NHD")
     if name == "skewed":
         g = torch.Generator().manual_seed(3)
         lens = tuple(_randint(g, 128, 512, 63) + [100_000])
@@ -115,7 +120,7 @@ def workload(name: str) -> Workload:
 
 WORKLOADS = ("worked_example", "llama8b_step", "skewed", "shared_prefix", "token_sparse")
 # the same Llama-shaped step over an E4M3 cache
-EXTRA_WORKLOADS = ("llama8b_step_fp8",)
+EXTRA_WORKLOADS = ("llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd")
 
 
 def page_table(kv_lens, page_size, page_ids=None):
@@ -203,17 +208,26 @@ def make_q(w: Workload, device="cpu", layers=None, seed_offset=0):
             for _ in range(layers)]
 
 
+def _layout(x, w: Workload):
+    """An NHD cache in the workload's layout (HND: heads before slots)."""
+    return x.permute(0, 1, 3, 2, 4).contiguous() if w.kv_layout == "HND" else x
+
+
 def make_kv(w: Workload, device="cpu", layers=None, seed_offset=0):
     """bf16 paged caches ~ N(0, 1): list (one per layer) of NHD tensors
-    [pool_pages, 2, P, Hkv, D] (K at index 0 of dim 1, V at index 1)."""
+    [pool_pages, 2, P, Hkv, D] (K at index 0 of dim 1, V at index 1), or the
+    same values as HND [pool_pages, 2, Hkv, P, D] for an HND workload."""
     layers = w.layers if layers is None else layers
     g = _generator(10_000 * w.seed + 29 + seed_offset, device)
     shape = (w.pool_pages, 2, w.page_size, w.hkv, w.head_dim)
-    return [torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device)
+    return [_layout(torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device), w)
             for _ in range(layers)]
 
 
-def make_kv_fp8(w: Workload, device="cpu", layers=None, seed_offset=0, amax=4.0):
+FP8_AMAX = 4.0   # N(0, 1) values are clipped to +-4 (the E4M3 maximum 448 after scaling)
+
+
+def make_kv_fp8(w: Workload, device="cpu", layers=None, seed_offset=0, amax=FP8_AMAX):
     """E4M3 paged caches (torch.float8_e4m3fn, NHD) holding N(0, 1) / scale
     values, scale = amax / 448 so that amax maps to the largest E4M3 value;
     returns (caches, scale) -- the attended K and V are scale * cache."""
@@ -224,7 +238,8 @@ def make_kv_fp8(w: Workload, device="cpu", layers=None, seed_offset=0, amax=4.0)
     caches = []
     for _ in range(layers):
         x = torch.randn(shape, generator=g, dtype=torch.bfloat16, device=device)
-        caches.append((x.float() / scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn))
+        caches.append(_layout((x.float() / scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn),
+                              w))
     return caches, scale
 
 

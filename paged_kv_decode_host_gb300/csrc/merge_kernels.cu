@@ -35,9 +35,13 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // merge_indptr[u] .. merge_indptr[u+1] into out / lse.
 // Block = 256 threads = 8 warps; blocks take (unit, head) tasks in a
 // grid-stride loop over a grid of 8 blocks per decode CTA, so every task of a
-// typical plan is in flight at once.  Warp w folds slots w, w + 8, ... with
-// the running-max recurrence (lane = 4 dims); the 8 warp states are then
-// combined in warp order.  Fixed assignment and order: bit-reproducible.
+// typical plan is in flight at once.  Two passes over the unit's slots: the
+// block first takes M = max L over all of them, then warp w sums
+// exp(L - M) O and exp(L - M) over slots w, w + 8, ... (lane = 4 dims) -- with
+// M known up front no term rescales the running sum, so a warp's loads are
+// independent and stay in flight together (a request split into hundreds of
+// chunks folds in a few memory latencies).  The 8 warp sums are added in warp
+// order.  Fixed assignment and order: bit-reproducible.
 __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
   constexpr int kWarps = kMergeThreads / 32;
   __shared__ float wm[kWarps];
@@ -60,43 +64,44 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
       pdl_wait();   // partial states and outputs belong to the decode kernel
       waited = true;
     }
-    float m = -CUDART_INF_F, z = 0.f;
+    // ---- pass 1: M = max over the unit's chunk LSEs (log2 units)
+    float mx = -CUDART_INF_F;
+    for (int s = s0 + threadIdx.x; s < s1; s += kMergeThreads)
+      mx = fmaxf(mx, a.l_part[(int64_t)s * a.hq + h] * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) wm[warp] = mx;
+    __syncthreads();
+    float m = wm[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, wm[w]);
+    // ---- pass 2: this warp's share of sum exp2(L - M) O and sum exp2(L - M)
+    float z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
     for (int s = s0 + warp; s < s1; s += kWarps) {
-      const float l2 = a.l_part[(int64_t)s * a.hq + h] * kLog2e;
+      const float w = exp2f(a.l_part[(int64_t)s * a.hq + h] * kLog2e - m);
       const float4 o = *reinterpret_cast<const float4*>(
           a.o_part + ((int64_t)s * a.hq + h) * kHeadDim + 4 * lane);
-      const float m_new = fmaxf(m, l2);
-      const float sc = exp2f(m - m_new);
-      const float w = exp2f(l2 - m_new);
-      acc.x = fmaf(w, o.x, acc.x * sc);
-      acc.y = fmaf(w, o.y, acc.y * sc);
-      acc.z = fmaf(w, o.z, acc.z * sc);
-      acc.w = fmaf(w, o.w, acc.w * sc);
-      z = fmaf(z, sc, w);
-      m = m_new;
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+      z += w;
     }
     *reinterpret_cast<float4*>(&wacc[warp][4 * lane]) = acc;
-    if (lane == 0) {
-      wm[warp] = m;
-      wz[warp] = z;
-    }
+    if (lane == 0) wz[warp] = z;
     __syncthreads();
     if (threadIdx.x < kHeadDim) {
-      float mm = wm[0];
-#pragma unroll
-      for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, wm[w]);
       float o = 0.f, zt = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float sc = exp2f(wm[w] - mm);   // 0 for a warp that saw no slot
-        o = fmaf(wacc[w][threadIdx.x], sc, o);
-        zt = fmaf(wz[w], sc, zt);
+        o += wacc[w][threadIdx.x];
+        zt += wz[w];
       }
       const int64_t qrow = (int64_t)req * a.hq + h;
       a.out[qrow * kHeadDim + threadIdx.x] = (uint16_t)f32_to_bf16_rne(o / zt);
-      if (threadIdx.x == 0 && a.lse != nullptr) a.lse[qrow] = (mm + log2f(zt)) * kLn2;
+      if (threadIdx.x == 0 && a.lse != nullptr) a.lse[qrow] = (m + log2f(zt)) * kLn2;
     }
     __syncthreads();
   }

@@ -176,7 +176,10 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.num_pages = c.num_pages;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim) * (double)k_scale);
   a.v_scale = v_scale;
-  a.hnd = (c.flags & PKD_FLAG_HND) ? 1 : 0;
+  // page size 1: HND and NHD are the same bytes, and a token's K and V rows
+  // are adjacent (one copy moves both)
+  a.hnd = ((c.flags & PKD_FLAG_HND) && c.page_size > 1) ? 1 : 0;
+  a.kv_merged = (c.page_size == 1 && !ctx->kind.tmap) ? 1 : 0;
   if (ctx->kind.tmap && kv != nullptr) {
     const int st = kv_map_for(ctx, kv, &a.kv_map);
     if (st != PKD_OK) return st;

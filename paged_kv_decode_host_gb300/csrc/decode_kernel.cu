@@ -155,6 +155,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // are conflict-free.
 __host__ __device__ __forceinline__ int row_stride(int row_bytes) { return row_bytes + 16; }
 
+// Token-row stage geometry: token t's K row at t * tok_stride and its V row
+// at v_base + t * tok_stride.  Separate copies: all K rows, then all V rows,
+// each at the padded row stride.  Merged copies (page size 1, where a
+// token's K and V rows are adjacent in the cache): [K row | V row] per token
+// at stride 2 row + 16, so one copy moves both.  Both strides are 16 bytes
+// past a multiple of 128: 8-row fragment loads stay conflict-free.
+__device__ __forceinline__ int rows_tok_stride(const DecodeArgs& a) {
+  return a.kv_merged ? 2 * a.row_bytes + 16 : row_stride(a.row_bytes);
+}
+__device__ __forceinline__ int rows_v_base(const DecodeArgs& a, int tokens) {
+  return a.kv_merged ? a.row_bytes : tokens * row_stride(a.row_bytes);
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // launch early, and wait for the previous kernel before touching its data.
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -214,7 +227,8 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
   constexpr int kBoxes = kTokens / 16;
   const int P = a.page_size;
   const int row = a.row_bytes;
-  const int rs = row_stride(row);
+  const int rs = rows_tok_stride(a);
+  const int vb = rows_v_base(a, kTokens);
   const uint32_t box = (uint32_t)(16 * row);
   const uint64_t policy = l2_evict_first_policy();
   bool waited = false;  // programmatic-launch wait, before the first KV read
@@ -262,11 +276,15 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
                           0, 2 * page + c, &full[slot], policy);
         } else {
           uint8_t* dk = st + (size_t)lane * rs;
-          if (!a.hnd) {
+          uint8_t* dv = st + vb + (size_t)lane * rs;
+          if (a.kv_merged) {
+            // page size 1: K row and V row back to back, one copy
+            bulk_copy_g2s(dk, a.kv + (int64_t)page * a.page_bytes, (uint32_t)(2 * row), &full[slot],
+                          policy);
+          } else if (!a.hnd) {
             const uint8_t* src = a.kv + (int64_t)page * a.page_bytes + (int64_t)(tok % P) * row;
             bulk_copy_g2s(dk, src, (uint32_t)row, &full[slot], policy);
-            bulk_copy_g2s(dk + (size_t)kTokens * rs, src + (int64_t)P * row, (uint32_t)row,
-                          &full[slot], policy);
+            bulk_copy_g2s(dv, src + (int64_t)P * row, (uint32_t)row, &full[slot], policy);
           } else {
             // HND: the token's KV heads sit P rows of one head apart
             const int hb = row / a.hkv;
@@ -274,8 +292,8 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
             for (int h = 0; h < a.hkv; ++h) {
               const uint8_t* sk = src + (int64_t)h * P * hb;
               bulk_copy_g2s(dk + h * hb, sk, (uint32_t)hb, &full[slot], policy);
-              bulk_copy_g2s(dk + (size_t)kTokens * rs + h * hb, sk + (int64_t)P * row,
-                            (uint32_t)hb, &full[slot], policy);
+              bulk_copy_g2s(dv + h * hb, sk + (int64_t)P * row, (uint32_t)hb, &full[slot],
+                            policy);
             }
           }
         }
@@ -318,7 +336,7 @@ __device__ void run_consumer_fma(const DecodeArgs& a, int it0, int it1, const ui
   const int hk = warp;
   const int hw = lane >> 4;
   const int li = lane & 15;
-  const int rs = row_stride(a.row_bytes);
+  const int rs = rows_tok_stride(a);
 
   // Which (head, step) values this lane holds after the reduce-scatter.
   int vbase = 0;
@@ -371,7 +389,7 @@ __device__ void run_consumer_fma(const DecodeArgs& a, int it0, int it1, const ui
         return;
       }
       const uint8_t* ks = stages + (size_t)slot * stage_bytes + hk * (kHeadDim * 2) + li * 16;
-      const uint8_t* vs = ks + (size_t)kTS * rs;
+      const uint8_t* vs = ks + rows_v_base(a, kTS);
 
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
@@ -561,16 +579,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // token 8 nt + L % 8, 16-byte chunk 4 kp + L / 8 of the head's 256 bytes.
 // V (transposed), for dim pair dp: token (L / 8 & 1) * 8 + L % 8, chunk
 // 2 dp + L / 16.
-//  * token rows: token t at t * rs (K rows, then V rows), head at hk * 256;
+//  * token rows: K row of token t at t * rs, V row at v_base + t * rs (see
+//    rows_tok_stride), head at hk * 256;
 //  * page tiles: K box at 0, V box at 16 * row_bytes; inside a box the
 //    128-byte line (2 hk + chunk / 8) * 16 + t holds the chunk at position
 //    (chunk % 8) ^ (t % 8).
 template <bool kTiles>
 struct Bf16Frags {
   uint32_t k, v, kx, vx;
-  int rs;
+  int rs, vz;   // token-row stride; V rows' base (token rows)
   __device__ __forceinline__ Bf16Frags(const DecodeArgs& a, int hk, int lane) {
-    rs = row_stride(a.row_bytes);
+    vz = 0;
+    rs = rows_tok_stride(a);
     const int r = lane & 7;
     if constexpr (kTiles) {
       k = (uint32_t)((hk * 32 + r) * 128);
@@ -579,9 +599,10 @@ struct Bf16Frags {
       vx = (uint32_t)(((lane >> 4) ^ r) << 4);
     } else {
       k = (uint32_t)(r * rs + hk * (kHeadDim * 2) + (lane >> 3) * 16);
-      v = (uint32_t)(kTS * rs + (((lane >> 3) & 1) * 8 + r) * rs + hk * (kHeadDim * 2) +
-                     (lane >> 4) * 16);
+      v = (uint32_t)(rows_v_base(a, kTS) + (((lane >> 3) & 1) * 8 + r) * rs +
+                     hk * (kHeadDim * 2) + (lane >> 4) * 16);
       kx = vx = 0;
+      vz = rows_v_base(a, kTS);
     }
   }
   __device__ __forceinline__ uint32_t kaddr(uint32_t sbase, int nt, int kp) const {
@@ -605,7 +626,7 @@ struct Bf16Frags {
       for (int r = n + (lane >> 4); r < kTS; r += 2)
         *reinterpret_cast<uint4*>(z + r * 128) = make_uint4(0, 0, 0, 0);
     } else {
-      uint8_t* z = stage + (size_t)kTS * rs + hk * (kHeadDim * 2) + (lane & 15) * 16;
+      uint8_t* z = stage + vz + hk * (kHeadDim * 2) + (lane & 15) * 16;
       for (int r = n + (lane >> 4); r < kTS; r += 2)
         *reinterpret_cast<uint4*>(z + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
     }
@@ -989,16 +1010,18 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t r, uint32_t& lo, uint
 // 16 st + 8 nt + L % 8, 16-byte chunk 4 kq + L / 8 of the head's 128 bytes.
 // V (trans), for x4 vp: token 16 st + (L / 8 & 1) * 8 + L % 8, chunk
 // 2 vp + L / 16.
-//  * token rows: token t at t * rs (K rows, then V rows), head at hk * 128;
+//  * token rows: K row of token t at t * rs, V row at v_base + t * rs (see
+//    rows_tok_stride), head at hk * 128;
 //  * page tiles: K box st at st * box, V box st at (2 + st) * box (box =
 //    16 * row_bytes); inside a box the line hk * 16 + t holds chunk c at
 //    position c ^ (t % 8).
 template <bool kTiles>
 struct Fp8Frags {
   uint32_t k, v, kx, vx, box;
-  int rs;
+  int rs, vz;   // token-row stride; V rows' base (token rows)
   __device__ __forceinline__ Fp8Frags(const DecodeArgs& a, int hk, int lane) {
-    rs = row_stride(a.row_bytes);
+    rs = rows_tok_stride(a);
+    vz = 0;
     box = (uint32_t)(16 * a.row_bytes);
     const int r = lane & 7;
     if constexpr (kTiles) {
@@ -1008,9 +1031,10 @@ struct Fp8Frags {
       vx = (uint32_t)(((lane >> 4) ^ r) << 4);
     } else {
       k = (uint32_t)(r * rs + hk * kHeadDim + (lane >> 3) * 16);
-      v = (uint32_t)(kFp8Tokens * rs + (((lane >> 3) & 1) * 8 + r) * rs + hk * kHeadDim +
-                     (lane >> 4) * 16);
+      v = (uint32_t)(rows_v_base(a, kFp8Tokens) + (((lane >> 3) & 1) * 8 + r) * rs +
+                     hk * kHeadDim + (lane >> 4) * 16);
       kx = vx = 0;
+      vz = rows_v_base(a, kFp8Tokens);
     }
   }
   __device__ __forceinline__ uint32_t kaddr(uint32_t sbase, int st, int nt, int kq) const {
@@ -1034,7 +1058,7 @@ struct Fp8Frags {
       for (int r = n + (lane >> 3); r < end; r += 4)
         *reinterpret_cast<uint4*>(z + (r >> 4) * box + (r & 15) * 128) = make_uint4(0, 0, 0, 0);
     } else {
-      uint8_t* z = stage + (size_t)kFp8Tokens * rs + hk * kHeadDim + (lane & 7) * 16;
+      uint8_t* z = stage + vz + hk * kHeadDim + (lane & 7) * 16;
       for (int r = n + (lane >> 3); r < kFp8Tokens; r += 4)
         *reinterpret_cast<uint4*>(z + (size_t)r * rs) = make_uint4(0, 0, 0, 0);
     }

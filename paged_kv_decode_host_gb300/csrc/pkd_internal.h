@@ -100,6 +100,8 @@ struct DecodeArgs {
   float scale_log2;          // k_scale * log2(e) / sqrt(D)
   float v_scale;             // multiplies the output (1 for an unscaled cache)
   int32_t hnd;               // 1: cache is HND [pages][2][Hkv][P][D] (else NHD)
+  int32_t kv_merged;         // token rows, page size 1: a token's K and V rows are adjacent
+                             // in the cache and move in one copy
   // Page-tile producer only: 5-D map over the cache (128-byte chunk, token
   // slot, 128-byte half of a head, KV head, 2 * page + {0 K, 1 V}) whose
   // 16-token box lands in shared memory with the 128-byte swizzle.

@@ -143,6 +143,8 @@ def _check(status, what):
 
 
 def _host_i32(a) -> np.ndarray:
+    if type(a) is np.ndarray and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a   # the common case, checked first: plan() runs every decode step
     try:
         import torch
         if isinstance(a, torch.Tensor):

@@ -123,31 +123,47 @@ void split_sorted(const std::vector<int64_t>& lens, int64_t chunk, int64_t alpha
 // Returns the makespan and the CTA of each item.  The CTA loads sit in a
 // flat binary min-heap keyed by (load, CTA id); giving an item to the top
 // CTA only grows its key, so one sift-down per item keeps the heap (the same
-// choice as pop + push, at half the work).
+// choice as pop + push, at half the work).  The leading run of equal-cost
+// items (the whole chunks) needs no heap: from equal loads, ties by CTA id
+// hand them out round-robin, so item j of the run goes to CTA j mod n_cta;
+// the heap is built once after it.  Keys are unique (CTA ids), so any valid
+// heap gives the same choices.
+void sift_down(std::pair<int64_t, int32_t>* h, size_t n, size_t i) {
+  const std::pair<int64_t, int32_t> v = h[i];
+  for (;;) {
+    size_t c = 2 * i + 1;
+    if (c >= n) break;
+    if (c + 1 < n && h[c + 1] < h[c]) ++c;
+    if (!(h[c] < v)) break;
+    h[i] = h[c];
+    i = c;
+  }
+  h[i] = v;
+}
+
 int64_t lpt(const std::vector<Item>& items, int32_t n_cta, std::vector<int32_t>* owner,
             std::vector<std::pair<int64_t, int32_t>>* heap) {
-  // all loads 0: the heap in CTA id order is already a valid min-heap
   heap->resize((size_t)n_cta);
   std::pair<int64_t, int32_t>* h = heap->data();
-  for (int32_t c = 0; c < n_cta; ++c) h[c] = std::make_pair((int64_t)0, c);
   owner->resize(items.size());
-  int64_t makespan = 0;
   const size_t n = (size_t)n_cta;
-  for (size_t idx = 0; idx < items.size(); ++idx) {
+  // leading equal-cost run: round-robin
+  size_t k = 0;
+  const int64_t w0 = items.empty() ? 0 : items[0].cost;
+  while (k < items.size() && items[k].cost == w0) {
+    (*owner)[k] = (int32_t)(k % n);
+    ++k;
+  }
+  const int64_t q = (int64_t)(k / n), r = (int64_t)(k % n);
+  for (int32_t c = 0; c < n_cta; ++c) h[c] = std::make_pair(w0 * (q + (c < r ? 1 : 0)), c);
+  int64_t makespan = w0 * (q + (r > 0 ? 1 : 0));
+  if (r > 0)   // loads are not all equal: order them into a heap
+    for (size_t i = n / 2; i-- > 0;) sift_down(h, n, i);
+  for (size_t idx = k; idx < items.size(); ++idx) {
     (*owner)[idx] = h[0].second;
     h[0].first += items[idx].cost;
     makespan = std::max(makespan, h[0].first);
-    size_t i = 0;
-    const std::pair<int64_t, int32_t> v = h[0];
-    for (;;) {
-      size_t c = 2 * i + 1;
-      if (c >= n) break;
-      if (c + 1 < n && h[c + 1] < h[c]) ++c;
-      if (!(h[c] < v)) break;
-      h[i] = h[c];
-      i = c;
-    }
-    h[i] = v;
+    sift_down(h, n, 0);
   }
   return makespan;
 }
@@ -247,6 +263,18 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   std::vector<std::pair<int64_t, int32_t>> heap;
   int64_t best_chunk = -1, best_span = 0;
   for (int64_t c : cands) {
+    if (best_chunk >= 0) {
+      // a later (smaller) candidate must beat the best makespan strictly;
+      // skip it when even its lower bound -- its costliest item, or its total
+      // cost spread evenly -- cannot
+      int64_t n_it = 0, top = 0;
+      for (int64_t l : lens) {
+        n_it += ceil_div(l, c);
+        top = std::max(top, std::min(l, c));
+      }
+      const int64_t lb = std::max(alpha + top, ceil_div(total + alpha * n_it, n_cta));
+      if (lb >= best_span) continue;
+    }
     split_sorted(lens, c, alpha, &whole, &rest, &items);
     int64_t span = lpt(items, n_cta, &owner, &heap);
     if (best_chunk < 0 || span < best_span) {

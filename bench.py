@@ -191,6 +191,44 @@ def _plan(d, group_indptr, table):
         d.plan_shared(group_indptr, *table)
 
 
+class _ComposedGraph:
+    """A torch CUDA graph of one shared-prefix step: the prefix level and the
+    suffix level (each a decode + merge through the C ABI) on two streams,
+    joined by merge_states."""
+
+    layers = 1
+
+    def __init__(self, g):
+        self.g = g
+
+    def launch(self):
+        self.g.replay()
+
+
+def _composed_step_graph(ds, q, kv, po, pl, so, sl, out, lse, side, dev):
+    import torch
+
+    import paged_kv_decode_host_gb300 as pkd
+    main = torch.cuda.Stream(device=dev)
+    # warm up outside the capture (plans are already published)
+    with torch.cuda.stream(main):
+        ds[0].run(q, kv, out=po, lse=pl)
+        ds[1].run(q, kv, out=so, lse=sl)
+        pkd.merge_states(po, pl, so, sl, out, lse)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        ds[0].run(q, kv, out=po, lse=pl)
+        with torch.cuda.stream(side):
+            ds[1].run(q, kv, out=so, lse=sl)
+        main.wait_stream(side)
+        pkd.merge_states(po, pl, so, sl, out, lse)
+    return _ComposedGraph(g)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -251,17 +289,23 @@ def run_ours(args, rank, world):
     graphs = [[] for _ in range(n_sets)]
     tgraphs = [[] for _ in range(n_sets)]
     if w.prefix_tokens:
-        # prefix run + suffix run + merge_states, per cache copy
+        # prefix run + suffix run + merge_states, per cache copy.  The step
+        # graph holds all three: the two levels are independent and run on
+        # two captured streams, merge_states joins them.  The timing graphs
+        # (event nodes around each decode launch) keep the levels apart.
         po = [torch.empty_like(qs[0]) for _ in range(copies)]
         pl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
         so = [torch.empty_like(qs[0]) for _ in range(copies)]
         sl = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in range(copies)]
+        side = torch.cuda.Stream(device=dev)
         for si, ds in enumerate(sets):
             for c in range(copies):
-                for timing, dst in ((False, graphs), (True, tgraphs)):
-                    gp = ds[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=timing)
-                    gs = ds[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=timing)
-                    dst[si].append((gp, gs, c))
+                gp = ds[0].capture([qs[0]], [kvs[c]], [po[c]], [pl[c]], timing=True)
+                gs = ds[1].capture([qs[0]], [kvs[c]], [so[c]], [sl[c]], timing=True)
+                tgraphs[si].append((gp, gs, c))
+                graphs[si].append((_composed_step_graph(ds, qs[0], kvs[c], po[c], pl[c], so[c],
+                                                        sl[c], outs[0], lses[0], side, dev),
+                                   None, c))
     else:
         for si, ds in enumerate(sets):
             for c in range(copies):
@@ -298,7 +342,7 @@ def run_ours(args, rank, world):
         stream.wait_event(copied[si])
         gp, gs, c = graph_of(k)
         gp.launch()
-        if gs is not None:
+        if gs is not None:   # timing graphs of the shared-prefix step
             gs.launch()
             pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
         if host:
@@ -367,8 +411,8 @@ def run_ours(args, rank, world):
     e2e = run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, dev)
 
     clocks = sampler.summary()
-    gp0, gs0, _ = graphs[0][0]
-    launches_per_step = 2 * gp0.layers + (2 * gs0.layers + 1 if gs0 is not None else 0)
+    gp0, _, _ = graphs[0][0]
+    launches_per_step = 5 if w.prefix_tokens else 2 * gp0.layers
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),

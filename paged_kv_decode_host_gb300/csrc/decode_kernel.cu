@@ -881,20 +881,33 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
       if (n < kTS)
         fr.zero_v_tail(const_cast<uint8_t*>(stages) + (size_t)slot * stage_bytes, a.row_bytes, hk,
                        lane, n);
-      float sc[2][4];
+      // S = Q K^T as four independent MMA chains (N tile x K-step parity),
+      // summed at the end: the tile is all 16 rows, so chain latency, not
+      // issue, bounds a single chain
+      float sc[2][4], sx[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sc[nt][c] = 0.f;
+        for (int c = 0; c < 4; ++c) sc[nt][c] = sx[nt][c] = 0.f;
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(fr.kaddr(sbase, nt, kp), b0, b1, b2, b3);
-          mma_bf16_full(sc[nt], qa0[2 * kp], qa1[2 * kp], qa2[2 * kp], qa3[2 * kp], b0, b1);
-          mma_bf16_full(sc[nt], qa0[2 * kp + 1], qa1[2 * kp + 1], qa2[2 * kp + 1],
-                        qa3[2 * kp + 1], b2, b3);
-        }
+      for (int kp = 0; kp < 4; ++kp) {
+        uint32_t b[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          ldsm_x4(fr.kaddr(sbase, nt, kp), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          mma_bf16_full(sc[nt], qa0[2 * kp], qa1[2 * kp], qa2[2 * kp], qa3[2 * kp], b[nt][0],
+                        b[nt][1]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          mma_bf16_full(sx[nt], qa0[2 * kp + 1], qa1[2 * kp + 1], qa2[2 * kp + 1],
+                        qa3[2 * kp + 1], b[nt][2], b[nt][3]);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[nt][c] += sx[nt][c];
       float s0[4], s1[4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)

@@ -310,6 +310,21 @@ int pkd_graph_capture(pkd_ctx *ctx, int32_t layers, const void *const *q,
                       const void *const *kv, void *const *out,
                       float *const *lse, const float *kv_scales, uint32_t flags,
                       pkd_graph **graph);
+/* pkd_graph_capture with the step's host I/O in the graph: q_host[l]
+ * (page-locked host memory, the layer's [batch][Hq][D] bf16 queries) is
+ * copied to q[l] before layer l runs, and out[l] / lse[l] are copied back to
+ * out_host[l] / lse_host[l] (page-locked) after it.  The copies run on their
+ * own captured streams: every layer's query copy may start when the graph
+ * starts, and each layer's results leave while later layers compute.  Any of
+ * q_host, out_host, lse_host may be NULL (no copy of that kind); lse_host
+ * needs lse.  Sizes come from the plan current at capture (its batch).
+ * Errors: INVALID_ARG, NO_PLAN, CUDA (also for host memory that is not
+ * page-locked). */
+int pkd_graph_capture_io(pkd_ctx *ctx, int32_t layers, const void *const *q,
+                         const void *const *kv, void *const *out, float *const *lse,
+                         const float *kv_scales, const void *const *q_host,
+                         void *const *out_host, float *const *lse_host, uint32_t flags,
+                         pkd_graph **graph);
 /* Launch the captured step on `stream`.  Errors: INVALID_ARG, CUDA. */
 int pkd_graph_launch(pkd_graph *graph, void *stream);
 /* After the launch has completed: decode-kernel milliseconds per layer

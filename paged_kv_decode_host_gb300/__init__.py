@@ -45,7 +45,7 @@ EXPORTS = (
     "pkd_workspace_bytes", "pkd_create", "pkd_destroy", "pkd_plan",
     "pkd_get_plan_info", "pkd_run", "pkd_merge_states", "pkd_last_device_error",
     "pkd_read_schedule", "pkd_plan_host", "pkd_schedule_layout",
-    "pkd_graph_capture", "pkd_graph_launch", "pkd_graph_layer_times",
+    "pkd_graph_capture", "pkd_graph_capture_io", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
     "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
 )
@@ -115,6 +115,8 @@ def load():
         "pkd_schedule_layout": (ctypes.c_int, [cfgp, vp]),
         "pkd_graph_capture": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, u32,
                                              ctypes.POINTER(vp)]),
+        "pkd_graph_capture_io": (ctypes.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, u32,
+                                                ctypes.POINTER(vp)]),
         "pkd_graph_launch": (ctypes.c_int, [vp, vp]),
         "pkd_graph_layer_times": (ctypes.c_int, [vp, vp]),
         "pkd_graph_destroy": (None, [vp]),
@@ -424,11 +426,28 @@ class BatchDecodeWithPagedKVCache:
         _check(st, "pkd_run")
         return (out, lse) if return_lse else out
 
-    def capture(self, qs, kvs, outs, lses=None, timing=False, kv_scales=None) -> Graph:
-        """Capture len(qs) runs (one decode step over all layers) in a graph."""
+    def capture(self, qs, kvs, outs, lses=None, timing=False, kv_scales=None, host_qs=None,
+                host_outs=None, host_lses=None) -> Graph:
+        """Capture len(qs) runs (one decode step over all layers) in a graph.
+        With host buffers (page-locked CPU tensors shaped like qs / outs /
+        lses) the graph also copies each layer's queries in from host_qs and
+        its results out to host_outs / host_lses, overlapped with the other
+        layers' kernels."""
+        import torch
         n = len(qs)
         for l in range(n):
             self._check_run_args(qs[l], kvs[l], outs[l], lses[l] if lses else None)
+        for name, hs, ds in (("host_qs", host_qs, qs), ("host_outs", host_outs, outs),
+                             ("host_lses", host_lses, lses)):
+            if hs is None:
+                continue
+            if ds is None or len(hs) != n:
+                raise ValueError(f"{name} needs one host tensor per layer (and the device side)")
+            for h, d in zip(hs, ds):
+                if (h.is_cuda or not h.is_pinned() or h.dtype != d.dtype or h.shape != d.shape
+                        or not h.is_contiguous()):
+                    raise ValueError(f"{name}: page-locked contiguous CPU tensors shaped and "
+                                     f"typed like the device buffers")
         P = ctypes.c_void_p * n
         q_arr = P(*[t.data_ptr() for t in qs])
         kv_arr = P(*[t.data_ptr() for t in kvs])
@@ -439,11 +458,14 @@ class BatchDecodeWithPagedKVCache:
         sc = None
         if kv_scales is not None:
             sc = (ctypes.c_float * (2 * n))(*[float(x) for pair in kv_scales for x in pair])
-        st = load().pkd_graph_capture(self._h, n, as_vp(q_arr), as_vp(kv_arr), as_vp(o_arr),
-                                      as_vp(l_arr), as_vp(sc),
-                                      GRAPH_TIMING if timing else 0, ctypes.byref(h))
-        _check(st, "pkd_graph_capture")
-        return Graph(self, h, n, (list(qs), list(kvs), list(outs), list(lses or [])))
+        host = [P(*[t.data_ptr() for t in hs]) if hs is not None else None
+                for hs in (host_qs, host_outs, host_lses)]
+        st = load().pkd_graph_capture_io(self._h, n, as_vp(q_arr), as_vp(kv_arr), as_vp(o_arr),
+                                         as_vp(l_arr), as_vp(sc), *[as_vp(a) for a in host],
+                                         GRAPH_TIMING if timing else 0, ctypes.byref(h))
+        _check(st, "pkd_graph_capture_io")
+        return Graph(self, h, n, (list(qs), list(kvs), list(outs), list(lses or []), host_qs,
+                                  host_outs, host_lses))
 
     def device_error(self, stream=None) -> int:
         v = ctypes.c_int32()

@@ -492,9 +492,19 @@ int pkd_read_schedule(pkd_ctx* ctx, int32_t* host_words, size_t max_words, void*
 int pkd_graph_capture(pkd_ctx* ctx, int32_t layers, const void* const* q, const void* const* kv,
                       void* const* out, float* const* lse, const float* kv_scales,
                       uint32_t flags, pkd_graph** graph) {
+  return pkd_graph_capture_io(ctx, layers, q, kv, out, lse, kv_scales, nullptr, nullptr, nullptr,
+                              flags, graph);
+}
+
+int pkd_graph_capture_io(pkd_ctx* ctx, int32_t layers, const void* const* q,
+                         const void* const* kv, void* const* out, float* const* lse,
+                         const float* kv_scales, const void* const* q_host,
+                         void* const* out_host, float* const* lse_host, uint32_t flags,
+                         pkd_graph** graph) {
   if (ctx == nullptr || graph == nullptr || layers < 1 || q == nullptr || kv == nullptr ||
       out == nullptr)
     return PKD_E_INVALID_ARG;
+  if (lse_host != nullptr && lse == nullptr) return PKD_E_INVALID_ARG;
   if ((flags & ~PKD_GRAPH_TIMING) != 0) return PKD_E_INVALID_ARG;
   *graph = nullptr;
   if (ctx->epoch == 0) return PKD_E_NO_PLAN;
@@ -502,7 +512,14 @@ int pkd_graph_capture(pkd_ctx* ctx, int32_t layers, const void* const* q, const 
     if (!q[l] || !kv[l] || !out[l] || !aligned(q[l], 16) || !aligned(kv[l], 16) ||
         !aligned(out[l], 16) || (lse && !aligned(lse[l], 4)))
       return PKD_E_INVALID_ARG;
+    if ((q_host && !q_host[l]) || (out_host && !out_host[l]) || (lse_host && !lse_host[l]))
+      return PKD_E_INVALID_ARG;
   }
+  const pkd_config& c = ctx->cfg;
+  const size_t rows = (size_t)ctx->info.batch * c.num_qo_heads;
+  const size_t q_bytes = rows * c.head_dim * 2, lse_bytes = rows * 4;
+  const bool copy_in = q_host != nullptr && rows > 0;
+  const bool copy_out = (out_host != nullptr || lse_host != nullptr) && rows > 0;
   pkd_graph* g = new (std::nothrow) pkd_graph();
   if (!g) return PKD_E_INVALID_ARG;
   g->ctx = ctx;
@@ -517,28 +534,83 @@ int pkd_graph_capture(pkd_ctx* ctx, int32_t layers, const void* const* q, const 
       }
     }
   }
-  cudaStream_t cs;
-  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
-    pkd_graph_destroy(g);
-    return PKD_E_CUDA;
-  }
+  // main capture stream, plus one stream for the query copies and one for
+  // the result copies (forked from the main stream, joined before the end);
+  // fork / join events exist only while capturing
+  cudaStream_t cs = nullptr, cin = nullptr, cout = nullptr;
+  std::vector<cudaEvent_t> evs;
+  auto new_event = [&evs]() -> cudaEvent_t {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    evs.push_back(e);
+    return e;
+  };
   int st = PKD_OK;
-  cudaGraph_t graph_def = nullptr;
-  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess ||
+      (copy_in && cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking) != cudaSuccess) ||
+      (copy_out && cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking) != cudaSuccess))
     st = PKD_E_CUDA;
-  } else {
+  cudaEvent_t fork = nullptr;
+  std::vector<cudaEvent_t> q_ready, done;
+  if (st == PKD_OK) {
+    fork = new_event();
+    for (int l = 0; l < layers; ++l) {
+      q_ready.push_back(copy_in ? new_event() : nullptr);
+      done.push_back(copy_out ? new_event() : nullptr);
+    }
+    if (!fork || (copy_in && !q_ready.back()) || (copy_out && !done.back())) st = PKD_E_CUDA;
+  }
+  cudaEvent_t in_end = st == PKD_OK && copy_in ? new_event() : nullptr;
+  cudaEvent_t out_end = st == PKD_OK && copy_out ? new_event() : nullptr;
+  if ((copy_in && !in_end) || (copy_out && !out_end)) st = PKD_E_CUDA;
+  cudaGraph_t graph_def = nullptr;
+  if (st == PKD_OK && cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    st = PKD_E_CUDA;
+  else if (st == PKD_OK) {
+    auto ok = [&st](cudaError_t e) {
+      if (e != cudaSuccess && st == PKD_OK) st = PKD_E_CUDA;
+      return st == PKD_OK;
+    };
+    ok(cudaEventRecord(fork, cs));
+    if (copy_in && ok(cudaStreamWaitEvent(cin, fork, 0))) {
+      for (int l = 0; l < layers && st == PKD_OK; ++l) {
+        // q[l] is the caller's device query buffer: the copy refills it
+        ok(cudaMemcpyAsync(const_cast<void*>(q[l]), q_host[l], q_bytes, cudaMemcpyHostToDevice,
+                           cin));
+        ok(cudaEventRecord(q_ready[l], cin));
+      }
+    }
+    if (copy_out) ok(cudaStreamWaitEvent(cout, fork, 0));
     for (int l = 0; l < layers && st == PKD_OK; ++l) {
+      if (copy_in && !ok(cudaStreamWaitEvent(cs, q_ready[l], 0))) break;
       const float ks = kv_scales ? kv_scales[2 * l] : 1.f;
       const float vs = kv_scales ? kv_scales[2 * l + 1] : 1.f;
-      st = launch_run(ctx, q[l], kv[l], out[l], lse ? lse[l] : nullptr, ks, vs, cs,
-                      timing ? g->ev[2 * l] : nullptr, timing ? g->ev[2 * l + 1] : nullptr);
+      const int r = launch_run(ctx, q[l], kv[l], out[l], lse ? lse[l] : nullptr, ks, vs, cs,
+                               timing ? g->ev[2 * l] : nullptr,
+                               timing ? g->ev[2 * l + 1] : nullptr);
+      if (r != PKD_OK) {
+        st = r;
+        break;
+      }
+      if (copy_out && ok(cudaEventRecord(done[l], cs)) &&
+          ok(cudaStreamWaitEvent(cout, done[l], 0))) {
+        if (out_host) ok(cudaMemcpyAsync(out_host[l], out[l], q_bytes, cudaMemcpyDeviceToHost, cout));
+        if (lse_host)
+          ok(cudaMemcpyAsync(lse_host[l], lse[l], lse_bytes, cudaMemcpyDeviceToHost, cout));
+      }
     }
+    // join the copy streams back into the main stream
+    if (copy_in && ok(cudaEventRecord(in_end, cin))) ok(cudaStreamWaitEvent(cs, in_end, 0));
+    if (copy_out && ok(cudaEventRecord(out_end, cout))) ok(cudaStreamWaitEvent(cs, out_end, 0));
     if (cudaStreamEndCapture(cs, &graph_def) != cudaSuccess && st == PKD_OK) st = PKD_E_CUDA;
   }
   if (st == PKD_OK && cudaGraphInstantiate(&g->exec, graph_def, 0) != cudaSuccess)
     st = PKD_E_CUDA;
   if (graph_def) cudaGraphDestroy(graph_def);
-  cudaStreamDestroy(cs);
+  for (cudaEvent_t e : evs) cudaEventDestroy(e);
+  if (cin) cudaStreamDestroy(cin);
+  if (cout) cudaStreamDestroy(cout);
+  if (cs) cudaStreamDestroy(cs);
   if (st != PKD_OK) {
     pkd_graph_destroy(g);
     return st;

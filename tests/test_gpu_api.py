@@ -122,3 +122,49 @@ def test_unsupported_shapes_rejected():
         with pytest.raises(pkd.PkdError):
             pkd.BatchDecodeWithPagedKVCache(hq, hkv, d, 16, max_batch=4, max_num_pages=8,
                                             num_pages=8)
+
+
+def test_graph_capture_with_host_io():
+    """pkd_graph_capture_io: the graph copies each layer's queries in from
+    page-locked host memory and its out / lse back; new host queries between
+    launches give the results of direct runs on them, bit for bit."""
+    layers = 3
+    w = workloads.Workload("io", 7, 32, 8, 128, 16, layers, (700, 37, 1500, 5), 200)
+    t = workloads.make_tables(w)
+    qs_host_src = workloads.make_q(w, device="cpu")
+    kvs = workloads.make_kv(w, device="cuda")
+    dec = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, 16, max_batch=w.batch,
+                                          max_num_pages=int(t["indptr"][-1]),
+                                          num_pages=w.pool_pages, num_ctas=9, alpha=0,
+                                          min_chunk_tokens=16)
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    assert dec.plan_info()["num_units"] >= 1           # split requests: the merge runs too
+    q_dev = [torch.zeros_like(x, device="cuda") for x in qs_host_src]
+    out_dev = [torch.empty_like(x) for x in q_dev]
+    lse_dev = [torch.empty(w.batch, w.hq, dtype=torch.float32, device="cuda") for _ in q_dev]
+    hq = [x.pin_memory() for x in qs_host_src]
+    ho = [torch.zeros(x.shape, dtype=x.dtype).pin_memory() for x in q_dev]
+    hl = [torch.zeros(w.batch, w.hq, dtype=torch.float32).pin_memory() for _ in q_dev]
+    with pytest.raises(ValueError):                       # host buffers must be page-locked
+        dec.capture(q_dev, kvs, out_dev, lse_dev, host_qs=[x.clone() for x in qs_host_src])
+    g = dec.capture(q_dev, kvs, out_dev, lse_dev, host_qs=hq, host_outs=ho, host_lses=hl)
+    for rnd in range(2):
+        if rnd == 1:                                      # new queries, same graph
+            for x in hq:
+                x.copy_((x.float() * -0.5).to(torch.bfloat16))
+        g.launch()
+        torch.cuda.synchronize()
+        for l in range(layers):
+            o, s = dec.run(hq[l].cuda(), kvs[l])
+            torch.cuda.synchronize()
+            assert torch.equal(ho[l], o.cpu()) and torch.equal(hl[l], s.cpu())
+    ref_o, ref_l = oracle_decode(hq[1], kvs[1], t, w)
+    assert np.abs(ho[1].double().numpy() - ref_o).max() <= 2e-2
+    assert np.abs(hl[1].double().numpy() - ref_l).max() <= 1e-3
+    g.close()
+    assert dec.device_error() == 0
+
+
+def oracle_decode(q, kv, t, w):
+    import oracle
+    return oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=w.hq, hkv=w.hkv)

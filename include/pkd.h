@@ -119,6 +119,17 @@ typedef struct pkd_config {
  * of 16) only the tensor map changes; token-row copies become one copy per
  * token and KV head.  Combinable with every other flag. */
 #define PKD_FLAG_HND 32u
+/* Dense shared-prefix kernel (with PKD_FLAG_SHARED_PREFIX; bf16 cache, page
+ * size a multiple of 16).  A shared prefix is a dense contraction: up to
+ * 128 / g requests of a group read the same pages, so their 128 query rows
+ * of one KV head form one 128-row tile ("FlashInfer 完全拆解", Composable
+ * Format).  Plans then cut groups into blocks of 128 / g requests and give
+ * every (block, KV head, chunk) its own work item; the kernel runs S = Q K^T
+ * and O += P V on the 5th-generation tensor cores (tcgen05.mma, accumulators
+ * in tensor memory), streaming the head's page tiles with TMA.  Not
+ * combinable with PKD_FLAG_FMA_CONSUMER, PKD_FLAG_KV_FP8 or
+ * PKD_FLAG_ROW_COPIES. */
+#define PKD_FLAG_DENSE_PREFIX 128u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;

@@ -101,6 +101,7 @@ class Plan:
     merge_indptr: list        # [n_units + 1]
     page_list: list           # the CSR page ids, as given
     lens: list                # per block (per request without grouping)
+    heads: list = None        # per item: its KV head (per-head plans), else 0
 
     @property
     def n_items(self):
@@ -160,13 +161,16 @@ def search_chunk(lens, *, page_size: int, n_cta: int, floor: int) -> int:
 
 def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
          alpha: int, min_chunk_tokens: int, chunk_divisors=(1, 2, 4), group_indptr=None,
-         rows: int = 1, chunk_rule: str = "closed") -> Plan:
+         rows: int = 1, chunk_rule: str = "closed", per_head: int = 1) -> Plan:
     """Schedule a decode step.  Without ``group_indptr`` the table has one row
     per request.  With it (a shared-prefix level, "FlashInfer 完全拆解",
     section Composable Format) the table has one row per group, requests
     group_indptr[j] .. group_indptr[j+1]-1 share group j's pages, and each
     group's requests are cut into blocks of ``rows`` consecutive requests; a
-    work item covers one block."""
+    work item covers one block.  With ``per_head`` = Hkv (the dense-prefix
+    kernel, whose tile is one KV head's rows of a block) the unit of work is
+    (block, KV head), units ordered block-major, and an item covers one
+    head of one block."""
     row_lens = lengths(indptr, last, indices, page_size, num_pages)
     P = page_size
     if group_indptr is None:
@@ -182,12 +186,14 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
             for r in range(gi[j], gi[j + 1], rows):
                 blocks.append((r, min(rows, gi[j + 1] - r), j))
     lens = [row_lens[b[2]] for b in blocks]
-    W = sum(lens)
+    # units of work: (block, head), block-major
+    ulens = [l for l in lens for _ in range(per_head)]
+    W = sum(ulens)
     L = _ceil_div(W, n_cta)
     floor = _round_up(max(min_chunk_tokens, 1), P)
     cands = []
     if chunk_rule == "search":
-        cands.append(search_chunk(lens, page_size=P, n_cta=n_cta, floor=floor))
+        cands.append(search_chunk(ulens, page_size=P, n_cta=n_cta, floor=floor))
     elif chunk_rule == "closed":
         for k in chunk_divisors:
             c = max(_round_up(_ceil_div(L, k), P), floor)
@@ -197,7 +203,7 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
         raise ValueError("chunk_rule must be 'closed' or 'search'")
     best = None
     for c in cands:
-        queues, makespan = _lpt(_split(lens, c, alpha), n_cta)
+        queues, makespan = _lpt(_split(ulens, c, alpha), n_cta)
         if best is None or makespan < best[1]:
             best = (c, makespan, queues)
     chunk, makespan, queues = best
@@ -217,9 +223,12 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
 
     cta_indptr = [0]
     items = []
+    heads = []
     indptr = [int(x) for x in indptr]
     for q in queues:
-        for cost, bi, k, tb, te in q:
+        for cost, u, k, tb, te in q:
+            bi, head = divmod(u, per_head)
+            heads.append(head)
             r0, n, row = blocks[bi]
             split = bi in block_slot
             dst = block_slot[bi] + k if split else -1
@@ -230,4 +239,4 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
         cta_indptr.append(len(items))
     page_list = [int(x) for x in indices[: indptr[-1] if indptr else 0]]
     return Plan(chunk, makespan, cta_indptr, items, units, merge_indptr,
-                page_list, lens)
+                page_list, lens, heads)

@@ -174,6 +174,7 @@ FLAG_KV_FP8 = 8         # E4M3 cache with per-call K / V scales
 FLAG_ROW_COPIES = 16    # force one KV copy per token row (no page-tile tensor map)
 FLAG_CHUNK_SEARCH = 64  # chunk = largest page multiple still giving >= N_CTA items
 FLAG_HND = 32           # cache layout [pages, 2, Hkv, P, D] instead of NHD [pages, 2, P, Hkv, D]
+FLAG_DENSE_PREFIX = 128  # shared prefix on tcgen05 tensor cores: 128-row tiles, one KV head per item
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -225,12 +226,13 @@ def decode_schedule(words, off, info):
     cta_indptr = words[off[0]:off[0] + n_cta + 1].tolist()
     it = words[off[1]:off[1] + 8 * n_items].reshape(n_items, 8)
     items = [tuple(int(x) for x in r[:7]) for r in it]
+    heads = [int(r[7]) for r in it]
     un = words[off[2]:off[2] + 2 * n_units].reshape(n_units, 2)
     units = [tuple(int(x) for x in r) for r in un]
     merge_indptr = words[off[3]:off[3] + n_units + 1].tolist()
     page_list = words[off[4]:off[4] + nnz].tolist()
     return dict(cta_indptr=cta_indptr, items=items, units=units, merge_indptr=merge_indptr,
-                page_list=page_list, header=words[:16].tolist())
+                page_list=page_list, header=words[:16].tolist(), heads=heads)
 
 
 def _stream_ptr(stream=None):

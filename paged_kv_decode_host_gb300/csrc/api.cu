@@ -62,12 +62,17 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 bool valid_flags(uint32_t f) {
   const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX |
                          PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES | PKD_FLAG_CHUNK_SEARCH |
-                         PKD_FLAG_HND;
+                         PKD_FLAG_HND | PKD_FLAG_DENSE_PREFIX;
   if (f & ~known) return false;
   if ((f & PKD_FLAG_FMA_CONSUMER) &&
       (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8)))
     return false;
   if ((f & PKD_FLAG_SHARED_PREFIX) && (f & PKD_FLAG_KV_FP8)) return false;
+  // the dense-prefix kernel: shared-prefix plans, tensor cores, bf16 page tiles
+  if ((f & PKD_FLAG_DENSE_PREFIX) &&
+      (!(f & PKD_FLAG_SHARED_PREFIX) ||
+       (f & (PKD_FLAG_FMA_CONSUMER | PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES))))
+    return false;
   return true;
 }
 

@@ -29,8 +29,10 @@ enum HeaderWord {
 };
 
 // req (first of the block), tok_begin, tok_end, dst_slot, first page index,
-// requests in the block, slot stride per request, 0
+// requests in the block, slot stride per request, KV head (dense-prefix
+// plans: one KV head per item; otherwise 0 and the item covers all heads)
 constexpr int kItemWords = 8;
+constexpr int kDenseRows = 128;   // query rows of one dense-prefix tile
 
 // Fixed word offsets of the schedule arrays, all derived from capacities.
 struct Layout {
@@ -59,12 +61,24 @@ inline int64_t max_items_for(int64_t max_batch, int64_t n_cta) {
   return max_batch + 4 * n_cta + 8;
 }
 
+// Requests per row block of a shared-prefix plan: the rows of one
+// tensor-core tile per KV head over g query heads (16 for the mma.sync
+// consumer, 128 for the dense-prefix kernel); 1 without grouping.
+inline int32_t block_rows(const pkd_config& c) {
+  if (!(c.flags & PKD_FLAG_SHARED_PREFIX)) return 1;
+  const int32_t g = c.num_qo_heads / c.num_kv_heads;
+  return ((c.flags & PKD_FLAG_DENSE_PREFIX) ? kDenseRows : 16) / g;
+}
+
 inline Layout make_layout(const pkd_config& c, int64_t n_cta) {
   Layout L{};
   L.max_items = max_items_for(c.max_batch, n_cta);
-  // a shared-prefix block of 16 / g requests writes one slot per request
-  L.max_slots = L.max_items * ((c.flags & PKD_FLAG_SHARED_PREFIX)
-                                   ? 16 / (c.num_qo_heads / c.num_kv_heads) : 1);
+  // a shared-prefix block writes one slot per request and chunk
+  L.max_slots = L.max_items * block_rows(c);
+  // dense-prefix plans give every KV head of a block its own items:
+  // items <= Hkv * blocks + 4 n_cta
+  if (c.flags & PKD_FLAG_DENSE_PREFIX)
+    L.max_items = (int64_t)c.num_kv_heads * c.max_batch + 4 * n_cta + 8;
   L.cta_indptr = H_WORDS;
   L.items = align_up(L.cta_indptr + n_cta + 1, 8);
   L.units = L.items + L.max_items * kItemWords;

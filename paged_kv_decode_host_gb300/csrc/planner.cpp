@@ -180,9 +180,12 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 // Row blocks: a block is a run of consecutive requests that attend over the
 // same pages (table row).  Without grouping every request is its own block;
 // with grouping (a shared prefix, FlashInfer 完全拆解, Composable Format) the
-// requests of a group are cut into blocks of `rows` = 16 / g requests, the
-// query rows one tensor-core tile holds per KV head, so one read of the
-// group's pages serves the whole block.
+// requests of a group are cut into blocks of `rows` requests -- the query
+// rows one tensor-core tile holds per KV head (16 / g for the mma.sync
+// consumer, 128 / g for the dense-prefix kernel) -- so one read of the
+// group's pages serves the whole block.  Dense-prefix plans split the work
+// of a block further by KV head: the unit of work is (block, head), and the
+// chunk bound, the split and LPT run over those units.
 int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
                           const int32_t* group_indptr, int32_t n_rows, const int32_t* indptr,
                           const int32_t* indices, const int32_t* last, int32_t* words,
@@ -192,7 +195,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   if (n_rows > 0 && (indptr == nullptr || last == nullptr)) return PKD_E_INVALID_ARG;
   const int64_t P = cfg.page_size;
   const int32_t group = cfg.num_qo_heads / cfg.num_kv_heads;
-  const int32_t rows = group_indptr ? 16 / group : 1;
+  const int32_t rows = group_indptr ? block_rows(cfg) : 1;
+  const int32_t heads = (group_indptr && (cfg.flags & PKD_FLAG_DENSE_PREFIX))
+                            ? cfg.num_kv_heads : 1;   // units per block
+  (void)group;
 
   // requests
   int32_t batch = n_rows;
@@ -241,8 +247,16 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     lens = row_len;
   }
   const int32_t n_blocks = (int32_t)blocks.size();
+  // work units: block-major, head-minor (unit u = block u / heads, head u % heads)
+  std::vector<int64_t> unit_lens;
+  if (heads > 1) {
+    unit_lens.reserve(lens.size() * heads);
+    for (int64_t l : lens)
+      for (int32_t hk = 0; hk < heads; ++hk) unit_lens.push_back(l);
+  }
+  const std::vector<int64_t>& ulens = heads > 1 ? unit_lens : lens;
   int64_t total = 0;
-  for (int64_t l : lens) total += l;
+  for (int64_t l : ulens) total += l;
 
   // ---- P1 + P2 + P3: chunk candidates, split, LPT; keep the best
   const int64_t alpha = cfg.alpha < 0 ? kDefaultAlpha : cfg.alpha;
@@ -251,7 +265,7 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   const int64_t work_bound = ceil_div(total, n_cta);
   std::vector<int64_t> cands;
   if (cfg.flags & PKD_FLAG_CHUNK_SEARCH) {
-    cands.push_back(search_chunk(lens, n_cta, P, floor_c));
+    cands.push_back(search_chunk(ulens, n_cta, P, floor_c));
   } else {
     for (int64_t k : {1, 2, 4}) {
       int64_t c = std::max(ceil_div(ceil_div(work_bound, k), P) * P, floor_c);
@@ -268,14 +282,14 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
       // skip it when even its lower bound -- its costliest item, or its total
       // cost spread evenly -- cannot
       int64_t n_it = 0, top = 0;
-      for (int64_t l : lens) {
+      for (int64_t l : ulens) {
         n_it += ceil_div(l, c);
         top = std::max(top, std::min(l, c));
       }
       const int64_t lb = std::max(alpha + top, ceil_div(total + alpha * n_it, n_cta));
       if (lb >= best_span) continue;
     }
-    split_sorted(lens, c, alpha, &whole, &rest, &items);
+    split_sorted(ulens, c, alpha, &whole, &rest, &items);
     int64_t span = lpt(items, n_cta, &owner, &heap);
     if (best_chunk < 0 || span < best_span) {
       best_chunk = c;
@@ -319,16 +333,17 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   int32_t* item_words = words + L.items;
   for (int64_t p = 0; p < n_items; ++p) {
     const Item& it = best_items[by_pos[p]];
-    const Block& bk = blocks[it.req];
+    const int32_t b = it.req / heads;   // it.req is the unit
+    const Block& bk = blocks[b];
     int32_t* w = item_words + p * kItemWords;
     w[0] = bk.req_first;
     w[1] = it.tok_begin;
     w[2] = it.tok_end;
-    w[3] = first_slot[it.req] >= 0 ? first_slot[it.req] + it.chunk_idx : -1;
+    w[3] = first_slot[b] >= 0 ? first_slot[b] + it.chunk_idx : -1;
     w[4] = (int32_t)(indptr[bk.table_row] + it.tok_begin / P);  // index of the first page
     w[5] = bk.n_req;
-    w[6] = first_slot[it.req] >= 0 ? n_chunks[it.req] : 0;     // slot stride per request
-    w[7] = 0;
+    w[6] = first_slot[b] >= 0 ? n_chunks[b] : 0;     // slot stride per request
+    w[7] = it.req % heads;                           // KV head (dense prefix), else 0
   }
   int32_t* unit_words = words + L.units;
   int32_t* merge_indptr = words + L.merge_indptr;
@@ -365,7 +380,9 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     info->num_items = (int32_t)n_items;
     info->num_units = (int32_t)units.size();
     info->num_slots = (int32_t)n_slots;
-    info->total_tokens = total;
+    int64_t tokens = 0;   // sum of the blocks' lengths (not per head)
+    for (int64_t l : lens) tokens += l;
+    info->total_tokens = tokens;
     info->makespan = best_span;
     info->nnz = (int32_t)nnz;
     info->schedule_words = (int32_t)(L.page_list + nnz);

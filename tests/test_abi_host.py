@@ -211,3 +211,51 @@ def test_grouped_plan_bit_exact_random(lib, seed):
     assert got["merge_indptr"] == ref.merge_indptr
     assert got["page_list"] == ref.page_list
     assert got["header"][15] == 16 // g
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_dense_prefix_plan_bit_exact_random(lib, seed):
+    """Dense-prefix plans (blocks of 128 / g requests, one KV head per work
+    item) against the oracle's per-head restatement, word for word; every
+    (request, head, token) covered exactly once."""
+    rng = np.random.default_rng(700 + seed)
+    P = int(rng.choice([16, 32, 64]))
+    hkv = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    n_groups = int(rng.integers(1, 4))
+    sizes = rng.integers(1, 300, n_groups).tolist()
+    group_indptr = np.array([0] + np.cumsum(sizes).tolist(), dtype=np.int32)
+    lens = rng.integers(1, 12000, n_groups).tolist()
+    pool = sum(-(-l // P) for l in lens) + 4
+    indptr, indices, last = workloads.page_table(lens, P, rng.permutation(pool).astype(np.int32))
+    n_cta = int(rng.choice([3, 64, 152]))
+    flags = pkd.FLAG_SHARED_PREFIX | pkd.FLAG_DENSE_PREFIX
+    rule = "closed"
+    if seed % 3 == 2:
+        flags |= pkd.FLAG_CHUNK_SEARCH
+        rule = "search"
+    cfg = pkd.make_config(g * hkv, hkv, 128, P, int(group_indptr[-1]), int(indptr[-1]), pool,
+                          32, 256, n_cta, flags)
+    words, info, off = pkd.plan_host_shared(cfg, group_indptr, indptr, indices, last)
+    got = pkd.decode_schedule(words, off, info)
+    ref = oplan.plan(indptr, indices, last, page_size=P, num_pages=pool, n_cta=n_cta, alpha=32,
+                     min_chunk_tokens=256, group_indptr=group_indptr, rows=128 // g,
+                     chunk_rule=rule, per_head=hkv)
+    assert info["chunk_tokens"] == ref.chunk and info["makespan"] == ref.makespan
+    assert got["cta_indptr"] == ref.cta_indptr
+    assert got["items"] == [tuple(x) for x in ref.items]
+    assert got["heads"] == ref.heads
+    assert got["units"] == [tuple(x) for x in ref.units]
+    assert got["merge_indptr"] == ref.merge_indptr
+    assert got["header"][15] == 128 // g
+    assert info["total_tokens"] == sum(ref.lens)
+    # coverage per head: each (request, head, token) exactly once
+    req_row = [j for j in range(len(lens)) for _ in range(sizes[j])]
+    seen = {}
+    for (r0, tb, te, dst, fp, n, stride), hd in zip(got["items"], got["heads"]):
+        assert 0 <= hd < hkv and n <= 128 // g
+        for r in range(r0, r0 + n):
+            a = seen.setdefault((r, hd), np.zeros(lens[req_row[r]], np.int32))
+            a[tb:te] += 1
+    assert len(seen) == len(req_row) * hkv
+    assert all(np.all(a == 1) for a in seen.values())

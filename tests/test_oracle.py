@@ -462,3 +462,19 @@ def test_search_rule_plan_coverage(seed):
     floor = -(-256 // P) * P
     assert p.chunk == oplan.search_chunk(lens, page_size=P, n_cta=n_cta, floor=floor)
     assert len(p.items) <= len(lens) + 4 * n_cta + 8
+
+
+def test_per_head_plan_hand_worked():
+    """Dense-prefix (per-head) plan: one group of 3 requests sharing 40 tokens
+    (P 16), Hkv 2, 2 CTAs, alpha 0, floor 16, blocks of 32 requests.  Units
+    (block 0, head 0) and (block 0, head 1), 40 tokens each: W = 80, L = 40 ->
+    chunk 48: one 40-token item per unit, one per CTA (makespan 40); the
+    chunks 32 and 16 also give 40 (ties keep the larger chunk)."""
+    indptr, indices, last = workloads.page_table([40], 16)
+    p = oplan.plan(indptr, indices, last, page_size=16, num_pages=3, n_cta=2, alpha=0,
+                   min_chunk_tokens=16, group_indptr=[0, 3], rows=32, per_head=2)
+    assert p.chunk == 48 and p.makespan == 40
+    assert p.cta_indptr == [0, 1, 2]
+    assert p.items == [(0, 0, 40, -1, 0, 3, 0), (0, 0, 40, -1, 0, 3, 0)]
+    assert p.heads == [0, 1]
+    assert p.units == [] and p.merge_indptr == [0]

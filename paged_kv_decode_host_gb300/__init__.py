@@ -283,7 +283,7 @@ class BatchDecodeWithPagedKVCache:
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
                  use_tensor_cores=None, shared_prefix=False, kv_dtype="bf16", kv_layout="NHD",
-                 row_copies=False, chunk_rule="closed", device=None):
+                 row_copies=False, chunk_rule="closed", dense_prefix=False, device=None):
         import torch
         if kv_layout not in ("NHD", "HND"):
             raise ValueError("kv_layout must be 'NHD' [pages, 2, P, Hkv, D] or "
@@ -306,6 +306,10 @@ class BatchDecodeWithPagedKVCache:
             flags |= FLAG_ROW_COPIES
         if kv_layout == "HND":
             flags |= FLAG_HND
+        if dense_prefix:
+            if not shared_prefix:
+                raise ValueError("dense_prefix needs shared_prefix=True")
+            flags |= FLAG_DENSE_PREFIX
         if chunk_rule not in ("closed", "search"):
             raise ValueError("chunk_rule must be 'closed' or 'search'")
         if chunk_rule == "search":

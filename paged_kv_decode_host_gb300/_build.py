@@ -17,8 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkd.so")
-SOURCES = ["planner.cpp", "api.cu", "decode_kernel.cu", "merge_kernels.cu",
-           "static_scratch.cu", "append_kernel.cu"]
+SOURCES = ["planner.cpp", "api.cu", "decode_kernel.cu", "prefix_tc_kernel.cu",
+           "merge_kernels.cu", "static_scratch.cu", "append_kernel.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

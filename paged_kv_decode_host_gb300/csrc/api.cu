@@ -49,6 +49,7 @@ struct pkd_ctx {
 struct pkd_graph {
   pkd_ctx* ctx = nullptr;
   int32_t layers = 0;
+  int32_t batch = 0;   // the plan's batch at capture (dense-prefix graphs hold q maps of it)
   cudaGraphExec_t exec = nullptr;
   std::vector<cudaEvent_t> ev;  // [2 * layers] when timing
 };
@@ -87,6 +88,9 @@ int check_config(const pkd_config* c) {
   if (c->num_qo_heads < 1 || c->num_qo_heads % c->num_kv_heads != 0)
     return PKD_E_UNSUPPORTED_SHAPE;
   if (!valid_group(c->num_qo_heads / c->num_kv_heads)) return PKD_E_UNSUPPORTED_SHAPE;
+  // the dense-prefix kernel reads 16-token page tiles
+  if ((c->flags & PKD_FLAG_DENSE_PREFIX) && c->page_size % 16 != 0)
+    return PKD_E_UNSUPPORTED_SHAPE;
   // a page must fit the copy-size and tx-count limits of one stage
   if ((int64_t)c->page_size * c->num_kv_heads * kHeadDim * 2 * 2 > (int64_t)1 << 30)
     return PKD_E_UNSUPPORTED_SHAPE;
@@ -105,10 +109,12 @@ DecodeKind kind_for(const pkd_config* c, const void* probe_address) {
   k.block = (c->flags & PKD_FLAG_SHARED_PREFIX) != 0;
   k.fp8 = (c->flags & PKD_FLAG_KV_FP8) != 0;
   k.tmap = k.mma && c->page_size % 16 == 0 && !(c->flags & PKD_FLAG_ROW_COPIES);
+  k.dense = (c->flags & PKD_FLAG_DENSE_PREFIX) != 0;
   if (k.tmap && probe_address != nullptr) {
     CUtensorMap m;
     k.tmap = encode_kv_map(probe_address, c->num_pages, c->page_size, c->num_kv_heads, k.fp8,
-                           (c->flags & PKD_FLAG_HND) != 0, &m) == cudaSuccess;
+                           (c->flags & PKD_FLAG_HND) != 0, k.dense ? 1 : c->num_kv_heads,
+                           &m) == cudaSuccess;
   }
   return k;
 }
@@ -144,7 +150,8 @@ int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out) {
   e.kv = kv;
   const pkd_config& c = ctx->cfg;
   if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8,
-                    (c.flags & PKD_FLAG_HND) != 0, &e.map) != cudaSuccess)
+                    (c.flags & PKD_FLAG_HND) != 0, ctx->kind.dense ? 1 : c.num_kv_heads,
+                    &e.map) != cudaSuccess)
     return PKD_E_CUDA;
   constexpr size_t kMaxMaps = 128;
   if (ctx->kv_maps.size() < kMaxMaps) {
@@ -189,6 +196,9 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
     const int st = kv_map_for(ctx, kv, &a.kv_map);
     if (st != PKD_OK) return st;
   }
+  if (ctx->kind.dense && ctx->info.batch > 0 &&
+      encode_q_map(q, ctx->info.batch, c.num_qo_heads, c.num_kv_heads, &a.q_map) != cudaSuccess)
+    return PKD_E_CUDA;
   if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
   if (launch_decode(ctx->kind, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
@@ -294,6 +304,10 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
   if (!ctx) return PKD_E_INVALID_ARG;
   ctx->cfg = *cfg;
   ctx->kind = kind_for(cfg, d_workspace);
+  if (ctx->kind.dense && !ctx->kind.tmap) {   // the driver refused the page-tile map
+    delete ctx;
+    return PKD_E_UNSUPPORTED_SHAPE;
+  }
   st = resolve_ctas(cfg, ctx->kind, &ctx->n_cta, &ctx->smem_bytes);
   if (st != PKD_OK) {
     delete ctx;
@@ -529,6 +543,7 @@ int pkd_graph_capture_io(pkd_ctx* ctx, int32_t layers, const void* const* q,
   if (!g) return PKD_E_INVALID_ARG;
   g->ctx = ctx;
   g->layers = layers;
+  g->batch = ctx->info.batch;
   const bool timing = (flags & PKD_GRAPH_TIMING) != 0;
   if (timing) {
     g->ev.assign((size_t)2 * layers, nullptr);
@@ -626,6 +641,8 @@ int pkd_graph_capture_io(pkd_ctx* ctx, int32_t layers, const void* const* q,
 
 int pkd_graph_launch(pkd_graph* g, void* stream) {
   if (g == nullptr || g->exec == nullptr) return PKD_E_INVALID_ARG;
+  // a dense-prefix graph's query maps cover the batch it was captured with
+  if (g->ctx->kind.dense && g->ctx->info.batch != g->batch) return PKD_E_STALE_PLAN;
   if (cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKD_E_CUDA;
   return PKD_OK;

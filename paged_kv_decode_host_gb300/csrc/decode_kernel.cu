@@ -49,107 +49,14 @@
 #include <mutex>
 
 #include "pkd_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace pkd {
 namespace {
 
+using namespace dev;
+
 constexpr int kTS = kWarpTokens;                 // tokens per stage
-constexpr unsigned kFull = 0xffffffffu;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false on timeout, or when `abort_flag` (if given) is raised.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (abort_flag && *abort_flag) return false;
-      if (global_ns() - t0 > kTimeoutNs) return false;
-    }
-  }
-}
-
-// L2 policy for the KV stream: every byte is read once per layer, so mark it
-// evict-first and leave L2 to the schedule, queries and partial states.
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// 1-D TMA bulk copy global -> shared, completion counted in bytes on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// 5-D tensor-map copy global -> shared (box of the map at the given
-// coordinates, innermost first), completion counted in bytes on `bar`.
-__device__ __forceinline__ void tensor_copy_g2s(void* dst, const CUtensorMap* map, int c0, int c1,
-                                                int c2, int c3, int c4, uint64_t* bar,
-                                                uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Order this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA) writes to the same bytes.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Shared-memory stride of one token row (all KV heads): 16 bytes of padding
 // shift consecutive rows across banks, so 8-row fragment loads of one head
 // are conflict-free.
@@ -166,18 +73,6 @@ __device__ __forceinline__ int rows_tok_stride(const DecodeArgs& a) {
 }
 __device__ __forceinline__ int rows_v_base(const DecodeArgs& a, int tokens) {
   return a.kv_merged ? a.row_bytes : tokens * row_stride(a.row_bytes);
-}
-
-// Programmatic dependent launch: let the next kernel in the stream start its
-// launch early, and wait for the previous kernel before touching its data.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ void raise_error(int32_t* err, volatile int* abort_flag, int code) {
-  atomicOr(err, code);
-  *abort_flag = 1;
 }
 
 // 8 bf16 (one uint4) -> 8 fp32, exact.
@@ -1353,6 +1248,7 @@ const void* kernel_ptr_g(const DecodeKind& k) {
 }
 
 const void* kernel_for(const DecodeKind& k) {
+  if (k.dense) return prefix_tc_kernel_ptr();
   if ((k.block || k.fp8) && !k.mma) return nullptr;
   if (k.block && k.fp8) return nullptr;
   switch (k.group) {
@@ -1366,7 +1262,9 @@ const void* kernel_for(const DecodeKind& k) {
 
 }  // namespace
 
-int decode_threads(int hkv) { return (hkv + 1) * 32; }
+int decode_threads(int hkv, const DecodeKind& k) {
+  return k.dense ? prefix_tc_threads() : (hkv + 1) * 32;
+}
 
 bool use_mma_consumer(int group, uint32_t flags) {
   if (flags & PKD_FLAG_FMA_CONSUMER) return false;
@@ -1376,6 +1274,7 @@ bool use_mma_consumer(int group, uint32_t flags) {
 }
 
 int decode_smem_bytes(int hkv, const DecodeKind& k) {
+  if (k.dense) return prefix_tc_smem_bytes();
   const int row = hkv * kHeadDim * (k.fp8 ? 1 : 2);
   const int tokens = k.fp8 ? kFp8Tokens : kTS;
   return kStages * stage_bytes_for(row, tokens, k.tmap) + (k.tmap ? 1024 : 0) +
@@ -1395,7 +1294,7 @@ cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes) {
 cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* blocks_per_sm) {
   const void* f = kernel_for(k);
   if (!f) return cudaErrorInvalidValue;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, decode_threads(hkv),
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, decode_threads(hkv, k),
                                                        (size_t)smem_bytes);
 }
 
@@ -1405,7 +1304,7 @@ cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, in
   if (!f) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(decode_threads(hkv));
+  cfg.blockDim = dim3(decode_threads(hkv, k));
   cfg.dynamicSmemBytes = (size_t)smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1422,8 +1321,9 @@ cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, in
 // {row, 128, D * E, P * row} (NHD) or {D * E, 128, P * D * E, P * row} (HND);
 // box {chunk, 16 tokens, all halves, all heads, one K or V page}, which lands
 // as [head][half][token][128 B] with the 128-byte swizzle in either layout.
-cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
-                          bool fp8, bool hnd, CUtensorMap* map) {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -1434,9 +1334,43 @@ cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, 
         q == cudaDriverEntryPointSuccess)
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
+  return encode;
+}
+
+}  // namespace
+
+// The query map: dims (innermost first) {64 elements, 128-byte half, query
+// head within the group, KV head, request} with byte strides {128, 256,
+// g * 256, Hq * 256}; box {64, 1 half, g heads, 1 KV head, 128 / g
+// requests}, which lands as 128 rows (request-major, head-minor) of 128
+// bytes with the 128-byte swizzle: one half of a dense tile's A operand.
+// Requests past the batch read as zeros.
+cudaError_t encode_q_map(const void* q, int32_t batch, int32_t hq, int32_t hkv,
+                         CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  if (q == nullptr || (uintptr_t)q % 16 != 0 || batch < 1 || hkv < 1 || hq % hkv != 0)
+    return cudaErrorInvalidValue;
+  const int32_t g = hq / hkv;
+  if (g > 8 || kDenseRows % g != 0) return cudaErrorInvalidValue;
+  const cuuint64_t row = (cuuint64_t)kHeadDim * 2;
+  const cuuint64_t dims[5] = {64, 2, (cuuint64_t)g, (cuuint64_t)hkv, (cuuint64_t)batch};
+  const cuuint64_t strides[4] = {128, row, (cuuint64_t)g * row, (cuuint64_t)hq * row};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)g, 1, (cuuint32_t)(kDenseRows / g)};
+  const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(q), dims,
+                            strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
+                          bool fp8, bool hnd, int32_t box_heads, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
   if (kv == nullptr || (uintptr_t)kv % 16 != 0 || page_size % 16 != 0 || num_pages < 1 ||
-      hkv < 1 || hkv > kMaxKvHeads)
+      hkv < 1 || hkv > kMaxKvHeads || box_heads < 1 || box_heads > hkv)
     return cudaErrorInvalidValue;
   const int E = fp8 ? 1 : 2;
   const cuuint64_t row = (cuuint64_t)hkv * kHeadDim * E;
@@ -1447,7 +1381,7 @@ cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, 
   const cuuint64_t strides[4] = {hnd ? head : row, 128, hnd ? (cuuint64_t)page_size * head : head,
                                  (cuuint64_t)page_size * row};
   const cuuint32_t box[5] = {(cuuint32_t)(128 / E), 16, (cuuint32_t)(kHeadDim * E / 128),
-                             (cuuint32_t)hkv, 1};
+                             (cuuint32_t)box_heads, 1};
   const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
   const CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                             5, const_cast<void*>(kv), dims, strides, box, elem_strides,

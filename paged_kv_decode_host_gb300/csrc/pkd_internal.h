@@ -120,6 +120,10 @@ struct DecodeArgs {
   // slot, 128-byte half of a head, KV head, 2 * page + {0 K, 1 V}) whose
   // 16-token box lands in shared memory with the 128-byte swizzle.
   CUtensorMap kv_map;
+  // Dense-prefix kernel only: q [B][Hq][D] as 5-D {64 dims, half, head in
+  // group, KV head, request}; its box is one KV head's 128 query rows of a
+  // block (128 / g requests x g heads) and one 128-byte half.
+  CUtensorMap q_map;
 };
 
 struct MergeArgs {
@@ -141,16 +145,25 @@ struct DecodeKind {
   bool fp8 = false;    // the cache holds e4m3 (tensor-core consumer only)
   bool tmap = false;   // page-tile producer: one tensor-map copy per 16 tokens of K or V
                        // (P % 16 == 0, tensor-core consumers); else one copy per token row
+  bool dense = false;  // dense shared-prefix kernel (tcgen05, one KV head per item)
 };
 int decode_smem_bytes(int hkv, const DecodeKind& k);
-int decode_threads(int hkv);
+int decode_threads(int hkv, const DecodeKind& k);
+// The dense shared-prefix kernel (prefix_tc_kernel.cu).
+const void* prefix_tc_kernel_ptr();
+int prefix_tc_smem_bytes();
+int prefix_tc_threads();
 cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes);
 cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* blocks_per_sm);
 cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, int hkv,
                           int smem_bytes, cudaStream_t stream);
-// Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`.
+// Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`;
+// a box holds box_heads KV heads (all of them, or 1 for the dense kernel).
 cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
-                          bool fp8, bool hnd, CUtensorMap* map);
+                          bool fp8, bool hnd, int32_t box_heads, CUtensorMap* map);
+// Encode the dense kernel's query map of q [batch][Hq][D] bf16.
+cudaError_t encode_q_map(const void* q, int32_t batch, int32_t hq, int32_t hkv,
+                         CUtensorMap* map);
 // Consumer variant for a group size: tensor cores (mma.sync) or CUDA cores.
 bool use_mma_consumer(int group, uint32_t flags);
 // Merge grid for a persistent decode grid of n_cta CTAs.

@@ -276,6 +276,8 @@ def run_ours(args, rank, world):
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
                                                 chunk_rule=args.chunk_rule,
+                                                dense_prefix=(gi is not None and
+                                                              args.prefix_kernel == "dense"),
                                                 device=dev)
             _plan(d, gi, (ip, ix, la))
             decs.append(d)
@@ -442,6 +444,7 @@ def run_ours(args, rank, world):
             "alg_bytes_per_step": int(step_bytes),
             "consumer": args.consumer,
             "chunk_rule": args.chunk_rule,
+            "prefix_kernel": args.prefix_kernel if w.prefix_tokens else None,
             "l2": "inputs larger than L2 (each layer's cache >= 0.49 GB, distinct per replay)",
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
                                           "makespan")},
@@ -819,6 +822,9 @@ def main():
     ap.add_argument("--chunk-rule", choices=["closed", "search"], default="closed",
                     help="split chunk: closed-form work bound (default) or the largest chunk "
                          "that still gives every CTA an item (binary search)")
+    ap.add_argument("--prefix-kernel", choices=["dense", "mma"], default="dense",
+                    help="shared-prefix level: the tcgen05 dense kernel (128-row tiles per KV "
+                         "head) or the mma.sync row-block consumer (16-row tiles)")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per step (0: the workload's own); smaller for profiling captures")
     args = ap.parse_args()

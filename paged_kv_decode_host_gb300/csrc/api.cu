@@ -113,8 +113,7 @@ DecodeKind kind_for(const pkd_config* c, const void* probe_address) {
   if (k.tmap && probe_address != nullptr) {
     CUtensorMap m;
     k.tmap = encode_kv_map(probe_address, c->num_pages, c->page_size, c->num_kv_heads, k.fp8,
-                           (c->flags & PKD_FLAG_HND) != 0, k.dense ? 1 : c->num_kv_heads,
-                           &m) == cudaSuccess;
+                           (c->flags & PKD_FLAG_HND) != 0, k.dense, &m) == cudaSuccess;
   }
   return k;
 }
@@ -150,8 +149,7 @@ int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out) {
   e.kv = kv;
   const pkd_config& c = ctx->cfg;
   if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8,
-                    (c.flags & PKD_FLAG_HND) != 0, ctx->kind.dense ? 1 : c.num_kv_heads,
-                    &e.map) != cudaSuccess)
+                    (c.flags & PKD_FLAG_HND) != 0, ctx->kind.dense, &e.map) != cudaSuccess)
     return PKD_E_CUDA;
   constexpr size_t kMaxMaps = 128;
   if (ctx->kv_maps.size() < kMaxMaps) {

@@ -1366,11 +1366,11 @@ cudaError_t encode_q_map(const void* q, int32_t batch, int32_t hq, int32_t hkv,
 }
 
 cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
-                          bool fp8, bool hnd, int32_t box_heads, CUtensorMap* map) {
+                          bool fp8, bool hnd, bool head_half_box, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
   if (kv == nullptr || (uintptr_t)kv % 16 != 0 || page_size % 16 != 0 || num_pages < 1 ||
-      hkv < 1 || hkv > kMaxKvHeads || box_heads < 1 || box_heads > hkv)
+      hkv < 1 || hkv > kMaxKvHeads)
     return cudaErrorInvalidValue;
   const int E = fp8 ? 1 : 2;
   const cuuint64_t row = (cuuint64_t)hkv * kHeadDim * E;
@@ -1380,8 +1380,9 @@ cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, 
   const cuuint64_t head = (cuuint64_t)kHeadDim * E;
   const cuuint64_t strides[4] = {hnd ? head : row, 128, hnd ? (cuuint64_t)page_size * head : head,
                                  (cuuint64_t)page_size * row};
-  const cuuint32_t box[5] = {(cuuint32_t)(128 / E), 16, (cuuint32_t)(kHeadDim * E / 128),
-                             (cuuint32_t)box_heads, 1};
+  const cuuint32_t box[5] = {(cuuint32_t)(128 / E), 16,
+                             head_half_box ? 1u : (cuuint32_t)(kHeadDim * E / 128),
+                             head_half_box ? 1u : (cuuint32_t)hkv, 1};
   const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
   const CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                             5, const_cast<void*>(kv), dims, strides, box, elem_strides,

@@ -157,10 +157,12 @@ cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes);
 cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* blocks_per_sm);
 cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, int hkv,
                           int smem_bytes, cudaStream_t stream);
-// Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`;
-// a box holds box_heads KV heads (all of them, or 1 for the dense kernel).
+// Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`.
+// A box is 16 tokens of all KV heads (the decode kernel) or, with
+// head_half_box, 16 tokens of one 128-byte half of one KV head (the dense
+// kernel, which lays the halves of 64 tokens out as two 8 KB matrices).
 cudaError_t encode_kv_map(const void* kv, int32_t num_pages, int32_t page_size, int32_t hkv,
-                          bool fp8, bool hnd, int32_t box_heads, CUtensorMap* map);
+                          bool fp8, bool hnd, bool head_half_box, CUtensorMap* map);
 // Encode the dense kernel's query map of q [batch][Hq][D] bf16.
 cudaError_t encode_q_map(const void* q, int32_t batch, int32_t hq, int32_t hkv,
                          CUtensorMap* map);

@@ -11,14 +11,16 @@
 // GB300 design (one CTA per SM, 6 warps):
 //  * warp 4 (producer) loads the item's Q tile once (two TMA tensor copies,
 //    128 rows x 128 dims, 128-byte swizzle) and streams the KV head's page
-//    tiles (one TMA tensor copy per 16 tokens of K or V, 4 KB) into a 4-deep
-//    ring of 64-token stages;
+//    tiles into a 4-deep ring of 64-token stages: one TMA tensor copy per 16
+//    tokens, 128-byte half of the head, and K or V (2 KB), placed so that each
+//    half of a stage's K (and V) is one [64 tokens][128 B] swizzled matrix --
+//    a whole round is one MMA operand however the pages are scattered;
 //  * warp 5 (one lane) issues tcgen05.mma: per round of 64 tokens, S into a
-//    double-buffered tensor-memory tile (M 128, N 16 per page tile, K 128 in
-//    8 steps, both operands K-major from shared memory), then, once the
-//    softmax warps have written P, O += P V (M 128, N 128, K 16 per page
-//    tile, A = P from tensor memory, B = V N-major from shared memory);
-//    completion goes to mbarriers through tcgen05.commit;
+//    double-buffered tensor-memory tile (M 128, N 64, K 128 in 8 steps, both
+//    operands K-major from shared memory), then, once the softmax warps have
+//    written P, O += P V (M 128, N 128, K 16 per page tile, A = P from tensor
+//    memory, B = V N-major from shared memory); completion goes to mbarriers
+//    through tcgen05.commit;
 //  * warps 0-3 (softmax, one query row per thread = one tensor-memory lane)
 //    read S with tcgen05.ld, keep the row's running max and sum in registers,
 //    write P (bf16) to tensor memory with tcgen05.st, and in the epilogue read
@@ -46,8 +48,10 @@ using namespace dev;
 constexpr int kTcThreads = 192;       // 4 softmax warps, producer, MMA warp
 constexpr int kTcStages = 4;
 constexpr int kRoundTok = 64;         // tokens per round = 4 page tiles of 16
-constexpr int kTileBytes = 4096;      // one KV head, 16 tokens, 128 dims, bf16
-constexpr int kStageBytes = 2 * 4 * kTileBytes;   // K tiles 0..3, then V tiles 0..3
+constexpr int kBoxBytes = 2048;       // 16 tokens x one 128-byte half of a KV head
+constexpr int kHalfBytes = 4 * kBoxBytes;         // one half of a round: [64 tokens][128 B]
+constexpr int kKvBytes = 2 * kHalfBytes;          // K (or V) of a round: two halves
+constexpr int kStageBytes = 2 * kKvBytes;         // K, then V
 constexpr int kQBytes = kDenseRows * kHeadDim * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 128, kColP = 256;
@@ -151,6 +155,14 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2^x, one SFU instruction (softmax weights: relative error far below the
+// bf16 rounding P gets next; -inf gives 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
   a += 0x7fffu + ((a >> 16) & 1u);   // round to nearest even (finite inputs)
@@ -227,30 +239,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           tensor_copy_g2s(sQ + h * (kQBytes / 2), &a.q_map, 0, h, 0, head, req, &sh->qfull, policy);
       }
       __syncwarp();
-      for (int t = tb; t < te; t += kRoundTok, ++st) {
+      // page ids of the item's 16-token tiles, 32 tiles at a time: lane i
+      // holds tile base + i (tb is page-aligned, so tile i starts 16 i tokens
+      // into the item's pages)
+      const int ntiles = (te - tb + 15) >> 4;
+      int base = -32, my_page = 0;
+      for (int t = tb, k = 0; t < te; t += kRoundTok, ++st, ++k) {
         const int n = min(kRoundTok, te - t);
         const int nbox = (n + 15) >> 4;
+        const int tile0 = 4 * k;
+        if (tile0 + 4 > base + 32) {
+          base = tile0;
+          my_page = 0;
+          if (base + lane < ntiles) {
+            my_page = a.sched[a.off_pages + poff + (16 * (base + lane)) / P];
+            if ((unsigned)my_page >= (unsigned)a.num_pages) {
+              atomicOr(a.err, PKD_DEV_ERR_BOUNDS);
+              my_page = 0;
+            }
+          }
+        }
         const int slot = st % kTcStages;
         const uint32_t round = (uint32_t)(st / kTcStages);
         if (round > 0 && !tc_wait(&sh->empty[slot], (round - 1) & 1u, abort_flag, a.err, lane)) {
           ok = false;
           break;
         }
-        // lane 2 j + c copies tile j of K (c = 0) or V (c = 1)
-        const int j = lane >> 1, c = lane & 1;
-        int page = -1;
-        if (j < nbox) {
-          page = a.sched[a.off_pages + poff + (t + 16 * j - tb) / P];
-          if ((unsigned)page >= (unsigned)a.num_pages) {
-            atomicOr(a.err, PKD_DEV_ERR_BOUNDS);
-            page = 0;
-          }
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], (uint32_t)(2 * nbox * kTileBytes));
+        // lane 4 j + 2 c + h copies half h of tile j of K (c = 0) or V (c = 1)
+        const int j = lane >> 2, c = (lane >> 1) & 1, h = lane & 1;
+        const int page = __shfl_sync(kFull, my_page, (tile0 + (j & 3) - base) & 31);
+        if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], (uint32_t)(4 * nbox * kBoxBytes));
         __syncwarp();
-        if (page >= 0)
-          tensor_copy_g2s(stages + (size_t)slot * kStageBytes + (c * 4 + j) * kTileBytes, &a.kv_map,
-                          0, (t + 16 * j) % P, 0, head, 2 * page + c, &sh->full[slot], policy);
+        if (j < nbox)
+          tensor_copy_g2s(stages + (size_t)slot * kStageBytes + c * kKvBytes + h * kHalfBytes +
+                              j * kBoxBytes,
+                          &a.kv_map, 0, (t + 16 * j) % P, h, head, 2 * page + c, &sh->full[slot],
+                          policy);
       }
     }
     // drain: the last phase of every slot, and the last Q tile
@@ -261,7 +285,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
     }
   } else if (warp == 5) {
     // ----------------------------------------------------- MMA issue (lane 0)
-    const uint32_t idesc_s = mma_idesc(kDenseRows, 16, 0);
     const uint32_t idesc_o = mma_idesc(kDenseRows, kHeadDim, 1);
     const uint32_t q0 = smem_u32(sQ), st0 = smem_u32(stages);
     int rho = 0;     // global round = stage index
@@ -275,14 +298,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         return false;
       if (lane == 0) {
         tc_fence_after();
-        const int nbox = (n + 15) >> 4;
+        // N = the round's tokens rounded up to whole tiles (tiles past them
+        // were not copied)
+        const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
         const uint32_t kbase = st0 + (uint32_t)(slot * kStageBytes);
-        for (int j = 0; j < nbox; ++j)
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + kColS + 64 * b + 16 * j,
-                   smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
-                   smem_desc(kbase + j * kTileBytes + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
-                   idesc_s, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + kColS + 64 * b,
+                 smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                 smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024), idesc_s,
+                 kk > 0);
         mma_commit(&sh->sfull[b]);
       }
       __syncwarp();
@@ -325,16 +349,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           break;
         }
         const int nbox = (n + 15) >> 4;
-        uint8_t* vbase = stages + (size_t)slot * kStageBytes + 4 * kTileBytes;
+        uint8_t* vbase = stages + (size_t)slot * kStageBytes + kKvBytes;
         if (n & 15) {
           // slots past the item's end in the last tile: P is 0 there, but
           // 0 x NaN would poison O, so zero those V rows (both halves)
           const int v0 = n & 15;
-          uint8_t* tile = vbase + (nbox - 1) * kTileBytes;
+          uint8_t* tile = vbase + (nbox - 1) * kBoxBytes;
           for (int i = lane; i < 2 * (16 - v0) * 8; i += 32) {
             const int h = i / ((16 - v0) * 8), rem = i % ((16 - v0) * 8);
             const int row = v0 + rem / 8, chunk = rem % 8;
-            *reinterpret_cast<uint4*>(tile + h * 2048 + row * 128 + chunk * 16) =
+            *reinterpret_cast<uint4*>(tile + h * kHalfBytes + row * 128 + chunk * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
@@ -345,7 +369,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           const uint32_t vb = smem_u32(vbase);
           for (int j = 0; j < nbox; ++j)
             mma_ts(tmem + kColO, tmem + kColP + 32 * b + 8 * j,
-                   smem_desc(vb + j * kTileBytes, 2048, 1024), idesc_o, k > 0 || j > 0);
+                   smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, k > 0 || j > 0);
           mma_commit(&sh->pfree[b]);
           mma_commit(&sh->empty[slot]);
         }
@@ -395,13 +419,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->sfree[b]);
         float x[64];
-        float mx = -CUDART_INF_F;
+        float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const float v = __uint_as_float(j < 32 ? s0[j] : s1[j - 32]) * a.scale_log2;
           x[j] = j < n ? v : -CUDART_INF_F;
-          mx = fmaxf(mx, x[j]);
+          mq[j & 3] = fmaxf(mq[j & 3], x[j]);
         }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         // P buffer b was read by the P.V MMAs of round r - 2
         if (r >= 2 && !pv_wait(r - 2)) {
           ok = false;
@@ -434,14 +459,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           if (need) m_used = mx;
         }
         uint32_t pw[32];
-        float psum = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float p0 = exp2f(x[2 * j] - m_used), p1 = exp2f(x[2 * j + 1] - m_used);
-          psum += p0 + p1;
+          const float p0 = fast_exp2(x[2 * j] - m_used), p1 = fast_exp2(x[2 * j + 1] - m_used);
+          ps[j & 3] += p0 + p1;
           pw[j] = pack_bf16(p0, p1);
         }
-        l += psum;
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         tmem_st32(tmem + lane_off + kColP + 32 * b, pw);
         tmem_wait_st();
         tc_fence_before();

@@ -813,7 +813,7 @@ def main():
     ap.add_argument("--workload", default="llama8b_step",
                     choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix",
                              "llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd",
-                             "append"])
+                             "shared_prefix_hnd", "append"])
     ap.add_argument("--consumer", choices=["auto", "fma", "mma"], default="auto",
                     help="decode-kernel consumer: the default, or forced CUDA-core (fma) / "
                          "tensor-core (mma) folding of the GQA group")

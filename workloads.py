@@ -103,6 +103,11 @@ def workload(name: str) -> Workload:
         g = torch.Generator().manual_seed(3)
         lens = tuple(_randint(g, 128, 512, 63) + [100_000])
         return Workload(name, 3, 32, 8, 128, 16, 1, lens, _pages_for(lens, 16))
+    if name == "shared_prefix_hnd":
+        w = workload("shared_prefix")
+        return Workload(name, w.seed, w.hq, w.hkv, w.head_dim, w.page_size, w.layers, w.lens,
+                        w.pool_pages, prefix_tokens=w.prefix_tokens, suffix_lens=w.suffix_lens,
+                        kv_layout="HND")
     if name == "shared_prefix":
         g = torch.Generator().manual_seed(4)
         suffix = tuple(_randint(g, 64, 1024, 32))
@@ -120,7 +125,8 @@ def workload(name: str) -> Workload:
 
 WORKLOADS = ("worked_example", "llama8b_step", "skewed", "shared_prefix", "token_sparse")
 # the same Llama-shaped step over an E4M3 cache
-EXTRA_WORKLOADS = ("llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd")
+EXTRA_WORKLOADS = ("llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd",
+                   "shared_prefix_hnd")
 
 
 def page_table(kv_lens, page_size, page_ids=None):

@@ -304,9 +304,10 @@ int pkd_plan_host_shared(const pkd_config *cfg, const int32_t *group_indptr,
  *   off[3] merge_indptr[num_units + 1]
  *   off[4] page_list[nnz]    (the CSR indices, unchanged)
  *   off[5] total words
- * Header words 0..15 hold: magic, batch, Hq, Hkv, D, P, num_ctas,
+ * Header words 0..31 hold: magic, batch, Hq, Hkv, D, P, num_ctas,
  * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (clamped to
- * int32), split floor, requests per block.  Errors: INVALID_ARG. */
+ * int32), split floor, requests per block, the most chunks of any split
+ * request, then zeros.  Errors: INVALID_ARG. */
 int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 
 /* ---- CUDA-graph capture of a whole decode step ------------------------- */

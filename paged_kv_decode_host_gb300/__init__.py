@@ -232,7 +232,7 @@ def decode_schedule(words, off, info):
     merge_indptr = words[off[3]:off[3] + n_units + 1].tolist()
     page_list = words[off[4]:off[4] + nnz].tolist()
     return dict(cta_indptr=cta_indptr, items=items, units=units, merge_indptr=merge_indptr,
-                page_list=page_list, header=words[:16].tolist(), heads=heads)
+                page_list=page_list, header=words[:32].tolist(), heads=heads)
 
 
 def _stream_ptr(stream=None):

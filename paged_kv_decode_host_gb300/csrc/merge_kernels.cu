@@ -32,16 +32,22 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // Contraction of split chunks (the reduction map built by the planner): for
 // each split request u and query head h, fold the partial states in slots
-// merge_indptr[u] .. merge_indptr[u+1] into out / lse.
-// Block = 256 threads = 8 warps; blocks take (unit, head) tasks in a
-// grid-stride loop over a grid of 8 blocks per decode CTA, so every task of a
-// typical plan is in flight at once.  Two passes over the unit's slots: the
-// block first takes M = max L over all of them, then warp w sums
-// exp(L - M) O and exp(L - M) over slots w, w + 8, ... (lane = 4 dims) -- with
-// M known up front no term rescales the running sum, so a warp's loads are
-// independent and stay in flight together (a request split into hundreds of
-// chunks folds in a few memory latencies).  The 8 warp sums are added in warp
-// order.  Fixed assignment and order: bit-reproducible.
+// merge_indptr[u] .. merge_indptr[u+1] into out / lse.  Block = 256 threads
+// = 8 warps, grid = 8 blocks per decode CTA; (unit, head) tasks:
+//  * one block per task by default: the block first takes M = max L over the
+//    unit's chunks, then warp w sums exp(L - M) O and exp(L - M) over slots
+//    w, w + 8, ... (lane = 4 dims); the 8 warp sums are added in warp order;
+//  * with at least 4 tasks per block (hundreds of split requests), one warp
+//    per task for units of at most 32 chunks: lane i reads chunk i's L, the
+//    warp takes M and the weights w_i = exp(L_i - M) with shuffles, then
+//    every lane sums w_i O_i over its 4 dims -- no block barrier; longer
+//    units still get a block.  (Measured: with few tasks the block form is
+//    the faster one, as every block then carries work.)
+// With M known up front no term rescales a running sum, so the loads of a
+// warp stay in flight together.  Fixed assignment and order:
+// bit-reproducible.
+constexpr int kWarpSlots = 32;
+
 __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
   constexpr int kWarps = kMergeThreads / 32;
   __shared__ float wm[kWarps];
@@ -54,14 +60,60 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   const int64_t tasks = (int64_t)n_units * a.hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool waited = false;
-  for (int64_t task = blockIdx.x; task < tasks; task += gridDim.x) {
+  const bool warp_mode = tasks >= (int64_t)4 * gridDim.x;
+  // ---- short units, many tasks: a warp per task
+  const int64_t n_warps = (int64_t)gridDim.x * kWarps;
+  const int64_t warp_tasks = warp_mode ? tasks : 0;
+  for (int64_t task = (int64_t)blockIdx.x * kWarps + warp; task < warp_tasks; task += n_warps) {
     const int u = (int)(task / a.hq);
     const int h = (int)(task % a.hq);
-    const int req = a.sched[a.off_units + 2 * u];
     const int s0 = a.sched[a.off_merge + u];
-    const int s1 = a.sched[a.off_merge + u + 1];
+    const int n = a.sched[a.off_merge + u + 1] - s0;
+    if (n > kWarpSlots) continue;
+    const int req = a.sched[a.off_units + 2 * u];
     if (!waited) {
       pdl_wait();   // partial states and outputs belong to the decode kernel
+      waited = true;
+    }
+    const float l2 = lane < n ? a.l_part[(int64_t)(s0 + lane) * a.hq + h] * kLog2e : -CUDART_INF_F;
+    float m = l2;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float w_lane = lane < n ? exp2f(l2 - m) : 0.f;
+    float z = w_lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float w = __shfl_sync(0xffffffffu, w_lane, i);
+      const float4 o = *reinterpret_cast<const float4*>(
+          a.o_part + ((int64_t)(s0 + i) * a.hq + h) * kHeadDim + 4 * lane);
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+    const float inv = 1.f / z;
+    const int64_t qrow = (int64_t)req * a.hq + h;
+    *reinterpret_cast<uint2*>(a.out + qrow * kHeadDim + 4 * lane) =
+        make_uint2(f32_to_bf16_rne(acc.x * inv) | (f32_to_bf16_rne(acc.y * inv) << 16),
+                   f32_to_bf16_rne(acc.z * inv) | (f32_to_bf16_rne(acc.w * inv) << 16));
+    if (lane == 0 && a.lse != nullptr) a.lse[qrow] = (m + log2f(z)) * kLn2;
+  }
+  // ---- a block per task (in warp mode only the long units, and only when
+  // the plan has any)
+  const int64_t block_tasks =
+      (!warp_mode || a.sched[H_MAXCHUNKS] > kWarpSlots) ? tasks : 0;
+  for (int64_t task = blockIdx.x; task < block_tasks; task += gridDim.x) {
+    const int u = (int)(task / a.hq);
+    const int h = (int)(task % a.hq);
+    const int s0 = a.sched[a.off_merge + u];
+    const int s1 = a.sched[a.off_merge + u + 1];
+    if (warp_mode && s1 - s0 <= kWarpSlots) continue;   // the same for the whole block
+    const int req = a.sched[a.off_units + 2 * u];
+    if (!waited) {
+      pdl_wait();
       waited = true;
     }
     // ---- pass 1: M = max over the unit's chunk LSEs (log2 units)

@@ -21,11 +21,12 @@ constexpr int kDefaultAlpha = 32;
 constexpr int kDefaultMinChunk = 256;
 constexpr int kMergeThreads = 256;
 
-// Schedule header words (first 16 int32 of the workspace).
+// Schedule header words (first 32 int32 of the workspace; 17..31 are 0).
 enum HeaderWord {
   H_MAGIC = 0, H_BATCH, H_HQ, H_HKV, H_D, H_P, H_NCTA, H_NITEMS, H_NUNITS,
   H_NSLOTS, H_CHUNK, H_ALPHA, H_NNZ, H_MAKESPAN, H_MINCHUNK, H_BLOCK,
-  H_WORDS = 16
+  H_MAXCHUNKS,   // most chunks of any split request (0: nothing split)
+  H_WORDS = 32
 };
 
 // req (first of the block), tok_begin, tok_end, dst_slot, first page index,

@@ -372,6 +372,9 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   h[H_MAKESPAN] = (int32_t)std::min<int64_t>(best_span, 0x7fffffff);
   h[H_MINCHUNK] = (int32_t)floor_c;
   h[H_BLOCK] = rows;
+  int32_t max_chunks = 0;
+  for (const auto& un : units) max_chunks = std::max(max_chunks, un.second);
+  h[H_MAXCHUNKS] = max_chunks;
 
   if (info) {
     info->batch = batch;

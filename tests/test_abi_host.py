@@ -76,6 +76,9 @@ def _compare(cfg, indptr, indices, last, alpha, min_chunk, chunk_rule="closed"):
     ref = oplan.plan(indptr, indices, last, page_size=cfg.page_size, num_pages=cfg.num_pages,
                      n_cta=cfg.num_ctas, alpha=alpha, min_chunk_tokens=min_chunk,
                      chunk_rule=chunk_rule)
+    # header word 16: the most chunks of any split request
+    assert got["header"][16] == max([n for _, n in ref.units], default=0)
+    assert got["header"][17:] == [0] * 15
     assert info["chunk_tokens"] == ref.chunk
     assert info["makespan"] == ref.makespan
     assert info["num_items"] == ref.n_items

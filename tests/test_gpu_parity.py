@@ -281,3 +281,52 @@ def test_merge_states_against_oracle():
     pkd.merge_states(va2, sa2, vb, sb, v_out=va2, s_out=sa2)
     torch.cuda.synchronize()
     assert torch.equal(va2, vo) and torch.equal(sa2, so)
+
+
+def test_merge_paths_at_the_32_chunk_boundary():
+    """A request split into 32 chunks is folded by one warp, one split into
+    33 by a whole block: both against the oracle."""
+    lens = [512, 528, 40]
+    w = workloads.Workload("m32", 77, 32, 8, 128, 16, 1, tuple(lens),
+                           sum(-(-l // 16) for l in lens) + 2)
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    dec = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, 16, max_batch=3,
+                                          max_num_pages=int(t["indptr"][-1]),
+                                          num_pages=w.pool_pages, num_ctas=68, alpha=0,
+                                          min_chunk_tokens=16, chunk_rule="search")
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    info = dec.plan_info()
+    assert info["chunk_tokens"] == 16
+    words, info, off = dec.schedule()
+    units = pkd.decode_schedule(words, off, info)["units"]
+    assert sorted(n for _, n in units) == [3, 32, 33]
+    out, lse = dec.run(q, kv)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=32, hkv=8)
+    _check(out, lse, ref_o, ref_l)
+
+
+def test_merge_warp_mode_many_units():
+    """At least 4 merge tasks per merge block: the warp-per-task merge,
+    against the oracle on every element (20 requests, 16 split, Hq 16 ->
+    256 tasks for 8 CTAs x 8 merge blocks)."""
+    rng = np.random.default_rng(20)
+    lens = rng.integers(200, 1200, 20).tolist()
+    w = workloads.Workload("mw", 78, 16, 2, 128, 16, 1, tuple(lens),
+                           sum(-(-l // 16) for l in lens) + 2)
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    dec = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, 16, max_batch=w.batch,
+                                          max_num_pages=int(t["indptr"][-1]),
+                                          num_pages=w.pool_pages, num_ctas=8, alpha=0,
+                                          min_chunk_tokens=16)
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    info = dec.plan_info()
+    assert info["num_units"] * w.hq >= 4 * 8 * 8      # tasks >= 4 x merge blocks
+    out, lse = dec.run(q, kv)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=w.hq, hkv=w.hkv)
+    _check(out, lse, ref_o, ref_l)

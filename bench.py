@@ -40,7 +40,17 @@ import workloads  # noqa: E402
 METRIC = "decode-step KV throughput: achieved HBM GB/s (% of GB300 peak) and steps/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_decode_host_gb300", "csrc", "decode_kernel.cu")
+# the decode kernel's sources: a profile's counters stand for the kernel built from these
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_host_gb300", "csrc", f)
+                  for f in ("decode_kernel.cu", "sm103_ptx.cuh", "pkd_internal.h")]
+
+
+def kernel_source_sha256():
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # --------------------------------------------------------------------- bytes
@@ -78,8 +88,7 @@ def traffic_from_profile(workload):
     try:
         with open(os.path.join(PROFILE_DIR, f"decode_kernel_{workload}.md")) as f:
             text = f.read()
-        with open(KERNEL_SOURCE, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sha = kernel_source_sha256()
     except OSError:
         return None
     vals = {}
@@ -275,7 +284,7 @@ def run_ours(args, rank, world):
                                                 num_pages=w.pool_pages,
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
-                                                chunk_rule=args.chunk_rule,
+                                                chunk_rule=args.chunk_rule, alpha=args.alpha,
                                                 dense_prefix=(gi is not None and
                                                               args.prefix_kernel == "dense"),
                                                 device=dev)
@@ -444,8 +453,11 @@ def run_ours(args, rank, world):
             "alg_bytes_per_step": int(step_bytes),
             "consumer": args.consumer,
             "chunk_rule": args.chunk_rule,
+            "alpha": args.alpha if args.alpha >= 0 else "default (32)",
             "prefix_kernel": args.prefix_kernel if w.prefix_tokens else None,
-            "l2": "inputs larger than L2 (each layer's cache >= 0.49 GB, distinct per replay)",
+            "l2": (f"inputs larger than L2: {n_kv} distinct caches of "
+                   f"{kvs[0].numel() * kvs[0].element_size() / 1e9:.2f} GB, "
+                   + ("one per layer" if copies == 1 else "rotated over replays")),
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
                                           "makespan")},
             "parallelism": f"replicas x{world} (no collective)",
@@ -822,6 +834,8 @@ def main():
     ap.add_argument("--chunk-rule", choices=["closed", "search"], default="closed",
                     help="split chunk: closed-form work bound (default) or the largest chunk "
                          "that still gives every CTA an item (binary search)")
+    ap.add_argument("--alpha", type=int, default=-1,
+                    help="planner per-item cost in tokens (cost = alpha + tokens); -1: default")
     ap.add_argument("--prefix-kernel", choices=["dense", "mma"], default="dense",
                     help="shared-prefix level: the tcgen05 dense kernel (128-row tiles per KV "
                          "head) or the mma.sync row-block consumer (16-row tiles)")

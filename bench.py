@@ -193,11 +193,11 @@ def _views(w, t):
     return [("full", None, (t["indptr"], t["indices"], t["last"]))]
 
 
-def _plan(d, group_indptr, table):
+def _plan(d, group_indptr, table, stream=None):
     if group_indptr is None:
-        d.plan(*table)
+        d.plan(*table, stream=stream)
     else:
-        d.plan_shared(group_indptr, *table)
+        d.plan_shared(group_indptr, *table, stream=stream)
 
 
 class _ComposedGraph:
@@ -343,10 +343,9 @@ def run_ours(args, rank, world):
         memory and out / lse go back to it, inside the step."""
         si = k % n_sets
         copy_stream.wait_event(done[si])
-        with torch.cuda.stream(copy_stream):
-            for (name, gi, table), d in zip(views, sets[si]):
-                _plan(d, gi, table)
-            copied[si].record(copy_stream)
+        for (name, gi, table), d in zip(views, sets[si]):
+            _plan(d, gi, table, stream=copy_stream)
+        copied[si].record(copy_stream)
         if host:
             for x, h in zip(qs, host["q"]):
                 x.copy_(h, non_blocking=True)
@@ -522,9 +521,9 @@ def run_e2e_pipelined(args, sets, views, kvs, kv_scales, layers, copies, qs, out
         # results went back
         h2d_stream.wait_event(ran[si])
         h2d_stream.wait_event(back[si])
+        for (name, gi, table), d in zip(views, sets[si]):
+            _plan(d, gi, table, stream=h2d_stream)
         with torch.cuda.stream(h2d_stream):
-            for (name, gi, table), d in zip(views, sets[si]):
-                _plan(d, gi, table)
             for x, h in zip(dq[si], hq):
                 x.copy_(h, non_blocking=True)
             ready[si].record(h2d_stream)

@@ -164,7 +164,7 @@ def _host_i32(a) -> np.ndarray:
 
 
 def _ptr(a: np.ndarray):
-    return ctypes.c_void_p(a.ctypes.data) if a.size else ctypes.c_void_p(0)
+    return a.ctypes.data if a.size else None
 
 
 FLAG_FMA_CONSUMER = 1   # fold the GQA group onto CUDA cores (fp32 FMA)
@@ -235,10 +235,25 @@ def decode_schedule(words, off, info):
                 page_list=page_list, header=words[:32].tolist(), heads=heads)
 
 
+_current_raw_stream = None
+
+
 def _stream_ptr(stream=None):
-    import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    """cudaStream_t of `stream`, else of torch's current stream on the
+    current device (looked up without building a Stream object: plan / run
+    are per-step host calls)."""
+    global _current_raw_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _current_raw_stream is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        dev = getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and dev is not None:
+            _current_raw_stream = lambda: raw(dev())
+        else:
+            _current_raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _current_raw_stream()
 
 
 class Graph:
@@ -325,23 +340,26 @@ class BatchDecodeWithPagedKVCache:
             _check(lib.pkd_create(ctypes.byref(self.cfg), ctypes.c_void_p(self.workspace.data_ptr()),
                                   nbytes, ctypes.byref(h)), "pkd_create")
         self._h = h
+        self._lib = lib
+        self._ep = ctypes.c_uint64()
+        self._ep_ref = ctypes.byref(self._ep)
         self.epoch = 0
         self.batch = None
 
     # -- plan ---------------------------------------------------------------
     def plan(self, indptr, indices, last_page_len, stream=None):
         """Schedule one decode step from host int32 arrays.  Returns the epoch."""
-        lib = load()
         indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
-        batch = int(last.shape[0])
+        batch = last.shape[0]
         if indptr.shape[0] != batch + 1:
             raise PkdError(-2, "indptr must have batch + 1 entries")
-        if batch and indices.shape[0] < int(indptr[-1]):
+        if batch and indices.shape[0] < indptr[batch]:
             raise PkdError(-2, "indices shorter than indptr[-1]")
-        ep = ctypes.c_uint64()
-        _check(lib.pkd_plan(self._h, _ptr(indptr), _ptr(indices), _ptr(last), batch,
-                            _stream_ptr(stream), ctypes.byref(ep)), "pkd_plan")
-        self.epoch = ep.value
+        st = self._lib.pkd_plan(self._h, _ptr(indptr), _ptr(indices), _ptr(last), batch,
+                                _stream_ptr(stream), self._ep_ref)
+        if st:
+            _check(st, "pkd_plan")
+        self.epoch = self._ep.value
         self.batch = batch
         return self.epoch
 
@@ -349,17 +367,16 @@ class BatchDecodeWithPagedKVCache:
         """Plan a shared-prefix level: requests group_indptr[j] ..
         group_indptr[j+1]-1 attend over group j's pages (CSR over groups).
         Needs ``shared_prefix=True``.  Returns the epoch."""
-        lib = load()
         gi = _host_i32(group_indptr)
         indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
-        n_groups = int(last.shape[0])
+        n_groups = last.shape[0]
         if gi.shape[0] != n_groups + 1 or indptr.shape[0] != n_groups + 1:
             raise PkdError(-2, "group_indptr and indptr need one entry per group + 1")
-        ep = ctypes.c_uint64()
-        _check(lib.pkd_plan_shared(self._h, _ptr(gi), n_groups, _ptr(indptr), _ptr(indices),
-                                   _ptr(last), _stream_ptr(stream), ctypes.byref(ep)),
-               "pkd_plan_shared")
-        self.epoch = ep.value
+        st = self._lib.pkd_plan_shared(self._h, _ptr(gi), n_groups, _ptr(indptr), _ptr(indices),
+                                       _ptr(last), _stream_ptr(stream), self._ep_ref)
+        if st:
+            _check(st, "pkd_plan_shared")
+        self.epoch = self._ep.value
         self.batch = int(gi[-1]) if n_groups else 0
         return self.epoch
 

@@ -370,13 +370,10 @@ static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n
                                  indptr, indices, last_page_len, words, &info);
   if (st != PKD_OK) return st;
   const Layout& L = ctx->layout;
-  // fixed-size part: header, cta queues, items, units, merge map
-  if (cudaMemcpyAsync(ctx->ws, words, (size_t)L.page_list * 4, cudaMemcpyHostToDevice, s) !=
-      cudaSuccess)
-    return PKD_E_CUDA;
-  if (info.nnz > 0 &&
-      cudaMemcpyAsync(ctx->ws + (size_t)L.page_list * 4, words + L.page_list,
-                      (size_t)info.nnz * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  // one copy: the fixed-size part (header, cta queues, items, units, merge
+  // map) and the page list right behind it, as laid out in the workspace
+  if (cudaMemcpyAsync(ctx->ws, words, ((size_t)L.page_list + (size_t)info.nnz) * 4,
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
     return PKD_E_CUDA;
   if (cudaEventRecord(ctx->staged[k], s) != cudaSuccess) return PKD_E_CUDA;
   ctx->staged_pending[k] = true;

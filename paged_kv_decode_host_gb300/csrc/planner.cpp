@@ -168,6 +168,22 @@ int64_t lpt(const std::vector<Item>& items, int32_t n_cta, std::vector<int32_t>*
   return makespan;
 }
 
+struct Block {
+  int32_t req_first, n_req, table_row;
+};
+
+// Working arrays of one plan, kept per host thread between calls: the planner
+// runs every decode step, and reusing their storage takes the allocator off
+// that path.  Every array is cleared or resized before use.
+struct Scratch {
+  std::vector<int64_t> row_len, lens, unit_lens, cands;
+  std::vector<Block> blocks;
+  std::vector<Item> items, best_items, whole, rest;
+  std::vector<int32_t> owner, best_owner, first_slot, n_chunks, count, fill, by_pos;
+  std::vector<std::pair<int64_t, int32_t>> heap;
+  std::vector<std::pair<int32_t, int32_t>> units;
+};
+
 }  // namespace
 
 int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
@@ -210,8 +226,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   }
   if (batch > cfg.max_batch) return PKD_E_CAPACITY;
 
+  thread_local Scratch sc;
   // ---- P0: table check and lengths (per table row)
-  std::vector<int64_t> row_len((size_t)n_rows);
+  std::vector<int64_t>& row_len = sc.row_len;
+  row_len.resize((size_t)n_rows);
   int64_t nnz = 0;
   if (n_rows > 0) {
     if (indptr[0] != 0) return PKD_E_BAD_TABLE;
@@ -231,11 +249,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   }
 
   // ---- row blocks
-  struct Block {
-    int32_t req_first, n_req, table_row;
-  };
-  std::vector<Block> blocks;
-  std::vector<int64_t> lens;  // per block: tokens of its table row
+  std::vector<Block>& blocks = sc.blocks;
+  std::vector<int64_t>& lens = sc.lens;  // per block: tokens of its table row
+  blocks.clear();
+  lens.clear();
   if (group_indptr) {
     for (int32_t j = 0; j < n_rows; ++j)
       for (int32_t r = group_indptr[j]; r < group_indptr[j + 1]; r += rows) {
@@ -244,13 +261,13 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
       }
   } else {
     for (int32_t i = 0; i < n_rows; ++i) blocks.push_back(Block{i, 1, i});
-    lens = row_len;
+    lens.assign(row_len.begin(), row_len.end());
   }
   const int32_t n_blocks = (int32_t)blocks.size();
   // work units: block-major, head-minor (unit u = block u / heads, head u % heads)
-  std::vector<int64_t> unit_lens;
+  std::vector<int64_t>& unit_lens = sc.unit_lens;
+  unit_lens.clear();
   if (heads > 1) {
-    unit_lens.reserve(lens.size() * heads);
     for (int64_t l : lens)
       for (int32_t hk = 0; hk < heads; ++hk) unit_lens.push_back(l);
   }
@@ -263,7 +280,8 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   const int64_t min_chunk = cfg.min_chunk_tokens < 0 ? kDefaultMinChunk : cfg.min_chunk_tokens;
   const int64_t floor_c = ceil_div(std::max<int64_t>(min_chunk, 1), P) * P;
   const int64_t work_bound = ceil_div(total, n_cta);
-  std::vector<int64_t> cands;
+  std::vector<int64_t>& cands = sc.cands;
+  cands.clear();
   if (cfg.flags & PKD_FLAG_CHUNK_SEARCH) {
     cands.push_back(search_chunk(ulens, n_cta, P, floor_c));
   } else {
@@ -272,9 +290,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
       if (std::find(cands.begin(), cands.end(), c) == cands.end()) cands.push_back(c);
     }
   }
-  std::vector<Item> items, best_items, whole, rest;
-  std::vector<int32_t> owner, best_owner;
-  std::vector<std::pair<int64_t, int32_t>> heap;
+  std::vector<Item>& items = sc.items;
+  std::vector<Item>& best_items = sc.best_items;
+  std::vector<int32_t>& owner = sc.owner;
+  std::vector<int32_t>& best_owner = sc.best_owner;
   int64_t best_chunk = -1, best_span = 0;
   for (int64_t c : cands) {
     if (best_chunk >= 0) {
@@ -289,8 +308,8 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
       const int64_t lb = std::max(alpha + top, ceil_div(total + alpha * n_it, n_cta));
       if (lb >= best_span) continue;
     }
-    split_sorted(ulens, c, alpha, &whole, &rest, &items);
-    int64_t span = lpt(items, n_cta, &owner, &heap);
+    split_sorted(ulens, c, alpha, &sc.whole, &sc.rest, &items);
+    int64_t span = lpt(items, n_cta, &owner, &sc.heap);
     if (best_chunk < 0 || span < best_span) {
       best_chunk = c;
       best_span = span;
@@ -303,9 +322,12 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 
   // ---- P4: reduction map: every request of a split block is a unit with
   // one slot per chunk, units in ascending request order, slots in chunk order
-  std::vector<int32_t> first_slot((size_t)n_blocks, -1);  // slot of the block's first request
-  std::vector<int32_t> n_chunks((size_t)n_blocks, 1);
-  std::vector<std::pair<int32_t, int32_t>> units;
+  std::vector<int32_t>& first_slot = sc.first_slot;  // slot of the block's first request
+  std::vector<int32_t>& n_chunks = sc.n_chunks;
+  std::vector<std::pair<int32_t, int32_t>>& units = sc.units;
+  first_slot.assign((size_t)n_blocks, -1);
+  n_chunks.assign((size_t)n_blocks, 1);
+  units.clear();
   int64_t n_slots = 0;
   for (int32_t b = 0; b < n_blocks; ++b) {
     const int64_t nc = ceil_div(lens[b], best_chunk);
@@ -321,13 +343,16 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   if (n_slots > L.max_slots || (int64_t)units.size() > L.max_items) return PKD_E_CAPACITY;
 
   // ---- serialize: queues in CTA order, each in assignment (LPT) order
-  std::vector<int32_t> count((size_t)n_cta, 0);
+  std::vector<int32_t>& count = sc.count;
+  count.assign((size_t)n_cta, 0);
   for (int64_t j = 0; j < n_items; ++j) count[best_owner[j]]++;
   int32_t* cta_indptr = words + L.cta_indptr;
   cta_indptr[0] = 0;
   for (int32_t c = 0; c < n_cta; ++c) cta_indptr[c + 1] = cta_indptr[c] + count[c];
-  std::vector<int32_t> fill(cta_indptr, cta_indptr + n_cta);
-  std::vector<int32_t> by_pos((size_t)n_items);
+  std::vector<int32_t>& fill = sc.fill;
+  std::vector<int32_t>& by_pos = sc.by_pos;
+  fill.assign(cta_indptr, cta_indptr + n_cta);
+  by_pos.resize((size_t)n_items);
   for (int64_t j = 0; j < n_items; ++j) by_pos[fill[best_owner[j]]++] = (int32_t)j;
 
   int32_t* item_words = words + L.items;

@@ -77,6 +77,19 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   return true;
 }
 
+// non-blocking: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -163,11 +176,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// two floats to a bf16 pair, round to nearest even (lo in the low half)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
-  a += 0x7fffu + ((a >> 16) & 1u);   // round to nearest even (finite inputs)
-  b += 0x7fffu + ((b >> 16) & 1u);
-  return (a >> 16) | (b & 0xffff0000u);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ int rounds_of(int tb, int te) { return (te - tb + kRoundTok - 1) / kRoundTok; }
@@ -285,97 +298,117 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
     }
   } else if (warp == 5) {
     // ----------------------------------------------------- MMA issue (lane 0)
+    // An event loop over two cursors: the next score MMA (round rs) and the
+    // next P.V MMA (round rp), each issued as soon as its inputs are ready,
+    // so S for a later round never queues behind the P.V of an earlier one
+    // (S(r + 1) can go out while the softmax warps still work on round r).
     const uint32_t idesc_o = mma_idesc(kDenseRows, kHeadDim, 1);
     const uint32_t q0 = smem_u32(sQ), st0 = smem_u32(stages);
-    int rho = 0;     // global round = stage index
-    bool ok = true;
-    // S for round r of tokens [t, t + n): tiles j < nbox
-    auto issue_s = [&](int r, int n) -> bool {
-      const int slot = r % kTcStages, b = r & 1;
-      if (!tc_wait(&sh->full[slot], (uint32_t)((r / kTcStages) & 1), abort_flag, a.err, lane))
-        return false;
-      if (r >= 2 && !tc_wait(&sh->sfree[b], (uint32_t)(((r >> 1) - 1) & 1), abort_flag, a.err, lane))
-        return false;
-      if (lane == 0) {
-        tc_fence_after();
-        // N = the round's tokens rounded up to whole tiles (tiles past them
-        // were not copied)
-        const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
-        const uint32_t kbase = st0 + (uint32_t)(slot * kStageBytes);
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + kColS + 64 * b,
-                 smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
-                 smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024), idesc_s,
-                 kk > 0);
-        mma_commit(&sh->sfull[b]);
-      }
-      __syncwarp();
-      return true;
+    int s_it = it0, s_k = 0, rs = 0;    // next S: item, round within it, global round
+    int p_it = it0, p_k = 0, rp = 0;    // next P.V
+    bool ok = true, idle = false;
+    unsigned long long idle_t0 = 0;
+    uint32_t spins = 0;
+    auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(kFull, mbar_test_wait(bar, parity));
     };
-    for (int it = it0; it < it1 && ok; ++it) {
-      const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
-      const int tb = item[1], te = item[2];
-      const int nr = rounds_of(tb, te);
-      if (!tc_wait(&sh->qfull, (uint32_t)((it - it0) & 1), abort_flag, a.err, lane)) {
-        ok = false;
-        break;
-      }
-      const int r0 = rho;
-      if (!issue_s(r0, min(kRoundTok, te - tb))) {
-        ok = false;
-        break;
-      }
-      if (nr == 1 && lane == 0) mma_commit(&sh->qfree);
-      for (int k = 0; k < nr && ok; ++k) {
-        const int r = r0 + k, b = r & 1, slot = r % kTcStages;
-        const int t = tb + k * kRoundTok;
-        const int n = min(kRoundTok, te - t);
-        if (k + 1 < nr) {
-          const int t1 = t + kRoundTok;
-          if (!issue_s(r + 1, min(kRoundTok, te - t1))) {
-            ok = false;
-            break;
+    while (ok && p_it < it1) {
+      bool progress = false;
+      // ---- S of round rs: K tiles landed, Q tile loaded (first round of
+      // an item), S buffer read by the softmax warps (round rs - 2)
+      if (s_it < it1) {
+        const int32_t* item = a.sched + a.off_items + (int64_t)s_it * kItemWords;
+        const int tb = item[1], te = item[2];
+        const int slot = rs % kTcStages, b = rs & 1;
+        if ((s_k > 0 || ready(&sh->qfull, (uint32_t)((s_it - it0) & 1))) &&
+            ready(&sh->full[slot], (uint32_t)((rs / kTcStages) & 1)) &&
+            (rs < 2 || ready(&sh->sfree[b], (uint32_t)(((rs >> 1) - 1) & 1)))) {
+          const int n = min(kRoundTok, te - (tb + s_k * kRoundTok));
+          const bool last = (s_k + 1) * kRoundTok >= te - tb;
+          if (lane == 0) {
+            tc_fence_after();
+            // N = the round's tokens rounded up to whole tiles (tiles past
+            // them were not copied)
+            const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
+            const uint32_t kbase = st0 + (uint32_t)(slot * kStageBytes);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + kColS + 64 * b,
+                     smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                     smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                     idesc_s, kk > 0);
+            mma_commit(&sh->sfull[b]);
+            if (last) mma_commit(&sh->qfree);   // the item's last score MMA
           }
-          if (k + 2 == nr && lane == 0) mma_commit(&sh->qfree);   // the item's last S issued
-        }
-        if (!tc_wait(&sh->pfull[b], (uint32_t)((r >> 1) & 1), abort_flag, a.err, lane)) {
-          ok = false;
-          break;
-        }
-        // the previous item's epilogue must have read O before it is overwritten
-        if (k == 0 && it > it0 &&
-            !tc_wait(&sh->ofree, (uint32_t)((it - it0 - 1) & 1), abort_flag, a.err, lane)) {
-          ok = false;
-          break;
-        }
-        const int nbox = (n + 15) >> 4;
-        uint8_t* vbase = stages + (size_t)slot * kStageBytes + kKvBytes;
-        if (n & 15) {
-          // slots past the item's end in the last tile: P is 0 there, but
-          // 0 x NaN would poison O, so zero those V rows (both halves)
-          const int v0 = n & 15;
-          uint8_t* tile = vbase + (nbox - 1) * kBoxBytes;
-          for (int i = lane; i < 2 * (16 - v0) * 8; i += 32) {
-            const int h = i / ((16 - v0) * 8), rem = i % ((16 - v0) * 8);
-            const int row = v0 + rem / 8, chunk = rem % 8;
-            *reinterpret_cast<uint4*>(tile + h * kHalfBytes + row * 128 + chunk * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
           __syncwarp();
+          ++rs;
+          if (last) {
+            ++s_it;
+            s_k = 0;
+          } else {
+            ++s_k;
+          }
+          progress = true;
         }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t vb = smem_u32(vbase);
-          for (int j = 0; j < nbox; ++j)
-            mma_ts(tmem + kColO, tmem + kColP + 32 * b + 8 * j,
-                   smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, k > 0 || j > 0);
-          mma_commit(&sh->pfree[b]);
-          mma_commit(&sh->empty[slot]);
-        }
-        __syncwarp();
       }
-      rho = r0 + nr;
+      // ---- P.V of round rp: P written (and, first round of an item, the
+      // previous item's O read by the epilogue)
+      if (rp < rs) {
+        const int32_t* item = a.sched + a.off_items + (int64_t)p_it * kItemWords;
+        const int tb = item[1], te = item[2];
+        const int slot = rp % kTcStages, b = rp & 1;
+        if (ready(&sh->pfull[b], (uint32_t)((rp >> 1) & 1)) &&
+            (p_k > 0 || p_it == it0 || ready(&sh->ofree, (uint32_t)((p_it - it0 - 1) & 1)))) {
+          const int n = min(kRoundTok, te - (tb + p_k * kRoundTok));
+          const bool last = (p_k + 1) * kRoundTok >= te - tb;
+          const int nbox = (n + 15) >> 4;
+          uint8_t* vbase = stages + (size_t)slot * kStageBytes + kKvBytes;
+          if (n & 15) {
+            // slots past the item's end in the last tile: P is 0 there, but
+            // 0 x NaN would poison O, so zero those V rows (both halves)
+            const int v0 = n & 15;
+            uint8_t* tile = vbase + (nbox - 1) * kBoxBytes;
+            for (int i = lane; i < 2 * (16 - v0) * 8; i += 32) {
+              const int h = i / ((16 - v0) * 8), rem = i % ((16 - v0) * 8);
+              const int row = v0 + rem / 8, chunk = rem % 8;
+              *reinterpret_cast<uint4*>(tile + h * kHalfBytes + row * 128 + chunk * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t vb = smem_u32(vbase);
+            for (int j = 0; j < nbox; ++j)
+              mma_ts(tmem + kColO, tmem + kColP + 32 * b + 8 * j,
+                     smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, p_k > 0 || j > 0);
+            mma_commit(&sh->pfree[b]);
+            mma_commit(&sh->empty[slot]);
+          }
+          __syncwarp();
+          ++rp;
+          if (last) {
+            ++p_it;
+            p_k = 0;
+          } else {
+            ++p_k;
+          }
+          progress = true;
+        }
+      }
+      if (progress) {
+        idle = false;
+      } else if (!idle) {
+        idle = true;
+        idle_t0 = global_ns();
+        spins = 0;
+      } else if ((++spins & 31u) == 0) {
+        const bool give_up = *abort_flag != 0 || global_ns() - idle_t0 > kTimeoutNs;
+        if (__any_sync(kFull, give_up)) {
+          if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+          ok = false;
+        }
+      }
     }
     if (lane == 0) {
       mma_commit(&sh->fin);
@@ -418,15 +451,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->sfree[b]);
-        float x[64];
+        // row max of the raw scores (the scale is positive); slots past the
+        // item's end (a partial last round, the same n for every row) are
+        // -inf so that their weights come out 0
+        if (n < kRoundTok) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= n) (j < 32 ? s0[j] : s1[j - 32]) = __float_as_uint(-CUDART_INF_F);
+        }
         float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float v = __uint_as_float(j < 32 ? s0[j] : s1[j - 32]) * a.scale_log2;
-          x[j] = j < n ? v : -CUDART_INF_F;
-          mq[j & 3] = fmaxf(mq[j & 3], x[j]);
+        for (int j = 0; j < 32; ++j) {
+          mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(s0[j]));
+          mq[(j + 2) & 3] = fmaxf(mq[(j + 2) & 3], __uint_as_float(s1[j]));
         }
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
         // P buffer b was read by the P.V MMAs of round r - 2
         if (r >= 2 && !pv_wait(r - 2)) {
           ok = false;
@@ -458,12 +497,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           l *= alpha;
           if (need) m_used = mx;
         }
+        // weights 2^(s scale_log2 - m_used), one FMA and one exp2 each
         uint32_t pw[32];
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        const float neg_m = -m_used;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float p0 = fast_exp2(x[2 * j] - m_used), p1 = fast_exp2(x[2 * j + 1] - m_used);
-          ps[j & 3] += p0 + p1;
+          const uint32_t* src = j < 16 ? s0 : s1;
+          const int c = 2 * (j & 15);
+          const float p0 = fast_exp2(fmaf(__uint_as_float(src[c]), a.scale_log2, neg_m));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(src[c + 1]), a.scale_log2, neg_m));
+          ps[j & 3] += p0;
+          ps[(j + 2) & 3] += p1;
           pw[j] = pack_bf16(p0, p1);
         }
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);

@@ -265,6 +265,21 @@ int pkd_append_kv_ex(const void *k_new, const void *v_new, const int32_t *batch_
                      void *kv, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
                      int32_t head_dim, uint32_t flags, int32_t *err, void *stream);
 
+/* Self-test of the device-side bounded waits (failure detection without a
+ * GPU fault; FlashInfer, in depth, "Failure modes in production": errors come
+ * back as status, never as a hang).  Launches one small kernel on `stream`
+ * whose waits, on barriers nothing arrives on, use the same bounded wait as
+ * the decode and prefix kernels: with mode 0 one wait runs out its limit
+ * (about 2 s) and ORs PKD_DEV_ERR_TIMEOUT into *d_err; with mode 1 a second
+ * waiter, started half a limit later, must stop on the first one's abort
+ * flag instead of running out its own limit.  d_err (int32) and d_wait_ns
+ * (2 x uint64: each wait's duration, 0 for a wait that was not run) are
+ * device pointers owned by the caller, who zeroes *d_err and synchronizes
+ * before reading them.  Errors: INVALID_ARG (mode not 0 or 1, null pointer),
+ * CUDA (launch failed). */
+int pkd_selftest_bounded_wait(int32_t mode, int32_t *d_err, unsigned long long *d_wait_ns,
+                              void *stream);
+
 /* Read and clear the device error word (synchronizes `stream`).
  * *dev_err receives PKD_DEV_ERR_* bits (0 = none). */
 int pkd_last_device_error(pkd_ctx *ctx, void *stream, int32_t *dev_err);

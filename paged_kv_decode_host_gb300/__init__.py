@@ -48,6 +48,7 @@ EXPORTS = (
     "pkd_graph_capture", "pkd_graph_capture_io", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
     "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
+    "pkd_selftest_bounded_wait",
 )
 
 
@@ -130,6 +131,7 @@ def load():
         "pkd_plan_shared": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(u64)]),
         "pkd_plan_host_shared": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp, sz,
                                                 ctypes.POINTER(PlanInfo)]),
+        "pkd_selftest_bounded_wait": (ctypes.c_int, [i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -506,6 +508,21 @@ class BatchDecodeWithPagedKVCache:
             self.close()
         except Exception:
             pass
+
+
+def selftest_bounded_wait(mode=0, device=None):
+    """Run the device-side bounded-wait self-test (see pkd_selftest_bounded_wait)
+    and wait for it.  Returns (error bits, [wait 0 ns, wait 1 ns])."""
+    import torch
+    dev = torch.device("cuda" if device is None else device)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ns = torch.zeros(2, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        _check(load().pkd_selftest_bounded_wait(int(mode), ctypes.c_void_p(err.data_ptr()),
+                                                ctypes.c_void_p(ns.data_ptr()), _stream_ptr()),
+               "pkd_selftest_bounded_wait")
+        torch.cuda.synchronize(dev)
+    return int(err.item()), [int(x) for x in ns.tolist()]
 
 
 def merge_states(v_a, s_a, v_b, s_b, v_out=None, s_out=None, stream=None):

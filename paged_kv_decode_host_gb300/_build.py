@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkd.so")
 SOURCES = ["planner.cpp", "api.cu", "decode_kernel.cu", "prefix_tc_kernel.cu",
-           "merge_kernels.cu", "static_scratch.cu", "append_kernel.cu"]
+           "merge_kernels.cu", "static_scratch.cu", "append_kernel.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

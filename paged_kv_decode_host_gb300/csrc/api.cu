@@ -44,6 +44,7 @@ struct pkd_ctx {
   int next_staging = 0;
   uint64_t epoch = 0;
   pkd_plan_info info{};
+  int32_t max_chunks = 0;   // header word H_MAXCHUNKS of the published plan
 };
 
 struct pkd_graph {
@@ -213,7 +214,8 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   m.off_units = ctx->layout.units;
   m.off_merge = ctx->layout.merge_indptr;
   m.hq = c.num_qo_heads;
-  if (launch_merge_partials(m, ctx->merge_grid, stream) != cudaSuccess) return PKD_E_CUDA;
+  if (launch_merge_partials(m, ctx->merge_grid, ctx->max_chunks, stream) != cudaSuccess)
+    return PKD_E_CUDA;
   return PKD_OK;
 }
 
@@ -380,6 +382,7 @@ static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n
   ctx->next_staging = k ^ 1;
   info.page_tiles = ctx->kind.tmap ? 1 : 0;
   ctx->info = info;
+  ctx->max_chunks = words[H_MAXCHUNKS];
   ctx->epoch += 1;
   if (epoch) *epoch = ctx->epoch;
   return PKD_OK;

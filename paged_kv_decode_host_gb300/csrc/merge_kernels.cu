@@ -44,10 +44,16 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 //    units still get a block.  (Measured: with few tasks the block form is
 //    the faster one, as every block then carries work.)
 // With M known up front no term rescales a running sum, so the loads of a
-// warp stay in flight together.  Fixed assignment and order:
-// bit-reproducible.
+// warp can stay in flight together.  kBatch > 1 (plans that split a request
+// into more than kLongUnit chunks) makes that explicit in the block path: a
+// warp issues the loads of kBatch slots before adding their terms, so a
+// 250-chunk request costs a few memory round trips per warp instead of one
+// per slot; it needs more registers (fewer resident blocks), which plans of
+// short units do not repay, so they get kBatch = 1.  The terms are added in
+// the same order either way.  Fixed assignment and order: bit-reproducible.
 constexpr int kWarpSlots = 32;
 
+template <int kBatch>
 __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
   constexpr int kWarps = kMergeThreads / 32;
   __shared__ float wm[kWarps];
@@ -128,18 +134,47 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) m = fmaxf(m, wm[w]);
     // ---- pass 2: this warp's share of sum exp2(L - M) O and sum exp2(L - M)
+    // slots w, w + 8, ... (in batches of kBatch: a batch's loads are all
+    // issued before its terms are added, in the same order)
     float z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kBatch == 1) {
 #pragma unroll 8
-    for (int s = s0 + warp; s < s1; s += kWarps) {
-      const float w = exp2f(a.l_part[(int64_t)s * a.hq + h] * kLog2e - m);
-      const float4 o = *reinterpret_cast<const float4*>(
-          a.o_part + ((int64_t)s * a.hq + h) * kHeadDim + 4 * lane);
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
-      z += w;
+      for (int s = s0 + warp; s < s1; s += kWarps) {
+        const float w = exp2f(a.l_part[(int64_t)s * a.hq + h] * kLog2e - m);
+        const float4 o = *reinterpret_cast<const float4*>(
+            a.o_part + ((int64_t)s * a.hq + h) * kHeadDim + 4 * lane);
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+        z += w;
+      }
+    }
+    for (int base = s0 + warp; kBatch > 1 && base < s1; base += kBatch * kWarps) {
+      float lv[kBatch];
+      float4 ov[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int s = base + j * kWarps;
+        if (s < s1) {
+          lv[j] = a.l_part[(int64_t)s * a.hq + h];
+          ov[j] = *reinterpret_cast<const float4*>(a.o_part + ((int64_t)s * a.hq + h) * kHeadDim +
+                                                   4 * lane);
+        } else {
+          lv[j] = -CUDART_INF_F;   // weight 0
+          ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float w = exp2f(lv[j] * kLog2e - m);
+        acc.x = fmaf(w, ov[j].x, acc.x);
+        acc.y = fmaf(w, ov[j].y, acc.y);
+        acc.z = fmaf(w, ov[j].z, acc.z);
+        acc.w = fmaf(w, ov[j].w, acc.w);
+        z += w;
+      }
     }
     *reinterpret_cast<float4*>(&wacc[warp][4 * lane]) = acc;
     if (lane == 0) wz[warp] = z;
@@ -207,7 +242,8 @@ __global__ void __launch_bounds__(256) merge_states_kernel(
 
 }  // namespace
 
-cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_merge_partials(const MergeArgs& a, int grid, int32_t max_chunks,
+                                  cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMergeThreads);
@@ -218,7 +254,8 @@ cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t str
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_partials_kernel, a);
+  if (max_chunks > kLongUnit) return cudaLaunchKernelEx(&cfg, merge_partials_kernel<8>, a);
+  return cudaLaunchKernelEx(&cfg, merge_partials_kernel<1>, a);
 }
 
 cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,

@@ -171,7 +171,12 @@ cudaError_t encode_q_map(const void* q, int32_t batch, int32_t hq, int32_t hkv,
 bool use_mma_consumer(int group, uint32_t flags);
 // Merge grid for a persistent decode grid of n_cta CTAs.
 inline int merge_grid_for(int n_cta) { return 8 * n_cta; }
-cudaError_t launch_merge_partials(const MergeArgs& a, int grid, cudaStream_t stream);
+// max_chunks: the most chunks of any split request of the plan (header word
+// H_MAXCHUNKS); above kLongUnit the merge keeps several slots' loads in flight
+// per warp.  Any value gives the same results.
+constexpr int32_t kLongUnit = 64;
+cudaError_t launch_merge_partials(const MergeArgs& a, int grid, int32_t max_chunks,
+                                  cudaStream_t stream);
 cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,
                                 const float* s_b, void* v_out, float* s_out,
                                 int64_t rows, int head_dim, cudaStream_t stream);

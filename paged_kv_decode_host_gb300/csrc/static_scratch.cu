@@ -150,7 +150,7 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
   m.off_units = L.units;
   m.off_merge = L.merge_indptr;
   m.hq = cfg->num_qo_heads;
-  if (launch_merge_partials(m, merge_grid_for(cfg->num_ctas), s) != cudaSuccess)
+  if (launch_merge_partials(m, merge_grid_for(cfg->num_ctas), h[H_MAXCHUNKS], s) != cudaSuccess)
     return PKD_E_CUDA;
   return PKD_OK;
 }

@@ -308,6 +308,33 @@ def test_merge_paths_at_the_32_chunk_boundary():
     _check(out, lse, ref_o, ref_l)
 
 
+def test_merge_batched_loads_for_long_units():
+    """A plan with a request split into more than 64 chunks takes the merge
+    whose warps keep several slots' loads in flight (units of 64, 65 and 130
+    chunks in one plan), against the oracle."""
+    lens = [1024, 1040, 2080, 40]
+    w = workloads.Workload("m130", 79, 32, 8, 128, 16, 1, tuple(lens),
+                           sum(-(-l // 16) for l in lens) + 2)
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    dec = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, 16, max_batch=4,
+                                          max_num_pages=int(t["indptr"][-1]),
+                                          num_pages=w.pool_pages, num_ctas=152, alpha=0,
+                                          min_chunk_tokens=16, chunk_rule="search")
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    words, info, off = dec.schedule()
+    assert info["chunk_tokens"] == 16
+    units = pkd.decode_schedule(words, off, info)["units"]
+    assert sorted(n for _, n in units) == [3, 64, 65, 130]
+    out, lse = dec.run(q, kv)
+    out2, lse2 = dec.run(q, kv)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    ref_o, ref_l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=32, hkv=8)
+    _check(out, lse, ref_o, ref_l)
+
+
 def test_merge_warp_mode_many_units():
     """At least 4 merge tasks per merge block: the warp-per-task merge,
     against the oracle on every element (20 requests, 16 split, Hq 16 ->

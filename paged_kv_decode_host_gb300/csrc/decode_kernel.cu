@@ -115,7 +115,7 @@ __device__ __forceinline__ void rs_level(const float (&v)[N], float (&o)[N / 2],
 // are in-page bytes the consumers mask (scores) or zero (V).
 // Token rows: stage = [K rows][V rows] at the padded row stride; lane j
 // copies token j's K row and V row (valid tokens only).
-template <int kTokens, bool kTiles>
+template <int kTokens, bool kTiles, int kRing>
 __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* stages,
                              int stage_bytes, uint64_t* full, uint64_t* empty,
                              volatile int* abort_flag, int lane) {
@@ -134,8 +134,8 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
     const int tb = item[1], te = item[2], poff = item[4];
     for (int t = tb; t < te; t += kTokens) {
       const int n = min(kTokens, te - t);
-      const int slot = (int)(stage % kStages);
-      const uint32_t round = stage / kStages;
+      const int slot = (int)(stage % kRing);
+      const uint32_t round = stage / kRing;
       // this lane's token (rows) or box (tiles), and its page id
       const int nbox = (n + 15) >> 4;
       const int tok = kTiles ? t + 16 * (lane >> 1) : t + lane;
@@ -200,9 +200,9 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
   // Drain: wait for the last issued phase of every slot, so no copy is in
   // flight into shared memory when the CTA exits.
   if (lane == 0) {
-    for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+    for (uint32_t s = 0; s < (uint32_t)kRing; ++s) {
       if (stage > s) {
-        const uint32_t last_round = (stage - 1 - s) / kStages;
+        const uint32_t last_round = (stage - 1 - s) / kRing;
         if (!mbar_wait(&full[s], last_round & 1u, nullptr)) atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
       }
     }
@@ -221,7 +221,7 @@ struct Shape {
   static constexpr int TOKBITS = (G == 1) ? 14 : (16 / G - 1);
 };
 
-template <int G>
+template <int G, int kRing>
 __device__ void run_consumer_fma(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                              int stage_bytes, uint64_t* full, uint64_t* empty,
                              volatile int* abort_flag, float* pbuf, float* sbuf, int warp,
@@ -277,8 +277,8 @@ __device__ void run_consumer_fma(const DecodeArgs& a, int it0, int it1, const ui
 
     for (int t = tb; t < te; t += kTS) {
       const int n = min(kTS, te - t);
-      const int slot = (int)(stage % kStages);
-      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      const int slot = (int)(stage % kRing);
+      const bool got = mbar_wait(&full[slot], (stage / kRing) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
         return;
@@ -545,7 +545,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int req, int h
   }
 }
 
-template <int G, bool kTiles>
+template <int G, bool kTiles, int kRing>
 __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                                  int stage_bytes, uint64_t* full, uint64_t* empty,
                                  volatile int* abort_flag, int warp, int lane) {
@@ -583,8 +583,8 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
 
     for (int t = tb; t < te; t += kTS) {
       const int n = min(kTS, te - t);
-      const int slot = (int)(stage % kStages);
-      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      const int slot = (int)(stage % kRing);
+      const bool got = mbar_wait(&full[slot], (stage / kRing) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
         return;
@@ -723,7 +723,7 @@ __device__ __forceinline__ float softmax_row(float (&s4)[4], float& m_run, float
   return alpha;
 }
 
-template <int G, bool kTiles>
+template <int G, bool kTiles, int kRing>
 __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
                                        const uint8_t* stages, int stage_bytes, uint64_t* full,
                                        uint64_t* empty, volatile int* abort_flag, int warp,
@@ -766,8 +766,8 @@ __device__ void run_consumer_mma_block(const DecodeArgs& a, int it0, int it1,
 
     for (int t = tb; t < te; t += kTS) {
       const int n = min(kTS, te - t);
-      const int slot = (int)(stage % kStages);
-      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      const int slot = (int)(stage % kRing);
+      const bool got = mbar_wait(&full[slot], (stage / kRing) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
         return;
@@ -1065,7 +1065,7 @@ __device__ __forceinline__ void fp8_stage(const Fp8Frags<kTiles>& fr, uint32_t s
   }
 }
 
-template <int G, bool kTiles>
+template <int G, bool kTiles, int kRing>
 __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, const uint8_t* stages,
                                      int stage_bytes, uint64_t* full, uint64_t* empty,
                                      volatile int* abort_flag, int warp, int lane) {
@@ -1118,8 +1118,8 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
 
     for (int t = tb; t < te; t += T) {
       const int n = min(T, te - t);
-      const int slot = (int)(stage % kStages);
-      const bool got = mbar_wait(&full[slot], (stage / kStages) & 1u, abort_flag);
+      const int slot = (int)(stage % kRing);
+      const bool got = mbar_wait(&full[slot], (stage / kRing) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
         return;
@@ -1176,23 +1176,24 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kStageTokens = kFp8 ? kFp8Tokens : kTS;
+  constexpr int kRing = ring_depth(kMma, kBlock, kFp8);
   const int stage_bytes = stage_bytes_for(a.row_bytes, kStageTokens, kTiles);
   // the 128-byte swizzle repeats every 1024 bytes: page-tile stages start on
   // a 1024-byte boundary (the launch reserves the slack)
   uint8_t* stages = smem;
   if constexpr (kTiles) stages += (1024u - (smem_u32(smem) & 1023u)) & 1023u;
-  float* pbuf_all = reinterpret_cast<float*>(stages + (size_t)kStages * stage_bytes);
+  float* pbuf_all = reinterpret_cast<float*>(stages + (size_t)kRing * stage_bytes);
   float* sbuf_all = pbuf_all + kMaxKvHeads * kTS * G;
   uint64_t* full = reinterpret_cast<uint64_t*>(sbuf_all + kMaxKvHeads * 32);
-  uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  uint64_t* empty = full + kRing;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kRing);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_cons = a.hkv;
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], (uint32_t)n_cons);
     }
@@ -1214,20 +1215,20 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
     return;
   }
   if (warp == n_cons) {
-    run_producer<kStageTokens, kTiles>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+    run_producer<kStageTokens, kTiles, kRing>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
                                        lane);
   } else if (warp < n_cons) {
     if constexpr (kFp8) {
-      run_consumer_mma_fp8<G, kTiles>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+      run_consumer_mma_fp8<G, kTiles, kRing>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
                                       warp, lane);
     } else if constexpr (kBlock) {
-      run_consumer_mma_block<G, kTiles>(a, it0, it1, stages, stage_bytes, full, empty,
+      run_consumer_mma_block<G, kTiles, kRing>(a, it0, it1, stages, stage_bytes, full, empty,
                                         abort_flag, warp, lane);
     } else if constexpr (kMma) {
-      run_consumer_mma<G, kTiles>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
+      run_consumer_mma<G, kTiles, kRing>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag, warp,
                                   lane);
     } else {
-      run_consumer_fma<G>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
+      run_consumer_fma<G, kRing>(a, it0, it1, stages, stage_bytes, full, empty, abort_flag,
                           pbuf_all + warp * kTS * G, sbuf_all + warp * 32, warp, lane);
     }
   }
@@ -1277,8 +1278,9 @@ int decode_smem_bytes(int hkv, const DecodeKind& k) {
   if (k.dense) return prefix_tc_smem_bytes();
   const int row = hkv * kHeadDim * (k.fp8 ? 1 : 2);
   const int tokens = k.fp8 ? kFp8Tokens : kTS;
-  return kStages * stage_bytes_for(row, tokens, k.tmap) + (k.tmap ? 1024 : 0) +
-         kMaxKvHeads * kTS * k.group * 4 + kMaxKvHeads * 32 * 4 + 2 * kStages * 8 + 16;
+  const int ring = ring_depth(k.mma, k.block, k.fp8);
+  return ring * stage_bytes_for(row, tokens, k.tmap) + (k.tmap ? 1024 : 0) +
+         kMaxKvHeads * kTS * k.group * 4 + kMaxKvHeads * 32 * 4 + 2 * ring * 8 + 16;
 }
 
 cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes) {

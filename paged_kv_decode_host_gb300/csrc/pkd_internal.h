@@ -16,7 +16,15 @@ constexpr int32_t kMagic = 0x31444B50;  // "PKD1"
 constexpr int kHeadDim = 128;           // the decode kernel's D
 constexpr int kMaxKvHeads = 8;          // one consumer warp per KV head
 constexpr int kWarpTokens = 16;         // tokens per stage (each warp sees all 16)
-constexpr int kStages = 3;              // shared-memory ring depth
+// Shared-memory ring depth (stages of 16 tokens, 32 for E4M3) per consumer:
+// with the bf16 tensor-core consumer two stages in flight per SM read HBM
+// faster than three (fewer page-tile copies outstanding: measured on the
+// Llama-shaped step, its HND form and the token-sparse batch); the consumers
+// with more arithmetic per byte (E4M3, CUDA cores, shared-prefix row blocks)
+// need the third stage to cover it.
+__host__ __device__ constexpr int ring_depth(bool mma, bool block, bool fp8) {
+  return (mma && !block && !fp8) ? 2 : 3;
+}
 constexpr int kDefaultAlpha = 32;
 constexpr int kDefaultMinChunk = 256;
 constexpr int kMergeThreads = 256;

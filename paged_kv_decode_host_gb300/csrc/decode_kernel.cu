@@ -126,7 +126,6 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
   const int vb = rows_v_base(a, kTokens);
   const uint32_t box = (uint32_t)(16 * row);
   const uint64_t policy = l2_evict_first_policy();
-  bool waited = false;  // programmatic-launch wait, before the first KV read
   uint32_t stage = 0;
   bool ok = true;
   for (int it = it0; it < it1 && ok; ++it) {
@@ -160,10 +159,6 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
                                                   : (uint32_t)(2 * n * row));
       __syncwarp();
       if (page >= 0) {
-        if (!waited) {
-          pdl_wait();
-          waited = true;
-        }
         uint8_t* st = stages + (size_t)slot * stage_bytes;
         if constexpr (kTiles) {
           const int c = lane & 1;
@@ -196,7 +191,7 @@ __device__ void run_producer(const DecodeArgs& a, int it0, int it1, uint8_t* sta
       ++stage;
     }
   }
-  if (!waited) pdl_wait();
+  pdl_wait();   // complete only after the previous kernel (see the kernel's note)
   // Drain: wait for the last issued phase of every slot, so no copy is in
   // flight into shared memory when the CTA exits.
   if (lane == 0) {
@@ -1201,11 +1196,16 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  // The schedule is only ever written by host-to-device copies, which order
-  // fully before this kernel, so it is read before the programmatic-launch
-  // wait.  q, the KV cache, the outputs and the partial states may belong to
-  // the previous kernel in the stream: each role waits (griddepcontrol.wait)
-  // before touching them.
+  // Programmatic dependent launch: this grid may start while the previous
+  // kernel in the stream still runs.  The schedule is only ever written by
+  // host-to-device copies, which order fully before this kernel, and the KV
+  // cache is never written by a kernel that lets its dependents start early
+  // (the merge and prefix kernels do not write it; the append kernel and any
+  // kernel launched without the programmatic attribute release dependents
+  // only when they complete), so the producer streams KV tiles at once.  q,
+  // the outputs and the partial states may belong to the previous kernel:
+  // the consumers wait (griddepcontrol.wait) before touching them, and every
+  // role waits before the grid completes.
   const int it0 = a.sched[a.off_cta + blockIdx.x];
   const int it1 = a.sched[a.off_cta + blockIdx.x + 1];
   if (it0 >= it1) {

@@ -206,12 +206,14 @@ int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
  * expect_epoch: 0 accepts any plan; otherwise must equal the current plan's
  * epoch (STALE_PLAN otherwise).  Launches the decode kernel and the merge
  * kernel on `stream`, with programmatic dependent launch: the decode kernel
- * may start while the previous kernel in the stream runs and reads the KV
- * cache at once, so a kernel that writes the cache ahead of it in the same
+ * may start while the previous kernel in the stream runs and reads q and
+ * the KV cache at once, so a kernel that writes them ahead of it in the same
  * stream must not release its dependents before it completes (kernels
  * launched without the programmatic attribute, such as pkd_append_kv's,
- * never do); q, out and lse are touched only after the previous kernel
- * completes.  Errors: INVALID_ARG, NO_PLAN, STALE_PLAN, CUDA. */
+ * never do), and q and kv must not alias the out / lse of an earlier run
+ * still in the stream; out, lse and the partial states are written only
+ * after the previous kernel completes.
+ * Errors: INVALID_ARG, NO_PLAN, STALE_PLAN, CUDA. */
 int pkd_run(pkd_ctx *ctx, const void *q, const void *kv, void *out, float *lse,
             uint64_t expect_epoch, void *stream);
 

@@ -554,7 +554,9 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
   // the item and its queries are fetched one item ahead
   const int32_t* item = a.sched + a.off_items + (int64_t)it0 * kItemWords;
   int req = item[0], tb = item[1], te = item[2], dst = item[3];
-  pdl_wait();   // q may come from the previous kernel in the stream
+  // q is read at once, like the KV cache; the first write (outputs or the
+  // partial states the previous kernel may still read) waits for it
+  bool waited = false;
   uint32_t qa0[8], qa2[8];
   load_q_frags<G>(a, req, hk, grp, tig, row_ok, qa0, qa2);
 
@@ -582,6 +584,7 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
       const bool got = mbar_wait(&full[slot], (stage / kRing) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+        if (!waited) pdl_wait();   // complete only after the previous kernel
         return;
       }
       const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
@@ -650,6 +653,10 @@ __device__ void run_consumer_mma(const DecodeArgs& a, int it0, int it1, const ui
     float l = l_run;
     l += __shfl_xor_sync(kFull, l, 1);
     l += __shfl_xor_sync(kFull, l, 2);
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
     if (row_ok) {
       const float inv = a.v_scale / l;
       const float lse_nat = (m_run + log2f(l)) * 0.69314718055994530942f;
@@ -1071,7 +1078,7 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
   const bool row_ok = grp < G;
   const uint32_t stage0 = smem_u32(stages);
   const Fp8Frags<kTiles> fr(a, hk, lane);
-  pdl_wait();
+  bool waited = false;   // q is read at once; the first write waits (see run_consumer_mma)
   uint32_t stage = 0;
   for (int it = it0; it < it1; ++it) {
     const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
@@ -1117,6 +1124,7 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
       const bool got = mbar_wait(&full[slot], (stage / kRing) & 1u, abort_flag);
       if (!__all_sync(kFull, got)) {
         if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+        if (!waited) pdl_wait();   // complete only after the previous kernel
         return;
       }
       const uint32_t sbase = stage0 + (uint32_t)(slot * stage_bytes);
@@ -1134,6 +1142,10 @@ __device__ void run_consumer_mma_fp8(const DecodeArgs& a, int it0, int it1, cons
     float l = l_run;
     l += __shfl_xor_sync(kFull, l, 1);
     l += __shfl_xor_sync(kFull, l, 2);
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
     if (row_ok) {
       const float inv = a.v_scale / l;
       const float lse_nat = (m_run + log2f(l)) * 0.69314718055994530942f;
@@ -1202,9 +1214,11 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
   // cache is never written by a kernel that lets its dependents start early
   // (the merge and prefix kernels do not write it; the append kernel and any
   // kernel launched without the programmatic attribute release dependents
-  // only when they complete), so the producer streams KV tiles at once.  q,
-  // the outputs and the partial states may belong to the previous kernel:
-  // the consumers wait (griddepcontrol.wait) before touching them, and every
+  // only when they complete), so the producer streams KV tiles at once; the
+  // same holds for q, which the tensor-core consumers read at once too.  The
+  // outputs and the partial states may still be read by the previous kernel
+  // (the merge of the previous layer reads the partial-state slots): every
+  // consumer waits (griddepcontrol.wait) before its first write, and every
   // role waits before the grid completes.
   const int it0 = a.sched[a.off_cta + blockIdx.x];
   const int it1 = a.sched[a.off_cta + blockIdx.x + 1];

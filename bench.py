@@ -672,6 +672,109 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
                                       f"heads, fp64, one thread"}}
 
 
+# The Composable Format latency table of the pages (FlashInfer 完全拆解,
+# Composable Format 只在复用足够大时占优): (shared prefix tokens, batch) with
+# 128-token suffixes, and their microseconds for the composable and the single
+# format (FP16, GPU of that paper, not stated per table) -- context only.
+PREFIX_GRID = [(1024, 16, 45.17, 46.52), (8192, 16, 88.67, 226.57), (32768, 16, 217.42, 945.67),
+               (1024, 64, 87.86, 130.49), (8192, 64, 125.76, 931.75), (32768, 64, 254.54, 4090.0)]
+
+
+def run_prefix_sweep(args, rank, world):
+    """Shared prefix, composable against single format, over the pages' grid.
+    Composable: the prefix level planned once for the whole batch (the dense
+    tcgen05 kernel reads the prefix once per KV head) and the suffix level,
+    on two streams, joined by merge_states -- one CUDA graph.  Single: every
+    request over its full page table (prefix pages then its own), one decode
+    + merge.  GPU time per step: graph replays back to back, rotating over
+    enough cache copies that the step's bytes are not L2-resident; the host
+    plans once per case (its cost is not in these numbers)."""
+    import torch
+
+    import paged_kv_decode_host_gb300 as pkd
+
+    pkd.build()
+    pkd.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+    reps = max(args.steps, 20)
+    rows = []
+    launches = 0
+    for prefix, B, pages_comp, pages_single in PREFIX_GRID:
+        w = workloads.shared_prefix_case(prefix, B)
+        t = workloads.make_tables(w)
+        P = w.page_size
+        n_pre = prefix // P
+        pool_bytes = w.pool_pages * 2 * P * w.hkv * w.head_dim * 2
+        copies = max(2, int(np.ceil(1.2e9 / pool_bytes)))
+        kvs = workloads.make_kv(w, device=dev, layers=copies)
+        q = workloads.make_q(w, device=dev, layers=1)[0]
+        mk = lambda **kw: pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P,
+                                                         max_batch=B, num_pages=w.pool_pages,
+                                                         device=dev, **kw)
+        pre = mk(max_num_pages=n_pre, shared_prefix=True, dense_prefix=True)
+        pre.plan_shared(np.array([0, B], np.int32), np.array([0, n_pre], np.int32),
+                        np.asarray(t["prefix"][1][:n_pre], np.int32), np.array([P], np.int32))
+        suf = mk(max_num_pages=int(t["suffix"][0][-1]))
+        suf.plan(*t["suffix"])
+        single = mk(max_num_pages=int(t["indptr"][-1]))
+        single.plan(t["indptr"], t["indices"], t["last"])
+        po, so, out_c, out_s = (torch.empty_like(q) for _ in range(4))
+        pl, sl, lse_c, lse_s = (torch.empty(B, w.hq, dtype=torch.float32, device=dev)
+                                for _ in range(4))
+        comp = [_composed_step_graph((pre, suf), q, kvs[c], po, pl, so, sl, out_c, lse_c, side,
+                                     dev) for c in range(copies)]
+        sing = [single.capture([q], [kvs[c]], [out_s], [lse_s]) for c in range(copies)]
+        us = {}
+        for name, gs in (("composable", comp), ("single", sing)):
+            for k in range(3):
+                gs[k % copies].launch()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(reps):
+                gs[k % copies].launch()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us[name] = e0.elapsed_time(e1) * 1e3 / reps
+        # the two formats compute the same states (up to rounding)
+        comp[0].launch()
+        sing[0].launch()
+        torch.cuda.synchronize()
+        diff = float((out_c.float() - out_s.float()).abs().max())
+        ldiff = float((lse_c - lse_s).abs().max())
+        launches += reps * (5 + 2)
+        kv_once = (prefix + 128 * B) * 2 * w.hkv * w.head_dim * 2
+        rows.append({"prefix": prefix, "batch": B, "suffix": 128,
+                     "composable_us": round(us["composable"], 2),
+                     "single_us": round(us["single"], 2),
+                     "speedup": round(us["single"] / us["composable"], 2),
+                     "composable_GBps_prefix_once": round(kv_once / (us["composable"] * 1e3), 1),
+                     "single_GBps_per_request_reads": round(
+                         (prefix + 128) * B * 2 * w.hkv * w.head_dim * 2 / (us["single"] * 1e3), 1),
+                     "max_abs_diff_out": round(diff, 5), "max_abs_diff_lse": round(ldiff, 6),
+                     "pages_us_composable": pages_comp, "pages_us_single": pages_single,
+                     "cache_copies": copies})
+        for g in sing:
+            g.close()
+        del kvs, comp, sing, pre, suf, single
+        torch.cuda.empty_cache()
+    big = rows[-1]
+    return {"metric": "shared-prefix decode latency, composable vs single format "
+                      "(GPU us per step, CUDA-graph replay)",
+            "value": big["composable_us"], "unit": "us", "n_gpus": world, "steps": reps,
+            "warmup": 3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/KV, scattered pages)",
+            "config": {"workload": "prefix_sweep", "hq": 32, "hkv": 8, "head_dim": 128,
+                       "page_size": 16, "suffix": 128,
+                       "l2": "cache copies rotated per replay, >= 1.2 GB in total"},
+            "table": rows, "gpu_launches": launches,
+            "note": "pages_us_*: the pages' table (FP16, other GPU), context only"}
+
+
 def run_append(args, rank, world):
     """append_paged_kv_cache for the Llama-shaped step: each of the 64
     requests appends its new token (K and V rows, all 8 KV heads) into its
@@ -785,6 +888,9 @@ def run_reference(args, rank, world):
     import torch
     if args.workload == "append":
         return run_reference_append(args, world)
+    if args.workload == "prefix_sweep":
+        raise SystemExit("the reference arm times the oracle on one workload at a time; "
+                         "prefix_sweep is a table of GPU timings")
     w = workloads.workload(args.workload)
     t = workloads.make_tables(w)
     from oracle import _bits, _u8
@@ -838,7 +944,7 @@ def main():
     ap.add_argument("--workload", default="llama8b_step",
                     choices=["llama8b_step", "skewed", "token_sparse", "shared_prefix",
                              "llama8b_step_fp8", "llama8b_step_hnd", "llama8b_step_fp8_hnd",
-                             "shared_prefix_hnd", "append"])
+                             "shared_prefix_hnd", "append", "prefix_sweep"])
     ap.add_argument("--consumer", choices=["auto", "fma", "mma"], default="auto",
                     help="decode-kernel consumer: the default, or forced CUDA-core (fma) / "
                          "tensor-core (mma) folding of the GQA group")
@@ -869,8 +975,12 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    line = run_append(args, rank, world) if args.workload == "append" else \
-        run_ours(args, rank, world)
+    if args.workload == "append":
+        line = run_append(args, rank, world)
+    elif args.workload == "prefix_sweep":
+        line = run_prefix_sweep(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

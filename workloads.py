@@ -116,6 +116,9 @@ def workload(name: str) -> Workload:
         pool = prefix // 16 + _pages_for(suffix, 16)
         return Workload(name, 4, 32, 8, 128, 16, 1, lens, pool,
                         prefix_tokens=prefix, suffix_lens=suffix)
+    if name.startswith("prefix_") and "_b" in name:   # prefix_<tokens>_b<batch>
+        prefix, batch = name[len("prefix_"):].split("_b")
+        return shared_prefix_case(int(prefix), int(batch))
     if name == "token_sparse":
         g = torch.Generator().manual_seed(5)
         lens = tuple(_randint(g, 512, 2048, 512))
@@ -161,6 +164,19 @@ def page_table(kv_lens, page_size, page_ids=None):
 def _perm(seed: int, n: int) -> np.ndarray:
     g = torch.Generator().manual_seed(1000 + seed)
     return torch.randperm(n, generator=g).numpy().astype(np.int32)
+
+
+def shared_prefix_case(prefix: int, batch: int, suffix: int = 128) -> Workload:
+    """A batch of `batch` requests sharing a `prefix`-token prefix, each with
+    its own `suffix`-token tail (page size 16, Hq 32 / Hkv 8, D 128): the
+    shape of the Composable Format latency table (FlashInfer 完全拆解,
+    Composable Format 只在复用足够大时占优: suffix 128, batch 16 and 64,
+    prefix 1,024 / 8,192 / 32,768)."""
+    suffix_lens = tuple([suffix] * batch)
+    lens = tuple(prefix + s for s in suffix_lens)
+    pool = prefix // 16 + _pages_for(suffix_lens, 16)
+    return Workload(f"prefix_{prefix}_b{batch}", 6, 32, 8, 128, 16, 1, lens, pool,
+                    prefix_tokens=prefix, suffix_lens=suffix_lens)
 
 
 def make_tables(w: Workload):

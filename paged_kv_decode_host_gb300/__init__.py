@@ -238,6 +238,23 @@ def decode_schedule(words, off, info):
 
 
 _current_raw_stream = None
+_fast_plan = None     # the CPython plan fast path (module), False when not built
+_NOT_HANDLED = 1000   # its status for inputs it leaves to the general path
+
+
+def _fast():
+    """The compiled marshalling fast path for plan / plan_shared, if built."""
+    global _fast_plan
+    if _fast_plan is None:
+        try:
+            from . import _pkd_plan as m
+            lib = load()
+            m.init(ctypes.cast(lib.pkd_plan, ctypes.c_void_p).value,
+                   ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value)
+            _fast_plan = m
+        except ImportError:
+            _fast_plan = False
+    return _fast_plan or None
 
 
 def _stream_ptr(stream=None):
@@ -342,6 +359,7 @@ class BatchDecodeWithPagedKVCache:
             _check(lib.pkd_create(ctypes.byref(self.cfg), ctypes.c_void_p(self.workspace.data_ptr()),
                                   nbytes, ctypes.byref(h)), "pkd_create")
         self._h = h
+        self._hv = h.value
         self._lib = lib
         self._ep = ctypes.c_uint64()
         self._ep_ref = ctypes.byref(self._ep)
@@ -351,6 +369,15 @@ class BatchDecodeWithPagedKVCache:
     # -- plan ---------------------------------------------------------------
     def plan(self, indptr, indices, last_page_len, stream=None):
         """Schedule one decode step from host int32 arrays.  Returns the epoch."""
+        fast = _fast()
+        if fast is not None:
+            st, ep = fast.plan(self._hv, indptr, indices, last_page_len, _stream_ptr(stream))
+            if st != _NOT_HANDLED:
+                if st:
+                    _check(st, "pkd_plan")
+                self.epoch = ep
+                self.batch = len(last_page_len)
+                return ep
         indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
         batch = last.shape[0]
         if indptr.shape[0] != batch + 1:
@@ -369,6 +396,16 @@ class BatchDecodeWithPagedKVCache:
         """Plan a shared-prefix level: requests group_indptr[j] ..
         group_indptr[j+1]-1 attend over group j's pages (CSR over groups).
         Needs ``shared_prefix=True``.  Returns the epoch."""
+        fast = _fast()
+        if fast is not None:
+            st, ep = fast.plan_shared(self._hv, group_indptr, indptr, indices, last_page_len,
+                                      _stream_ptr(stream))
+            if st != _NOT_HANDLED:
+                if st:
+                    _check(st, "pkd_plan_shared")
+                self.epoch = ep
+                self.batch = int(group_indptr[-1]) if len(last_page_len) else 0
+                return ep
         gi = _host_i32(group_indptr)
         indptr, indices, last = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
         n_groups = last.shape[0]

@@ -2,6 +2,9 @@
 
 Each translation unit compiles in its own nvcc process (in parallel); the
 objects are linked into ``paged_kv_decode_host_gb300/libpkd.so``.  No CMake.
+Beside it, when the Python headers are installed, the host C compiler builds
+``_pkd_plan``: the binding's argument-marshalling fast path for the per-step
+plan calls (the binding falls back to ctypes without it).
 """
 from __future__ import annotations
 
@@ -9,6 +12,7 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
 from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -20,6 +24,28 @@ LIB = os.path.join(HERE, "libpkd.so")
 SOURCES = ["planner.cpp", "api.cu", "decode_kernel.cu", "prefix_tc_kernel.cu",
            "merge_kernels.cu", "static_scratch.cu", "append_kernel.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+PYPLAN = os.path.join(HERE, "_pkd_plan" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
+def _python_include():
+    inc = sysconfig.get_paths().get("include")
+    return inc if inc and os.path.exists(os.path.join(inc, "Python.h")) else None
+
+
+def _build_fast_plan():
+    """The CPython plan fast path; None when no Python headers or C compiler."""
+    inc = _python_include()
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if inc is None or cc is None:
+        return None
+    tmp = PYPLAN + f".tmp{os.getpid()}"
+    r = subprocess.run([cc, "-O2", "-shared", "-fPIC", f"-I{inc}",
+                        os.path.join(CSRC, "pyplan.c"), "-o", tmp], capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(f"_pkd_plan not built (ctypes path used):\n{r.stderr}\n")
+        return None
+    os.replace(tmp, PYPLAN)
+    return PYPLAN
 
 
 def _nvcc() -> str:
@@ -36,6 +62,8 @@ def _flags():
 
 def _stale() -> bool:
     if not os.path.exists(LIB):
+        return True
+    if _python_include() is not None and not os.path.exists(PYPLAN):
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "pkd.h")]
@@ -59,8 +87,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    with ThreadPoolExecutor(max_workers=len(SOURCES) + 1) as ex:
+        fast = ex.submit(_build_fast_plan)
         objs = list(ex.map(compile_one, SOURCES))
+        fast.result()
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared", "-o", tmp, *objs, *ARCH, "-Xcompiler", "-fPIC", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -262,3 +262,56 @@ def test_dense_prefix_plan_bit_exact_random(lib, seed):
             a[tb:te] += 1
     assert len(seen) == len(req_row) * hkv
     assert all(np.all(a == 1) for a in seen.values())
+
+
+def test_plan_fast_path_marshalling():
+    """The compiled plan fast path hands the C ABI the arrays' own buffers,
+    the batch and the stream, returns the entry point's status and epoch, and
+    leaves every input it cannot pass as-is (int64, lists, short or
+    non-contiguous arrays) to the general path (status 1000).  Checked on
+    the CPU against a stand-in entry point; the real ones are restored."""
+    import ctypes
+    m = pytest.importorskip("paged_kv_decode_host_gb300._pkd_plan")
+    lib = pkd.load()
+    calls = []
+    plan_t = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                              ctypes.POINTER(ctypes.c_uint64))
+    shared_t = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64))
+
+    def fake_plan(ctx, ip, ix, la, batch, stream, ep):
+        calls.append(("plan", ctx, ip, ix, la, batch, stream))
+        ep[0] = 41
+        return -2 if batch == 3 else 0
+
+    def fake_shared(ctx, gi, ng, ip, ix, la, stream, ep):
+        calls.append(("shared", ctx, gi, ng, ip, ix, la, stream))
+        ep[0] = 42
+        return 0
+
+    cb_plan, cb_shared = plan_t(fake_plan), shared_t(fake_shared)
+    try:
+        m.init(ctypes.cast(cb_plan, ctypes.c_void_p).value,
+               ctypes.cast(cb_shared, ctypes.c_void_p).value)
+        ip = np.array([0, 3, 4], np.int32)
+        ix = np.arange(4, dtype=np.int32)
+        la = np.array([5, 16], np.int32)
+        assert m.plan(123, ip, ix, la, 456) == (0, 41)
+        assert calls[-1] == ("plan", 123, ip.ctypes.data, ix.ctypes.data, la.ctypes.data, 2, 456)
+        ip3, la3 = np.array([0, 1, 2, 4], np.int32), np.array([1, 1, 1], np.int32)
+        assert m.plan(1, ip3, ix, la3, 0)[0] == -2          # the entry point's status
+        n = len(calls)
+        for args in ((ip.astype(np.int64), ix, la), ([0, 3, 4], ix, la), (ip, ix[:2], la),
+                     (ip[:2], ix, la), (np.zeros(6, np.int32)[::2], ix, la)):
+            assert m.plan(1, *args, 0)[0] == 1000
+        assert len(calls) == n                               # none reached the entry point
+        gi = np.array([0, 32], np.int32)
+        assert m.plan_shared(7, gi, np.array([0, 4], np.int32), ix, np.array([16], np.int32),
+                             9) == (0, 42)
+        assert calls[-1][0] == "shared" and calls[-1][3] == 1 and calls[-1][7] == 9
+        assert m.plan_shared(7, gi, ip, ix, la, 9)[0] == 1000   # groups mismatch
+    finally:
+        m.init(ctypes.cast(lib.pkd_plan, ctypes.c_void_p).value,
+               ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value)

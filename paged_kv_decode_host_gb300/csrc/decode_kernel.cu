@@ -13,9 +13,10 @@
 // GB300 design:
 //  * Grid = the plan's fixed CTA count (persistent; only the queue contents
 //    change between plans, so launches can be captured in a CUDA graph).
-//  * One producer warp streams the item's tokens into a 3-deep ring of
-//    shared-memory stages with TMA (completion on an mbarrier, L2
-//    evict-first).  A stage holds 16 tokens (32 for an e4m3 cache).  Two
+//  * One producer warp streams the item's tokens into a ring of shared-memory
+//    stages with TMA (completion on an mbarrier, L2 evict-first): two stages
+//    deep for the bf16 tensor-core consumer, three for the others
+//    (ring_depth).  A stage holds 16 tokens (32 for an e4m3 cache).  Two
 //    producers:
 //      - page tiles (page size a multiple of 16): one tensor-map copy
 //        (cp.async.bulk.tensor, 5-D) moves 16 tokens of K (or V) of all KV
@@ -35,8 +36,10 @@
 //    (mma.sync m16n8k16, bf16 in, fp32 accumulate); the CUDA-core consumer
 //    (fp32 FMA, lanes split D, reduce-scatter of the dot products across a
 //    half-warp) is kept as an option.  Softmax statistics are fp32.
-//  * Programmatic dependent launch: CTAs trigger the next kernel at start and
-//    wait for the previous one only before touching q / KV / outputs.
+//  * Programmatic dependent launch: CTAs trigger the next kernel at start; the
+//    producer streams KV tiles at once, the tensor-core consumers read q at
+//    once and wait for the previous kernel only before their first write of
+//    outputs or partial states (see the note in decode_kernel).
 //  * Every wait is bounded (~2 s of %globaltimer); on timeout the kernel sets
 //    the device error word, stops issuing copies, waits (bounded) for the
 //    copies already in flight, and returns.

@@ -3,17 +3,21 @@
 Every step of the computation runs in the CUDA library (``libpkd.so``, built
 in-tree by :func:`build`); this module only marshals arguments: it checks
 dtypes, shapes and devices, passes ``tensor.data_ptr()`` and the current
-CUDA stream through ctypes, and raises on a non-zero status.  There is no
-fallback: if the library is missing or was built for another machine, the
-import of the binding fails loudly.
+CUDA stream through ctypes (the per-step plan calls through the small
+compiled ``_pkd_plan`` module when it was built), and raises on a non-zero
+status.  There is no fallback: if the library is missing or was built for
+another machine, loading it fails loudly.
 
 API (names follow the pages' plan / run / merge_states):
 
 * :class:`BatchDecodeWithPagedKVCache` -- ``plan(indptr, indices,
-  last_page_len)`` once per step, ``run(q, kv_cache)`` once per layer,
-  ``capture(...)`` for a CUDA graph of a whole step.
+  last_page_len)`` (or ``plan_shared`` for a shared-prefix level) once per
+  step, ``run(q, kv_cache)`` once per layer, ``capture(...)`` for a CUDA
+  graph of a whole step.
 * :func:`merge_states` -- exact LSE merge of two attention states.
+* :func:`append_kv` -- write a step's new K / V rows into their page slots.
 * :func:`plan_host` -- the scheduler alone on the host (no GPU), for tests.
+* :func:`selftest_bounded_wait` -- the device-side bounded-wait self-test.
 """
 from __future__ import annotations
 
@@ -24,7 +28,8 @@ import numpy as np
 
 __all__ = [
     "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states", "append_kv",
-    "plan_host", "schedule_layout", "Graph", "STATUS",
+    "plan_host", "plan_host_shared", "schedule_layout", "selftest_bounded_wait", "Graph",
+    "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

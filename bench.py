@@ -254,8 +254,8 @@ def run_ours(args, rank, world):
     nnz = int(t["indptr"][-1])
     layers = args.layers if args.layers > 0 else w.layers
     # distinct caches per replay for single-layer workloads so no step reads
-    # another step's bytes out of L2
-    copies = 1 if layers > 1 else max(1, int(np.ceil(
+    # another step's bytes out of L2: at least 4, and at least 1.2 GB in all
+    copies = 1 if layers > 1 else max(4, int(np.ceil(
         1.2e9 / (w.pool_pages * 2 * P * w.hkv * w.head_dim * w.kv_elem_bytes))))
     n_kv = layers * copies
     if w.kv_dtype == "e4m3":

@@ -273,6 +273,22 @@ int pkd_append_kv_ex(const void *k_new, const void *v_new, const int32_t *batch_
                      void *kv, int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
                      int32_t head_dim, uint32_t flags, int32_t *err, void *stream);
 
+/* pkd_append_kv_ex for every layer of a step in one launch: the layers share
+ * the step's tokens and page table (batch_indices, positions, indptr,
+ * indices, last_page_len, as in pkd_append_kv), and layer l's rows
+ * k_new[l] / v_new[l] ([n][Hkv][D] each) go into cache kv[l].  k_new, v_new
+ * and kv are HOST arrays of `layers` device pointers (1 <= layers <= 128),
+ * read before the call returns; every layer's cache has the same shape and
+ * flags.  Tokens outside the table are skipped in every layer and flagged
+ * once in *err.  Errors: INVALID_ARG (as pkd_append_kv_ex, layers out of
+ * range, a null or misaligned pointer), CUDA. */
+int pkd_append_kv_layers(int32_t layers, const void *const *k_new, const void *const *v_new,
+                         void *const *kv, const int32_t *batch_indices,
+                         const int32_t *positions, int32_t n, const int32_t *indptr,
+                         const int32_t *indices, const int32_t *last_page_len, int32_t batch,
+                         int32_t num_pages, int32_t page_size, int32_t num_kv_heads,
+                         int32_t head_dim, uint32_t flags, int32_t *err, void *stream);
+
 /* Self-test of the device-side bounded waits (failure detection without a
  * GPU fault; FlashInfer, in depth, "Failure modes in production": errors come
  * back as status, never as a hang).  Launches one small kernel on `stream`

@@ -28,7 +28,8 @@ import numpy as np
 
 __all__ = [
     "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states", "append_kv",
-    "plan_host", "plan_host_shared", "schedule_layout", "selftest_bounded_wait", "Graph",
+    "append_kv_layers", "plan_host", "plan_host_shared", "schedule_layout",
+    "selftest_bounded_wait", "Graph",
     "STATUS",
 ]
 
@@ -53,7 +54,7 @@ EXPORTS = (
     "pkd_graph_capture", "pkd_graph_capture_io", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
     "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
-    "pkd_selftest_bounded_wait",
+    "pkd_selftest_bounded_wait", "pkd_append_kv_layers",
 )
 
 
@@ -137,6 +138,8 @@ def load():
         "pkd_plan_host_shared": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp, sz,
                                                 ctypes.POINTER(PlanInfo)]),
         "pkd_selftest_bounded_wait": (ctypes.c_int, [i32, vp, vp, vp]),
+        "pkd_append_kv_layers": (ctypes.c_int, [i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32,
+                                                i32, i32, i32, i32, ctypes.c_uint32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -637,3 +640,60 @@ def append_kv(k_new, v_new, batch_indices, positions, indptr, indices, last_page
         ctypes.c_void_p(err.data_ptr() if err is not None else 0), _stream_ptr(stream))
     _check(st, "pkd_append_kv_ex")
     return kv_cache
+
+
+def append_kv_layers(k_news, v_news, batch_indices, positions, indptr, indices, last_page_len,
+                     kv_caches, err=None, stream=None, kv_layout="NHD"):
+    """append_kv for every layer of a step in one launch: layer l's rows
+    k_news[l] / v_news[l] go into kv_caches[l]; the layers share the tokens
+    and the page table (arguments otherwise as append_kv)."""
+    import torch
+    layers = len(kv_caches)
+    if not 1 <= layers <= 128 or len(k_news) != layers or len(v_news) != layers:
+        raise ValueError("one k_new, v_new and cache per layer, 1 to 128 layers")
+    c0, k0 = kv_caches[0], k_news[0]
+    for l in range(layers):
+        for name, t, ref in (("kv_caches", kv_caches[l], c0), ("k_news", k_news[l], k0),
+                             ("v_news", v_news[l], k0)):
+            if t.dtype != ref.dtype or t.shape != ref.shape or not t.is_cuda or \
+                    not t.is_contiguous():
+                raise ValueError(f"{name}[{l}] must match layer 0's dtype and shape "
+                                 "(contiguous, on the GPU)")
+    fp8 = c0.dtype in (torch.float8_e4m3fn, torch.uint8)
+    kv_dt = c0.dtype if fp8 else torch.bfloat16
+    for name, t, dt in (("k_new", k0, kv_dt), ("kv_cache", c0, kv_dt),
+                        ("batch_indices", batch_indices, torch.int32),
+                        ("positions", positions, torch.int32), ("indptr", indptr, torch.int32),
+                        ("indices", indices, torch.int32),
+                        ("last_page_len", last_page_len, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if kv_layout not in ("NHD", "HND"):
+        raise ValueError("kv_layout must be 'NHD' or 'HND'")
+    n = int(k0.shape[0])
+    if kv_layout == "NHD":
+        pages, two, P, hkv, D = c0.shape
+    else:
+        pages, two, hkv, P, D = c0.shape
+    if two != 2 or tuple(k0.shape) != (n, hkv, D):
+        raise ValueError(f"k_new / v_new must be [n, Hkv, D] matching the {kv_layout} cache")
+    if batch_indices.numel() != n or positions.numel() != n:
+        raise ValueError("batch_indices and positions need one entry per new token")
+    batch = int(last_page_len.numel())
+    if indptr.numel() != batch + 1:
+        raise ValueError("indptr must have batch + 1 entries")
+    if err is not None and (err.dtype != torch.int32 or not err.is_cuda):
+        raise TypeError("err must be an int32 CUDA tensor")
+    flags = (FLAG_HND if kv_layout == "HND" else 0) | (FLAG_KV_FP8 if fp8 else 0)
+
+    def ptrs(ts):
+        return (ctypes.c_void_p * layers)(*[t.data_ptr() for t in ts])
+
+    st = load().pkd_append_kv_layers(
+        layers, ptrs(k_news), ptrs(v_news), ptrs(kv_caches),
+        ctypes.c_void_p(batch_indices.data_ptr()), ctypes.c_void_p(positions.data_ptr()), n,
+        ctypes.c_void_p(indptr.data_ptr()), ctypes.c_void_p(indices.data_ptr()),
+        ctypes.c_void_p(last_page_len.data_ptr()), batch, int(pages), int(P), int(hkv), int(D),
+        flags, ctypes.c_void_p(err.data_ptr() if err is not None else 0), _stream_ptr(stream))
+    _check(st, "pkd_append_kv_layers")
+    return kv_caches

@@ -15,6 +15,7 @@
 #include <new>
 #include <vector>
 
+#include "append_layers.h"
 #include "pkd_internal.h"
 
 using namespace pkd;
@@ -478,6 +479,41 @@ int pkd_append_kv_ex(const void* k_new, const void* v_new, const int32_t* batch_
                     batch, kv, num_pages, page_size, num_kv_heads, (int32_t)head_bytes,
                     (flags & PKD_FLAG_HND) != 0, err,
                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKD_E_CUDA;
+  return PKD_OK;
+}
+
+int pkd_append_kv_layers(int32_t layers, const void* const* k_new, const void* const* v_new,
+                         void* const* kv, const int32_t* batch_indices, const int32_t* positions,
+                         int32_t n, const int32_t* indptr, const int32_t* indices,
+                         const int32_t* last_page_len, int32_t batch, int32_t num_pages,
+                         int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
+                         uint32_t flags, int32_t* err, void* stream) {
+  if ((flags & ~(PKD_FLAG_HND | PKD_FLAG_KV_FP8)) != 0) return PKD_E_INVALID_ARG;
+  if (layers < 1 || layers > kMaxAppendLayers || !k_new || !v_new || !kv)
+    return PKD_E_INVALID_ARG;
+  const int elem = (flags & PKD_FLAG_KV_FP8) ? 1 : 2;
+  if (n < 0 || batch < 0 || num_pages < 1 || page_size < 1 || num_kv_heads < 1 ||
+      head_dim < 1 || ((int64_t)head_dim * elem) % 16 != 0)
+    return PKD_E_INVALID_ARG;
+  if (n == 0) return PKD_OK;
+  if (!batch_indices || !positions || !indptr || !indices || !last_page_len || !aligned(err, 4))
+    return PKD_E_INVALID_ARG;
+  const int64_t head_bytes = (int64_t)head_dim * elem;
+  if (head_bytes * num_kv_heads > (1 << 24)) return PKD_E_INVALID_ARG;
+  AppendLayers L{};
+  for (int32_t l = 0; l < layers; ++l) {
+    if (!k_new[l] || !v_new[l] || !kv[l] || !aligned(k_new[l], 16) || !aligned(v_new[l], 16) ||
+        !aligned(kv[l], 16))
+      return PKD_E_INVALID_ARG;
+    L.k_new[l] = k_new[l];
+    L.v_new[l] = v_new[l];
+    L.kv[l] = kv[l];
+  }
+  if (launch_append_layers(L, layers, batch_indices, positions, n, indptr, indices,
+                           last_page_len, batch, num_pages, page_size, num_kv_heads,
+                           (int32_t)head_bytes, (flags & PKD_FLAG_HND) != 0, err,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKD_E_CUDA;
   return PKD_OK;
 }

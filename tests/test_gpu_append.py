@@ -84,3 +84,57 @@ def test_append_then_decode_reads_new_token():
     for i in range(2):
         for h in range(hq):
             assert torch.equal(out[i, h], v_new[i, h // (hq // hkv)])
+
+
+@pytest.mark.parametrize("layout,fp8", [("NHD", False), ("HND", False), ("NHD", True)])
+def test_append_layers_matches_oracle_per_layer(layout, fp8):
+    """pkd_append_kv_layers: one launch writes every layer's rows; each
+    layer's cache equals the oracle's append of that layer's rows, bit for
+    bit, and tokens outside the table are skipped in every layer."""
+    P, hkv, D, layers = 16, 8, 128, 5
+    rng = np.random.default_rng(91 + 2 * fp8 + (layout == "HND"))
+    lens = rng.integers(1, 200, 12).tolist()
+    pool = sum(-(-l // P) for l in lens) + 5
+    indptr, indices, last = workloads.page_table(lens, P, rng.permutation(pool).astype(np.int32))
+    b = list(range(len(lens))) + [len(lens) + 2]          # the last one is outside the table
+    pos = [l - 1 for l in lens] + [0]
+    n = len(b)
+    g = torch.Generator(device="cuda").manual_seed(13)
+    shape = (pool, 2, P, hkv, D) if layout == "NHD" else (pool, 2, hkv, P, D)
+
+    def rnd(*s):
+        x = torch.randn(*s, generator=g, device="cuda")
+        return x.to(torch.float8_e4m3fn) if fp8 else x.to(torch.bfloat16)
+
+    kvs = [rnd(*shape) for _ in range(layers)]
+    ks = [rnd(n, hkv, D) for _ in range(layers)]
+    vs = [rnd(n, hkv, D) for _ in range(layers)]
+    bits = (lambda t: t.detach().cpu().contiguous().view(torch.uint8).numpy()) if fp8 else _bits
+    refs = []
+    for l in range(layers):
+        ref, skipped = oappend.append_kv(bits(kvs[l]), bits(ks[l]), bits(vs[l]), b, pos,
+                                         indptr, indices, last, P, layout=layout)
+        assert len(skipped) == 1
+        refs.append(ref)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = lambda a: torch.tensor(np.asarray(a, dtype=np.int32), device="cuda")
+    pkd.append_kv_layers(ks, vs, dev(b), dev(pos), dev(indptr), dev(indices), dev(last), kvs,
+                         err=err, kv_layout=layout)
+    torch.cuda.synchronize()
+    for l in range(layers):
+        np.testing.assert_array_equal(bits(kvs[l]), refs[l])
+    assert int(err.item()) == pkd.DEV_ERR_BOUNDS
+
+
+def test_append_layers_rejects_bad_arguments():
+    kv = torch.zeros(4, 2, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    i32 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ip = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):                       # no layers
+        pkd.append_kv_layers([], [], i32, i32, ip, i32, i32, [])
+    with pytest.raises(ValueError):                       # layer shapes differ
+        pkd.append_kv_layers([k, k], [k, k], i32, i32, ip, i32, i32, [kv, kv[:2].clone()])
+    lib = pkd.load()
+    assert lib.pkd_append_kv_layers(0, None, None, None, None, None, 1, None, None, None, 1, 4,
+                                    16, 8, 128, 0, None, None) == -1

@@ -702,7 +702,13 @@ def run_prefix_sweep(args, rank, world):
     reps = max(args.steps, 20)
     rows = []
     launches = 0
-    for prefix, B, pages_comp, pages_single in PREFIX_GRID:
+    grid = PREFIX_GRID
+    if args.sweep_cases:
+        want = {tuple(int(x) for x in c.split("x")) for c in args.sweep_cases.split(",")}
+        grid = [row for row in PREFIX_GRID if (row[0], row[1]) in want]
+        if not grid:
+            raise SystemExit(f"--sweep-cases {args.sweep_cases}: no such (prefix x batch)")
+    for prefix, B, pages_comp, pages_single in grid:
         w = workloads.shared_prefix_case(prefix, B)
         t = workloads.make_tables(w)
         P = w.page_size
@@ -967,6 +973,8 @@ def main():
     ap.add_argument("--chunk-rule", choices=["closed", "search"], default="closed",
                     help="split chunk: closed-form work bound (default) or the largest chunk "
                          "that still gives every CTA an item (binary search)")
+    ap.add_argument("--sweep-cases", default="",
+                    help="prefix_sweep: only these cases, e.g. 32768x64,1024x16 (prefix x batch)")
     ap.add_argument("--alpha", type=int, default=-1,
                     help="planner per-item cost in tokens (cost = alpha + tokens); -1: default")
     ap.add_argument("--prefix-kernel", choices=["dense", "mma"], default="dense",

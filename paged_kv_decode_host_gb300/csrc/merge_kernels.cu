@@ -46,9 +46,9 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // With M known up front no term rescales a running sum, so the loads of a
 // warp can stay in flight together.  kBatch > 1 (plans that split a request
 // into more than kLongUnit chunks) makes that explicit in the block path: a
-// warp issues the loads of kBatch slots before adding their terms, so a
-// 250-chunk request costs a few memory round trips per warp instead of one
-// per slot; it needs more registers (fewer resident blocks), which plans of
+// warp issues the loads of kBatch slots before adding their terms (the first
+// batch's already before the max pass), so a 250-chunk request costs a few
+// memory round trips per warp instead of one per slot; it needs more registers (fewer resident blocks), which plans of
 // short units do not repay, so they get kBatch = 1.  The terms are added in
 // the same order either way.  Fixed assignment and order: bit-reproducible.
 constexpr int kWarpSlots = 32;
@@ -122,6 +122,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
       pdl_wait();
       waited = true;
     }
+    // kBatch > 1: this warp's first batch of slots is loaded before pass 1,
+    // so its round trip overlaps the max pass's
+    float lv[kBatch];
+    float4 ov[kBatch];
+    auto load_batch = [&](int base) {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int s = base + j * kWarps;
+        if (s < s1) {
+          lv[j] = a.l_part[(int64_t)s * a.hq + h];
+          ov[j] = *reinterpret_cast<const float4*>(a.o_part + ((int64_t)s * a.hq + h) * kHeadDim +
+                                                   4 * lane);
+        } else {
+          lv[j] = -CUDART_INF_F;   // weight 0
+          ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    };
+    if constexpr (kBatch > 1) load_batch(s0 + warp);
     // ---- pass 1: M = max over the unit's chunk LSEs (log2 units)
     float mx = -CUDART_INF_F;
     for (int s = s0 + threadIdx.x; s < s1; s += kMergeThreads)
@@ -152,20 +171,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
       }
     }
     for (int base = s0 + warp; kBatch > 1 && base < s1; base += kBatch * kWarps) {
-      float lv[kBatch];
-      float4 ov[kBatch];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int s = base + j * kWarps;
-        if (s < s1) {
-          lv[j] = a.l_part[(int64_t)s * a.hq + h];
-          ov[j] = *reinterpret_cast<const float4*>(a.o_part + ((int64_t)s * a.hq + h) * kHeadDim +
-                                                   4 * lane);
-        } else {
-          lv[j] = -CUDART_INF_F;   // weight 0
-          ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
+      if (base != s0 + warp) load_batch(base);
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const float w = exp2f(lv[j] * kLog2e - m);

@@ -213,8 +213,15 @@ class _ComposedGraph:
     def launch(self):
         self.g.replay()
 
+    def close(self):
+        self.g = None
 
-def _composed_step_graph(ds, q, kv, po, pl, so, sl, out, lse, side, dev):
+
+def _composed_step_graph(ds, q, kv, po, pl, so, sl, out, lse, side, dev, io=None):
+    """io = (copy streams (in, out), [(device dst, host src)], [(host dst,
+    device src)]): copies captured on two branches of the graph that run
+    beside the step's kernels (the next step's q in, the previous step's
+    results out)."""
     import torch
 
     import paged_kv_decode_host_gb300 as pkd
@@ -230,11 +237,21 @@ def _composed_step_graph(ds, q, kv, po, pl, so, sl, out, lse, side, dev):
         fork = torch.cuda.Event()
         fork.record(main)
         side.wait_event(fork)
+        if io is not None:
+            (s_in, s_out), copies_in, copies_out = io
+            for st, pairs in ((s_in, copies_in), (s_out, copies_out)):
+                st.wait_event(fork)
+                with torch.cuda.stream(st):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
         ds[0].run(q, kv, out=po, lse=pl)
         with torch.cuda.stream(side):
             ds[1].run(q, kv, out=so, lse=sl)
         main.wait_stream(side)
         pkd.merge_states(po, pl, so, sl, out, lse)
+        if io is not None:
+            main.wait_stream(s_in)
+            main.wait_stream(s_out)
     return _ComposedGraph(g)
 
 
@@ -331,7 +348,6 @@ def run_ours(args, rank, world):
     done = [torch.cuda.Event() for _ in range(n_sets)]
     for e in done:
         e.record(stream)
-    host = {}
 
     use = {"graphs": graphs}
 
@@ -339,27 +355,18 @@ def run_ours(args, rank, world):
         return use["graphs"][k % n_sets][(k // n_sets) % copies]
 
     def step(k):
-        """One decode step.  With host buffers (e2e): q comes from pinned host
-        memory and out / lse go back to it, inside the step."""
+        """One decode step on device-resident q / out / lse."""
         si = k % n_sets
         copy_stream.wait_event(done[si])
         for (name, gi, table), d in zip(views, sets[si]):
             _plan(d, gi, table, stream=copy_stream)
         copied[si].record(copy_stream)
-        if host:
-            for x, h in zip(qs, host["q"]):
-                x.copy_(h, non_blocking=True)
         stream.wait_event(copied[si])
         gp, gs, c = graph_of(k)
         gp.launch()
         if gs is not None:   # timing graphs of the shared-prefix step
             gs.launch()
             pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
-        if host:
-            for x, h in zip(outs, host["out"]):
-                h.copy_(x, non_blocking=True)
-            for x, h in zip(lses, host["lse"]):
-                h.copy_(x, non_blocking=True)
         done[si].record(stream)
 
     for k in range(args.warmup):
@@ -419,10 +426,26 @@ def run_ours(args, rank, world):
 
     # end to end: host q in, host out back, plan from host tables, per step
     if w.prefix_tokens:
-        e2e = run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, dev)
+        side_e2e = [torch.cuda.Stream(device=dev) for _ in range(3)]
+
+        def capture_io(si, dq, do, dl, hq, ho, hl, c):
+            # step of set si: computes on set si's q / out / lse while the
+            # next step's q goes into the other set's buffer and the previous
+            # step's results come back from it
+            nx = 1 - si
+            return _composed_step_graph(
+                sets[si], dq[si][0], kvs[c], po[c], pl[c], so[c], sl[c], do[si][0], dl[si][0],
+                side_e2e[0], dev,
+                io=((side_e2e[1], side_e2e[2]), [(dq[nx][0], hq[0])],
+                    [(ho[0], do[nx][0]), (hl[0], dl[nx][0])]))
+        e2e = run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stream,
+                               step_bytes, world, dev)
     else:
-        e2e = run_e2e_pipelined(args, sets, views, kvs, kv_scales, layers, copies, qs, outs,
-                                lses, stream, step_bytes, world, dev)
+        def capture(si, dq, do, dl, c):
+            return sets[si][0].capture(dq, kvs[c * layers:(c + 1) * layers], do, dl,
+                                       kv_scales=kv_scales)
+        e2e = run_e2e_pipelined(args, sets, views, capture, copies, qs, outs, lses, stream,
+                                step_bytes, world, dev)
 
     clocks = sampler.summary()
     gp0, _, _ = graphs[0][0]
@@ -483,8 +506,8 @@ def run_ours(args, rank, world):
     return line
 
 
-def run_e2e_pipelined(args, sets, views, kvs, kv_scales, layers, copies, qs, outs, lses,
-                      stream, step_bytes, world, dev):
+def run_e2e_pipelined(args, sets, views, capture, copies, qs, outs, lses, stream, step_bytes,
+                      world, dev):
     """The step through the public API with host buffers, the way a serving
     loop pipelines it: step k's queries go host -> device on a copy stream
     (DMA engines) while step k-1's graph runs, and step k's out + lse go back
@@ -492,7 +515,8 @@ def run_e2e_pipelined(args, sets, views, kvs, kv_scales, layers, copies, qs, out
     each own a set of device q / out / lse buffers, so no copy touches a
     buffer a running graph uses.  Every step still moves its own inputs in
     and its own results out inside the timed region (the last step's results
-    are on the host when it ends)."""
+    are on the host when it ends).  capture(set, q, out, lse, cache copy)
+    returns the step graph of a planning context over those buffers."""
     import torch
     n_sets = len(sets)
     hq = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in qs]
@@ -503,8 +527,7 @@ def run_e2e_pipelined(args, sets, views, kvs, kv_scales, layers, copies, qs, out
     dq = [[torch.empty_like(x) for x in qs] for _ in range(n_sets)]
     do = [[torch.empty_like(x) for x in outs] for _ in range(n_sets)]
     dl = [[torch.empty_like(x) for x in lses] for _ in range(n_sets)]
-    graphs = [[sets[si][0].capture(dq[si], kvs[c * layers:(c + 1) * layers], do[si], dl[si],
-                                   kv_scales=kv_scales) for c in range(copies)]
+    graphs = [[capture(si, dq[si], do[si], dl[si], c) for c in range(copies)]
               for si in range(n_sets)]
     h2d_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
@@ -555,56 +578,113 @@ def run_e2e_pipelined(args, sets, views, kvs, kv_scales, layers, copies, qs, out
     e1.record(stream)
     torch.cuda.synchronize()
     wall = (time.perf_counter() - t0) * 1e3 / steps
-    ms = max(e0.elapsed_time(e1) / steps, wall)
+    gpu_ms = e0.elapsed_time(e1) / steps
+    ms = max(gpu_ms, wall)
     for row in graphs:
         for g in row:
             g.close()
     ms = max_over_ranks(ms, world, dev)
     return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d + sched),
+            "ms_per_step": round(ms, 5), "ms_gpu_events": round(gpu_ms, 5),
+            "ms_host_wall": round(wall, 5), "h2d_bytes_per_step": int(h2d + sched),
             "d2h_bytes_per_step": int(d2h),
             "what": "pinned host q -> device (copy stream), plan from host tables (schedule "
                     "H2D), graph replay, out + lse -> pinned host (copy stream); steps "
                     "pipelined over two buffer sets; KV cache resident"}
 
 
-def run_e2e(args, step, host, decs, qs, outs, lses, stream, step_bytes, world, dev):
-    """Same step through the public API with host buffers: pinned host q in,
-    out + lse back to pinned host, around the step graph, inside the timed
-    region."""
+def run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stream, step_bytes,
+                     world, dev):
+    """The step through the public API with host buffers, for steps short
+    enough that per-call host work would bound a loop that issues every copy
+    itself: one graph per step runs the step's kernels on one set of device
+    q / out / lse buffers and, on two branches beside them, copies the next
+    step's q from pinned host memory into the other set and the previous
+    step's out + lse from the other set back to pinned host memory.  The
+    first step's q goes in before the loop's first graph and the last step's
+    results come back after its last one, both inside the timed region, so
+    every timed step moves its own inputs in and its own results out.  A step
+    costs the host its plan calls (into alternating planning contexts: a
+    context's schedule is rewritten only after the step that read it is
+    done) and one graph launch.  capture_io(set, device q / out / lse sets,
+    host q / out / lse, cache copy) returns such a graph."""
     import torch
+    n_sets = len(sets)
+    assert n_sets == 2
     hq = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in qs]
     for h, x in zip(hq, qs):
         h.copy_(x)
     ho = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
     hl = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in lses]
-    host["q"], host["out"], host["lse"] = hq, ho, hl
+    dq = [[torch.empty_like(x) for x in qs] for _ in range(n_sets)]
+    do = [[torch.empty_like(x) for x in outs] for _ in range(n_sets)]
+    dl = [[torch.empty_like(x) for x in lses] for _ in range(n_sets)]
+    graphs = [[capture_io(si, dq, do, dl, hq, ho, hl, c) for c in range(copies)]
+              for si in range(n_sets)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(n_sets)]
+    done = [torch.cuda.Event() for _ in range(n_sets)]
+    for e in done:
+        e.record(stream)
+
+    def step(k):
+        si = k % n_sets
+        copy_stream.wait_event(done[si])
+        for (name, gi, table), d in zip(views, sets[si]):
+            _plan(d, gi, table, stream=copy_stream)
+        copied[si].record(copy_stream)
+        stream.wait_event(copied[si])
+        graphs[si][(k // n_sets) % copies].launch()
+        done[si].record(stream)
+
+    def prologue():
+        with torch.cuda.stream(stream):
+            for x, h in zip(dq[0], hq):
+                x.copy_(h, non_blocking=True)
+
+    def epilogue(last):
+        with torch.cuda.stream(stream):
+            for x, h in zip(do[last % n_sets], ho):
+                h.copy_(x, non_blocking=True)
+            for x, h in zip(dl[last % n_sets], hl):
+                h.copy_(x, non_blocking=True)
+
     h2d = sum(x.numel() * x.element_size() for x in qs)
     d2h = sum(x.numel() * x.element_size() for x in outs) + sum(x.numel() * 4 for x in lses)
-    sched = sum(4 * d.plan_info()["schedule_words"] for d in decs)
-    steps = max(3, args.steps // 2)
-    try:
-        for k in range(3):
-            step(k)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        t0 = time.perf_counter()
-        e0.record(stream)
-        for k in range(steps):
-            step(k)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        wall = (time.perf_counter() - t0) * 1e3 / steps
-        ms = max(e0.elapsed_time(e1) / steps, wall)
-    finally:
-        host.clear()
+    sched = sum(4 * d.plan_info()["schedule_words"] for d in sets[0])
+    steps = max(4, args.steps // 2) // 2 * 2
+    prologue()
+    for k in range(4):
+        step(k)
+    epilogue(3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    prologue()
+    for k in range(steps):
+        step(k)
+    epilogue(steps - 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) * 1e3 / steps
+    gpu_ms = e0.elapsed_time(e1) / steps
+    ms = max(gpu_ms, wall)
+    for row in graphs:
+        for g in row:
+            g.close()
     ms = max_over_ranks(ms, world, dev)
     return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d + sched),
+            "ms_per_step": round(ms, 5), "ms_gpu_events": round(gpu_ms, 5),
+            "ms_host_wall": round(wall, 5), "h2d_bytes_per_step": int(h2d + sched),
             "d2h_bytes_per_step": int(d2h),
-            "what": "pinned host q -> device, plan from host tables (schedule H2D), graph "
-                    "replay, out + lse -> pinned host; KV cache resident"}
+            "what": "plan from host tables (schedule H2D on a copy stream), then one graph "
+                    "per step: both levels + merge_states on one buffer set while the next "
+                    "step's q (pinned host -> device) and the previous step's out + lse "
+                    "(device -> pinned host) move on two branches beside them; the first q "
+                    "and the last results are copied inside the timed region too; KV cache "
+                    "resident"}
 
 
 # ------------------------------------------------------------ cpu baseline

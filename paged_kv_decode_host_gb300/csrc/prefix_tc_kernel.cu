@@ -11,13 +11,15 @@
 // GB300 design (one CTA per SM, 6 warps):
 //  * warp 4 (producer) loads the item's Q tile once (two TMA tensor copies,
 //    128 rows x 128 dims, 128-byte swizzle) and streams the KV head's page
-//    tiles into a 4-deep ring of 64-token stages: one TMA tensor copy per 16
+//    tiles into a 3-deep ring of 128-token stages: one TMA tensor copy per 16
 //    tokens, 128-byte half of the head, and K or V (2 KB), placed so that each
-//    half of a stage's K (and V) is one [64 tokens][128 B] swizzled matrix --
+//    half of a stage's K (and V) is one [128 tokens][128 B] swizzled matrix --
 //    a whole round is one MMA operand however the pages are scattered;
-//  * warp 5 (one lane) issues tcgen05.mma: per round of 64 tokens, S into a
-//    double-buffered tensor-memory tile (M 128, N 64, K 128 in 8 steps, both
-//    operands K-major from shared memory), then, once the softmax warps have
+//  * warp 5 (one lane) issues tcgen05.mma: per round of 128 tokens, S into a
+//    double-buffered tensor-memory tile (M 128, N 128, K 128 in 8 steps, both
+//    operands K-major from shared memory; 128-token rounds because these
+//    single-CTA MMAs run at about 2.8 k flop per cycle per SM with N 64 but
+//    5.1 k with N 128), then, once the softmax warps have
 //    written P, O += P V (M 128, N 128, K 16 per page tile, A = P from tensor
 //    memory, B = V N-major from shared memory); completion goes to mbarriers
 //    through tcgen05.commit;
@@ -28,8 +30,8 @@
 //    the exponentials is only raised when a round's max exceeds it by more
 //    than 2^8 (then O is rescaled in tensor memory), so most rounds touch O
 //    not at all; the result is the same softmax, P stays <= 256.
-// Tensor memory (512 columns): O [0, 128), S [128, 256) as two 64-column
-// buffers, P [256, 320) as two 32-column buffers (16-bit pairs).
+// Tensor memory (512 columns): O [0, 128), S [128, 384) as two 128-column
+// buffers, P [384, 512) as two 64-column buffers (16-bit pairs).
 // Every wait is bounded; on timeout the kernel sets the device error word,
 // stops, waits (bounded) for its copies and MMAs, frees tensor memory and
 // returns.
@@ -46,15 +48,20 @@ namespace {
 using namespace dev;
 
 constexpr int kTcThreads = 192;       // 4 softmax warps, producer, MMA warp
-constexpr int kTcStages = 4;
-constexpr int kRoundTok = 64;         // tokens per round = 4 page tiles of 16
+constexpr int kTcStages = 3;
+constexpr int kRoundTok = 128;        // tokens per round = 8 page tiles of 16
+constexpr int kRoundTiles = kRoundTok / 16;
 constexpr int kBoxBytes = 2048;       // 16 tokens x one 128-byte half of a KV head
-constexpr int kHalfBytes = 4 * kBoxBytes;         // one half of a round: [64 tokens][128 B]
+constexpr int kHalfBytes = kRoundTiles * kBoxBytes;   // one half of a round: [128 tokens][128 B]
 constexpr int kKvBytes = 2 * kHalfBytes;          // K (or V) of a round: two halves
 constexpr int kStageBytes = 2 * kKvBytes;         // K, then V
 constexpr int kQBytes = kDenseRows * kHeadDim * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 128, kColP = 256;
+// O [0, 128); S: two 128-column fp32 buffers [128, 384); P: two 64-column
+// buffers of bf16 pairs [384, 512)
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 384;
+constexpr uint32_t kSCols = kRoundTok, kPCols = kRoundTok / 2;
+static_assert(kColP + 2 * kPCols <= kTmemCols, "tensor-memory columns");
 constexpr float kRescaleLog2 = 8.f;   // raise the exponent base past 2^8 growth only
 
 struct TcSmem {
@@ -66,6 +73,8 @@ struct TcSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(1024 + kQBytes + kTcStages * kStageBytes + sizeof(TcSmem) <= 227 * 1024,
+              "dynamic shared memory of one CTA");
 
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                         int32_t* err, int lane) {
@@ -260,8 +269,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
       for (int t = tb, k = 0; t < te; t += kRoundTok, ++st, ++k) {
         const int n = min(kRoundTok, te - t);
         const int nbox = (n + 15) >> 4;
-        const int tile0 = 4 * k;
-        if (tile0 + 4 > base + 32) {
+        const int tile0 = kRoundTiles * k;
+        if (tile0 + kRoundTiles > base + 32) {
           base = tile0;
           my_page = 0;
           if (base + lane < ntiles) {
@@ -278,9 +287,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           ok = false;
           break;
         }
-        // lane 4 j + 2 c + h copies half h of tile j of K (c = 0) or V (c = 1)
+        // lane 4 j + 2 c + h copies half h of tile j of K (c = 0) or V (c = 1):
+        // the 8 tiles of a round take all 32 lanes
         const int j = lane >> 2, c = (lane >> 1) & 1, h = lane & 1;
-        const int page = __shfl_sync(kFull, my_page, (tile0 + (j & 3) - base) & 31);
+        const int page = __shfl_sync(kFull, my_page, (tile0 + j - base) & 31);
         if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], (uint32_t)(4 * nbox * kBoxBytes));
         __syncwarp();
         if (j < nbox)
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
             const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
             const uint32_t kbase = st0 + (uint32_t)(slot * kStageBytes);
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + kColS + 64 * b,
+              mma_ss(tmem + kColS + kSCols * b,
                      smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
                      smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
                      idesc_s, kk > 0);
@@ -380,7 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
             tc_fence_after();
             const uint32_t vb = smem_u32(vbase);
             for (int j = 0; j < nbox; ++j)
-              mma_ts(tmem + kColO, tmem + kColP + 32 * b + 8 * j,
+              mma_ts(tmem + kColO, tmem + kColP + kPCols * b + 8 * j,
                      smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, p_k > 0 || j > 0);
             mma_commit(&sh->pfree[b]);
             mma_commit(&sh->empty[slot]);
@@ -444,9 +454,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           break;
         }
         tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tmem + lane_off + kColS + 64 * b, s0);
-        tmem_ld32(tmem + lane_off + kColS + 64 * b + 32, s1);
+        uint32_t sv[kRoundTok / 32][32];
+#pragma unroll
+        for (int q = 0; q < kRoundTok / 32; ++q)
+          tmem_ld32(tmem + lane_off + kColS + kSCols * b + 32 * q, sv[q]);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -456,15 +467,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         // -inf so that their weights come out 0
         if (n < kRoundTok) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j >= n) (j < 32 ? s0[j] : s1[j - 32]) = __float_as_uint(-CUDART_INF_F);
+          for (int q = 0; q < kRoundTok / 32; ++q)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (32 * q + j >= n) sv[q][j] = __float_as_uint(-CUDART_INF_F);
         }
         float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(s0[j]));
-          mq[(j + 2) & 3] = fmaxf(mq[(j + 2) & 3], __uint_as_float(s1[j]));
-        }
+        for (int q = 0; q < kRoundTok / 32; ++q)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(sv[q][j]));
         const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
         // P buffer b was read by the P.V MMAs of round r - 2
         if (r >= 2 && !pv_wait(r - 2)) {
@@ -497,22 +509,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
           l *= alpha;
           if (need) m_used = mx;
         }
-        // weights 2^(s scale_log2 - m_used), one FMA and one exp2 each
-        uint32_t pw[32];
+        // weights 2^(s scale_log2 - m_used), one FMA and one exp2 each; P
+        // column c of the buffer holds tokens 2c and 2c + 1, written 64
+        // tokens (32 columns) at a time
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         const float neg_m = -m_used;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t* src = j < 16 ? s0 : s1;
-          const int c = 2 * (j & 15);
-          const float p0 = fast_exp2(fmaf(__uint_as_float(src[c]), a.scale_log2, neg_m));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(src[c + 1]), a.scale_log2, neg_m));
-          ps[j & 3] += p0;
-          ps[(j + 2) & 3] += p1;
-          pw[j] = pack_bf16(p0, p1);
+        for (int hh = 0; hh < kRoundTok / 64; ++hh) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t* src = sv[2 * hh + (j >> 4)];
+            const int c = 2 * (j & 15);
+            const float p0 = fast_exp2(fmaf(__uint_as_float(src[c]), a.scale_log2, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(src[c + 1]), a.scale_log2, neg_m));
+            ps[j & 3] += p0;
+            ps[(j + 2) & 3] += p1;
+            pw[j] = pack_bf16(p0, p1);
+          }
+          tmem_st32(tmem + lane_off + kColP + kPCols * b + 32 * hh, pw);
         }
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        tmem_st32(tmem + lane_off + kColP + 32 * b, pw);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

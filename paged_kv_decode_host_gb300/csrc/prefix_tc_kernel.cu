@@ -8,13 +8,15 @@
 // the KV head are 128 rows of one dense tile, so the item is a real
 // contraction: S = Q K^T (128 x 16 per page tile) and O += P V (128 x 128).
 //
-// GB300 design (one CTA per SM, 6 warps):
+// GB300 design (one CTA per SM, 7 warps):
 //  * warp 4 (producer) loads the item's Q tile once (two TMA tensor copies,
-//    128 rows x 128 dims, 128-byte swizzle) and streams the KV head's page
-//    tiles into a 3-deep ring of 128-token stages: one TMA tensor copy per 16
-//    tokens, 128-byte half of the head, and K or V (2 KB), placed so that each
-//    half of a stage's K (and V) is one [128 tokens][128 B] swizzled matrix --
-//    a whole round is one MMA operand however the pages are scattered;
+//    128 rows x 128 dims, 128-byte swizzle) and streams the KV head's K page
+//    tiles into a 3-deep ring of 128-token slots; warp 6 streams V into a
+//    ring of its own, so a K slot is refilled as soon as its score MMAs are
+//    done instead of waiting for the round's P.V.  One TMA tensor copy moves
+//    16 tokens of one 128-byte half of the head (2 KB), placed so that each
+//    half of a slot is one [128 tokens][128 B] swizzled matrix -- a whole
+//    round is one MMA operand however the pages are scattered;
 //  * warp 5 (one lane) issues tcgen05.mma: per round of 128 tokens, S into a
 //    double-buffered tensor-memory tile (M 128, N 128, K 128 in 8 steps, both
 //    operands K-major from shared memory; 128-token rounds because these
@@ -47,7 +49,7 @@ namespace {
 
 using namespace dev;
 
-constexpr int kTcThreads = 192;       // 4 softmax warps, producer, MMA warp
+constexpr int kTcThreads = 224;       // 4 softmax warps, K producer, MMA warp, V producer
 constexpr int kTcStages = 3;
 constexpr int kRoundTok = 128;        // tokens per round = 8 page tiles of 16
 constexpr int kRoundTiles = kRoundTok / 16;
@@ -65,7 +67,8 @@ static_assert(kColP + 2 * kPCols <= kTmemCols, "tensor-memory columns");
 constexpr float kRescaleLog2 = 8.f;   // raise the exponent base past 2^8 growth only
 
 struct TcSmem {
-  uint64_t full[kTcStages], empty[kTcStages];
+  uint64_t fullk[kTcStages], emptyk[kTcStages];   // K ring: landed / read by the score MMAs
+  uint64_t fullv[kTcStages], emptyv[kTcStages];   // V ring: landed / read by the P.V MMAs
   uint64_t qfull, qfree;
   uint64_t sfull[2], sfree[2];
   uint64_t pfull[2], pfree[2];
@@ -211,8 +214,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], 1);
+      mbar_init(&sh->fullk[s], 1);
+      mbar_init(&sh->emptyk[s], 1);
+      mbar_init(&sh->fullv[s], 1);
+      mbar_init(&sh->emptyv[s], 1);
     }
     mbar_init(&sh->qfull, 1);
     mbar_init(&sh->qfree, 1);
@@ -241,21 +246,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
   const int P = a.page_size;
   const int g = a.hq / a.hkv;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == 4 || warp == 6) {
+    // ----------------------------------------------------------- producers
+    // warp 4: the Q tiles and the K ring; warp 6: the V ring.  The rings are
+    // apart so that a K slot is refilled as soon as its score MMAs are done,
+    // not only once the round's P.V MMAs have read its V.
+    const int c = warp == 4 ? 0 : 1;
+    uint64_t* full = c ? sh->fullv : sh->fullk;
+    uint64_t* empty = c ? sh->emptyv : sh->emptyk;
+    uint8_t* ring = stages + (size_t)c * kTcStages * kKvBytes;
     const uint64_t policy = l2_evict_first_policy();
     pdl_wait();   // q and the cache may come from the previous kernel
-    int st = 0;
+    int st = 0, nq = 0;
     bool ok = true;
     for (int it = it0; it < it1 && ok; ++it) {
       const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
       const int req = item[0], tb = item[1], te = item[2], poff = item[4], head = item[7];
       // Q tile of the item (the previous item's score MMAs must be done)
-      if (it > it0 && !tc_wait(&sh->qfree, (uint32_t)((it - it0 - 1) & 1), abort_flag, a.err, lane)) {
+      if (c == 0 && it > it0 &&
+          !tc_wait(&sh->qfree, (uint32_t)((it - it0 - 1) & 1), abort_flag, a.err, lane)) {
         ok = false;
         break;
       }
-      if (lane == 0) {
+      if (c == 0 && lane == 0) {
+        ++nq;
         mbar_arrive_expect_tx(&sh->qfull, (uint32_t)kQBytes);
         for (int h = 0; h < 2; ++h)
           tensor_copy_g2s(sQ + h * (kQBytes / 2), &a.q_map, 0, h, 0, head, req, &sh->qfull, policy);
@@ -283,28 +297,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         }
         const int slot = st % kTcStages;
         const uint32_t round = (uint32_t)(st / kTcStages);
-        if (round > 0 && !tc_wait(&sh->empty[slot], (round - 1) & 1u, abort_flag, a.err, lane)) {
+        if (round > 0 && !tc_wait(&empty[slot], (round - 1) & 1u, abort_flag, a.err, lane)) {
           ok = false;
           break;
         }
-        // lane 4 j + 2 c + h copies half h of tile j of K (c = 0) or V (c = 1):
-        // the 8 tiles of a round take all 32 lanes
-        const int j = lane >> 2, c = (lane >> 1) & 1, h = lane & 1;
-        const int page = __shfl_sync(kFull, my_page, (tile0 + j - base) & 31);
-        if (lane == 0) mbar_arrive_expect_tx(&sh->full[slot], (uint32_t)(4 * nbox * kBoxBytes));
+        // lane 2 j + h (lanes 0-15) copies half h of tile j of K (c = 0) or
+        // V (c = 1)
+        const int j = lane >> 1, h = lane & 1;
+        const int page = __shfl_sync(kFull, my_page, (tile0 + (j & 7) - base) & 31);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * nbox * kBoxBytes));
         __syncwarp();
         if (j < nbox)
-          tensor_copy_g2s(stages + (size_t)slot * kStageBytes + c * kKvBytes + h * kHalfBytes +
-                              j * kBoxBytes,
-                          &a.kv_map, 0, (t + 16 * j) % P, h, head, 2 * page + c, &sh->full[slot],
+          tensor_copy_g2s(ring + (size_t)slot * kKvBytes + h * kHalfBytes + j * kBoxBytes,
+                          &a.kv_map, 0, (t + 16 * j) % P, h, head, 2 * page + c, &full[slot],
                           policy);
       }
     }
     // drain: the last phase of every slot, and the last Q tile
     if (lane == 0) {
       for (int s = 0; s < kTcStages; ++s)
-        if (st > s && !mbar_wait(&sh->full[s], (uint32_t)(((st - 1 - s) / kTcStages) & 1), nullptr))
+        if (st > s && !mbar_wait(&full[s], (uint32_t)(((st - 1 - s) / kTcStages) & 1), nullptr))
           atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
+      if (nq > 0 && !mbar_wait(&sh->qfull, (uint32_t)((nq - 1) & 1), nullptr))
+        atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
     }
   } else if (warp == 5) {
     // ----------------------------------------------------- MMA issue (lane 0)
@@ -331,7 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         const int tb = item[1], te = item[2];
         const int slot = rs % kTcStages, b = rs & 1;
         if ((s_k > 0 || ready(&sh->qfull, (uint32_t)((s_it - it0) & 1))) &&
-            ready(&sh->full[slot], (uint32_t)((rs / kTcStages) & 1)) &&
+            ready(&sh->fullk[slot], (uint32_t)((rs / kTcStages) & 1)) &&
             (rs < 2 || ready(&sh->sfree[b], (uint32_t)(((rs >> 1) - 1) & 1)))) {
           const int n = min(kRoundTok, te - (tb + s_k * kRoundTok));
           const bool last = (s_k + 1) * kRoundTok >= te - tb;
@@ -340,13 +355,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
             // N = the round's tokens rounded up to whole tiles (tiles past
             // them were not copied)
             const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
-            const uint32_t kbase = st0 + (uint32_t)(slot * kStageBytes);
+            const uint32_t kbase = st0 + (uint32_t)(slot * kKvBytes);
             for (int kk = 0; kk < 8; ++kk)
               mma_ss(tmem + kColS + kSCols * b,
                      smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
                      smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
                      idesc_s, kk > 0);
             mma_commit(&sh->sfull[b]);
+            mma_commit(&sh->emptyk[slot]);
             if (last) mma_commit(&sh->qfree);   // the item's last score MMA
           }
           __syncwarp();
@@ -367,11 +383,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         const int tb = item[1], te = item[2];
         const int slot = rp % kTcStages, b = rp & 1;
         if (ready(&sh->pfull[b], (uint32_t)((rp >> 1) & 1)) &&
+            ready(&sh->fullv[slot], (uint32_t)((rp / kTcStages) & 1)) &&
             (p_k > 0 || p_it == it0 || ready(&sh->ofree, (uint32_t)((p_it - it0 - 1) & 1)))) {
           const int n = min(kRoundTok, te - (tb + p_k * kRoundTok));
           const bool last = (p_k + 1) * kRoundTok >= te - tb;
           const int nbox = (n + 15) >> 4;
-          uint8_t* vbase = stages + (size_t)slot * kStageBytes + kKvBytes;
+          uint8_t* vbase = stages + (size_t)(kTcStages + slot) * kKvBytes;
           if (n & 15) {
             // slots past the item's end in the last tile: P is 0 there, but
             // 0 x NaN would poison O, so zero those V rows (both halves)
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
               mma_ts(tmem + kColO, tmem + kColP + kPCols * b + 8 * j,
                      smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, p_k > 0 || j > 0);
             mma_commit(&sh->pfree[b]);
-            mma_commit(&sh->empty[slot]);
+            mma_commit(&sh->emptyv[slot]);
           }
           __syncwarp();
           ++rp;

@@ -910,12 +910,7 @@ def run_append(args, rank, world):
         return gr
 
     def time_graph(gr):
-        # a step is a few microseconds of GPU work, less than one graph
-        # launch costs the host: the stream first spins (bounded, ~20 us per
-        # step) while the replays are queued behind it, so the events time
-        # the replays back to back, not the host's launch rate
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(int(40_000 * (args.steps + 2)))
         e0.record()
         for _ in range(args.steps):
             gr.replay()

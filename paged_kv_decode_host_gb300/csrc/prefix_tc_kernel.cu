@@ -8,7 +8,7 @@
 // the KV head are 128 rows of one dense tile, so the item is a real
 // contraction: S = Q K^T (128 x 16 per page tile) and O += P V (128 x 128).
 //
-// GB300 design (one CTA per SM, 7 warps):
+// GB300 design (one CTA per SM, 8 warps):
 //  * warp 4 (producer) loads the item's Q tile once (two TMA tensor copies,
 //    128 rows x 128 dims, 128-byte swizzle) and streams the KV head's K page
 //    tiles into a 3-deep ring of 128-token slots; warp 6 streams V into a
@@ -17,14 +17,18 @@
 //    16 tokens of one 128-byte half of the head (2 KB), placed so that each
 //    half of a slot is one [128 tokens][128 B] swizzled matrix -- a whole
 //    round is one MMA operand however the pages are scattered;
-//  * warp 5 (one lane) issues tcgen05.mma: per round of 128 tokens, S into a
-//    double-buffered tensor-memory tile (M 128, N 128, K 128 in 8 steps, both
-//    operands K-major from shared memory; 128-token rounds because these
-//    single-CTA MMAs run at about 2.8 k flop per cycle per SM with N 64 but
-//    5.1 k with N 128), then, once the softmax warps have
-//    written P, O += P V (M 128, N 128, K 16 per page tile, A = P from tensor
-//    memory, B = V N-major from shared memory); completion goes to mbarriers
-//    through tcgen05.commit;
+//  * warp 5 (one lane) issues the score MMAs: per round of 128 tokens, S
+//    into a double-buffered tensor-memory tile (M 128, N 128, K 128 in 8
+//    steps, both operands K-major from shared memory; 128-token rounds
+//    because these single-CTA MMAs run at about 2.8 k flop per cycle per SM
+//    with N 64 but 5.1 k with N 128);
+//  * warp 7 (one lane) issues the P.V MMAs once the softmax warps have
+//    written P: O += P V (M 128, N 128, K 16 per page tile, A = P from
+//    tensor memory, B = V N-major from shared memory).  Two issuing warps
+//    because an issuing thread stalls while the tensor core works through
+//    what it was given before: with one thread for both streams, each held
+//    the other up.  Completion goes to mbarriers through tcgen05.commit,
+//    which tracks the issuing thread's own MMAs;
 //  * warps 0-3 (softmax, one query row per thread = one tensor-memory lane)
 //    read S with tcgen05.ld, keep the row's running max and sum in registers,
 //    write P (bf16) to tensor memory with tcgen05.st, and in the epilogue read
@@ -49,7 +53,8 @@ namespace {
 
 using namespace dev;
 
-constexpr int kTcThreads = 224;       // 4 softmax warps, K producer, MMA warp, V producer
+// 4 softmax warps, K producer, score-MMA warp, V producer, P.V-MMA warp
+constexpr int kTcThreads = 256;
 constexpr int kTcStages = 3;
 constexpr int kRoundTok = 128;        // tokens per round = 8 page tiles of 16
 constexpr int kRoundTiles = kRoundTok / 16;
@@ -87,19 +92,6 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
     return false;
   }
   return true;
-}
-
-// non-blocking: has the phase with this parity completed?
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -228,7 +220,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
       mbar_init(&sh->pfree[b], 1);
     }
     mbar_init(&sh->ofree, 4);
-    mbar_init(&sh->fin, 1);
+    mbar_init(&sh->fin, 2);
     sh->abort_flag = 0;
     fence_mbar_init();
   }
@@ -322,119 +314,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const __grid_c
         atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
     }
   } else if (warp == 5) {
-    // ----------------------------------------------------- MMA issue (lane 0)
-    // An event loop over two cursors: the next score MMA (round rs) and the
-    // next P.V MMA (round rp), each issued as soon as its inputs are ready,
-    // so S for a later round never queues behind the P.V of an earlier one
-    // (S(r + 1) can go out while the softmax warps still work on round r).
-    const uint32_t idesc_o = mma_idesc(kDenseRows, kHeadDim, 1);
+    // ----------------------------------------- score MMAs (lane 0 issues)
+    // S of round r: its K tiles landed, Q loaded (first round of an item)
+    // and its S buffer read by the softmax warps (round r - 2).  The P.V
+    // MMAs come from warp 7, so neither stream waits behind the other's
+    // issue (an issuing thread stalls while the tensor core works through
+    // what it was given before).
     const uint32_t q0 = smem_u32(sQ), st0 = smem_u32(stages);
-    int s_it = it0, s_k = 0, rs = 0;    // next S: item, round within it, global round
-    int p_it = it0, p_k = 0, rp = 0;    // next P.V
-    bool ok = true, idle = false;
-    unsigned long long idle_t0 = 0;
-    uint32_t spins = 0;
-    auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(kFull, mbar_test_wait(bar, parity));
-    };
-    while (ok && p_it < it1) {
-      bool progress = false;
-      // ---- S of round rs: K tiles landed, Q tile loaded (first round of
-      // an item), S buffer read by the softmax warps (round rs - 2)
-      if (s_it < it1) {
-        const int32_t* item = a.sched + a.off_items + (int64_t)s_it * kItemWords;
-        const int tb = item[1], te = item[2];
-        const int slot = rs % kTcStages, b = rs & 1;
-        if ((s_k > 0 || ready(&sh->qfull, (uint32_t)((s_it - it0) & 1))) &&
-            ready(&sh->fullk[slot], (uint32_t)((rs / kTcStages) & 1)) &&
-            (rs < 2 || ready(&sh->sfree[b], (uint32_t)(((rs >> 1) - 1) & 1)))) {
-          const int n = min(kRoundTok, te - (tb + s_k * kRoundTok));
-          const bool last = (s_k + 1) * kRoundTok >= te - tb;
-          if (lane == 0) {
-            tc_fence_after();
-            // N = the round's tokens rounded up to whole tiles (tiles past
-            // them were not copied)
-            const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
-            const uint32_t kbase = st0 + (uint32_t)(slot * kKvBytes);
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + kColS + kSCols * b,
-                     smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
-                     smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                     idesc_s, kk > 0);
-            mma_commit(&sh->sfull[b]);
-            mma_commit(&sh->emptyk[slot]);
-            if (last) mma_commit(&sh->qfree);   // the item's last score MMA
-          }
-          __syncwarp();
-          ++rs;
-          if (last) {
-            ++s_it;
-            s_k = 0;
-          } else {
-            ++s_k;
-          }
-          progress = true;
-        }
+    int r = 0;
+    bool ok = true;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
+      const int tb = item[1], te = item[2];
+      const int nr = rounds_of(tb, te);
+      if (!tc_wait(&sh->qfull, (uint32_t)((it - it0) & 1), abort_flag, a.err, lane)) {
+        ok = false;
+        break;
       }
-      // ---- P.V of round rp: P written (and, first round of an item, the
-      // previous item's O read by the epilogue)
-      if (rp < rs) {
-        const int32_t* item = a.sched + a.off_items + (int64_t)p_it * kItemWords;
-        const int tb = item[1], te = item[2];
-        const int slot = rp % kTcStages, b = rp & 1;
-        if (ready(&sh->pfull[b], (uint32_t)((rp >> 1) & 1)) &&
-            ready(&sh->fullv[slot], (uint32_t)((rp / kTcStages) & 1)) &&
-            (p_k > 0 || p_it == it0 || ready(&sh->ofree, (uint32_t)((p_it - it0 - 1) & 1)))) {
-          const int n = min(kRoundTok, te - (tb + p_k * kRoundTok));
-          const bool last = (p_k + 1) * kRoundTok >= te - tb;
-          const int nbox = (n + 15) >> 4;
-          uint8_t* vbase = stages + (size_t)(kTcStages + slot) * kKvBytes;
-          if (n & 15) {
-            // slots past the item's end in the last tile: P is 0 there, but
-            // 0 x NaN would poison O, so zero those V rows (both halves)
-            const int v0 = n & 15;
-            uint8_t* tile = vbase + (nbox - 1) * kBoxBytes;
-            for (int i = lane; i < 2 * (16 - v0) * 8; i += 32) {
-              const int h = i / ((16 - v0) * 8), rem = i % ((16 - v0) * 8);
-              const int row = v0 + rem / 8, chunk = rem % 8;
-              *reinterpret_cast<uint4*>(tile + h * kHalfBytes + row * 128 + chunk * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t vb = smem_u32(vbase);
-            for (int j = 0; j < nbox; ++j)
-              mma_ts(tmem + kColO, tmem + kColP + kPCols * b + 8 * j,
-                     smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, p_k > 0 || j > 0);
-            mma_commit(&sh->pfree[b]);
-            mma_commit(&sh->emptyv[slot]);
-          }
-          __syncwarp();
-          ++rp;
-          if (last) {
-            ++p_it;
-            p_k = 0;
-          } else {
-            ++p_k;
-          }
-          progress = true;
-        }
-      }
-      if (progress) {
-        idle = false;
-      } else if (!idle) {
-        idle = true;
-        idle_t0 = global_ns();
-        spins = 0;
-      } else if ((++spins & 31u) == 0) {
-        const bool give_up = *abort_flag != 0 || global_ns() - idle_t0 > kTimeoutNs;
-        if (__any_sync(kFull, give_up)) {
-          if (lane == 0) raise_error(a.err, abort_flag, PKD_DEV_ERR_TIMEOUT);
+      for (int k = 0; k < nr; ++k, ++r) {
+        const int slot = r % kTcStages, b = r & 1;
+        if (!tc_wait(&sh->fullk[slot], (uint32_t)((r / kTcStages) & 1), abort_flag, a.err, lane) ||
+            (r >= 2 &&
+             !tc_wait(&sh->sfree[b], (uint32_t)(((r >> 1) - 1) & 1), abort_flag, a.err, lane))) {
           ok = false;
+          break;
         }
+        const int n = min(kRoundTok, te - (tb + k * kRoundTok));
+        if (lane == 0) {
+          tc_fence_after();
+          // N = the round's tokens rounded up to whole tiles (tiles past
+          // them were not copied)
+          const uint32_t idesc_s = mma_idesc(kDenseRows, 16 * ((n + 15) >> 4), 0);
+          const uint32_t kbase = st0 + (uint32_t)(slot * kKvBytes);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + kColS + kSCols * b,
+                   smem_desc(q0 + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                   smem_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                   idesc_s, kk > 0);
+          mma_commit(&sh->sfull[b]);
+          mma_commit(&sh->emptyk[slot]);
+          if (k == nr - 1) mma_commit(&sh->qfree);   // the item's last score MMA
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      mma_commit(&sh->fin);
+      if (!mbar_wait(&sh->fin, 0, nullptr)) atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 7) {
+    // ------------------------------------------ P.V MMAs (lane 0 issues)
+    // P.V of round r: P written, its V tiles landed and, first round of an
+    // item, the previous item's O read by the epilogue
+    const uint32_t idesc_o = mma_idesc(kDenseRows, kHeadDim, 1);
+    int r = 0;
+    bool ok = true;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
+      const int tb = item[1], te = item[2];
+      const int nr = rounds_of(tb, te);
+      for (int k = 0; k < nr; ++k, ++r) {
+        const int slot = r % kTcStages, b = r & 1;
+        if (!tc_wait(&sh->pfull[b], (uint32_t)((r >> 1) & 1), abort_flag, a.err, lane) ||
+            !tc_wait(&sh->fullv[slot], (uint32_t)((r / kTcStages) & 1), abort_flag, a.err, lane) ||
+            (k == 0 && it > it0 &&
+             !tc_wait(&sh->ofree, (uint32_t)((it - it0 - 1) & 1), abort_flag, a.err, lane))) {
+          ok = false;
+          break;
+        }
+        const int n = min(kRoundTok, te - (tb + k * kRoundTok));
+        const int nbox = (n + 15) >> 4;
+        uint8_t* vbase = stages + (size_t)(kTcStages + slot) * kKvBytes;
+        if (n & 15) {
+          // slots past the item's end in the last tile: P is 0 there, but
+          // 0 x NaN would poison O, so zero those V rows (both halves)
+          const int v0 = n & 15;
+          uint8_t* tile = vbase + (nbox - 1) * kBoxBytes;
+          for (int i = lane; i < 2 * (16 - v0) * 8; i += 32) {
+            const int h = i / ((16 - v0) * 8), rem = i % ((16 - v0) * 8);
+            const int row = v0 + rem / 8, chunk = rem % 8;
+            *reinterpret_cast<uint4*>(tile + h * kHalfBytes + row * 128 + chunk * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t vb = smem_u32(vbase);
+          for (int j = 0; j < nbox; ++j)
+            mma_ts(tmem + kColO, tmem + kColP + kPCols * b + 8 * j,
+                   smem_desc(vb + j * kBoxBytes, kHalfBytes, 1024), idesc_o, k > 0 || j > 0);
+          mma_commit(&sh->pfree[b]);
+          mma_commit(&sh->emptyv[slot]);
+        }
+        __syncwarp();
       }
     }
     if (lane == 0) {

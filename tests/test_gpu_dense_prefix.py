@@ -155,6 +155,44 @@ def test_dense_prefix_workload_composed_and_graph():
     assert pre.device_error() == 0
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_dense_prefix_longest_sweep_case(layout):
+    """The largest case of the composable-format sweep: 64 requests over a
+    32,768-token prefix (two 128-row tiles per KV head, items of ~20
+    128-token rounds, every ring slot reused many times), each with its own
+    128-token suffix; prefix level on the dense kernel, suffixes on the
+    decode kernel, merge_states; every output against the oracle."""
+    w = workloads.shared_prefix_case(32768, 64)
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    P = w.page_size
+    n_pre = w.prefix_tokens // P
+    hnd = layout == "HND"
+    if hnd:   # the same values in the HND layout: [pages, 2, Hkv, P, D]
+        kv = kv.permute(0, 1, 3, 2, 4).contiguous()
+    pre = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, P, max_batch=w.batch,
+                                          max_num_pages=n_pre, num_pages=w.pool_pages,
+                                          shared_prefix=True, dense_prefix=True,
+                                          kv_layout=layout)
+    suf = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, 128, P, max_batch=w.batch,
+                                          max_num_pages=int(t["suffix"][0][-1]),
+                                          num_pages=w.pool_pages, kv_layout=layout)
+    pre.plan_shared(np.array([0, w.batch], np.int32), np.array([0, n_pre], np.int32),
+                    t["prefix"][1][:n_pre], np.array([P], np.int32))
+    info = pre.plan_info()
+    assert info["num_units"] == w.batch            # every request's prefix is split
+    suf.plan(*t["suffix"])
+    op, lp = pre.run(q, kv)
+    os_, ls = suf.run(q, kv)
+    out, lse = pkd.merge_states(op, lp, os_, ls)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=w.hq, hkv=w.hkv,
+                                 layout=layout)
+    _check(out, lse, ref_o, ref_l)
+    assert pre.device_error() == 0 and suf.device_error() == 0
+
+
 def test_dense_prefix_rejects_unsupported():
     with pytest.raises(ValueError):
         pkd.BatchDecodeWithPagedKVCache(32, 8, 128, 16, max_batch=4, max_num_pages=8,

@@ -111,15 +111,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id):
+    def __init__(self, gpu_id, period_ms=20):
         self.gpu_id = gpu_id
+        self.period_ms = period_ms   # query-only sampling; short timed regions need a fast rate
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -704,6 +705,27 @@ def _oracle_sample(w, t, q_bits, kv_bits, rows_req, nthreads=None):
     return time.perf_counter() - t0
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
     """The fp64 oracle on the host cores, on a bounded sample of the same
     workload (requests of layer 0, all query heads), in the metric's unit."""
@@ -735,14 +757,18 @@ def cpu_baseline(w, t, qs, kvs, budget_s=12.0, q_bits=None, kv_bits=None):
             s_lens, sum(-(-l // w.page_size) for l in s_lens))
         return bytes_ / secs / 1e9
 
-    sample = sample_for(budget_s, None)
-    secs = _oracle_sample(w, t, q_bits, kv_bits, sample)
+    # the same sample timed three times (a third of the budget each): median
+    sample = sample_for(budget_s / 3.0, None)
+    runs = sorted(_oracle_sample(w, t, q_bits, kv_bits, sample) for _ in range(3))
+    secs = runs[1]
     passes = len(sample) / w.batch
     # one host core, on a sample a sixth of the budget long
     sample1 = sample_for(budget_s / 6.0, 1)
     secs1 = _oracle_sample(w, t, q_bits, kv_bits, sample1, 1)
     return {"value": round(gbs(sample, secs), 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "cpu_model": cpu_model(),
             "kind": "oracle", "seconds": round(secs, 3),
+            "runs_s": [round(x, 3) for x in runs], "statistic": "median of 3",
             "sample": f"layer 0: {len(sample)} request rows ({passes:.2f} passes over the "
                       f"{w.batch} requests, {sum(lens[i] for i in sample)} tokens) x {w.hq} "
                       f"query heads, fp64, all host cores",
@@ -1026,11 +1052,55 @@ def run_reference(args, rank, world):
                    "hkv": w.hkv, "head_dim": w.head_dim, "page_size": w.page_size,
                    "sample_per_step": last["sample"] if last else None},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": last["sample"] if last else None},
+                         "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": last["sample"] if last else None},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
+
+
+# ------------------------------------------------------- other workloads
+
+# The other synthetic configurations a decode step is quoted on, timed in the
+# same process after the headline: the 63 + 100,000-token skewed batch, the
+# page-size-1 token-sparse batch and the shared-prefix step.
+OTHER_WORKLOADS = ("skewed", "token_sparse", "shared_prefix")
+
+
+def run_other_workloads(args, rank, world, names=OTHER_WORKLOADS):
+    """Each workload as its own bench run (same timing, roofline and e2e
+    legs, no CPU baseline), summarised under one key of the headline line."""
+    import gc
+
+    import torch
+    res = {}
+    for name in names:
+        gc.collect()
+        torch.cuda.empty_cache()
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.layers = name, args.other_steps, 0
+        sub.warmup = max(args.warmup, 10)
+        sub.no_cpu_baseline = True
+        ln = run_ours(sub, rank, world)
+        rf = ln["roofline"]
+        res[name] = {
+            "value": ln["value"], "unit": ln["unit"], "pct_of_peak": ln["pct_of_peak"],
+            "ms_per_step": ln["ms_per_step"], "steps_per_s": ln["steps_per_s"],
+            "steps": ln["steps"], "warmup": ln["warmup"],
+            "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "frac", "traffic",
+                                            "launch_ms_mean")},
+            "e2e": {k: ln["e2e"][k] for k in ("value", "unit", "ms_per_step",
+                                               "h2d_bytes_per_step", "d2h_bytes_per_step")},
+            "clocks": ln["clocks"], "gpu_launches": ln["gpu_launches"],
+            "config": {k: ln["config"][k] for k in ("batch", "hq", "hkv", "page_size",
+                                                    "total_tokens_per_layer",
+                                                    "alg_bytes_per_step", "l2", "plan",
+                                                    "prefix_kernel")},
+        }
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
 
 
 # --------------------------------------------------------------------- main
@@ -1062,6 +1132,10 @@ def main():
                          "head) or the mma.sync row-block consumer (16-row tiles)")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per step (0: the workload's own); smaller for profiling captures")
+    ap.add_argument("--other-steps", type=int, default=300,
+                    help="timed steps of each other workload reported with the default one")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="report the selected workload alone")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1083,6 +1157,9 @@ def main():
         line = run_prefix_sweep(args, rank, world)
     else:
         line = run_ours(args, rank, world)
+        if (args.workload == "llama8b_step" and args.layers == 0 and
+                not args.no_other_workloads):
+            line["other_workloads"] = run_other_workloads(args, rank, world)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()

@@ -130,6 +130,21 @@ typedef struct pkd_config {
  * combinable with PKD_FLAG_FMA_CONSUMER, PKD_FLAG_KV_FP8 or
  * PKD_FLAG_ROW_COPIES. */
 #define PKD_FLAG_DENSE_PREFIX 128u
+/* Cascade context ("FlashInfer, in depth", "Prefill, masks and shared
+ * prefixes" and "Cascades, Merges, and the Autotuner": attention once per
+ * prefix level, then one merge; "FlashInfer 完全拆解", Composable Format).
+ * Plans made with pkd_plan_cascade hold both levels of a decode step: the
+ * shared-prefix level (work items over one KV head of a block of up to
+ * 128 / g requests, as PKD_FLAG_DENSE_PREFIX) and every request's own suffix
+ * (work items over a request's token range, all KV heads, as pkd_plan).
+ * pkd_run then launches one kernel whose first CTAs run the prefix items on
+ * the 5th-generation tensor cores and whose other CTAs run the suffix items
+ * on the decode path, side by side, every item writing a partial state; one
+ * merge folds each request's prefix and suffix states into out / lse.  The
+ * planner splits the grid between the levels by a cost model.  bf16 cache,
+ * page size a multiple of 16; combinable with PKD_FLAG_HND and
+ * PKD_FLAG_MMA_CONSUMER only. */
+#define PKD_FLAG_CASCADE 256u
 
 typedef struct pkd_ctx pkd_ctx;
 typedef struct pkd_graph pkd_graph;
@@ -304,8 +319,10 @@ int pkd_append_kv_layers(int32_t layers, const void *const *k_new, const void *c
 int pkd_selftest_bounded_wait(int32_t mode, int32_t *d_err, unsigned long long *d_wait_ns,
                               void *stream);
 
-/* Read and clear the device error word (synchronizes `stream`).
- * *dev_err receives PKD_DEV_ERR_* bits (0 = none). */
+/* Read and clear the context's device error word: the read and the reset
+ * are ordered on `stream` after the work already in it, and the call waits
+ * for `stream` only (work on other streams keeps running).  *dev_err
+ * receives PKD_DEV_ERR_* bits (0 = none).  Errors: INVALID_ARG, CUDA. */
 int pkd_last_device_error(pkd_ctx *ctx, void *stream, int32_t *dev_err);
 
 /* Copy the schedule in the device workspace back to the host (test aid;
@@ -346,7 +363,8 @@ int pkd_plan_host_shared(const pkd_config *cfg, const int32_t *group_indptr,
  * Header words 0..31 hold: magic, batch, Hq, Hkv, D, P, num_ctas,
  * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (clamped to
  * int32), split floor, requests per block, the most chunks of any split
- * request, then zeros.  Errors: INVALID_ARG. */
+ * request, the max_batch and max_num_pages the offsets were laid out for,
+ * then zeros.  Errors: INVALID_ARG. */
 int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 
 /* ---- CUDA-graph capture of a whole decode step ------------------------- */
@@ -394,12 +412,22 @@ void pkd_graph_destroy(pkd_graph *graph);
  * chunks, the same kernels as pkd_run) with the schedule and the partial
  * states in a static 32 MiB device array inside this library (held by every
  * GPU that loads the library until the process exits).  It calls no
- * allocator: no cudaMalloc / cudaFree / cudaMallocHost, no pkd_create.
- *   cfg            : the configuration; cfg->num_ctas must be > 0 and equal
- *                    the value the schedule was planned for
+ * allocator: no cudaMalloc / cudaFree / cudaMallocHost, no pkd_create.  Its
+ * decode kernel copies KV one token row per bulk copy (the producer pkd_run
+ * uses when page tiles are off), since it keeps no tensor maps.
+ *   cfg            : the configuration (no flags but the consumer ones);
+ *                    cfg->num_ctas must be > 0 and equal the value the
+ *                    schedule was planned for
  *   schedule_words : host buffer written by pkd_plan_host(cfg, ...) for this
- *                    step (num_words = its length, >= page_list offset + nnz);
- *                    copied with cudaMemcpyAsync on `stream`
+ *                    step (num_words = its length, >= page_list offset + nnz).
+ *                    It is checked before use: planned for this cfg (shape,
+ *                    CTA count, max_batch and max_num_pages, which fix the
+ *                    word offsets), queues, requests, pages and partial-state
+ *                    slots all in range.  It is copied with cudaMemcpyAsync
+ *                    on `stream`; from pageable memory that copy is staged
+ *                    before the call returns, from page-locked memory it is
+ *                    asynchronous and the buffer must stay unchanged until
+ *                    the stream has passed it.
  *   q, kv, out, lse: as for pkd_run
  * The whole layout for cfg (make sure max_batch / max_num_pages are not
  * larger than needed) must fit the 32 MiB array, else PKD_E_SCRATCH_LIMIT.
@@ -408,11 +436,22 @@ void pkd_graph_destroy(pkd_graph *graph);
  * work overlaps race, so serialise them on one stream.  The first call on a
  * device sets the device up (looks up the array's address and the kernel
  * attribute) with that device current; make it before any stream capture.
+ * Device-side errors (a page id outside the pool, a bounded wait that gave
+ * up) land in the array's error word: read them with
+ * pkd_static_scratch_last_error.
  * Errors: INVALID_ARG (null / misaligned pointer, schedule not matching cfg),
  * UNSUPPORTED_SHAPE, SCRATCH_LIMIT, CUDA. */
 int pkd_run_static_scratch(const pkd_config *cfg, const int32_t *schedule_words,
                            size_t num_words, const void *q, const void *kv,
                            void *out, float *lse, void *stream);
+
+/* Read and clear the device error word of the static array for the layout
+ * of cfg (the word the last pkd_run_static_scratch call with this cfg
+ * cleared and its kernels set): a stream-ordered read, then the reset, then
+ * a wait for `stream` only.  Allocates nothing.  *dev_err receives
+ * PKD_DEV_ERR_* bits (0 = none).  Errors: INVALID_ARG, UNSUPPORTED_SHAPE,
+ * SCRATCH_LIMIT (cfg as for pkd_run_static_scratch), CUDA. */
+int pkd_static_scratch_last_error(const pkd_config *cfg, void *stream, int32_t *dev_err);
 
 /* Human-readable name of a status code. */
 const char *pkd_status_str(int status);

@@ -54,7 +54,7 @@ EXPORTS = (
     "pkd_graph_capture", "pkd_graph_capture_io", "pkd_graph_launch", "pkd_graph_layer_times",
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
     "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
-    "pkd_selftest_bounded_wait", "pkd_append_kv_layers",
+    "pkd_selftest_bounded_wait", "pkd_append_kv_layers", "pkd_static_scratch_last_error",
 )
 
 
@@ -130,6 +130,7 @@ def load():
         "pkd_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pkd_version": (ctypes.c_int, []),
         "pkd_run_static_scratch": (ctypes.c_int, [cfgp, vp, sz, vp, vp, vp, vp, vp]),
+        "pkd_static_scratch_last_error": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(i32)]),
         "pkd_append_kv": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
                                          i32, i32, vp, vp]),
         "pkd_append_kv_ex": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,

@@ -40,6 +40,7 @@ struct pkd_ctx {
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
   int32_t* staging[2] = {nullptr, nullptr};
+  int32_t* err_host = nullptr;   // page-locked landing word of the device error word
   cudaEvent_t staged[2] = {nullptr, nullptr};
   bool staged_pending[2] = {false, false};
   int next_staging = 0;
@@ -335,6 +336,11 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
     }
     std::memset(ctx->staging[k], 0, (size_t)ctx->layout.words * 4);
   }
+  if (cudaMallocHost(&ctx->err_host, sizeof(int32_t)) != cudaSuccess) {
+    pkd_destroy(ctx);
+    return PKD_E_CUDA;
+  }
+  *ctx->err_host = 0;
   if (cudaMemset(ctx->ws + ctx->layout.err_byte, 0, 4) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     pkd_destroy(ctx);
@@ -353,6 +359,7 @@ void pkd_destroy(pkd_ctx* ctx) {
     }
     if (ctx->staging[k]) cudaFreeHost(ctx->staging[k]);
   }
+  if (ctx->err_host) cudaFreeHost(ctx->err_host);
   delete ctx;
 }
 
@@ -521,13 +528,13 @@ int pkd_append_kv_layers(int32_t layers, const void* const* k_new, const void* c
 int pkd_last_device_error(pkd_ctx* ctx, void* stream, int32_t* dev_err) {
   if (ctx == nullptr || dev_err == nullptr) return PKD_E_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t v = 0;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return PKD_E_CUDA;
-  if (cudaMemcpy(&v, ctx->ws + ctx->layout.err_byte, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+  // read, then reset, both behind the stream's work; wait for this stream only
+  uint8_t* word = ctx->ws + ctx->layout.err_byte;
+  if (cudaMemcpyAsync(ctx->err_host, word, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return PKD_E_CUDA;
-  if (cudaMemset(ctx->ws + ctx->layout.err_byte, 0, 4) != cudaSuccess) return PKD_E_CUDA;
-  if (cudaDeviceSynchronize() != cudaSuccess) return PKD_E_CUDA;
-  *dev_err = v;
+  if (cudaMemsetAsync(word, 0, 4, s) != cudaSuccess) return PKD_E_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKD_E_CUDA;
+  *dev_err = *ctx->err_host;
   return PKD_OK;
 }
 

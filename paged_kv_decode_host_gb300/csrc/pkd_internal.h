@@ -29,11 +29,15 @@ constexpr int kDefaultAlpha = 32;
 constexpr int kDefaultMinChunk = 256;
 constexpr int kMergeThreads = 256;
 
-// Schedule header words (first 32 int32 of the workspace; 17..31 are 0).
+// Schedule header words (first 32 int32 of the workspace; 19..31 are 0).
 enum HeaderWord {
   H_MAGIC = 0, H_BATCH, H_HQ, H_HKV, H_D, H_P, H_NCTA, H_NITEMS, H_NUNITS,
   H_NSLOTS, H_CHUNK, H_ALPHA, H_NNZ, H_MAKESPAN, H_MINCHUNK, H_BLOCK,
   H_MAXCHUNKS,   // most chunks of any split request (0: nothing split)
+  H_MAXBATCH,    // the capacities the word offsets were laid out for
+  H_MAXPAGES,    //   (config max_batch and max_num_pages)
+  H_NPRE,        // cascade plans: CTAs [0, H_NPRE) run the shared-prefix items
+  H_PCHUNK,      // cascade plans: the shared-prefix level's chunk (tokens)
   H_WORDS = 32
 };
 
@@ -42,6 +46,32 @@ enum HeaderWord {
 // plans: one KV head per item; otherwise 0 and the item covers all heads)
 constexpr int kItemWords = 8;
 constexpr int kDenseRows = 128;   // query rows of one dense-prefix tile
+
+// Cascade plans (PKD_FLAG_CASCADE): a shared-prefix level, whose items the
+// dense tensor-core role runs, and the requests' own suffix level, whose
+// items the decode role runs, share one launch over disjoint CTA ranges and
+// one reduction map.  The planner balances the two ranges with a cost model
+// in suffix-token units: a suffix item costs alpha + tokens (every KV head of
+// a token: 4 KB of K and V at Hkv 8), a prefix item (one KV head of a block
+// of up to 128 query rows) costs (kCascadePrefixAlpha + tokens) *
+// kCascadePrefixCost16 / 16.  Measured: a 128-token round of the dense role
+// takes about 1 us, a decode CTA streams a token of all 8 heads in about
+// 70-90 ns, so a prefix token of one head costs about an eighth of a suffix
+// token.  The suffix chunk floor is lower than a plain plan's, since the
+// suffix level gets only part of the grid.
+#ifndef PKD_CASCADE_PREFIX_COST16
+#define PKD_CASCADE_PREFIX_COST16 2
+#endif
+#ifndef PKD_CASCADE_PREFIX_ALPHA
+#define PKD_CASCADE_PREFIX_ALPHA 128
+#endif
+#ifndef PKD_CASCADE_SUFFIX_FLOOR
+#define PKD_CASCADE_SUFFIX_FLOOR 128
+#endif
+constexpr int64_t kCascadePrefixCost16 = PKD_CASCADE_PREFIX_COST16;
+constexpr int64_t kCascadePrefixAlpha = PKD_CASCADE_PREFIX_ALPHA;
+constexpr int64_t kCascadeSuffixFloor = PKD_CASCADE_SUFFIX_FLOOR;
+constexpr int64_t kCascadePrefixFloor = 128;   // one round of the dense role
 
 // Fixed word offsets of the schedule arrays, all derived from capacities.
 struct Layout {
@@ -74,8 +104,9 @@ inline int64_t max_items_for(int64_t max_batch, int64_t n_cta) {
 // tensor-core tile per KV head over g query heads (16 for the mma.sync
 // consumer, 128 for the dense-prefix kernel); 1 without grouping.
 inline int32_t block_rows(const pkd_config& c) {
-  if (!(c.flags & PKD_FLAG_SHARED_PREFIX)) return 1;
   const int32_t g = c.num_qo_heads / c.num_kv_heads;
+  if (c.flags & PKD_FLAG_CASCADE) return kDenseRows / g;
+  if (!(c.flags & PKD_FLAG_SHARED_PREFIX)) return 1;
   return ((c.flags & PKD_FLAG_DENSE_PREFIX) ? kDenseRows : 16) / g;
 }
 
@@ -88,6 +119,15 @@ inline Layout make_layout(const pkd_config& c, int64_t n_cta) {
   // items <= Hkv * blocks + 4 n_cta
   if (c.flags & PKD_FLAG_DENSE_PREFIX)
     L.max_items = (int64_t)c.num_kv_heads * c.max_batch + 4 * n_cta + 8;
+  if (c.flags & PKD_FLAG_CASCADE) {
+    // prefix items <= Hkv * blocks + 2 n_pre, suffix items <= batch + 2 n_suf
+    // (chunks at least half the level's work bound); every request is a
+    // unit whose slots are its prefix chunks then its suffix chunks:
+    // prefix slots <= batch + 2 R n_pre / Hkv, suffix slots <= batch + 2 n_suf
+    const int64_t R = block_rows(c);
+    L.max_items = (int64_t)(c.num_kv_heads + 1) * c.max_batch + 2 * n_cta + 16;
+    L.max_slots = 2 * (int64_t)c.max_batch + (2 * R / c.num_kv_heads + 2) * n_cta + 16;
+  }
   L.cta_indptr = H_WORDS;
   L.items = align_up(L.cta_indptr + n_cta + 1, 8);
   L.units = L.items + L.max_items * kItemWords;
@@ -205,6 +245,15 @@ int plan_schedule(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
                           const int32_t* group_indptr, int32_t n_rows, const int32_t* indptr,
                           const int32_t* indices, const int32_t* last, int32_t* words,
+                          pkd_plan_info* info);
+// A cascade plan: groups of requests (group_indptr) sharing prefix table rows
+// (p_*, one row per group) and every request's own suffix table row (s_*,
+// one row per request).
+int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                          const int32_t* group_indptr, int32_t n_groups,
+                          const int32_t* p_indptr, const int32_t* p_indices,
+                          const int32_t* p_last, const int32_t* s_indptr,
+                          const int32_t* s_indices, const int32_t* s_last, int32_t* words,
                           pkd_plan_info* info);
 
 }  // namespace pkd

@@ -400,6 +400,8 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   int32_t max_chunks = 0;
   for (const auto& un : units) max_chunks = std::max(max_chunks, un.second);
   h[H_MAXCHUNKS] = max_chunks;
+  h[H_MAXBATCH] = cfg.max_batch;
+  h[H_MAXPAGES] = cfg.max_num_pages;
 
   if (info) {
     info->batch = batch;

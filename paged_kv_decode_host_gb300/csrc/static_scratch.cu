@@ -73,6 +73,55 @@ int scratch_address(int group, bool mma, uint8_t** out) {
   return PKD_OK;
 }
 
+// A schedule handed in from the host is checked before it reaches the GPU:
+// it must have been planned for this very layout (same capacities, hence the
+// same word offsets), and every index the kernels follow from it must stay
+// inside the arrays and the scratch: CTA queues monotone within the item
+// list, each item's requests inside the batch, its pages inside the page
+// list and its partial-state slots below the layout's slot count; each split
+// request's slots likewise.  O(items + units) on the host.
+bool schedule_fits(const int32_t* w, const Layout& L) {
+  const int32_t batch = w[H_BATCH], n_cta = w[H_NCTA], n_items = w[H_NITEMS];
+  const int32_t n_units = w[H_NUNITS], nnz = w[H_NNZ], P = w[H_P];
+  if (batch < 0 || n_units < 0 || n_units > L.max_items || P < 1) return false;
+  const int32_t* cta = w + L.cta_indptr;
+  if (cta[0] != 0 || cta[n_cta] != n_items) return false;
+  for (int32_t c = 0; c < n_cta; ++c)
+    if (cta[c + 1] < cta[c]) return false;
+  for (int32_t j = 0; j < n_items; ++j) {
+    const int32_t* it = w + L.items + (int64_t)j * kItemWords;
+    const int32_t req = it[0], t0 = it[1], t1 = it[2], slot = it[3], page0 = it[4];
+    const int32_t n_req = it[5], stride = it[6];
+    if (n_req != 1 || req < 0 || req >= batch || t0 < 0 || t1 <= t0) return false;
+    if (page0 < 0 || (int64_t)page0 + (t1 - 1 - t0 + (t0 % P)) / P >= nnz) return false;
+    if (slot < -1 || slot >= L.max_slots || stride < 0) return false;
+  }
+  const int32_t* units = w + L.units;
+  const int32_t* merge = w + L.merge_indptr;
+  if (merge[0] != 0) return false;
+  for (int32_t u = 0; u < n_units; ++u)
+    if (units[2 * u] < 0 || units[2 * u] >= batch || merge[u + 1] < merge[u] ||
+        merge[u + 1] > L.max_slots)
+      return false;
+  return true;
+}
+
+// The configuration checks shared by both entry points of this file.
+int check_static_config(const pkd_config* cfg, int* group) {
+  if (cfg == nullptr) return PKD_E_INVALID_ARG;
+  if ((cfg->flags & ~(PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER)) != 0 ||
+      cfg->flags == (PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER) || cfg->num_ctas < 1 ||
+      cfg->head_dim != kHeadDim || cfg->num_kv_heads < 1 || cfg->num_kv_heads > kMaxKvHeads ||
+      cfg->num_qo_heads < 1 || cfg->num_qo_heads % cfg->num_kv_heads != 0 ||
+      cfg->page_size < 1 || cfg->num_pages < 1 || cfg->max_batch < 0 || cfg->max_num_pages < 0)
+    return PKD_E_INVALID_ARG;
+  *group = cfg->num_qo_heads / cfg->num_kv_heads;
+  if (*group != 1 && *group != 2 && *group != 4 && *group != 8) return PKD_E_UNSUPPORTED_SHAPE;
+  if (make_layout(*cfg, cfg->num_ctas).total_bytes > kStaticScratchBytes)
+    return PKD_E_SCRATCH_LIMIT;
+  return PKD_OK;
+}
+
 }  // namespace
 }  // namespace pkd
 
@@ -81,24 +130,21 @@ using namespace pkd;
 extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* schedule_words,
                                       size_t num_words, const void* q, const void* kv, void* out,
                                       float* lse, void* stream) {
-  if (cfg == nullptr || schedule_words == nullptr) return PKD_E_INVALID_ARG;
-  if ((cfg->flags & ~(PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER)) != 0 ||
-      cfg->flags == (PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER) || cfg->num_ctas < 1 || cfg->head_dim != kHeadDim ||
-      cfg->num_kv_heads < 1 || cfg->num_kv_heads > kMaxKvHeads || cfg->num_qo_heads < 1 ||
-      cfg->num_qo_heads % cfg->num_kv_heads != 0 || cfg->page_size < 1 || cfg->num_pages < 1 ||
-      cfg->max_batch < 0 || cfg->max_num_pages < 0)
-    return PKD_E_INVALID_ARG;
-  const int group = cfg->num_qo_heads / cfg->num_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8) return PKD_E_UNSUPPORTED_SHAPE;
+  int group = 0;
+  int st = check_static_config(cfg, &group);
+  if (st != PKD_OK) return st;
+  if (schedule_words == nullptr) return PKD_E_INVALID_ARG;
   const Layout L = make_layout(*cfg, cfg->num_ctas);
-  if (L.total_bytes > kStaticScratchBytes) return PKD_E_SCRATCH_LIMIT;
   // the schedule must be pkd_plan_host's output for this very configuration
   if ((int64_t)num_words < L.page_list) return PKD_E_INVALID_ARG;
   const int32_t* h = schedule_words;
   if (h[H_MAGIC] != kMagic || h[H_HQ] != cfg->num_qo_heads || h[H_HKV] != cfg->num_kv_heads ||
       h[H_D] != cfg->head_dim || h[H_P] != cfg->page_size || h[H_NCTA] != cfg->num_ctas ||
+      h[H_MAXBATCH] != cfg->max_batch || h[H_MAXPAGES] != cfg->max_num_pages ||
+      h[H_BATCH] < 0 || h[H_BATCH] > cfg->max_batch || h[H_BLOCK] != 1 ||
       h[H_NITEMS] < 0 || h[H_NITEMS] > L.max_items || h[H_NNZ] < 0 ||
-      h[H_NNZ] > cfg->max_num_pages || (int64_t)num_words < L.page_list + h[H_NNZ])
+      h[H_NNZ] > cfg->max_num_pages || (int64_t)num_words < L.page_list + h[H_NNZ] ||
+      !schedule_fits(h, L))
     return PKD_E_INVALID_ARG;
   if (h[H_BATCH] > 0) {
     if (q == nullptr || kv == nullptr || out == nullptr) return PKD_E_INVALID_ARG;
@@ -107,7 +153,7 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
   }
   const bool mma = use_mma_consumer(group, cfg->flags);
   uint8_t* ws = nullptr;
-  int st = scratch_address(group, mma, &ws);
+  st = scratch_address(group, mma, &ws);
   if (st != PKD_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t sched_bytes = ((size_t)L.page_list + (size_t)h[H_NNZ]) * 4;
@@ -152,5 +198,28 @@ extern "C" int pkd_run_static_scratch(const pkd_config* cfg, const int32_t* sche
   m.hq = cfg->num_qo_heads;
   if (launch_merge_partials(m, merge_grid_for(cfg->num_ctas), h[H_MAXCHUNKS], s) != cudaSuccess)
     return PKD_E_CUDA;
+  return PKD_OK;
+}
+
+extern "C" int pkd_static_scratch_last_error(const pkd_config* cfg, void* stream,
+                                             int32_t* dev_err) {
+  int group = 0;
+  int st = check_static_config(cfg, &group);
+  if (st != PKD_OK) return st;
+  if (dev_err == nullptr) return PKD_E_INVALID_ARG;
+  uint8_t* ws = nullptr;
+  st = scratch_address(group, use_mma_consumer(group, cfg->flags), &ws);
+  if (st != PKD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t off = make_layout(*cfg, cfg->num_ctas).err_byte;
+  int32_t v = 0;
+  // stream-ordered read of the word, then its reset, then a wait for this
+  // stream only (pageable destination: the copy completes before it returns)
+  if (cudaMemcpyFromSymbolAsync(&v, g_static_scratch, sizeof v, off, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return PKD_E_CUDA;
+  if (cudaMemsetAsync(ws + off, 0, sizeof v, s) != cudaSuccess) return PKD_E_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKD_E_CUDA;
+  *dev_err = v;
   return PKD_OK;
 }

@@ -78,7 +78,8 @@ def _compare(cfg, indptr, indices, last, alpha, min_chunk, chunk_rule="closed"):
                      chunk_rule=chunk_rule)
     # header word 16: the most chunks of any split request
     assert got["header"][16] == max([n for _, n in ref.units], default=0)
-    assert got["header"][17:] == [0] * 15
+    assert got["header"][17:19] == [cfg.max_batch, cfg.max_num_pages]
+    assert got["header"][19:] == [0] * 13
     assert info["chunk_tokens"] == ref.chunk
     assert info["makespan"] == ref.makespan
     assert info["num_items"] == ref.n_items
@@ -315,3 +316,54 @@ def test_plan_fast_path_marshalling():
     finally:
         m.init(ctypes.cast(lib.pkd_plan, ctypes.c_void_p).value,
                ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value)
+
+
+def test_static_scratch_rejects_mismatched_schedules(lib):
+    """pkd_run_static_scratch checks a host schedule against the layout of the
+    configuration it is given before anything reaches the GPU: a schedule
+    planned for other capacities (other word offsets) or with an index out of
+    range is refused with INVALID_ARG, no CUDA call made."""
+    import torch
+    if torch.cuda.is_available():
+        # stand-in device pointers below: never let a schedule that the check
+        # should refuse reach a real GPU
+        pytest.skip("host-only check; runs where no GPU is present")
+    w = workloads.workload("skewed")
+    t = workloads.make_tables(w)
+    nnz = int(t["indptr"][-1])
+    cfg = pkd.make_config(w.hq, w.hkv, 128, 16, w.batch, nnz, w.pool_pages, -1, -1, 152)
+    words, info, off = pkd.plan_host(cfg, t["indptr"], t["indices"], t["last"])
+    fake = ctypes.c_void_p(1 << 12)   # aligned, non-null: only the schedule decides
+
+    def run(c, wd):
+        return lib.pkd_run_static_scratch(ctypes.byref(c), ctypes.c_void_p(wd.ctypes.data),
+                                          wd.size, fake, fake, fake, fake, None)
+
+    # the untouched schedule passes every host check and only then needs the
+    # device (none here: a CUDA error, not INVALID_ARG)
+    assert run(cfg, words) == -8
+
+    for field, delta in (("max_batch", 1), ("max_num_pages", 16)):
+        other = pkd.make_config(w.hq, w.hkv, 128, 16, w.batch, nnz, w.pool_pages, -1, -1, 152)
+        setattr(other, field, getattr(other, field) + delta)
+        # planned for cfg, run against a layout with other offsets
+        assert run(other, np.resize(words, pkd.schedule_layout(other)[5])) == -1
+    corrupt = []
+    item0 = off[1]
+    bad = words.copy()
+    bad[item0 + 3] = 10 ** 6                      # partial-state slot past the layout
+    corrupt.append(bad)
+    bad = words.copy()
+    bad[item0 + 4] = nnz                          # first page past the page list
+    corrupt.append(bad)
+    bad = words.copy()
+    bad[item0 + 0] = w.batch                      # request outside the batch
+    corrupt.append(bad)
+    bad = words.copy()
+    bad[off[0] + 1] = bad[off[0] + 2] + 1         # CTA queues out of order
+    corrupt.append(bad)
+    bad = words.copy()
+    bad[off[3] + 1] = 10 ** 6                     # merge range past the slots
+    corrupt.append(bad)
+    for bad in corrupt:
+        assert run(cfg, bad) == -1

@@ -168,3 +168,26 @@ def test_graph_capture_with_host_io():
 def oracle_decode(q, kv, t, w):
     import oracle
     return oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=w.hq, hkv=w.hkv)
+
+
+def test_error_poll_waits_for_its_own_stream_only():
+    """pkd_last_device_error orders its read and reset on the caller's
+    stream and waits for that stream alone: a long kernel on another stream
+    is still running when the poll returns."""
+    import time
+    w, t, q, kv, dec = _setup()
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    dec.run(q, kv)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    poll = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(int(2e9))        # about a second of spinning at GB300 clocks
+    t0 = time.perf_counter()
+    err = dec.device_error(stream=poll)
+    dt = time.perf_counter() - t0
+    still_running = not side.query()
+    side.synchronize()
+    assert err == 0
+    assert still_running, "the poll waited for another stream's kernel"
+    assert dt < 0.25, dt

@@ -181,21 +181,33 @@ def aggregate_throughput(bytes_per_rank_step, ms_per_step, world):
 
 # ---------------------------------------------------------------- our arm
 
-def _views(w, t):
-    """(name, group_indptr or None, (indptr, indices, last)) per planned level.
-    The shared prefix is one group: every request over the 512 prefix pages,
-    planned as a shared-prefix level (FlashInfer 完全拆解, Composable Format)."""
+def _views(w, t, prefix_mode="cascade"):
+    """(name, group_indptr or None, tables) per planned context.  The shared
+    prefix is one group: every request over the prefix pages (FlashInfer
+    完全拆解, Composable Format).  "cascade": one context plans the prefix
+    level and the suffixes together (tables = (prefix, suffix)); "levels":
+    a shared-prefix context and a plain one, joined by merge_states."""
     if w.prefix_tokens:
         n_pre = w.prefix_tokens // w.page_size
         prefix = (np.array([0, n_pre], np.int32), np.asarray(t["prefix"][1][:n_pre], np.int32),
                   np.array([w.page_size], np.int32))
-        return [("prefix", np.array([0, w.batch], np.int32), prefix),
-                ("suffix", None, t["suffix"])]
+        gi = np.array([0, w.batch], np.int32)
+        if prefix_mode == "cascade":
+            return [("cascade", gi, (prefix, t["suffix"]))]
+        return [("prefix", gi, prefix), ("suffix", None, t["suffix"])]
     return [("full", None, (t["indptr"], t["indices"], t["last"]))]
 
 
-def _plan(d, group_indptr, table, stream=None):
-    if group_indptr is None:
+def _nnz(name, table):
+    if name == "cascade":
+        return int(table[0][0][-1]) + int(table[1][0][-1])
+    return int(table[0][-1])
+
+
+def _plan(d, group_indptr, table, stream=None, name=None):
+    if name == "cascade":
+        d.plan_cascade(group_indptr, table[0], table[1], stream=stream)
+    elif group_indptr is None:
         d.plan(*table, stream=stream)
     else:
         d.plan_shared(group_indptr, *table, stream=stream)
@@ -256,6 +268,33 @@ def _composed_step_graph(ds, q, kv, po, pl, so, sl, out, lse, side, dev, io=None
     return _ComposedGraph(g)
 
 
+def _cascade_step_graph(dec, q, kv, out, lse, dev, io):
+    """A torch CUDA graph of one cascade step (the launch and its merge)
+    with, on two branches beside it, the next step's q copied in from pinned
+    host memory and the previous step's out + lse copied back (io = ((in
+    stream, out stream), [(device dst, host src)], [(host dst, device
+    src)]))."""
+    import torch
+    main = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(main):
+        dec.run(q, kv, out=out, lse=lse)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    (s_in, s_out), copies_in, copies_out = io
+    with torch.cuda.graph(g, stream=main):
+        fork = torch.cuda.Event()
+        fork.record(main)
+        for st, pairs in ((s_in, copies_in), (s_out, copies_out)):
+            st.wait_event(fork)
+            with torch.cuda.stream(st):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+        dec.run(q, kv, out=out, lse=lse)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+    return _ComposedGraph(g)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -285,7 +324,8 @@ def run_ours(args, rank, world):
     qs = workloads.make_q(w, device=dev, layers=layers)
     outs = [torch.empty_like(x) for x in qs]
     lses = [torch.empty(w.batch, w.hq, dtype=torch.float32, device=dev) for _ in qs]
-    views = _views(w, t)
+    views = _views(w, t, args.prefix_mode)
+    cascade = views[0][0] == "cascade"
     # Two planning contexts used on alternate steps: the schedule of step k+1
     # is uploaded on a copy stream while step k's kernels run (each context's
     # workspace is rewritten only after the step that last read it is done).
@@ -293,20 +333,21 @@ def run_ours(args, rank, world):
     sets = []
     for _ in range(n_sets):
         decs = []
-        for name, gi, (ip, ix, la) in views:
+        for name, gi, tables in views:
             d = pkd.BatchDecodeWithPagedKVCache(w.hq, w.hkv, w.head_dim, P, max_batch=w.batch,
-                                                max_num_pages=int(ip[-1]),
-                                                shared_prefix=gi is not None,
+                                                max_num_pages=_nnz(name, tables),
+                                                shared_prefix=gi is not None and not cascade,
+                                                cascade=cascade,
                                                 kv_dtype=w.kv_dtype,
                                                 kv_layout=w.kv_layout,
                                                 num_pages=w.pool_pages,
                                                 use_tensor_cores={"auto": None, "fma": False,
                                                                   "mma": True}[args.consumer],
                                                 chunk_rule=args.chunk_rule, alpha=args.alpha,
-                                                dense_prefix=(gi is not None and
-                                                              args.prefix_kernel == "dense"),
+                                                dense_prefix=(gi is not None and not cascade
+                                                              and args.prefix_kernel == "dense"),
                                                 device=dev)
-            _plan(d, gi, (ip, ix, la))
+            _plan(d, gi, tables, name=name)
             decs.append(d)
         sets.append(decs)
     decs = sets[0]
@@ -317,7 +358,14 @@ def run_ours(args, rank, world):
     # they are kept out of the step timing).
     graphs = [[] for _ in range(n_sets)]
     tgraphs = [[] for _ in range(n_sets)]
-    if w.prefix_tokens:
+    if cascade:
+        # one context: the cascade launch and its merge, per cache copy
+        for si, ds in enumerate(sets):
+            for c in range(copies):
+                for timing, dst in ((False, graphs), (True, tgraphs)):
+                    dst[si].append((ds[0].capture([qs[0]], [kvs[c]], [outs[0]], [lses[0]],
+                                                  timing=timing), None, c))
+    elif w.prefix_tokens:
         # prefix run + suffix run + merge_states, per cache copy.  The step
         # graph holds all three: the two levels are independent and run on
         # two captured streams, merge_states joins them.  The timing graphs
@@ -360,7 +408,7 @@ def run_ours(args, rank, world):
         si = k % n_sets
         copy_stream.wait_event(done[si])
         for (name, gi, table), d in zip(views, sets[si]):
-            _plan(d, gi, table, stream=copy_stream)
+            _plan(d, gi, table, stream=copy_stream, name=name)
         copied[si].record(copy_stream)
         stream.wait_event(copied[si])
         gp, gs, c = graph_of(k)
@@ -410,9 +458,12 @@ def run_ours(args, rank, world):
         io = w.batch * w.hq * (w.head_dim * 2 * 2 + 4)
         table = 4 * (n_pre + 3 + 2 + int(t["suffix"][0][-1]) + 2 * w.batch + 1)
         step_bytes = kv_bytes + io + table
-        # per launch: the prefix level reads the shared pages once for all requests
-        layer_bytes = [alg_bytes_per_layer(w, [w.prefix_tokens], n_pre),
-                       alg_bytes_per_layer(w, suf_lens, int(t["suffix"][0][-1]))]
+        if cascade:   # one launch moves the whole step
+            layer_bytes = [step_bytes]
+        else:
+            # per launch: the prefix level reads the shared pages once for all requests
+            layer_bytes = [alg_bytes_per_layer(w, [w.prefix_tokens], n_pre),
+                           alg_bytes_per_layer(w, suf_lens, int(t["suffix"][0][-1]))]
     else:
         lb = alg_bytes_per_layer(w, lens, nnz)
         step_bytes = lb * layers
@@ -426,7 +477,18 @@ def run_ours(args, rank, world):
     info = decs[0].plan_info()
 
     # end to end: host q in, host out back, plan from host tables, per step
-    if w.prefix_tokens:
+    if cascade:
+        side_e2e = [torch.cuda.Stream(device=dev) for _ in range(2)]
+
+        def capture_io(si, dq, do, dl, hq, ho, hl, c):
+            nx = 1 - si
+            return _cascade_step_graph(
+                sets[si][0], dq[si][0], kvs[c], do[si][0], dl[si][0], dev,
+                io=((side_e2e[0], side_e2e[1]), [(dq[nx][0], hq[0])],
+                    [(ho[0], do[nx][0]), (hl[0], dl[nx][0])]))
+        e2e = run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stream,
+                               step_bytes, world, dev)
+    elif w.prefix_tokens:
         side_e2e = [torch.cuda.Stream(device=dev) for _ in range(3)]
 
         def capture_io(si, dq, do, dl, hq, ho, hl, c):
@@ -450,7 +512,7 @@ def run_ours(args, rank, world):
 
     clocks = sampler.summary()
     gp0, _, _ = graphs[0][0]
-    launches_per_step = 5 if w.prefix_tokens else 2 * gp0.layers
+    launches_per_step = 5 if (w.prefix_tokens and not cascade) else 2 * gp0.layers
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -477,12 +539,14 @@ def run_ours(args, rank, world):
             "consumer": args.consumer,
             "chunk_rule": args.chunk_rule,
             "alpha": args.alpha if args.alpha >= 0 else "default (32)",
-            "prefix_kernel": args.prefix_kernel if w.prefix_tokens else None,
+            "prefix_kernel": (("cascade (dense tensor-core prefix role + decode role, one "
+                               "launch, one merge)") if cascade else args.prefix_kernel)
+                             if w.prefix_tokens else None,
             "l2": (f"inputs larger than L2: {n_kv} distinct caches of "
                    f"{kvs[0].numel() * kvs[0].element_size() / 1e9:.2f} GB, "
                    + ("one per layer" if copies == 1 else "rotated over replays")),
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
-                                          "makespan")},
+                                          "makespan", "prefix_ctas", "prefix_chunk_tokens")},
             "parallelism": f"replicas x{world} (no collective)",
         },
         "roofline": {
@@ -546,7 +610,7 @@ def run_e2e_pipelined(args, sets, views, capture, copies, qs, outs, lses, stream
         h2d_stream.wait_event(ran[si])
         h2d_stream.wait_event(back[si])
         for (name, gi, table), d in zip(views, sets[si]):
-            _plan(d, gi, table, stream=h2d_stream)
+            _plan(d, gi, table, stream=h2d_stream, name=name)
         with torch.cuda.stream(h2d_stream):
             for x, h in zip(dq[si], hq):
                 x.copy_(h, non_blocking=True)
@@ -632,7 +696,7 @@ def run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stre
         si = k % n_sets
         copy_stream.wait_event(done[si])
         for (name, gi, table), d in zip(views, sets[si]):
-            _plan(d, gi, table, stream=copy_stream)
+            _plan(d, gi, table, stream=copy_stream, name=name)
         copied[si].record(copy_stream)
         stream.wait_event(copied[si])
         graphs[si][(k // n_sets) % copies].launch()
@@ -790,9 +854,10 @@ def run_prefix_sweep(args, rank, world):
     """Shared prefix, composable against single format, over the pages' grid.
     Composable: the prefix level planned once for the whole batch (the dense
     tcgen05 kernel reads the prefix once per KV head) and the suffix level,
-    on two streams, joined by merge_states -- one CUDA graph.  Single: every
-    request over its full page table (prefix pages then its own), one decode
-    + merge.  GPU time per step: graph replays back to back, rotating over
+    on two streams, joined by merge_states -- one CUDA graph.  Cascade: both
+    levels in one plan, one launch (dense prefix CTAs beside decode CTAs)
+    and one merge.  Single: every request over its full page table (prefix
+    pages then its own), one decode + merge.  GPU time per step: graph replays back to back, rotating over
     enough cache copies that the step's bytes are not L2-resident; the host
     plans once per case (its cost is not in these numbers)."""
     import torch
@@ -833,14 +898,20 @@ def run_prefix_sweep(args, rank, world):
         suf.plan(*t["suffix"])
         single = mk(max_num_pages=int(t["indptr"][-1]))
         single.plan(t["indptr"], t["indices"], t["last"])
-        po, so, out_c, out_s = (torch.empty_like(q) for _ in range(4))
-        pl, sl, lse_c, lse_s = (torch.empty(B, w.hq, dtype=torch.float32, device=dev)
-                                for _ in range(4))
+        gi = np.array([0, B], np.int32)
+        prefix_t = (np.array([0, n_pre], np.int32), np.asarray(t["prefix"][1][:n_pre], np.int32),
+                    np.array([P], np.int32))
+        casc = mk(max_num_pages=n_pre + int(t["suffix"][0][-1]), cascade=True)
+        casc.plan_cascade(gi, prefix_t, t["suffix"])
+        po, so, out_c, out_s, out_k = (torch.empty_like(q) for _ in range(5))
+        pl, sl, lse_c, lse_s, lse_k = (torch.empty(B, w.hq, dtype=torch.float32, device=dev)
+                                       for _ in range(5))
         comp = [_composed_step_graph((pre, suf), q, kvs[c], po, pl, so, sl, out_c, lse_c, side,
                                      dev) for c in range(copies)]
         sing = [single.capture([q], [kvs[c]], [out_s], [lse_s]) for c in range(copies)]
+        cgr = [casc.capture([q], [kvs[c]], [out_k], [lse_k]) for c in range(copies)]
         us = {}
-        for name, gs in (("composable", comp), ("single", sing)):
+        for name, gs in (("composable", comp), ("single", sing), ("cascade", cgr)):
             for k in range(3):
                 gs[k % copies].launch()
             torch.cuda.synchronize()
@@ -855,24 +926,31 @@ def run_prefix_sweep(args, rank, world):
         # the two formats compute the same states (up to rounding)
         comp[0].launch()
         sing[0].launch()
+        cgr[0].launch()
         torch.cuda.synchronize()
-        diff = float((out_c.float() - out_s.float()).abs().max())
-        ldiff = float((lse_c - lse_s).abs().max())
-        launches += reps * (5 + 2)
+        diff = float(max((out_c.float() - out_s.float()).abs().max(),
+                         (out_k.float() - out_s.float()).abs().max()))
+        ldiff = float(max((lse_c - lse_s).abs().max(), (lse_k - lse_s).abs().max()))
+        launches += reps * (5 + 2 + 2)
+        cinfo = casc.plan_info()
         kv_once = (prefix + 128 * B) * 2 * w.hkv * w.head_dim * 2
         rows.append({"prefix": prefix, "batch": B, "suffix": 128,
                      "composable_us": round(us["composable"], 2),
+                     "cascade_us": round(us["cascade"], 2),
                      "single_us": round(us["single"], 2),
                      "speedup": round(us["single"] / us["composable"], 2),
+                     "cascade_speedup": round(us["single"] / us["cascade"], 2),
+                     "cascade_plan": {k: cinfo[k] for k in ("prefix_ctas", "prefix_chunk_tokens",
+                                                            "chunk_tokens", "num_items")},
                      "composable_GBps_prefix_once": round(kv_once / (us["composable"] * 1e3), 1),
                      "single_GBps_per_request_reads": round(
                          (prefix + 128) * B * 2 * w.hkv * w.head_dim * 2 / (us["single"] * 1e3), 1),
                      "max_abs_diff_out": round(diff, 5), "max_abs_diff_lse": round(ldiff, 6),
                      "pages_us_composable": pages_comp, "pages_us_single": pages_single,
                      "cache_copies": copies})
-        for g in sing:
+        for g in sing + cgr:
             g.close()
-        del kvs, comp, sing, pre, suf, single
+        del kvs, comp, sing, cgr, pre, suf, single, casc
         torch.cuda.empty_cache()
     big = rows[-1]
     return {"metric": "shared-prefix decode latency, composable vs single format "
@@ -1127,6 +1205,9 @@ def main():
                     help="prefix_sweep: only these cases, e.g. 32768x64,1024x16 (prefix x batch)")
     ap.add_argument("--alpha", type=int, default=-1,
                     help="planner per-item cost in tokens (cost = alpha + tokens); -1: default")
+    ap.add_argument("--prefix-mode", choices=["cascade", "levels"], default="cascade",
+                    help="shared-prefix step: one cascade plan and launch with one merge, or "
+                         "two levels (prefix context + suffix context) joined by merge_states")
     ap.add_argument("--prefix-kernel", choices=["dense", "mma"], default="dense",
                     help="shared-prefix level: the tcgen05 dense kernel (128-row tiles per KV "
                          "head) or the mma.sync row-block consumer (16-row tiles)")

@@ -166,6 +166,9 @@ typedef struct pkd_plan_info {
                                   copy per token row (pkd_plan /
                                   pkd_plan_shared fill it; pkd_plan_host
                                   leaves it 0)                              */
+    int32_t prefix_ctas;       /* cascade plans: CTAs given the shared-prefix
+                                  level (0 otherwise)                       */
+    int32_t prefix_chunk_tokens; /* cascade plans: that level's chunk        */
 } pkd_plan_info;
 
 /* Bytes of device workspace needed for this configuration.  With
@@ -208,6 +211,24 @@ int pkd_plan(pkd_ctx *ctx, const int32_t *indptr, const int32_t *indices,
 int pkd_plan_shared(pkd_ctx *ctx, const int32_t *group_indptr, int32_t num_groups,
                     const int32_t *indptr, const int32_t *indices,
                     const int32_t *last_page_len, void *stream, uint64_t *epoch);
+
+/* Plan a cascade step (needs a context created with PKD_FLAG_CASCADE): the
+ * shared-prefix level and every request's own suffix in one schedule.
+ * Requests group_indptr[j] .. group_indptr[j+1]-1 (group_indptr[0] = 0,
+ * strictly increasing, batch = group_indptr[num_groups]) share group j's
+ * prefix pages p_indices[p_indptr[j] .. p_indptr[j+1]) with p_last[j] tokens
+ * in the last one; request r's own pages are s_indices[s_indptr[r] ..
+ * s_indptr[r+1]) with s_last[r] (every request has at least one suffix
+ * token).  Request r attends over its prefix then its suffix: pkd_run
+ * returns out / lse over both, merged ("FlashInfer, in depth", "Prefill,
+ * masks and shared prefixes": the shared pages once for all queries, each
+ * suffix separately, one LSE combine).  Host arrays, int32, copied before
+ * the call returns.  The page capacity (max_num_pages) covers both tables.
+ * Errors: INVALID_ARG, BAD_TABLE, CAPACITY, CUDA. */
+int pkd_plan_cascade(pkd_ctx *ctx, const int32_t *group_indptr, int32_t num_groups,
+                     const int32_t *p_indptr, const int32_t *p_indices, const int32_t *p_last,
+                     const int32_t *s_indptr, const int32_t *s_indices, const int32_t *s_last,
+                     void *stream, uint64_t *epoch);
 
 /* Summary of the current plan.  Errors: INVALID_ARG, NO_PLAN. */
 int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
@@ -346,6 +367,15 @@ int pkd_plan_host_shared(const pkd_config *cfg, const int32_t *group_indptr,
                          const int32_t *last_page_len, int32_t *host_words,
                          size_t max_words, pkd_plan_info *info);
 
+/* pkd_plan_host for a cascade plan (cfg->flags has PKD_FLAG_CASCADE;
+ * arguments as pkd_plan_cascade). */
+int pkd_plan_host_cascade(const pkd_config *cfg, const int32_t *group_indptr,
+                          int32_t num_groups, const int32_t *p_indptr,
+                          const int32_t *p_indices, const int32_t *p_last,
+                          const int32_t *s_indptr, const int32_t *s_indices,
+                          const int32_t *s_last, int32_t *host_words, size_t max_words,
+                          pkd_plan_info *info);
+
 /* Word offsets of the schedule arrays (see pkd_plan_host):
  *   off[0] cta_indptr[num_ctas + 1]
  *   off[1] items[num_items][8] = {req, tok_begin, tok_end, dst_slot,
@@ -355,7 +385,10 @@ int pkd_plan_host_shared(const pkd_config *cfg, const int32_t *group_indptr,
  *          without grouping); dst_slot -1 = write through to out/lse, else
  *          request req + i writes slot dst_slot + i * slot_stride;
  *          first_page = indptr[table row] + tok_begin / P, an index into
- *          page_list)
+ *          page_list; cascade plans: prefix items have slot stride -1 and
+ *          dst_slot = their chunk index, request req + i writing slot
+ *          merge_indptr[req + i] + dst_slot; the page list holds the prefix
+ *          table's indices, then the suffix table's)
  *   off[2] units[num_units][2] = {req, num_chunks}
  *   off[3] merge_indptr[num_units + 1]
  *   off[4] page_list[nnz]    (the CSR indices, unchanged)
@@ -364,7 +397,8 @@ int pkd_plan_host_shared(const pkd_config *cfg, const int32_t *group_indptr,
  * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (clamped to
  * int32), split floor, requests per block, the most chunks of any split
  * request, the max_batch and max_num_pages the offsets were laid out for,
- * then zeros.  Errors: INVALID_ARG. */
+ * (cascade plans) the CTAs of the prefix level and its chunk, then zeros.
+ * Errors: INVALID_ARG. */
 int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 
 /* ---- CUDA-graph capture of a whole decode step ------------------------- */

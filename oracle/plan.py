@@ -240,3 +240,187 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
     page_list = [int(x) for x in indices[: indptr[-1] if indptr else 0]]
     return Plan(chunk, makespan, cta_indptr, items, units, merge_indptr,
                 page_list, lens, heads)
+
+
+@dataclass
+class CascadePlan:
+    n_pre: int                # CTAs [0, n_pre) run the prefix items
+    chunk_pre: int
+    chunk_suf: int
+    makespan: int             # in suffix-token units (the larger level's)
+    cta_indptr: list
+    items: list               # (first request, tok_begin, tok_end, dst, first page index,
+    #                           requests, slot stride, KV head), queue order
+    units: list               # (request, slots) for every request
+    merge_indptr: list
+    page_list: list           # prefix table's page ids, then the suffix table's
+
+
+def _level(ulens, n, page_size, floor, alpha):
+    """One level of a cascade plan: closed-form chunk candidates (the work
+    bound over the level's n CTAs, and its half), page-rounded and not below
+    the floor; the smaller LPT makespan wins (ties: the larger chunk)."""
+    bound = _ceil_div(sum(ulens), n)
+    best = None
+    prev = None
+    for k in (1, 2):
+        c = max(_round_up(_ceil_div(bound, k), page_size), floor)
+        if c == prev:
+            continue
+        prev = c
+        if best is not None:
+            # a makespan is at least the costliest item and the mean load:
+            # a candidate that cannot beat the best strictly is not scheduled
+            n_it = sum(_ceil_div(l, c) for l in ulens)
+            lb = max(alpha + max(min(l, c) for l in ulens),
+                     _ceil_div(sum(ulens) + alpha * n_it, n))
+            if lb >= best[1]:
+                continue
+        queues, span = _lpt(_split(ulens, c, alpha), n)
+        if best is None or span < best[1]:
+            best = (c, span, queues)
+    return best
+
+
+def _prefix_level(block_lens, hkv, n, page_size, floor, alpha):
+    """The prefix level of a cascade plan on a budget of n CTAs: at most one
+    item per CTA.  Every block starts with one chunk per KV head; while hkv
+    more CTAs are left, the block with the longest chunk (ties: the first)
+    gets one more chunk per head, unless its chunk would fall below the
+    floor.  Chunks are page-rounded; item j goes to CTA j.  With more heads
+    than CTAs the (block, head) units stay whole and LPT places them.
+    Returns (span, queues, chunk per block, CTAs used)."""
+    nb = len(block_lens)
+    if nb * hkv > n:
+        top = max(max(block_lens), 1)
+        units = [l for l in block_lens for _ in range(hkv)]
+        queues, span = _lpt(_split(units, top, alpha), n)
+        return span, queues, [top] * nb, n
+    m = [1] * nb
+    chunk = [_round_up(l, page_size) for l in block_lens]
+    budget = n - nb * hkv
+    while budget >= hkv:
+        b = max(range(nb), key=lambda i: (chunk[i], -i))
+        nxt = _round_up(_ceil_div(block_lens[b], m[b] + 1), page_size)
+        if nxt < floor:
+            break
+        m[b] += 1
+        chunk[b] = nxt
+        budget -= hkv
+    queues, span = [], 0
+    for b, l in enumerate(block_lens):
+        for h in range(hkv):
+            k, t = 0, 0
+            while t < l:
+                e = min(t + chunk[b], l)
+                queues.append([(alpha + e - t, b * hkv + h, k, t, e)])
+                span = max(span, alpha + e - t)
+                t, k = e, k + 1
+    return span, queues, chunk, len(queues)
+
+
+def plan_cascade(group_indptr, prefix, suffix, *, page_size: int, num_pages: int, n_cta: int,
+                 hkv: int, rows: int, alpha: int, prefix_alpha: int, prefix_cost16: int,
+                 suffix_floor: int, prefix_floor: int = 128) -> CascadePlan:
+    """A decode step whose requests share prefix pages in groups and each own
+    a suffix ("FlashInfer, in depth", "Prefill, masks and shared prefixes" and
+    "Cascades, Merges, and the Autotuner": the shared part once for all
+    queries, each suffix apart, one merge of the two states; "FlashInfer
+    完全拆解", Composable Format), planned as one schedule:
+
+    * prefix work units are (block of up to ``rows`` requests of a group,
+      KV head), block-major; suffix units are the requests;
+    * the grid is cut at n_pre: CTAs [0, n_pre) take the prefix level (at
+      most one item each, see _prefix_level), the rest the suffix level,
+      split at its own closed-form chunk and scheduled by LPT (P1-P3 above)
+      on its own CTAs;
+    * prefix items cost (prefix_alpha + tokens) * prefix_cost16 / 16 in
+      suffix-token units, suffix items alpha + tokens; the prefix budget
+      starts where each level gets CTAs in proportion to its total cost (in
+      steps of hkv above one CTA per unit when the grid allows, rounded to
+      the nearest step) and climbs: both neighbouring budgets of the best so
+      far are scheduled (the lower first) while the predicted makespan falls
+      strictly; the suffix gets every CTA the prefix items do not use;
+    * every request is a unit of the reduction map whose slots are its
+      prefix chunks then its suffix chunks (all items write partial states).
+    """
+    P = page_size
+    gi = [int(x) for x in group_indptr]
+    p_ip, p_ix, p_last = prefix
+    s_ip, s_ix, s_last = suffix
+    pre_len = lengths(p_ip, p_last, p_ix, P, num_pages)
+    suf_len = lengths(s_ip, s_last, s_ix, P, num_pages)
+    if len(gi) != len(pre_len) + 1 or (gi and gi[0] != 0):
+        raise TableError("group_indptr must have one entry per group + 1, starting at 0")
+    batch = gi[-1] if gi else 0
+    if len(suf_len) != batch:
+        raise TableError("one suffix row per request")
+    blocks = []                          # (first request, n, group)
+    for j in range(len(pre_len)):
+        if gi[j + 1] <= gi[j]:
+            raise TableError(f"group {j} has no request")
+        for r in range(gi[j], gi[j + 1], rows):
+            blocks.append((r, min(rows, gi[j + 1] - r), j))
+    block_of = {}
+    for b, (r0, n, j) in enumerate(blocks):
+        for r in range(r0, r0 + n):
+            block_of[r] = b
+    block_lens = [pre_len[j] for (_, _, j) in blocks]
+    pre_cost = sum(hkv * (prefix_alpha + l) * prefix_cost16 for l in block_lens)
+    suf_cost = sum((alpha + l) * 16 for l in suf_len)
+    floor_s = _round_up(max(suffix_floor, 1), P)
+    floor_p = _round_up(prefix_floor, P)
+    best = None
+    if batch:
+        units = len(blocks) * hkv
+        split = units <= n_cta - 1
+        base, step = (units, hkv) if split else (1, 1)
+        j_max = (n_cta - 1 - base) // step
+        prop = (n_cta * pre_cost + (pre_cost + suf_cost) // 2) // (pre_cost + suf_cost)
+        j0 = min(max((max(prop - base, 0) + step // 2) // step, 0), j_max)
+
+        def schedule(j):
+            pre = _prefix_level(block_lens, hkv, base + step * j, P, floor_p, prefix_alpha)
+            suf = _level(suf_len, n_cta - pre[3], P, floor_s, alpha)
+            return (max(pre[0] * prefix_cost16, suf[1] * 16), j, pre, suf)
+
+        best = schedule(j0)
+        tried = {j0}
+        while True:
+            at = best[1]
+            for nb in (at - 1, at + 1):
+                if 0 <= nb <= j_max and nb not in tried:
+                    tried.add(nb)
+                    cand = schedule(nb)
+                    if cand[0] < best[0]:
+                        best = cand
+            if best[1] == at:
+                break
+    if best is None:
+        return CascadePlan(0, 0, 0, 0, [0] * (n_cta + 1), [], [], [0], [])
+    span, _, (_, q_pre, block_chunk, n_pre), (c_s, _, q_suf) = best
+    np_block = [_ceil_div(l, c) for l, c in zip(block_lens, block_chunk)]
+    units, merge_indptr = [], [0]
+    for r in range(batch):
+        n = np_block[block_of[r]] + _ceil_div(suf_len[r], c_s)
+        units.append((r, n))
+        merge_indptr.append(merge_indptr[-1] + n)
+    p_ip = [int(x) for x in p_ip]
+    s_ip = [int(x) for x in s_ip]
+    nnz_p = p_ip[-1] if p_ip else 0
+    cta_indptr, items = [0], []
+    for q in q_pre:
+        for cost, u, k, tb, te in q:
+            b, head = divmod(u, hkv)
+            r0, n, j = blocks[b]
+            items.append((r0, tb, te, k, p_ip[j] + tb // P, n, -1, head))
+        cta_indptr.append(len(items))
+    for q in q_suf:
+        for cost, r, k, tb, te in q:
+            items.append((r, tb, te, merge_indptr[r] + np_block[block_of[r]] + k,
+                          nnz_p + s_ip[r] + tb // P, 1, 0, 0))
+        cta_indptr.append(len(items))
+    page_list = [int(x) for x in p_ix[:nnz_p]] + [int(x) for x in s_ix[:s_ip[-1] if s_ip else 0]]
+    chunk_pre = max((min(c, l) for c, l in zip(block_chunk, block_lens)), default=0)
+    return CascadePlan(n_pre, chunk_pre, c_s, span // 16, cta_indptr, items, units,
+                       merge_indptr, page_list)

@@ -17,6 +17,9 @@ API (names follow the pages' plan / run / merge_states):
 * :func:`merge_states` -- exact LSE merge of two attention states.
 * :func:`append_kv` -- write a step's new K / V rows into their page slots.
 * :func:`plan_host` -- the scheduler alone on the host (no GPU), for tests.
+* ``cascade=True`` contexts: ``plan_cascade(group_indptr, prefix, suffix)``
+  plans a shared prefix and every request's own suffix together; ``run``
+  returns attention over both, merged.
 * :func:`selftest_bounded_wait` -- the device-side bounded-wait self-test.
 """
 from __future__ import annotations
@@ -28,7 +31,7 @@ import numpy as np
 
 __all__ = [
     "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states", "append_kv",
-    "append_kv_layers", "plan_host", "plan_host_shared", "schedule_layout",
+    "append_kv_layers", "plan_host", "plan_host_shared", "plan_host_cascade", "schedule_layout",
     "selftest_bounded_wait", "Graph",
     "STATUS",
 ]
@@ -55,6 +58,7 @@ EXPORTS = (
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
     "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
     "pkd_selftest_bounded_wait", "pkd_append_kv_layers", "pkd_static_scratch_last_error",
+    "pkd_plan_cascade", "pkd_plan_host_cascade",
 )
 
 
@@ -78,7 +82,8 @@ class PlanInfo(ctypes.Structure):
                 ("num_units", ctypes.c_int32), ("num_slots", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("makespan", ctypes.c_int64),
                 ("nnz", ctypes.c_int32), ("schedule_words", ctypes.c_int32),
-                ("page_tiles", ctypes.c_int32)]
+                ("page_tiles", ctypes.c_int32), ("prefix_ctas", ctypes.c_int32),
+                ("prefix_chunk_tokens", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -131,6 +136,10 @@ def load():
         "pkd_version": (ctypes.c_int, []),
         "pkd_run_static_scratch": (ctypes.c_int, [cfgp, vp, sz, vp, vp, vp, vp, vp]),
         "pkd_static_scratch_last_error": (ctypes.c_int, [cfgp, vp, ctypes.POINTER(i32)]),
+        "pkd_plan_cascade": (ctypes.c_int, [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                            ctypes.POINTER(u64)]),
+        "pkd_plan_host_cascade": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                                 ctypes.POINTER(PlanInfo)]),
         "pkd_append_kv": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
                                          i32, i32, vp, vp]),
         "pkd_append_kv_ex": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
@@ -186,6 +195,7 @@ FLAG_ROW_COPIES = 16    # force one KV copy per token row (no page-tile tensor m
 FLAG_CHUNK_SEARCH = 64  # chunk = largest page multiple still giving >= N_CTA items
 FLAG_HND = 32           # cache layout [pages, 2, Hkv, P, D] instead of NHD [pages, 2, P, Hkv, D]
 FLAG_DENSE_PREFIX = 128  # shared prefix on tcgen05 tensor cores: 128-row tiles, one KV head per item
+FLAG_CASCADE = 256      # both levels of a shared-prefix step in one plan, one launch, one merge
 
 
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, max_batch, max_num_pages,
@@ -229,6 +239,37 @@ def plan_host_shared(cfg: Config, group_indptr, indptr, indices, last_page_len):
     return words, info.as_dict(), off
 
 
+def _cascade_tables(group_indptr, prefix, suffix):
+    gi = _host_i32(group_indptr)
+    p = [_host_i32(x) for x in prefix]
+    q = [_host_i32(x) for x in suffix]
+    n_groups = p[2].shape[0]
+    batch = q[2].shape[0]
+    if gi.shape[0] != n_groups + 1 or p[0].shape[0] != n_groups + 1:
+        raise PkdError(-2, "group_indptr and the prefix indptr need one entry per group + 1")
+    if q[0].shape[0] != batch + 1 or (n_groups and int(gi[-1]) != batch):
+        raise PkdError(-2, "the suffix table needs one row per request of the groups")
+    for ip, ix in ((p[0], p[1]), (q[0], q[1])):
+        if ip.shape[0] > 1 and ix.shape[0] < ip[-1]:
+            raise PkdError(-2, "indices shorter than indptr[-1]")
+    return gi, n_groups, p, q
+
+
+def plan_host_cascade(cfg: Config, group_indptr, prefix, suffix):
+    """The C++ scheduler for a cascade step, on the host.  prefix = (indptr,
+    indices, last_page_len) over groups, suffix = the same over requests."""
+    lib = load()
+    gi, n_groups, p, q = _cascade_tables(group_indptr, prefix, suffix)
+    off = schedule_layout(cfg)
+    words = np.zeros(off[5], dtype=np.int32)
+    info = PlanInfo()
+    st = lib.pkd_plan_host_cascade(ctypes.byref(cfg), _ptr(gi), n_groups, *[_ptr(x) for x in p],
+                                   *[_ptr(x) for x in q], _ptr(words), words.size,
+                                   ctypes.byref(info))
+    _check(st, "pkd_plan_host_cascade")
+    return words, info.as_dict(), off
+
+
 def decode_schedule(words, off, info):
     """Unpack schedule words into python lists (same shape as the plan
     restatement's fields)."""
@@ -259,7 +300,8 @@ def _fast():
             from . import _pkd_plan as m
             lib = load()
             m.init(ctypes.cast(lib.pkd_plan, ctypes.c_void_p).value,
-                   ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value)
+                   ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value,
+                   ctypes.cast(lib.pkd_plan_cascade, ctypes.c_void_p).value)
             _fast_plan = m
         except ImportError:
             _fast_plan = False
@@ -326,7 +368,8 @@ class BatchDecodeWithPagedKVCache:
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, *, max_batch,
                  max_num_pages, num_pages, alpha=-1, min_chunk_tokens=-1, num_ctas=0,
                  use_tensor_cores=None, shared_prefix=False, kv_dtype="bf16", kv_layout="NHD",
-                 row_copies=False, chunk_rule="closed", dense_prefix=False, device=None):
+                 row_copies=False, chunk_rule="closed", dense_prefix=False, cascade=False,
+                 device=None):
         import torch
         if kv_layout not in ("NHD", "HND"):
             raise ValueError("kv_layout must be 'NHD' [pages, 2, P, Hkv, D] or "
@@ -353,6 +396,12 @@ class BatchDecodeWithPagedKVCache:
             if not shared_prefix:
                 raise ValueError("dense_prefix needs shared_prefix=True")
             flags |= FLAG_DENSE_PREFIX
+        if cascade:
+            if shared_prefix or dense_prefix or row_copies or kv_dtype != "bf16" or \
+                    use_tensor_cores is False or chunk_rule != "closed":
+                raise ValueError("a cascade context runs both levels itself: bf16 cache, "
+                                 "tensor cores, the closed-form chunk rule")
+            flags |= FLAG_CASCADE
         if chunk_rule not in ("closed", "search"):
             raise ValueError("chunk_rule must be 'closed' or 'search'")
         if chunk_rule == "search":
@@ -426,6 +475,32 @@ class BatchDecodeWithPagedKVCache:
             _check(st, "pkd_plan_shared")
         self.epoch = self._ep.value
         self.batch = int(gi[-1]) if n_groups else 0
+        return self.epoch
+
+    def plan_cascade(self, group_indptr, prefix, suffix, stream=None):
+        """Plan a cascade step (needs ``cascade=True``): requests
+        group_indptr[j] .. group_indptr[j+1]-1 share group j's prefix pages,
+        prefix = (indptr, indices, last_page_len) over groups; suffix = the
+        same over requests, each request's own pages.  ``run`` then returns
+        attention over prefix + suffix, merged.  Returns the epoch."""
+        fast = _fast()
+        if fast is not None:
+            st, ep = fast.plan_cascade(self._hv, group_indptr, *prefix, *suffix,
+                                       _stream_ptr(stream))
+            if st != _NOT_HANDLED:
+                if st:
+                    _check(st, "pkd_plan_cascade")
+                self.epoch = ep
+                self.batch = len(suffix[2])
+                return ep
+        gi, n_groups, p, q = _cascade_tables(group_indptr, prefix, suffix)
+        st = self._lib.pkd_plan_cascade(self._h, _ptr(gi), n_groups, *[_ptr(x) for x in p],
+                                        *[_ptr(x) for x in q], _stream_ptr(stream),
+                                        self._ep_ref)
+        if st:
+            _check(st, "pkd_plan_cascade")
+        self.epoch = self._ep.value
+        self.batch = int(q[2].shape[0])
         return self.epoch
 
     def plan_info(self):

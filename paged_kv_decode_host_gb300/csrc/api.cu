@@ -23,6 +23,7 @@ using namespace pkd;
 struct KvMapEntry {
   const void* kv = nullptr;
   CUtensorMap map{};
+  CUtensorMap map_dense{};   // cascade contexts: the dense role's per-head map too
 };
 
 struct pkd_ctx {
@@ -66,8 +67,12 @@ bool valid_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 bool valid_flags(uint32_t f) {
   const uint32_t known = PKD_FLAG_FMA_CONSUMER | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX |
                          PKD_FLAG_KV_FP8 | PKD_FLAG_ROW_COPIES | PKD_FLAG_CHUNK_SEARCH |
-                         PKD_FLAG_HND | PKD_FLAG_DENSE_PREFIX;
+                         PKD_FLAG_HND | PKD_FLAG_DENSE_PREFIX | PKD_FLAG_CASCADE;
   if (f & ~known) return false;
+  // a cascade context runs both of its levels itself: bf16 page tiles,
+  // tensor cores, either layout
+  if ((f & PKD_FLAG_CASCADE) && (f & ~(PKD_FLAG_CASCADE | PKD_FLAG_MMA_CONSUMER | PKD_FLAG_HND)))
+    return false;
   if ((f & PKD_FLAG_FMA_CONSUMER) &&
       (f & (PKD_FLAG_MMA_CONSUMER | PKD_FLAG_SHARED_PREFIX | PKD_FLAG_KV_FP8)))
     return false;
@@ -91,8 +96,8 @@ int check_config(const pkd_config* c) {
   if (c->num_qo_heads < 1 || c->num_qo_heads % c->num_kv_heads != 0)
     return PKD_E_UNSUPPORTED_SHAPE;
   if (!valid_group(c->num_qo_heads / c->num_kv_heads)) return PKD_E_UNSUPPORTED_SHAPE;
-  // the dense-prefix kernel reads 16-token page tiles
-  if ((c->flags & PKD_FLAG_DENSE_PREFIX) && c->page_size % 16 != 0)
+  // the dense-prefix kernel (and the cascade kernel) read 16-token page tiles
+  if ((c->flags & (PKD_FLAG_DENSE_PREFIX | PKD_FLAG_CASCADE)) && c->page_size % 16 != 0)
     return PKD_E_UNSUPPORTED_SHAPE;
   // a page must fit the copy-size and tx-count limits of one stage
   if ((int64_t)c->page_size * c->num_kv_heads * kHeadDim * 2 * 2 > (int64_t)1 << 30)
@@ -113,10 +118,15 @@ DecodeKind kind_for(const pkd_config* c, const void* probe_address) {
   k.fp8 = (c->flags & PKD_FLAG_KV_FP8) != 0;
   k.tmap = k.mma && c->page_size % 16 == 0 && !(c->flags & PKD_FLAG_ROW_COPIES);
   k.dense = (c->flags & PKD_FLAG_DENSE_PREFIX) != 0;
+  k.cascade = (c->flags & PKD_FLAG_CASCADE) != 0;
   if (k.tmap && probe_address != nullptr) {
     CUtensorMap m;
+    const bool hnd = (c->flags & PKD_FLAG_HND) != 0;
     k.tmap = encode_kv_map(probe_address, c->num_pages, c->page_size, c->num_kv_heads, k.fp8,
-                           (c->flags & PKD_FLAG_HND) != 0, k.dense, &m) == cudaSuccess;
+                           hnd, k.dense, &m) == cudaSuccess;
+    if (k.cascade)   // the cascade kernel needs the dense role's map too
+      k.tmap = k.tmap && encode_kv_map(probe_address, c->num_pages, c->page_size,
+                                       c->num_kv_heads, false, hnd, true, &m) == cudaSuccess;
   }
   return k;
 }
@@ -141,18 +151,24 @@ int resolve_ctas(const pkd_config* c, const DecodeKind& k, int32_t* n_cta, int* 
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-// The page-tile map of the cache at kv (cached per address).
-int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out) {
+// The page-tile map(s) of the cache at kv (cached per address).
+int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out, CUtensorMap* out_dense = nullptr) {
   for (const KvMapEntry& e : ctx->kv_maps)
     if (e.kv == kv) {
       *out = e.map;
+      if (out_dense) *out_dense = e.map_dense;
       return PKD_OK;
     }
   KvMapEntry e;
   e.kv = kv;
   const pkd_config& c = ctx->cfg;
-  if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8,
-                    (c.flags & PKD_FLAG_HND) != 0, ctx->kind.dense, &e.map) != cudaSuccess)
+  const bool hnd = (c.flags & PKD_FLAG_HND) != 0;
+  if (encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, ctx->kind.fp8, hnd,
+                    ctx->kind.dense, &e.map) != cudaSuccess)
+    return PKD_E_CUDA;
+  if (ctx->kind.cascade &&
+      encode_kv_map(kv, c.num_pages, c.page_size, c.num_kv_heads, false, hnd, true,
+                    &e.map_dense) != cudaSuccess)
     return PKD_E_CUDA;
   constexpr size_t kMaxMaps = 128;
   if (ctx->kv_maps.size() < kMaxMaps) {
@@ -162,6 +178,7 @@ int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out) {
     ctx->next_map = (ctx->next_map + 1) % kMaxMaps;
   }
   *out = e.map;
+  if (out_dense) *out_dense = e.map_dense;
   return PKD_OK;
 }
 
@@ -183,6 +200,7 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   a.off_cta = ctx->layout.cta_indptr;
   a.off_items = ctx->layout.items;
   a.off_pages = ctx->layout.page_list;
+  a.off_merge = ctx->layout.merge_indptr;
   a.hq = c.num_qo_heads;
   a.hkv = c.num_kv_heads;
   a.page_size = c.page_size;
@@ -193,18 +211,30 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   // are adjacent (one copy moves both)
   a.hnd = ((c.flags & PKD_FLAG_HND) && c.page_size > 1) ? 1 : 0;
   a.kv_merged = (c.page_size == 1 && !ctx->kind.tmap) ? 1 : 0;
+  CascadeArgs ca{};
   if (ctx->kind.tmap && kv != nullptr) {
-    const int st = kv_map_for(ctx, kv, &a.kv_map);
+    const int st = kv_map_for(ctx, kv, &a.kv_map, ctx->kind.cascade ? &ca.pre.kv_map : nullptr);
     if (st != PKD_OK) return st;
   }
-  if (ctx->kind.dense && ctx->info.batch > 0 &&
+  if ((ctx->kind.dense || ctx->kind.cascade) && ctx->info.batch > 0 &&
       encode_q_map(q, ctx->info.batch, c.num_qo_heads, c.num_kv_heads, &a.q_map) != cudaSuccess)
     return PKD_E_CUDA;
   if (ev_before && cudaEventRecordWithFlags(ev_before, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
-  if (launch_decode(ctx->kind, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
-      cudaSuccess)
+  if (ctx->kind.cascade) {
+    // the suffix role: a's all-heads map; the prefix role: the same
+    // arguments with the dense per-head map (and a's query map)
+    const CUtensorMap dense_map = ca.pre.kv_map;
+    ca.suf = a;
+    ca.pre = a;
+    ca.pre.kv_map = dense_map;
+    if (launch_cascade(ctx->kind, ca, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
+        cudaSuccess)
+      return PKD_E_CUDA;
+  } else if (launch_decode(ctx->kind, a, ctx->n_cta, c.num_kv_heads, ctx->smem_bytes, stream) !=
+             cudaSuccess) {
     return PKD_E_CUDA;
+  }
   if (ev_after && cudaEventRecordWithFlags(ev_after, stream, cudaEventRecordExternal) != cudaSuccess)
     return PKD_E_CUDA;
   MergeArgs m{};
@@ -274,12 +304,28 @@ int pkd_plan_host_shared(const pkd_config* cfg, const int32_t* group_indptr, int
                                last_page_len, host_words, info);
 }
 
+int pkd_plan_host_cascade(const pkd_config* cfg, const int32_t* group_indptr,
+                          int32_t num_groups, const int32_t* p_indptr, const int32_t* p_indices,
+                          const int32_t* p_last, const int32_t* s_indptr,
+                          const int32_t* s_indices, const int32_t* s_last, int32_t* host_words,
+                          size_t max_words, pkd_plan_info* info) {
+  int st = check_config(cfg);
+  if (st != PKD_OK) return st;
+  if (cfg->num_ctas < 2 || host_words == nullptr || !(cfg->flags & PKD_FLAG_CASCADE))
+    return PKD_E_INVALID_ARG;
+  Layout L = make_layout(*cfg, cfg->num_ctas);
+  if (max_words < (size_t)L.words) return PKD_E_INVALID_ARG;
+  return plan_schedule_cascade(*cfg, cfg->num_ctas, L, group_indptr, num_groups, p_indptr,
+                               p_indices, p_last, s_indptr, s_indices, s_last, host_words, info);
+}
+
 int pkd_plan_host(const pkd_config* cfg, const int32_t* indptr, const int32_t* indices,
                   const int32_t* last_page_len, int32_t batch, int32_t* host_words,
                   size_t max_words, pkd_plan_info* info) {
   int st = check_config(cfg);
   if (st != PKD_OK) return st;
-  if (cfg->num_ctas < 1 || host_words == nullptr) return PKD_E_INVALID_ARG;
+  if (cfg->num_ctas < 1 || host_words == nullptr || (cfg->flags & PKD_FLAG_CASCADE))
+    return PKD_E_INVALID_ARG;
   Layout L = make_layout(*cfg, cfg->num_ctas);
   if (max_words < (size_t)L.words) return PKD_E_INVALID_ARG;
   return plan_schedule(*cfg, cfg->num_ctas, L, indptr, indices, last_page_len, batch,
@@ -306,7 +352,7 @@ int pkd_create(const pkd_config* cfg, void* d_workspace, size_t workspace_bytes,
   if (!ctx) return PKD_E_INVALID_ARG;
   ctx->cfg = *cfg;
   ctx->kind = kind_for(cfg, d_workspace);
-  if (ctx->kind.dense && !ctx->kind.tmap) {   // the driver refused the page-tile map
+  if ((ctx->kind.dense || ctx->kind.cascade) && !ctx->kind.tmap) {   // the driver refused a map
     delete ctx;
     return PKD_E_UNSUPPORTED_SHAPE;
   }
@@ -363,10 +409,12 @@ void pkd_destroy(pkd_ctx* ctx) {
   delete ctx;
 }
 
-// Plan (grouped or not) into the next staging buffer and publish it.
-static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n_rows,
-                            const int32_t* indptr, const int32_t* indices,
-                            const int32_t* last_page_len, void* stream, uint64_t* epoch) {
+}  // extern "C"
+
+// Plan into the next staging buffer (plan_fn(words, info) runs the planner)
+// and publish it.
+template <typename PlanFn>
+static int plan_and_publish(pkd_ctx* ctx, PlanFn plan_fn, void* stream, uint64_t* epoch) {
   if (ctx == nullptr) return PKD_E_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int k = ctx->next_staging;
@@ -376,8 +424,7 @@ static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n
   }
   int32_t* words = ctx->staging[k];
   pkd_plan_info info{};
-  int st = plan_schedule_grouped(ctx->cfg, ctx->n_cta, ctx->layout, group_indptr, n_rows,
-                                 indptr, indices, last_page_len, words, &info);
+  int st = plan_fn(words, &info);
   if (st != PKD_OK) return st;
   const Layout& L = ctx->layout;
   // one copy: the fixed-size part (header, cta queues, items, units, merge
@@ -396,9 +443,18 @@ static int plan_and_publish(pkd_ctx* ctx, const int32_t* group_indptr, int32_t n
   return PKD_OK;
 }
 
+extern "C" {
+
 int pkd_plan(pkd_ctx* ctx, const int32_t* indptr, const int32_t* indices,
              const int32_t* last_page_len, int32_t batch, void* stream, uint64_t* epoch) {
-  return plan_and_publish(ctx, nullptr, batch, indptr, indices, last_page_len, stream, epoch);
+  if (ctx == nullptr || ctx->kind.cascade) return PKD_E_INVALID_ARG;
+  return plan_and_publish(
+      ctx,
+      [&](int32_t* words, pkd_plan_info* info) {
+        return plan_schedule_grouped(ctx->cfg, ctx->n_cta, ctx->layout, nullptr, batch, indptr,
+                                     indices, last_page_len, words, info);
+      },
+      stream, epoch);
 }
 
 int pkd_plan_shared(pkd_ctx* ctx, const int32_t* group_indptr, int32_t num_groups,
@@ -406,8 +462,28 @@ int pkd_plan_shared(pkd_ctx* ctx, const int32_t* group_indptr, int32_t num_group
                     void* stream, uint64_t* epoch) {
   if (ctx == nullptr || !ctx->kind.block) return PKD_E_INVALID_ARG;
   if (num_groups > 0 && group_indptr == nullptr) return PKD_E_INVALID_ARG;
-  return plan_and_publish(ctx, group_indptr, num_groups, indptr, indices, last_page_len, stream,
-                          epoch);
+  return plan_and_publish(
+      ctx,
+      [&](int32_t* words, pkd_plan_info* info) {
+        return plan_schedule_grouped(ctx->cfg, ctx->n_cta, ctx->layout, group_indptr, num_groups,
+                                     indptr, indices, last_page_len, words, info);
+      },
+      stream, epoch);
+}
+
+int pkd_plan_cascade(pkd_ctx* ctx, const int32_t* group_indptr, int32_t num_groups,
+                     const int32_t* p_indptr, const int32_t* p_indices, const int32_t* p_last,
+                     const int32_t* s_indptr, const int32_t* s_indices, const int32_t* s_last,
+                     void* stream, uint64_t* epoch) {
+  if (ctx == nullptr || !ctx->kind.cascade) return PKD_E_INVALID_ARG;
+  return plan_and_publish(
+      ctx,
+      [&](int32_t* words, pkd_plan_info* info) {
+        return plan_schedule_cascade(ctx->cfg, ctx->n_cta, ctx->layout, group_indptr, num_groups,
+                                     p_indptr, p_indices, p_last, s_indptr, s_indices, s_last,
+                                     words, info);
+      },
+      stream, epoch);
 }
 
 int pkd_get_plan_info(const pkd_ctx* ctx, pkd_plan_info* info) {
@@ -682,8 +758,10 @@ int pkd_graph_capture_io(pkd_ctx* ctx, int32_t layers, const void* const* q,
 
 int pkd_graph_launch(pkd_graph* g, void* stream) {
   if (g == nullptr || g->exec == nullptr) return PKD_E_INVALID_ARG;
-  // a dense-prefix graph's query maps cover the batch it was captured with
-  if (g->ctx->kind.dense && g->ctx->info.batch != g->batch) return PKD_E_STALE_PLAN;
+  // a dense-prefix (or cascade) graph's query maps cover the batch it was
+  // captured with
+  if ((g->ctx->kind.dense || g->ctx->kind.cascade) && g->ctx->info.batch != g->batch)
+    return PKD_E_STALE_PLAN;
   if (cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKD_E_CUDA;
   return PKD_OK;

@@ -52,6 +52,7 @@
 #include <mutex>
 
 #include "pkd_internal.h"
+#include "prefix_tc_body.cuh"
 #include "sm103_ptx.cuh"
 
 namespace pkd {
@@ -1181,10 +1182,11 @@ __host__ __device__ __forceinline__ int stage_bytes_for(int row_bytes, int token
   return 2 * tokens * (tiles ? row_bytes : row_stride(row_bytes));
 }
 
+// The decode role over the dynamic shared memory at `smem`: the whole
+// decode kernel, and the suffix CTAs of the cascade kernel.  Warps past the
+// producer (a fused launch may have more) do nothing.
 template <int G, bool kMma, bool kBlock, bool kFp8, bool kTiles>
-__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
-    decode_kernel(const __grid_constant__ DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void decode_body(const DecodeArgs& a, uint8_t* smem) {
   constexpr int kStageTokens = kFp8 ? kFp8Tokens : kTS;
   constexpr int kRing = ring_depth(kMma, kBlock, kFp8);
   const int stage_bytes = stage_bytes_for(a.row_bytes, kStageTokens, kTiles);
@@ -1251,6 +1253,30 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
   }
 }
 
+template <int G, bool kMma, bool kBlock, bool kFp8, bool kTiles>
+__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
+    decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  decode_body<G, kMma, kBlock, kFp8, kTiles>(a, smem);
+}
+
+// Cascade kernel (plans made by pkd_plan_cascade): CTAs [0, n_pre) run the
+// shared-prefix level's items with the dense tensor-core role, the others
+// the suffix level's items with the decode role (tensor-core consumer, page
+// tiles), side by side in one launch; both write partial states only.  The
+// split n_pre is read from the schedule header, so a captured launch follows
+// each new plan.  Roles keep their own shared-memory layouts inside the
+// launch's (the larger of the two) and their own programmatic-launch rules.
+template <int G>
+__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
+    cascade_kernel(const __grid_constant__ CascadeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];   // each role aligns its own layout
+  if ((int)blockIdx.x < a.pre.sched[H_NPRE])
+    tc::prefix_tc_body<true>(a.pre, smem);
+  else
+    decode_body<G, true, false, false, true>(a.suf, smem);
+}
+
 template <int G, bool kTiles>
 const void* kernel_ptr(const DecodeKind& k) {
   if (k.fp8) return reinterpret_cast<const void*>(&decode_kernel<G, true, false, true, kTiles>);
@@ -1265,7 +1291,18 @@ const void* kernel_ptr_g(const DecodeKind& k) {
   return k.tmap ? kernel_ptr<G, true>(k) : kernel_ptr<G, false>(k);
 }
 
+const void* cascade_ptr(int group) {
+  switch (group) {
+    case 1: return reinterpret_cast<const void*>(&cascade_kernel<1>);
+    case 2: return reinterpret_cast<const void*>(&cascade_kernel<2>);
+    case 4: return reinterpret_cast<const void*>(&cascade_kernel<4>);
+    case 8: return reinterpret_cast<const void*>(&cascade_kernel<8>);
+    default: return nullptr;
+  }
+}
+
 const void* kernel_for(const DecodeKind& k) {
+  if (k.cascade) return (k.mma && k.tmap && !k.fp8 && !k.block) ? cascade_ptr(k.group) : nullptr;
   if (k.dense) return prefix_tc_kernel_ptr();
   if ((k.block || k.fp8) && !k.mma) return nullptr;
   if (k.block && k.fp8) return nullptr;
@@ -1281,6 +1318,7 @@ const void* kernel_for(const DecodeKind& k) {
 }  // namespace
 
 int decode_threads(int hkv, const DecodeKind& k) {
+  if (k.cascade) return (hkv + 1 > 8 ? hkv + 1 : 8) * 32;   // decode role, or the 8 dense roles
   return k.dense ? prefix_tc_threads() : (hkv + 1) * 32;
 }
 
@@ -1292,6 +1330,12 @@ bool use_mma_consumer(int group, uint32_t flags) {
 }
 
 int decode_smem_bytes(int hkv, const DecodeKind& k) {
+  if (k.cascade) {
+    DecodeKind d = k;
+    d.cascade = false;
+    const int dec = decode_smem_bytes(hkv, d);
+    return dec > tc::smem_bytes() ? dec : tc::smem_bytes();
+  }
   if (k.dense) return prefix_tc_smem_bytes();
   const int row = hkv * kHeadDim * (k.fp8 ? 1 : 2);
   const int tokens = k.fp8 ? kFp8Tokens : kTS;
@@ -1315,6 +1359,24 @@ cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* 
   if (!f) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, decode_threads(hkv, k),
                                                        (size_t)smem_bytes);
+}
+
+cudaError_t launch_cascade(const DecodeKind& k, const CascadeArgs& a, int grid, int hkv,
+                           int smem_bytes, cudaStream_t stream) {
+  const void* f = kernel_for(k);
+  if (!f || !k.cascade) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(decode_threads(hkv, k));
+  cfg.dynamicSmemBytes = (size_t)smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<CascadeArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, int hkv,

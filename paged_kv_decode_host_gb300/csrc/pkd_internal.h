@@ -54,16 +54,21 @@ constexpr int kDenseRows = 128;   // query rows of one dense-prefix tile
 // in suffix-token units: a suffix item costs alpha + tokens (every KV head of
 // a token: 4 KB of K and V at Hkv 8), a prefix item (one KV head of a block
 // of up to 128 query rows) costs (kCascadePrefixAlpha + tokens) *
-// kCascadePrefixCost16 / 16.  Measured: a 128-token round of the dense role
-// takes about 1 us, a decode CTA streams a token of all 8 heads in about
-// 70-90 ns, so a prefix token of one head costs about an eighth of a suffix
-// token.  The suffix chunk floor is lower than a plain plan's, since the
-// suffix level gets only part of the grid.
+// kCascadePrefixCost16 / 16.  Measured on the 8,192-token prefix x 32
+// requests step, with both roles streaming at once (HBM saturated, about
+// 2.4 us per memory round trip): a dense CTA takes about 5 us from launch to
+// its first scores and about 2.5 us per 128-token round after that, a
+// decode CTA about 65 ns per token of all 8 heads -- a prefix token of one
+// head costs about a quarter of a suffix token, and a prefix item carries
+// about 256 prefix tokens' worth of fixed cost.  Split by these, both roles
+// end within a microsecond of each other (per-CTA clock stamps).  The suffix
+// chunk floor is lower than a plain plan's, since the suffix level gets only
+// part of the grid.
 #ifndef PKD_CASCADE_PREFIX_COST16
-#define PKD_CASCADE_PREFIX_COST16 2
+#define PKD_CASCADE_PREFIX_COST16 4
 #endif
 #ifndef PKD_CASCADE_PREFIX_ALPHA
-#define PKD_CASCADE_PREFIX_ALPHA 128
+#define PKD_CASCADE_PREFIX_ALPHA 256
 #endif
 #ifndef PKD_CASCADE_SUFFIX_FLOOR
 #define PKD_CASCADE_SUFFIX_FLOOR 128
@@ -158,6 +163,7 @@ struct DecodeArgs {
   float* lse;                // fp32 [B][Hq] or null
   int64_t page_bytes;        // 2 * P * row_bytes
   int64_t off_cta, off_items, off_pages;
+  int64_t off_merge;         // merge_indptr (cascade prefix items take their slots from it)
   int32_t hq, hkv, page_size, num_pages;
   int32_t row_bytes;         // Hkv * D * element bytes: one token of one page, all heads
   float scale_log2;          // k_scale * log2(e) / sqrt(D)
@@ -173,6 +179,13 @@ struct DecodeArgs {
   // group, KV head, request}; its box is one KV head's 128 query rows of a
   // block (128 / g requests x g heads) and one 128-byte half.
   CUtensorMap q_map;
+};
+
+// The cascade kernel's arguments: the shared-prefix role's (dense tile maps)
+// and the suffix role's (all-heads page-tile map), over one schedule.
+struct CascadeArgs {
+  DecodeArgs pre;
+  DecodeArgs suf;
 };
 
 struct MergeArgs {
@@ -195,6 +208,7 @@ struct DecodeKind {
   bool tmap = false;   // page-tile producer: one tensor-map copy per 16 tokens of K or V
                        // (P % 16 == 0, tensor-core consumers); else one copy per token row
   bool dense = false;  // dense shared-prefix kernel (tcgen05, one KV head per item)
+  bool cascade = false;  // cascade kernel: dense prefix role + decode role (page tiles)
 };
 int decode_smem_bytes(int hkv, const DecodeKind& k);
 int decode_threads(int hkv, const DecodeKind& k);
@@ -206,6 +220,8 @@ cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes);
 cudaError_t decode_occupancy(const DecodeKind& k, int hkv, int smem_bytes, int* blocks_per_sm);
 cudaError_t launch_decode(const DecodeKind& k, const DecodeArgs& a, int grid, int hkv,
                           int smem_bytes, cudaStream_t stream);
+cudaError_t launch_cascade(const DecodeKind& k, const CascadeArgs& a, int grid, int hkv,
+                           int smem_bytes, cudaStream_t stream);
 // Encode the page-tile map of a cache at `kv` (16-byte aligned) into `map`.
 // A box is 16 tokens of all KV heads (the decode kernel) or, with
 // head_half_box, 16 tokens of one 128-byte half of one KV head (the dense

@@ -420,4 +420,369 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   return PKD_OK;
 }
 
+// ---------------------------------------------------------------- cascade
+//
+// One decode step with a shared-prefix level and a suffix level, planned
+// together ("FlashInfer, in depth", "Cascades, Merges, and the Autotuner":
+// attention once per level, then a merge; "FlashInfer 完全拆解", Composable
+// Format and 先切长 KV，再做最长任务优先分配).  The grid is cut in two: CTAs
+// [0, n_pre) take the prefix items -- over units (block of up to R requests
+// of a group, KV head) as in a dense-prefix plan -- and CTAs [n_pre, n_cta)
+// the suffix items -- over units (request), all KV heads, as in a plain
+// plan, with the closed-form chunk of the suffix level's own work bound (and
+// its half) and LPT on its own CTAs.
+//
+// The prefix level gives every CTA at most one item (a dense CTA's second
+// item waits for its query tile and its first item's epilogue, which costs
+// more than a longer first item): with a budget of n CTAs, every block
+// starts with one chunk per KV head, and while Hkv more CTAs are left the
+// block whose chunk is longest (ties: the first block) gets one more chunk
+// per head -- every head of a block keeps the same chunks, so a request's
+// prefix slots hold all its heads -- unless that would cut it below the
+// floor.  Chunks are page-rounded (a block may end up with fewer than its
+// share); item j goes to CTA j and unused budget goes to the suffix level.
+// When the blocks' heads outnumber the grid, the prefix units are not split
+// and LPT places them on the n_pre CTAs instead.
+//
+// n_pre balances the two levels' predicted makespans in one cost unit
+// (suffix tokens: kCascadePrefixCost16): starting from the budget that gives
+// each level CTAs in proportion to its total cost (in steps of Hkv when
+// every head can have a CTA, rounded to the nearest step), it climbs to
+// neighbouring budgets (the lower one first) while the predicted makespan
+// falls strictly.  Every item writes a partial state: request r's slots are
+// merge_indptr[r] .. merge_indptr[r + 1], its prefix chunks first, then its
+// suffix chunks, and one merge folds them.  Prefix items mark themselves with
+// slot stride -1 and carry their chunk index as dst_slot (a block's requests
+// have different slot bases); suffix items carry their slot.
+namespace {
+
+struct LevelPlan {
+  int64_t chunk = 0, span = 0;
+  std::vector<Item> items;
+  std::vector<int32_t> owner;
+  std::vector<int64_t> block_chunk;   // prefix level: the chunk of each block
+  int32_t ctas = 0;                   // prefix level: CTAs its items use
+};
+
+// Closed-form chunk candidates (the work bound over n CTAs, and its half),
+// page-rounded and not below floor_c; the smaller predicted makespan wins
+// (ties: the larger chunk).  A candidate whose makespan lower bound (its
+// costliest item, or its total cost spread evenly) cannot beat the best so
+// far is not scheduled.
+void plan_level(const std::vector<int64_t>& ulens, int64_t total, int32_t n, int64_t P,
+                int64_t floor_c, int64_t alpha, Scratch& sc, LevelPlan* out) {
+  out->chunk = -1;
+  const int64_t bound = ceil_div(total, n);
+  int64_t prev = -1;
+  for (int64_t k : {1, 2}) {
+    const int64_t c = std::max(ceil_div(ceil_div(bound, k), P) * P, floor_c);
+    if (c == prev) continue;
+    prev = c;
+    if (out->chunk >= 0) {
+      int64_t n_it = 0, top = 0;
+      for (int64_t l : ulens) {
+        n_it += ceil_div(l, c);
+        top = std::max(top, std::min(l, c));
+      }
+      if (std::max(alpha + top, ceil_div(total + alpha * n_it, n)) >= out->span) continue;
+    }
+    split_sorted(ulens, c, alpha, &sc.whole, &sc.rest, &sc.items);
+    const int64_t span = lpt(sc.items, n, &sc.owner, &sc.heap);
+    if (out->chunk < 0 || span < out->span) {
+      out->chunk = c;
+      out->span = span;
+      out->items.swap(sc.items);
+      out->owner.swap(sc.owner);
+    }
+  }
+}
+
+// The prefix level of a cascade plan on a budget of n CTAs (see above).
+// block_len: each block's prefix length; units = blocks x hkv.
+void plan_prefix(const std::vector<int64_t>& block_len, int32_t hkv, int32_t n, int64_t P,
+                 int64_t floor_c, int64_t alpha, Scratch& sc, LevelPlan* out) {
+  const int32_t n_blocks = (int32_t)block_len.size();
+  out->items.clear();
+  out->owner.clear();
+  out->block_chunk.assign((size_t)n_blocks, 0);
+  out->span = 0;
+  if ((int64_t)n_blocks * hkv > n) {
+    // unsplit (block, head) units by LPT
+    sc.unit_lens.clear();
+    for (int64_t l : block_len)
+      for (int32_t h = 0; h < hkv; ++h) sc.unit_lens.push_back(l);
+    int64_t top = 0;
+    for (int64_t l : block_len) top = std::max(top, l);
+    split_sorted(sc.unit_lens, std::max<int64_t>(top, 1), alpha, &sc.whole, &sc.rest,
+                 &out->items);
+    out->span = lpt(out->items, n, &out->owner, &sc.heap);
+    for (int32_t b = 0; b < n_blocks; ++b) out->block_chunk[b] = std::max<int64_t>(top, 1);
+    out->ctas = n;
+    return;
+  }
+  std::vector<int32_t>& m = sc.n_chunks;
+  m.assign((size_t)n_blocks, 1);
+  for (int32_t b = 0; b < n_blocks; ++b) out->block_chunk[b] = ceil_div(block_len[b], P) * P;
+  for (int64_t budget = n - (int64_t)n_blocks * hkv; budget >= hkv; budget -= hkv) {
+    int32_t top = 0;
+    for (int32_t b = 1; b < n_blocks; ++b)
+      if (out->block_chunk[b] > out->block_chunk[top]) top = b;
+    const int64_t next = ceil_div(ceil_div(block_len[top], m[top] + 1), P) * P;
+    if (next < floor_c) break;
+    m[top] += 1;
+    out->block_chunk[top] = next;
+  }
+  for (int32_t b = 0; b < n_blocks; ++b) {
+    const int64_t c = out->block_chunk[b];
+    for (int32_t h = 0; h < hkv; ++h) {
+      int32_t k = 0;
+      for (int64_t t = 0; t < block_len[b]; t += c, ++k) {
+        const int64_t e = std::min(t + c, block_len[b]);
+        out->owner.push_back((int32_t)out->items.size());
+        out->items.push_back(Item{alpha + (e - t), b * hkv + h, k, (int32_t)t, (int32_t)e});
+        out->span = std::max(out->span, alpha + (e - t));
+      }
+    }
+  }
+  out->ctas = (int32_t)out->items.size();
+}
+
+// Table rows of one level: validate and return the lengths.
+int row_lengths(const int32_t* indptr, const int32_t* last, int32_t rows, int64_t P,
+                std::vector<int64_t>* len) {
+  len->resize((size_t)rows);
+  if (rows == 0) return PKD_OK;
+  if (indptr == nullptr || last == nullptr) return PKD_E_INVALID_ARG;
+  if (indptr[0] != 0) return PKD_E_BAD_TABLE;
+  for (int32_t i = 0; i < rows; ++i) {
+    const int64_t n = (int64_t)indptr[i + 1] - indptr[i];
+    if (n < 1 || last[i] < 1 || last[i] > P) return PKD_E_BAD_TABLE;
+    (*len)[i] = P * (n - 1) + last[i];
+    if ((*len)[i] > 0x7fffffffLL) return PKD_E_CAPACITY;
+  }
+  return PKD_OK;
+}
+
+struct CascadeScratch {
+  std::vector<int64_t> pre_row, suf_len, block_len;
+  std::vector<Block> blocks;
+  std::vector<int32_t> block_of, np_block, ns_req, count, fill;
+  LevelPlan pre, suf, best_pre, best_suf;
+};
+
+}  // namespace
+
+int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                          const int32_t* group_indptr, int32_t n_groups,
+                          const int32_t* p_indptr, const int32_t* p_indices,
+                          const int32_t* p_last, const int32_t* s_indptr,
+                          const int32_t* s_indices, const int32_t* s_last, int32_t* words,
+                          pkd_plan_info* info) {
+  if (n_groups < 0 || n_cta < 2 || words == nullptr) return PKD_E_INVALID_ARG;
+  if (n_groups > 0 && group_indptr == nullptr) return PKD_E_INVALID_ARG;
+  const int64_t P = cfg.page_size;
+  const int32_t R = block_rows(cfg);
+  const int32_t hkv = cfg.num_kv_heads;
+  thread_local Scratch sc;
+  thread_local CascadeScratch cs;
+
+  // ---- requests, groups, both tables
+  int32_t batch = 0;
+  if (n_groups > 0) {
+    if (group_indptr[0] != 0) return PKD_E_BAD_TABLE;
+    for (int32_t j = 0; j < n_groups; ++j)
+      if (group_indptr[j + 1] <= group_indptr[j]) return PKD_E_BAD_TABLE;
+    batch = group_indptr[n_groups];
+  }
+  if (batch > cfg.max_batch) return PKD_E_CAPACITY;
+  int st = row_lengths(p_indptr, p_last, n_groups, P, &cs.pre_row);
+  if (st != PKD_OK) return st;
+  st = row_lengths(s_indptr, s_last, batch, P, &cs.suf_len);
+  if (st != PKD_OK) return st;
+  const int64_t nnz_p = n_groups > 0 ? p_indptr[n_groups] : 0;
+  const int64_t nnz_s = batch > 0 ? s_indptr[batch] : 0;
+  if (nnz_p + nnz_s > cfg.max_num_pages) return PKD_E_CAPACITY;
+  if ((nnz_p > 0 && p_indices == nullptr) || (nnz_s > 0 && s_indices == nullptr))
+    return PKD_E_INVALID_ARG;
+  // page list: the prefix table's indices, then the suffix table's
+  if (!copy_checked(p_indices, words + L.page_list, nnz_p, cfg.num_pages) ||
+      !copy_checked(s_indices, words + L.page_list + nnz_p, nnz_s, cfg.num_pages))
+    return PKD_E_BAD_TABLE;
+
+  // ---- prefix blocks (units: block x KV head) and the levels' total costs
+  cs.blocks.clear();
+  cs.block_len.clear();
+  cs.block_of.assign((size_t)batch, 0);
+  int64_t pre_cost = 0;
+  for (int32_t j = 0; j < n_groups; ++j)
+    for (int32_t r = group_indptr[j]; r < group_indptr[j + 1]; r += R) {
+      const int32_t n = std::min(R, group_indptr[j + 1] - r);
+      for (int32_t i = 0; i < n; ++i) cs.block_of[r + i] = (int32_t)cs.blocks.size();
+      cs.blocks.push_back(Block{r, n, j});
+      cs.block_len.push_back(cs.pre_row[j]);
+      pre_cost += hkv * (kCascadePrefixAlpha + cs.pre_row[j]) * kCascadePrefixCost16;
+    }
+  const int64_t alpha = cfg.alpha < 0 ? kDefaultAlpha : cfg.alpha;
+  int64_t suf_total = 0, suf_cost = 0;
+  for (int64_t l : cs.suf_len) {
+    suf_total += l;
+    suf_cost += (alpha + l) * 16;
+  }
+  const int64_t floor_s = ceil_div(
+      std::max<int64_t>(cfg.min_chunk_tokens < 0 ? kCascadeSuffixFloor : cfg.min_chunk_tokens, 1),
+      P) * P;
+  const int64_t floor_p = ceil_div(kCascadePrefixFloor, P) * P;
+
+  // ---- the CTA split (see above)
+  int32_t n_pre = 0;
+  int64_t best_span = 0;
+  if (batch > 0) {
+    const int64_t units = (int64_t)cs.blocks.size() * hkv;
+    // budgets: units + step * j when every head can have a CTA, else 1 .. n_cta - 1
+    const bool split = units <= n_cta - 1;
+    const int64_t base = split ? units : 1, step = split ? hkv : 1;
+    const int64_t j_max = (n_cta - 1 - base) / step;
+    const int64_t all = pre_cost + suf_cost;
+    const int64_t prop = (n_cta * pre_cost + all / 2) / all;
+    const int64_t j0 = std::min<int64_t>(
+        std::max<int64_t>((std::max<int64_t>(prop - base, 0) + step / 2) / step, 0), j_max);
+    int64_t best_j = -1;
+    auto evaluate = [&](int64_t j) {
+      plan_prefix(cs.block_len, hkv, (int32_t)(base + step * j), P, floor_p, kCascadePrefixAlpha,
+                  sc, &cs.pre);
+      plan_level(cs.suf_len, suf_total, n_cta - cs.pre.ctas, P, floor_s, alpha, sc, &cs.suf);
+      const int64_t span = std::max(cs.pre.span * kCascadePrefixCost16, cs.suf.span * 16);
+      if (best_j < 0 || span < best_span) {
+        best_span = span;
+        best_j = j;
+        std::swap(cs.best_pre, cs.pre);
+        std::swap(cs.best_suf, cs.suf);
+      }
+    };
+    evaluate(j0);
+    int64_t lo_done = j0, hi_done = j0;   // budgets [lo_done, hi_done] scheduled
+    for (;;) {
+      const int64_t at = best_j;
+      if (at - 1 >= 0 && at - 1 < lo_done) {
+        evaluate(at - 1);
+        lo_done = at - 1;
+      }
+      if (at + 1 <= j_max && at + 1 > hi_done) {
+        evaluate(at + 1);
+        hi_done = at + 1;
+      }
+      if (best_j == at) break;
+    }
+    n_pre = cs.best_pre.ctas;
+  } else {
+    cs.best_pre = LevelPlan{};
+    cs.best_suf = LevelPlan{};
+  }
+  const LevelPlan& pre = cs.best_pre;
+  const LevelPlan& suf = cs.best_suf;
+  const int64_t n_items = (int64_t)pre.items.size() + (int64_t)suf.items.size();
+  if (n_items > L.max_items || batch > L.max_items) return PKD_E_CAPACITY;
+
+  // ---- reduction map: every request a unit, prefix chunks then suffix chunks
+  const int32_t n_blocks = (int32_t)cs.blocks.size();
+  cs.np_block.assign((size_t)n_blocks, 0);
+  int64_t max_pchunk = 0;
+  for (int32_t b = 0; b < n_blocks; ++b) {
+    cs.np_block[b] = (int32_t)ceil_div(cs.block_len[b], pre.block_chunk[b]);
+    max_pchunk = std::max(max_pchunk, std::min(pre.block_chunk[b], cs.block_len[b]));
+  }
+  cs.ns_req.assign((size_t)batch, 0);
+  int32_t* merge_indptr = words + L.merge_indptr;
+  int32_t* unit_words = words + L.units;
+  merge_indptr[0] = 0;
+  int32_t max_chunks = 0;
+  for (int32_t r = 0; r < batch; ++r) {
+    cs.ns_req[r] = (int32_t)ceil_div(cs.suf_len[r], suf.chunk);
+    const int32_t n = cs.np_block[cs.block_of[r]] + cs.ns_req[r];
+    unit_words[2 * r] = r;
+    unit_words[2 * r + 1] = n;
+    merge_indptr[r + 1] = merge_indptr[r] + n;
+    max_chunks = std::max(max_chunks, n);
+  }
+  const int64_t n_slots = batch > 0 ? merge_indptr[batch] : 0;
+  if (n_slots > L.max_slots) return PKD_E_CAPACITY;
+
+  // ---- queues: prefix items on CTAs [0, n_pre), suffix items after
+  cs.count.assign((size_t)n_cta, 0);
+  for (int32_t o : pre.owner) cs.count[o]++;
+  for (int32_t o : suf.owner) cs.count[n_pre + o]++;
+  int32_t* cta_indptr = words + L.cta_indptr;
+  cta_indptr[0] = 0;
+  for (int32_t c = 0; c < n_cta; ++c) cta_indptr[c + 1] = cta_indptr[c] + cs.count[c];
+  cs.fill.assign(cta_indptr, cta_indptr + n_cta);
+  int32_t* item_words = words + L.items;
+  for (size_t j = 0; j < pre.items.size(); ++j) {
+    const Item& it = pre.items[j];
+    const Block& bk = cs.blocks[it.req / hkv];
+    int32_t* w = item_words + (int64_t)cs.fill[pre.owner[j]]++ * kItemWords;
+    w[0] = bk.req_first;
+    w[1] = it.tok_begin;
+    w[2] = it.tok_end;
+    w[3] = it.chunk_idx;                       // slot of request r: merge_indptr[r] + chunk
+    w[4] = (int32_t)(p_indptr[bk.table_row] + it.tok_begin / P);
+    w[5] = bk.n_req;
+    w[6] = -1;                                 // cascade prefix item
+    w[7] = it.req % hkv;
+  }
+  for (size_t j = 0; j < suf.items.size(); ++j) {
+    const Item& it = suf.items[j];
+    const int32_t r = it.req;
+    int32_t* w = item_words + (int64_t)cs.fill[n_pre + suf.owner[j]]++ * kItemWords;
+    w[0] = r;
+    w[1] = it.tok_begin;
+    w[2] = it.tok_end;
+    w[3] = merge_indptr[r] + cs.np_block[cs.block_of[r]] + it.chunk_idx;
+    w[4] = (int32_t)(nnz_p + s_indptr[r] + it.tok_begin / P);
+    w[5] = 1;
+    w[6] = 0;
+    w[7] = 0;
+  }
+
+  int32_t* h = words;
+  std::memset(h, 0, sizeof(int32_t) * H_WORDS);
+  h[H_MAGIC] = kMagic;
+  h[H_BATCH] = batch;
+  h[H_HQ] = cfg.num_qo_heads;
+  h[H_HKV] = cfg.num_kv_heads;
+  h[H_D] = cfg.head_dim;
+  h[H_P] = cfg.page_size;
+  h[H_NCTA] = n_cta;
+  h[H_NITEMS] = (int32_t)n_items;
+  h[H_NUNITS] = batch;
+  h[H_NSLOTS] = (int32_t)n_slots;
+  h[H_CHUNK] = (int32_t)std::max<int64_t>(suf.chunk, 0);
+  h[H_ALPHA] = (int32_t)alpha;
+  h[H_NNZ] = (int32_t)(nnz_p + nnz_s);
+  h[H_MAKESPAN] = (int32_t)std::min<int64_t>(best_span / 16, 0x7fffffff);
+  h[H_MINCHUNK] = (int32_t)floor_s;
+  h[H_BLOCK] = R;
+  h[H_MAXCHUNKS] = max_chunks;
+  h[H_MAXBATCH] = cfg.max_batch;
+  h[H_MAXPAGES] = cfg.max_num_pages;
+  h[H_NPRE] = n_pre;
+  h[H_PCHUNK] = (int32_t)max_pchunk;
+
+  if (info) {
+    info->batch = batch;
+    info->num_ctas = n_cta;
+    info->chunk_tokens = h[H_CHUNK];
+    info->num_items = (int32_t)n_items;
+    info->num_units = batch;
+    info->num_slots = (int32_t)n_slots;
+    info->total_tokens = suf_total;
+    for (const Block& bk : cs.blocks) info->total_tokens += cs.pre_row[bk.table_row] * bk.n_req;
+    info->makespan = best_span / 16;
+    info->nnz = (int32_t)(nnz_p + nnz_s);
+    info->schedule_words = (int32_t)(L.page_list + nnz_p + nnz_s);
+    info->prefix_ctas = n_pre;
+    info->prefix_chunk_tokens = h[H_PCHUNK];
+  }
+  return PKD_OK;
+}
+
 }  // namespace pkd

@@ -1,11 +1,13 @@
 /* CPython fast path for the per-step planning calls of the Python binding:
- * pkd_plan and pkd_plan_shared with the page table passed as int32 arrays
+ * pkd_plan, pkd_plan_shared and pkd_plan_cascade with the page tables passed as int32 arrays
  * through the buffer protocol (no per-argument ctypes conversion).  It only
  * marshals arguments: the entry points are the C ABI's own, whose addresses
  * the binding hands over once (init), so this module does not link libpkd.
  *
  * plan(ctx, indptr, indices, last, stream) -> (status, epoch)
  * plan_shared(ctx, group_indptr, indptr, indices, last, stream) -> (status, epoch)
+ * plan_cascade(ctx, group_indptr, p_indptr, p_indices, p_last, s_indptr, s_indices, s_last,
+ *              stream) -> (status, epoch)
  *
  * status is the C ABI's return value, or NOT_HANDLED (1000) when an argument
  * is not a 1-D C-contiguous int32 buffer: the caller then takes its general
@@ -21,18 +23,26 @@ typedef int (*plan_shared_fn)(void *ctx, const int32_t *group_indptr, int32_t nu
                               const int32_t *indptr, const int32_t *indices,
                               const int32_t *last, void *stream, uint64_t *epoch);
 
+typedef int (*plan_cascade_fn)(void *ctx, const int32_t *group_indptr, int32_t num_groups,
+                               const int32_t *p_indptr, const int32_t *p_indices,
+                               const int32_t *p_last, const int32_t *s_indptr,
+                               const int32_t *s_indices, const int32_t *s_last, void *stream,
+                               uint64_t *epoch);
+
 static plan_fn g_plan = NULL;
 static plan_shared_fn g_plan_shared = NULL;
+static plan_cascade_fn g_plan_cascade = NULL;
 
 #define NOT_HANDLED 1000
 #define BAD_TABLE (-2)
 
 static PyObject *init(PyObject *self, PyObject *args) {
-  unsigned long long p, ps;
+  unsigned long long p, ps, pc = 0;
   (void)self;
-  if (!PyArg_ParseTuple(args, "KK", &p, &ps)) return NULL;
+  if (!PyArg_ParseTuple(args, "KK|K", &p, &ps, &pc)) return NULL;
   g_plan = (plan_fn)(uintptr_t)p;
   g_plan_shared = (plan_shared_fn)(uintptr_t)ps;
+  g_plan_cascade = (plan_cascade_fn)(uintptr_t)pc;
   Py_RETURN_NONE;
 }
 
@@ -115,8 +125,46 @@ static PyObject *plan_shared(PyObject *self, PyObject *args) {
   return Py_BuildValue("iK", st, (unsigned long long)epoch);
 }
 
+static PyObject *plan_cascade(PyObject *self, PyObject *args) {
+  unsigned long long ctx, stream;
+  PyObject *objs[7];
+  Py_buffer v[7];   /* group_indptr, prefix (indptr, indices, last), suffix (same) */
+  (void)self;
+  if (!PyArg_ParseTuple(args, "KOOOOOOOK", &ctx, &objs[0], &objs[1], &objs[2], &objs[3],
+                        &objs[4], &objs[5], &objs[6], &stream))
+    return NULL;
+  if (g_plan_cascade == NULL) return Py_BuildValue("iK", NOT_HANDLED, 0ULL);
+  for (int k = 0; k < 7; ++k) {
+    if (!get_i32(objs[k], &v[k])) {
+      for (int j = 0; j < k; ++j) PyBuffer_Release(&v[j]);
+      return Py_BuildValue("iK", NOT_HANDLED, 0ULL);
+    }
+  }
+  const Py_ssize_t groups = v[3].shape[0], batch = v[6].shape[0];
+  const int32_t *gi = (const int32_t *)v[0].buf;
+  int st;
+  uint64_t epoch = 0;
+  if (v[0].shape[0] != groups + 1 || v[1].shape[0] != groups + 1 || v[4].shape[0] != batch + 1 ||
+      groups > INT32_MAX || (groups > 0 && gi[groups] != batch) ||
+      (groups > 0 && v[2].shape[0] < ((const int32_t *)v[1].buf)[groups]) ||
+      (batch > 0 && v[5].shape[0] < ((const int32_t *)v[4].buf)[batch])) {
+    st = NOT_HANDLED;
+  } else {
+    st = g_plan_cascade((void *)(uintptr_t)ctx, gi, (int32_t)groups, (const int32_t *)v[1].buf,
+                        v[2].shape[0] ? (const int32_t *)v[2].buf : NULL,
+                        (const int32_t *)v[3].buf, (const int32_t *)v[4].buf,
+                        v[5].shape[0] ? (const int32_t *)v[5].buf : NULL,
+                        (const int32_t *)v[6].buf, (void *)(uintptr_t)stream, &epoch);
+  }
+  for (int k = 0; k < 7; ++k) PyBuffer_Release(&v[k]);
+  return Py_BuildValue("iK", st, (unsigned long long)epoch);
+}
+
 static PyMethodDef methods[] = {
-    {"init", init, METH_VARARGS, "init(plan_address, plan_shared_address)"},
+    {"plan_cascade", plan_cascade, METH_VARARGS,
+     "plan_cascade(ctx, group_indptr, p_indptr, p_indices, p_last, s_indptr, s_indices, "
+     "s_last, stream) -> (status, epoch)"},
+    {"init", init, METH_VARARGS, "init(plan_address, plan_shared_address[, plan_cascade_address])"},
     {"plan", plan, METH_VARARGS, "plan(ctx, indptr, indices, last, stream) -> (status, epoch)"},
     {"plan_shared", plan_shared, METH_VARARGS,
      "plan_shared(ctx, group_indptr, indptr, indices, last, stream) -> (status, epoch)"},

@@ -57,12 +57,13 @@ def test_config_validation(lib):
     ]
     for c in bad:
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -3
-    for bad_flags in (3, 5, 7, 9, 12, 28, 33 | 4 | 8, 128, 256, 0x80000000):
+    for bad_flags in (3, 5, 7, 9, 12, 28, 33 | 4 | 8, 128, 512, 256 | 1, 256 | 4, 256 | 8,
+                      256 | 16, 256 | 64, 256 | 128, 0x80000000):
         c = _cfg(16)
         c.flags = bad_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == -1
     for ok_flags in (0, 1, 2, 4, 6, 8, 10, 16, 17, 18, 20, 24, 32, 33, 36, 40, 56, 64, 65, 66,
-                     68, 72, 88, 120):
+                     68, 72, 88, 120, 256, 256 | 2, 256 | 32, 256 | 34):
         c = _cfg(16)
         c.flags = ok_flags
         assert lib.pkd_schedule_layout(ctypes.byref(c), off) == 0
@@ -292,10 +293,21 @@ def test_plan_fast_path_marshalling():
         ep[0] = 42
         return 0
 
+    vp = ctypes.c_void_p
+    cascade_t = ctypes.CFUNCTYPE(ctypes.c_int, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp,
+                                 ctypes.POINTER(ctypes.c_uint64))
+
+    def fake_cascade(ctx, gi, ng, pip, pix, pla, sip, six, sla, stream, ep):
+        calls.append(("cascade", ctx, gi, ng, pip, pix, pla, sip, six, sla, stream))
+        ep[0] = 43
+        return 0
+
     cb_plan, cb_shared = plan_t(fake_plan), shared_t(fake_shared)
+    cb_cascade = cascade_t(fake_cascade)
     try:
         m.init(ctypes.cast(cb_plan, ctypes.c_void_p).value,
-               ctypes.cast(cb_shared, ctypes.c_void_p).value)
+               ctypes.cast(cb_shared, ctypes.c_void_p).value,
+               ctypes.cast(cb_cascade, ctypes.c_void_p).value)
         ip = np.array([0, 3, 4], np.int32)
         ix = np.arange(4, dtype=np.int32)
         la = np.array([5, 16], np.int32)
@@ -313,9 +325,25 @@ def test_plan_fast_path_marshalling():
                              9) == (0, 42)
         assert calls[-1][0] == "shared" and calls[-1][3] == 1 and calls[-1][7] == 9
         assert m.plan_shared(7, gi, ip, ix, la, 9)[0] == 1000   # groups mismatch
+        # cascade: one group of 2 requests over 4 prefix pages, suffixes of 3 and 1 pages
+        g2 = np.array([0, 2], np.int32)
+        pre = (np.array([0, 4], np.int32), ix, np.array([16], np.int32))
+        suf = (ip, ix, la)
+        assert m.plan_cascade(5, g2, *pre, *suf, 8) == (0, 43)
+        assert calls[-1] == ("cascade", 5, g2.ctypes.data, 1, pre[0].ctypes.data,
+                             ix.ctypes.data, pre[2].ctypes.data, ip.ctypes.data, ix.ctypes.data,
+                             la.ctypes.data, 8)
+        n = len(calls)
+        for bad in ((np.array([0, 3], np.int32), *pre, *suf),           # group size != batch
+                    (g2, *pre, ip.astype(np.int64), ix, la),             # int64 suffix indptr
+                    (g2, pre[0], ix[:3], pre[2], *suf),                  # prefix indices short
+                    (g2, *pre, ip, ix[:3], la)):                         # suffix indices short
+            assert m.plan_cascade(5, *bad, 8)[0] == 1000
+        assert len(calls) == n
     finally:
         m.init(ctypes.cast(lib.pkd_plan, ctypes.c_void_p).value,
-               ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value)
+               ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value,
+               ctypes.cast(lib.pkd_plan_cascade, ctypes.c_void_p).value)
 
 
 def test_static_scratch_rejects_mismatched_schedules(lib):
@@ -367,3 +395,96 @@ def test_static_scratch_rejects_mismatched_schedules(lib):
     corrupt.append(bad)
     for bad in corrupt:
         assert run(cfg, bad) == -1
+
+
+def _cascade_cfg(hq, hkv, batch, nnz, pool, n_cta, flags=0):
+    return pkd.make_config(hq, hkv, 128, 16, batch, nnz, pool, -1, -1, n_cta,
+                           pkd.FLAG_CASCADE | flags)
+
+
+def _compare_cascade(cfg, gi, prefix, suffix):
+    words, info, off = pkd.plan_host_cascade(cfg, gi, prefix, suffix)
+    g = cfg.num_qo_heads // cfg.num_kv_heads
+    ref = oplan.plan_cascade(gi, prefix, suffix, page_size=16, num_pages=cfg.num_pages,
+                             n_cta=cfg.num_ctas, hkv=cfg.num_kv_heads, rows=128 // g, alpha=32,
+                             prefix_alpha=256, prefix_cost16=4, suffix_floor=128)
+    got = pkd.decode_schedule(words, off, info)
+    items = [tuple(int(x) for x in r)
+             for r in words[off[1]:off[1] + 8 * info["num_items"]].reshape(-1, 8)]
+    assert info["prefix_ctas"] == ref.n_pre == got["header"][19]
+    assert info["prefix_chunk_tokens"] == ref.chunk_pre == got["header"][20]
+    assert info["chunk_tokens"] == ref.chunk_suf
+    assert info["makespan"] == ref.makespan
+    assert got["cta_indptr"] == ref.cta_indptr
+    assert items == ref.items
+    assert got["units"] == [tuple(x) for x in ref.units]
+    assert got["merge_indptr"] == ref.merge_indptr
+    assert got["page_list"] == ref.page_list
+    assert got["header"][16] == max((n for _, n in ref.units), default=0)
+    return info
+
+
+def test_cascade_plan_bit_exact_shared_prefix_workload(lib):
+    w = workloads.workload("shared_prefix")
+    t = workloads.make_tables(w)
+    n_pre = w.prefix_tokens // 16
+    prefix = (np.array([0, n_pre], np.int32), np.asarray(t["prefix"][1][:n_pre], np.int32),
+              np.array([16], np.int32))
+    cfg = _cascade_cfg(32, 8, w.batch, n_pre + int(t["suffix"][0][-1]), w.pool_pages, 152)
+    info = _compare_cascade(cfg, np.array([0, w.batch], np.int32), prefix, t["suffix"])
+    assert 1 <= info["prefix_ctas"] < 152
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_cascade_plan_bit_exact_random(lib, seed):
+    rng = np.random.default_rng(300 + seed)
+    n_groups = int(rng.integers(1, 5))
+    sizes = rng.integers(1, 60, n_groups).tolist()
+    gi = np.array([0] + np.cumsum(sizes).tolist(), np.int32)
+    B = int(gi[-1])
+    plens = rng.integers(1, 30000, n_groups).tolist()
+    slens = rng.integers(1, 4000, B).tolist()
+    n_pp = sum(-(-l // 16) for l in plens)
+    n_sp = sum(-(-l // 16) for l in slens)
+    pool = n_pp + n_sp + 7
+    ids = rng.permutation(pool).astype(np.int32)
+    prefix = workloads.page_table(plens, 16, ids[:n_pp])
+    suffix = workloads.page_table(slens, 16, ids[n_pp:n_pp + n_sp])
+    hq, hkv = [(32, 8), (64, 8), (16, 8), (8, 8), (8, 2)][seed % 5]
+    n_cta = int(rng.choice([2, 40, 152]))
+    cfg = _cascade_cfg(hq, hkv, B + int(rng.integers(0, 9)), n_pp + n_sp, pool, n_cta)
+    _compare_cascade(cfg, gi, prefix, suffix)
+
+
+def test_cascade_plan_errors(lib):
+    prefix = workloads.page_table([100], 16)                       # pages 0..6
+    suffix = workloads.page_table([5, 20], 16, np.array([7, 8, 9], np.int32))
+    cfg = _cascade_cfg(32, 8, 2, 10, 10, 152)
+    gi = np.array([0, 2], np.int32)
+    words, info, off = pkd.plan_host_cascade(cfg, gi, prefix, suffix)
+    assert info["batch"] == 2 and info["num_units"] == 2
+    with pytest.raises(pkd.PkdError) as e:                        # group with no request
+        pkd.plan_host_cascade(cfg, np.array([0, 0], np.int32), prefix,
+                              workloads.page_table([], 16))
+    assert e.value.status == -2
+    bad = (suffix[0], suffix[1], np.array([5, 17], np.int32))      # last page length > P
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.plan_host_cascade(cfg, gi, prefix, bad)
+    assert e.value.status == -2
+    small = _cascade_cfg(32, 8, 2, 9, 10, 152)                      # 10 pages > capacity 9
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.plan_host_cascade(small, gi, prefix, suffix)
+    assert e.value.status == -7
+    out_of_pool = (suffix[0], np.array([7, 8, 10], np.int32), suffix[2])
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.plan_host_cascade(cfg, gi, prefix, out_of_pool)
+    assert e.value.status == -2
+    with pytest.raises(pkd.PkdError) as e:                        # a plain plan on it
+        pkd.plan_host(cfg, *suffix)
+    assert e.value.status == -1
+    for flags in (pkd.FLAG_SHARED_PREFIX, pkd.FLAG_KV_FP8, pkd.FLAG_FMA_CONSUMER,
+                  pkd.FLAG_ROW_COPIES, pkd.FLAG_CHUNK_SEARCH):
+        c = _cascade_cfg(32, 8, 2, 10, 10, 152, flags)
+        assert lib.pkd_schedule_layout(ctypes.byref(c), (ctypes.c_int64 * 6)()) == -1
+    c = pkd.make_config(32, 8, 128, 8, 2, 10, 10, -1, -1, 152, pkd.FLAG_CASCADE)   # P 8
+    assert lib.pkd_schedule_layout(ctypes.byref(c), (ctypes.c_int64 * 6)()) == -3

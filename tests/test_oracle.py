@@ -478,3 +478,105 @@ def test_per_head_plan_hand_worked():
     assert p.items == [(0, 0, 40, -1, 0, 3, 0), (0, 0, 40, -1, 0, 3, 0)]
     assert p.heads == [0, 1]
     assert p.units == [] and p.merge_indptr == [0]
+
+
+# ---- cascade plans (shared prefix + suffixes in one schedule)
+
+def cascade_coverage_check(p, group_indptr, prefix, suffix, P, hkv):
+    """Independent check of a cascade schedule: for every request and KV
+    head, each token of its group's prefix and of its own suffix is covered
+    exactly once; page references agree with the two tables; each request's
+    slots merge_indptr[r] .. merge_indptr[r+1] are written exactly once per
+    KV head (prefix chunks first, then suffix chunks); CTAs [0, n_pre) hold
+    only prefix items."""
+    p_ip, p_ix, p_last = [list(map(int, x)) for x in prefix]
+    s_ip, s_ix, s_last = [list(map(int, x)) for x in suffix]
+    gi = list(map(int, group_indptr))
+    batch = gi[-1]
+    group_of = [j for j in range(len(gi) - 1) for _ in range(gi[j], gi[j + 1])]
+    plen = [P * (p_ip[j + 1] - p_ip[j] - 1) + p_last[j] for j in range(len(p_last))]
+    slen = [P * (s_ip[r + 1] - s_ip[r] - 1) + s_last[r] for r in range(batch)]
+    nnz_p = p_ip[-1]
+    pre_seen = [np.zeros((hkv, plen[group_of[r]]), np.int32) for r in range(batch)]
+    suf_seen = [np.zeros(slen[r], np.int32) for r in range(batch)]
+    slot_seen = [np.zeros((hkv, p.merge_indptr[r + 1] - p.merge_indptr[r]), np.int32)
+                 for r in range(batch)]
+    n_pre_items = p.cta_indptr[p.n_pre]
+    for idx, (r0, tb, te, dst, fp, n, stride, head) in enumerate(p.items):
+        assert tb % P == 0 and tb < te
+        if idx < n_pre_items:
+            assert stride == -1 and 0 <= head < hkv
+            j = group_of[r0]
+            assert all(group_of[r] == j for r in range(r0, r0 + n)) and te <= plen[j]
+            assert fp == p_ip[j] + tb // P
+            for t in range(tb, te):
+                assert p.page_list[fp + (t - tb) // P] == p_ix[p_ip[j] + t // P]
+            for r in range(r0, r0 + n):
+                pre_seen[r][head, tb:te] += 1
+                slot_seen[r][head, dst] += 1
+        else:
+            assert n == 1 and stride == 0 and head == 0 and te <= slen[r0]
+            assert fp == nnz_p + s_ip[r0] + tb // P
+            for t in range(tb, te):
+                assert p.page_list[fp + (t - tb) // P] == s_ix[s_ip[r0] + t // P]
+            suf_seen[r0][tb:te] += 1
+            slot_seen[r0][:, dst - p.merge_indptr[r0]] += 1
+    for r in range(batch):
+        assert np.all(pre_seen[r] == 1) and np.all(suf_seen[r] == 1)
+        assert np.all(slot_seen[r] == 1)
+        assert p.units[r] == (r, p.merge_indptr[r + 1] - p.merge_indptr[r])
+    assert p.cta_indptr[0] == 0 and p.cta_indptr[-1] == len(p.items)
+    assert all(a <= b for a, b in zip(p.cta_indptr, p.cta_indptr[1:]))
+
+
+def test_cascade_plan_hand_worked():
+    """One group of 2 requests sharing 32 tokens, suffixes of 5 and 20 tokens
+    (P 16, Hkv 1, blocks of 2), 3 CTAs, alpha 0, prefix alpha 0, prefix cost
+    16/16 (a prefix token costs a suffix token), both floors 16.
+    One unit (1 block x 1 head) fits the grid, so budgets are 1 + j (j <= 1).
+    Costs: prefix 32 x 16 = 512, suffix 25 x 16 = 400 -> proportional
+    (3 x 512 + 456) // 912 = 2 CTAs -> j = 1.  Budget 2: the block starts at
+    chunk 32, one more CTA gives it chunk 16 (not below the floor): two
+    items of 16 on CTAs 0 and 1 (span 16); the suffix on the 1 CTA left:
+    bound 25 -> chunk 32, items 20 and 5 (span 25; chunk 16 also gives 25,
+    the larger kept) -> max(16, 25) = 25.  Budget 1 (j = 0): one prefix
+    item of 32 -> 32, worse.  So n_pre = 2, makespan 25.  Request slots: 2
+    prefix chunks + 1 suffix chunk each -> merge_indptr [0, 3, 6]; the suffix
+    items (longest first) write slots 3 + 2 = 5 (request 1) and 0 + 2 = 2
+    (request 0)."""
+    prefix = workloads.page_table([32], 16)            # pages 0, 1
+    suffix = workloads.page_table([5, 20], 16, np.array([2, 3, 4], np.int32))
+    p = oplan.plan_cascade([0, 2], prefix, suffix, page_size=16, num_pages=5, n_cta=3, hkv=1,
+                           rows=2, alpha=0, prefix_alpha=0, prefix_cost16=16, suffix_floor=16,
+                           prefix_floor=16)
+    assert (p.n_pre, p.chunk_pre, p.chunk_suf, p.makespan) == (2, 16, 32, 25)
+    assert p.cta_indptr == [0, 1, 2, 4]
+    assert p.items == [(0, 0, 16, 0, 0, 2, -1, 0), (0, 16, 32, 1, 1, 2, -1, 0),
+                       (1, 0, 20, 5, 3, 1, 0, 0), (0, 0, 5, 2, 2, 1, 0, 0)]
+    assert p.units == [(0, 3), (1, 3)] and p.merge_indptr == [0, 3, 6]
+    assert p.page_list == [0, 1, 2, 3, 4]
+    cascade_coverage_check(p, [0, 2], prefix, suffix, 16, 1)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_cascade_plan_coverage_random(seed):
+    rng = np.random.default_rng(70 + seed)
+    P = 16
+    n_groups = int(rng.integers(1, 4))
+    sizes = rng.integers(1, 70, n_groups).tolist()
+    gi = [0] + np.cumsum(sizes).tolist()
+    B = gi[-1]
+    plens = rng.integers(1, 20000, n_groups).tolist()
+    slens = rng.integers(1, 3000, B).tolist()
+    pool = sum(-(-l // P) for l in plens) + sum(-(-l // P) for l in slens) + 3
+    ids = rng.permutation(pool).astype(np.int32)
+    n_pp = sum(-(-l // P) for l in plens)
+    prefix = workloads.page_table(plens, P, ids[:n_pp])
+    suffix = workloads.page_table(slens, P, ids[n_pp:])
+    hkv = int(rng.choice([1, 2, 8]))
+    n_cta = int(rng.choice([2, 19, 152]))
+    p = oplan.plan_cascade(gi, prefix, suffix, page_size=P, num_pages=pool, n_cta=n_cta, hkv=hkv,
+                           rows=int(rng.choice([16, 32, 128])), alpha=32, prefix_alpha=128,
+                           prefix_cost16=2, suffix_floor=128)
+    assert 1 <= p.n_pre <= n_cta - 1
+    cascade_coverage_check(p, gi, prefix, suffix, P, hkv)

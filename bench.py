@@ -850,6 +850,12 @@ PREFIX_GRID = [(1024, 16, 45.17, 46.52), (8192, 16, 88.67, 226.57), (32768, 16, 
                (1024, 64, 87.86, 130.49), (8192, 64, 125.76, 931.75), (32768, 64, 254.54, 4090.0)]
 
 
+# Short shared prefixes around the point where the cascade stops paying
+# (not in the pages' table): the format advice is checked on them too.
+EXTRA_PREFIX_CASES = [(16, 16, None, None), (128, 16, None, None), (256, 16, None, None),
+                      (16, 64, None, None), (128, 64, None, None)]
+
+
 def run_prefix_sweep(args, rank, world):
     """Shared prefix, composable against single format, over the pages' grid.
     Composable: the prefix level planned once for the whole batch (the dense
@@ -873,10 +879,10 @@ def run_prefix_sweep(args, rank, world):
     reps = max(args.steps, 20)
     rows = []
     launches = 0
-    grid = PREFIX_GRID
+    grid = PREFIX_GRID + EXTRA_PREFIX_CASES
     if args.sweep_cases:
         want = {tuple(int(x) for x in c.split("x")) for c in args.sweep_cases.split(",")}
-        grid = [row for row in PREFIX_GRID if (row[0], row[1]) in want]
+        grid = [row for row in grid if (row[0], row[1]) in want]
         if not grid:
             raise SystemExit(f"--sweep-cases {args.sweep_cases}: no such (prefix x batch)")
     for prefix, B, pages_comp, pages_single in grid:
@@ -933,6 +939,10 @@ def run_prefix_sweep(args, rank, world):
         ldiff = float(max((lse_c - lse_s).abs().max(), (lse_k - lse_s).abs().max()))
         launches += reps * (5 + 2 + 2)
         cinfo = casc.plan_info()
+        acfg = pkd.make_config(w.hq, w.hkv, w.head_dim, P, B, n_pre + int(t["suffix"][0][-1]),
+                               w.pool_pages, -1, -1, cinfo["num_ctas"], pkd.FLAG_CASCADE)
+        advice = pkd.advise_format(acfg, gi, prefix_t, t["suffix"])
+        auto = "cascade" if advice["use_cascade"] else "single"
         kv_once = (prefix + 128 * B) * 2 * w.hkv * w.head_dim * 2
         rows.append({"prefix": prefix, "batch": B, "suffix": 128,
                      "composable_us": round(us["composable"], 2),
@@ -942,6 +952,10 @@ def run_prefix_sweep(args, rank, world):
                      "cascade_speedup": round(us["single"] / us["cascade"], 2),
                      "cascade_plan": {k: cinfo[k] for k in ("prefix_ctas", "prefix_chunk_tokens",
                                                             "chunk_tokens", "num_items")},
+                     "advice": {"format": auto, "cascade_us": round(advice["cascade_us"], 1),
+                                "single_us": round(advice["single_us"], 1)},
+                     "auto_us": round(us[auto], 2),
+                     "auto_vs_best": round(us[auto] / min(us.values()), 3),
                      "composable_GBps_prefix_once": round(kv_once / (us["composable"] * 1e3), 1),
                      "single_GBps_per_request_reads": round(
                          (prefix + 128) * B * 2 * w.hkv * w.head_dim * 2 / (us["single"] * 1e3), 1),
@@ -952,7 +966,8 @@ def run_prefix_sweep(args, rank, world):
             g.close()
         del kvs, comp, sing, cgr, pre, suf, single, casc
         torch.cuda.empty_cache()
-    big = rows[-1]
+    big = [r for r in rows if r["prefix"] == 32768 and r["batch"] == 64] or rows[-1:]
+    big = big[0]
     return {"metric": "shared-prefix decode latency, composable vs single format "
                       "(GPU us per step, CUDA-graph replay)",
             "value": big["composable_us"], "unit": "us", "n_gpus": world, "steps": reps,

@@ -230,6 +230,28 @@ int pkd_plan_cascade(pkd_ctx *ctx, const int32_t *group_indptr, int32_t num_grou
                      const int32_t *s_indptr, const int32_t *s_indices, const int32_t *s_last,
                      void *stream, uint64_t *epoch);
 
+/* Format advice for a shared-prefix step ("FlashInfer 完全拆解", Composable
+ * Format 只在复用足够大时占优: splitting off the shared prefix pays only when
+ * the reuse is large enough).  For the same tables as pkd_plan_cascade (page
+ * ids are not needed), predicts the GPU time per layer of the cascade plan
+ * and of the single format -- every request over its whole table, prefix
+ * pages then its own, planned by pkd_plan -- from each planner's predicted
+ * makespan with time = a + b x makespan (constants fitted on GB300 over the
+ * pages' grid of prefix length x batch), and picks the faster.  Host only,
+ * no CUDA call; cfg is the cascade context's configuration (flags
+ * PKD_FLAG_CASCADE, num_ctas >= 2, the grid the plans would use). */
+typedef struct pkd_format_advice {
+    int32_t use_cascade;       /* 1: the cascade plan is predicted faster   */
+    int32_t prefix_ctas;       /* the cascade plan's prefix CTAs            */
+    int64_t cascade_makespan;  /* cascade planner, suffix-token units       */
+    int64_t single_makespan;   /* plain planner over whole requests, tokens */
+    float cascade_us;          /* predicted microseconds per layer          */
+    float single_us;
+} pkd_format_advice;
+int pkd_advise_format(const pkd_config *cfg, const int32_t *group_indptr, int32_t num_groups,
+                      const int32_t *p_indptr, const int32_t *p_last, const int32_t *s_indptr,
+                      const int32_t *s_last, pkd_format_advice *advice);
+
 /* Summary of the current plan.  Errors: INVALID_ARG, NO_PLAN. */
 int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
 

@@ -31,7 +31,8 @@ import numpy as np
 
 __all__ = [
     "build", "load", "PkdError", "BatchDecodeWithPagedKVCache", "merge_states", "append_kv",
-    "append_kv_layers", "plan_host", "plan_host_shared", "plan_host_cascade", "schedule_layout",
+    "append_kv_layers", "plan_host", "plan_host_shared", "plan_host_cascade", "advise_format",
+    "schedule_layout",
     "selftest_bounded_wait", "Graph",
     "STATUS",
 ]
@@ -58,7 +59,7 @@ EXPORTS = (
     "pkd_graph_destroy", "pkd_status_str", "pkd_version", "pkd_run_static_scratch",
     "pkd_append_kv", "pkd_append_kv_ex", "pkd_plan_shared", "pkd_plan_host_shared", "pkd_run_scaled",
     "pkd_selftest_bounded_wait", "pkd_append_kv_layers", "pkd_static_scratch_last_error",
-    "pkd_plan_cascade", "pkd_plan_host_cascade",
+    "pkd_plan_cascade", "pkd_plan_host_cascade", "pkd_advise_format",
 )
 
 
@@ -74,6 +75,15 @@ class Config(ctypes.Structure):
         "num_qo_heads", "num_kv_heads", "head_dim", "page_size", "max_batch",
         "max_num_pages", "num_pages", "alpha", "min_chunk_tokens", "num_ctas")] + [
         ("flags", ctypes.c_uint32)]
+
+
+class FormatAdvice(ctypes.Structure):
+    _fields_ = [("use_cascade", ctypes.c_int32), ("prefix_ctas", ctypes.c_int32),
+                ("cascade_makespan", ctypes.c_int64), ("single_makespan", ctypes.c_int64),
+                ("cascade_us", ctypes.c_float), ("single_us", ctypes.c_float)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class PlanInfo(ctypes.Structure):
@@ -140,6 +150,8 @@ def load():
                                             ctypes.POINTER(u64)]),
         "pkd_plan_host_cascade": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz,
                                                  ctypes.POINTER(PlanInfo)]),
+        "pkd_advise_format": (ctypes.c_int, [cfgp, vp, i32, vp, vp, vp, vp,
+                                             ctypes.POINTER(FormatAdvice)]),
         "pkd_append_kv": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
                                          i32, i32, vp, vp]),
         "pkd_append_kv_ex": (ctypes.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32, i32,
@@ -268,6 +280,20 @@ def plan_host_cascade(cfg: Config, group_indptr, prefix, suffix):
                                    ctypes.byref(info))
     _check(st, "pkd_plan_host_cascade")
     return words, info.as_dict(), off
+
+
+def advise_format(cfg: Config, group_indptr, prefix, suffix):
+    """Which format a shared-prefix step should take: the cascade plan or
+    every request over its whole table (see pkd_advise_format).  cfg: a
+    cascade configuration with num_ctas >= 2; prefix / suffix as for
+    plan_cascade (page ids are not read).  Returns a dict with use_cascade
+    and both predictions (microseconds per layer)."""
+    lib = load()
+    gi, n_groups, p, q = _cascade_tables(group_indptr, prefix, suffix)
+    adv = FormatAdvice()
+    _check(lib.pkd_advise_format(ctypes.byref(cfg), _ptr(gi), n_groups, _ptr(p[0]), _ptr(p[2]),
+                                 _ptr(q[0]), _ptr(q[2]), ctypes.byref(adv)), "pkd_advise_format")
+    return adv.as_dict()
 
 
 def decode_schedule(words, off, info):

@@ -319,6 +319,17 @@ int pkd_plan_host_cascade(const pkd_config* cfg, const int32_t* group_indptr,
                                p_indices, p_last, s_indptr, s_indices, s_last, host_words, info);
 }
 
+int pkd_advise_format(const pkd_config* cfg, const int32_t* group_indptr, int32_t num_groups,
+                      const int32_t* p_indptr, const int32_t* p_last, const int32_t* s_indptr,
+                      const int32_t* s_last, pkd_format_advice* advice) {
+  int st = check_config(cfg);
+  if (st != PKD_OK) return st;
+  if (cfg->num_ctas < 2 || advice == nullptr || !(cfg->flags & PKD_FLAG_CASCADE))
+    return PKD_E_INVALID_ARG;
+  return advise_format(*cfg, cfg->num_ctas, group_indptr, num_groups, p_indptr, p_last, s_indptr,
+                       s_last, advice);
+}
+
 int pkd_plan_host(const pkd_config* cfg, const int32_t* indptr, const int32_t* indices,
                   const int32_t* last_page_len, int32_t batch, int32_t* host_words,
                   size_t max_words, pkd_plan_info* info) {

@@ -1185,10 +1185,10 @@ __host__ __device__ __forceinline__ int stage_bytes_for(int row_bytes, int token
 // The decode role over the dynamic shared memory at `smem`: the whole
 // decode kernel, and the suffix CTAs of the cascade kernel.  Warps past the
 // producer (a fused launch may have more) do nothing.
-template <int G, bool kMma, bool kBlock, bool kFp8, bool kTiles>
+template <int G, bool kMma, bool kBlock, bool kFp8, bool kTiles, int kRingSel = 0>
 __device__ __forceinline__ void decode_body(const DecodeArgs& a, uint8_t* smem) {
   constexpr int kStageTokens = kFp8 ? kFp8Tokens : kTS;
-  constexpr int kRing = ring_depth(kMma, kBlock, kFp8);
+  constexpr int kRing = kRingSel > 0 ? kRingSel : ring_depth(kMma, kBlock, kFp8);
   const int stage_bytes = stage_bytes_for(a.row_bytes, kStageTokens, kTiles);
   // the 128-byte swizzle repeats every 1024 bytes: page-tile stages start on
   // a 1024-byte boundary (the launch reserves the slack)
@@ -1274,7 +1274,7 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
   if ((int)blockIdx.x < a.pre.sched[H_NPRE])
     tc::prefix_tc_body<true>(a.pre, smem);
   else
-    decode_body<G, true, false, false, true>(a.suf, smem);
+    decode_body<G, true, false, false, true, kCascadeSuffixRing>(a.suf, smem);
 }
 
 template <int G, bool kTiles>
@@ -1330,18 +1330,14 @@ bool use_mma_consumer(int group, uint32_t flags) {
 }
 
 int decode_smem_bytes(int hkv, const DecodeKind& k) {
-  if (k.cascade) {
-    DecodeKind d = k;
-    d.cascade = false;
-    const int dec = decode_smem_bytes(hkv, d);
-    return dec > tc::smem_bytes() ? dec : tc::smem_bytes();
-  }
   if (k.dense) return prefix_tc_smem_bytes();
   const int row = hkv * kHeadDim * (k.fp8 ? 1 : 2);
   const int tokens = k.fp8 ? kFp8Tokens : kTS;
-  const int ring = ring_depth(k.mma, k.block, k.fp8);
-  return ring * stage_bytes_for(row, tokens, k.tmap) + (k.tmap ? 1024 : 0) +
-         kMaxKvHeads * kTS * k.group * 4 + kMaxKvHeads * 32 * 4 + 2 * ring * 8 + 16;
+  // the cascade kernel: its decode role's ring, or the dense role's layout
+  const int ring = k.cascade ? kCascadeSuffixRing : ring_depth(k.mma, k.block, k.fp8);
+  const int dec = ring * stage_bytes_for(row, tokens, k.tmap) + (k.tmap ? 1024 : 0) +
+                  kMaxKvHeads * kTS * k.group * 4 + kMaxKvHeads * 32 * 4 + 2 * ring * 8 + 16;
+  return (k.cascade && tc::smem_bytes() > dec) ? tc::smem_bytes() : dec;
 }
 
 cudaError_t decode_prepare(const DecodeKind& k, int smem_bytes) {

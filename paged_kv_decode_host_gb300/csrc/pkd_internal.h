@@ -77,6 +77,14 @@ constexpr int64_t kCascadePrefixCost16 = PKD_CASCADE_PREFIX_COST16;
 constexpr int64_t kCascadePrefixAlpha = PKD_CASCADE_PREFIX_ALPHA;
 constexpr int64_t kCascadeSuffixFloor = PKD_CASCADE_SUFFIX_FLOOR;
 constexpr int64_t kCascadePrefixFloor = 128;   // one round of the dense role
+// The cascade kernel's decode role has the shared memory the dense role
+// needs (about 227 KB), so its ring holds three 64 KB stages instead of the
+// plain decode kernel's two: with part of the grid streaming the suffixes,
+// each of those CTAs keeps more bytes in flight.
+#ifndef PKD_CASCADE_SUFFIX_RING
+#define PKD_CASCADE_SUFFIX_RING 3
+#endif
+constexpr int kCascadeSuffixRing = PKD_CASCADE_SUFFIX_RING;
 
 // Fixed word offsets of the schedule arrays, all derived from capacities.
 struct Layout {
@@ -262,6 +270,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
                           const int32_t* group_indptr, int32_t n_rows, const int32_t* indptr,
                           const int32_t* indices, const int32_t* last, int32_t* words,
                           pkd_plan_info* info);
+// Which format a shared-prefix step should take (pkd_advise_format).
+int advise_format(const pkd_config& cfg, int32_t n_cta, const int32_t* group_indptr,
+                  int32_t n_groups, const int32_t* p_indptr, const int32_t* p_last,
+                  const int32_t* s_indptr, const int32_t* s_last, pkd_format_advice* out);
 // A cascade plan: groups of requests (group_indptr) sharing prefix table rows
 // (p_*, one row per group) and every request's own suffix table row (s_*,
 // one row per request).

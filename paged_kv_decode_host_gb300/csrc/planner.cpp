@@ -572,21 +572,20 @@ struct CascadeScratch {
 
 }  // namespace
 
-int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
-                          const int32_t* group_indptr, int32_t n_groups,
-                          const int32_t* p_indptr, const int32_t* p_indices,
-                          const int32_t* p_last, const int32_t* s_indptr,
-                          const int32_t* s_indices, const int32_t* s_last, int32_t* words,
-                          pkd_plan_info* info) {
-  if (n_groups < 0 || n_cta < 2 || words == nullptr) return PKD_E_INVALID_ARG;
+// The cascade plan's search over the tables' lengths (no page ids): blocks,
+// both levels' costs, and the CTA split; the chosen levels are left in
+// cs.best_pre / cs.best_suf.  *n_pre, *span (1/16 suffix-token units) and
+// *batch are set.
+int cascade_search(const pkd_config& cfg, int32_t n_cta, const int32_t* group_indptr,
+                   int32_t n_groups, const int32_t* p_indptr, const int32_t* p_last,
+                   const int32_t* s_indptr, const int32_t* s_last, Scratch& sc, CascadeScratch& cs,
+                   int32_t* batch_out, int32_t* n_pre_out, int64_t* span_out, int64_t* alpha_out,
+                   int64_t* floor_s_out) {
+  if (n_groups < 0 || n_cta < 2) return PKD_E_INVALID_ARG;
   if (n_groups > 0 && group_indptr == nullptr) return PKD_E_INVALID_ARG;
   const int64_t P = cfg.page_size;
   const int32_t R = block_rows(cfg);
   const int32_t hkv = cfg.num_kv_heads;
-  thread_local Scratch sc;
-  thread_local CascadeScratch cs;
-
-  // ---- requests, groups, both tables
   int32_t batch = 0;
   if (n_groups > 0) {
     if (group_indptr[0] != 0) return PKD_E_BAD_TABLE;
@@ -599,15 +598,6 @@ int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   if (st != PKD_OK) return st;
   st = row_lengths(s_indptr, s_last, batch, P, &cs.suf_len);
   if (st != PKD_OK) return st;
-  const int64_t nnz_p = n_groups > 0 ? p_indptr[n_groups] : 0;
-  const int64_t nnz_s = batch > 0 ? s_indptr[batch] : 0;
-  if (nnz_p + nnz_s > cfg.max_num_pages) return PKD_E_CAPACITY;
-  if ((nnz_p > 0 && p_indices == nullptr) || (nnz_s > 0 && s_indices == nullptr))
-    return PKD_E_INVALID_ARG;
-  // page list: the prefix table's indices, then the suffix table's
-  if (!copy_checked(p_indices, words + L.page_list, nnz_p, cfg.num_pages) ||
-      !copy_checked(s_indices, words + L.page_list + nnz_p, nnz_s, cfg.num_pages))
-    return PKD_E_BAD_TABLE;
 
   // ---- prefix blocks (units: block x KV head) and the levels' total costs
   cs.blocks.clear();
@@ -678,6 +668,42 @@ int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     cs.best_pre = LevelPlan{};
     cs.best_suf = LevelPlan{};
   }
+  *batch_out = batch;
+  *n_pre_out = n_pre;
+  *span_out = best_span;
+  *alpha_out = alpha;
+  *floor_s_out = floor_s;
+  return PKD_OK;
+}
+
+int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
+                          const int32_t* group_indptr, int32_t n_groups,
+                          const int32_t* p_indptr, const int32_t* p_indices,
+                          const int32_t* p_last, const int32_t* s_indptr,
+                          const int32_t* s_indices, const int32_t* s_last, int32_t* words,
+                          pkd_plan_info* info) {
+  if (words == nullptr) return PKD_E_INVALID_ARG;
+  const int64_t P = cfg.page_size;
+  const int32_t R = block_rows(cfg);
+  const int32_t hkv = cfg.num_kv_heads;
+  thread_local Scratch sc;
+  thread_local CascadeScratch cs;
+  int32_t batch = 0, n_pre = 0;
+  int64_t best_span = 0, alpha = 0, floor_s = 0;
+  int st = cascade_search(cfg, n_cta, group_indptr, n_groups, p_indptr, p_last, s_indptr, s_last,
+                          sc, cs, &batch, &n_pre, &best_span, &alpha, &floor_s);
+  if (st != PKD_OK) return st;
+  const int64_t nnz_p = n_groups > 0 ? p_indptr[n_groups] : 0;
+  const int64_t nnz_s = batch > 0 ? s_indptr[batch] : 0;
+  if (nnz_p + nnz_s > cfg.max_num_pages) return PKD_E_CAPACITY;
+  if ((nnz_p > 0 && p_indices == nullptr) || (nnz_s > 0 && s_indices == nullptr))
+    return PKD_E_INVALID_ARG;
+  // page list: the prefix table's indices, then the suffix table's
+  if (!copy_checked(p_indices, words + L.page_list, nnz_p, cfg.num_pages) ||
+      !copy_checked(s_indices, words + L.page_list + nnz_p, nnz_s, cfg.num_pages))
+    return PKD_E_BAD_TABLE;
+  int64_t suf_total = 0;
+  for (int64_t l : cs.suf_len) suf_total += l;
   const LevelPlan& pre = cs.best_pre;
   const LevelPlan& suf = cs.best_suf;
   const int64_t n_items = (int64_t)pre.items.size() + (int64_t)suf.items.size();
@@ -782,6 +808,69 @@ int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
     info->prefix_ctas = n_pre;
     info->prefix_chunk_tokens = h[H_PCHUNK];
   }
+  return PKD_OK;
+}
+
+// ---------------------------------------------------------------- advice
+//
+// Which format serves a shared-prefix step faster ("FlashInfer 完全拆解",
+// Composable Format 只在复用足够大时占优: the split into a shared level only
+// pays once the reuse is large enough): the cascade plan (shared prefix once,
+// suffixes apart, one merge) or the single format (every request over its
+// whole table, prefix pages then its own).  Each is predicted from its own
+// planner's makespan M: the cascade search above, and the plain planner's
+// chunk choice (candidates L, L/2, L/4 of the work bound, floor 256, alpha
+// 32) over the concatenated lengths.  Time per layer = a + b M, fitted on
+// GB300 over the pages' grid of shared prefix x batch (1,024 / 8,192 /
+// 32,768 tokens x 16 / 64 requests, 128-token suffixes) and the 8,192 x 32
+// step: cascade 15.3 us + 0.0498 us per unit (the merge and the dense role's
+// set-up make its fixed part larger), single 10.2 us + 0.0481 us per token.
+constexpr double kAdviceCascadeUs0 = 15.3, kAdviceCascadeUsPerUnit = 0.0498;
+constexpr double kAdviceSingleUs0 = 10.2, kAdviceSingleUsPerToken = 0.0481;
+
+// The plain planner's makespan for these lengths (its chunk candidates and
+// LPT, without the schedule).
+int64_t plain_makespan(const std::vector<int64_t>& lens, int32_t n_cta, int64_t P, Scratch& sc) {
+  int64_t total = 0;
+  for (int64_t l : lens) total += l;
+  if (lens.empty()) return 0;
+  const int64_t alpha = kDefaultAlpha;
+  const int64_t floor_c = ceil_div(kDefaultMinChunk, P) * P;
+  const int64_t bound = ceil_div(total, n_cta);
+  int64_t best = -1;
+  std::vector<int64_t> seen;
+  for (int64_t k : {1, 2, 4}) {
+    const int64_t c = std::max(ceil_div(ceil_div(bound, k), P) * P, floor_c);
+    if (std::find(seen.begin(), seen.end(), c) != seen.end()) continue;
+    seen.push_back(c);
+    split_sorted(lens, c, alpha, &sc.whole, &sc.rest, &sc.items);
+    const int64_t span = lpt(sc.items, n_cta, &sc.owner, &sc.heap);
+    if (best < 0 || span < best) best = span;
+  }
+  return best;
+}
+
+int advise_format(const pkd_config& cfg, int32_t n_cta, const int32_t* group_indptr,
+                  int32_t n_groups, const int32_t* p_indptr, const int32_t* p_last,
+                  const int32_t* s_indptr, const int32_t* s_last, pkd_format_advice* out) {
+  if (out == nullptr) return PKD_E_INVALID_ARG;
+  thread_local Scratch sc;
+  thread_local CascadeScratch cs;
+  int32_t batch = 0, n_pre = 0;
+  int64_t span = 0, alpha = 0, floor_s = 0;
+  const int st = cascade_search(cfg, n_cta, group_indptr, n_groups, p_indptr, p_last, s_indptr,
+                                s_last, sc, cs, &batch, &n_pre, &span, &alpha, &floor_s);
+  if (st != PKD_OK) return st;
+  std::vector<int64_t> whole((size_t)batch);
+  for (int32_t r = 0; r < batch; ++r) whole[r] = cs.block_len[cs.block_of[r]] + cs.suf_len[r];
+  const int64_t ms = plain_makespan(whole, n_cta, cfg.page_size, sc);
+  std::memset(out, 0, sizeof(*out));
+  out->prefix_ctas = n_pre;
+  out->cascade_makespan = span / 16;
+  out->single_makespan = ms;
+  out->cascade_us = (float)(kAdviceCascadeUs0 + kAdviceCascadeUsPerUnit * (double)(span / 16));
+  out->single_us = (float)(kAdviceSingleUs0 + kAdviceSingleUsPerToken * (double)ms);
+  out->use_cascade = batch > 0 && out->cascade_us < out->single_us ? 1 : 0;
   return PKD_OK;
 }
 

@@ -488,3 +488,35 @@ def test_cascade_plan_errors(lib):
         assert lib.pkd_schedule_layout(ctypes.byref(c), (ctypes.c_int64 * 6)()) == -1
     c = pkd.make_config(32, 8, 128, 8, 2, 10, 10, -1, -1, 152, pkd.FLAG_CASCADE)   # P 8
     assert lib.pkd_schedule_layout(ctypes.byref(c), (ctypes.c_int64 * 6)()) == -3
+
+
+def test_format_advice_matches_both_planners(lib):
+    """pkd_advise_format predicts each format from its own planner: its
+    cascade makespan is the cascade plan's, its single-format makespan the
+    plain plan's over every request's whole table (prefix pages, then its
+    own); the longer the shared prefix, the larger the predicted gain."""
+    gains = []
+    for prefix_tokens, batch in ((16, 16), (1024, 16), (8192, 16), (8192, 64), (32768, 64)):
+        w = workloads.shared_prefix_case(prefix_tokens, batch)
+        t = workloads.make_tables(w)
+        n_pre = prefix_tokens // 16
+        prefix = (np.array([0, n_pre], np.int32), np.asarray(t["prefix"][1][:n_pre], np.int32),
+                  np.array([16], np.int32))
+        gi = np.array([0, batch], np.int32)
+        cfg = _cascade_cfg(32, 8, batch, n_pre + int(t["suffix"][0][-1]), w.pool_pages, 152)
+        adv = pkd.advise_format(cfg, gi, prefix, t["suffix"])
+        _, info, _ = pkd.plan_host_cascade(cfg, gi, prefix, t["suffix"])
+        assert adv["cascade_makespan"] == info["makespan"]
+        assert adv["prefix_ctas"] == info["prefix_ctas"]
+        plain = pkd.make_config(32, 8, 128, 16, batch, int(t["indptr"][-1]), w.pool_pages, -1, -1,
+                                152)
+        _, pinfo, _ = pkd.plan_host(plain, t["indptr"], t["indices"], t["last"])
+        assert adv["single_makespan"] == pinfo["makespan"]
+        assert adv["use_cascade"] == int(adv["cascade_us"] < adv["single_us"])
+        gains.append(adv["single_us"] / adv["cascade_us"])
+    assert gains[0] < 1.0 < gains[1]                   # a one-page prefix: no reuse to win
+    assert gains == sorted(gains)
+    with pytest.raises(pkd.PkdError):                  # a plain configuration is refused
+        pkd.advise_format(pkd.make_config(32, 8, 128, 16, 16, 100, 100, -1, -1, 152),
+                          np.array([0, 1], np.int32), workloads.page_table([16], 16),
+                          workloads.page_table([5], 16))

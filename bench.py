@@ -42,7 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # the decode kernel's sources: a profile's counters stand for the kernel built from these
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_kv_decode_host_gb300", "csrc", f)
-                  for f in ("decode_kernel.cu", "sm103_ptx.cuh", "pkd_internal.h")]
+                  for f in ("decode_kernel.cu", "sm103_ptx.cuh", "pkd_internal.h",
+                            "prefix_tc_body.cuh")]
 
 
 def kernel_source_sha256():
@@ -81,12 +82,12 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profile(workload):
-    """DRAM bytes per decode launch of this workload from the committed ncu
-    summary (profiles/decode_kernel_<workload>.md), if it was taken on the
-    current kernel source (else None)."""
+def traffic_from_profile(workload, kernel="decode_kernel"):
+    """DRAM bytes per launch of this workload's dominant kernel from the
+    committed ncu summary (profiles/<kernel>_<workload>.md), if it was taken
+    on the current kernel source (else None)."""
     try:
-        with open(os.path.join(PROFILE_DIR, f"decode_kernel_{workload}.md")) as f:
+        with open(os.path.join(PROFILE_DIR, f"{kernel}_{workload}.md")) as f:
             text = f.read()
         sha = kernel_source_sha256()
     except OSError:
@@ -314,6 +315,8 @@ def run_ours(args, rank, world):
     # another step's bytes out of L2: at least 4, and at least 1.2 GB in all
     copies = 1 if layers > 1 else max(4, int(np.ceil(
         1.2e9 / (w.pool_pages * 2 * P * w.hkv * w.head_dim * w.kv_elem_bytes))))
+    if args.copies > 0:   # fewer cache copies (a smaller device footprint for counter captures)
+        copies = args.copies
     n_kv = layers * copies
     if w.kv_dtype == "e4m3":
         kvs, kv_scale = workloads.make_kv_fp8(w, device=dev, layers=n_kv)
@@ -554,8 +557,10 @@ def run_ours(args, rank, world):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback",
             "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": traffic_from_profile(args.workload),
-            "kernel": "decode_kernel", "launch_ms_mean": round(k1_mean_ms, 5),
+            "traffic": traffic_from_profile(args.workload,
+                                            "cascade_kernel" if cascade else "decode_kernel"),
+            "kernel": "cascade_kernel" if cascade else "decode_kernel",
+            "launch_ms_mean": round(k1_mean_ms, 5),
             "launch_gbs_min": round(min(k1_gbs), 1) if k1_gbs else None,
             "launch_gbs_max": round(max(k1_gbs), 1) if k1_gbs else None,
             "timing": "CUDA event nodes around each decode launch inside a replayed copy of "
@@ -1228,6 +1233,9 @@ def main():
                          "head) or the mma.sync row-block consumer (16-row tiles)")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per step (0: the workload's own); smaller for profiling captures")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="cache copies rotated by single-layer workloads (0: enough for 1.2 GB); "
+                         "fewer only to keep profiling captures small")
     ap.add_argument("--other-steps", type=int, default=300,
                     help="timed steps of each other workload reported with the default one")
     ap.add_argument("--no-other-workloads", action="store_true",

@@ -246,7 +246,8 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   m.off_units = ctx->layout.units;
   m.off_merge = ctx->layout.merge_indptr;
   m.hq = c.num_qo_heads;
-  if (launch_merge_partials(m, ctx->merge_grid, ctx->max_chunks, stream) != cudaSuccess)
+  if (launch_merge_partials(m, ctx->merge_grid, ctx->max_chunks, stream,
+                            ctx->kind.cascade) != cudaSuccess)
     return PKD_E_CUDA;
   return PKD_OK;
 }

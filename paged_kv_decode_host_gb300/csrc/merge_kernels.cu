@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(256) merge_states_kernel(
 }  // namespace
 
 cudaError_t launch_merge_partials(const MergeArgs& a, int grid, int32_t max_chunks,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool batch_short) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMergeThreads);
@@ -261,6 +261,8 @@ cudaError_t launch_merge_partials(const MergeArgs& a, int grid, int32_t max_chun
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_chunks > kLongUnit) return cudaLaunchKernelEx(&cfg, merge_partials_kernel<8>, a);
+  if (batch_short && max_chunks <= 4 * (kMergeThreads / 32))
+    return cudaLaunchKernelEx(&cfg, merge_partials_kernel<4>, a);
   return cudaLaunchKernelEx(&cfg, merge_partials_kernel<1>, a);
 }
 

@@ -247,8 +247,10 @@ inline int merge_grid_for(int n_cta) { return 8 * n_cta; }
 // H_MAXCHUNKS); above kLongUnit the merge keeps several slots' loads in flight
 // per warp.  Any value gives the same results.
 constexpr int32_t kLongUnit = 64;
+// batch_short (cascade plans: every request a unit of a few slots): units of
+// at most 32 slots load all their slots in one batch per warp (4 each).
 cudaError_t launch_merge_partials(const MergeArgs& a, int grid, int32_t max_chunks,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, bool batch_short = false);
 cudaError_t launch_merge_states(const void* v_a, const float* s_a, const void* v_b,
                                 const float* s_b, void* v_out, float* s_out,
                                 int64_t rows, int head_dim, cudaStream_t stream);

@@ -1188,8 +1188,9 @@ def run_other_workloads(args, rank, world, names=OTHER_WORKLOADS):
             "steps": ln["steps"], "warmup": ln["warmup"],
             "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "frac", "traffic",
                                             "launch_ms_mean")},
-            "e2e": {k: ln["e2e"][k] for k in ("value", "unit", "ms_per_step",
-                                               "h2d_bytes_per_step", "d2h_bytes_per_step")},
+            "e2e": {k: ln["e2e"][k] for k in ("value", "unit", "ms_per_step", "ms_gpu_events",
+                                               "ms_host_wall", "h2d_bytes_per_step",
+                                               "d2h_bytes_per_step")},
             "clocks": ln["clocks"], "gpu_launches": ln["gpu_launches"],
             "config": {k: ln["config"][k] for k in ("batch", "hq", "hkv", "page_size",
                                                     "total_tokens_per_layer",

@@ -338,9 +338,10 @@ def plan_cascade(group_indptr, prefix, suffix, *, page_size: int, num_pages: int
       suffix-token units, suffix items alpha + tokens; the prefix budget
       starts where each level gets CTAs in proportion to its total cost (in
       steps of hkv above one CTA per unit when the grid allows, rounded to
-      the nearest step) and climbs: both neighbouring budgets of the best so
-      far are scheduled (the lower first) while the predicted makespan falls
-      strictly; the suffix gets every CTA the prefix items do not use;
+      the nearest step) and moves toward the level whose makespan is the
+      larger (more prefix CTAs when the prefix level bounds the step), one
+      step at a time while the predicted makespan falls strictly; the suffix
+      gets every CTA the prefix items do not use;
     * every request is a unit of the reduction map whose slots are its
       prefix chunks then its suffix chunks (all items write partial states).
     """
@@ -385,17 +386,16 @@ def plan_cascade(group_indptr, prefix, suffix, *, page_size: int, num_pages: int
             return (max(pre[0] * prefix_cost16, suf[1] * 16), j, pre, suf)
 
         best = schedule(j0)
-        tried = {j0}
-        while True:
-            at = best[1]
-            for nb in (at - 1, at + 1):
-                if 0 <= nb <= j_max and nb not in tried:
-                    tried.add(nb)
-                    cand = schedule(nb)
-                    if cand[0] < best[0]:
-                        best = cand
-            if best[1] == at:
+        p_span = best[2][0] * prefix_cost16
+        s_span = best[3][1] * 16
+        step_dir = (p_span > s_span) - (p_span < s_span)
+        j = j0 + step_dir
+        while step_dir and 0 <= j <= j_max:
+            cand = schedule(j)
+            if cand[0] >= best[0]:
                 break
+            best = cand
+            j += step_dir
     if best is None:
         return CascadePlan(0, 0, 0, 0, [0] * (n_cta + 1), [], [], [0], [])
     span, _, (_, q_pre, block_chunk, n_pre), (c_s, _, q_suf) = best

@@ -106,6 +106,11 @@ void split_sorted(const std::vector<int64_t>& lens, int64_t chunk, int64_t alpha
                   std::vector<Item>* whole, std::vector<Item>* rest, std::vector<Item>* out) {
   whole->clear();
   rest->clear();
+  size_t n = 0;
+  for (int64_t l : lens) n += (size_t)ceil_div(l, chunk);
+  whole->reserve(n);
+  rest->reserve(lens.size());
+  out->reserve(n);
   for (size_t i = 0; i < lens.size(); ++i) {
     int32_t k = 0;
     for (int64_t t = 0; t < lens[i]; t += chunk, ++k) {
@@ -447,9 +452,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 // n_pre balances the two levels' predicted makespans in one cost unit
 // (suffix tokens: kCascadePrefixCost16): starting from the budget that gives
 // each level CTAs in proportion to its total cost (in steps of Hkv when
-// every head can have a CTA, rounded to the nearest step), it climbs to
-// neighbouring budgets (the lower one first) while the predicted makespan
-// falls strictly.  Every item writes a partial state: request r's slots are
+// every head can have a CTA, rounded to the nearest step), it moves toward
+// the level whose makespan is the larger (more prefix CTAs when the prefix
+// level bounds the step, fewer when the suffix level does), one step at a
+// time while the predicted makespan falls strictly.  Every item writes a partial state: request r's slots are
 // merge_indptr[r] .. merge_indptr[r + 1], its prefix chunks first, then its
 // suffix chunks, and one merge folds them.  Prefix items mark themselves with
 // slot stride -1 and carry their chunk index as dst_slot (a block's requests
@@ -650,18 +656,14 @@ int cascade_search(const pkd_config& cfg, int32_t n_cta, const int32_t* group_in
       }
     };
     evaluate(j0);
-    int64_t lo_done = j0, hi_done = j0;   // budgets [lo_done, hi_done] scheduled
-    for (;;) {
-      const int64_t at = best_j;
-      if (at - 1 >= 0 && at - 1 < lo_done) {
-        evaluate(at - 1);
-        lo_done = at - 1;
-      }
-      if (at + 1 <= j_max && at + 1 > hi_done) {
-        evaluate(at + 1);
-        hi_done = at + 1;
-      }
-      if (best_j == at) break;
+    // move toward the level that bounds the makespan (more prefix CTAs when
+    // the prefix level does), one step at a time, while it improves
+    const int64_t p_span = cs.best_pre.span * kCascadePrefixCost16;
+    const int64_t s_span = cs.best_suf.span * 16;
+    const int64_t dir = p_span > s_span ? 1 : (p_span < s_span ? -1 : 0);
+    for (int64_t j = j0 + dir; dir != 0 && j >= 0 && j <= j_max; j += dir) {
+      evaluate(j);
+      if (best_j != j) break;
     }
     n_pre = cs.best_pre.ctas;
   } else {

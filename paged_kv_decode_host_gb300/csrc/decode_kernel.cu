@@ -1268,11 +1268,11 @@ __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
 // each new plan.  Roles keep their own shared-memory layouts inside the
 // launch's (the larger of the two) and their own programmatic-launch rules.
 template <int G>
-__global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
+__global__ void __launch_bounds__(tc::kTcThreads, 1)
     cascade_kernel(const __grid_constant__ CascadeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];   // each role aligns its own layout
   if ((int)blockIdx.x < a.pre.sched[H_NPRE])
-    tc::prefix_tc_body<true>(a.pre, smem);
+    tc::prefix_tc_body(a.pre, smem);
   else
     decode_body<G, true, false, false, true, kCascadeSuffixRing>(a.suf, smem);
 }
@@ -1318,7 +1318,7 @@ const void* kernel_for(const DecodeKind& k) {
 }  // namespace
 
 int decode_threads(int hkv, const DecodeKind& k) {
-  if (k.cascade) return (hkv + 1 > 8 ? hkv + 1 : 8) * 32;   // decode role, or the 8 dense roles
+  if (k.cascade) return tc::kTcThreads;   // the dense role's 12 warps (the decode role uses hkv + 1)
   return k.dense ? prefix_tc_threads() : (hkv + 1) * 32;
 }
 

@@ -10,31 +10,40 @@
 // the KV head are 128 rows of one dense tile, so the item is a real
 // contraction: S = Q K^T (128 x 16 per page tile) and O += P V (128 x 128).
 //
-// GB300 design (one CTA per SM, 8 warps):
-//  * warp 4 (producer) loads the item's Q tile once (two TMA tensor copies,
+// GB300 design (one CTA per SM, 12 warps):
+//  * warp 8 (producer) loads the item's Q tile once (two TMA tensor copies,
 //    128 rows x 128 dims, 128-byte swizzle) and streams the KV head's K page
-//    tiles into a 3-deep ring of 128-token slots; warp 6 streams V into a
+//    tiles into a 3-deep ring of 128-token slots; warp 10 streams V into a
 //    ring of its own, so a K slot is refilled as soon as its score MMAs are
 //    done instead of waiting for the round's P.V.  One TMA tensor copy moves
 //    16 tokens of one 128-byte half of the head (2 KB), placed so that each
 //    half of a slot is one [128 tokens][128 B] swizzled matrix -- a whole
 //    round is one MMA operand however the pages are scattered;
-//  * warp 5 (one lane) issues the score MMAs: per round of 128 tokens, S
+//  * warp 9 (one lane) issues the score MMAs: per round of 128 tokens, S
 //    into a double-buffered tensor-memory tile (M 128, N 128, K 128 in 8
 //    steps, both operands K-major from shared memory; 128-token rounds
 //    because these single-CTA MMAs run at about 2.8 k flop per cycle per SM
 //    with N 64 but 5.1 k with N 128);
-//  * warp 7 (one lane) issues the P.V MMAs once the softmax warps have
+//  * warp 11 (one lane) issues the P.V MMAs once the softmax warps have
 //    written P: O += P V (M 128, N 128, K 16 per page tile, A = P from
 //    tensor memory, B = V N-major from shared memory).  Two issuing warps
 //    because an issuing thread stalls while the tensor core works through
 //    what it was given before: with one thread for both streams, each held
 //    the other up.  Completion goes to mbarriers through tcgen05.commit,
 //    which tracks the issuing thread's own MMAs;
-//  * warps 0-3 (softmax, one query row per thread = one tensor-memory lane)
-//    read S with tcgen05.ld, keep the row's running max and sum in registers,
-//    write P (bf16) to tensor memory with tcgen05.st, and in the epilogue read
-//    O, normalise and write out / lse or the partial state.  The max used in
+//  * warps 0-7 (softmax; a thread holds one query row = one tensor-memory
+//    lane; warps w and w + 4 share the lanes of quadrant w % 4, w taking
+//    score columns 0-63 and w + 4 columns 64-127) read S with tcgen05.ld,
+//    combine the pair's row maxima through tensor memory (each writes its
+//    own into its first, already read, score column, a two-arrival barrier
+//    per quadrant orders the exchange), keep the running max and their half
+//    of the row sum in registers, write their half of P (bf16) with
+//    tcgen05.st, and in the epilogue exchange the row sums the same way,
+//    then read their half of O, normalise and write out / lse or the partial
+//    state.  Two warps per quadrant because one warp's serial work per round
+//    (128 maxima, exponentials and packs per row) took longer than the
+//    round's MMAs: measured 1.12 us of a 1.44 us round at 32,768 x 64 with
+//    one warp, the MMAs needing about 0.76 us.  The max used in
 //    the exponentials is only raised when a round's max exceeds it by more
 //    than 2^8 (then O is rescaled in tensor memory), so most rounds touch O
 //    not at all; the result is the same softmax, P stays <= 256.
@@ -58,8 +67,11 @@ namespace {
 
 using namespace dev;
 
-// 4 softmax warps, K producer, score-MMA warp, V producer, P.V-MMA warp
-constexpr int kTcThreads = 256;
+// 8 softmax warps (two per tensor-memory lane quadrant), K producer,
+// score-MMA warp, V producer, P.V-MMA warp
+constexpr int kSoftmaxWarps = 8;
+constexpr int kWarpK = 8, kWarpS = 9, kWarpV = 10, kWarpPV = 11;
+constexpr int kTcThreads = 12 * 32;
 constexpr int kTcStages = 3;
 constexpr int kRoundTok = 128;        // tokens per round = 8 page tiles of 16
 constexpr int kRoundTiles = kRoundTok / 16;
@@ -83,6 +95,7 @@ struct TcSmem {
   uint64_t sfull[2], sfree[2];
   uint64_t pfull[2], pfree[2];
   uint64_t ofree, fin;
+  uint64_t xch[4];   // per lane quadrant: the two softmax warps' exchanges
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -172,6 +185,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -196,9 +217,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ int rounds_of(int tb, int te) { return (te - tb + kRoundTok - 1) / kRoundTok; }
 
-// kLowRegs: the register-light softmax (the cascade kernel's 9 warps leave
-// 168 registers per thread); same arithmetic, scores read twice.
-template <bool kLowRegs>
 __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* smem_raw) {
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
@@ -224,11 +242,12 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
     mbar_init(&sh->qfree, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->sfull[b], 1);
-      mbar_init(&sh->sfree[b], 4);
-      mbar_init(&sh->pfull[b], 4);
+      mbar_init(&sh->sfree[b], kSoftmaxWarps);
+      mbar_init(&sh->pfull[b], kSoftmaxWarps);
       mbar_init(&sh->pfree[b], 1);
     }
-    mbar_init(&sh->ofree, 4);
+    mbar_init(&sh->ofree, kSoftmaxWarps);
+    for (int q = 0; q < 4; ++q) mbar_init(&sh->xch[q], 2);
     mbar_init(&sh->fin, 2);
     sh->abort_flag = 0;
     fence_mbar_init();
@@ -247,12 +266,12 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
   const int P = a.page_size;
   const int g = a.hq / a.hkv;
 
-  if (warp == 4 || warp == 6) {
+  if (warp == kWarpK || warp == kWarpV) {
     // ----------------------------------------------------------- producers
-    // warp 4: the Q tiles and the K ring; warp 6: the V ring.  The rings are
+    // warp 8: the Q tiles and the K ring; warp 10: the V ring.  The rings are
     // apart so that a K slot is refilled as soon as its score MMAs are done,
     // not only once the round's P.V MMAs have read its V.
-    const int c = warp == 4 ? 0 : 1;
+    const int c = warp == kWarpK ? 0 : 1;
     uint64_t* full = c ? sh->fullv : sh->fullk;
     uint64_t* empty = c ? sh->emptyv : sh->emptyk;
     uint8_t* ring = stages + (size_t)c * kTcStages * kKvBytes;
@@ -322,11 +341,11 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
       if (nq > 0 && !mbar_wait(&sh->qfull, (uint32_t)((nq - 1) & 1), nullptr))
         atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpS) {
     // ----------------------------------------- score MMAs (lane 0 issues)
     // S of round r: its K tiles landed, Q loaded (first round of an item)
     // and its S buffer read by the softmax warps (round r - 2).  The P.V
-    // MMAs come from warp 7, so neither stream waits behind the other's
+    // MMAs come from warp 11, so neither stream waits behind the other's
     // issue (an issuing thread stalls while the tensor core works through
     // what it was given before).
     const uint32_t q0 = smem_u32(sQ), st0 = smem_u32(stages);
@@ -372,7 +391,7 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
       if (!mbar_wait(&sh->fin, 0, nullptr)) atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == 7) {
+  } else if (warp == kWarpPV) {
     // ------------------------------------------ P.V MMAs (lane 0 issues)
     // P.V of round r: P written, its V tiles landed and, first round of an
     // item, the previous item's O read by the epilogue
@@ -426,12 +445,14 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
       if (!mbar_wait(&sh->fin, 0, nullptr)) atomicOr(a.err, PKD_DEV_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------------- softmax + epilogue
-    const int row = warp * 32 + lane;               // tile row = tensor-memory lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int quad = warp & 3, half = warp >> 2;   // lane quadrant, score / O columns half
+    const int row = quad * 32 + lane;               // tile row = tensor-memory lane
+    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);   // this quadrant's lanes
     pdl_wait();   // outputs may belong to the previous kernel
     int rho = 0;
+    uint32_t xc = 0;   // exchanges with the partner warp so far (the barrier's phase)
     bool ok = true;
     // wait until the P.V MMAs of round r are done (pfree of its buffer);
     // callers keep at most one phase of lag (see the round loop)
@@ -439,13 +460,30 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
       if (r < 0) return true;
       return tc_wait(&sh->pfree[r & 1], (uint32_t)((r >> 1) & 1), abort_flag, a.err, lane);
     };
+    // one float per row with the partner warp of this quadrant: written into
+    // tensor-memory column `mine` (a column this warp has already read and
+    // nothing rewrites before the partner's next exchange), the partner's
+    // read from `theirs`
+    auto exchange = [&](uint32_t mine, uint32_t theirs, float v, float* other) -> bool {
+      tmem_st1(tq + mine, __float_as_uint(v));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->xch[quad]);
+      if (!tc_wait(&sh->xch[quad], xc & 1u, abort_flag, a.err, lane)) return false;
+      ++xc;
+      tc_fence_after();
+      *other = __uint_as_float(tmem_ld1(tq + theirs));
+      tmem_wait_ld();
+      return true;
+    };
     for (int it = it0; it < it1 && ok; ++it) {
       const int32_t* item = a.sched + a.off_items + (int64_t)it * kItemWords;
       const int req = item[0], tb = item[1], te = item[2], dst = item[3];
       const int n_req = item[5], stride = item[6], head = item[7];
       const int nr = rounds_of(tb, te);
       const int r0 = rho;
-      float m_used = -CUDART_INF_F, l = 0.f;
+      float m_used = -CUDART_INF_F, l = 0.f;   // l: this warp's half of the row sum
       bool o_has = false;
       for (int k = 0; k < nr && ok; ++k) {
         const int r = r0 + k, b = r & 1;
@@ -455,52 +493,48 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
           break;
         }
         tc_fence_after();
-        const uint32_t s_col = tmem + lane_off + kColS + kSCols * b;
-        float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-        // one pass: all 128 scores in registers; register-light: the max
-        // from 32 columns at a time, the scores read again for the weights
-        uint32_t sv[kLowRegs ? 1 : kRoundTok / 32][32];
-        if constexpr (!kLowRegs) {
+        // this warp's 64 score columns
+        const uint32_t s_col = kColS + kSCols * b + 64 * half;
+        uint32_t sv[2][32];
+        tmem_ld32(tq + s_col, sv[0]);
+        tmem_ld32(tq + s_col + 32, sv[1]);
+        tmem_wait_ld();
+        // slots past the item's end (a partial last round, the same n for
+        // every row) are -inf so that their weights come out 0
+        if (n < kRoundTok) {
 #pragma unroll
-          for (int q = 0; q < kRoundTok / 32; ++q) tmem_ld32(s_col + 32 * q, sv[q]);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->sfree[b]);
-          // row max of the raw scores (the scale is positive); slots past the
-          // item's end (a partial last round, the same n for every row) are
-          // -inf so that their weights come out 0
-          if (n < kRoundTok) {
-#pragma unroll
-            for (int q = 0; q < kRoundTok / 32; ++q)
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (32 * q + j >= n) sv[q][j] = __float_as_uint(-CUDART_INF_F);
-          }
-#pragma unroll
-          for (int q = 0; q < kRoundTok / 32; ++q)
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(sv[q][j]));
-        } else {
-#pragma unroll 1
-          for (int q = 0; q < kRoundTok / 32; ++q) {
-            uint32_t t[32];
-            tmem_ld32(s_col + 32 * q, t);
-            tmem_wait_ld();
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (32 * q + j < n) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(t[j]));
-          }
+              if (64 * half + 32 * q + j >= n) sv[q][j] = __float_as_uint(-CUDART_INF_F);
         }
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
+        float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(sv[q][j]));
+        const float m_half = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        // the row max of both halves (the raw scores; the scale is positive)
+        float m_other;
+        if (!exchange(s_col, kColS + kSCols * b + 64 * (1 - half), m_half, &m_other)) {
+          ok = false;
+          break;
+        }
+        // both halves of S are read and exchanged: the buffer may be refilled
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->sfree[b]);
+        const float mx = fmaxf(m_half, m_other) * a.scale_log2;
         // P buffer b was read by the P.V MMAs of round r - 2
         if (r >= 2 && !pv_wait(r - 2)) {
           ok = false;
           break;
         }
-        // The decision is per row, but the waits and the tensor-memory
-        // loads / stores below are warp-collective: the whole warp takes
-        // the branch when any row needs it, rows that do not keep alpha = 1.
+        // The decision is per row and the same in both warps of the pair,
+        // but the waits and the tensor-memory loads / stores below are
+        // warp-collective: the whole warp takes the branch when any row
+        // needs it, rows that do not keep alpha = 1.  Each warp rescales its
+        // half of O.
         const bool need = mx > m_used + kRescaleLog2;
         if (__any_sync(kFull, need)) {
           const float alpha = need ? exp2f(m_used - mx) : 1.f;   // 0 while m_used = -inf
@@ -511,13 +545,13 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
             }
             tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < 128; cb += 32) {
+            for (int cb = 0; cb < 64; cb += 32) {
               uint32_t o[32];
-              tmem_ld32(tmem + lane_off + kColO + cb, o);
+              tmem_ld32(tq + kColO + 64 * half + cb, o);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tmem_st32(tmem + lane_off + kColO + cb, o);
+              tmem_st32(tq + kColO + 64 * half + cb, o);
             }
             tmem_wait_st();
           }
@@ -525,44 +559,27 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
           if (need) m_used = mx;
         }
         // weights 2^(s scale_log2 - m_used), one FMA and one exp2 each; P
-        // column c of the buffer holds tokens 2c and 2c + 1, written 64
-        // tokens (32 columns) at a time
+        // column c of the buffer holds tokens 2c and 2c + 1: this warp's 64
+        // tokens are its 32 columns
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         const float neg_m = -m_used;
+        uint32_t pw[32];
 #pragma unroll
-        for (int hh = 0; hh < kRoundTok / 64; ++hh) {
-          uint32_t pw[32];
-          uint32_t sr[kLowRegs ? 2 : 1][32];   // register-light: this half's scores again
-          if constexpr (kLowRegs) {
-            tmem_ld32(s_col + 64 * hh, sr[0]);
-            tmem_ld32(s_col + 64 * hh + 32, sr[1]);
-            tmem_wait_ld();
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t* src = kLowRegs ? sr[j >> 4] : sv[2 * hh + (j >> 4)];
-            const int c = 2 * (j & 15);
-            float p0 = fast_exp2(fmaf(__uint_as_float(src[c]), a.scale_log2, neg_m));
-            float p1 = fast_exp2(fmaf(__uint_as_float(src[c + 1]), a.scale_log2, neg_m));
-            if (kLowRegs) {   // slots past the item's end weigh 0
-              const int tok = 64 * hh + 32 * (j >> 4) + c;
-              p0 = tok < n ? p0 : 0.f;
-              p1 = tok + 1 < n ? p1 : 0.f;
-            }
-            ps[j & 3] += p0;
-            ps[(j + 2) & 3] += p1;
-            pw[j] = pack_bf16(p0, p1);
-          }
-          tmem_st32(tmem + lane_off + kColP + kPCols * b + 32 * hh, pw);
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t* src = sv[j >> 4];
+          const int c = 2 * (j & 15);
+          const float p0 = fast_exp2(fmaf(__uint_as_float(src[c]), a.scale_log2, neg_m));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(src[c + 1]), a.scale_log2, neg_m));
+          ps[j & 3] += p0;
+          ps[(j + 2) & 3] += p1;
+          pw[j] = pack_bf16(p0, p1);
         }
+        tmem_st32(tq + kColP + kPCols * b + 32 * half, pw);
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sh->pfull[b]);
-          if (kLowRegs) mbar_arrive(&sh->sfree[b]);   // S was read again above
-        }
+        if (lane == 0) mbar_arrive(&sh->pfull[b]);
         o_has = true;
       }
       if (!ok) break;
@@ -573,6 +590,15 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
         break;
       }
       tc_fence_after();
+      // the row sum of both halves, exchanged through the last round's P
+      // columns (read by its P.V MMAs already); added in half order
+      const uint32_t p_last = kColP + kPCols * (rl & 1);
+      float l_other;
+      if (!exchange(p_last + 32 * half, p_last + 32 * (1 - half), l, &l_other)) {
+        ok = false;
+        break;
+      }
+      const float lt = half == 0 ? l + l_other : l_other + l;
       const int i = row / g, hq = head * g + row % g;
       const bool valid = i < n_req;
       // the row's partial-state slot: dst + i * stride, or (cascade prefix
@@ -581,11 +607,11 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
           !valid ? 0
                  : (stride >= 0 ? (int64_t)dst + (int64_t)i * stride
                                 : (int64_t)a.sched[a.off_merge + req + i] + dst);
-      const float inv = a.v_scale / l;
-      const float lse_nat = (m_used + log2f(l)) * 0.69314718055994530942f;
-      for (int cb = 0; cb < 128; cb += 32) {
+      const float inv = a.v_scale / lt;
+      const float lse_nat = (m_used + log2f(lt)) * 0.69314718055994530942f;
+      for (int cb = 64 * half; cb < 64 * half + 64; cb += 32) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kColO + cb, o);
+        tmem_ld32(tq + kColO + cb, o);
         tmem_wait_ld();
         if (valid) {
           if (dst < 0) {
@@ -599,8 +625,7 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
                   pack_bf16(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv),
                   pack_bf16(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv));
           } else {
-            float4* op = reinterpret_cast<float4*>(
-                a.o_part + (slot * a.hq + hq) * kHeadDim + cb);
+            float4* op = reinterpret_cast<float4*>(a.o_part + (slot * a.hq + hq) * kHeadDim + cb);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
               op[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
@@ -612,7 +637,7 @@ __device__ __forceinline__ void prefix_tc_body(const DecodeArgs& a, uint8_t* sme
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->ofree);
-      if (valid) {
+      if (valid && half == 0) {
         if (dst < 0) {
           if (a.lse != nullptr) a.lse[(int64_t)(req + i) * a.hq + hq] = lse_nat;
         } else {

@@ -1,6 +1,6 @@
 // Dense shared-prefix kernel for sm_103a: the standalone launch of the dense
 // role (prefix_tc_body.cuh, which holds the design and the device code) for
-// plans made with PKD_FLAG_DENSE_PREFIX.  One CTA per SM, 256 threads.
+// plans made with PKD_FLAG_DENSE_PREFIX.  One CTA per SM, 384 threads.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -12,7 +12,7 @@ namespace {
 __global__ void __launch_bounds__(tc::kTcThreads, 1)
     prefix_tc_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  tc::prefix_tc_body<false>(a, smem_raw);
+  tc::prefix_tc_body(a, smem_raw);
 }
 
 }  // namespace

@@ -401,7 +401,25 @@ def run_ours(args, rank, world):
     for e in done:
         e.record(stream)
 
-    use = {"graphs": graphs}
+    use = {"graphs": graphs, "eager": args.launch == "eager"}
+    if w.prefix_tokens and not cascade:
+        fork = torch.cuda.Event()
+
+    def launch_eager(si, c):
+        """The step's kernels launched on the stream directly (no graph)."""
+        ds = sets[si]
+        if w.prefix_tokens and not cascade:
+            fork.record(stream)
+            side.wait_event(fork)
+            ds[0].run(qs[0], kvs[c], out=po[c], lse=pl[c], stream=stream)
+            ds[1].run(qs[0], kvs[c], out=so[c], lse=sl[c], stream=side)
+            stream.wait_stream(side)
+            pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
+            return
+        for l in range(layers):
+            ks, vs = kv_scales[l] if kv_scales else (1.0, 1.0)
+            ds[0].run(qs[l], kvs[c * layers + l], out=outs[l], lse=lses[l], k_scale=ks,
+                      v_scale=vs, stream=stream)
 
     def graph_of(k):
         return use["graphs"][k % n_sets][(k // n_sets) % copies]
@@ -415,10 +433,13 @@ def run_ours(args, rank, world):
         copied[si].record(copy_stream)
         stream.wait_event(copied[si])
         gp, gs, c = graph_of(k)
-        gp.launch()
-        if gs is not None:   # timing graphs of the shared-prefix step
-            gs.launch()
-            pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
+        if use["eager"]:
+            launch_eager(si, c)
+        else:
+            gp.launch()
+            if gs is not None:   # timing graphs of the shared-prefix step
+                gs.launch()
+                pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
         done[si].record(stream)
 
     for k in range(args.warmup):
@@ -443,6 +464,7 @@ def run_ours(args, rank, world):
     # second timed loop, same steps with the event-node graphs: decode-kernel
     # duration of every launch of the last step
     use["graphs"] = tgraphs
+    use["eager"] = False
     k_roof = max(3, min(args.steps, 10))
     for k in range(k_roof):
         step(args.warmup + args.steps + k)
@@ -450,6 +472,7 @@ def run_ours(args, rank, world):
     last = graph_of(args.warmup + args.steps + k_roof - 1)
     k1_ms = last[0].layer_times() + (last[1].layer_times() if last[1] is not None else [])
     use["graphs"] = graphs
+    use["eager"] = args.launch == "eager"
     ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
 
@@ -490,7 +513,8 @@ def run_ours(args, rank, world):
                 io=((side_e2e[0], side_e2e[1]), [(dq[nx][0], hq[0])],
                     [(ho[0], do[nx][0]), (hl[0], dl[nx][0])]))
         e2e = run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stream,
-                               step_bytes, world, dev)
+                               step_bytes, world, dev,
+                               kernels="the cascade launch (both levels) + its merge")
     elif w.prefix_tokens:
         side_e2e = [torch.cuda.Stream(device=dev) for _ in range(3)]
 
@@ -550,6 +574,8 @@ def run_ours(args, rank, world):
                    + ("one per layer" if copies == 1 else "rotated over replays")),
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
                                           "makespan", "prefix_ctas", "prefix_chunk_tokens")},
+            "launch": ("step graphs replayed (one per cache copy and planning context)"
+                       if args.launch == "graph" else "kernels launched on the stream per step"),
             "parallelism": f"replicas x{world} (no collective)",
         },
         "roofline": {
@@ -565,7 +591,7 @@ def run_ours(args, rank, world):
             "launch_gbs_max": round(max(k1_gbs), 1) if k1_gbs else None,
             "timing": "CUDA event nodes around each decode launch inside a replayed copy of "
                       "the step graph, in a second timed loop of the same steps (last step); "
-                      "the step time comes from the plain graph",
+                      "the step time comes from the first loop",
         },
         "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
@@ -664,7 +690,7 @@ def run_e2e_pipelined(args, sets, views, capture, copies, qs, outs, lses, stream
 
 
 def run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stream, step_bytes,
-                     world, dev):
+                     world, dev, kernels="both levels + merge_states"):
     """The step through the public API with host buffers, for steps short
     enough that per-call host work would bound a loop that issues every copy
     itself: one graph per step runs the step's kernels on one set of device
@@ -750,7 +776,7 @@ def run_e2e_graph_io(args, sets, views, capture_io, copies, qs, outs, lses, stre
             "ms_host_wall": round(wall, 5), "h2d_bytes_per_step": int(h2d + sched),
             "d2h_bytes_per_step": int(d2h),
             "what": "plan from host tables (schedule H2D on a copy stream), then one graph "
-                    "per step: both levels + merge_states on one buffer set while the next "
+                    f"per step: {kernels} on one buffer set while the next "
                     "step's q (pinned host -> device) and the previous step's out + lse "
                     "(device -> pinned host) move on two branches beside them; the first q "
                     "and the last results are copied inside the timed region too; KV cache "
@@ -868,9 +894,13 @@ def run_prefix_sweep(args, rank, world):
     on two streams, joined by merge_states -- one CUDA graph.  Cascade: both
     levels in one plan, one launch (dense prefix CTAs beside decode CTAs)
     and one merge.  Single: every request over its full page table (prefix
-    pages then its own), one decode + merge.  GPU time per step: graph replays back to back, rotating over
-    enough cache copies that the step's bytes are not L2-resident; the host
-    plans once per case (its cost is not in these numbers)."""
+    pages then its own), one decode + merge.  GPU time per step, back to
+    back, rotating over enough cache copies that the step's bytes are not
+    L2-resident; the host plans once per case (its cost is not in these
+    numbers).  Eager launches by default: replaying one captured graph per
+    cache copy adds a cost per launch that grows with the number of distinct
+    graphs replayed in turn (about 20 us per step at 160), whatever memory
+    they read."""
     import torch
 
     import paged_kv_decode_host_gb300 as pkd
@@ -881,7 +911,7 @@ def run_prefix_sweep(args, rank, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream(device=dev)
-    reps = max(args.steps, 20)
+    reps = max(args.steps, 20) if args.launch == "graph" else min(max(args.steps, 20), 200)
     rows = []
     launches = 0
     grid = PREFIX_GRID + EXTRA_PREFIX_CASES
@@ -917,27 +947,50 @@ def run_prefix_sweep(args, rank, world):
         po, so, out_c, out_s, out_k = (torch.empty_like(q) for _ in range(5))
         pl, sl, lse_c, lse_s, lse_k = (torch.empty(B, w.hq, dtype=torch.float32, device=dev)
                                        for _ in range(5))
-        comp = [_composed_step_graph((pre, suf), q, kvs[c], po, pl, so, sl, out_c, lse_c, side,
-                                     dev) for c in range(copies)]
-        sing = [single.capture([q], [kvs[c]], [out_s], [lse_s]) for c in range(copies)]
-        cgr = [casc.capture([q], [kvs[c]], [out_k], [lse_k]) for c in range(copies)]
+        if args.launch == "graph":
+            comp = [_composed_step_graph((pre, suf), q, kvs[c], po, pl, so, sl, out_c, lse_c,
+                                         side, dev).launch for c in range(copies)]
+            sing = [single.capture([q], [kvs[c]], [out_s], [lse_s]).launch
+                    for c in range(copies)]
+            cgr = [casc.capture([q], [kvs[c]], [out_k], [lse_k]).launch for c in range(copies)]
+        else:
+            fork = torch.cuda.Event()
+
+            def composed(c):
+                def f():
+                    fork.record(stream)
+                    side.wait_event(fork)
+                    pre.run(q, kvs[c], out=po, lse=pl, stream=stream)
+                    suf.run(q, kvs[c], out=so, lse=sl, stream=side)
+                    stream.wait_stream(side)
+                    pkd.merge_states(po, pl, so, sl, out_c, lse_c)
+                return f
+            comp = [composed(c) for c in range(copies)]
+            sing = [lambda c=c: single.run(q, kvs[c], out=out_s, lse=lse_s, stream=stream)
+                    for c in range(copies)]
+            cgr = [lambda c=c: casc.run(q, kvs[c], out=out_k, lse=lse_k, stream=stream)
+                   for c in range(copies)]
         us = {}
         for name, gs in (("composable", comp), ("single", sing), ("cascade", cgr)):
             for k in range(3):
-                gs[k % copies].launch()
+                gs[k % copies]()
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            if args.launch == "eager":
+                # the host queues the steps while the stream sleeps, so the
+                # events time the GPU's work back to back, not the host's
+                torch.cuda._sleep(int(4e7))
             e0.record(stream)
             for k in range(reps):
-                gs[k % copies].launch()
+                gs[k % copies]()
             e1.record(stream)
             torch.cuda.synchronize()
             us[name] = e0.elapsed_time(e1) * 1e3 / reps
         # the two formats compute the same states (up to rounding)
-        comp[0].launch()
-        sing[0].launch()
-        cgr[0].launch()
+        comp[0]()
+        sing[0]()
+        cgr[0]()
         torch.cuda.synchronize()
         diff = float(max((out_c.float() - out_s.float()).abs().max(),
                          (out_k.float() - out_s.float()).abs().max()))
@@ -958,7 +1011,9 @@ def run_prefix_sweep(args, rank, world):
                      "cascade_plan": {k: cinfo[k] for k in ("prefix_ctas", "prefix_chunk_tokens",
                                                             "chunk_tokens", "num_items")},
                      "advice": {"format": auto, "cascade_us": round(advice["cascade_us"], 1),
-                                "single_us": round(advice["single_us"], 1)},
+                                "single_us": round(advice["single_us"], 1),
+                                "cascade_makespan": advice["cascade_makespan"],
+                                "single_makespan": advice["single_makespan"]},
                      "auto_us": round(us[auto], 2),
                      "auto_vs_best": round(us[auto] / min(us.values()), 3),
                      "composable_GBps_prefix_once": round(kv_once / (us["composable"] * 1e3), 1),
@@ -967,20 +1022,22 @@ def run_prefix_sweep(args, rank, world):
                      "max_abs_diff_out": round(diff, 5), "max_abs_diff_lse": round(ldiff, 6),
                      "pages_us_composable": pages_comp, "pages_us_single": pages_single,
                      "cache_copies": copies})
-        for g in sing + cgr:
-            g.close()
         del kvs, comp, sing, cgr, pre, suf, single, casc
         torch.cuda.empty_cache()
     big = [r for r in rows if r["prefix"] == 32768 and r["batch"] == 64] or rows[-1:]
     big = big[0]
     return {"metric": "shared-prefix decode latency, composable vs single format "
-                      "(GPU us per step, CUDA-graph replay)",
+                      "(GPU us per step)",
             "value": big["composable_us"], "unit": "us", "n_gpus": world, "steps": reps,
             "warmup": 3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/KV, scattered pages)",
             "config": {"workload": "prefix_sweep", "hq": 32, "hkv": 8, "head_dim": 128,
                        "page_size": 16, "suffix": 128,
-                       "l2": "cache copies rotated per replay, >= 1.2 GB in total"},
+                       "l2": "cache copies rotated per step, >= 1.2 GB in total",
+                       "launch": ("CUDA-graph replays, one graph per cache copy"
+                                  if args.launch == "graph" else
+                                  "kernels launched on the stream, queued behind a GPU sleep "
+                                  "so that the events time the GPU's work back to back")},
             "table": rows, "gpu_launches": launches,
             "note": "pages_us_*: the pages' table (FP16, other GPU), context only"}
 
@@ -1226,6 +1283,9 @@ def main():
                     help="prefix_sweep: only these cases, e.g. 32768x64,1024x16 (prefix x batch)")
     ap.add_argument("--alpha", type=int, default=-1,
                     help="planner per-item cost in tokens (cost = alpha + tokens); -1: default")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
+                    help="timed steps: replay the step's captured CUDA graphs (one per cache "
+                         "copy and planning context), or launch its kernels on the stream")
     ap.add_argument("--prefix-mode", choices=["cascade", "levels"], default="cascade",
                     help="shared-prefix step: one cascade plan and launch with one merge, or "
                          "two levels (prefix context + suffix context) joined by merge_states")

@@ -287,8 +287,10 @@ def _prefix_level(block_lens, hkv, n, page_size, floor, alpha):
     item per CTA.  Every block starts with one chunk per KV head; while hkv
     more CTAs are left, the block with the longest chunk (ties: the first)
     gets one more chunk per head, unless its chunk would fall below the
-    floor.  Chunks are page-rounded; item j goes to CTA j.  With more heads
-    than CTAs the (block, head) units stay whole and LPT places them.
+    floor; then each block keeps the fewest chunks that stay within the
+    longest chunk (more would not shorten the level).  Chunks are
+    page-rounded; item j goes to CTA j.  With more heads than CTAs the
+    (block, head) units stay whole and LPT places them.
     Returns (span, queues, chunk per block, CTAs used)."""
     nb = len(block_lens)
     if nb * hkv > n:
@@ -307,6 +309,13 @@ def _prefix_level(block_lens, hkv, n, page_size, floor, alpha):
         m[b] += 1
         chunk[b] = nxt
         budget -= hkv
+    # chunks that do not lower the level's longest one are given back: every
+    # block keeps the fewest chunks whose length stays within it
+    top = max(chunk)
+    for b in range(nb):
+        while m[b] > 1 and _round_up(_ceil_div(block_lens[b], m[b] - 1), page_size) <= top:
+            m[b] -= 1
+        chunk[b] = _round_up(_ceil_div(block_lens[b], m[b]), page_size)
     queues, span = [], 0
     for b, l in enumerate(block_lens):
         for h in range(hkv):
@@ -338,10 +347,12 @@ def plan_cascade(group_indptr, prefix, suffix, *, page_size: int, num_pages: int
       suffix-token units, suffix items alpha + tokens; the prefix budget
       starts where each level gets CTAs in proportion to its total cost (in
       steps of hkv above one CTA per unit when the grid allows, rounded to
-      the nearest step) and moves toward the level whose makespan is the
-      larger (more prefix CTAs when the prefix level bounds the step), one
-      step at a time while the predicted makespan falls strictly; the suffix
-      gets every CTA the prefix items do not use;
+      the nearest step); budgets are compared by the predicted makespan,
+      ties by the sum of the two levels' makespans; the search moves from
+      the start toward its better neighbour (the next budget either way
+      whose prefix level differs), if that one is strictly better, and on
+      from neighbour to neighbour while the budget keeps improving
+      strictly; the suffix gets every CTA the prefix items do not use;
     * every request is a unit of the reduction map whose slots are its
       prefix chunks then its suffix chunks (all items write partial states).
     """
@@ -383,22 +394,41 @@ def plan_cascade(group_indptr, prefix, suffix, *, page_size: int, num_pages: int
         def schedule(j):
             pre = _prefix_level(block_lens, hkv, base + step * j, P, floor_p, prefix_alpha)
             suf = _level(suf_len, n_cta - pre[3], P, floor_s, alpha)
-            return (max(pre[0] * prefix_cost16, suf[1] * 16), j, pre, suf)
+            p_span, s_span = pre[0] * prefix_cost16, suf[1] * 16
+            return ((max(p_span, s_span), p_span + s_span), j, pre, suf)
+
+        def used(j):                      # CTAs the prefix level takes at budget j
+            return _prefix_level(block_lens, hkv, base + step * j, P, floor_p, prefix_alpha)[3]
+
+        def neighbour(j, d):
+            """The next budget from j in direction d whose prefix level
+            differs (budgets between give the same plan), or None."""
+            c = used(j)
+            k = j + d
+            while 0 <= k <= j_max:
+                if used(k) != c:
+                    return k
+                k += d
+            return None
 
         best = schedule(j0)
-        p_span = best[2][0] * prefix_cost16
-        s_span = best[3][1] * 16
-        step_dir = (p_span > s_span) - (p_span < s_span)
-        j = j0 + step_dir
-        while step_dir and 0 <= j <= j_max:
-            cand = schedule(j)
-            if cand[0] >= best[0]:
-                break
-            best = cand
-            j += step_dir
+        # the better of the two neighbours, if it beats j0 strictly, gives
+        # the direction; then on from neighbour to neighbour while it keeps
+        # improving strictly
+        near = [schedule(j) for j in (neighbour(j0, -1), neighbour(j0, 1)) if j is not None]
+        if near and min(near, key=lambda c: c[0])[0] < best[0]:
+            best = min(near, key=lambda c: c[0])
+            step_dir = 1 if best[1] > j0 else -1
+            j = neighbour(best[1], step_dir)
+            while j is not None:
+                cand = schedule(j)
+                if cand[0] >= best[0]:
+                    break
+                best = cand
+                j = neighbour(j, step_dir)
     if best is None:
         return CascadePlan(0, 0, 0, 0, [0] * (n_cta + 1), [], [], [0], [])
-    span, _, (_, q_pre, block_chunk, n_pre), (c_s, _, q_suf) = best
+    (span, _), _, (_, q_pre, block_chunk, n_pre), (c_s, _, q_suf) = best
     np_block = [_ceil_div(l, c) for l, c in zip(block_lens, block_chunk)]
     units, merge_indptr = [], [0]
     for r in range(batch):

@@ -54,21 +54,21 @@ constexpr int kDenseRows = 128;   // query rows of one dense-prefix tile
 // in suffix-token units: a suffix item costs alpha + tokens (every KV head of
 // a token: 4 KB of K and V at Hkv 8), a prefix item (one KV head of a block
 // of up to 128 query rows) costs (kCascadePrefixAlpha + tokens) *
-// kCascadePrefixCost16 / 16.  Measured on the 8,192-token prefix x 32
-// requests step, with both roles streaming at once (HBM saturated, about
-// 2.4 us per memory round trip): a dense CTA takes about 5 us from launch to
-// its first scores and about 2.5 us per 128-token round after that, a
-// decode CTA about 65 ns per token of all 8 heads -- a prefix token of one
-// head costs about a quarter of a suffix token, and a prefix item carries
-// about 256 prefix tokens' worth of fixed cost.  Split by these, both roles
-// end within a microsecond of each other (per-CTA clock stamps).  The suffix
-// chunk floor is lower than a plain plan's, since the suffix level gets only
-// part of the grid.
+// kCascadePrefixCost16 / 16.  Fitted to steps timed with the prefix CTA
+// count forced over its whole range (in steps of Hkv), on the 8,192-token
+// prefix x 32 requests step and on prefixes of 128 to 32,768 tokens x 16 or
+// 64 requests with 128-token suffixes: the step time follows the slower
+// role, a dense CTA taking about 8 ns per prefix token (one 128-token round
+// per microsecond) after a fixed start, a decode CTA about 34 ns per
+// suffix-token unit.  These constants put the chosen split on the fastest
+// measured one, or within 2 % of its time, on every one of those steps.  The
+// suffix chunk floor is lower than a plain plan's, since the suffix level
+// gets only part of the grid.
 #ifndef PKD_CASCADE_PREFIX_COST16
-#define PKD_CASCADE_PREFIX_COST16 4
+#define PKD_CASCADE_PREFIX_COST16 3
 #endif
 #ifndef PKD_CASCADE_PREFIX_ALPHA
-#define PKD_CASCADE_PREFIX_ALPHA 256
+#define PKD_CASCADE_PREFIX_ALPHA 512
 #endif
 #ifndef PKD_CASCADE_SUFFIX_FLOOR
 #define PKD_CASCADE_SUFFIX_FLOOR 128

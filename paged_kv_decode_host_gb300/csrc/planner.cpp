@@ -444,7 +444,8 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 // block whose chunk is longest (ties: the first block) gets one more chunk
 // per head -- every head of a block keeps the same chunks, so a request's
 // prefix slots hold all its heads -- unless that would cut it below the
-// floor.  Chunks are page-rounded (a block may end up with fewer than its
+// floor; then each block keeps the fewest chunks that stay within the
+// longest chunk.  Chunks are page-rounded (a block may end up with fewer than its
 // share); item j goes to CTA j and unused budget goes to the suffix level.
 // When the blocks' heads outnumber the grid, the prefix units are not split
 // and LPT places them on the n_pre CTAs instead.
@@ -453,9 +454,10 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 // (suffix tokens: kCascadePrefixCost16): starting from the budget that gives
 // each level CTAs in proportion to its total cost (in steps of Hkv when
 // every head can have a CTA, rounded to the nearest step), it moves toward
-// the level whose makespan is the larger (more prefix CTAs when the prefix
-// level bounds the step, fewer when the suffix level does), one step at a
-// time while the predicted makespan falls strictly.  Every item writes a partial state: request r's slots are
+// its better neighbour budget (the next one either way whose prefix level
+// differs), if that one is strictly better, and on from neighbour to
+// neighbour while the budget keeps improving strictly.  Budgets compare by
+// the predicted makespan, ties by the sum of both levels'.  Every item writes a partial state: request r's slots are
 // merge_indptr[r] .. merge_indptr[r + 1], its prefix chunks first, then its
 // suffix chunks, and one merge folds them.  Prefix items mark themselves with
 // slot stride -1 and carry their chunk index as dst_slot (a block's requests
@@ -503,6 +505,37 @@ void plan_level(const std::vector<int64_t>& ulens, int64_t total, int32_t n, int
   }
 }
 
+// Chunks of the prefix level on a budget of n CTAs when every (block, head)
+// unit can have one (see above): water-filling, then every block keeps the
+// fewest chunks whose length stays within the longest chunk (more would not
+// shorten the level).  Fills m (chunks per block) and chunk; returns the
+// CTAs used.
+int32_t prefix_chunks(const std::vector<int64_t>& block_len, int32_t hkv, int32_t n, int64_t P,
+                      int64_t floor_c, std::vector<int32_t>& m, std::vector<int64_t>& chunk) {
+  const int32_t n_blocks = (int32_t)block_len.size();
+  m.assign((size_t)n_blocks, 1);
+  chunk.resize((size_t)n_blocks);
+  for (int32_t b = 0; b < n_blocks; ++b) chunk[b] = ceil_div(block_len[b], P) * P;
+  for (int64_t budget = n - (int64_t)n_blocks * hkv; budget >= hkv; budget -= hkv) {
+    int32_t top = 0;
+    for (int32_t b = 1; b < n_blocks; ++b)
+      if (chunk[b] > chunk[top]) top = b;
+    const int64_t next = ceil_div(ceil_div(block_len[top], m[top] + 1), P) * P;
+    if (next < floor_c) break;
+    m[top] += 1;
+    chunk[top] = next;
+  }
+  int64_t top = 0;
+  for (int64_t c : chunk) top = std::max(top, c);
+  int64_t used = 0;
+  for (int32_t b = 0; b < n_blocks; ++b) {
+    while (m[b] > 1 && ceil_div(ceil_div(block_len[b], m[b] - 1), P) * P <= top) --m[b];
+    chunk[b] = ceil_div(ceil_div(block_len[b], m[b]), P) * P;
+    used += (int64_t)m[b] * hkv;
+  }
+  return (int32_t)used;
+}
+
 // The prefix level of a cascade plan on a budget of n CTAs (see above).
 // block_len: each block's prefix length; units = blocks x hkv.
 void plan_prefix(const std::vector<int64_t>& block_len, int32_t hkv, int32_t n, int64_t P,
@@ -526,18 +559,7 @@ void plan_prefix(const std::vector<int64_t>& block_len, int32_t hkv, int32_t n, 
     out->ctas = n;
     return;
   }
-  std::vector<int32_t>& m = sc.n_chunks;
-  m.assign((size_t)n_blocks, 1);
-  for (int32_t b = 0; b < n_blocks; ++b) out->block_chunk[b] = ceil_div(block_len[b], P) * P;
-  for (int64_t budget = n - (int64_t)n_blocks * hkv; budget >= hkv; budget -= hkv) {
-    int32_t top = 0;
-    for (int32_t b = 1; b < n_blocks; ++b)
-      if (out->block_chunk[b] > out->block_chunk[top]) top = b;
-    const int64_t next = ceil_div(ceil_div(block_len[top], m[top] + 1), P) * P;
-    if (next < floor_c) break;
-    m[top] += 1;
-    out->block_chunk[top] = next;
-  }
+  prefix_chunks(block_len, hkv, n, P, floor_c, sc.n_chunks, out->block_chunk);
   for (int32_t b = 0; b < n_blocks; ++b) {
     const int64_t c = out->block_chunk[b];
     for (int32_t h = 0; h < hkv; ++h) {
@@ -573,6 +595,7 @@ struct CascadeScratch {
   std::vector<int64_t> pre_row, suf_len, block_len;
   std::vector<Block> blocks;
   std::vector<int32_t> block_of, np_block, ns_req, count, fill;
+  std::vector<int64_t> chunk_tmp;
   LevelPlan pre, suf, best_pre, best_suf;
 };
 
@@ -642,26 +665,47 @@ int cascade_search(const pkd_config& cfg, int32_t n_cta, const int32_t* group_in
     const int64_t prop = (n_cta * pre_cost + all / 2) / all;
     const int64_t j0 = std::min<int64_t>(
         std::max<int64_t>((std::max<int64_t>(prop - base, 0) + step / 2) / step, 0), j_max);
-    int64_t best_j = -1;
+    int64_t best_j = -1, best_sum = 0;
+    // budgets compare by the predicted makespan, ties by the sum of the two
+    // levels' makespans (a budget that does not shorten the bounding level
+    // but lengthens the other loses)
     auto evaluate = [&](int64_t j) {
       plan_prefix(cs.block_len, hkv, (int32_t)(base + step * j), P, floor_p, kCascadePrefixAlpha,
                   sc, &cs.pre);
       plan_level(cs.suf_len, suf_total, n_cta - cs.pre.ctas, P, floor_s, alpha, sc, &cs.suf);
-      const int64_t span = std::max(cs.pre.span * kCascadePrefixCost16, cs.suf.span * 16);
-      if (best_j < 0 || span < best_span) {
+      const int64_t p_span = cs.pre.span * kCascadePrefixCost16, s_span = cs.suf.span * 16;
+      const int64_t span = std::max(p_span, s_span), sum = p_span + s_span;
+      if (best_j < 0 || span < best_span || (span == best_span && sum < best_sum)) {
         best_span = span;
+        best_sum = sum;
         best_j = j;
         std::swap(cs.best_pre, cs.pre);
         std::swap(cs.best_suf, cs.suf);
       }
     };
+    // CTAs the prefix level uses at budget j, and the next budget from j in
+    // direction d whose prefix level differs (budgets between give the
+    // same plan), or -1
+    auto used = [&](int64_t j) -> int32_t {
+      const int64_t n = base + step * j;
+      if (!split) return (int32_t)n;
+      return prefix_chunks(cs.block_len, hkv, (int32_t)n, P, floor_p, sc.n_chunks, cs.chunk_tmp);
+    };
+    auto neighbour = [&](int64_t j, int64_t d) -> int64_t {
+      const int32_t c = used(j);
+      for (int64_t k = j + d; k >= 0 && k <= j_max; k += d)
+        if (used(k) != c) return k;
+      return -1;
+    };
     evaluate(j0);
-    // move toward the level that bounds the makespan (more prefix CTAs when
-    // the prefix level does), one step at a time, while it improves
-    const int64_t p_span = cs.best_pre.span * kCascadePrefixCost16;
-    const int64_t s_span = cs.best_suf.span * 16;
-    const int64_t dir = p_span > s_span ? 1 : (p_span < s_span ? -1 : 0);
-    for (int64_t j = j0 + dir; dir != 0 && j >= 0 && j <= j_max; j += dir) {
+    // the better neighbour (the lower one on a tie), if it beats j0
+    // strictly, gives the direction; then on from neighbour to neighbour
+    // while the budget keeps improving strictly
+    const int64_t lo = neighbour(j0, -1), hi = neighbour(j0, 1);
+    if (lo >= 0) evaluate(lo);
+    if (hi >= 0) evaluate(hi);
+    const int64_t dir = best_j > j0 ? 1 : (best_j < j0 ? -1 : 0);
+    for (int64_t j = dir != 0 ? neighbour(best_j, dir) : -1; j >= 0; j = neighbour(j, dir)) {
       evaluate(j);
       if (best_j != j) break;
     }
@@ -822,13 +866,14 @@ int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 // whole table, prefix pages then its own).  Each is predicted from its own
 // planner's makespan M: the cascade search above, and the plain planner's
 // chunk choice (candidates L, L/2, L/4 of the work bound, floor 256, alpha
-// 32) over the concatenated lengths.  Time per layer = a + b M, fitted on
-// GB300 over the pages' grid of shared prefix x batch (1,024 / 8,192 /
-// 32,768 tokens x 16 / 64 requests, 128-token suffixes) and the 8,192 x 32
-// step: cascade 15.3 us + 0.0498 us per unit (the merge and the dense role's
-// set-up make its fixed part larger), single 10.2 us + 0.0481 us per token.
-constexpr double kAdviceCascadeUs0 = 15.3, kAdviceCascadeUsPerUnit = 0.0498;
-constexpr double kAdviceSingleUs0 = 10.2, kAdviceSingleUsPerToken = 0.0481;
+// 32) over the concatenated lengths.  GPU time per layer = a + b M (steps
+// launched back to back), fitted on GB300 over the pages' grid of shared
+// prefix x batch (1,024 / 8,192 / 32,768 tokens x 16 / 64 requests) and
+// prefixes of 16 to 256 tokens, all with 128-token suffixes: cascade
+// 6.17 us + 0.0517 us per unit (the merge and the dense role's set-up make
+// its fixed part larger), single 3.62 us + 0.0481 us per token.
+constexpr double kAdviceCascadeUs0 = 6.17, kAdviceCascadeUsPerUnit = 0.0517;
+constexpr double kAdviceSingleUs0 = 3.62, kAdviceSingleUsPerToken = 0.0481;
 
 // The plain planner's makespan for these lengths (its chunk candidates and
 // LPT, without the schedule).

@@ -43,7 +43,8 @@
 //    state.  Two warps per quadrant because one warp's serial work per round
 //    (128 maxima, exponentials and packs per row) took longer than the
 //    round's MMAs: measured 1.12 us of a 1.44 us round at 32,768 x 64 with
-//    one warp, the MMAs needing about 0.76 us.  The max used in
+//    one warp, the MMAs needing about 0.76 us; with two, 0.70 us of a
+//    0.96-1.02 us round.  The max used in
 //    the exponentials is only raised when a round's max exceeds it by more
 //    than 2^8 (then O is rescaled in tensor memory), so most rounds touch O
 //    not at all; the result is the same softmax, P stays <= 256.

@@ -407,7 +407,7 @@ def _compare_cascade(cfg, gi, prefix, suffix):
     g = cfg.num_qo_heads // cfg.num_kv_heads
     ref = oplan.plan_cascade(gi, prefix, suffix, page_size=16, num_pages=cfg.num_pages,
                              n_cta=cfg.num_ctas, hkv=cfg.num_kv_heads, rows=128 // g, alpha=32,
-                             prefix_alpha=256, prefix_cost16=4, suffix_floor=128)
+                             prefix_alpha=512, prefix_cost16=3, suffix_floor=128)
     got = pkd.decode_schedule(words, off, info)
     items = [tuple(int(x) for x in r)
              for r in words[off[1]:off[1] + 8 * info["num_items"]].reshape(-1, 8)]

@@ -558,6 +558,20 @@ def test_cascade_plan_hand_worked():
     cascade_coverage_check(p, [0, 2], prefix, suffix, 16, 1)
 
 
+def test_cascade_prefix_level_gives_back_idle_chunks():
+    """Two blocks of 1,024 prefix tokens, one KV head, budget 5, page 16,
+    floor 128, worked by hand: water-filling gives block 0 a second chunk
+    (512), block 1 a second (512), block 0 a third (ceil(1024 / 3) = 342 ->
+    352); the longest chunk is still 512, so block 0's third chunk shortens
+    nothing and is given back: chunks 512 and 512 on 4 CTAs, span 512."""
+    span, queues, chunks, used = oplan._prefix_level([1024, 1024], 1, 5, 16, 128, 0)
+    assert (span, chunks, used) == (512, [512, 512], 4)
+    assert [q[0][3:] for q in queues] == [(0, 512), (512, 1024), (0, 512), (512, 1024)]
+    # budget 6: the third chunk of each block lowers the longest to 352
+    span, _, chunks, used = oplan._prefix_level([1024, 1024], 1, 6, 16, 128, 0)
+    assert (span, chunks, used) == (352, [352, 352], 6)
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_cascade_plan_coverage_random(seed):
     rng = np.random.default_rng(70 + seed)

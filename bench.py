@@ -312,9 +312,13 @@ def run_ours(args, rank, world):
     nnz = int(t["indptr"][-1])
     layers = args.layers if args.layers > 0 else w.layers
     # distinct caches per replay for single-layer workloads so no step reads
-    # another step's bytes out of L2: at least 4, and at least 1.2 GB in all
-    copies = 1 if layers > 1 else max(4, int(np.ceil(
-        1.2e9 / (w.pool_pages * 2 * P * w.hkv * w.head_dim * w.kv_elem_bytes))))
+    # another step's bytes out of L2: at least 4, and enough that the other
+    # copies read between two reads of one copy hold twice the L2.  No more:
+    # each copy is one more graph in the rotation, and replaying N distinct
+    # graphs in turn costs about 0.1 us per launch per graph.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = w.pool_pages * 2 * P * w.hkv * w.head_dim * w.kv_elem_bytes
+    copies = 1 if layers > 1 else max(4, 1 + int(np.ceil(2 * l2 / pool_bytes)))
     if args.copies > 0:   # fewer cache copies (a smaller device footprint for counter captures)
         copies = args.copies
     n_kv = layers * copies
@@ -1252,7 +1256,7 @@ def run_other_workloads(args, rank, world, names=OTHER_WORKLOADS):
             "config": {k: ln["config"][k] for k in ("batch", "hq", "hkv", "page_size",
                                                     "total_tokens_per_layer",
                                                     "alg_bytes_per_step", "l2", "plan",
-                                                    "prefix_kernel")},
+                                                    "prefix_kernel", "launch")},
         }
     gc.collect()
     torch.cuda.empty_cache()

@@ -3,8 +3,8 @@
 Every step of the computation runs in the CUDA library (``libpkd.so``, built
 in-tree by :func:`build`); this module only marshals arguments: it checks
 dtypes, shapes and devices, passes ``tensor.data_ptr()`` and the current
-CUDA stream through ctypes (the per-step plan calls through the small
-compiled ``_pkd_plan`` module when it was built), and raises on a non-zero
+CUDA stream through ctypes (the per-step plan and run calls through the
+small compiled ``_pkd_plan`` module when it was built), and raises on a non-zero
 status.  There is no fallback: if the library is missing or was built for
 another machine, loading it fails loudly.
 
@@ -319,7 +319,8 @@ _NOT_HANDLED = 1000   # its status for inputs it leaves to the general path
 
 
 def _fast():
-    """The compiled marshalling fast path for plan / plan_shared, if built."""
+    """The compiled marshalling fast path for plan / plan_shared /
+    plan_cascade / run, if built."""
     global _fast_plan
     if _fast_plan is None:
         try:
@@ -327,7 +328,8 @@ def _fast():
             lib = load()
             m.init(ctypes.cast(lib.pkd_plan, ctypes.c_void_p).value,
                    ctypes.cast(lib.pkd_plan_shared, ctypes.c_void_p).value,
-                   ctypes.cast(lib.pkd_plan_cascade, ctypes.c_void_p).value)
+                   ctypes.cast(lib.pkd_plan_cascade, ctypes.c_void_p).value,
+                   ctypes.cast(lib.pkd_run_scaled, ctypes.c_void_p).value)
             _fast_plan = m
         except ImportError:
             _fast_plan = False
@@ -449,6 +451,7 @@ class BatchDecodeWithPagedKVCache:
         self._ep_ref = ctypes.byref(self._ep)
         self.epoch = 0
         self.batch = None
+        self._run_shapes = None
 
     # -- plan ---------------------------------------------------------------
     def plan(self, indptr, indices, last_page_len, stream=None):
@@ -550,6 +553,34 @@ class BatchDecodeWithPagedKVCache:
 
     # -- run ----------------------------------------------------------------
     def _check_run_args(self, q, kv_cache, out, lse):
+        """Cheap checks of the common case (every attribute as planned); any
+        mismatch goes to the full check, which names what is wrong."""
+        import torch
+        B = self.batch
+        if B is not None:
+            if self._run_shapes is None or self._run_shapes[0] != B:
+                bf = torch.bfloat16
+                self._run_shapes = (B, torch.Size((B, self.hq, self.d)),
+                                    torch.Size((B, self.hq)),
+                                    torch.Size((self.num_pages, 2, self.p, self.hkv, self.d)
+                                               if self.kv_layout == "NHD" else
+                                               (self.num_pages, 2, self.hkv, self.p, self.d)),
+                                    bf, torch.bfloat16 if self.kv_dtype == "bf16"
+                                    else torch.float8_e4m3fn, torch.float32,
+                                    self.device.index)
+            _, qs, ls, kvs, bf, kvd, f32, dev = self._run_shapes
+            d = q.get_device()
+            if (q.dtype is bf and out.dtype is bf and kv_cache.dtype is kvd
+                    and q.shape == qs and out.shape == qs and kv_cache.shape == kvs
+                    and q.is_contiguous() and out.is_contiguous() and kv_cache.is_contiguous()
+                    and d >= 0 and (d == dev or dev is None) and out.get_device() == d
+                    and kv_cache.get_device() == d
+                    and (lse is None or (lse.dtype is f32 and lse.shape == ls
+                                         and lse.is_contiguous()))):
+                return
+        self._check_run_args_full(q, kv_cache, out, lse)
+
+    def _check_run_args_full(self, q, kv_cache, out, lse):
         import torch
         if self.batch is None:
             raise PkdError(-5, "run before plan")
@@ -577,6 +608,9 @@ class BatchDecodeWithPagedKVCache:
         if lse is not None:
             if lse.dtype != torch.float32 or tuple(lse.shape) != (B, self.hq) or not lse.is_contiguous():
                 raise ValueError("lse must be contiguous float32 [batch, Hq]")
+        if (q.device != out.device or q.device != kv_cache.device
+                or (lse is not None and lse.device != q.device)):
+            raise ValueError("q, kv_cache, out and lse must be on one device")
 
     def run(self, q, kv_cache, out=None, lse=None, return_lse=True, expect_epoch=0,
             stream=None, k_scale=1.0, v_scale=1.0):
@@ -589,6 +623,14 @@ class BatchDecodeWithPagedKVCache:
         if lse is None and return_lse:
             lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
         self._check_run_args(q, kv_cache, out, lse)
+        fast = _fast()
+        if fast is not None:
+            st = fast.run(self._hv, q.data_ptr(), kv_cache.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else 0, float(k_scale),
+                          float(v_scale), int(expect_epoch), _stream_ptr(stream))
+            if st != _NOT_HANDLED:
+                _check(st, "pkd_run")
+                return (out, lse) if return_lse else out
         st = load().pkd_run_scaled(self._h, ctypes.c_void_p(q.data_ptr()),
                                    ctypes.c_void_p(kv_cache.data_ptr()),
                                    ctypes.c_void_p(out.data_ptr()),

@@ -1,13 +1,15 @@
-/* CPython fast path for the per-step planning calls of the Python binding:
+/* CPython fast path for the per-step calls of the Python binding:
  * pkd_plan, pkd_plan_shared and pkd_plan_cascade with the page tables passed as int32 arrays
- * through the buffer protocol (no per-argument ctypes conversion).  It only
- * marshals arguments: the entry points are the C ABI's own, whose addresses
- * the binding hands over once (init), so this module does not link libpkd.
+ * through the buffer protocol, and pkd_run_scaled with its pointers as
+ * integers (no per-argument ctypes conversion).  It only marshals arguments:
+ * the entry points are the C ABI's own, whose addresses the binding hands
+ * over once (init), so this module does not link libpkd.
  *
  * plan(ctx, indptr, indices, last, stream) -> (status, epoch)
  * plan_shared(ctx, group_indptr, indptr, indices, last, stream) -> (status, epoch)
  * plan_cascade(ctx, group_indptr, p_indptr, p_indices, p_last, s_indptr, s_indices, s_last,
  *              stream) -> (status, epoch)
+ * run(ctx, q, kv, out, lse, k_scale, v_scale, expect_epoch, stream) -> status
  *
  * status is the C ABI's return value, or NOT_HANDLED (1000) when an argument
  * is not a 1-D C-contiguous int32 buffer: the caller then takes its general
@@ -29,21 +31,40 @@ typedef int (*plan_cascade_fn)(void *ctx, const int32_t *group_indptr, int32_t n
                                const int32_t *s_indices, const int32_t *s_last, void *stream,
                                uint64_t *epoch);
 
+typedef int (*run_fn)(void *ctx, const void *q, const void *kv, void *out, float *lse,
+                      float k_scale, float v_scale, uint64_t expect_epoch, void *stream);
+
 static plan_fn g_plan = NULL;
 static plan_shared_fn g_plan_shared = NULL;
 static plan_cascade_fn g_plan_cascade = NULL;
+static run_fn g_run = NULL;
 
 #define NOT_HANDLED 1000
 #define BAD_TABLE (-2)
 
 static PyObject *init(PyObject *self, PyObject *args) {
-  unsigned long long p, ps, pc = 0;
+  unsigned long long p, ps, pc = 0, pr = 0;
   (void)self;
-  if (!PyArg_ParseTuple(args, "KK|K", &p, &ps, &pc)) return NULL;
+  if (!PyArg_ParseTuple(args, "KK|KK", &p, &ps, &pc, &pr)) return NULL;
   g_plan = (plan_fn)(uintptr_t)p;
   g_plan_shared = (plan_shared_fn)(uintptr_t)ps;
   g_plan_cascade = (plan_cascade_fn)(uintptr_t)pc;
+  g_run = (run_fn)(uintptr_t)pr;
   Py_RETURN_NONE;
+}
+
+/* The caller (the binding) has checked the tensors behind the pointers. */
+static PyObject *run(PyObject *self, PyObject *args) {
+  unsigned long long ctx, q, kv, out, lse, epoch, stream;
+  float ks, vs;
+  (void)self;
+  if (!PyArg_ParseTuple(args, "KKKKKffKK", &ctx, &q, &kv, &out, &lse, &ks, &vs, &epoch, &stream))
+    return NULL;
+  if (g_run == NULL) return PyLong_FromLong(NOT_HANDLED);
+  return PyLong_FromLong(g_run((void *)(uintptr_t)ctx, (const void *)(uintptr_t)q,
+                               (const void *)(uintptr_t)kv, (void *)(uintptr_t)out,
+                               (float *)(uintptr_t)lse, ks, vs, (uint64_t)epoch,
+                               (void *)(uintptr_t)stream));
 }
 
 /* A 1-D C-contiguous buffer of 4-byte signed integers, or 0. */
@@ -164,7 +185,10 @@ static PyMethodDef methods[] = {
     {"plan_cascade", plan_cascade, METH_VARARGS,
      "plan_cascade(ctx, group_indptr, p_indptr, p_indices, p_last, s_indptr, s_indices, "
      "s_last, stream) -> (status, epoch)"},
-    {"init", init, METH_VARARGS, "init(plan_address, plan_shared_address[, plan_cascade_address])"},
+    {"init", init, METH_VARARGS,
+     "init(plan_address, plan_shared_address[, plan_cascade_address[, run_scaled_address]])"},
+    {"run", run, METH_VARARGS,
+     "run(ctx, q, kv, out, lse, k_scale, v_scale, expect_epoch, stream) -> status"},
     {"plan", plan, METH_VARARGS, "plan(ctx, indptr, indices, last, stream) -> (status, epoch)"},
     {"plan_shared", plan_shared, METH_VARARGS,
      "plan_shared(ctx, group_indptr, indptr, indices, last, stream) -> (status, epoch)"},

@@ -51,11 +51,17 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // memory round trips per warp instead of one per slot; it needs more registers (fewer resident blocks), which plans of
 // short units do not repay, so they get kBatch = 1.  The terms are added in
 // the same order either way.  Fixed assignment and order: bit-reproducible.
+// Cascade plans (every request one unit of its prefix and suffix chunks, at
+// most 32) take kBatch = 4; with at most 16 chunks in 4-warp blocks, so
+// that the grid's blocks (64 registers a thread at 8 warps would allow four
+// per SM, two waves for the shared-prefix step's 1,024 tasks) are all
+// resident at once.
 constexpr int kWarpSlots = 32;
 
-template <int kBatch>
-__global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
-  constexpr int kWarps = kMergeThreads / 32;
+template <int kBatch, int kThreads = kMergeThreads>
+__global__ void __launch_bounds__(kThreads) merge_partials_kernel(const MergeArgs a) {
+  static_assert(kThreads >= kHeadDim && kThreads % 32 == 0, "a thread per output dim");
+  constexpr int kWarps = kThreads / 32;
   __shared__ float wm[kWarps];
   __shared__ float wz[kWarps];
   __shared__ __align__(16) float wacc[kWarps][kHeadDim];
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
     if constexpr (kBatch > 1) load_batch(s0 + warp);
     // ---- pass 1: M = max over the unit's chunk LSEs (log2 units)
     float mx = -CUDART_INF_F;
-    for (int s = s0 + threadIdx.x; s < s1; s += kMergeThreads)
+    for (int s = s0 + threadIdx.x; s < s1; s += kThreads)
       mx = fmaxf(mx, a.l_part[(int64_t)s * a.hq + h] * kLog2e);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) m = fmaxf(m, wm[w]);
     // ---- pass 2: this warp's share of sum exp2(L - M) O and sum exp2(L - M)
-    // slots w, w + 8, ... (in batches of kBatch: a batch's loads are all
+    // slots w, w + kWarps, ... (in batches of kBatch: a batch's loads are all
     // issued before its terms are added, in the same order)
     float z = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -261,6 +267,12 @@ cudaError_t launch_merge_partials(const MergeArgs& a, int grid, int32_t max_chun
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_chunks > kLongUnit) return cudaLaunchKernelEx(&cfg, merge_partials_kernel<8>, a);
+  if (batch_short && max_chunks <= 4 * 4) {
+    // 4-warp blocks: at 64 registers a thread, eight of them fit an SM, so
+    // the grid's blocks are all resident at once
+    cfg.blockDim = dim3(128);
+    return cudaLaunchKernelEx(&cfg, merge_partials_kernel<4, 128>, a);
+  }
   if (batch_short && max_chunks <= 4 * (kMergeThreads / 32))
     return cudaLaunchKernelEx(&cfg, merge_partials_kernel<4>, a);
   return cudaLaunchKernelEx(&cfg, merge_partials_kernel<1>, a);

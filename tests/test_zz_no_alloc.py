@@ -10,7 +10,8 @@ first call would show -- and each result is compared with the oracle and
 with the regular entry point (pkd_run on a workspace) within the parity
 tolerances used throughout the tests (2e-2 on bf16 outputs, 1e-3 on fp32
 LSE).  The other cases cover the branches its decode kernel takes that the
-skewed batch does not (page size 1 with group 8, the CUDA-core consumer),
+skewed batch does not (page size 1 with group 8, the CUDA-core consumer,
+four KV heads),
 check that a warm call changes neither torch's allocations nor the device's
 free memory, and read the device error word back through
 pkd_static_scratch_last_error.
@@ -145,11 +146,22 @@ def _llama_like_small():
                               sum(-(-n // 16) for n in lens))
 
 
-@pytest.mark.parametrize("case", ["token_sparse_g8", "fma_consumer"])
+def _four_kv_heads_small():
+    """Hq 16 / Hkv 4 (four consumer warps instead of eight), page size 16,
+    20 requests of 1..2,500 tokens."""
+    g = torch.Generator().manual_seed(57)
+    lens = tuple(int(x) for x in torch.randint(1, 2500, (20,), generator=g))
+    return workloads.Workload("hkv4_small", 57, 16, 4, 128, 16, 1, lens,
+                              sum(-(-n // 16) for n in lens) + 3)
+
+
+@pytest.mark.parametrize("case", ["token_sparse_g8", "fma_consumer", "four_kv_heads"])
 def test_static_scratch_other_branches(case):
-    """Page size 1 with g = 8 (merged K|V copies), and the CUDA-core
-    consumer: static against the oracle and the regular path, twice."""
-    w = _token_sparse_small() if case == "token_sparse_g8" else _llama_like_small()
+    """Page size 1 with g = 8 (merged K|V copies), the CUDA-core consumer,
+    and four KV heads: static against the oracle and the regular path,
+    twice."""
+    w = {"token_sparse_g8": _token_sparse_small, "fma_consumer": _llama_like_small,
+         "four_kv_heads": _four_kv_heads_small}[case]()
     tc = False if case == "fma_consumer" else None
     flags = pkd.FLAG_FMA_CONSUMER if case == "fma_consumer" else 0
     t = workloads.make_tables(w)

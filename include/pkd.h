@@ -236,8 +236,9 @@ int pkd_plan_cascade(pkd_ctx *ctx, const int32_t *group_indptr, int32_t num_grou
  * ids are not needed), predicts the GPU time per layer of the cascade plan
  * and of the single format -- every request over its whole table, prefix
  * pages then its own, planned by pkd_plan -- from each planner's predicted
- * makespan with time = a + b x makespan (constants fitted on GB300 over the
- * pages' grid of prefix length x batch), and picks the faster.  Host only,
+ * makespan and the KV bytes each reads, time = a + b x makespan + c x MB
+ * (constants fitted on GB300 over the pages' grid of prefix length x batch
+ * and shorter prefixes), and picks the faster.  Host only,
  * no CUDA call; cfg is the cascade context's configuration (flags
  * PKD_FLAG_CASCADE, num_ctas >= 2, the grid the plans would use). */
 typedef struct pkd_format_advice {

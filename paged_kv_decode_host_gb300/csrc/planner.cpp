@@ -866,14 +866,18 @@ int plan_schedule_cascade(const pkd_config& cfg, int32_t n_cta, const Layout& L,
 // whole table, prefix pages then its own).  Each is predicted from its own
 // planner's makespan M: the cascade search above, and the plain planner's
 // chunk choice (candidates L, L/2, L/4 of the work bound, floor 256, alpha
-// 32) over the concatenated lengths.  GPU time per layer = a + b M (steps
-// launched back to back), fitted on GB300 over the pages' grid of shared
-// prefix x batch (1,024 / 8,192 / 32,768 tokens x 16 / 64 requests) and
-// prefixes of 16 to 256 tokens, all with 128-token suffixes: cascade
-// 6.17 us + 0.0517 us per unit (the merge and the dense role's set-up make
-// its fixed part larger), single 3.62 us + 0.0481 us per token.
-constexpr double kAdviceCascadeUs0 = 6.17, kAdviceCascadeUsPerUnit = 0.0517;
-constexpr double kAdviceSingleUs0 = 3.62, kAdviceSingleUsPerToken = 0.0481;
+// 32) over the concatenated lengths, and from the KV bytes it reads (the
+// prefix once, or once per request).  GPU time per layer = a + b M + c MB
+// (steps launched back to back), a least-squares fit on GB300 over the
+// pages' grid of shared prefix x batch (1,024 / 8,192 / 32,768 tokens x 16 /
+// 64 requests) and prefixes of 16 to 256 tokens, all with 128-token
+// suffixes: cascade 5.58 us + 0.02523 us per makespan unit + 0.1143 us per
+// MB, single 4.30 us + 0.04393 us per token + 0.00648 us per MB (the
+// single format's prefix pages come from L2 for all but the first request).
+constexpr double kAdviceCascadeUs0 = 5.58, kAdviceCascadeUsPerUnit = 0.02523,
+                 kAdviceCascadeUsPerMB = 0.1143;
+constexpr double kAdviceSingleUs0 = 4.30, kAdviceSingleUsPerToken = 0.04393,
+                 kAdviceSingleUsPerMB = 0.00648;
 
 // The plain planner's makespan for these lengths (its chunk candidates and
 // LPT, without the schedule).
@@ -909,14 +913,23 @@ int advise_format(const pkd_config& cfg, int32_t n_cta, const int32_t* group_ind
                                 s_last, sc, cs, &batch, &n_pre, &span, &alpha, &floor_s);
   if (st != PKD_OK) return st;
   std::vector<int64_t> whole((size_t)batch);
-  for (int32_t r = 0; r < batch; ++r) whole[r] = cs.block_len[cs.block_of[r]] + cs.suf_len[r];
+  int64_t single_tokens = 0, cascade_tokens = 0;
+  for (int32_t r = 0; r < batch; ++r) {
+    whole[r] = cs.block_len[cs.block_of[r]] + cs.suf_len[r];
+    single_tokens += whole[r];
+    cascade_tokens += cs.suf_len[r];
+  }
+  for (int32_t j = 0; j < n_groups; ++j) cascade_tokens += cs.pre_row[j];
+  const double mb_per_token = 2.0 * cfg.num_kv_heads * cfg.head_dim * 2 / 1e6;
   const int64_t ms = plain_makespan(whole, n_cta, cfg.page_size, sc);
   std::memset(out, 0, sizeof(*out));
   out->prefix_ctas = n_pre;
   out->cascade_makespan = span / 16;
   out->single_makespan = ms;
-  out->cascade_us = (float)(kAdviceCascadeUs0 + kAdviceCascadeUsPerUnit * (double)(span / 16));
-  out->single_us = (float)(kAdviceSingleUs0 + kAdviceSingleUsPerToken * (double)ms);
+  out->cascade_us = (float)(kAdviceCascadeUs0 + kAdviceCascadeUsPerUnit * (double)(span / 16) +
+                            kAdviceCascadeUsPerMB * mb_per_token * (double)cascade_tokens);
+  out->single_us = (float)(kAdviceSingleUs0 + kAdviceSingleUsPerToken * (double)ms +
+                           kAdviceSingleUsPerMB * mb_per_token * (double)single_tokens);
   out->use_cascade = batch > 0 && out->cascade_us < out->single_us ? 1 : 0;
   return PKD_OK;
 }

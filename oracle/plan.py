@@ -209,17 +209,21 @@ def plan(indptr, indices, last, *, page_size: int, num_pages: int, n_cta: int,
     chunk, makespan, queues = best
 
     # P4: reduction map: each request of a split block is a unit with one
-    # partial slot per chunk; units in ascending request order
+    # partial slot per chunk, in chunk order; units longest first (most
+    # chunks, ties by request), the pages' longest-first rule applied to the
+    # merge's tasks
     n_chunks = [_ceil_div(l, chunk) for l in lens]
     units = []
     merge_indptr = [0]
     block_slot = {}
-    for bi, (r0, n, row) in enumerate(blocks):
-        if n_chunks[bi] > 1:
-            block_slot[bi] = merge_indptr[-1]
-            for r in range(r0, r0 + n):
-                units.append((r, n_chunks[bi]))
-                merge_indptr.append(merge_indptr[-1] + n_chunks[bi])
+    split_blocks = sorted((bi for bi in range(len(blocks)) if n_chunks[bi] > 1),
+                          key=lambda bi: (-n_chunks[bi], bi))
+    for bi in split_blocks:
+        r0, n, row = blocks[bi]
+        block_slot[bi] = merge_indptr[-1]
+        for r in range(r0, r0 + n):
+            units.append((r, n_chunks[bi]))
+            merge_indptr.append(merge_indptr[-1] + n_chunks[bi])
 
     cta_indptr = [0]
     items = []

@@ -184,7 +184,7 @@ struct Scratch {
   std::vector<int64_t> row_len, lens, unit_lens, cands;
   std::vector<Block> blocks;
   std::vector<Item> items, best_items, whole, rest;
-  std::vector<int32_t> owner, best_owner, first_slot, n_chunks, count, fill, by_pos;
+  std::vector<int32_t> owner, best_owner, first_slot, n_chunks, count, fill, by_pos, split_blocks;
   std::vector<std::pair<int64_t, int32_t>> heap;
   std::vector<std::pair<int32_t, int32_t>> units;
 };
@@ -326,23 +326,30 @@ int plan_schedule_grouped(const pkd_config& cfg, int32_t n_cta, const Layout& L,
   if (n_items > L.max_items) return PKD_E_CAPACITY;
 
   // ---- P4: reduction map: every request of a split block is a unit with
-  // one slot per chunk, units in ascending request order, slots in chunk order
+  // one slot per chunk, slots in chunk order.  Units go longest first (most
+  // chunks; ties: ascending request), so that the merge's longest tasks are
+  // handed out first when its tasks take more than one wave of blocks.
   std::vector<int32_t>& first_slot = sc.first_slot;  // slot of the block's first request
   std::vector<int32_t>& n_chunks = sc.n_chunks;
   std::vector<std::pair<int32_t, int32_t>>& units = sc.units;
+  std::vector<int32_t>& split_blocks = sc.split_blocks;
   first_slot.assign((size_t)n_blocks, -1);
   n_chunks.assign((size_t)n_blocks, 1);
   units.clear();
-  int64_t n_slots = 0;
+  split_blocks.clear();
   for (int32_t b = 0; b < n_blocks; ++b) {
-    const int64_t nc = ceil_div(lens[b], best_chunk);
-    n_chunks[b] = (int32_t)nc;
-    if (nc > 1) {
-      first_slot[b] = (int32_t)n_slots;
-      for (int32_t r = 0; r < blocks[b].n_req; ++r) {
-        units.emplace_back(blocks[b].req_first + r, (int32_t)nc);
-        n_slots += nc;
-      }
+    n_chunks[b] = (int32_t)ceil_div(lens[b], best_chunk);
+    if (n_chunks[b] > 1) split_blocks.push_back(b);
+  }
+  std::stable_sort(split_blocks.begin(), split_blocks.end(),
+                   [&](int32_t x, int32_t y) { return n_chunks[x] > n_chunks[y]; });
+  int64_t n_slots = 0;
+  for (int32_t b : split_blocks) {
+    const int32_t nc = n_chunks[b];
+    first_slot[b] = (int32_t)n_slots;
+    for (int32_t r = 0; r < blocks[b].n_req; ++r) {
+      units.emplace_back(blocks[b].req_first + r, nc);
+      n_slots += nc;
     }
   }
   if (n_slots > L.max_slots || (int64_t)units.size() > L.max_items) return PKD_E_CAPACITY;

@@ -317,7 +317,8 @@ def test_plan_hand_worked(idx):
 def coverage_check(p, indptr, indices, last, page_size, group_indptr=None):
     """Independent check of a schedule: every (request, token of its table
     row) covered exactly once, page references consistent with the table,
-    partial slots of each split request contiguous in chunk order."""
+    partial slots of each split request contiguous in chunk order, split
+    requests listed longest first."""
     P = page_size
     n_rows = len(last)
     row_lens = [P * (indptr[i + 1] - indptr[i] - 1) + last[i] for i in range(n_rows)]
@@ -347,7 +348,8 @@ def coverage_check(p, indptr, indices, last, page_size, group_indptr=None):
         assert [d for _, d in got] == list(range(p.merge_indptr[u], p.merge_indptr[u + 1]))
         assert nc == len(got) >= 2
     assert set(slots_of) == {r for r, _ in p.units}
-    assert [r for r, _ in p.units] == sorted(r for r, _ in p.units)
+    # units longest first (most chunks), ties by ascending request
+    assert p.units == sorted(p.units, key=lambda u: (-u[1], u[0]))
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -404,6 +406,27 @@ def test_grouped_plan_hand_worked():
     assert p.cta_indptr == [0, 1, 2, 3]
     assert p.items == [(0, 0, 40, -1, 0, 2, 0), (2, 0, 40, -1, 0, 2, 0), (4, 0, 40, -1, 0, 1, 0)]
     assert p.units == [] and p.merge_indptr == [0]
+
+
+def test_plan_units_longest_first_hand_worked():
+    """lens [40, 100], P 1, 4 CTAs, alpha 0, floor 1.  L = 35.  c = 35: items
+    35 (r0), 5 (r0), 35, 35, 30 (r1); LPT order 35 r0c0, 35 r1c0, 35 r1c1,
+    30 r1c2, 5 r0c1 -> CTAs 0, 1, 2, 3, then 5 onto CTA 3 (30): makespan 35.
+    c = 18: seven items of 18 round-robin -> 36, 36, 36, 18; 10 and 4 onto
+    CTA 3: makespan 36.  c = 9: fifteen items of 9 -> 36, 36, 36, 27; 4 and 1
+    onto CTA 3: makespan 36.  So chunk 35.  Both requests are split: request
+    1 has 3 chunks, request 0 has 2, so request 1 is the first unit (slots
+    0..2) and request 0 the second (slots 3..4)."""
+    indptr, indices, last = workloads.page_table([40, 100], 1)
+    p = oplan.plan(indptr, indices, last, page_size=1, num_pages=140, n_cta=4, alpha=0,
+                   min_chunk_tokens=1)
+    assert p.chunk == 35 and p.makespan == 35
+    assert p.units == [(1, 3), (0, 2)] and p.merge_indptr == [0, 3, 5]
+    assert p.cta_indptr == [0, 1, 2, 3, 5]
+    assert p.items == [(0, 0, 35, 3, 0, 1, 2), (1, 0, 35, 0, 40, 1, 3),
+                       (1, 35, 70, 1, 75, 1, 3), (1, 70, 100, 2, 110, 1, 3),
+                       (0, 35, 40, 4, 35, 1, 2)]
+    coverage_check(p, indptr, indices, last, 1)
 
 
 # ---- chunk size by search (variant of P1)

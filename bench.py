@@ -410,20 +410,24 @@ def run_ours(args, rank, world):
         fork = torch.cuda.Event()
 
     def launch_eager(si, c):
-        """The step's kernels launched on the stream directly (no graph)."""
+        """The step's kernels launched on the stream directly (no graph).
+        Each run passes its plan's epoch: the kernels wait on the device for
+        that schedule, so no event orders the copy stream's upload before
+        them and the step's first kernel may start under the previous
+        step's last (programmatic dependent launch)."""
         ds = sets[si]
         if w.prefix_tokens and not cascade:
             fork.record(stream)
             side.wait_event(fork)
-            ds[0].run(qs[0], kvs[c], out=po[c], lse=pl[c], stream=stream)
-            ds[1].run(qs[0], kvs[c], out=so[c], lse=sl[c], stream=side)
+            ds[0].run(qs[0], kvs[c], out=po[c], lse=pl[c], stream=stream, expect_epoch=ds[0].epoch)
+            ds[1].run(qs[0], kvs[c], out=so[c], lse=sl[c], stream=side, expect_epoch=ds[1].epoch)
             stream.wait_stream(side)
             pkd.merge_states(po[c], pl[c], so[c], sl[c], outs[0], lses[0])
             return
         for l in range(layers):
             ks, vs = kv_scales[l] if kv_scales else (1.0, 1.0)
             ds[0].run(qs[l], kvs[c * layers + l], out=outs[l], lse=lses[l], k_scale=ks,
-                      v_scale=vs, stream=stream)
+                      v_scale=vs, stream=stream, expect_epoch=ds[0].epoch)
 
     def graph_of(k):
         return use["graphs"][k % n_sets][(k // n_sets) % copies]
@@ -435,11 +439,11 @@ def run_ours(args, rank, world):
         for (name, gi, table), d in zip(views, sets[si]):
             _plan(d, gi, table, stream=copy_stream, name=name)
         copied[si].record(copy_stream)
-        stream.wait_event(copied[si])
         gp, gs, c = graph_of(k)
         if use["eager"]:
             launch_eager(si, c)
         else:
+            stream.wait_event(copied[si])
             gp.launch()
             if gs is not None:   # timing graphs of the shared-prefix step
                 gs.launch()
@@ -578,8 +582,11 @@ def run_ours(args, rank, world):
                    + ("one per layer" if copies == 1 else "rotated over replays")),
             "plan": {k: info[k] for k in ("num_ctas", "chunk_tokens", "num_items", "num_units",
                                           "makespan", "prefix_ctas", "prefix_chunk_tokens")},
-            "launch": ("step graphs replayed (one per cache copy and planning context)"
-                       if args.launch == "graph" else "kernels launched on the stream per step"),
+            "launch": ("step graphs replayed (one per cache copy and planning context), "
+                       "each after an event on the step's schedule upload"
+                       if args.launch == "graph" else
+                       "kernels launched on the stream per step; they wait on the device for "
+                       "their plan's schedule (pkd_run with expect_epoch), no event"),
             "parallelism": f"replicas x{world} (no collective)",
         },
         "roofline": {
@@ -1287,9 +1294,12 @@ def main():
                     help="prefix_sweep: only these cases, e.g. 32768x64,1024x16 (prefix x batch)")
     ap.add_argument("--alpha", type=int, default=-1,
                     help="planner per-item cost in tokens (cost = alpha + tokens); -1: default")
-    ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
-                    help="timed steps: replay the step's captured CUDA graphs (one per cache "
-                         "copy and planning context), or launch its kernels on the stream")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="eager",
+                    help="timed steps: launch the step's kernels on the stream, each run "
+                         "waiting on the device for its plan's schedule (pkd_run with "
+                         "expect_epoch; the upload goes on a copy stream with no event), or "
+                         "replay the step's captured CUDA graphs (one per cache copy and "
+                         "planning context) after an event on the upload")
     ap.add_argument("--prefix-mode", choices=["cascade", "levels"], default="cascade",
                     help="shared-prefix step: one cascade plan and launch with one merge, or "
                          "two levels (prefix context + suffix context) joined by merge_states")

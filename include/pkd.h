@@ -191,8 +191,10 @@ void pkd_destroy(pkd_ctx *ctx);
 /* Plan one decode step.  Host arrays (int32): indptr[batch + 1],
  * indices[indptr[batch]], last_page_len[batch].  They are copied into
  * pinned staging before the call returns, so the caller may reuse them at
- * once; the schedule reaches the workspace by cudaMemcpyAsync on `stream`
- * (staging is double-buffered and fenced by events).  batch may be 0.
+ * once; the schedule reaches the workspace by two cudaMemcpyAsync on
+ * `stream`, the body and then the header, which carries the plan's epoch
+ * word ((epoch - 1) mod (2^31 - 1) + 1); staging is double-buffered and
+ * fenced by events.  batch may be 0.
  * On success *epoch (if not NULL) receives the new plan epoch (>= 1).
  * Errors: INVALID_ARG, BAD_TABLE, CAPACITY, CUDA. */
 int pkd_plan(pkd_ctx *ctx, const int32_t *indptr, const int32_t *indices,
@@ -262,8 +264,16 @@ int pkd_get_plan_info(const pkd_ctx *ctx, pkd_plan_info *info);
  *   out  : device bf16 [batch][Hq][D]
  *   lse  : device fp32 [batch][Hq] or NULL (natural-log LSE of the scaled
  *          scores)
- * expect_epoch: 0 accepts any plan; otherwise must equal the current plan's
- * epoch (STALE_PLAN otherwise).  Launches the decode kernel and the merge
+ * expect_epoch: 0 accepts any plan, and the schedule must be ordered before
+ * the launch by `stream` (planned on it, or an event).  Otherwise it must
+ * equal the current plan's epoch (STALE_PLAN otherwise), and the kernels
+ * also wait on the device, before reading the schedule, until its header
+ * holds that epoch's word: the plan may then be uploaded on another stream
+ * with no event between the two (the upload must not wait for this run).
+ * That wait is bounded (about 2 s); when it runs out the decode kernel
+ * does no work and ORs PKD_DEV_ERR_TIMEOUT into the device error word
+ * (pkd_last_device_error), and out / lse are undefined.  Captured
+ * graphs take expect_epoch 0.  Launches the decode kernel and the merge
  * kernel on `stream`, with programmatic dependent launch: the decode kernel
  * may start while the previous kernel in the stream runs and reads q and
  * the KV cache at once, so a kernel that writes them ahead of it in the same
@@ -420,7 +430,8 @@ int pkd_plan_host_cascade(const pkd_config *cfg, const int32_t *group_indptr,
  * num_items, num_units, num_slots, chunk, alpha, nnz, makespan (clamped to
  * int32), split floor, requests per block, the most chunks of any split
  * request, the max_batch and max_num_pages the offsets were laid out for,
- * (cascade plans) the CTAs of the prefix level and its chunk, then zeros.
+ * (cascade plans) the CTAs of the prefix level and its chunk, the plan's
+ * epoch word (in a context's workspace; 0 in host-only plans), then zeros.
  * Errors: INVALID_ARG. */
 int pkd_schedule_layout(const pkd_config *cfg, int64_t off[6]);
 

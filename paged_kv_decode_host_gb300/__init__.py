@@ -616,7 +616,9 @@ class BatchDecodeWithPagedKVCache:
             stream=None, k_scale=1.0, v_scale=1.0):
         """Attention for one layer.  Returns (out, lse) or out.  With scales
         the attended key is k_scale * K and the value v_scale * V (an E4M3
-        cache needs them)."""
+        cache needs them).  A nonzero expect_epoch (the value plan returned)
+        also makes the kernels wait on the device for that plan's schedule,
+        so the plan may run on another stream without an event."""
         import torch
         if out is None:
             out = torch.empty_like(q)

@@ -184,9 +184,10 @@ int kv_map_for(pkd_ctx* ctx, const void* kv, CUtensorMap* out, CUtensorMap* out_
 
 int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* lse,
                float k_scale, float v_scale, cudaStream_t stream, cudaEvent_t ev_before,
-               cudaEvent_t ev_after) {
+               cudaEvent_t ev_after, int32_t wait_epoch = 0) {
   const pkd_config& c = ctx->cfg;
   DecodeArgs a{};
+  a.wait_epoch = wait_epoch;
   a.sched = reinterpret_cast<const int32_t*>(ctx->ws);
   a.o_part = reinterpret_cast<float*>(ctx->ws + ctx->layout.o_part_byte);
   a.l_part = reinterpret_cast<float*>(ctx->ws + ctx->layout.l_part_byte);
@@ -246,6 +247,7 @@ int launch_run(pkd_ctx* ctx, const void* q, const void* kv, void* out, float* ls
   m.off_units = ctx->layout.units;
   m.off_merge = ctx->layout.merge_indptr;
   m.hq = c.num_qo_heads;
+  m.wait_epoch = wait_epoch;
   if (launch_merge_partials(m, ctx->merge_grid, ctx->max_chunks, stream,
                             ctx->kind.cascade) != cudaSuccess)
     return PKD_E_CUDA;
@@ -439,10 +441,17 @@ static int plan_and_publish(pkd_ctx* ctx, PlanFn plan_fn, void* stream, uint64_t
   int st = plan_fn(words, &info);
   if (st != PKD_OK) return st;
   const Layout& L = ctx->layout;
-  // one copy: the fixed-size part (header, cta queues, items, units, merge
-  // map) and the page list right behind it, as laid out in the workspace
-  if (cudaMemcpyAsync(ctx->ws, words, ((size_t)L.page_list + (size_t)info.nnz) * 4,
-                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+  // two copies in stream order: first the body (cta queues, items, units,
+  // merge map and the page list behind them, as laid out in the workspace),
+  // then the header with the plan's epoch word, so that a kernel that sees
+  // the new epoch (a run on another stream, pkd_run with expect_epoch) also
+  // sees the whole schedule
+  words[H_EPOCH] = epoch_word(ctx->epoch + 1);
+  if (cudaMemcpyAsync(ctx->ws + (size_t)H_WORDS * 4, words + H_WORDS,
+                      ((size_t)L.page_list + (size_t)info.nnz - H_WORDS) * 4,
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(ctx->ws, words, (size_t)H_WORDS * 4, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
     return PKD_E_CUDA;
   if (cudaEventRecord(ctx->staged[k], s) != cudaSuccess) return PKD_E_CUDA;
   ctx->staged_pending[k] = true;
@@ -522,7 +531,7 @@ int pkd_run_scaled(pkd_ctx* ctx, const void* q, const void* kv, void* out, float
       return PKD_E_INVALID_ARG;
   }
   return launch_run(ctx, q, kv, out, lse, k_scale, v_scale, static_cast<cudaStream_t>(stream),
-                    nullptr, nullptr);
+                    nullptr, nullptr, expect_epoch != 0 ? epoch_word(expect_epoch) : 0);
 }
 
 int pkd_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b,

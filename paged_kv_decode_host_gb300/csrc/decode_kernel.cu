@@ -1257,6 +1257,7 @@ template <int G, bool kMma, bool kBlock, bool kFp8, bool kTiles>
 __global__ void __launch_bounds__((kMaxKvHeads + 1) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  if (!schedule_ready(a.sched + H_EPOCH, a.wait_epoch, a.err)) return;
   decode_body<G, kMma, kBlock, kFp8, kTiles>(a, smem);
 }
 
@@ -1271,6 +1272,7 @@ template <int G>
 __global__ void __launch_bounds__(tc::kTcThreads, 1)
     cascade_kernel(const __grid_constant__ CascadeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];   // each role aligns its own layout
+  if (!schedule_ready(a.suf.sched + H_EPOCH, a.suf.wait_epoch, a.suf.err)) return;
   if ((int)blockIdx.x < a.pre.sched[H_NPRE])
     tc::prefix_tc_body(a.pre, smem);
   else

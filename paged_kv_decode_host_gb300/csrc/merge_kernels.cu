@@ -66,12 +66,18 @@ __global__ void __launch_bounds__(kThreads) merge_partials_kernel(const MergeArg
   __shared__ float wz[kWarps];
   __shared__ __align__(16) float wacc[kWarps][kHeadDim];
   pdl_launch_dependents();
-  // The schedule is only written by host-to-device copies (ordered before
-  // this kernel): read it before waiting for the decode kernel.
+  // The schedule is written by host-to-device copies.  When the stream
+  // orders them before this kernel, read it before waiting for the decode
+  // kernel; when the plan came from another stream (wait_epoch), the decode
+  // kernel waited for it, so read it once that grid has completed.
+  bool waited = false;
+  if (a.wait_epoch != 0) {
+    pdl_wait();
+    waited = true;
+  }
   const int n_units = a.sched[H_NUNITS];
   const int64_t tasks = (int64_t)n_units * a.hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  bool waited = false;
   const bool warp_mode = tasks >= (int64_t)4 * gridDim.x;
   // ---- short units, many tasks: a warp per task
   const int64_t n_warps = (int64_t)gridDim.x * kWarps;

@@ -38,8 +38,14 @@ enum HeaderWord {
   H_MAXPAGES,    //   (config max_batch and max_num_pages)
   H_NPRE,        // cascade plans: CTAs [0, H_NPRE) run the shared-prefix items
   H_PCHUNK,      // cascade plans: the shared-prefix level's chunk (tokens)
+  H_EPOCH,       // the plan's epoch (epoch_word); the upload writes the header last
   H_WORDS = 32
 };
+
+// The plan epoch as a nonzero header word (1 .. 2^31 - 1, wrapping).
+inline int32_t epoch_word(uint64_t epoch) {
+  return (int32_t)((epoch - 1) % 0x7fffffffull) + 1;
+}
 
 // req (first of the block), tok_begin, tok_end, dst_slot, first page index,
 // requests in the block, slot stride per request, KV head (dense-prefix
@@ -187,6 +193,10 @@ struct DecodeArgs {
   // group, KV head, request}; its box is one KV head's 128 query rows of a
   // block (128 / g requests x g heads) and one 128-byte half.
   CUtensorMap q_map;
+  // Nonzero: before reading the schedule, wait (bounded) until its header
+  // holds this epoch word -- the plan was uploaded on another stream with no
+  // event ordering it before this launch.  0: the stream orders it.
+  int32_t wait_epoch = 0;
 };
 
 // The cascade kernel's arguments: the shared-prefix role's (dense tile maps)
@@ -204,6 +214,7 @@ struct MergeArgs {
   float* lse;
   int64_t off_units, off_merge;
   int32_t hq;
+  int32_t wait_epoch = 0;   // nonzero: read the schedule only after the decode grid completes
 };
 
 // Kernel launchers (decode_kernel.cu / merge_kernels.cu).

@@ -12,6 +12,7 @@ namespace {
 __global__ void __launch_bounds__(tc::kTcThreads, 1)
     prefix_tc_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (!dev::schedule_ready(a.sched + H_EPOCH, a.wait_epoch, a.err)) return;
   tc::prefix_tc_body(a, smem_raw);
 }
 

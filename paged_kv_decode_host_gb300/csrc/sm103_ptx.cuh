@@ -119,5 +119,37 @@ __device__ __forceinline__ void raise_error(int32_t* err, volatile int* abort_fl
   *abort_flag = 1;
 }
 
+// Block-wide: when `want` is nonzero, thread 0 waits (bounded, kTimeoutNs)
+// until the schedule header's epoch word equals it.  The plan's upload
+// writes the header after the rest of the schedule, so the acquire load
+// that sees the epoch also sees the whole schedule.  Every thread of the
+// block must call it.  On timeout it ORs PKD_DEV_ERR_TIMEOUT into *err,
+// waits for the previous grid (so that this grid's completion still implies
+// the earlier ones') and returns false: the caller returns without work.
+__device__ __forceinline__ bool schedule_ready(const int32_t* epoch_word_ptr, int32_t want,
+                                               int32_t* err) {
+  if (want == 0) return true;
+  int late = 0;
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+      int32_t v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(epoch_word_ptr) : "memory");
+      if (v == want) break;
+      if ((it & 15u) == 15u && global_ns() - t0 > kTimeoutNs) {
+        late = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  if (__syncthreads_or(late)) {
+    if (threadIdx.x == 0) atomicOr(err, PKD_DEV_ERR_TIMEOUT);
+    pdl_wait();
+    return false;
+  }
+  return true;
+}
+
 }  // namespace dev
 }  // namespace pkd

@@ -191,3 +191,66 @@ def test_error_poll_waits_for_its_own_stream_only():
     assert err == 0
     assert still_running, "the poll waited for another stream's kernel"
     assert dt < 0.25, dt
+
+
+def _second_tables():
+    """Another batch of three over the same 64-page pool (29 pages)."""
+    w2 = workloads.Workload("api2", 2, 32, 8, 128, 16, 1, (200, 150, 90), 64)
+    return w2, workloads.make_tables(w2)
+
+
+def test_run_waits_on_the_device_for_a_plan_from_another_stream():
+    """pkd_run with expect_epoch: the plan is uploaded on a side stream held
+    back by a GPU sleep, and the run is issued on another stream with no
+    event between them.  The kernels wait for the new schedule's epoch word
+    and compute the new plan, not the one still in the workspace."""
+    w, t, q, kv, dec = _setup()
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    dec.run(q, kv)
+    torch.cuda.synchronize()
+    w2, t2 = _second_tables()
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((q.shape[0], q.shape[1]), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(int(1e8))        # tens of milliseconds
+    ep = dec.plan(t2["indptr"], t2["indices"], t2["last"], stream=side)
+    dec.run(q, kv, out=out, lse=lse, expect_epoch=ep, stream=main)
+    held_back = not side.query()
+    torch.cuda.synchronize()
+    assert held_back, "the upload had already landed when the run was issued"
+    ref_o, ref_l = oracle_decode(q, kv, t2, w2)
+    assert np.abs(out.double().cpu().numpy() - ref_o).max() <= 2e-2
+    assert np.abs(lse.double().cpu().numpy() - ref_l).max() <= 1e-3
+    assert dec.device_error() == 0
+
+
+def test_device_wait_for_a_late_plan_times_out_cleanly():
+    """The device-side wait for a plan's schedule is bounded: an upload held
+    back past it (a GPU sleep of several seconds on its stream) makes the run
+    report PKD_DEV_ERR_TIMEOUT, and the context stays usable: the same plan,
+    once landed, runs correctly."""
+    w, t, q, kv, dec = _setup()
+    dec.plan(t["indptr"], t["indices"], t["last"])
+    dec.run(q, kv)
+    torch.cuda.synchronize()
+    w2, t2 = _second_tables()
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(int(1.2e10))
+    ep = dec.plan(t2["indptr"], t2["indices"], t2["last"], stream=side)
+    dec.run(q, kv, out=out, lse=lse, expect_epoch=ep, stream=main)
+    main.synchronize()
+    # the timeout bit says the wait gave up before the upload landed
+    assert dec.device_error(stream=main) == pkd.DEV_ERR_TIMEOUT
+    side.synchronize()
+    dec.run(q, kv, out=out, lse=lse, expect_epoch=ep, stream=main)
+    main.synchronize()
+    ref_o, ref_l = oracle_decode(q, kv, t2, w2)
+    assert np.abs(out.double().cpu().numpy() - ref_o).max() <= 2e-2
+    assert np.abs(lse.double().cpu().numpy() - ref_l).max() <= 1e-3
+    assert dec.device_error(stream=main) == 0

@@ -141,6 +141,8 @@ def test_device_schedule_matches_host_planner():
     hwords, hinfo, hoff = pkd.plan_host(cfg, t["indptr"], t["indices"], t["last"])
     assert off == hoff
     n = off[4] + info["nnz"]
+    assert words[21] == 1                     # the device header carries the plan's epoch
+    hwords[21] = words[21]                    # (host-only plans leave it 0)
     np.testing.assert_array_equal(words[:n], hwords[:n])
     from oracle import plan as oplan
     ref = oplan.plan(t["indptr"], t["indices"], t["last"], page_size=16,

@@ -1234,39 +1234,72 @@ def run_reference(args, rank, world):
 OTHER_WORKLOADS = ("skewed", "token_sparse", "shared_prefix")
 
 
+def _child_env(local_rank):
+    """Environment for a single-process bench run on this rank's GPU."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE", "MASTER_ADDR",
+                        "MASTER_PORT", "GROUP_RANK", "ROLE_RANK", "TORCHELASTIC_RUN_ID")}
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    devs = [d for d in visible.split(",") if d.strip()] if visible else None
+    env["CUDA_VISIBLE_DEVICES"] = devs[local_rank] if devs else str(local_rank)
+    return env
+
+
 def run_other_workloads(args, rank, world, names=OTHER_WORKLOADS):
     """Each workload as its own bench run (same timing, roofline and e2e
-    legs, no CPU baseline), summarised under one key of the headline line."""
+    legs, no CPU baseline), summarised under one key of the headline line.
+    Each runs in a fresh process on this rank's GPU, as it would standalone:
+    in a process that has already run other workloads the per-step host
+    work (planning, launches) ran measurably slower, and the single-layer
+    steps are short enough for the host to matter.  With several ranks,
+    every rank runs its own and the whole-job figures take the slowest."""
     import gc
 
     import torch
+    gc.collect()
+    torch.cuda.empty_cache()
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    dev = torch.device("cuda", local_rank)
     res = {}
     for name in names:
-        gc.collect()
-        torch.cuda.empty_cache()
-        sub = argparse.Namespace(**vars(args))
-        sub.workload, sub.steps, sub.layers = name, args.other_steps, 0
-        sub.warmup = max(args.warmup, 10)
-        sub.no_cpu_baseline = True
-        ln = run_ours(sub, rank, world)
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", name,
+               "--steps", str(args.other_steps), "--warmup", str(max(args.warmup, 10)),
+               "--no-other-workloads", "--no-cpu-baseline", "--launch", args.launch,
+               "--consumer", args.consumer, "--chunk-rule", args.chunk_rule,
+               "--alpha", str(args.alpha), "--prefix-mode", args.prefix_mode,
+               "--prefix-kernel", args.prefix_kernel]
+        r = subprocess.run(cmd, env=_child_env(local_rank), capture_output=True, text=True,
+                           cwd=ROOT)
+        lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+        if r.returncode != 0 or not lines:
+            raise RuntimeError(f"{name} bench run failed ({r.returncode}): {r.stderr[-2000:]}")
+        ln = json.loads(lines[-1])
+        step_bytes = ln["config"]["alg_bytes_per_step"]
+        ms = max_over_ranks(ln["ms_per_step"], world, dev)
+        e2e = dict(ln["e2e"])
+        e2e_ms = max_over_ranks(e2e["ms_per_step"], world, dev)
+        if world > 1:
+            e2e["value"] = round(aggregate_throughput(step_bytes, e2e_ms, world), 2)
+            e2e["ms_per_step"] = round(e2e_ms, 5)
         rf = ln["roofline"]
+        value = aggregate_throughput(step_bytes, ms, world)
         res[name] = {
-            "value": ln["value"], "unit": ln["unit"], "pct_of_peak": ln["pct_of_peak"],
-            "ms_per_step": ln["ms_per_step"], "steps_per_s": ln["steps_per_s"],
+            "value": round(value, 2), "unit": ln["unit"],
+            "pct_of_peak": round(100.0 * value / world / rf["peak"], 2),
+            "ms_per_step": round(ms, 5), "steps_per_s": round(1e3 / ms, 3),
             "steps": ln["steps"], "warmup": ln["warmup"],
             "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "frac", "traffic",
                                             "launch_ms_mean")},
-            "e2e": {k: ln["e2e"][k] for k in ("value", "unit", "ms_per_step", "ms_gpu_events",
-                                               "ms_host_wall", "h2d_bytes_per_step",
-                                               "d2h_bytes_per_step")},
+            "e2e": {k: e2e[k] for k in ("value", "unit", "ms_per_step", "ms_gpu_events",
+                                        "ms_host_wall", "h2d_bytes_per_step",
+                                        "d2h_bytes_per_step")},
             "clocks": ln["clocks"], "gpu_launches": ln["gpu_launches"],
             "config": {k: ln["config"][k] for k in ("batch", "hq", "hkv", "page_size",
                                                     "total_tokens_per_layer",
                                                     "alg_bytes_per_step", "l2", "plan",
                                                     "prefix_kernel", "launch")},
+            "process": "own (a bench.py run of this workload alone on this GPU)",
         }
-    gc.collect()
-    torch.cuda.empty_cache()
     return res
 
 

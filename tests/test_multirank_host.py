@@ -49,3 +49,19 @@ def test_single_rank_passthrough():
     import bench
     assert bench.max_over_ranks(2.5, 1, None) == 2.5
     assert bench.aggregate_throughput(2e9, 1.0, 1) == pytest.approx(2000.0)
+
+
+def test_child_env_runs_a_single_process_on_the_ranks_gpu(monkeypatch):
+    """The extra workloads' child runs drop the launcher's rank variables and
+    see only this rank's GPU (the rank's entry of CUDA_VISIBLE_DEVICES, else
+    its local rank)."""
+    import bench
+    for k, v in (("RANK", "3"), ("WORLD_SIZE", "4"), ("LOCAL_RANK", "3"),
+                 ("MASTER_ADDR", "127.0.0.1"), ("MASTER_PORT", "29500")):
+        monkeypatch.setenv(k, v)
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    env = bench._child_env(3)
+    assert not {"RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"} & set(env)
+    assert env["CUDA_VISIBLE_DEVICES"] == "3"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "4,5,6,7")
+    assert bench._child_env(1)["CUDA_VISIBLE_DEVICES"] == "5"

@@ -183,3 +183,39 @@ def test_cascade_prefix_sweep_cases(prefix_tokens, batch):
                                  hkv=w.hkv)
     _check(out, lse, ref_o, ref_l)
     assert dec.device_error() == 0
+
+
+def test_cascade_run_waits_on_the_device_for_a_plan_from_another_stream():
+    """A cascade plan uploaded on a side stream held back by a GPU sleep, and
+    the run issued on another stream with expect_epoch and no event: the
+    cascade kernel waits for the new schedule (its split H_NPRE included)
+    and computes the new plan."""
+    w = workloads.workload("shared_prefix")
+    t = workloads.make_tables(w)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    gi, prefix, suffix = _workload_tables(w, t)
+    dec = _context(w, gi, prefix, suffix)
+    # first plan: the suffixes cut to at most 100 tokens
+    s_ip, s_ix, s_last = suffix
+    lens = [min(100, 16 * (int(s_ip[r + 1] - s_ip[r]) - 1) + int(s_last[r]))
+            for r in range(w.batch)]
+    short = workloads.page_table(lens, 16, np.concatenate(
+        [s_ix[s_ip[r]:s_ip[r] + -(-lens[r] // 16)] for r in range(w.batch)]).astype(np.int32))
+    dec.plan_cascade(gi, prefix, short)
+    dec.run(q, kv)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((w.batch, w.hq), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(int(1e8))
+    ep = dec.plan_cascade(gi, prefix, suffix, stream=side)      # the full suffixes
+    dec.run(q, kv, out=out, lse=lse, expect_epoch=ep, stream=main)
+    held_back = not side.query()
+    torch.cuda.synchronize()
+    assert held_back, "the upload had already landed when the run was issued"
+    ref_o, ref_l = oracle.decode(q, kv, t["indptr"], t["indices"], t["last"], hq=w.hq,
+                                 hkv=w.hkv)
+    _check(out, lse, ref_o, ref_l)
+    assert dec.device_error() == 0

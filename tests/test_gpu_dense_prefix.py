@@ -204,3 +204,40 @@ def test_dense_prefix_rejects_unsupported():
         pkd.BatchDecodeWithPagedKVCache(32, 8, 128, 16, max_batch=4, max_num_pages=8,
                                         num_pages=8, shared_prefix=True, dense_prefix=True,
                                         kv_dtype="e4m3")
+
+
+def test_dense_prefix_run_waits_on_the_device_for_a_plan_from_another_stream():
+    """The standalone dense kernel with a plan uploaded on a side stream held
+    back by a GPU sleep and the run issued on another stream with
+    expect_epoch and no event: it computes the new plan (two groups) rather
+    than the one already in the workspace (one group of all requests)."""
+    sizes, glens, P, hq, hkv = [12, 30], [5000, 2500], 16, 32, 8
+    rng = np.random.default_rng(41)
+    B = sum(sizes)
+    pool = sum(-(-l // P) for l in glens) + 3
+    indptr, indices, last = workloads.page_table(glens, P, rng.permutation(pool).astype(np.int32))
+    w = workloads.Workload("dpx", 841, hq, hkv, 128, P, 1, tuple([1] * B), pool)
+    q = workloads.make_q(w, device="cuda")[0]
+    kv = workloads.make_kv(w, device="cuda")[0]
+    dec = pkd.BatchDecodeWithPagedKVCache(hq, hkv, 128, P, max_batch=B,
+                                          max_num_pages=int(indptr[-1]), num_pages=pool,
+                                          shared_prefix=True, dense_prefix=True)
+    # first plan: every request over group 0's pages
+    dec.plan_shared(np.array([0, B], np.int32), indptr[:2], indices, last[:1])
+    dec.run(q, kv)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((B, hq), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(int(1e8))
+    ep = dec.plan_shared(np.array([0] + np.cumsum(sizes).tolist(), np.int32), indptr, indices,
+                         last, stream=side)
+    dec.run(q, kv, out=out, lse=lse, expect_epoch=ep, stream=main)
+    held_back = not side.query()
+    torch.cuda.synchronize()
+    assert held_back, "the upload had already landed when the run was issued"
+    e_ip, e_ix, e_last = _expand(sizes, indptr, indices, last)
+    ref_o, ref_l = oracle.decode(q, kv, e_ip, e_ix, e_last, hq=hq, hkv=hkv)
+    _check(out, lse, ref_o, ref_l)
+    assert dec.device_error() == 0

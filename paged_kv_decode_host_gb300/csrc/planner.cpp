@@ -484,8 +484,17 @@ struct LevelPlan {
 // (ties: the larger chunk).  A candidate whose makespan lower bound (its
 // costliest item, or its total cost spread evenly) cannot beat the best so
 // far is not scheduled.
+// Split results already computed for these lengths, by chunk (one search
+// evaluates several budgets, and their candidates often share a chunk).
+// Entries past `used` keep their storage for the next search.
+struct SplitCache {
+  std::vector<std::pair<int64_t, std::vector<Item>>> e;
+  size_t used = 0;
+};
+
 void plan_level(const std::vector<int64_t>& ulens, int64_t total, int32_t n, int64_t P,
-                int64_t floor_c, int64_t alpha, Scratch& sc, LevelPlan* out) {
+                int64_t floor_c, int64_t alpha, Scratch& sc, LevelPlan* out,
+                SplitCache* cache = nullptr) {
   out->chunk = -1;
   const int64_t bound = ceil_div(total, n);
   int64_t prev = -1;
@@ -501,7 +510,24 @@ void plan_level(const std::vector<int64_t>& ulens, int64_t total, int32_t n, int
       }
       if (std::max(alpha + top, ceil_div(total + alpha * n_it, n)) >= out->span) continue;
     }
-    split_sorted(ulens, c, alpha, &sc.whole, &sc.rest, &sc.items);
+    bool cached = false;
+    if (cache != nullptr) {
+      for (size_t i = 0; i < cache->used; ++i)
+        if (cache->e[i].first == c) {
+          sc.items.assign(cache->e[i].second.begin(), cache->e[i].second.end());
+          cached = true;
+          break;
+        }
+    }
+    if (!cached) {
+      split_sorted(ulens, c, alpha, &sc.whole, &sc.rest, &sc.items);
+      if (cache != nullptr) {
+        if (cache->used == cache->e.size()) cache->e.emplace_back();
+        cache->e[cache->used].first = c;
+        cache->e[cache->used].second.assign(sc.items.begin(), sc.items.end());
+        ++cache->used;
+      }
+    }
     const int64_t span = lpt(sc.items, n, &sc.owner, &sc.heap);
     if (out->chunk < 0 || span < out->span) {
       out->chunk = c;
@@ -603,6 +629,7 @@ struct CascadeScratch {
   std::vector<Block> blocks;
   std::vector<int32_t> block_of, np_block, ns_req, count, fill;
   std::vector<int64_t> chunk_tmp;
+  SplitCache split_cache;   // the suffix level's splits, by chunk, within one search
   LevelPlan pre, suf, best_pre, best_suf;
 };
 
@@ -672,6 +699,7 @@ int cascade_search(const pkd_config& cfg, int32_t n_cta, const int32_t* group_in
     const int64_t prop = (n_cta * pre_cost + all / 2) / all;
     const int64_t j0 = std::min<int64_t>(
         std::max<int64_t>((std::max<int64_t>(prop - base, 0) + step / 2) / step, 0), j_max);
+    cs.split_cache.used = 0;
     int64_t best_j = -1, best_sum = 0;
     // budgets compare by the predicted makespan, ties by the sum of the two
     // levels' makespans (a budget that does not shorten the bounding level
@@ -679,7 +707,8 @@ int cascade_search(const pkd_config& cfg, int32_t n_cta, const int32_t* group_in
     auto evaluate = [&](int64_t j) {
       plan_prefix(cs.block_len, hkv, (int32_t)(base + step * j), P, floor_p, kCascadePrefixAlpha,
                   sc, &cs.pre);
-      plan_level(cs.suf_len, suf_total, n_cta - cs.pre.ctas, P, floor_s, alpha, sc, &cs.suf);
+      plan_level(cs.suf_len, suf_total, n_cta - cs.pre.ctas, P, floor_s, alpha, sc, &cs.suf,
+                 &cs.split_cache);
       const int64_t p_span = cs.pre.span * kCascadePrefixCost16, s_span = cs.suf.span * 16;
       const int64_t span = std::max(p_span, s_span), sum = p_span + s_span;
       if (best_j < 0 || span < best_span || (span == best_span && sum < best_sum)) {

@@ -453,6 +453,35 @@ def run_ours(args, rank, world):
     for k in range(args.warmup):
         step(k)
     torch.cuda.synchronize()
+    # --launch auto: a short untimed trial of both launch modes on this
+    # machine (after the warm-up, before the timed steps); the faster one is
+    # timed.  Single-layer steps of a few tens of microseconds are close to
+    # host-bound with per-step launches, so which mode wins depends on the
+    # host; the trial times are reported with the choice.
+    launch_trial = None
+    chosen = args.launch
+    if args.launch == "auto":
+        n_trial = max(10, min(args.steps // 2, 100))
+        launch_trial = {}
+        idx = args.warmup
+        for mode in ("graph", "eager"):
+            use["eager"] = mode == "eager"
+            for _ in range(3):
+                step(idx)
+                idx += 1
+            torch.cuda.synchronize()
+            t0e = torch.cuda.Event(enable_timing=True)
+            t1e = torch.cuda.Event(enable_timing=True)
+            t0e.record(stream)
+            for _ in range(n_trial):
+                step(idx)
+                idx += 1
+            t1e.record(stream)
+            torch.cuda.synchronize()
+            launch_trial[mode] = round(max_over_ranks(t0e.elapsed_time(t1e) / n_trial, world,
+                                                      dev), 5)
+        chosen = "eager" if launch_trial["eager"] <= launch_trial["graph"] else "graph"
+        use["eager"] = chosen == "eager"
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -480,7 +509,7 @@ def run_ours(args, rank, world):
     last = graph_of(args.warmup + args.steps + k_roof - 1)
     k1_ms = last[0].layer_times() + (last[1].layer_times() if last[1] is not None else [])
     use["graphs"] = graphs
-    use["eager"] = args.launch == "eager"
+    use["eager"] = chosen == "eager"
     ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
 
@@ -584,9 +613,11 @@ def run_ours(args, rank, world):
                                           "makespan", "prefix_ctas", "prefix_chunk_tokens")},
             "launch": ("step graphs replayed (one per cache copy and planning context), "
                        "each after an event on the step's schedule upload"
-                       if args.launch == "graph" else
+                       if chosen == "graph" else
                        "kernels launched on the stream per step; they wait on the device for "
-                       "their plan's schedule (pkd_run with expect_epoch), no event"),
+                       "their plan's schedule (pkd_run with expect_epoch), no event")
+                      + (f"; chosen by --launch auto from an untimed trial of "
+                         f"{launch_trial} ms per step" if launch_trial else ""),
             "parallelism": f"replicas x{world} (no collective)",
         },
         "roofline": {
@@ -988,7 +1019,7 @@ def run_prefix_sweep(args, rank, world):
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            if args.launch == "eager":
+            if args.launch != "graph":
                 # the host queues the steps while the stream sleeps, so the
                 # events time the GPU's work back to back, not the host's
                 torch.cuda._sleep(int(4e7))
@@ -1327,12 +1358,14 @@ def main():
                     help="prefix_sweep: only these cases, e.g. 32768x64,1024x16 (prefix x batch)")
     ap.add_argument("--alpha", type=int, default=-1,
                     help="planner per-item cost in tokens (cost = alpha + tokens); -1: default")
-    ap.add_argument("--launch", choices=["graph", "eager"], default="eager",
+    ap.add_argument("--launch", choices=["auto", "graph", "eager"], default="auto",
                     help="timed steps: launch the step's kernels on the stream, each run "
                          "waiting on the device for its plan's schedule (pkd_run with "
                          "expect_epoch; the upload goes on a copy stream with no event), or "
                          "replay the step's captured CUDA graphs (one per cache copy and "
-                         "planning context) after an event on the upload")
+                         "planning context) after an event on the upload; auto: whichever "
+                         "an untimed trial after the warm-up finds faster on this machine "
+                         "(prefix_sweep: auto is eager)")
     ap.add_argument("--prefix-mode", choices=["cascade", "levels"], default="cascade",
                     help="shared-prefix step: one cascade plan and launch with one merge, or "
                          "two levels (prefix context + suffix context) joined by merge_states")
